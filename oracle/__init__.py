@@ -1,0 +1,150 @@
+"""fp64 CPU oracle for normalized (ELU+1) linear attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference legs of ``bench.py`` may import this package.
+It shares no code with the CUDA library and never imports it.
+
+The arithmetic lives in ``la_oracle.c`` (plain C, double precision,
+token-serial); this module only marshals numpy arrays.  Sources for every
+formula are cited in that file's header:
+
+* causal prefill (inclusive read): "线性注意力从头到尾讲清楚" §7; "Linear
+  Attention: Accumulating KV in a Fixed-Size State", "Summarize state
+  updates and reads with equations"; "Linear Attention Math", "The recurrent
+  form".
+* global read: "线性注意力从头到尾讲清楚" §5 and §8; "Linear Attention Math",
+  "The associativity trick, written out".
+* decode step: one update-then-read of the causal recurrence on a persistent
+  state ("线性注意力从头到尾讲清楚" §7, last paragraph; "Linear Attention
+  Math", "The recurrent form").
+
+Arrays: q, k are ``[..., N, dk]``; v is ``[..., N, dv]``; leading dimensions
+are flattened into independent heads.  Results are float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import build_oracle, library_path
+
+PHI_KINDS = {"elu1": 0, "identity": 1}
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(
+            os.path.join(os.path.dirname(__file__), "la_oracle.c")
+        ):
+            build_oracle()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        L, I, D = ctypes.c_long, ctypes.c_int, ctypes.c_double
+        lib.lao_phi.argtypes = [D, I]
+        lib.lao_phi.restype = D
+        lib.lao_causal.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, L, L, I, I, D, I, I]
+        lib.lao_causal.restype = I
+        lib.lao_global.argtypes = [dp, dp, dp, dp, dp, dp, L, L, I, I, D, I, I]
+        lib.lao_global.restype = I
+        lib.lao_decode_step.argtypes = [dp, dp, dp, dp, dp, dp, L, I, I, D, I, I]
+        lib.lao_decode_step.restype = I
+        lib.lao_state_scalars.argtypes = [I, I]
+        lib.lao_state_scalars.restype = L
+        lib.lao_version.restype = I
+        _lib = lib
+    return _lib
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise ValueError(f"oracle {name} failed with status {rc}")
+
+
+def phi(x, kind: str = "elu1"):
+    """Feature map applied elementwise (scalar or array)."""
+    lib = _load()
+    arr = np.asarray(x, dtype=np.float64)
+    out = np.array([lib.lao_phi(float(t), PHI_KINDS[kind]) for t in arr.ravel()])
+    return out.reshape(arr.shape) if arr.shape else float(out[0])
+
+
+def _split(q, k, v):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim < 2 or q.shape != k.shape or v.shape[:-1] != q.shape[:-1]:
+        raise ValueError("q, k must be [..., N, dk] and v [..., N, dv] with equal leading dims")
+    lead = q.shape[:-2]
+    N, dk, dv = q.shape[-2], q.shape[-1], v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    return q, k, v, lead, BH, N, dk, dv
+
+
+def causal(q, k, v, eps: float = 1e-6, phi: str = "elu1", S0=None, z0=None, nthreads: int = 1):
+    """Causal prefill.  Returns (out [..., N, dv], S [..., dk, dv], z [..., dk])."""
+    lib = _load()
+    q, k, v, lead, BH, N, dk, dv = _split(q, k, v)
+    out = np.empty(lead + (N, dv))
+    S = np.empty(lead + (dk, dv))
+    z = np.empty(lead + (dk,))
+    S0 = None if S0 is None else _f64(np.broadcast_to(S0, lead + (dk, dv)))
+    z0 = None if z0 is None else _f64(np.broadcast_to(z0, lead + (dk,)))
+    rc = lib.lao_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(S), _ptr(z), _ptr(S0), _ptr(z0),
+                        BH, N, dk, dv, float(eps), PHI_KINDS[phi], int(nthreads))
+    _check(rc, "causal")
+    return out, S, z
+
+
+def global_(q, k, v, eps: float = 1e-6, phi: str = "elu1", nthreads: int = 1):
+    """Global (non-causal) form.  Returns (out, S, z) like :func:`causal`."""
+    lib = _load()
+    q, k, v, lead, BH, N, dk, dv = _split(q, k, v)
+    out = np.empty(lead + (N, dv))
+    S = np.empty(lead + (dk, dv))
+    z = np.empty(lead + (dk,))
+    rc = lib.lao_global(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(S), _ptr(z),
+                        BH, N, dk, dv, float(eps), PHI_KINDS[phi], int(nthreads))
+    _check(rc, "global")
+    return out, S, z
+
+
+def decode_step(q, k, v, S, z, eps: float = 1e-6, phi: str = "elu1", nthreads: int = 1):
+    """One decode step.  q, k: [..., dk]; v: [..., dv]; S: [..., dk, dv]; z: [..., dk].
+
+    Returns (out [..., dv], S_new, z_new); the inputs S, z are not modified.
+    """
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    lead = q.shape[:-1]
+    dk, dv = q.shape[-1], v.shape[-1]
+    if k.shape != q.shape or v.shape[:-1] != lead:
+        raise ValueError("decode_step: q, k must be [..., dk] and v [..., dv]")
+    S = _f64(S).copy()
+    z = _f64(z).copy()
+    if S.shape != lead + (dk, dv) or z.shape != lead + (dk,):
+        raise ValueError("decode_step: S must be [..., dk, dv] and z [..., dk]")
+    BH = int(np.prod(lead)) if lead else 1
+    out = np.empty(lead + (dv,))
+    rc = lib.lao_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(S), _ptr(z),
+                             BH, dk, dv, float(eps), PHI_KINDS[phi], int(nthreads))
+    _check(rc, "decode_step")
+    return out, S, z
+
+
+def state_scalars(m: int, dv: int) -> int:
+    """Persistent state size per head (matrix plus normalizer vector)."""
+    return int(_load().lao_state_scalars(m, dv))

@@ -1,0 +1,237 @@
+/*
+ * Plain, slow fp64 CPU oracle for normalized linear attention with the
+ * ELU(x)+1 feature map.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link or call
+ * this file; only the test-suite, the smoke check and the CPU-baseline leg
+ * of the benchmark use it.  It shares no code, header or constant with the
+ * CUDA library.
+ *
+ * Every quantity is computed token by token, in double precision, exactly
+ * as the pages write the method down; there is no chunking, blocking or
+ * reordering beyond the definition.
+ *
+ * Sources (page title, section / equation):
+ *  - "Linear Attention: Accumulating KV in a Fixed-Size State"
+ *    (ai-systems-engineering.com), "Summarize state updates and reads with
+ *    equations": S_{t+1} = S_t + k_t v_t^T, z_{t+1} = z_t + k_t,
+ *    y_t^T = q_t^T S_{t+1} / q_t^T z_{t+1}  (add first, then read).
+ *  - "线性注意力从头到尾讲清楚" (lilfry09.github.io), §4 (the eps-normalized
+ *    read o_i = phi(q_i)^T S / (phi(q_i)^T z + eps)), §5 (matrix form of the
+ *    global read), §7 (causal prefix recurrence S_t, z_t inclusive of t),
+ *    §8 (phi = elu + 1 applied separately to q and k; layout [B,H,N,.]).
+ *  - "Linear Attention Math" (aicassindra.com), "The recurrent form" and
+ *    "Feature maps: elu+1" (elu(x) > -1, so alpha = 1 and m = d).
+ *
+ * Feature map: phi(x) = ELU(x) + 1 with alpha = 1, i.e. x + 1 for x > 0 and
+ * exp(x) for x <= 0.  The identity map exists only so that the pages'
+ * worked examples, which are stated directly in feature space, can be fed
+ * through the same code.
+ *
+ * Layouts (row-major, last index fastest), per (b,h) head flattened to BH:
+ *   q, k : [BH, N, dk]    v : [BH, N, dv]    out : [BH, N, dv]
+ *   S    : [BH, dk, dv]   (rows = key-feature components, columns = value
+ *                          components)
+ *   z    : [BH, dk]
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define LAO_PHI_ELU1 0
+#define LAO_PHI_IDENTITY 1
+
+#define LAO_OK 0
+#define LAO_EINVAL (-1)
+#define LAO_ENOMEM (-2)
+
+int lao_version(void) { return 1; }
+
+/* Feature map (ELU(x)+1 with alpha = 1, or identity). */
+double lao_phi(double x, int kind) {
+  if (kind == LAO_PHI_IDENTITY) return x;
+  if (x > 0.0) return x + 1.0;
+  return exp(x);
+}
+
+/* One token of the recurrence on state (S, z): add phi(k) v^T and phi(k),
+ * then read the updated state with phi(q).  Writes dv outputs. */
+static void step_update_then_read(const double *q, const double *k, const double *v,
+                                  double *o, double *S, double *z, int dk, int dv,
+                                  double eps, int kind, double *qt, double *kt) {
+  for (int i = 0; i < dk; ++i) {
+    kt[i] = lao_phi(k[i], kind);
+    qt[i] = lao_phi(q[i], kind);
+  }
+  for (int i = 0; i < dk; ++i)
+    for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += kt[i] * v[j];
+  for (int i = 0; i < dk; ++i) z[i] += kt[i];
+  double den = 0.0;
+  for (int i = 0; i < dk; ++i) den += qt[i] * z[i];
+  for (int j = 0; j < dv; ++j) {
+    double num = 0.0;
+    for (int i = 0; i < dk; ++i) num += qt[i] * S[(size_t)i * dv + j];
+    o[j] = num / (den + eps);
+  }
+}
+
+enum { FORM_CAUSAL = 0, FORM_GLOBAL = 1, FORM_DECODE = 2 };
+
+typedef struct {
+  int form;
+  const double *q, *k, *v;
+  double *out, *S, *z;
+  const double *S0, *z0;
+  long h_begin, h_end, N;
+  int dk, dv, kind;
+  double eps;
+  int status;
+} job_t;
+
+static void run_head(const job_t *jb, long h, double *qt, double *kt) {
+  const int dk = jb->dk, dv = jb->dv;
+  const long N = jb->N;
+  const double *q = jb->q + (size_t)h * N * dk;
+  const double *k = jb->k + (size_t)h * N * dk;
+  const double *v = jb->v + (size_t)h * N * dv;
+  double *out = jb->out + (size_t)h * N * dv;
+  double *S = jb->S + (size_t)h * dk * dv;
+  double *z = jb->z + (size_t)h * dk;
+
+  if (jb->form == FORM_DECODE) {
+    /* S, z are the caller's persistent state: in/out. */
+    step_update_then_read(q, k, v, out, S, z, dk, dv, jb->eps, jb->kind, qt, kt);
+    return;
+  }
+  if (jb->S0) memcpy(S, jb->S0 + (size_t)h * dk * dv, sizeof(double) * dk * dv);
+  else memset(S, 0, sizeof(double) * dk * dv);
+  if (jb->z0) memcpy(z, jb->z0 + (size_t)h * dk, sizeof(double) * dk);
+  else memset(z, 0, sizeof(double) * dk);
+
+  if (jb->form == FORM_CAUSAL) {
+    for (long t = 0; t < N; ++t)
+      step_update_then_read(q + t * dk, k + t * dk, v + t * dv, out + t * dv, S, z, dk, dv,
+                            jb->eps, jb->kind, qt, kt);
+    return;
+  }
+  /* Global: S = sum_j phi(k_j) v_j^T and z = sum_j phi(k_j) over all N,
+   * then every position reads the same (S, z). */
+  for (long t = 0; t < N; ++t) {
+    for (int i = 0; i < dk; ++i) kt[i] = lao_phi(k[t * dk + i], jb->kind);
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += kt[i] * v[t * dv + j];
+    for (int i = 0; i < dk; ++i) z[i] += kt[i];
+  }
+  for (long t = 0; t < N; ++t) {
+    for (int i = 0; i < dk; ++i) qt[i] = lao_phi(q[t * dk + i], jb->kind);
+    double den = 0.0;
+    for (int i = 0; i < dk; ++i) den += qt[i] * z[i];
+    for (int j = 0; j < dv; ++j) {
+      double num = 0.0;
+      for (int i = 0; i < dk; ++i) num += qt[i] * S[(size_t)i * dv + j];
+      out[t * dv + j] = num / (den + jb->eps);
+    }
+  }
+}
+
+static void *worker(void *arg) {
+  job_t *jb = (job_t *)arg;
+  double *qt = (double *)malloc(sizeof(double) * jb->dk);
+  double *kt = (double *)malloc(sizeof(double) * jb->dk);
+  if (!qt || !kt) {
+    free(qt);
+    free(kt);
+    jb->status = LAO_ENOMEM;
+    return NULL;
+  }
+  for (long h = jb->h_begin; h < jb->h_end; ++h) run_head(jb, h, qt, kt);
+  free(qt);
+  free(kt);
+  jb->status = LAO_OK;
+  return NULL;
+}
+
+/* Spread independent heads over nthreads POSIX threads; each head stays
+ * token-serial. */
+static int run(job_t proto, long BH, int nthreads) {
+  if (BH < 0 || proto.N < 0 || proto.dk <= 0 || proto.dv <= 0 || !(proto.eps >= 0.0)) return LAO_EINVAL;
+  if (proto.kind != LAO_PHI_ELU1 && proto.kind != LAO_PHI_IDENTITY) return LAO_EINVAL;
+  if (BH == 0) return LAO_OK;
+  if (!proto.q || !proto.k || !proto.v || !proto.out || !proto.S || !proto.z) return LAO_EINVAL;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > BH) nthreads = (int)BH;
+  job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
+  pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!jobs || !tids) {
+    free(jobs);
+    free(tids);
+    return LAO_ENOMEM;
+  }
+  int status = LAO_OK;
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = proto;
+    jobs[t].h_begin = BH * t / nthreads;
+    jobs[t].h_end = BH * (t + 1) / nthreads;
+    jobs[t].status = LAO_ENOMEM;
+  }
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&tids[t], NULL, worker, &jobs[t]) != 0) break;
+    started = t;
+  }
+  worker(&jobs[0]);
+  /* Any thread that could not be started runs here, serially. */
+  for (int t = started + 1; t < nthreads; ++t) worker(&jobs[t]);
+  for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+  for (int t = 0; t < nthreads; ++t)
+    if (jobs[t].status != LAO_OK) status = jobs[t].status;
+  free(jobs);
+  free(tids);
+  return status;
+}
+
+/* Causal prefill: out[t] reads the state that includes token t.  S, z receive
+ * the final state.  S0, z0 (nullable) give an initial state; NULL means the
+ * zero state. */
+int lao_causal(const double *q, const double *k, const double *v, double *out, double *S,
+               double *z, const double *S0, const double *z0, long BH, long N, int dk, int dv,
+               double eps, int phi_kind, int nthreads) {
+  job_t p;
+  memset(&p, 0, sizeof p);
+  p.form = FORM_CAUSAL;
+  p.q = q; p.k = k; p.v = v; p.out = out; p.S = S; p.z = z; p.S0 = S0; p.z0 = z0;
+  p.N = N; p.dk = dk; p.dv = dv; p.kind = phi_kind; p.eps = eps;
+  return run(p, BH, nthreads);
+}
+
+/* Global (non-causal): every position reads the state of the whole sequence.
+ * S, z receive that state. */
+int lao_global(const double *q, const double *k, const double *v, double *out, double *S,
+               double *z, long BH, long N, int dk, int dv, double eps, int phi_kind,
+               int nthreads) {
+  job_t p;
+  memset(&p, 0, sizeof p);
+  p.form = FORM_GLOBAL;
+  p.q = q; p.k = k; p.v = v; p.out = out; p.S = S; p.z = z;
+  p.N = N; p.dk = dk; p.dv = dv; p.kind = phi_kind; p.eps = eps;
+  return run(p, BH, nthreads);
+}
+
+/* One recurrent decode step per head on the persistent state (S, z), which
+ * is read and written in place: update with (k, v), then read with q.
+ * q, k : [BH, dk], v, out : [BH, dv]. */
+int lao_decode_step(const double *q, const double *k, const double *v, double *out, double *S,
+                    double *z, long BH, int dk, int dv, double eps, int phi_kind, int nthreads) {
+  job_t p;
+  memset(&p, 0, sizeof p);
+  p.form = FORM_DECODE;
+  p.q = q; p.k = k; p.v = v; p.out = out; p.S = S; p.z = z;
+  p.N = 1; p.dk = dk; p.dv = dv; p.kind = phi_kind; p.eps = eps;
+  return run(p, BH, nthreads);
+}
+
+/* Persistent state size per head in scalars: an [m, dv] matrix plus an [m]
+ * vector ("Linear Attention: From Pairwise Reads to a Recurrent State",
+ * "Linear in which variable?"). */
+long lao_state_scalars(int m, int dv) { return (long)m * dv + m; }
