@@ -1,0 +1,388 @@
+"""Benchmark of the GB300 normalized linear attention library.
+
+One JSON line on rank 0.  The headline ``value`` is causal prefill
+throughput (B*H*N tokens/s) on the B=4, H=16, N=8192, d=128 bf16 workload;
+one step is one ``la_causal`` call on device-resident inputs.  The other
+forms on the hot path (global read, long-context causal prefill, the
+recurrent decode step) are timed in the same run and reported under
+``forms`` with their own roofline fractions.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle (token-serial recurrence) on
+the host cores instead, on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs its own seeded batch (weak scaling,
+no collective on the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from causal_linear_attention_attn_gb300 import inputs  # noqa: E402
+
+METRIC = "causal prefill tokens/s (B·H·N/s) & decode HBM GB/s, % of roofline, 1×GB300"
+HEADLINE = "causal_bf16"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129e6
+
+
+# --- distributed plumbing (host logic, covered by the gloo tests) -------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_workload(w: inputs.Workload, rank: int) -> inputs.Workload:
+    """Each rank draws its own batch (weak scaling): same shapes, distinct seed."""
+    return dataclasses.replace(w, seed=w.seed + 7919 * rank) if rank else w
+
+
+# --- roofline bookkeeping ------------------------------------------------------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def in_bytes(w):
+    return 4 if w.dtype == "f32" else 2
+
+
+def seq_bytes(w) -> float:
+    """Algorithmic HBM bytes of one prefill/global call: q,k,v read, fp32 out
+    written, final fp32 S and z written."""
+    tok = w.BH * w.N
+    return tok * (2 * w.dk + w.dv) * in_bytes(w) + tok * w.dv * 4 + w.BH * (w.dk * w.dv + w.dk) * 4
+
+
+def decode_bytes(w) -> float:
+    """Algorithmic HBM bytes of one decode step: S and z read and written (fp32),
+    q,k,v read, fp32 out written."""
+    return w.BH * (2 * (w.dk * w.dv + w.dk) * 4 + (2 * w.dk + w.dv) * in_bytes(w) + w.dv * 4)
+
+
+def ncu_traffic(kernel_key: str):
+    """Per-launch DRAM bytes measured by ncu for this kernel, if the kernel
+    source is unchanged since the capture (see profiles/traffic.json)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d:
+        return None
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in d["sources"]:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return d["bytes_per_launch"] if h.hexdigest()[:16] == d["sha"] else None
+
+
+# --- clocks --------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.lines, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.lines:
+            if t0 <= ts <= t1:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        loaded = [r for r in rows if (num(r[3]) or 0) >= 50] or rows
+        sm = [num(r[0]) for r in loaded if num(r[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(loaded[0][1]),
+                "power_w_max": max((num(r[2]) or 0) for r in loaded), "samples": len(loaded),
+                "reasons": sorted(reasons)}
+
+
+# --- timing helpers ---------------------------------------------------------------
+
+def time_device(fn, steps: int, warmup: int, world: int, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return a.elapsed_time(b) / steps  # ms per step (this rank)
+
+
+def roofline(alg_bytes: float, ms: float, hbm: float, src: str, traffic):
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
+            "alg_bytes_per_launch": alg_bytes}
+
+
+# --- our arm -----------------------------------------------------------------------
+
+def run_seq_form(L, w, steps, warmup, world, stream, hbm, src, gen_device="cuda"):
+    q, k, v = inputs.make_qkv(w, device=gen_device)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    out = torch.empty(w.B, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
+    S = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device="cuda")
+    z = torch.empty(w.B, w.H, w.dk, dtype=torch.float32, device="cuda")
+    fn = L.la_causal if w.form == "causal" else L.la_global
+    call = lambda: fn(q, k, v, out=out, S=S, z=z, eps=w.eps, stream=stream)
+    n0 = L.kernel_launches()
+    ms = time_device(call, steps, warmup, world, stream)
+    launches = (L.kernel_launches() - n0) // (steps + warmup) * steps
+    ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
+    tok = w.BH * w.N
+    res = {"workload": w.name, "tokens_per_s": world * tok / (ms * 1e-3), "ms_per_call": ms,
+           "roofline": roofline(seq_bytes(w), ms, hbm, src, ncu_traffic(f"{w.form}:{w.name}")),
+           "gpu_launches": launches}
+    return res, (q, k, v, out, S, z, fn)
+
+
+def run_e2e(L, w, bufs, steps, warmup, stream):
+    """Same call through host buffers: pinned q,k,v copied in, out/S/z copied back, every step."""
+    q, k, v, out, S, z, fn = bufs
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho, hS, hz = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out, S, z))
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        fn(q, k, v, out=out, S=S, z=z, eps=w.eps, stream=stream)
+        ho.copy_(out, non_blocking=True)
+        hS.copy_(S, non_blocking=True)
+        hz.copy_(z, non_blocking=True)
+
+    ms = time_device(step, steps, warmup, 1, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hS, hz))
+    return {"value": w.BH * w.N / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def run_decode(L, w, steps, warmup, world, stream, hbm, src):
+    kp, vp = inputs.decode_prefix(w, device="cuda")
+    _, S, z = L.la_causal(kp, kp, vp, eps=w.eps, stream=stream)
+    del kp, vp
+    nstage = steps + warmup
+    staged = [inputs.decode_step_qkv(w, s, device="cuda") for s in range(nstage)]
+    out = torch.empty(w.B, w.H, w.dv, dtype=torch.float32, device="cuda")
+    it = iter(staged)
+    call = lambda: L.la_decode_step(*next(it), S, z, out=out, eps=w.eps, stream=stream)
+    n0 = L.kernel_launches()
+    ms = time_device(call, steps, warmup, world, stream)
+    launches = (L.kernel_launches() - n0) // nstage * steps
+    ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
+    rl = roofline(decode_bytes(w), ms, hbm, src, ncu_traffic(f"decode:{w.name}"))
+    return {"workload": w.name, "us_per_step": ms * 1e3, "gbs": rl["achieved"], "frac_hbm": rl["frac"],
+            "seq_tokens_per_s": world * w.B / (ms * 1e-3), "steps_timed": steps, "roofline": rl,
+            "gpu_launches": launches}
+
+
+def cpu_baseline(w, target_s: float = 12.0):
+    """The oracle as it stands, token-serial fp64, heads spread over the host cores."""
+    import numpy as np
+
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    # calibrate on a short prefix of one head, then size the sample
+    q, k, v = inputs.make_qkv(w, N=min(w.N, 1024), heads=[0])
+    t = time.perf_counter()
+    oracle.causal(q.double().numpy(), k.double().numpy(), v.double().numpy(), eps=w.eps)
+    per_tok = (time.perf_counter() - t) / q.shape[1]
+    heads = max(1, min(w.BH, int(target_s * cores / (per_tok * w.N))))
+    N = w.N if heads > 1 or per_tok * w.N * 1.0 <= target_s else max(1, int(target_s / per_tok))
+    q, k, v = inputs.make_qkv(w, N=N, heads=list(range(min(heads, w.BH))))
+    fn = oracle.causal if w.form == "causal" else oracle.global_
+    args = [np.ascontiguousarray(t.double().numpy()) for t in (q, k, v)]
+    nthreads = min(cores, q.shape[0])
+    t = time.perf_counter()
+    fn(*args, eps=w.eps, nthreads=nthreads)
+    dt = time.perf_counter() - t
+    tok = q.shape[0] * q.shape[1]
+    return {"value": tok / dt, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{q.shape[0]} of {w.BH} heads x {q.shape[1]} tokens of {w.name}, {dt:.1f} s wall"}
+
+
+def main_ours(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    from causal_linear_attention_attn_gb300 import linattn as L
+
+    hbm, src = peaks()
+    stream = torch.cuda.current_stream()
+    w = rank_workload(inputs.WORKLOADS[args.workload], rank)
+    with ClockSampler(local) as clk:
+        t0 = clk.mark()
+        head, bufs = run_seq_form(L, w, args.steps, args.warmup, world, stream, hbm, src)
+        t1 = clk.mark()
+        forms = {}
+        if not args.no_extras:
+            for name in ("global_bf16", "causal_bf16_long"):
+                if name == args.workload:
+                    continue
+                wx = rank_workload(inputs.WORKLOADS[name], rank)
+                steps = max(3, args.steps // (10 if name == "causal_bf16_long" else 1))
+                forms[name], _ = run_seq_form(L, wx, steps, args.warmup, world, stream, hbm, src)
+                torch.cuda.empty_cache()
+            wd = rank_workload(inputs.WORKLOADS["decode_bf16"], rank)
+            forms["decode_bf16"] = run_decode(L, wd, args.decode_steps, args.warmup, world, stream, hbm, src)
+            torch.cuda.empty_cache()
+        t2 = clk.mark()
+    e2e = run_e2e(L, w, bufs, max(3, args.steps // 10), args.warmup, stream)
+    cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    if rank != 0:
+        return
+    clocks = clk.summary(t0, t1) or clk.summary(t0, t2)
+    ms = head["ms_per_call"]
+    line = {
+        "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded torch.randn, per-head seeds; drawn on the device)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d_k": w.dk, "d_v": w.dv, "eps": w.eps,
+                   "inputs": "q,k ~ N(0,1)/sqrt(128), v ~ N(0,1), bf16; out/S/z fp32",
+                   "l2": "inputs (402.7 MB) larger than L2 (129 MB); no flush needed",
+                   "parallelism": f"replicas x{world} (heads independent)"},
+        "roofline": head["roofline"], "gpu_launches": head["gpu_launches"], "e2e": e2e, "clocks": clocks,
+        "cpu_baseline": cpu, "forms": forms,
+    }
+    print(json.dumps(line))
+
+
+# --- reference arm: the oracle on the host cores -------------------------------------
+
+def main_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    # each step is a bounded sample sized so that the whole run stays near two minutes
+    step_s = max(0.2, min(args.ref_step_s, 120.0 / (args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, target_s=step_s)
+    vals = [cpu_baseline(w, target_s=step_s) for _ in range(args.steps)]
+    v = statistics.median(r["value"] for r in vals)
+    cb = dict(vals[0], value=v)
+    line = {"metric": METRIC, "impl": "reference", "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.randn)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d_k": w.dk, "d_v": w.dv},
+            "cpu_baseline": cb, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--no-extras", action="store_true", help="time the headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-step-s", type=float, default=10.0, help="max CPU seconds per reference step")
+    a = ap.parse_args(argv)
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        main_reference(a)
+    else:
+        main_ours(a)

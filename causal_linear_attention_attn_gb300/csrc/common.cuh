@@ -1,0 +1,41 @@
+// Device-side helpers shared by the linear attention kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace la {
+
+// Feature map phi(x) = ELU(x) + 1 with alpha = 1: x + 1 above zero, exp(x)
+// at or below ("Linear Attention Math", "Feature maps: elu+1"; the sketch in
+// "线性注意力从头到尾讲清楚" §8 uses elu(x) + 1).  Both branches give 1 at 0.
+__device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T *p) {
+  return to_f32(*p);
+}
+
+// Four consecutive inputs as float (p must be 8-byte aligned for bf16, 16 for f32).
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  float4 r;
+  r.x = __uint_as_float(u.x << 16);
+  r.y = __uint_as_float(u.x & 0xffff0000u);
+  r.z = __uint_as_float(u.y << 16);
+  r.w = __uint_as_float(u.y & 0xffff0000u);
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+}  // namespace la

@@ -1,0 +1,45 @@
+// Host-side launcher declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "linattn.h"
+
+namespace la {
+
+// One call's problem, heads flattened to BH = B * H.  Pointers are device
+// pointers as documented in linattn.h.
+struct Problem {
+  const void *q, *k, *v;
+  float *out, *S, *z;
+  int BH;
+  long N;
+  int dk, dv;
+  float eps;
+  la_dtype dt;
+  cudaStream_t stream;
+};
+
+// Exact fp32 CUDA-core chunked causal pass.  Processes tokens [0, n_proc) of
+// every head.  from_state: start from the caller's S, z instead of zero.
+// write_state: store the final S, z.
+cudaError_t launch_causal_simt(const Problem &p, long n_proc, bool from_state, bool write_state);
+
+// Global form: state build (S, z are zeroed and accumulated) then the read.
+cudaError_t launch_global_simt(const Problem &p);
+
+// One decode step, S and z in place.
+cudaError_t launch_decode(const Problem &p);
+
+// Count one successful kernel launch (reported by la_kernel_launches).
+void count_launch(unsigned n = 1);
+
+// Per-device attributes, filled once per device.
+struct DeviceInfo {
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  int max_smem_optin = 0;
+};
+const DeviceInfo &device_info(int dev);
+
+}  // namespace la

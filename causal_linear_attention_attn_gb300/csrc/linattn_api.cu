@@ -1,0 +1,154 @@
+// C ABI of liblinattn.so: argument validation, dispatch and status codes.
+// Every entry point validates before it touches the GPU; see linattn.h for
+// the contract of each call.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "internal.h"
+#include "linattn.h"
+
+namespace la {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+std::atomic<unsigned long long> g_launches{0};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+
+la_status from_cuda(cudaError_t e) {
+  switch (e) {
+    case cudaSuccess: return LA_OK;
+    case cudaErrorMemoryAllocation: return LA_ERR_OUT_OF_MEMORY;
+    case cudaErrorNoDevice:
+    case cudaErrorInsufficientDriver: return LA_ERR_NO_DEVICE;
+    default: return LA_ERR_LAUNCH;
+  }
+}
+
+// Shared checks.  need_seq: q,k,v,out are read/written (B*H*N > 0).
+la_status validate(const void *q, const void *k, const void *v, const float *out, const float *S,
+                   const float *z, int B, int H, long N, int dk, int dv, float eps, la_dtype dt) {
+  if (B < 0 || H < 0 || N < 0 || dk <= 0 || dv <= 0) return LA_ERR_INVALID_VALUE;
+  if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_VALUE;
+  if (dt != LA_F32 && dt != LA_BF16) return LA_ERR_UNSUPPORTED;
+  if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+  const long BH = (long)B * H;
+  if (BH > 0x7fffffffL) return LA_ERR_INVALID_VALUE;
+  if (BH > 0 && (!S || !z)) return LA_ERR_INVALID_VALUE;
+  if (BH > 0 && N > 0 && (!q || !k || !v || !out)) return LA_ERR_INVALID_VALUE;
+  const void *ptrs[6] = {q, k, v, out, S, z};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
+  return LA_OK;
+}
+
+la_status current_device(int *dev) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return LA_ERR_NO_DEVICE;
+  }
+  *dev = d;
+  return LA_OK;
+}
+
+}  // namespace
+
+void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+const DeviceInfo &device_info(int dev) {
+  if (dev < 0) cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
+  std::call_once(g_once[dev], [dev] {
+    DeviceInfo &i = g_info[dev];
+    cudaDeviceGetAttribute(&i.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&i.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&i.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&i.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  });
+  return g_info[dev];
+}
+
+}  // namespace la
+
+using la::Problem;
+
+extern "C" {
+
+int la_version(void) { return (1 << 16) | 0; }
+
+unsigned long long la_kernel_launches(void) { return la::g_launches.load(std::memory_order_relaxed); }
+
+const char *la_status_string(la_status s) {
+  switch (s) {
+    case LA_OK: return "success";
+    case LA_ERR_INVALID_VALUE: return "invalid argument (NULL pointer, negative size or bad eps)";
+    case LA_ERR_UNSUPPORTED: return "unsupported head dimension or dtype";
+    case LA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case LA_ERR_OUT_OF_MEMORY: return "out of device memory for scratch";
+    case LA_ERR_LAUNCH: return "kernel launch failed";
+    case LA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case LA_ERR_NO_DEVICE: return "no usable CUDA device";
+  }
+  return "unknown status";
+}
+
+static la_status causal_impl(const void *q, const void *k, const void *v, float *out, float *S, float *z,
+                             int B, int H, int N, int d_k, int d_v, float eps, la_dtype dt, void *stream,
+                             bool from_state) {
+  la_status st = la::validate(q, k, v, out, S, z, B, H, N, d_k, d_v, eps, dt);
+  if (st != LA_OK) return st;
+  if ((long)B * H == 0) return LA_OK;
+  int dev;
+  if ((st = la::current_device(&dev)) != LA_OK) return st;
+  Problem p{q, k, v, out, S, z, B * H, (long)N, d_k, d_v, eps, dt, (cudaStream_t)stream};
+  if (N == 0) {
+    if (from_state) return LA_OK;
+    cudaError_t e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)p.BH * d_k * d_v, p.stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(z, 0, sizeof(float) * (size_t)p.BH * d_k, p.stream);
+    return la::from_cuda(e);
+  }
+  return la::from_cuda(la::launch_causal_simt(p, p.N, from_state, true));
+}
+
+la_status la_causal(const void *q, const void *k, const void *v, float *out, float *S, float *z, int B, int H,
+                    int N, int d_k, int d_v, float eps, la_dtype dt, void *stream) {
+  return causal_impl(q, k, v, out, S, z, B, H, N, d_k, d_v, eps, dt, stream, false);
+}
+
+la_status la_causal_with_state(const void *q, const void *k, const void *v, float *out, float *S, float *z,
+                               int B, int H, int N, int d_k, int d_v, float eps, la_dtype dt, void *stream) {
+  return causal_impl(q, k, v, out, S, z, B, H, N, d_k, d_v, eps, dt, stream, true);
+}
+
+la_status la_global(const void *q, const void *k, const void *v, float *out, float *S, float *z, int B, int H,
+                    int N, int d_k, int d_v, float eps, la_dtype dt, void *stream) {
+  la_status st = la::validate(q, k, v, out, S, z, B, H, N, d_k, d_v, eps, dt);
+  if (st != LA_OK) return st;
+  if ((long)B * H == 0) return LA_OK;
+  int dev;
+  if ((st = la::current_device(&dev)) != LA_OK) return st;
+  Problem p{q, k, v, out, S, z, B * H, (long)N, d_k, d_v, eps, dt, (cudaStream_t)stream};
+  return la::from_cuda(la::launch_global_simt(p));
+}
+
+la_status la_decode_step(const void *q, const void *k, const void *v, float *out, float *S, float *z, int B,
+                         int H, int d_k, int d_v, float eps, la_dtype dt, void *stream) {
+  la_status st = la::validate(q, k, v, out, S, z, B, H, 1, d_k, d_v, eps, dt);
+  if (st != LA_OK) return st;
+  if ((long)B * H == 0) return LA_OK;
+  int dev;
+  if ((st = la::current_device(&dev)) != LA_OK) return st;
+  Problem p{q, k, v, out, S, z, B * H, 1L, d_k, d_v, eps, dt, (cudaStream_t)stream};
+  return la::from_cuda(la::launch_decode(p));
+}
+
+}  // extern "C"

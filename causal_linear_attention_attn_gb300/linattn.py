@@ -1,0 +1,148 @@
+"""Thin ctypes binding of ``liblinattn.so`` (argument marshalling only).
+
+Function names match the C ABI in ``include/linattn.h``.  Tensors are torch
+CUDA tensors; the binding checks shapes and dtypes, allocates outputs that
+were not supplied, passes raw device pointers and the current CUDA stream,
+and raises :class:`LinAttnError` on a non-OK status.  Every step of the
+computation runs in the library's kernels.  Importing this module fails if
+the library has not been built (``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblinattn.so")
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() before use")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+LA_F32, LA_BF16 = 0, 1
+STATUS_NAMES = {0: "LA_OK", 1: "LA_ERR_INVALID_VALUE", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_MISALIGNED",
+                4: "LA_ERR_OUT_OF_MEMORY", 5: "LA_ERR_LAUNCH", 6: "LA_ERR_TIMEOUT", 7: "LA_ERR_NO_DEVICE"}
+
+_vp, _fp, _i, _f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_SEQ_ARGS = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _i, _vp]
+for _name in ("la_global", "la_causal", "la_causal_with_state"):
+    getattr(lib, _name).argtypes = _SEQ_ARGS
+    getattr(lib, _name).restype = _i
+lib.la_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _f, _i, _vp]
+lib.la_decode_step.restype = _i
+lib.la_status_string.argtypes = [_i]
+lib.la_status_string.restype = ctypes.c_char_p
+lib.la_version.argtypes = []
+lib.la_version.restype = _i
+lib.la_kernel_launches.argtypes = []
+lib.la_kernel_launches.restype = ctypes.c_ulonglong
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn}: {STATUS_NAMES.get(code, code)} ({status_string(code)})")
+
+
+def status_string(code: int) -> str:
+    return lib.la_status_string(code).decode()
+
+
+def version() -> int:
+    return lib.la_version()
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LA_F32
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    raise TypeError(f"q, k, v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_in(q, k, v, nd):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != nd:
+            raise ValueError(f"{name} must be a contiguous {nd}-d CUDA tensor")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if q.shape != k.shape or q.shape[:-1] != v.shape[:-1]:
+        raise ValueError("q, k must have equal shapes and v the same leading dims")
+
+
+def _state(S, z, lead, dk, dv, dev):
+    if S is None:
+        S = torch.empty(*lead, dk, dv, dtype=torch.float32, device=dev)
+    if z is None:
+        z = torch.empty(*lead, dk, dtype=torch.float32, device=dev)
+    if S.dtype != torch.float32 or z.dtype != torch.float32 or not S.is_contiguous() or not z.is_contiguous():
+        raise ValueError("S and z must be contiguous float32 tensors")
+    if tuple(S.shape) != (*lead, dk, dv) or tuple(z.shape) != (*lead, dk):
+        raise ValueError(f"S must be {(*lead, dk, dv)} and z {(*lead, dk)}")
+    return S, z
+
+
+def _seq_call(fn, q, k, v, out, S, z, eps, stream, need_state_in=False):
+    _check_in(q, k, v, 4)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if need_state_in and (S is None or z is None):
+        raise ValueError(f"{fn} needs the initial state S, z")
+    S, z = _state(S, z, (B, H), dk, dv, q.device)
+    if out is None:
+        out = torch.empty(B, H, N, dv, dtype=torch.float32, device=q.device)
+    if out.dtype != torch.float32 or not out.is_contiguous() or tuple(out.shape) != (B, H, N, dv):
+        raise ValueError("out must be a contiguous float32 [B, H, N, d_v] tensor")
+    rc = getattr(lib, fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(S), _ptr(z), B, H, N, dk, dv, float(eps),
+                          _dt(q), _stream(stream))
+    if rc != 0:
+        raise LinAttnError(fn, rc)
+    return out, S, z
+
+
+def la_global(q, k, v, out=None, S=None, z=None, eps: float = 1e-6, stream=None):
+    """Global read; returns (out, S, z).  S, z are overwritten with the whole-sequence state."""
+    return _seq_call("la_global", q, k, v, out, S, z, eps, stream)
+
+
+def la_causal(q, k, v, out=None, S=None, z=None, eps: float = 1e-6, stream=None):
+    """Causal prefill from the zero state; returns (out, S, z) with the final state."""
+    return _seq_call("la_causal", q, k, v, out, S, z, eps, stream)
+
+
+def la_causal_with_state(q, k, v, S, z, out=None, eps: float = 1e-6, stream=None):
+    """Causal prefill continuing from (S, z), which are updated in place; returns (out, S, z)."""
+    return _seq_call("la_causal_with_state", q, k, v, out, S, z, eps, stream, need_state_in=True)
+
+
+def la_decode_step(q, k, v, S, z, out=None, eps: float = 1e-6, stream=None):
+    """One decode step; q, k [B, H, d_k], v [B, H, d_v]; S, z updated in place; returns out."""
+    _check_in(q, k, v, 3)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    S, z = _state(S, z, (B, H), dk, dv, q.device)
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=torch.float32, device=q.device)
+    rc = lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(S), _ptr(z), B, H, dk, dv, float(eps),
+                            _dt(q), _stream(stream))
+    if rc != 0:
+        raise LinAttnError("la_decode_step", rc)
+    return out
+
+
+def kernel_launches() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib.la_kernel_launches())

@@ -1,0 +1,158 @@
+/*
+ * linattn.h — C ABI of the GB300 (sm_103a) normalized linear attention
+ * library (liblinattn.so).
+ *
+ * The method: similarity sim(q, k) = phi(q)^T phi(k) with the feature map
+ * phi(x) = ELU(x) + 1 (alpha = 1: x + 1 for x > 0, exp(x) otherwise),
+ * applied separately to every query and key vector.  Keys and values are
+ * summarized in a state S = sum_j phi(k_j) v_j^T ([m, d_v], m = d_k) and a
+ * normalizer z = sum_j phi(k_j) ([m]); a query reads
+ *     o = phi(q)^T S / (phi(q)^T z + eps).
+ * Sources: "线性注意力从头到尾讲清楚" (lilfry09.github.io) §4 (eps-normalized
+ * read), §5 (matrix form), §7 (causal recurrence), §8 (phi = elu + 1,
+ * [B,H,N,.] layout); "Linear Attention Math" (aicassindra.com), "The
+ * associativity trick, written out", "The recurrent form", "Feature maps:
+ * elu+1"; "Linear Attention: Accumulating KV in a Fixed-Size State"
+ * (ai-systems-engineering.com), "Summarize state updates and reads with
+ * equations".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers are DEVICE pointers on the current CUDA device, except where a
+ * comment says otherwise.  Tensors are contiguous row-major, last index
+ * fastest:
+ *     q, k : [B, H, N, d_k]        v, out : [B, H, N, d_v]
+ *     S    : [B, H, d_k, d_v]      z      : [B, H, d_k]
+ * (the decode step drops the N axis).  Rows of S are key-feature
+ * components, columns value components.  q, k, v have the dtype given by
+ * `dt`; out, S and z are always float32.
+ *
+ * Ownership: the caller owns every buffer.  The library keeps no pointer
+ * after a call returns and never frees caller memory.  `out` must not
+ * overlap q, k, v, S or z.  Calls only enqueue work on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream) and never synchronize
+ * the host; errors raised by kernels that were enqueued successfully
+ * surface at the caller's next synchronization.
+ *
+ * Errors: every entry point validates its arguments before touching the
+ * GPU and returns a la_status; nothing is launched on error and no output
+ * is modified.  LA_ERR_INVALID_VALUE: a NULL pointer where data is
+ * needed, B, H, N < 0, d_k or d_v <= 0, or eps negative / not finite.
+ * LA_ERR_UNSUPPORTED: d_k or d_v not in {32, 64, 128}, or an unknown
+ * dtype.  LA_ERR_MISALIGNED: a pointer not 16-byte aligned.
+ * LA_ERR_NO_DEVICE: no usable CUDA device.  LA_ERR_OUT_OF_MEMORY:
+ * stream-ordered scratch could not be allocated.  LA_ERR_LAUNCH: a kernel
+ * launch failed (cudaGetLastError).
+ *
+ * Thread safety: calls may be made concurrently from several host threads;
+ * the only shared state is a per-device table of attributes filled once.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#if defined(__GNUC__)
+#define LA_API __attribute__((visibility("default")))
+#else
+#define LA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LA_F32 = 0,  /* q, k, v are float32 */
+  LA_BF16 = 1  /* q, k, v are bfloat16 */
+} la_dtype;
+
+typedef enum {
+  LA_OK = 0,
+  LA_ERR_INVALID_VALUE = 1,
+  LA_ERR_UNSUPPORTED = 2,
+  LA_ERR_MISALIGNED = 3,
+  LA_ERR_OUT_OF_MEMORY = 4,
+  LA_ERR_LAUNCH = 5,
+  LA_ERR_TIMEOUT = 6,
+  LA_ERR_NO_DEVICE = 7
+} la_status;
+
+/*
+ * Global (non-causal) linear attention: every position reads the state of
+ * the whole sequence,
+ *     S = sum_{j<N} phi(k_j) v_j^T,  z = sum_{j<N} phi(k_j),
+ *     out_i = phi(q_i)^T S / (phi(q_i)^T z + eps)      for every i.
+ * Source: "线性注意力从头到尾讲清楚" §5 (matrix form) and §8 (the einsum
+ * sketch); "Linear Attention Math", "The associativity trick, written out".
+ *
+ * q, k: [B,H,N,d_k]; v: [B,H,N,d_v] (dtype dt).  out: [B,H,N,d_v] float32,
+ * written.  S: [B,H,d_k,d_v], z: [B,H,d_k] float32, OVERWRITTEN with the
+ * whole-sequence state (the zero state when N == 0).  May allocate
+ * stream-ordered scratch on `stream`.  B*H == 0 is a no-op returning LA_OK.
+ */
+LA_API la_status la_global(const void *q, const void *k, const void *v, float *out, float *S, float *z,
+                    int B, int H, int N, int d_k, int d_v, float eps, la_dtype dt, void *stream);
+
+/*
+ * Causal prefill: position t reads the prefix state that INCLUDES token t,
+ *     S_t = S_{t-1} + phi(k_t) v_t^T,  z_t = z_{t-1} + phi(k_t),
+ *     out_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps),   S_{-1} = 0, z_{-1} = 0.
+ * Source: "线性注意力从头到尾讲清楚" §7; "Linear Attention Math", "The
+ * recurrent form"; "Linear Attention: Accumulating KV in a Fixed-Size
+ * State" (add the token, then read the updated state).  Computed in
+ * chunks ("Linear Attention: From Pairwise Reads to a Recurrent State",
+ * "A recurrence need not force token-serial training").
+ *
+ * Arguments as la_global.  S, z are OVERWRITTEN with the final prefix state
+ * S_{N-1}, z_{N-1}, ready to be passed to la_decode_step.
+ */
+LA_API la_status la_causal(const void *q, const void *k, const void *v, float *out, float *S, float *z,
+                    int B, int H, int N, int d_k, int d_v, float eps, la_dtype dt, void *stream);
+
+/*
+ * Causal prefill that continues from a given state: as la_causal, but the
+ * recurrence starts from the caller's S, z instead of zero (chunked prefill
+ * continuation; N new tokens appended to a sequence whose state is S, z).
+ * S, z are read, then OVERWRITTEN with the state after the N new tokens.
+ * With N == 0 the state is left unchanged.
+ * Source: the causal recurrence above applied to a persistent state
+ * ("线性注意力从头到尾讲清楚" §7, last paragraph: only S_t, z_t are kept).
+ */
+LA_API la_status la_causal_with_state(const void *q, const void *k, const void *v, float *out, float *S,
+                               float *z, int B, int H, int N, int d_k, int d_v, float eps,
+                               la_dtype dt, void *stream);
+
+/*
+ * One recurrent decode step per (b,h) on a persistent state: update, then
+ * read the updated state,
+ *     S += phi(k) v^T;  z += phi(k);  out = phi(q)^T S / (phi(q)^T z + eps).
+ * Source: "线性注意力从头到尾讲清楚" §7 (inference keeps only S_t, z_t);
+ * "Linear Attention Math", "The recurrent form" (O(1) time and memory per
+ * generated token).
+ *
+ * q, k: [B,H,d_k]; v: [B,H,d_v] (dtype dt).  out: [B,H,d_v] float32,
+ * written.  S: [B,H,d_k,d_v], z: [B,H,d_k] float32, read and written IN
+ * PLACE.  Allocates nothing.
+ */
+LA_API la_status la_decode_step(const void *q, const void *k, const void *v, float *out, float *S,
+                         float *z, int B, int H, int d_k, int d_v, float eps, la_dtype dt,
+                         void *stream);
+
+/* Static English description of a status code (never NULL). */
+LA_API const char *la_status_string(la_status s);
+
+/* Library ABI version: (major << 16) | minor. */
+LA_API int la_version(void);
+
+/*
+ * Diagnostics: number of kernels this library has enqueued in this process
+ * (all devices, all threads; a relaxed atomic counter incremented at every
+ * successful launch).  Read it before and after a region to count the
+ * library's launches inside it.
+ */
+LA_API unsigned long long la_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

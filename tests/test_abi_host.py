@@ -1,0 +1,111 @@
+"""C-ABI host checks that need no GPU: exported symbols, status strings and
+argument validation (every validation path returns before any CUDA call)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+from conftest import ROOT
+
+L = pytest.importorskip("causal_linear_attention_attn_gb300.linattn")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, NO_DEVICE = 0, 1, 2, 3, 7
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names.update(re.findall(r"LA_API\s+[\w\s\*]*?\b(la_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_symbols()
+    for n in ("la_global", "la_causal", "la_causal_with_state", "la_decode_step", "la_status_string",
+              "la_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for n in _declared_symbols():
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_version_and_status_strings():
+    assert L.version() >> 16 == 1
+    for code in range(8):
+        s = L.status_string(code)
+        assert isinstance(s, str) and s
+    assert L.status_string(99) == "unknown status"
+
+
+# A fake, 16-byte aligned, non-NULL address: never dereferenced, because every
+# call below fails validation (or has nothing to do) before touching the GPU.
+P = 1 << 20
+
+
+def seq(fn="la_causal", q=P, k=P, v=P, out=P, S=P, z=P, B=1, H=1, N=8, dk=32, dv=32, eps=1e-6, dt=1, stream=None):
+    return getattr(L.lib, fn)(q, k, v, out, S, z, B, H, N, dk, dv, eps, dt, stream)
+
+
+@pytest.mark.parametrize("fn", ["la_causal", "la_global", "la_causal_with_state"])
+def test_sequence_validation(fn):
+    assert seq(fn, q=None) == INVALID
+    assert seq(fn, v=None) == INVALID
+    assert seq(fn, out=None) == INVALID
+    assert seq(fn, S=None) == INVALID
+    assert seq(fn, z=None) == INVALID
+    assert seq(fn, B=-1) == INVALID
+    assert seq(fn, N=-3) == INVALID
+    assert seq(fn, dk=0) == INVALID
+    assert seq(fn, eps=-1e-6) == INVALID
+    assert seq(fn, eps=float("nan")) == INVALID
+    assert seq(fn, eps=float("inf")) == INVALID
+    assert seq(fn, dk=48) == UNSUPPORTED
+    assert seq(fn, dv=256) == UNSUPPORTED
+    assert seq(fn, dt=5) == UNSUPPORTED
+    assert seq(fn, q=P + 8) == MISALIGNED
+    assert seq(fn, out=P + 4) == MISALIGNED
+    assert seq(fn, z=P + 2) == MISALIGNED
+    # nothing to do: no heads
+    assert seq(fn, B=0) == OK
+    assert seq(fn, H=0, q=None, k=None, v=None, out=None, S=None, z=None) == OK
+    # empty sequences still need the state buffers (they are written or kept)
+    assert seq(fn, N=0, q=None, k=None, v=None, out=None, S=None) == INVALID
+
+
+def test_decode_validation():
+    f = L.lib.la_decode_step
+    args = dict(q=P, k=P, v=P, out=P, S=P, z=P, B=2, H=2, dk=64, dv=64, eps=1e-6, dt=1, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["q"], a["k"], a["v"], a["out"], a["S"], a["z"], a["B"], a["H"], a["dk"], a["dv"], a["eps"],
+                 a["dt"], a["stream"])
+
+    assert call(k=None) == INVALID
+    assert call(S=None) == INVALID
+    assert call(H=-1) == INVALID
+    assert call(eps=float("nan")) == INVALID
+    assert call(dv=96) == UNSUPPORTED
+    assert call(S=P + 4) == MISALIGNED
+    assert call(B=0) == OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_call_without_a_device_reports_no_device():
+    assert seq("la_causal") == NO_DEVICE
+    assert seq("la_global") == NO_DEVICE
+
+
+def test_binding_rejects_bad_tensors_before_the_library():
+    q = torch.zeros(1, 1, 4, 32)
+    with pytest.raises(ValueError):
+        L.la_causal(q, q, q)  # CPU tensors
+    with pytest.raises(ValueError):
+        L.la_decode_step(q, q, q, None, None)
