@@ -117,6 +117,8 @@ cudaError_t launch_t(const Problem &p) {
   long splits = (4L * di.sm_count + p.BH - 1) / p.BH;
   splits = std::max(1L, std::min(splits, (p.N + kT - 1) / kT));
   const size_t smem1 = sizeof(float) * ((size_t)kT * (p.dk + 1) + (size_t)kT * p.dv);
+  e = cudaFuncSetAttribute(global_state_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+  if (e != cudaSuccess) return e;
   global_state_kernel<Tin><<<dim3(p.BH, (unsigned)splits), kThreads, smem1, p.stream>>>(
       (const Tin *)p.k, (const Tin *)p.v, p.S, p.z, p.N, p.dk, p.dv, (int)splits);
   e = cudaGetLastError();

@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstdio>
 #include <mutex>
 
 #include "internal.h"
@@ -23,7 +24,13 @@ std::atomic<unsigned long long> g_launches{0};
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
 
+thread_local cudaError_t t_last_error = cudaSuccess;
+
 la_status from_cuda(cudaError_t e) {
+  if (e != cudaSuccess) {
+    t_last_error = e;
+    cudaGetLastError();  // clear a non-sticky error so later calls start clean
+  }
   switch (e) {
     case cudaSuccess: return LA_OK;
     case cudaErrorMemoryAllocation: return LA_ERR_OUT_OF_MEMORY;
@@ -53,7 +60,7 @@ la_status validate(const void *q, const void *k, const void *v, const float *out
 la_status current_device(int *dev) {
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess) {
-    cudaGetLastError();
+    t_last_error = cudaGetLastError();
     return LA_ERR_NO_DEVICE;
   }
   *dev = d;
@@ -84,6 +91,12 @@ using la::Problem;
 extern "C" {
 
 int la_version(void) { return (1 << 16) | 0; }
+
+const char *la_last_error_detail(void) {
+  static thread_local char buf[256];
+  snprintf(buf, sizeof buf, "%s: %s", cudaGetErrorName(la::t_last_error), cudaGetErrorString(la::t_last_error));
+  return buf;
+}
 
 unsigned long long la_kernel_launches(void) { return la::g_launches.load(std::memory_order_relaxed); }
 

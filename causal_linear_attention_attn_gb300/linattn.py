@@ -35,6 +35,8 @@ lib.la_status_string.argtypes = [_i]
 lib.la_status_string.restype = ctypes.c_char_p
 lib.la_version.argtypes = []
 lib.la_version.restype = _i
+lib.la_last_error_detail.argtypes = []
+lib.la_last_error_detail.restype = ctypes.c_char_p
 lib.la_kernel_launches.argtypes = []
 lib.la_kernel_launches.restype = ctypes.c_ulonglong
 
@@ -42,7 +44,8 @@ lib.la_kernel_launches.restype = ctypes.c_ulonglong
 class LinAttnError(RuntimeError):
     def __init__(self, fn: str, code: int):
         self.code = code
-        super().__init__(f"{fn}: {STATUS_NAMES.get(code, code)} ({status_string(code)})")
+        detail = f"; {lib.la_last_error_detail().decode()}" if code in (4, 5, 7) else ""
+        super().__init__(f"{fn}: {STATUS_NAMES.get(code, code)} ({status_string(code)}{detail})")
 
 
 def status_string(code: int) -> str:

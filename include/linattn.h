@@ -144,6 +144,13 @@ LA_API const char *la_status_string(la_status s);
 LA_API int la_version(void);
 
 /*
+ * Diagnostics: name and description of the CUDA runtime error behind the
+ * last LA_ERR_LAUNCH / LA_ERR_OUT_OF_MEMORY / LA_ERR_NO_DEVICE returned to
+ * the calling host thread ("no error" if none).  Static storage; never NULL.
+ */
+LA_API const char *la_last_error_detail(void);
+
+/*
  * Diagnostics: number of kernels this library has enqueued in this process
  * (all devices, all threads; a relaxed atomic counter incremented at every
  * successful launch).  Read it before and after a region to count the
