@@ -1,0 +1,616 @@
+// Chunked causal linear attention on the sm_103a tensor cores (tcgen05, TMEM, TMA).
+//
+// The causal recurrence S_t = S_{t-1} + phi(k_t) v_t^T, z_t = z_{t-1} + phi(k_t),
+// o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps) ("线性注意力从头到尾讲清楚" §7;
+// "Linear Attention Math", "The recurrent form") is evaluated over chunks of
+// C = 128 tokens: a chunk reads the state carried in from earlier chunks and
+// adds its own masked pairwise part, then folds its keys and values into the
+// state ("Linear Attention: From Pairwise Reads to a Recurrent State", "A
+// recurrence need not force token-serial training").  Per chunk, with
+// Q = phi(q), K = phi(k) rounded to bf16:
+//   P      = tril(Q K^T)                    128x128x128 MMA, fp32 in TMEM
+//   P_hi   = bf16(P), P_lo = bf16(P - P_hi) (the weights carry ~16 bits)
+//   num    = Q bf16(S_prev) + P_hi V + P_lo V      3 MMAs into one TMEM tile
+//   den    = Q . z_prev (fp32) + rowsum(P_hi + P_lo) + eps
+//   S     += K^T V                          fp32 accumulator resident in TMEM
+//   z     += column sums of K               fp32, CUDA cores
+// d_k = d_v = 128.  The numerator and denominator use the same rounded
+// weights, z never passes through bf16, and the state stays fp32.
+//
+// One CTA owns a contiguous segment of one head's tokens.  Long sequences are
+// split into segments; a first pass (the same kernel in state-only mode)
+// reduces K^T V over parts of the earlier segments, and each segment starts
+// from the sum of the parts before it.
+//
+// Warp roles (10 warps): 0 TMA producer; 1 MMA issuer and TMEM owner;
+// 2-5 feature-map warpgroup (phi in place on the staged Q/K tiles, z and the
+// cross-chunk denominator); 6-9 epilogue warpgroup (P split, bf16 state copy,
+// normalised fp32 outputs, final state).  Every mbarrier wait is bounded; a
+// wait that runs out raises the CTA abort word and the device status word,
+// the CTA drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace la {
+
+__device__ unsigned int g_device_status;
+
+namespace {
+using namespace tc;
+
+constexpr int kC = 128;               // tokens per chunk = MMA M
+constexpr int kD = 128;               // d_k = d_v
+constexpr uint32_t kBlk = 16384;      // one [128 rows x 64] bf16 block, 128-byte swizzled
+constexpr uint32_t kTile = 2 * kBlk;  // [128 x 128] bf16 tile
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpPhi = 2, kWarpEpi = 6;
+constexpr uint32_t kBarPhi = 1, kBarEpi = 2;  // named barrier ids
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
+constexpr int kExact = 64;  // leading tokens of each head computed by the exact fp32 pass
+
+template <bool kStateOnly>
+struct Layout {
+  static constexpr int kStages = kStateOnly ? 3 : 2;
+  static constexpr uint32_t Q = 0;
+  static constexpr uint32_t K = kStateOnly ? 0 : kStages * kTile;
+  static constexpr uint32_t V = K + kStages * kTile;
+  static constexpr uint32_t Sb = V + kStages * kTile;  // bf16 copy of the carried state (main mode)
+  static constexpr uint32_t DenX = kStateOnly ? Sb : Sb + kTile;
+  static constexpr uint32_t Z = DenX + kStages * kC * 4;
+  static constexpr uint32_t Bars = Z + kD * 4;
+  static constexpr uint32_t Misc = Bars + 16 * 8;
+  static constexpr uint32_t Bytes = Misc + 16;
+  static constexpr uint32_t Alloc = Bytes + 1024;  // slack for aligning the base to 1024 bytes
+  static constexpr uint32_t TmemCols = kStateOnly ? 128 : 512;
+};
+static_assert(Layout<false>::Alloc <= 232448, "shared memory budget");
+static_assert(Layout<true>::Alloc <= 232448, "shared memory budget");
+
+struct TcParams {
+  CUtensorMap tq, tk, tv;  // 3-D maps over [BH][N][128] bf16, box 64 x 128 x 1, 128-byte swizzle
+  float *out, *S_out, *z_out;
+  const float *S0, *z0;      // initial state (nullable = zero)
+  float *part_S, *part_z;    // state-only outputs / main-mode prefix inputs: [BH][nparts][128][128], [..][128]
+  long N;
+  int seg_len, nseg, part_len, nparts, parts_per_seg;
+  int n_exact;
+  float eps;
+};
+
+// OR of a per-thread flag over a named barrier's threads (also a barrier).
+__device__ __forceinline__ bool bar_or(uint32_t id, uint32_t threads, bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred pi, po;\nsetp.ne.u32 pi, %1, 0;\nbar.red.or.pred po, %2, %3, pi;\nselp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)flag), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that ignores the abort word: used only to drain copies and MMAs
+// already in flight before the CTA exits.
+__device__ __forceinline__ void wait_drain(uint64_t *bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      atomicOr(&g_device_status, kAbortTimeout);
+      return;
+    }
+}
+
+// phi on two packed bf16 values, evaluated in fp32 and rounded back to bf16.
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
+  float a = __uint_as_float(x << 16), b = __uint_as_float(x & 0xffff0000u);
+  a = a > 0.f ? a + 1.f : __expf(a);
+  b = b > 0.f ? b + 1.f : __expf(b);
+  __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint4 phi8(uint4 x) {
+  return make_uint4(phi_bf16x2(x.x), phi_bf16x2(x.y), phi_bf16x2(x.z), phi_bf16x2(x.w));
+}
+
+__device__ __forceinline__ float dot8(uint4 y, const float *z) {
+  const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    s = fmaf(__uint_as_float(w[e] << 16), z[2 * e], s);
+    s = fmaf(__uint_as_float(w[e] & 0xffff0000u), z[2 * e + 1], s);
+  }
+  return s;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// Write 32 values (columns col0 .. col0+31 of row `row`) as bf16 into a
+// [128 x 128] tile made of two 64-column swizzled blocks.
+__device__ __forceinline__ void store_row32_bf16(uint8_t *tile, int row, int col0, const float (&v)[32]) {
+  uint8_t *blk = tile + (col0 >> 6) * kBlk;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c = (col0 & 63) + q * 8;
+    *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c)) =
+        make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                   pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+  }
+}
+
+// K-major operand (rows of 64 K-elements): k-step ks covers K elements [16ks, 16ks+16).
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int ks) {
+  return sw128_desc(tile + (ks >> 2) * kBlk + (ks & 3) * 32, 16, 1024);
+}
+// MN-major operand (rows = K index, 64 M/N elements per row, two 64-wide blocks).
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int ks) {
+  return sw128_desc(tile + ks * 2048, kBlk, 1024);
+}
+
+template <bool kStateOnly>
+__global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_constant__ TcParams p) {
+  using Lay = Layout<kStateOnly>;
+  constexpr int kStages = Lay::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float *den_x = reinterpret_cast<float *>(sm + Lay::DenX);
+  float *zs = reinterpret_cast<float *>(sm + Lay::Z);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::Bars);
+  uint64_t *full = bars, *phi_done = bars + 3, *empty = bars + 6;
+  uint64_t *mma1_done = bars + 9, *pp_ready = bars + 10, *o_full = bars + 11, *sb_ready = bars + 12,
+           *o_free = bars + 13, *drain = bars + 14;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::Misc);
+  volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
+  unsigned int *status = &g_device_status;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  long t_begin, t_end;
+  int init_parts;
+  bool last_seg;
+  if (kStateOnly) {
+    t_begin = (long)blockIdx.x * p.part_len;
+    t_end = min(p.N, t_begin + p.part_len);
+    init_parts = 0;
+    last_seg = false;
+  } else {
+    t_begin = (long)blockIdx.x * p.seg_len;
+    t_end = min(p.N, t_begin + p.seg_len);
+    init_parts = blockIdx.x * p.parts_per_seg;
+    last_seg = (int)blockIdx.x == p.nseg - 1;
+  }
+  const int nchunks = (int)((t_end - t_begin + kC - 1) / kC);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&phi_done[s], 128);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(mma1_done, 1);
+    mbar_init(pp_ready, 128);
+    mbar_init(o_full, 1);
+    mbar_init(sb_ready, 128);
+    mbar_init(o_free, 128);
+    mbar_init(drain, 1);
+    *abort_word = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, Lay::TmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpTma) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      if (!kStateOnly) prefetch_tmap(&p.tq);
+      prefetch_tmap(&p.tk);
+      prefetch_tmap(&p.tv);
+      int issued = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kStages;
+        const uint32_t u = c / kStages;
+        if (c >= kStages && !mbar_wait(&empty[s], (u - 1) & 1, abort_word, status)) break;
+        const int tok = (int)(t_begin + (long)c * kC);
+        mbar_arrive_expect_tx(&full[s], (kStateOnly ? 2 : 3) * kTile);
+        if (!kStateOnly) {
+          tma_load_3d(sm + Lay::Q + s * kTile, &p.tq, &full[s], 0, tok, bh);
+          tma_load_3d(sm + Lay::Q + s * kTile + kBlk, &p.tq, &full[s], 64, tok, bh);
+        }
+        tma_load_3d(sm + Lay::K + s * kTile, &p.tk, &full[s], 0, tok, bh);
+        tma_load_3d(sm + Lay::K + s * kTile + kBlk, &p.tk, &full[s], 64, tok, bh);
+        tma_load_3d(sm + Lay::V + s * kTile, &p.tv, &full[s], 0, tok, bh);
+        tma_load_3d(sm + Lay::V + s * kTile + kBlk, &p.tv, &full[s], 64, tok, bh);
+        issued = c + 1;
+      }
+      // every issued copy must land before shared memory is released
+      for (int c = max(0, issued - kStages); c < issued; ++c) wait_drain(&full[c % kStages], (c / kStages) & 1);
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issuer (one thread) ----------------
+    if (lane == 0) {
+      const uint32_t tP = tmem + kColP, tO = tmem + kColO, tS = tmem + kColS;
+      constexpr uint32_t iKK = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t iKM = idesc_bf16_f32(128, 128, 0, 1);
+      constexpr uint32_t iMM = idesc_bf16_f32(128, 128, 1, 1);
+      const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V),
+                     sSb = smem_u32(sm + Lay::Sb);
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kStages;
+        const uint32_t u = c / kStages;
+        if (!mbar_wait(&phi_done[s], u & 1, abort_word, status)) break;
+        tc_fence_after();
+        const uint32_t q = sQ + s * kTile, k = sK + s * kTile, v = sV + s * kTile;
+        if (!kStateOnly) {
+          // P = Q K^T
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(q, ks), kdesc(k, ks), iKK, ks > 0);
+          if (!mbar_wait(sb_ready, c & 1, abort_word, status)) break;
+          if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status)) break;
+          tc_fence_after();
+          // O = Q bf16(S_prev)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(q, ks), mndesc(sSb, ks), iKM, ks > 0);
+        }
+        // S += K^T V
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16(tS, mndesc(k, ks), mndesc(v, ks), iMM, kStateOnly ? (c > 0 || ks > 0) : 1);
+        if (!kStateOnly) {
+          mma_commit(mma1_done);
+          if (!mbar_wait(pp_ready, c & 1, abort_word, status)) break;
+          tc_fence_after();
+          // O += P_hi V + P_lo V  (P_hi now lives in the Q tile, P_lo in the K tile)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(q, ks), mndesc(v, ks), iKM, 1);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(k, ks), mndesc(v, ks), iKM, 1);
+          mma_commit(o_full);
+        }
+        mma_commit(&empty[s]);
+      }
+      if (kStateOnly) mma_commit(mma1_done);
+      mma_commit(drain);
+      wait_drain(drain, 0);
+    }
+  } else if (warp < kWarpEpi) {
+    // ---------------- feature-map warpgroup ----------------
+    const int i = threadIdx.x - kWarpPhi * 32;  // row in the row pass, column in the column pass
+    // partial states of the first pass start from zero; a segment starts from the caller's state plus them
+    float z = (!kStateOnly && p.z0) ? p.z0[(long)bh * kD + i] : 0.f;
+    for (int qp = 0; qp < init_parts; ++qp) z += p.part_z[((long)bh * p.nparts + qp) * kD + i];
+    zs[i] = z;
+    named_bar(kBarPhi, 128);
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kStages;
+      const uint32_t u = c / kStages;
+      const bool ok = mbar_wait(&full[s], u & 1, abort_word, status);
+      if (bar_or(kBarPhi, 128, !ok)) break;
+      const int tv = (int)min((long)kC, t_end - (t_begin + (long)c * kC));
+      uint8_t *Kt = sm + Lay::K + s * kTile;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4 *ptr = reinterpret_cast<uint4 *>(Kt + h * kBlk + sw128_offset(i, j * 8));
+          *ptr = phi8(*ptr);
+        }
+      if (!kStateOnly) {
+        uint8_t *Qt = sm + Lay::Q + s * kTile;
+        float dx = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint4 *ptr = reinterpret_cast<uint4 *>(Qt + h * kBlk + sw128_offset(i, j * 8));
+            const uint4 y = phi8(*ptr);
+            *ptr = y;
+            dx += dot8(y, zs + h * 64 + j * 8);
+          }
+        den_x[s * kC + i] = dx;  // phi(q_i) . z_prev with the bf16 phi(q) the MMA reads
+      }
+      named_bar(kBarPhi, 128);  // every row transformed; every read of zs done
+      // column sums of phi(K) over the valid rows (bf16 values, as the MMA sees them)
+      const uint8_t *col = Kt + (i >> 6) * kBlk;
+      float acc = 0.f;
+      for (int t = 0; t < tv; ++t)
+        acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(col + sw128_offset(t, i & 63)));
+      zs[i] += acc;
+      fence_async_smem();
+      mbar_arrive(&phi_done[s]);
+      named_bar(kBarPhi, 128);  // zs complete before the next chunk reads it
+    }
+    if (!*abort_word) {
+      if (kStateOnly) p.part_z[((long)bh * p.nparts + blockIdx.x) * kD + i] = zs[i];
+      else if (last_seg) p.z_out[(long)bh * kD + i] = zs[i];
+    }
+  } else {
+    // ---------------- epilogue warpgroup ----------------
+    const int quarter = warp & 3;
+    const int T = quarter * 32 + lane;  // TMEM lane: chunk row (token) or state row (feature)
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint32_t r[32];
+    bool ok = true;
+    if (!kStateOnly) {
+      uint8_t *Sb = sm + Lay::Sb;
+      // initial state: caller's state plus the parts before this segment
+      for (int cb = 0; cb < 4; ++cb) {
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        if (p.S0) {
+          const float4 *src = reinterpret_cast<const float4 *>(p.S0 + ((long)bh * kD + T) * kD + cb * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 x = src[e];
+            v[4 * e] += x.x, v[4 * e + 1] += x.y, v[4 * e + 2] += x.z, v[4 * e + 3] += x.w;
+          }
+        }
+        for (int qp = 0; qp < init_parts; ++qp) {
+          const float4 *src = reinterpret_cast<const float4 *>(
+              p.part_S + (((long)bh * p.nparts + qp) * kD + T) * kD + cb * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 x = src[e];
+            v[4 * e] += x.x, v[4 * e + 1] += x.y, v[4 * e + 2] += x.z, v[4 * e + 3] += x.w;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(v[e]);
+        tmem_st32(tl + kColS + cb * 32, r);
+        store_row32_bf16(Sb, T, cb * 32, v);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(sb_ready);
+
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kStages;
+        const uint32_t u = c / kStages;
+        const long tok = t_begin + (long)c * kC;
+        const int tv = (int)min((long)kC, t_end - tok);
+        bool w = mbar_wait(&phi_done[s], u & 1, abort_word, status) &&
+                 mbar_wait(mma1_done, c & 1, abort_word, status);
+        if (bar_or(kBarEpi, 128, !w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float den = den_x[s * kC + T];
+        // P -> masked, split into bf16 hi/lo written over the (consumed) Q and K tiles
+        uint8_t *Ph = sm + Lay::Q + s * kTile, *Pl = sm + Lay::K + s * kTile;
+        float rs = 0.f;
+        for (int cb = 0; cb < 4; ++cb) {
+          tmem_ld32(tl + kColP + cb * 32, r);
+          float hv[32], lv[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = cb * 32 + e;
+            const float pv = (j <= T && j < tv) ? __uint_as_float(r[e]) : 0.f;
+            const float h = __bfloat162float(__float2bfloat16_rn(pv));
+            const float l = __bfloat162float(__float2bfloat16_rn(pv - h));
+            hv[e] = h;
+            lv[e] = l;
+            rs += h + l;
+          }
+          store_row32_bf16(Ph, T, cb * 32, hv);
+          store_row32_bf16(Pl, T, cb * 32, lv);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(pp_ready);
+        den = (den + rs) + p.eps;
+        // bf16 copy of the updated state for the next chunk's cross read
+        for (int cb = 0; cb < 4; ++cb) {
+          tmem_ld32(tl + kColS + cb * 32, r);
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+          store_row32_bf16(Sb, T, cb * 32, v);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(sb_ready);
+        // normalised outputs
+        w = mbar_wait(o_full, c & 1, abort_word, status);
+        if (bar_or(kBarEpi, 128, !w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float inv = 1.f / den;
+        const long row = tok + T;
+        const bool store = T < tv && row >= p.n_exact;
+        float4 *dst = reinterpret_cast<float4 *>(p.out + ((long)bh * p.N + row) * kD);
+        for (int cb = 0; cb < 4; ++cb) {
+          tmem_ld32(tl + kColO + cb * 32, r);
+          if (store) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[cb * 8 + e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                            __uint_as_float(r[4 * e + 2]) * inv,
+                                            __uint_as_float(r[4 * e + 3]) * inv);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(o_free);
+      }
+    } else {
+      const bool w = mbar_wait(mma1_done, 0, abort_word, status);
+      ok = !bar_or(kBarEpi, 128, !w);
+      tc_fence_after();
+    }
+    // final (or partial) state, fp32
+    if (ok && !*abort_word && (kStateOnly || last_seg)) {
+      float *dst = kStateOnly ? p.part_S + (((long)bh * p.nparts + blockIdx.x) * kD + T) * kD
+                              : p.S_out + ((long)bh * kD + T) * kD;
+      for (int cb = 0; cb < 4; ++cb) {
+        tmem_ld32(tl + kColS + cb * 32, r);
+        float4 *d4 = reinterpret_cast<float4 *>(dst + cb * 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          d4[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                              __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lay::TmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// [BH][N][128] bf16 viewed as a 3-D tensor; boxes of 64 features x 128 tokens x 1 head.
+bool make_map(CUtensorMap *m, const void *base, long BH, long N) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)N * kD * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kStateOnly>
+cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream) {
+  static std::once_flag once[2];
+  static cudaError_t attr_err[2];
+  std::call_once(once[kStateOnly], [] {
+    attr_err[kStateOnly] = cudaFuncSetAttribute(causal_tc_kernel<kStateOnly>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)Layout<kStateOnly>::Alloc);
+  });
+  if (attr_err[kStateOnly] != cudaSuccess) return attr_err[kStateOnly];
+  causal_tc_kernel<kStateOnly><<<grid, kThreads, Layout<kStateOnly>::Alloc, stream>>>(tp);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+}  // namespace
+
+bool causal_tc_supported(const Problem &p) {
+  const DeviceInfo &di = device_info(-1);
+  return p.dt == LA_BF16 && p.dk == kD && p.dv == kD && di.cc_major == 10 && di.cc_minor == 3 &&
+         p.N <= 0x7fffffffL && encode_fn() != nullptr;
+}
+
+cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
+  const DeviceInfo &di = device_info(-1);
+  const long sms = std::max(1, di.sm_count);
+  const long chunks = (p.N + kC - 1) / kC;
+  // segments per head: enough CTAs to cover the SMs once, at least 4 chunks each
+  long G = std::max(1L, std::min(sms / p.BH, chunks / 4));
+  const long seg_chunks = (chunks + G - 1) / G;
+  G = (chunks + seg_chunks - 1) / seg_chunks;
+  // first-pass parts per segment: the largest divisor of seg_chunks that keeps the pass within one wave
+  long r = 1;
+  if (G > 1)
+    for (long d = seg_chunks; d >= 1; --d)
+      if (seg_chunks % d == 0 && p.BH * (G - 1) * d <= sms) {
+        r = d;
+        break;
+      }
+  const long nparts = (G - 1) * r;
+
+  const size_t state_f = (size_t)kD * kD + kD;
+  const size_t scratch_f = (size_t)p.BH * nparts * state_f + (from_state ? (size_t)p.BH * state_f : 0);
+  float *scratch = nullptr;
+  cudaError_t e = cudaSuccess;
+  if (scratch_f) {
+    e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), scratch_f * sizeof(float), p.stream);
+    if (e != cudaSuccess) return e;
+  }
+  float *part_S = scratch;
+  float *part_z = scratch ? part_S + (size_t)p.BH * nparts * kD * kD : nullptr;
+  const float *S0 = nullptr, *z0 = nullptr;
+  if (from_state) {
+    // the last segment overwrites the caller's state, so every reader uses a copy
+    float *Sc = part_z + (size_t)p.BH * nparts * kD;
+    float *zc = Sc + (size_t)p.BH * kD * kD;
+    e = cudaMemcpyAsync(Sc, p.S, sizeof(float) * p.BH * kD * kD, cudaMemcpyDeviceToDevice, p.stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(zc, p.z, sizeof(float) * p.BH * kD, cudaMemcpyDeviceToDevice, p.stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(scratch, p.stream);
+      return e;
+    }
+    S0 = Sc;
+    z0 = zc;
+  }
+
+  TcParams tp;
+  memset(&tp, 0, sizeof tp);
+  if (!make_map(&tp.tq, p.q, p.BH, p.N) || !make_map(&tp.tk, p.k, p.BH, p.N) ||
+      !make_map(&tp.tv, p.v, p.BH, p.N)) {
+    if (scratch) cudaFreeAsync(scratch, p.stream);
+    return cudaErrorInvalidValue;
+  }
+  tp.out = p.out;
+  tp.S_out = p.S;
+  tp.z_out = p.z;
+  tp.S0 = S0;
+  tp.z0 = z0;
+  tp.part_S = part_S;
+  tp.part_z = part_z;
+  tp.N = p.N;
+  tp.seg_len = (int)(seg_chunks * kC);
+  tp.nseg = (int)G;
+  tp.part_len = (int)(seg_chunks / r * kC);
+  tp.nparts = (int)nparts;
+  tp.parts_per_seg = (int)r;
+  tp.n_exact = (int)std::min<long>(p.N, kExact);
+  tp.eps = p.eps;
+
+  if (nparts > 0) e = launch_kernel<true>(tp, dim3((unsigned)nparts, (unsigned)p.BH), p.stream);
+  if (e == cudaSuccess) e = launch_kernel<false>(tp, dim3((unsigned)G, (unsigned)p.BH), p.stream);
+  if (e == cudaSuccess) e = launch_causal_exact_head(p, tp.n_exact, S0, z0);
+  if (scratch) {
+    const cudaError_t f = cudaFreeAsync(scratch, p.stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return e;
+}
+
+cudaError_t read_and_clear_device_status(unsigned int *value) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_device_status, sizeof(unsigned int));
+  if (e == cudaSuccess && *value) e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
+  return e;
+}
+
+}  // namespace la

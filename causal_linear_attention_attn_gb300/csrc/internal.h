@@ -25,6 +25,17 @@ struct Problem {
 // write_state: store the final S, z.
 cudaError_t launch_causal_simt(const Problem &p, long n_proc, bool from_state, bool write_state);
 
+// Exact fp32 pass over tokens [0, n_exact) of every head (outputs only),
+// starting from (S0, z0) when given (device pointers), else from zero.
+cudaError_t launch_causal_exact_head(const Problem &p, long n_exact, const float *S0, const float *z0);
+
+// Tensor-core chunked causal path (bf16, d_k = d_v = 128, sm_103).
+bool causal_tc_supported(const Problem &p);
+cudaError_t launch_causal_tc(const Problem &p, bool from_state);
+
+// Read and clear the device status word (bounded-wait timeouts).
+cudaError_t read_and_clear_device_status(unsigned int *value);
+
 // Global form: state build (S, z are zeroed and accumulated) then the read.
 cudaError_t launch_global_simt(const Problem &p);
 

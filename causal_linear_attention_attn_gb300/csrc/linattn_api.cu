@@ -98,6 +98,18 @@ const char *la_last_error_detail(void) {
   return buf;
 }
 
+la_status la_device_status(void *stream) {
+  int dev;
+  la_status st = la::current_device(&dev);
+  if (st != LA_OK) return st;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return la::from_cuda(e);
+  unsigned int v = 0;
+  e = la::read_and_clear_device_status(&v);
+  if (e != cudaSuccess) return la::from_cuda(e);
+  return v ? LA_ERR_TIMEOUT : LA_OK;
+}
+
 unsigned long long la_kernel_launches(void) { return la::g_launches.load(std::memory_order_relaxed); }
 
 const char *la_status_string(la_status s) {
@@ -129,6 +141,7 @@ static la_status causal_impl(const void *q, const void *k, const void *v, float 
     if (e == cudaSuccess) e = cudaMemsetAsync(z, 0, sizeof(float) * (size_t)p.BH * d_k, p.stream);
     return la::from_cuda(e);
   }
+  if (la::causal_tc_supported(p)) return la::from_cuda(la::launch_causal_tc(p, from_state));
   return la::from_cuda(la::launch_causal_simt(p, p.N, from_state, true));
 }
 

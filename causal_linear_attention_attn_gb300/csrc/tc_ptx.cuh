@@ -15,10 +15,16 @@ namespace tc {
 // CTA drains quickly) and in a device status word the host can read back.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kAbortTimeout = 1u;
-constexpr long long kWaitLimit = 1ll << 26;  // try_wait polls (each polls ~hundreds of ns at most)
+constexpr unsigned long long kWaitNs = 4000000000ull;  // a wait gives up after 4 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -53,13 +59,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false if the
-// wait gave up: either this thread ran out of polls (it then raises the
-// abort word and the device status) or another thread already aborted.
+// wait gave up: either it ran past kWaitNs (this thread then raises the abort
+// word and the device status word) or another thread already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_word,
                                           unsigned int *status) {
-  for (long long i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (*abort_word) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) break;
   }
   atomicOr((unsigned int *)abort_word, kAbortTimeout);
   if (status) atomicOr(status, kAbortTimeout);

@@ -35,6 +35,8 @@ lib.la_status_string.argtypes = [_i]
 lib.la_status_string.restype = ctypes.c_char_p
 lib.la_version.argtypes = []
 lib.la_version.restype = _i
+lib.la_device_status.argtypes = [_vp]
+lib.la_device_status.restype = _i
 lib.la_last_error_detail.argtypes = []
 lib.la_last_error_detail.restype = ctypes.c_char_p
 lib.la_kernel_launches.argtypes = []
@@ -144,6 +146,11 @@ def la_decode_step(q, k, v, S, z, out=None, eps: float = 1e-6, stream=None):
     if rc != 0:
         raise LinAttnError("la_decode_step", rc)
     return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the device status: 0 = OK, 6 = a bounded wait timed out."""
+    return int(lib.la_device_status(_stream(stream)))
 
 
 def kernel_launches() -> int:

@@ -137,6 +137,15 @@ LA_API la_status la_decode_step(const void *q, const void *k, const void *v, flo
                          float *z, int B, int H, int d_k, int d_v, float eps, la_dtype dt,
                          void *stream);
 
+/*
+ * Synchronizes `stream`, then reads and clears the library's device status
+ * word on the current device.  Returns LA_ERR_TIMEOUT if a bounded
+ * device-side wait inside one of the library's kernels gave up since the
+ * last check (that call's outputs are not valid), LA_OK otherwise, or the
+ * error of the synchronization itself.
+ */
+LA_API la_status la_device_status(void *stream);
+
 /* Static English description of a status code (never NULL). */
 LA_API const char *la_status_string(la_status s);
 

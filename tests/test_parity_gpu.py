@@ -36,7 +36,9 @@ def _run(L, form, q, k, v, eps):
 
 
 SMALL = [(1, 1, 1, 32, 32), (1, 2, 63, 64, 32), (2, 1, 129, 32, 128), (1, 3, 300, 128, 128),
-         (1, 2, 1000, 128, 64), (2, 2, 257, 64, 64), (1, 1, 640, 128, 128)]
+         (1, 2, 1000, 128, 64), (2, 2, 257, 64, 64), (1, 1, 640, 128, 128),
+         # d = 128 bf16 shapes that split heads into several segments, with ragged tails
+         (1, 1, 2000, 128, 128), (1, 2, 1100, 128, 128), (3, 1, 4097, 128, 128), (1, 1, 127, 128, 128)]
 
 
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
@@ -163,10 +165,9 @@ def test_causal_prefix_then_decode_equals_longer_causal(cuda_lib):
         assert_close(o, ref[:, :, t], 2e-2, f"token {t}")
 
 
-@pytest.mark.parametrize("split", [1, 64, 200, 511])
-def test_causal_with_state_continues_the_prefix(cuda_lib, split):
+@pytest.mark.parametrize("split,N", [(1, 700), (64, 700), (200, 700), (511, 700), (1000, 3000), (129, 2200)])
+def test_causal_with_state_continues_the_prefix(cuda_lib, split, N):
     w = W["causal_bf16"]
-    N = 700
     q, k, v = inputs.make_qkv(w, N=N, B=1, H=2)
     ref, rS, rz = oracle_seq("causal", q, k, v, w.eps)
     d = lambda t: t.contiguous().to(DEV)
@@ -217,3 +218,11 @@ def test_large_magnitude_inputs_stay_finite(cuda_lib):
     out, S, z = _run(cuda_lib, "causal", q, k, v, w.eps)
     ro, rS, rz = oracle_seq("causal", q, k, v, w.eps)
     assert_close(out, ro, 2e-2, "out")
+
+
+def test_no_bounded_wait_timed_out(cuda_lib):
+    """Every tensor-core call above finished without a device-side wait giving up."""
+    w = W["causal_bf16"]
+    q, k, v = inputs.make_qkv(w, N=1500, B=1, H=2)
+    _run(cuda_lib, "causal", q, k, v, w.eps)
+    assert cuda_lib.device_status() == 0
