@@ -129,10 +129,12 @@ cudaError_t launch_t(const Problem &p, long n_proc, bool from_state, bool write_
   return e;
 }
 
-// Exact fp32 outputs for tokens [0, ne) of a head, output columns
-// [32*blockIdx.y, +32).  The leading tokens of a sequence read a state built
-// from few tokens, so their outputs are O(1) while the rest average down;
-// they get full fp32 weights here instead of the tensor cores' bf16 operands.
+// Exact fp32 outputs for tokens [0, ne) of a head (ne <= 64), 16 query rows
+// per CTA.  The leading tokens of a sequence read a state built from few
+// tokens, so their outputs are O(1) while later ones average down; they get
+// full fp32 weights here instead of the tensor cores' bf16 operands.
+constexpr int kHeadRows = 16;
+
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
     causal_exact_head_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
@@ -140,70 +142,68 @@ __global__ void __launch_bounds__(kThreads)
                              long N, int ne, int dk, int dv, float eps) {
   extern __shared__ float sm[];
   const int dkp = dk + 1;
-  float *Qs = sm;                     // [kT][dkp]
-  float *Ks = Qs + kT * dkp;          // [kT][dkp]
-  float *Vs = Ks + kT * dkp;          // [kT][32]
-  float *A = Vs + kT * 32;            // [kT][kT+1]
-  float *den = A + kT * (kT + 1);     // [kT]
-  float *Ss = den + kT;               // [dk][32] (with an initial state)
-  float *zz = Ss + dk * 32;           // [dk]
   const long bh = blockIdx.x;
-  const int c0 = blockIdx.y * 32;
+  const int r0 = blockIdx.y * kHeadRows;
+  const int rows = min(kHeadRows, ne - r0);
+  const int nk = r0 + rows;  // keys visible to these rows
+  float *Ks = sm;                          // [kT][dkp]
+  float *Vs = Ks + kT * dkp;               // [kT][dv]
+  float *Qs = Vs + kT * dv;                // [kHeadRows][dkp]
+  float *A = Qs + kHeadRows * dkp;         // [kHeadRows][kT+1]
+  float *den = A + kHeadRows * (kT + 1);   // [kHeadRows]
+  float *zz = den + kHeadRows;             // [dk]
   const int tid = threadIdx.x;
-  const Tin *qh = q + bh * N * dk, *kh = k + bh * N * dk, *vh = v + bh * N * dv;
-  for (int e = tid; e < ne * dk; e += kThreads) {
+  const Tin *qh = q + (bh * N + r0) * dk, *kh = k + bh * N * dk, *vh = v + bh * N * dv;
+  for (int e = tid; e < nk * dk; e += kThreads) {
     const int t = e / dk, i = e - t * dk;
-    Qs[t * dkp + i] = phi(ldf(qh + e));
     Ks[t * dkp + i] = phi(ldf(kh + e));
   }
-  for (int e = tid; e < ne * 32; e += kThreads) {
-    const int t = e >> 5, c = e & 31;
-    Vs[e] = ldf(vh + (long)t * dv + c0 + c);
+  for (int e = tid; e < nk * dv; e += kThreads) Vs[e] = ldf(vh + e);
+  for (int e = tid; e < rows * dk; e += kThreads) {
+    const int t = e / dk, i = e - t * dk;
+    Qs[t * dkp + i] = phi(ldf(qh + e));
   }
-  if (S0) {
-    for (int e = tid; e < dk * 32; e += kThreads) {
-      const int i = e >> 5, c = e & 31;
-      Ss[e] = S0[(bh * dk + i) * dv + c0 + c];
-    }
+  if (S0)
     for (int i = tid; i < dk; i += kThreads) zz[i] = z0[bh * dk + i];
-  }
   __syncthreads();
-  for (int e = tid; e < ne * ne; e += kThreads) {
-    const int t = e / ne, j = e - t * ne;
+  for (int e = tid; e < rows * nk; e += kThreads) {
+    const int t = e / nk, j = e - t * nk;
     float a = 0.f;
-    if (j <= t)
+    if (j <= r0 + t)
       for (int i = 0; i < dk; ++i) a = fmaf(Qs[t * dkp + i], Ks[j * dkp + i], a);
     A[t * (kT + 1) + j] = a;
   }
   __syncthreads();
-  for (int t = tid; t < ne; t += kThreads) {
+  for (int t = tid; t < rows; t += kThreads) {
     float d = 0.f;
     if (S0)
       for (int i = 0; i < dk; ++i) d = fmaf(Qs[t * dkp + i], zz[i], d);
     float a = 0.f;
-    for (int j = 0; j <= t; ++j) a += A[t * (kT + 1) + j];
+    for (int j = 0; j <= r0 + t; ++j) a += A[t * (kT + 1) + j];
     den[t] = (d + a) + eps;
   }
   __syncthreads();
-  for (int e = tid; e < ne * 32; e += kThreads) {
-    const int t = e >> 5, c = e & 31;
+  const float *Sh = S0 ? S0 + bh * dk * dv : nullptr;
+  for (int e = tid; e < rows * dv; e += kThreads) {
+    const int t = e / dv, c = e - t * dv;
     float n = 0.f;
-    if (S0)
-      for (int i = 0; i < dk; ++i) n = fmaf(Qs[t * dkp + i], Ss[i * 32 + c], n);
+    if (Sh)
+      for (int i = 0; i < dk; ++i) n = fmaf(Qs[t * dkp + i], Sh[i * dv + c], n);
     float m = 0.f;
-    for (int j = 0; j <= t; ++j) m = fmaf(A[t * (kT + 1) + j], Vs[j * 32 + c], m);
-    out[(bh * N + t) * dv + c0 + c] = (n + m) / den[t];
+    for (int j = 0; j <= r0 + t; ++j) m = fmaf(A[t * (kT + 1) + j], Vs[j * dv + c], m);
+    out[(bh * N + r0 + t) * dv + c] = (n + m) / den[t];
   }
 }
 
 template <typename Tin>
 cudaError_t launch_head_t(const Problem &p, int ne, const float *S0, const float *z0) {
-  const size_t smem = sizeof(float) * (2 * (size_t)kT * (p.dk + 1) + (size_t)kT * 32 + (size_t)kT * (kT + 1) +
-                                       kT + (size_t)p.dk * 32 + p.dk);
+  const size_t smem = sizeof(float) * ((size_t)kT * (p.dk + 1) + (size_t)kT * p.dv + (size_t)kHeadRows * (p.dk + 1) +
+                                       (size_t)kHeadRows * (kT + 1) + kHeadRows + p.dk);
   cudaError_t e = cudaFuncSetAttribute(causal_exact_head_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  causal_exact_head_kernel<Tin><<<dim3(p.BH, p.dv / 32), kThreads, smem, p.stream>>>(
+  const unsigned row_blocks = (unsigned)((ne + kHeadRows - 1) / kHeadRows);
+  causal_exact_head_kernel<Tin><<<dim3(p.BH, row_blocks), kThreads, smem, p.stream>>>(
       (const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, p.out, S0, z0, p.N, ne, p.dk, p.dv, p.eps);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();

@@ -50,10 +50,11 @@ constexpr int kC = 128;               // tokens per chunk = MMA M
 constexpr int kD = 128;               // d_k = d_v
 constexpr uint32_t kBlk = 16384;      // one [128 rows x 64] bf16 block, 128-byte swizzled
 constexpr uint32_t kTile = 2 * kBlk;  // [128 x 128] bf16 tile
-constexpr int kThreads = 320;
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpPhi = 2, kWarpEpi = 6;
+constexpr int kThreads = 448;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpPhi = 2, kWarpEpi = 10;
+constexpr int kPhiThreads = 256;  // warps 2-5 transform Q rows, warps 6-9 K rows
+constexpr uint32_t kBarK = 3;      // named barrier of the K warps
 constexpr uint32_t kBarPhi = 1, kBarEpi = 2;  // named barrier ids
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
 constexpr int kExact = 64;  // leading tokens of each head computed by the exact fp32 pass
 
 template <bool kStateOnly>
@@ -64,9 +65,10 @@ struct Layout {
   static constexpr uint32_t V = K + kStages * kTile;
   static constexpr uint32_t Sb = V + kStages * kTile;  // bf16 copy of the carried state (main mode)
   static constexpr uint32_t DenX = kStateOnly ? Sb : Sb + kTile;
-  static constexpr uint32_t Z = DenX + kStages * kC * 4;
+  static constexpr uint32_t Z = DenX + (kStateOnly ? 0 : kStages * kC * 4);
   static constexpr uint32_t Bars = Z + kD * 4;
-  static constexpr uint32_t Misc = Bars + 16 * 8;
+  static constexpr int kNumBars = 29;
+  static constexpr uint32_t Misc = Bars + kNumBars * 8;
   static constexpr uint32_t Bytes = Misc + 16;
   static constexpr uint32_t Alloc = Bytes + 1024;  // slack for aligning the base to 1024 bytes
   static constexpr uint32_t TmemCols = kStateOnly ? 128 : 512;
@@ -74,8 +76,14 @@ struct Layout {
 static_assert(Layout<false>::Alloc <= 232448, "shared memory budget");
 static_assert(Layout<true>::Alloc <= 232448, "shared memory budget");
 
+// TMEM columns (main mode): S accumulator, P (fp32, then split bf16 hi/lo in
+// place), the output accumulator, and two buffers of phi(Q) packed as bf16
+// pairs (the A operand of Q K^T and Q S).
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 256, kColQ = 384;
+
 struct TcParams {
   CUtensorMap tq, tk, tv;  // 3-D maps over [BH][N][128] bf16, box 64 x 128 x 1, 128-byte swizzle
+  CUtensorMap to;          // 3-D map over the fp32 output [BH][N][128], box 32 x 128 x 1, 128-byte swizzle
   float *out, *S_out, *z_out;
   const float *S0, *z0;      // initial state (nullable = zero)
   float *part_S, *part_z;    // state-only outputs / main-mode prefix inputs: [BH][nparts][128][128], [..][128]
@@ -107,13 +115,17 @@ __device__ __forceinline__ void wait_drain(uint64_t *bar, uint32_t parity) {
     }
 }
 
-// phi on two packed bf16 values, evaluated in fp32 and rounded back to bf16.
+// phi on two packed bf16 values.  Both branches are evaluated for both
+// halves and the result picked by the sign bit (no divergence): exp in fp32
+// rounded to bf16, and x + 1 as a bf16x2 add (the exact sum rounded once, the
+// same value as the fp32 sum rounded to bf16).  x = +-0 gives 1 either way.
 __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
-  float a = __uint_as_float(x << 16), b = __uint_as_float(x & 0xffff0000u);
-  a = a > 0.f ? a + 1.f : __expf(a);
-  b = b > 0.f ? b + 1.f : __expf(b);
-  __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t *>(&r);
+  const float a = __uint_as_float(x << 16), b = __uint_as_float(x & 0xffff0000u);
+  const __nv_bfloat162 e2 = __floats2bfloat162_rn(__expf(a), __expf(b));
+  const __nv_bfloat162 x1 = __hadd2(*reinterpret_cast<const __nv_bfloat162 *>(&x), __floats2bfloat162_rn(1.f, 1.f));
+  const uint32_t e = *reinterpret_cast<const uint32_t *>(&e2), p1 = *reinterpret_cast<const uint32_t *>(&x1);
+  const uint32_t m = ((x >> 15) & 0x00010001u) * 0xffffu;  // halves with the sign bit set take exp
+  return (e & m) | (p1 & ~m);
 }
 
 __device__ __forceinline__ uint4 phi8(uint4 x) {
@@ -122,11 +134,13 @@ __device__ __forceinline__ uint4 phi8(uint4 x) {
 
 __device__ __forceinline__ float dot8(uint4 y, const float *z) {
   const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+  const float4 z0 = *reinterpret_cast<const float4 *>(z), z1 = *reinterpret_cast<const float4 *>(z + 4);
+  const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
   float s = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    s = fmaf(__uint_as_float(w[e] << 16), z[2 * e], s);
-    s = fmaf(__uint_as_float(w[e] & 0xffff0000u), z[2 * e + 1], s);
+    s = fmaf(__uint_as_float(w[e] << 16), zz[2 * e], s);
+    s = fmaf(__uint_as_float(w[e] & 0xffff0000u), zz[2 * e + 1], s);
   }
   return s;
 }
@@ -138,14 +152,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 // Write 32 values (columns col0 .. col0+31 of row `row`) as bf16 into a
 // [128 x 128] tile made of two 64-column swizzled blocks.
-__device__ __forceinline__ void store_row32_bf16(uint8_t *tile, int row, int col0, const float (&v)[32]) {
+__device__ __forceinline__ void store_row32_bf16(uint8_t *tile, int row, int col0, const uint32_t (&r)[32]) {
   uint8_t *blk = tile + (col0 >> 6) * kBlk;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int c = (col0 & 63) + q * 8;
+    const float *v = reinterpret_cast<const float *>(r) + 8 * q;
     *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c)) =
-        make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
-                   pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+        make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
   }
 }
 
@@ -158,6 +172,50 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t tile, int ks) {
   return sw128_desc(tile + ks * 2048, kBlk, 1024);
 }
 
+// Column sums of the valid rows of a [128 x 128] bf16 tile: warp `w` (0..3) of
+// the group adds columns [32w, 32w+32); lane l takes the column pair
+// 32w + 2(l&15) over rows of parity l>>4, and the two parities meet through
+// one shuffle.  Lanes l < 16 return the sums of columns (c, c+1).
+__device__ __forceinline__ int column_pair_sums(const uint8_t *tile, int w, int lane, int rows, float &s0,
+                                                float &s1) {
+  const int c = 32 * w + 2 * (lane & 15);
+  const int par = lane >> 4;
+  const uint8_t *blk = tile + (c >> 6) * kBlk;
+  const int cc = c & 63;
+  // inside an 8-row swizzle atom the four rows of this parity sit at fixed offsets
+  uint32_t off[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) off[j] = sw128_offset(par + 2 * j, cc);
+  float a0 = 0.f, a1 = 0.f;
+  const int full = rows >> 3;
+#pragma unroll 2
+  for (int g = 0; g < full; ++g) {
+    const uint8_t *gb = blk + g * 1024;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t x = *reinterpret_cast<const uint32_t *>(gb + off[j]);
+      a0 += __uint_as_float(x << 16);
+      a1 += __uint_as_float(x & 0xffff0000u);
+    }
+  }
+  for (int t = 8 * full + par; t < rows; t += 2) {
+    const uint32_t x = *reinterpret_cast<const uint32_t *>(blk + sw128_offset(t, cc));
+    a0 += __uint_as_float(x << 16);
+    a1 += __uint_as_float(x & 0xffff0000u);
+  }
+  a0 += __shfl_xor_sync(0xffffffffu, a0, 16);
+  a1 += __shfl_xor_sync(0xffffffffu, a1, 16);
+  s0 = a0;
+  s1 = a1;
+  return c;
+}
+
+// Byte offset of fp32 element (row, col) in a [128 rows x 32] fp32 box written
+// with 128-byte rows and the 128-byte swizzle (16-byte chunks XOR row mod 8).
+__device__ __forceinline__ uint32_t sw128_offset_f32(uint32_t row, uint32_t col) {
+  return (row >> 3) * 1024u + (row & 7u) * 128u + ((((col >> 2) ^ row) & 7u) << 4) + ((col & 3u) << 2);
+}
+
 template <bool kStateOnly>
 __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_constant__ TcParams p) {
   using Lay = Layout<kStateOnly>;
@@ -167,9 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
   float *den_x = reinterpret_cast<float *>(sm + Lay::DenX);
   float *zs = reinterpret_cast<float *>(sm + Lay::Z);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::Bars);
-  uint64_t *full = bars, *phi_done = bars + 3, *empty = bars + 6;
-  uint64_t *mma1_done = bars + 9, *pp_ready = bars + 10, *o_full = bars + 11, *sb_ready = bars + 12,
-           *o_free = bars + 13, *drain = bars + 14;
+  // per stage: Q landed, K landed, V landed, phi applied, raw Q consumed, K free, V free
+  uint64_t *full_q = bars, *full_k = bars + 3, *full_v = bars + 6, *phi_done = bars + 9, *q_empty = bars + 12,
+           *k_empty = bars + 15, *v_empty = bars + 18;
+  uint64_t *mma1_done = bars + 21, *pp_ready = bars + 22, *o_full = bars + 23, *sb_ready = bars + 24,
+           *o_free = bars + 25, *drain = bars + 26, *qt_free = bars + 27;  // qt_free[2]: phi(Q) TMEM buffers
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::Misc);
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
   unsigned int *status = &g_device_status;
@@ -194,10 +254,17 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&phi_done[s], 128);
-      mbar_init(&empty[s], 1);
+      mbar_init(&full_q[s], 1);
+      mbar_init(&full_k[s], 1);
+      mbar_init(&full_v[s], 1);
+      mbar_init(&phi_done[s], kPhiThreads);
+      mbar_init(&q_empty[s], 128);
+      // main mode: the MMA commit plus the epilogue's 128 threads once they have read den_x[s]
+      mbar_init(&k_empty[s], kStateOnly ? 1 : 129);
+      mbar_init(&v_empty[s], 1);
     }
+    mbar_init(&qt_free[0], 1);
+    mbar_init(&qt_free[1], 1);
     mbar_init(mma1_done, 1);
     mbar_init(pp_ready, 128);
     mbar_init(o_full, 1);
@@ -219,123 +286,181 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
       if (!kStateOnly) prefetch_tmap(&p.tq);
       prefetch_tmap(&p.tk);
       prefetch_tmap(&p.tv);
-      int issued = 0;
+      int issued_q = 0, issued_k = 0, issued_v = 0;
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
         const uint32_t u = c / kStages;
-        if (c >= kStages && !mbar_wait(&empty[s], (u - 1) & 1, abort_word, status)) break;
         const int tok = (int)(t_begin + (long)c * kC);
-        mbar_arrive_expect_tx(&full[s], (kStateOnly ? 2 : 3) * kTile);
         if (!kStateOnly) {
-          tma_load_3d(sm + Lay::Q + s * kTile, &p.tq, &full[s], 0, tok, bh);
-          tma_load_3d(sm + Lay::Q + s * kTile + kBlk, &p.tq, &full[s], 64, tok, bh);
+          if (c >= kStages && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_word, status)) break;
+          mbar_arrive_expect_tx(&full_q[s], kTile);
+          tma_load_3d(sm + Lay::Q + s * kTile, &p.tq, &full_q[s], 0, tok, bh);
+          tma_load_3d(sm + Lay::Q + s * kTile + kBlk, &p.tq, &full_q[s], 64, tok, bh);
         }
-        tma_load_3d(sm + Lay::K + s * kTile, &p.tk, &full[s], 0, tok, bh);
-        tma_load_3d(sm + Lay::K + s * kTile + kBlk, &p.tk, &full[s], 64, tok, bh);
-        tma_load_3d(sm + Lay::V + s * kTile, &p.tv, &full[s], 0, tok, bh);
-        tma_load_3d(sm + Lay::V + s * kTile + kBlk, &p.tv, &full[s], 64, tok, bh);
-        issued = c + 1;
+        issued_q = c + 1;
+        if (c >= kStages && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_word, status)) break;
+        mbar_arrive_expect_tx(&full_k[s], kTile);
+        tma_load_3d(sm + Lay::K + s * kTile, &p.tk, &full_k[s], 0, tok, bh);
+        tma_load_3d(sm + Lay::K + s * kTile + kBlk, &p.tk, &full_k[s], 64, tok, bh);
+        issued_k = c + 1;
+        if (c >= kStages && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_word, status)) break;
+        mbar_arrive_expect_tx(&full_v[s], kTile);
+        tma_load_3d(sm + Lay::V + s * kTile, &p.tv, &full_v[s], 0, tok, bh);
+        tma_load_3d(sm + Lay::V + s * kTile + kBlk, &p.tv, &full_v[s], 64, tok, bh);
+        issued_v = c + 1;
       }
       // every issued copy must land before shared memory is released
-      for (int c = max(0, issued - kStages); c < issued; ++c) wait_drain(&full[c % kStages], (c / kStages) & 1);
+      if (!kStateOnly)
+        for (int c = max(0, issued_q - kStages); c < issued_q; ++c)
+          wait_drain(&full_q[c % kStages], (c / kStages) & 1);
+      for (int c = max(0, issued_k - kStages); c < issued_k; ++c)
+        wait_drain(&full_k[c % kStages], (c / kStages) & 1);
+      for (int c = max(0, issued_v - kStages); c < issued_v; ++c)
+        wait_drain(&full_v[c % kStages], (c / kStages) & 1);
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer (one thread) ----------------
     if (lane == 0) {
-      const uint32_t tP = tmem + kColP, tO = tmem + kColO, tS = tmem + kColS;
+      const uint32_t tO = tmem + kColO, tS = tmem + kColS, tP = tmem + kColP;
       constexpr uint32_t iKK = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t iKM = idesc_bf16_f32(128, 128, 0, 1);
       constexpr uint32_t iMM = idesc_bf16_f32(128, 128, 1, 1);
-      const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V),
-                     sSb = smem_u32(sm + Lay::Sb);
+      const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V), sSb = smem_u32(sm + Lay::Sb);
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
         const uint32_t u = c / kStages;
         if (!mbar_wait(&phi_done[s], u & 1, abort_word, status)) break;
-        tc_fence_after();
-        const uint32_t q = sQ + s * kTile, k = sK + s * kTile, v = sV + s * kTile;
+        if (!mbar_wait(&full_v[s], u & 1, abort_word, status)) break;
+        const uint32_t k = sK + s * kTile, v = sV + s * kTile;
         if (!kStateOnly) {
-          // P = Q K^T
+          const uint32_t tQ = tmem + kColQ + 64 * (c & 1);
+          // the single P tile is free once the previous chunk's P V has completed
+          if (c > 0 && !mbar_wait(o_full, (c - 1) & 1, abort_word, status)) break;
+          tc_fence_after();
+          // P = Q K^T, phi(Q) from tensor memory (8 columns per 16 features)
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(q, ks), kdesc(k, ks), iKK, ks > 0);
+          for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tP, tQ + 8 * ks, kdesc(k, ks), iKK, ks > 0);
           if (!mbar_wait(sb_ready, c & 1, abort_word, status)) break;
           if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status)) break;
           tc_fence_after();
           // O = Q bf16(S_prev)
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(q, ks), mndesc(sSb, ks), iKM, ks > 0);
+          for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSb, ks), iKM, ks > 0);
+        } else {
+          tc_fence_after();
         }
         // S += K^T V
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_bf16(tS, mndesc(k, ks), mndesc(v, ks), iMM, kStateOnly ? (c > 0 || ks > 0) : 1);
+        mma_commit(&k_empty[s]);
         if (!kStateOnly) {
+          mma_commit(&qt_free[c & 1]);
           mma_commit(mma1_done);
           if (!mbar_wait(pp_ready, c & 1, abort_word, status)) break;
           tc_fence_after();
-          // O += P_hi V + P_lo V  (P_hi now lives in the Q tile, P_lo in the K tile)
+          // O += P_hi V + P_lo V, P read from tensor memory: for keys [16ks, 16ks+16)
+          // columns 16ks..16ks+7 hold P_hi and 16ks+8..16ks+15 hold P_lo
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(q, ks), mndesc(v, ks), iKM, 1);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(k, ks), mndesc(v, ks), iKM, 1);
+          for (int ks = 0; ks < 8; ++ks) {
+            mma_bf16_ts(tO, tP + 16 * ks, mndesc(v, ks), iKM, 1);
+            mma_bf16_ts(tO, tP + 16 * ks + 8, mndesc(v, ks), iKM, 1);
+          }
           mma_commit(o_full);
+        } else {
+          mma_commit(&v_empty[s]);
         }
-        mma_commit(&empty[s]);
       }
       if (kStateOnly) mma_commit(mma1_done);
       mma_commit(drain);
       wait_drain(drain, 0);
     }
   } else if (warp < kWarpEpi) {
-    // ---------------- feature-map warpgroup ----------------
-    const int i = threadIdx.x - kWarpPhi * 32;  // row in the row pass, column in the column pass
-    // partial states of the first pass start from zero; a segment starts from the caller's state plus them
-    float z = (!kStateOnly && p.z0) ? p.z0[(long)bh * kD + i] : 0.f;
-    for (int qp = 0; qp < init_parts; ++qp) z += p.part_z[((long)bh * p.nparts + qp) * kD + i];
-    zs[i] = z;
-    named_bar(kBarPhi, 128);
+    // ---------------- feature-map warps: 2-5 on Q rows, 6-9 on K rows ----------------
+    const int pt = threadIdx.x - kWarpPhi * 32;  // 0..255
+    const bool is_q = warp < kWarpPhi + 4;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;         // tile row = TMEM lane of the phi(Q) buffer
+    const int kw = warp - (kWarpPhi + 4);         // K warp index 0..3 (column sums)
+    if (pt < kD) {
+      // partial states of the first pass start from zero; a segment starts from the caller's state plus them
+      float z = (!kStateOnly && p.z0) ? p.z0[(long)bh * kD + pt] : 0.f;
+      for (int qp = 0; qp < init_parts; ++qp) z += p.part_z[((long)bh * p.nparts + qp) * kD + pt];
+      zs[pt] = z;
+    }
+    named_bar(kBarPhi, kPhiThreads);
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % kStages;
       const uint32_t u = c / kStages;
-      const bool ok = mbar_wait(&full[s], u & 1, abort_word, status);
-      if (bar_or(kBarPhi, 128, !ok)) break;
       const int tv = (int)min((long)kC, t_end - (t_begin + (long)c * kC));
       uint8_t *Kt = sm + Lay::K + s * kTile;
+      float s0 = 0.f, s1 = 0.f;
+      int col = 0;
+      bool ok = true;
+      if (is_q) {
+        if (!kStateOnly) {
+          ok = mbar_wait(&full_q[s], u & 1, abort_word, status);
+          // phi(Q) row -> packed bf16 pairs -> tensor memory; den_x from the same rounded values.
+          // The phi(Q) buffer is free once the MMAs of the chunk two back have completed.
+          if (ok && c >= 2) ok = mbar_wait(&qt_free[c & 1], ((c >> 1) - 1) & 1, abort_word, status);
+          ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
+          if (ok) {
+            const uint8_t *Qt = sm + Lay::Q + s * kTile;
+            const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + 64 * (c & 1);
+            float dx = 0.f;
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {  // 32 features per step
+              uint4 xv[4];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+              for (int e = 0; e < 4; ++e)
+                xv[e] = *reinterpret_cast<const uint4 *>(Qt + (g >> 1) * kBlk + sw128_offset(row, (g & 1) * 32 + e * 8));
+              uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4 *ptr = reinterpret_cast<uint4 *>(Kt + h * kBlk + sw128_offset(i, j * 8));
-          *ptr = phi8(*ptr);
-        }
-      if (!kStateOnly) {
-        uint8_t *Qt = sm + Lay::Q + s * kTile;
-        float dx = 0.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint4 *ptr = reinterpret_cast<uint4 *>(Qt + h * kBlk + sw128_offset(i, j * 8));
-            const uint4 y = phi8(*ptr);
-            *ptr = y;
-            dx += dot8(y, zs + h * 64 + j * 8);
+              for (int e = 0; e < 4; ++e) {
+                const uint4 y = phi8(xv[e]);
+                w[4 * e] = y.x, w[4 * e + 1] = y.y, w[4 * e + 2] = y.z, w[4 * e + 3] = y.w;
+                dx += dot8(y, zs + g * 32 + e * 8);
+              }
+              tmem_st16(tq + 16 * g, w);
+            }
+            den_x[s * kC + row] = dx;  // phi(q_row) . z_prev
           }
-        den_x[s * kC + i] = dx;  // phi(q_i) . z_prev with the bf16 phi(q) the MMA reads
+          mbar_arrive(&q_empty[s]);  // raw Q consumed
+        }
+      } else {
+        ok = mbar_wait(&full_k[s], u & 1, abort_word, status);
+        if (bar_or(kBarK, 128, !ok)) {
+          ok = false;
+        } else {
+#pragma unroll 1
+          for (int g = 0; g < 4; ++g) {  // all loads of a step first: the in-place stores would order them
+            uint4 kv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              kv[e] = *reinterpret_cast<const uint4 *>(Kt + (g >> 1) * kBlk + sw128_offset(row, (g & 1) * 32 + e * 8));
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4 *>(Kt + (g >> 1) * kBlk + sw128_offset(row, (g & 1) * 32 + e * 8)) =
+                  phi8(kv[e]);
+          }
+          named_bar(kBarK, 128);  // every K row transformed
+          // column sums of phi(K) over the valid rows (bf16 values, as the MMA sees them)
+          col = column_pair_sums(Kt, kw, lane, tv, s0, s1);
+        }
       }
-      named_bar(kBarPhi, 128);  // every row transformed; every read of zs done
-      // column sums of phi(K) over the valid rows (bf16 values, as the MMA sees them)
-      const uint8_t *col = Kt + (i >> 6) * kBlk;
-      float acc = 0.f;
-      for (int t = 0; t < tv; ++t)
-        acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(col + sw128_offset(t, i & 63)));
-      zs[i] += acc;
+      if (bar_or(kBarPhi, kPhiThreads, !ok)) break;  // Q warps are done reading z
+      if (!is_q && lane < 16) {
+        zs[col] += s0;
+        zs[col + 1] += s1;
+      }
       fence_async_smem();
+      tc_fence_before();
       mbar_arrive(&phi_done[s]);
-      named_bar(kBarPhi, 128);  // zs complete before the next chunk reads it
+      named_bar(kBarPhi, kPhiThreads);  // z complete before the next chunk reads it
     }
-    if (!*abort_word) {
-      if (kStateOnly) p.part_z[((long)bh * p.nparts + blockIdx.x) * kD + i] = zs[i];
-      else if (last_seg) p.z_out[(long)bh * kD + i] = zs[i];
+    if (!*abort_word && pt < kD) {
+      if (kStateOnly) p.part_z[((long)bh * p.nparts + blockIdx.x) * kD + pt] = zs[pt];
+      else if (last_seg) p.z_out[(long)bh * kD + pt] = zs[pt];
     }
   } else {
     // ---------------- epilogue warpgroup ----------------
@@ -371,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
 #pragma unroll
         for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(v[e]);
         tmem_st32(tl + kColS + cb * 32, r);
-        store_row32_bf16(Sb, T, cb * 32, v);
+        store_row32_bf16(Sb, T, cb * 32, r);
       }
       fence_async_smem();
       tc_fence_before();
@@ -382,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
         const uint32_t u = c / kStages;
         const long tok = t_begin + (long)c * kC;
         const int tv = (int)min((long)kC, t_end - tok);
+        const uint32_t tP = tl + kColP;
         bool w = mbar_wait(&phi_done[s], u & 1, abort_word, status) &&
                  mbar_wait(mma1_done, c & 1, abort_word, status);
         if (bar_or(kBarEpi, 128, !w)) {
@@ -390,36 +516,45 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
         }
         tc_fence_after();
         float den = den_x[s * kC + T];
-        // P -> masked, split into bf16 hi/lo written over the (consumed) Q and K tiles
-        uint8_t *Ph = sm + Lay::Q + s * kTile, *Pl = sm + Lay::K + s * kTile;
+        mbar_arrive(&k_empty[s]);
+        // P -> causal mask -> bf16 hi/lo, written back over the same columns:
+        // keys [16g, 16g+16) become 8 columns of P_hi pairs then 8 of P_lo pairs.
+        // Key blocks right of this warp's rows are all masked (zeros).
         float rs = 0.f;
         for (int cb = 0; cb < 4; ++cb) {
-          tmem_ld32(tl + kColP + cb * 32, r);
-          float hv[32], lv[32];
+          if (cb > quarter) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = cb * 32 + e;
-            const float pv = (j <= T && j < tv) ? __uint_as_float(r[e]) : 0.f;
-            const float h = __bfloat162float(__float2bfloat16_rn(pv));
-            const float l = __bfloat162float(__float2bfloat16_rn(pv - h));
-            hv[e] = h;
-            lv[e] = l;
-            rs += h + l;
+            for (int e = 0; e < 32; ++e) r[e] = 0u;
+          } else {
+            tmem_ld32(tP + cb * 32, r);
+            uint32_t o[32];
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+#pragma unroll
+              for (int m = 0; m < 8; ++m) {
+                const int j = cb * 32 + g * 16 + 2 * m;
+                const float p0 = (j <= T && j < tv) ? __uint_as_float(r[g * 16 + 2 * m]) : 0.f;
+                const float p1 = (j + 1 <= T && j + 1 < tv) ? __uint_as_float(r[g * 16 + 2 * m + 1]) : 0.f;
+                const uint32_t hw = pack_bf16(p0, p1);
+                const float h0 = __uint_as_float(hw << 16), h1 = __uint_as_float(hw & 0xffff0000u);
+                const uint32_t lw = pack_bf16(p0 - h0, p1 - h1);
+                const float l0 = __uint_as_float(lw << 16), l1 = __uint_as_float(lw & 0xffff0000u);
+                rs += (h0 + l0) + (h1 + l1);
+                o[g * 16 + m] = hw;
+                o[g * 16 + 8 + m] = lw;
+              }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = o[e];
           }
-          store_row32_bf16(Ph, T, cb * 32, hv);
-          store_row32_bf16(Pl, T, cb * 32, lv);
+          tmem_st32(tP + cb * 32, r);
         }
-        fence_async_smem();
         tc_fence_before();
         mbar_arrive(pp_ready);
         den = (den + rs) + p.eps;
         // bf16 copy of the updated state for the next chunk's cross read
         for (int cb = 0; cb < 4; ++cb) {
           tmem_ld32(tl + kColS + cb * 32, r);
-          float v[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-          store_row32_bf16(Sb, T, cb * 32, v);
+          store_row32_bf16(Sb, T, cb * 32, r);
         }
         fence_async_smem();
         tc_fence_before();
@@ -431,28 +566,61 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
           break;
         }
         tc_fence_after();
+        // normalised rows -> the V tile of this stage (free: P V has completed) as two
+        // [128 x 32] fp32 swizzled boxes per half of the columns -> TMA stores.  Rows past
+        // the sequence end are clipped by the store; the leading exact rows are rewritten later.
+        // The second half is read from tensor memory before the first half's store drains,
+        // so the accumulator is released as early as possible.
         const float inv = 1.f / den;
-        const long row = tok + T;
-        const bool store = T < tv && row >= p.n_exact;
-        float4 *dst = reinterpret_cast<float4 *>(p.out + ((long)bh * p.N + row) * kD);
-        for (int cb = 0; cb < 4; ++cb) {
-          tmem_ld32(tl + kColO + cb * 32, r);
-          if (store) {
+        uint8_t *stage_o = sm + Lay::V + s * kTile;
+        uint32_t r2[32];
+        for (int b = 0; b < 2; ++b) {
+          tmem_ld32(tl + kColO + b * 32, r);
+          uint8_t *box = stage_o + b * kBlk;
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[cb * 8 + e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
-                                            __uint_as_float(r[4 * e + 2]) * inv,
-                                            __uint_as_float(r[4 * e + 3]) * inv);
-          }
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(box + sw128_offset_f32(T, 4 * q)) =
+                make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                            __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
         }
+        fence_async_smem();
+        named_bar(kBarEpi, 128);
+        if (T == 0) {
+          tma_store_3d(&p.to, stage_o, 0, (int)tok, bh);
+          tma_store_3d(&p.to, stage_o + kBlk, 32, (int)tok, bh);
+          bulk_commit();
+        }
+        tmem_ld32(tl + kColO + 64, r);
+        tmem_ld32(tl + kColO + 96, r2);
         tc_fence_before();
-        mbar_arrive(o_free);
+        mbar_arrive(o_free);  // the O accumulator has been read
+        if (T == 0) bulk_wait_read();
+        named_bar(kBarEpi, 128);  // the staging tile is free again
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          *reinterpret_cast<float4 *>(stage_o + sw128_offset_f32(T, 4 * q)) =
+              make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                          __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+          *reinterpret_cast<float4 *>(stage_o + kBlk + sw128_offset_f32(T, 4 * q)) =
+              make_float4(__uint_as_float(r2[4 * q]) * inv, __uint_as_float(r2[4 * q + 1]) * inv,
+                          __uint_as_float(r2[4 * q + 2]) * inv, __uint_as_float(r2[4 * q + 3]) * inv);
+        }
+        fence_async_smem();
+        named_bar(kBarEpi, 128);
+        if (T == 0) {
+          tma_store_3d(&p.to, stage_o, 64, (int)tok, bh);
+          tma_store_3d(&p.to, stage_o + kBlk, 96, (int)tok, bh);
+          bulk_commit();
+          bulk_wait_read();
+          mbar_arrive(&v_empty[s]);  // the V tile may be reloaded
+        }
       }
     } else {
       const bool w = mbar_wait(mma1_done, 0, abort_word, status);
       ok = !bar_or(kBarEpi, 128, !w);
       tc_fence_after();
     }
+    if (!kStateOnly && T == 0) bulk_wait_all();  // output stores complete before the CTA exits
     // final (or partial) state, fp32
     if (ok && !*abort_word && (kStateOnly || last_seg)) {
       float *dst = kStateOnly ? p.part_S + (((long)bh * p.nparts + blockIdx.x) * kD + T) * kD
@@ -503,6 +671,19 @@ bool make_map(CUtensorMap *m, const void *base, long BH, long N) {
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 output [BH][N][128]; boxes of 32 features x 128 tokens x 1 head (128-byte rows).
+bool make_out_map(CUtensorMap *m, void *base, long BH, long N) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)N * kD * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)kC, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
 template <bool kStateOnly>
@@ -576,7 +757,7 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
   TcParams tp;
   memset(&tp, 0, sizeof tp);
   if (!make_map(&tp.tq, p.q, p.BH, p.N) || !make_map(&tp.tk, p.k, p.BH, p.N) ||
-      !make_map(&tp.tv, p.v, p.BH, p.N)) {
+      !make_map(&tp.tv, p.v, p.BH, p.N) || !make_out_map(&tp.to, p.out, p.BH, p.N)) {
     if (scratch) cudaFreeAsync(scratch, p.stream);
     return cudaErrorInvalidValue;
   }
