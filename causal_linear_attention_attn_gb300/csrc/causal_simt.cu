@@ -129,14 +129,16 @@ cudaError_t launch_t(const Problem &p, long n_proc, bool from_state, bool write_
   return e;
 }
 
-// Exact fp32 outputs for tokens [0, ne) of a head (ne <= 64), 16 query rows
-// per CTA.  The leading tokens of a sequence read a state built from few
-// tokens, so their outputs are O(1) while later ones average down; they get
-// full fp32 weights here instead of the tensor cores' bf16 operands.
+// Exact fp32 outputs for tokens [0, ne) of a head (ne <= 64).  The leading
+// tokens of a sequence read a state built from few tokens, so their outputs
+// are O(1) while later ones average down; they get full fp32 weights here
+// instead of the tensor cores' bf16 operands.  One warp per query row t:
+// lanes split the keys j <= t for the weights phi(q_t).phi(k_j), then split
+// the output columns for sum_j w_j v_j.  A CTA covers 16 rows of one head.
 constexpr int kHeadRows = 16;
 
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kHeadRows * 32)
     causal_exact_head_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                              float *__restrict__ out, const float *__restrict__ S0, const float *__restrict__ z0,
                              long N, int ne, int dk, int dv, float eps) {
@@ -146,64 +148,75 @@ __global__ void __launch_bounds__(kThreads)
   const int r0 = blockIdx.y * kHeadRows;
   const int rows = min(kHeadRows, ne - r0);
   const int nk = r0 + rows;  // keys visible to these rows
-  float *Ks = sm;                          // [kT][dkp]
-  float *Vs = Ks + kT * dkp;               // [kT][dv]
-  float *Qs = Vs + kT * dv;                // [kHeadRows][dkp]
-  float *A = Qs + kHeadRows * dkp;         // [kHeadRows][kT+1]
-  float *den = A + kHeadRows * (kT + 1);   // [kHeadRows]
-  float *zz = den + kHeadRows;             // [dk]
-  const int tid = threadIdx.x;
+  float *Ks = sm;                      // [kT][dkp]
+  float *Vs = Ks + kT * dkp;           // [kT][dv]
+  float *Qs = Vs + kT * dv;            // [kHeadRows][dk]
+  float *W = Qs + kHeadRows * dk;      // [kHeadRows][kT] weights of each row
+  const int tid = threadIdx.x, nthr = kHeadRows * 32;
+  const int warp = tid >> 5, lane = tid & 31;
   const Tin *qh = q + (bh * N + r0) * dk, *kh = k + bh * N * dk, *vh = v + bh * N * dv;
-  for (int e = tid; e < nk * dk; e += kThreads) {
+  // eight elements per load (rows are 16-byte aligned for the supported sizes)
+  for (int e = 8 * tid; e < nk * dk; e += 8 * nthr) {
     const int t = e / dk, i = e - t * dk;
-    Ks[t * dkp + i] = phi(ldf(kh + e));
+    float f[8];
+    ld8(kh + e, f);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) Ks[t * dkp + i + x] = phi(f[x]);
   }
-  for (int e = tid; e < nk * dv; e += kThreads) Vs[e] = ldf(vh + e);
-  for (int e = tid; e < rows * dk; e += kThreads) {
-    const int t = e / dk, i = e - t * dk;
-    Qs[t * dkp + i] = phi(ldf(qh + e));
+  for (int e = 8 * tid; e < nk * dv; e += 8 * nthr) {
+    float f[8];
+    ld8(vh + e, f);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) Vs[e + x] = f[x];
   }
-  if (S0)
-    for (int i = tid; i < dk; i += kThreads) zz[i] = z0[bh * dk + i];
+  for (int e = 8 * tid; e < rows * dk; e += 8 * nthr) {
+    float f[8];
+    ld8(qh + e, f);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) Qs[e + x] = phi(f[x]);
+  }
   __syncthreads();
-  for (int e = tid; e < rows * nk; e += kThreads) {
-    const int t = e / nk, j = e - t * nk;
+  if (warp >= rows) return;
+  const int t = r0 + warp;  // this warp's query row
+  const float *qt = Qs + warp * dk;
+  float *wt = W + warp * kT;
+  // weights: lane handles keys j = lane, lane + 32
+  float wsum = 0.f;
+  for (int j = lane; j <= t; j += 32) {
     float a = 0.f;
-    if (j <= r0 + t)
-      for (int i = 0; i < dk; ++i) a = fmaf(Qs[t * dkp + i], Ks[j * dkp + i], a);
-    A[t * (kT + 1) + j] = a;
+    for (int i = 0; i < dk; ++i) a = fmaf(qt[i], Ks[j * dkp + i], a);
+    wt[j] = a;
+    wsum += a;
   }
-  __syncthreads();
-  for (int t = tid; t < rows; t += kThreads) {
-    float d = 0.f;
-    if (S0)
-      for (int i = 0; i < dk; ++i) d = fmaf(Qs[t * dkp + i], zz[i], d);
-    float a = 0.f;
-    for (int j = 0; j <= r0 + t; ++j) a += A[t * (kT + 1) + j];
-    den[t] = (d + a) + eps;
+  wsum = warp_sum(wsum);
+  float d = 0.f;
+  if (S0) {
+    for (int i = lane; i < dk; i += 32) d = fmaf(qt[i], z0[bh * dk + i], d);
+    d = warp_sum(d);
   }
-  __syncthreads();
+  const float den = (d + wsum) + eps;
+  __syncwarp();
+  // outputs: lane handles columns c = lane, lane + 32, ...
   const float *Sh = S0 ? S0 + bh * dk * dv : nullptr;
-  for (int e = tid; e < rows * dv; e += kThreads) {
-    const int t = e / dv, c = e - t * dv;
+  for (int c = lane; c < dv; c += 32) {
     float n = 0.f;
     if (Sh)
-      for (int i = 0; i < dk; ++i) n = fmaf(Qs[t * dkp + i], Sh[i * dv + c], n);
+      for (int i = 0; i < dk; ++i) n = fmaf(qt[i], Sh[i * dv + c], n);
     float m = 0.f;
-    for (int j = 0; j <= r0 + t; ++j) m = fmaf(A[t * (kT + 1) + j], Vs[j * dv + c], m);
-    out[(bh * N + r0 + t) * dv + c] = (n + m) / den[t];
+    for (int j = 0; j <= t; ++j) m = fmaf(wt[j], Vs[j * dv + c], m);
+    out[(bh * N + t) * dv + c] = (n + m) / den;
   }
 }
 
 template <typename Tin>
 cudaError_t launch_head_t(const Problem &p, int ne, const float *S0, const float *z0) {
-  const size_t smem = sizeof(float) * ((size_t)kT * (p.dk + 1) + (size_t)kT * p.dv + (size_t)kHeadRows * (p.dk + 1) +
-                                       (size_t)kHeadRows * (kT + 1) + kHeadRows + p.dk);
+  const size_t smem = sizeof(float) * ((size_t)kT * (p.dk + 1) + (size_t)kT * p.dv + (size_t)kHeadRows * p.dk +
+                                       (size_t)kHeadRows * kT);
   cudaError_t e = cudaFuncSetAttribute(causal_exact_head_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   const unsigned row_blocks = (unsigned)((ne + kHeadRows - 1) / kHeadRows);
-  causal_exact_head_kernel<Tin><<<dim3(p.BH, row_blocks), kThreads, smem, p.stream>>>(
+  causal_exact_head_kernel<Tin><<<dim3(p.BH, row_blocks), kHeadRows * 32, smem, p.stream>>>(
       (const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, p.out, S0, z0, p.N, ne, p.dk, p.dv, p.eps);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();

@@ -22,16 +22,20 @@
 // reduces K^T V over parts of the earlier segments, and each segment starts
 // from the sum of the parts before it.
 //
-// Warp roles (10 warps): 0 TMA producer; 1 MMA issuer and TMEM owner;
-// 2-5 feature-map warpgroup (phi in place on the staged Q/K tiles, z and the
-// cross-chunk denominator); 6-9 epilogue warpgroup (P split, bf16 state copy,
-// normalised fp32 outputs, final state).  Every mbarrier wait is bounded; a
-// wait that runs out raises the CTA abort word and the device status word,
-// the CTA drains its in-flight copies and MMAs, frees TMEM and exits.
+// Warp roles (18 warps): 0 TMA producer; 1 MMA issuer and TMEM owner;
+// 2-5 phi(Q) into tensor memory and the cross-chunk denominator phi(Q).z;
+// 6-9 phi(K) in place and the column sums that advance z; 10-13 P split,
+// denominator and bf16 state copy (and the final state); 14-17 normalised
+// fp32 outputs through shared memory and TMA stores.  Every mbarrier wait is
+// bounded; a wait that runs out raises the CTA abort word and the device
+// status word, the CTA drains its in-flight copies and MMAs, frees TMEM and
+// exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -50,10 +54,10 @@ constexpr int kC = 128;               // tokens per chunk = MMA M
 constexpr int kD = 128;               // d_k = d_v
 constexpr uint32_t kBlk = 16384;      // one [128 rows x 64] bf16 block, 128-byte swizzled
 constexpr uint32_t kTile = 2 * kBlk;  // [128 x 128] bf16 tile
-constexpr int kThreads = 448;
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpPhi = 2, kWarpEpi = 10;
-constexpr int kPhiThreads = 256;  // warps 2-5 transform Q rows, warps 6-9 K rows
-constexpr uint32_t kBarK = 3;      // named barrier of the K warps
+constexpr int kThreads = 576;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpPhi = 2, kWarpEpi = 10, kWarpOut = 14;
+constexpr uint32_t kBarOut = 4;  // named barrier of the output warps
+constexpr int kPhiThreads = 256;  // feature-map warps 2-9
 constexpr uint32_t kBarPhi = 1, kBarEpi = 2;  // named barrier ids
 constexpr int kExact = 64;  // leading tokens of each head computed by the exact fp32 pass
 
@@ -64,13 +68,16 @@ struct Layout {
   static constexpr uint32_t K = kStateOnly ? 0 : kStages * kTile;
   static constexpr uint32_t V = K + kStages * kTile;
   static constexpr uint32_t Sb = V + kStages * kTile;  // bf16 copy of the carried state (main mode)
-  static constexpr uint32_t DenX = kStateOnly ? Sb : Sb + kTile;
-  static constexpr uint32_t Z = DenX + (kStateOnly ? 0 : kStages * kC * 4);
+  static constexpr uint32_t DenX = kStateOnly ? Sb : Sb + kTile;       // phi(q).z per row, per stage
+  static constexpr uint32_t Den = DenX + (kStateOnly ? 0 : kStages * kC * 4);  // final denominators, 2 chunks
+  static constexpr uint32_t Z = Den + (kStateOnly ? 0 : 2 * kC * 4);
   static constexpr uint32_t Bars = Z + kD * 4;
-  static constexpr int kNumBars = 29;
+  static constexpr int kNumBars = 34;
   static constexpr uint32_t Misc = Bars + kNumBars * 8;
   static constexpr uint32_t Bytes = Misc + 16;
-  static constexpr uint32_t Alloc = Bytes + 1024;  // slack for aligning the base to 1024 bytes
+  // The dynamic shared memory base follows the 1 KB reserved per block and is
+  // 1024-aligned; the kernel checks this and refuses to run otherwise.
+  static constexpr uint32_t Alloc = Bytes;
   static constexpr uint32_t TmemCols = kStateOnly ? 128 : 512;
 };
 static_assert(Layout<false>::Alloc <= 232448, "shared memory budget");
@@ -80,6 +87,7 @@ static_assert(Layout<true>::Alloc <= 232448, "shared memory budget");
 // place), the output accumulator, and two buffers of phi(Q) packed as bf16
 // pairs (the A operand of Q K^T and Q S).
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 256, kColQ = 384;
+constexpr uint32_t kAbortMisaligned = 2u;  // status bit: shared memory base not 1024-aligned
 
 struct TcParams {
   CUtensorMap tq, tk, tv;  // 3-D maps over [BH][N][128] bf16, box 64 x 128 x 1, 128-byte swizzle
@@ -172,37 +180,33 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t tile, int ks) {
   return sw128_desc(tile + ks * 2048, kBlk, 1024);
 }
 
-// Column sums of the valid rows of a [128 x 128] bf16 tile: warp `w` (0..3) of
-// the group adds columns [32w, 32w+32); lane l takes the column pair
-// 32w + 2(l&15) over rows of parity l>>4, and the two parities meet through
-// one shuffle.  Lanes l < 16 return the sums of columns (c, c+1).
-__device__ __forceinline__ int column_pair_sums(const uint8_t *tile, int w, int lane, int rows, float &s0,
-                                                float &s1) {
-  const int c = 32 * w + 2 * (lane & 15);
-  const int par = lane >> 4;
+// Column sums of the valid rows of a [128 x 128] bf16 tile over eight warps:
+// warp `w` adds columns [16w, 16w+16); lane l takes the pair 16w + 2(l&7) over
+// rows t = (l>>3) mod 4, and the four row phases meet through two shuffles.
+// Lanes l < 8 return the sums of columns (c, c+1).
+__device__ __forceinline__ int column_pair_sums_8w(const uint8_t *tile, int w, int lane, int rows, float &s0,
+                                                   float &s1) {
+  const int c = 16 * w + 2 * (lane & 7);
+  const int ph = lane >> 3;
   const uint8_t *blk = tile + (c >> 6) * kBlk;
   const int cc = c & 63;
-  // inside an 8-row swizzle atom the four rows of this parity sit at fixed offsets
-  uint32_t off[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) off[j] = sw128_offset(par + 2 * j, cc);
+  const uint32_t off0 = sw128_offset(ph, cc), off1 = sw128_offset(ph + 4, cc);
   float a0 = 0.f, a1 = 0.f;
   const int full = rows >> 3;
-#pragma unroll 2
+#pragma unroll 4
   for (int g = 0; g < full; ++g) {
-    const uint8_t *gb = blk + g * 1024;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t x = *reinterpret_cast<const uint32_t *>(gb + off[j]);
-      a0 += __uint_as_float(x << 16);
-      a1 += __uint_as_float(x & 0xffff0000u);
-    }
+    const uint32_t x = *reinterpret_cast<const uint32_t *>(blk + g * 1024 + off0);
+    const uint32_t y = *reinterpret_cast<const uint32_t *>(blk + g * 1024 + off1);
+    a0 += __uint_as_float(x << 16) + __uint_as_float(y << 16);
+    a1 += __uint_as_float(x & 0xffff0000u) + __uint_as_float(y & 0xffff0000u);
   }
-  for (int t = 8 * full + par; t < rows; t += 2) {
+  for (int t = 8 * full + ph; t < rows; t += 4) {
     const uint32_t x = *reinterpret_cast<const uint32_t *>(blk + sw128_offset(t, cc));
     a0 += __uint_as_float(x << 16);
     a1 += __uint_as_float(x & 0xffff0000u);
   }
+  a0 += __shfl_xor_sync(0xffffffffu, a0, 8);
+  a1 += __shfl_xor_sync(0xffffffffu, a1, 8);
   a0 += __shfl_xor_sync(0xffffffffu, a0, 16);
   a1 += __shfl_xor_sync(0xffffffffu, a1, 16);
   s0 = a0;
@@ -217,19 +221,25 @@ __device__ __forceinline__ uint32_t sw128_offset_f32(uint32_t row, uint32_t col)
 }
 
 template <bool kStateOnly>
-__global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParams p) {
   using Lay = Layout<kStateOnly>;
   constexpr int kStages = Lay::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicOr(&g_device_status, kAbortMisaligned);
+    return;
+  }
+  uint8_t *sm = smem_raw;
   float *den_x = reinterpret_cast<float *>(sm + Lay::DenX);
+  float *den_s = reinterpret_cast<float *>(sm + Lay::Den);
   float *zs = reinterpret_cast<float *>(sm + Lay::Z);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::Bars);
   // per stage: Q landed, K landed, V landed, phi applied, raw Q consumed, K free, V free
   uint64_t *full_q = bars, *full_k = bars + 3, *full_v = bars + 6, *phi_done = bars + 9, *q_empty = bars + 12,
            *k_empty = bars + 15, *v_empty = bars + 18;
-  uint64_t *mma1_done = bars + 21, *pp_ready = bars + 22, *o_full = bars + 23, *sb_ready = bars + 24,
-           *o_free = bars + 25, *drain = bars + 26, *qt_free = bars + 27;  // qt_free[2]: phi(Q) TMEM buffers
+  uint64_t *s_full = bars + 21, *pp_ready = bars + 22, *o_full = bars + 23, *sb_ready = bars + 24,
+           *o_free = bars + 25, *drain = bars + 26, *p_full = bars + 27, *den_ready = bars + 28,  // [2]
+           *qt_free = bars + 30;  // [2]: phi(Q) tensor-memory buffers
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::Misc);
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
   unsigned int *status = &g_device_status;
@@ -258,19 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
       mbar_init(&full_k[s], 1);
       mbar_init(&full_v[s], 1);
       mbar_init(&phi_done[s], kPhiThreads);
-      mbar_init(&q_empty[s], 128);
+      mbar_init(&q_empty[s], kPhiThreads);
       // main mode: the MMA commit plus the epilogue's 128 threads once they have read den_x[s]
       mbar_init(&k_empty[s], kStateOnly ? 1 : 129);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(&qt_free[0], 1);
-    mbar_init(&qt_free[1], 1);
-    mbar_init(mma1_done, 1);
+    mbar_init(s_full, 1);
     mbar_init(pp_ready, 128);
     mbar_init(o_full, 1);
     mbar_init(sb_ready, 128);
     mbar_init(o_free, 128);
     mbar_init(drain, 1);
+    mbar_init(&qt_free[0], 1);
+    mbar_init(&qt_free[1], 1);
+    mbar_init(p_full, 1);
+    mbar_init(&den_ready[0], 128);
+    mbar_init(&den_ready[1], 128);
     *abort_word = 0;
     fence_barrier_init();
   }
@@ -332,61 +345,64 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
         if (!mbar_wait(&phi_done[s], u & 1, abort_word, status)) break;
         if (!mbar_wait(&full_v[s], u & 1, abort_word, status)) break;
         const uint32_t k = sK + s * kTile, v = sV + s * kTile;
-        if (!kStateOnly) {
-          const uint32_t tQ = tmem + kColQ + 64 * (c & 1);
-          // the single P tile is free once the previous chunk's P V has completed
-          if (c > 0 && !mbar_wait(o_full, (c - 1) & 1, abort_word, status)) break;
+        if (kStateOnly) {
           tc_fence_after();
-          // P = Q K^T, phi(Q) from tensor memory (8 columns per 16 features)
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tP, tQ + 8 * ks, kdesc(k, ks), iKK, ks > 0);
-          if (!mbar_wait(sb_ready, c & 1, abort_word, status)) break;
-          if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status)) break;
-          tc_fence_after();
-          // O = Q bf16(S_prev)
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSb, ks), iKM, ks > 0);
-        } else {
-          tc_fence_after();
-        }
-        // S += K^T V
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_bf16(tS, mndesc(k, ks), mndesc(v, ks), iMM, kStateOnly ? (c > 0 || ks > 0) : 1);
-        mma_commit(&k_empty[s]);
-        if (!kStateOnly) {
-          mma_commit(&qt_free[c & 1]);
-          mma_commit(mma1_done);
-          if (!mbar_wait(pp_ready, c & 1, abort_word, status)) break;
-          tc_fence_after();
-          // O += P_hi V + P_lo V, P read from tensor memory: for keys [16ks, 16ks+16)
-          // columns 16ks..16ks+7 hold P_hi and 16ks+8..16ks+15 hold P_lo
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            mma_bf16_ts(tO, tP + 16 * ks, mndesc(v, ks), iKM, 1);
-            mma_bf16_ts(tO, tP + 16 * ks + 8, mndesc(v, ks), iKM, 1);
-          }
-          mma_commit(o_full);
-        } else {
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tS, mndesc(k, ks), mndesc(v, ks), iMM, c > 0 || ks > 0);
+          mma_commit(&k_empty[s]);
           mma_commit(&v_empty[s]);
+          continue;
         }
+        const uint32_t tQ = tmem + kColQ + 64 * (c & 1);
+        // the single P tile is free once the previous chunk's P V has completed
+        if (c > 0 && !mbar_wait(o_full, (c - 1) & 1, abort_word, status)) break;
+        tc_fence_after();
+        // P = Q K^T, phi(Q) from tensor memory (8 columns per 16 features)
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tP, tQ + 8 * ks, kdesc(k, ks), iKK, ks > 0);
+        mma_commit(p_full);
+        // S += K^T V once the previous state has been copied out
+        if (!mbar_wait(sb_ready, c & 1, abort_word, status)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tS, mndesc(k, ks), mndesc(v, ks), iMM, 1);
+        // O = Q bf16(S_prev) once the previous outputs have been read
+        if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSb, ks), iKM, ks > 0);
+        mma_commit(s_full);
+        mma_commit(&qt_free[c & 1]);
+        mma_commit(&k_empty[s]);
+        if (!mbar_wait(pp_ready, c & 1, abort_word, status)) break;
+        tc_fence_after();
+        // O += P_hi V + P_lo V, P read from tensor memory: for keys [16ks, 16ks+16)
+        // columns 16ks..16ks+7 hold P_hi and 16ks+8..16ks+15 hold P_lo
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16_ts(tO, tP + 16 * ks, mndesc(v, ks), iKM, 1);
+          mma_bf16_ts(tO, tP + 16 * ks + 8, mndesc(v, ks), iKM, 1);
+        }
+        mma_commit(o_full);
       }
-      if (kStateOnly) mma_commit(mma1_done);
+      if (kStateOnly) mma_commit(s_full);
       mma_commit(drain);
       wait_drain(drain, 0);
     }
   } else if (warp < kWarpEpi) {
-    // ---------------- feature-map warps: 2-5 on Q rows, 6-9 on K rows ----------------
+    // ---------------- feature-map warps (8) ----------------
+    // Warp w takes rows 32*(w%4) .. +31 (its tensor-memory lane quarter) and
+    // the 64-feature half (w-2)/4 of both the Q and the K tile.
     const int pt = threadIdx.x - kWarpPhi * 32;  // 0..255
-    const bool is_q = warp < kWarpPhi + 4;
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;         // tile row = TMEM lane of the phi(Q) buffer
-    const int kw = warp - (kWarpPhi + 4);         // K warp index 0..3 (column sums)
+    const int half = (warp - kWarpPhi) >> 2;
+    const int row = quarter * 32 + lane;
     if (pt < kD) {
       // partial states of the first pass start from zero; a segment starts from the caller's state plus them
       float z = (!kStateOnly && p.z0) ? p.z0[(long)bh * kD + pt] : 0.f;
       for (int qp = 0; qp < init_parts; ++qp) z += p.part_z[((long)bh * p.nparts + qp) * kD + pt];
       zs[pt] = z;
+      if (!kStateOnly) den_x[pt] = den_x[kC + pt] = 0.f;
     }
     named_bar(kBarPhi, kPhiThreads);
     for (int c = 0; c < nchunks; ++c) {
@@ -394,62 +410,54 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
       const uint32_t u = c / kStages;
       const int tv = (int)min((long)kC, t_end - (t_begin + (long)c * kC));
       uint8_t *Kt = sm + Lay::K + s * kTile;
-      float s0 = 0.f, s1 = 0.f;
-      int col = 0;
-      bool ok = true;
-      if (is_q) {
-        if (!kStateOnly) {
-          ok = mbar_wait(&full_q[s], u & 1, abort_word, status);
-          // phi(Q) row -> packed bf16 pairs -> tensor memory; den_x from the same rounded values.
-          // The phi(Q) buffer is free once the MMAs of the chunk two back have completed.
-          if (ok && c >= 2) ok = mbar_wait(&qt_free[c & 1], ((c >> 1) - 1) & 1, abort_word, status);
-          ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
-          if (ok) {
-            const uint8_t *Qt = sm + Lay::Q + s * kTile;
-            const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + 64 * (c & 1);
-            float dx = 0.f;
+      bool ok = mbar_wait(&full_k[s], u & 1, abort_word, status);
+      if (!kStateOnly) {
+        ok = ok && mbar_wait(&full_q[s], u & 1, abort_word, status);
+        // this chunk's phi(Q) buffer is free once Q K^T and Q S of the chunk two back have completed
+        if (ok && c >= 2) ok = mbar_wait(&qt_free[c & 1], ((c >> 1) - 1) & 1, abort_word, status);
+      }
+      if (bar_or(kBarPhi, kPhiThreads, !ok)) break;
+      if (!kStateOnly) {
+        // phi(Q) half row -> packed bf16 pairs -> tensor memory; the partial phi(q).z_prev
+        // from the same rounded values meets its other half in shared memory
+        const uint8_t *Qb = sm + Lay::Q + s * kTile + half * kBlk;
+        const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + 64 * (c & 1) + 32 * half;
+        float dx = 0.f;
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) {  // 32 features per step
-              uint4 xv[4];
+        for (int g = 0; g < 2; ++g) {
+          uint4 xv[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                xv[e] = *reinterpret_cast<const uint4 *>(Qt + (g >> 1) * kBlk + sw128_offset(row, (g & 1) * 32 + e * 8));
-              uint32_t w[16];
+          for (int e = 0; e < 4; ++e) xv[e] = *reinterpret_cast<const uint4 *>(Qb + sw128_offset(row, g * 32 + e * 8));
+          uint32_t w[16];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const uint4 y = phi8(xv[e]);
-                w[4 * e] = y.x, w[4 * e + 1] = y.y, w[4 * e + 2] = y.z, w[4 * e + 3] = y.w;
-                dx += dot8(y, zs + g * 32 + e * 8);
-              }
-              tmem_st16(tq + 16 * g, w);
-            }
-            den_x[s * kC + row] = dx;  // phi(q_row) . z_prev
+          for (int e = 0; e < 4; ++e) {
+            const uint4 y = phi8(xv[e]);
+            w[4 * e] = y.x, w[4 * e + 1] = y.y, w[4 * e + 2] = y.z, w[4 * e + 3] = y.w;
+            dx += dot8(y, zs + half * 64 + g * 32 + e * 8);
           }
-          mbar_arrive(&q_empty[s]);  // raw Q consumed
+          tmem_st16(tq + 16 * g, w);
         }
-      } else {
-        ok = mbar_wait(&full_k[s], u & 1, abort_word, status);
-        if (bar_or(kBarK, 128, !ok)) {
-          ok = false;
-        } else {
+        atomicAdd(&den_x[s * kC + row], dx);
+        mbar_arrive(&q_empty[s]);  // raw Q consumed
+      }
+      {
+        // phi(K) half row in place (all loads of a step first: the in-place stores would order them)
+        uint8_t *Kb = Kt + half * kBlk;
 #pragma unroll 1
-          for (int g = 0; g < 4; ++g) {  // all loads of a step first: the in-place stores would order them
-            uint4 kv[4];
+        for (int g = 0; g < 2; ++g) {
+          uint4 kv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              kv[e] = *reinterpret_cast<const uint4 *>(Kt + (g >> 1) * kBlk + sw128_offset(row, (g & 1) * 32 + e * 8));
+          for (int e = 0; e < 4; ++e) kv[e] = *reinterpret_cast<const uint4 *>(Kb + sw128_offset(row, g * 32 + e * 8));
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              *reinterpret_cast<uint4 *>(Kt + (g >> 1) * kBlk + sw128_offset(row, (g & 1) * 32 + e * 8)) =
-                  phi8(kv[e]);
-          }
-          named_bar(kBarK, 128);  // every K row transformed
-          // column sums of phi(K) over the valid rows (bf16 values, as the MMA sees them)
-          col = column_pair_sums(Kt, kw, lane, tv, s0, s1);
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4 *>(Kb + sw128_offset(row, g * 32 + e * 8)) = phi8(kv[e]);
         }
       }
-      if (bar_or(kBarPhi, kPhiThreads, !ok)) break;  // Q warps are done reading z
-      if (!is_q && lane < 16) {
+      named_bar(kBarPhi, kPhiThreads);  // every K row transformed; every read of zs done
+      // column sums of phi(K) over the valid rows (bf16 values, as the MMA sees them)
+      float s0, s1;
+      const int col = column_pair_sums_8w(Kt, warp - kWarpPhi, lane, tv, s0, s1);
+      if (lane < 8) {
         zs[col] += s0;
         zs[col + 1] += s1;
       }
@@ -462,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
       if (kStateOnly) p.part_z[((long)bh * p.nparts + blockIdx.x) * kD + pt] = zs[pt];
       else if (last_seg) p.z_out[(long)bh * kD + pt] = zs[pt];
     }
-  } else {
-    // ---------------- epilogue warpgroup ----------------
+  } else if (warp < kWarpOut) {
+    // ---------------- P split, denominator and state copy (warps 10-13) ----------------
     const int quarter = warp & 3;
     const int T = quarter * 32 + lane;  // TMEM lane: chunk row (token) or state row (feature)
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -509,27 +517,29 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
         const int tv = (int)min((long)kC, t_end - tok);
         const uint32_t tP = tl + kColP;
         bool w = mbar_wait(&phi_done[s], u & 1, abort_word, status) &&
-                 mbar_wait(mma1_done, c & 1, abort_word, status);
+                 mbar_wait(p_full, c & 1, abort_word, status);
         if (bar_or(kBarEpi, 128, !w)) {
           ok = false;
           break;
         }
         tc_fence_after();
         float den = den_x[s * kC + T];
+        den_x[s * kC + T] = 0.f;  // the feature-map warps accumulate the next use of this slot
         mbar_arrive(&k_empty[s]);
         // P -> causal mask -> bf16 hi/lo, written back over the same columns:
         // keys [16g, 16g+16) become 8 columns of P_hi pairs then 8 of P_lo pairs.
         // Key blocks right of this warp's rows are all masked (zeros).
         float rs = 0.f;
+#pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           if (cb > quarter) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = 0u;
           } else {
             tmem_ld32(tP + cb * 32, r);
-            uint32_t o[32];
 #pragma unroll
-            for (int g = 0; g < 2; ++g)
+            for (int g = 0; g < 2; ++g) {
+              uint32_t o[16];
 #pragma unroll
               for (int m = 0; m < 8; ++m) {
                 const int j = cb * 32 + g * 16 + 2 * m;
@@ -538,20 +548,29 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
                 const uint32_t hw = pack_bf16(p0, p1);
                 const float h0 = __uint_as_float(hw << 16), h1 = __uint_as_float(hw & 0xffff0000u);
                 const uint32_t lw = pack_bf16(p0 - h0, p1 - h1);
-                const float l0 = __uint_as_float(lw << 16), l1 = __uint_as_float(lw & 0xffff0000u);
-                rs += (h0 + l0) + (h1 + l1);
-                o[g * 16 + m] = hw;
-                o[g * 16 + 8 + m] = lw;
+                rs += p0 + p1;  // equals the sum of hi + lo to within 2^-16 relative
+                o[m] = hw;
+                o[8 + m] = lw;
               }
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = o[e];
+              for (int e = 0; e < 16; ++e) r[g * 16 + e] = o[e];
+            }
           }
           tmem_st32(tP + cb * 32, r);
         }
+        den = (den + rs) + p.eps;
+        den_s[(c & 1) * kC + T] = den;
         tc_fence_before();
         mbar_arrive(pp_ready);
-        den = (den + rs) + p.eps;
+        mbar_arrive(&den_ready[c & 1]);
         // bf16 copy of the updated state for the next chunk's cross read
+        w = mbar_wait(s_full, c & 1, abort_word, status);
+        if (bar_or(kBarEpi, 128, !w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           tmem_ld32(tl + kColS + cb * 32, r);
           store_row32_bf16(Sb, T, cb * 32, r);
@@ -559,68 +578,12 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(sb_ready);
-        // normalised outputs
-        w = mbar_wait(o_full, c & 1, abort_word, status);
-        if (bar_or(kBarEpi, 128, !w)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // normalised rows -> the V tile of this stage (free: P V has completed) as two
-        // [128 x 32] fp32 swizzled boxes per half of the columns -> TMA stores.  Rows past
-        // the sequence end are clipped by the store; the leading exact rows are rewritten later.
-        // The second half is read from tensor memory before the first half's store drains,
-        // so the accumulator is released as early as possible.
-        const float inv = 1.f / den;
-        uint8_t *stage_o = sm + Lay::V + s * kTile;
-        uint32_t r2[32];
-        for (int b = 0; b < 2; ++b) {
-          tmem_ld32(tl + kColO + b * 32, r);
-          uint8_t *box = stage_o + b * kBlk;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4 *>(box + sw128_offset_f32(T, 4 * q)) =
-                make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
-                            __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
-        }
-        fence_async_smem();
-        named_bar(kBarEpi, 128);
-        if (T == 0) {
-          tma_store_3d(&p.to, stage_o, 0, (int)tok, bh);
-          tma_store_3d(&p.to, stage_o + kBlk, 32, (int)tok, bh);
-          bulk_commit();
-        }
-        tmem_ld32(tl + kColO + 64, r);
-        tmem_ld32(tl + kColO + 96, r2);
-        tc_fence_before();
-        mbar_arrive(o_free);  // the O accumulator has been read
-        if (T == 0) bulk_wait_read();
-        named_bar(kBarEpi, 128);  // the staging tile is free again
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          *reinterpret_cast<float4 *>(stage_o + sw128_offset_f32(T, 4 * q)) =
-              make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
-                          __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
-          *reinterpret_cast<float4 *>(stage_o + kBlk + sw128_offset_f32(T, 4 * q)) =
-              make_float4(__uint_as_float(r2[4 * q]) * inv, __uint_as_float(r2[4 * q + 1]) * inv,
-                          __uint_as_float(r2[4 * q + 2]) * inv, __uint_as_float(r2[4 * q + 3]) * inv);
-        }
-        fence_async_smem();
-        named_bar(kBarEpi, 128);
-        if (T == 0) {
-          tma_store_3d(&p.to, stage_o, 64, (int)tok, bh);
-          tma_store_3d(&p.to, stage_o + kBlk, 96, (int)tok, bh);
-          bulk_commit();
-          bulk_wait_read();
-          mbar_arrive(&v_empty[s]);  // the V tile may be reloaded
-        }
       }
     } else {
-      const bool w = mbar_wait(mma1_done, 0, abort_word, status);
+      const bool w = mbar_wait(s_full, 0, abort_word, status);
       ok = !bar_or(kBarEpi, 128, !w);
       tc_fence_after();
     }
-    if (!kStateOnly && T == 0) bulk_wait_all();  // output stores complete before the CTA exits
     // final (or partial) state, fp32
     if (ok && !*abort_word && (kStateOnly || last_seg)) {
       float *dst = kStateOnly ? p.part_S + (((long)bh * p.nparts + blockIdx.x) * kD + T) * kD
@@ -634,6 +597,68 @@ __global__ void __launch_bounds__(kThreads, 1) causal_tc_kernel(const __grid_con
                               __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
       }
     }
+  } else if (!kStateOnly) {
+    // ---------------- normalised outputs (warps 14-17) ----------------
+    const int quarter = warp & 3;
+    const int T = quarter * 32 + lane;  // TMEM lane = chunk row
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint32_t r[32], r2[32];
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kStages;
+      const long tok = t_begin + (long)c * kC;
+      bool w = mbar_wait(o_full, c & 1, abort_word, status) &&
+               mbar_wait(&den_ready[c & 1], (c >> 1) & 1, abort_word, status);
+      if (bar_or(kBarOut, 128, !w)) break;
+      tc_fence_after();
+      const float inv = 1.f / den_s[(c & 1) * kC + T];
+      // normalised rows -> the V tile of this stage (free: P V has completed) as two
+      // [128 x 32] fp32 swizzled boxes per half of the columns -> TMA stores.  Rows past
+      // the sequence end are clipped by the store; the leading exact rows are rewritten later.
+      // The second half is read from tensor memory before the first half's store drains,
+      // so the accumulator is released as early as possible.
+      uint8_t *stage_o = sm + Lay::V + s * kTile;
+      for (int b = 0; b < 2; ++b) {
+        tmem_ld32(tl + kColO + b * 32, r);
+        uint8_t *box = stage_o + b * kBlk;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4 *>(box + sw128_offset_f32(T, 4 * q)) =
+              make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                          __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+      }
+      fence_async_smem();
+      named_bar(kBarOut, 128);
+      if (T == 0) {
+        tma_store_3d(&p.to, stage_o, 0, (int)tok, bh);
+        tma_store_3d(&p.to, stage_o + kBlk, 32, (int)tok, bh);
+        bulk_commit();
+      }
+      tmem_ld32(tl + kColO + 64, r);
+      tmem_ld32(tl + kColO + 96, r2);
+      tc_fence_before();
+      mbar_arrive(o_free);  // the O accumulator has been read
+      if (T == 0) bulk_wait_read();
+      named_bar(kBarOut, 128);  // the staging tile is free again
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        *reinterpret_cast<float4 *>(stage_o + sw128_offset_f32(T, 4 * q)) =
+            make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                        __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+        *reinterpret_cast<float4 *>(stage_o + kBlk + sw128_offset_f32(T, 4 * q)) =
+            make_float4(__uint_as_float(r2[4 * q]) * inv, __uint_as_float(r2[4 * q + 1]) * inv,
+                        __uint_as_float(r2[4 * q + 2]) * inv, __uint_as_float(r2[4 * q + 3]) * inv);
+      }
+      fence_async_smem();
+      named_bar(kBarOut, 128);
+      if (T == 0) {
+        tma_store_3d(&p.to, stage_o, 64, (int)tok, bh);
+        tma_store_3d(&p.to, stage_o + kBlk, 96, (int)tok, bh);
+        bulk_commit();
+        bulk_wait_read();
+        mbar_arrive(&v_empty[s]);  // the V tile may be reloaded
+      }
+    }
+    if (T == 0) bulk_wait_all();  // output stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -698,7 +723,21 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream) {
   if (attr_err[kStateOnly] != cudaSuccess) return attr_err[kStateOnly];
   causal_tc_kernel<kStateOnly><<<grid, kThreads, Layout<kStateOnly>::Alloc, stream>>>(tp);
   const cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) count_launch();
+  if (e == cudaSuccess) {
+    count_launch();
+  } else if (getenv("LA_DEBUG")) {
+    cudaFuncAttributes fa;
+    int blocks = -1;
+    cudaFuncGetAttributes(&fa, causal_tc_kernel<kStateOnly>);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, causal_tc_kernel<kStateOnly>, kThreads,
+                                                  Layout<kStateOnly>::Alloc);
+    fprintf(stderr,
+            "linattn: causal_tc_kernel<%d> launch failed (%s): regs %d, max threads %d, static smem %zu, "
+            "max dynamic smem %d, requested dynamic %u, threads %d, occupancy %d\n",
+            (int)kStateOnly, cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes,
+            fa.maxDynamicSharedSizeBytes, Layout<kStateOnly>::Alloc, kThreads, blocks);
+    cudaGetLastError();
+  }
   return e;
 }
 

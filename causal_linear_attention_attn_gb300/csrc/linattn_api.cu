@@ -107,7 +107,8 @@ la_status la_device_status(void *stream) {
   unsigned int v = 0;
   e = la::read_and_clear_device_status(&v);
   if (e != cudaSuccess) return la::from_cuda(e);
-  return v ? LA_ERR_TIMEOUT : LA_OK;
+  if (v & 1u) return LA_ERR_TIMEOUT;
+  return v ? LA_ERR_LAUNCH : LA_OK;  // other bits: a kernel refused to run (e.g. misaligned shared memory)
 }
 
 unsigned long long la_kernel_launches(void) { return la::g_launches.load(std::memory_order_relaxed); }

@@ -141,8 +141,10 @@ LA_API la_status la_decode_step(const void *q, const void *k, const void *v, flo
  * Synchronizes `stream`, then reads and clears the library's device status
  * word on the current device.  Returns LA_ERR_TIMEOUT if a bounded
  * device-side wait inside one of the library's kernels gave up since the
- * last check (that call's outputs are not valid), LA_OK otherwise, or the
- * error of the synchronization itself.
+ * last check, LA_ERR_LAUNCH if a kernel refused to run on this device
+ * configuration (its shared-memory base was not 1024-byte aligned); in both
+ * cases that call's outputs are not valid.  LA_OK otherwise, or the error
+ * of the synchronization itself.
  */
 LA_API la_status la_device_status(void *stream);
 
