@@ -92,6 +92,7 @@ constexpr uint32_t kAbortMisaligned = 2u;  // status bit: shared memory base not
 struct TcParams {
   CUtensorMap tq, tk, tv;  // 3-D maps over [BH][N][128] bf16, box 64 x 128 x 1, 128-byte swizzle
   CUtensorMap to;          // 3-D map over the fp32 output [BH][N][128], box 32 x 128 x 1, 128-byte swizzle
+  CUtensorMap to_tail;     // the same tensor, box 32 x 64 x 1: rows 64..127 of a head's first chunk
   float *out, *S_out, *z_out;
   const float *S0, *z0;      // initial state (nullable = zero)
   float *part_S, *part_z;    // state-only outputs / main-mode prefix inputs: [BH][nparts][128][128], [..][128]
@@ -628,11 +629,19 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       }
       fence_async_smem();
       named_bar(kBarOut, 128);
-      if (T == 0) {
-        tma_store_3d(&p.to, stage_o, 0, (int)tok, bh);
-        tma_store_3d(&p.to, stage_o + kBlk, 32, (int)tok, bh);
-        bulk_commit();
+      // A head's first chunk stores only rows 64..127: the exact pass writes rows 0..63
+      // concurrently.  (Row 64 of a swizzled box starts 8 KB in, 1024-byte aligned.)
+      const bool head_chunk = tok == 0 && p.n_exact > 0;
+      if (T == 0 && !(head_chunk && p.N <= 64)) {
+        if (head_chunk) {
+          tma_store_3d(&p.to_tail, stage_o + 8192, 0, 64, bh);
+          tma_store_3d(&p.to_tail, stage_o + kBlk + 8192, 32, 64, bh);
+        } else {
+          tma_store_3d(&p.to, stage_o, 0, (int)tok, bh);
+          tma_store_3d(&p.to, stage_o + kBlk, 32, (int)tok, bh);
+        }
       }
+      if (T == 0) bulk_commit();
       tmem_ld32(tl + kColO + 64, r);
       tmem_ld32(tl + kColO + 96, r2);
       tc_fence_before();
@@ -651,8 +660,15 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       fence_async_smem();
       named_bar(kBarOut, 128);
       if (T == 0) {
-        tma_store_3d(&p.to, stage_o, 64, (int)tok, bh);
-        tma_store_3d(&p.to, stage_o + kBlk, 96, (int)tok, bh);
+        if (head_chunk) {
+          if (p.N > 64) {
+            tma_store_3d(&p.to_tail, stage_o + 8192, 64, 64, bh);
+            tma_store_3d(&p.to_tail, stage_o + kBlk + 8192, 96, 64, bh);
+          }
+        } else {
+          tma_store_3d(&p.to, stage_o, 64, (int)tok, bh);
+          tma_store_3d(&p.to, stage_o + kBlk, 96, (int)tok, bh);
+        }
         bulk_commit();
         bulk_wait_read();
         mbar_arrive(&v_empty[s]);  // the V tile may be reloaded
@@ -698,13 +714,13 @@ bool make_map(CUtensorMap *m, const void *base, long BH, long N) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 output [BH][N][128]; boxes of 32 features x 128 tokens x 1 head (128-byte rows).
-bool make_out_map(CUtensorMap *m, void *base, long BH, long N) {
+// fp32 output [BH][N][128]; boxes of 32 features x `rows` tokens x 1 head (128-byte rows).
+bool make_out_map(CUtensorMap *m, void *base, long BH, long N, uint32_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)N * kD * 4};
-  cuuint32_t box[3] = {32, (cuuint32_t)kC, 1};
+  cuuint32_t box[3] = {32, rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
@@ -742,6 +758,33 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream) {
 }
 
 }  // namespace
+
+// A low-priority stream per device for work forked off the caller's stream,
+// with the two events of the fork and the join.  Created once per device.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ok = false;
+  std::mutex mu;  // held from the fork record to the join wait (the events are shared)
+};
+
+SideStream &side_stream(int dev) {
+  constexpr int kMaxDev = 64;
+  static SideStream slots[kMaxDev];
+  static std::once_flag once[kMaxDev];
+  if (dev < 0) cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDev) dev = 0;
+  std::call_once(once[dev], [dev] {
+    SideStream &s = slots[dev];
+    int lo = 0, hi = 0;
+    cudaDeviceGetStreamPriorityRange(&lo, &hi);  // lo = numerically largest = lowest priority
+    s.ok = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, lo) == cudaSuccess &&
+           cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) == cudaSuccess;
+    if (!s.ok) cudaGetLastError();
+  });
+  return slots[dev];
+}
 
 bool causal_tc_supported(const Problem &p) {
   const DeviceInfo &di = device_info(-1);
@@ -796,7 +839,8 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
   TcParams tp;
   memset(&tp, 0, sizeof tp);
   if (!make_map(&tp.tq, p.q, p.BH, p.N) || !make_map(&tp.tk, p.k, p.BH, p.N) ||
-      !make_map(&tp.tv, p.v, p.BH, p.N) || !make_out_map(&tp.to, p.out, p.BH, p.N)) {
+      !make_map(&tp.tv, p.v, p.BH, p.N) || !make_out_map(&tp.to, p.out, p.BH, p.N, kC) ||
+      !make_out_map(&tp.to_tail, p.out, p.BH, p.N, 64)) {
     if (scratch) cudaFreeAsync(scratch, p.stream);
     return cudaErrorInvalidValue;
   }
@@ -816,9 +860,22 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
   tp.n_exact = (int)std::min<long>(p.N, kExact);
   tp.eps = p.eps;
 
-  if (nparts > 0) e = launch_kernel<true>(tp, dim3((unsigned)nparts, (unsigned)p.BH), p.stream);
+  // The exact pass over each head's leading tokens runs on a low-priority side
+  // stream, concurrently with the tensor-core passes (which leave those rows to it).
+  SideStream &side = side_stream(-1);
+  std::lock_guard<std::mutex> lock(side.mu);
+  if (!side.ok) e = cudaErrorNotReady;
+  if (e == cudaSuccess) e = cudaEventRecord(side.fork, p.stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
+  if (nparts > 0 && e == cudaSuccess) e = launch_kernel<true>(tp, dim3((unsigned)nparts, (unsigned)p.BH), p.stream);
   if (e == cudaSuccess) e = launch_kernel<false>(tp, dim3((unsigned)G, (unsigned)p.BH), p.stream);
-  if (e == cudaSuccess) e = launch_causal_exact_head(p, tp.n_exact, S0, z0);
+  if (e == cudaSuccess) {
+    Problem ps = p;
+    ps.stream = side.stream;
+    e = launch_causal_exact_head(ps, tp.n_exact, S0, z0);
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(side.join, side.stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p.stream, side.join, 0);
   if (scratch) {
     const cudaError_t f = cudaFreeAsync(scratch, p.stream);
     if (e == cudaSuccess) e = f;
