@@ -883,6 +883,99 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
   return e;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the tensor-core causal pass (la_causal_noalloc).
+// The partial states of the first pass live in this fixed array instead of a
+// stream-ordered allocation; every device that loads the library keeps it
+// until the process exits.  All calls share it and nothing in it needs to
+// start at zero (every partial state is written before it is read), but calls
+// that overlap on the GPU would race on it.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;  // 16 MiB
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+namespace {
+struct NoAllocScratch {
+  float *ptr = nullptr;
+  cudaError_t err = cudaErrorNotReady;
+};
+
+// Device address of the fixed scratch array, looked up once per device (with
+// that device current) on the first call that needs it.
+NoAllocScratch &noalloc_scratch(int dev) {
+  constexpr int kMaxDev = 64;
+  static NoAllocScratch slots[kMaxDev];
+  static std::once_flag once[kMaxDev];
+  if (dev < 0 || dev >= kMaxDev) dev = 0;
+  std::call_once(once[dev], [dev] {
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    slots[dev].err = e;
+    if (e == cudaSuccess) slots[dev].ptr = static_cast<float *>(ptr);
+    else cudaGetLastError();
+  });
+  return slots[dev];
+}
+}  // namespace
+
+size_t noalloc_scratch_capacity_bytes() { return kNoAllocScratchFloats * sizeof(float); }
+
+cudaError_t launch_causal_tc_noalloc(const Problem &p, int dev, bool *too_large) {
+  *too_large = false;
+  const DeviceInfo &di = device_info(dev);
+  const long sms = std::max(1, di.sm_count);
+  const long chunks = (p.N + kC - 1) / kC;
+  // the same partition as la_causal: segments per head, first-pass parts per segment
+  long G = std::max(1L, std::min(sms / p.BH, chunks / 4));
+  const long seg_chunks = (chunks + G - 1) / G;
+  G = (chunks + seg_chunks - 1) / seg_chunks;
+  long r = 1;
+  if (G > 1)
+    for (long d = seg_chunks; d >= 1; --d)
+      if (seg_chunks % d == 0 && p.BH * (G - 1) * d <= sms) {
+        r = d;
+        break;
+      }
+  const long nparts = (G - 1) * r;
+  const size_t need = (size_t)p.BH * nparts * ((size_t)kD * kD + kD);
+  if (need > kNoAllocScratchFloats) {
+    *too_large = true;
+    return cudaSuccess;
+  }
+  float *part_S = nullptr, *part_z = nullptr;
+  if (need) {
+    NoAllocScratch &sc = noalloc_scratch(dev);
+    if (sc.err != cudaSuccess) return sc.err;
+    part_S = sc.ptr;
+    part_z = part_S + (size_t)p.BH * nparts * kD * kD;
+  }
+  TcParams tp;
+  memset(&tp, 0, sizeof tp);
+  if (!make_map(&tp.tq, p.q, p.BH, p.N) || !make_map(&tp.tk, p.k, p.BH, p.N) ||
+      !make_map(&tp.tv, p.v, p.BH, p.N) || !make_out_map(&tp.to, p.out, p.BH, p.N, kC) ||
+      !make_out_map(&tp.to_tail, p.out, p.BH, p.N, 64))
+    return cudaErrorInvalidValue;
+  tp.out = p.out;
+  tp.S_out = p.S;
+  tp.z_out = p.z;
+  tp.part_S = part_S;
+  tp.part_z = part_z;
+  tp.N = p.N;
+  tp.seg_len = (int)(seg_chunks * kC);
+  tp.nseg = (int)G;
+  tp.part_len = (int)(seg_chunks / r * kC);
+  tp.nparts = (int)nparts;
+  tp.parts_per_seg = (int)r;
+  tp.n_exact = (int)std::min<long>(p.N, kExact);
+  tp.eps = p.eps;
+  cudaError_t e = cudaSuccess;
+  if (nparts > 0) e = launch_kernel<true>(tp, dim3((unsigned)nparts, (unsigned)p.BH), p.stream);
+  if (e == cudaSuccess) e = launch_kernel<false>(tp, dim3((unsigned)G, (unsigned)p.BH), p.stream);
+  // the exact pass over the leading tokens, after the main pass on the same stream
+  if (e == cudaSuccess) e = launch_causal_exact_head(p, tp.n_exact, nullptr, nullptr);
+  return e;
+}
+
 cudaError_t read_and_clear_device_status(unsigned int *value) {
   unsigned int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(value, g_device_status, sizeof(unsigned int));

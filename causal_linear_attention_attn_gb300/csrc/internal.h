@@ -33,6 +33,12 @@ cudaError_t launch_causal_exact_head(const Problem &p, long n_exact, const float
 bool causal_tc_supported(const Problem &p);
 cudaError_t launch_causal_tc(const Problem &p, bool from_state);
 
+// Allocation-free tensor-core causal pass from the zero state: the first
+// pass's partial states use a fixed device array instead of an allocation.
+// Sets *too_large (and launches nothing) if they would not fit.
+cudaError_t launch_causal_tc_noalloc(const Problem &p, int dev, bool *too_large);
+size_t noalloc_scratch_capacity_bytes();
+
 // Read and clear the device status word (bounded-wait timeouts).
 cudaError_t read_and_clear_device_status(unsigned int *value);
 

@@ -123,6 +123,7 @@ const char *la_status_string(la_status s) {
     case LA_ERR_LAUNCH: return "kernel launch failed";
     case LA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
     case LA_ERR_NO_DEVICE: return "no usable CUDA device";
+    case LA_ERR_TOO_LARGE: return "problem needs more scratch than the fixed buffer of la_causal_noalloc";
   }
   return "unknown status";
 }
@@ -154,6 +155,26 @@ la_status la_causal(const void *q, const void *k, const void *v, float *out, flo
 la_status la_causal_with_state(const void *q, const void *k, const void *v, float *out, float *S, float *z,
                                int B, int H, int N, int d_k, int d_v, float eps, la_dtype dt, void *stream) {
   return causal_impl(q, k, v, out, S, z, B, H, N, d_k, d_v, eps, dt, stream, true);
+}
+
+la_status la_causal_noalloc(const void *q, const void *k, const void *v, float *out, float *S, float *z, int B,
+                            int H, int N, int d_k, int d_v, float eps, la_dtype dt, void *stream) {
+  la_status st = la::validate(q, k, v, out, S, z, B, H, N, d_k, d_v, eps, dt);
+  if (st != LA_OK) return st;
+  if ((long)B * H == 0) return LA_OK;
+  int dev;
+  if ((st = la::current_device(&dev)) != LA_OK) return st;
+  Problem p{q, k, v, out, S, z, B * H, (long)N, d_k, d_v, eps, dt, (cudaStream_t)stream};
+  if (N == 0) {
+    cudaError_t e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)p.BH * d_k * d_v, p.stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(z, 0, sizeof(float) * (size_t)p.BH * d_k, p.stream);
+    return la::from_cuda(e);
+  }
+  if (!la::causal_tc_supported(p)) return la::from_cuda(la::launch_causal_simt(p, p.N, false, true));
+  bool too_large = false;
+  const cudaError_t e = la::launch_causal_tc_noalloc(p, dev, &too_large);
+  if (too_large) return LA_ERR_TOO_LARGE;
+  return la::from_cuda(e);
 }
 
 la_status la_global(const void *q, const void *k, const void *v, float *out, float *S, float *z, int B, int H,

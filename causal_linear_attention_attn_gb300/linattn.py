@@ -22,11 +22,12 @@ lib = ctypes.CDLL(LIB_PATH)
 
 LA_F32, LA_BF16 = 0, 1
 STATUS_NAMES = {0: "LA_OK", 1: "LA_ERR_INVALID_VALUE", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_MISALIGNED",
-                4: "LA_ERR_OUT_OF_MEMORY", 5: "LA_ERR_LAUNCH", 6: "LA_ERR_TIMEOUT", 7: "LA_ERR_NO_DEVICE"}
+                4: "LA_ERR_OUT_OF_MEMORY", 5: "LA_ERR_LAUNCH", 6: "LA_ERR_TIMEOUT", 7: "LA_ERR_NO_DEVICE",
+                8: "LA_ERR_TOO_LARGE"}
 
 _vp, _fp, _i, _f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _SEQ_ARGS = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _i, _vp]
-for _name in ("la_global", "la_causal", "la_causal_with_state"):
+for _name in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc"):
     getattr(lib, _name).argtypes = _SEQ_ARGS
     getattr(lib, _name).restype = _i
 lib.la_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _f, _i, _vp]
@@ -126,6 +127,15 @@ def la_global(q, k, v, out=None, S=None, z=None, eps: float = 1e-6, stream=None)
 def la_causal(q, k, v, out=None, S=None, z=None, eps: float = 1e-6, stream=None):
     """Causal prefill from the zero state; returns (out, S, z) with the final state."""
     return _seq_call("la_causal", q, k, v, out, S, z, eps, stream)
+
+
+def la_causal_noalloc(q, k, v, out=None, S=None, z=None, eps: float = 1e-6, stream=None):
+    """la_causal without device allocation inside the library (fixed scratch; see linattn.h).
+
+    Pass preallocated out, S, z to keep the whole call allocation-free: the
+    binding only allocates the outputs that were not supplied.
+    """
+    return _seq_call("la_causal_noalloc", q, k, v, out, S, z, eps, stream)
 
 
 def la_causal_with_state(q, k, v, S, z, out=None, eps: float = 1e-6, stream=None):

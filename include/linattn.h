@@ -73,7 +73,8 @@ typedef enum {
   LA_ERR_OUT_OF_MEMORY = 4,
   LA_ERR_LAUNCH = 5,
   LA_ERR_TIMEOUT = 6,
-  LA_ERR_NO_DEVICE = 7
+  LA_ERR_NO_DEVICE = 7,
+  LA_ERR_TOO_LARGE = 8
 } la_status;
 
 /*
@@ -120,6 +121,33 @@ LA_API la_status la_causal(const void *q, const void *k, const void *v, float *o
 LA_API la_status la_causal_with_state(const void *q, const void *k, const void *v, float *out, float *S,
                                float *z, int B, int H, int N, int d_k, int d_v, float eps,
                                la_dtype dt, void *stream);
+
+/*
+ * la_causal without any device memory allocation.  The pages have no
+ * counterpart to this call; it exists for callers that must not allocate
+ * device memory once they are running: serving runtimes that reserve all of
+ * their memory up front and forbid allocation after warm-up (so that memory
+ * use and latency stay flat), and processes in which another framework's
+ * caching allocator already holds nearly all device memory, so that a
+ * stream-ordered allocation made by la_causal could fail mid-run.
+ *
+ * Same arguments, results and errors as la_causal.  The partial states that
+ * la_causal allocates per call (for long sequences split into segments) live
+ * here in one fixed 16 MiB device array inside the library instead; every
+ * GPU that loads the library keeps that array until the process exits.  If
+ * a problem would need more than 16 MiB of partial states (more than 254
+ * segment parts of 128x128 fp32 in total), the call returns
+ * LA_ERR_TOO_LARGE and launches nothing.  All calls share the array, so
+ * calls whose work overlaps on the GPU (different streams, or different host
+ * threads on the same device) race on it and give wrong results: order them.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Everything else is enqueued on `stream`; the
+ * leading-token pass runs on `stream` too (no second stream is used).
+ */
+LA_API la_status la_causal_noalloc(const void *q, const void *k, const void *v, float *out, float *S,
+                                   float *z, int B, int H, int N, int d_k, int d_v, float eps, la_dtype dt,
+                                   void *stream);
 
 /*
  * One recurrent decode step per (b,h) on a persistent state: update, then

@@ -25,7 +25,7 @@ def _declared_symbols():
 
 def test_header_declares_the_entry_points():
     names = _declared_symbols()
-    for n in ("la_global", "la_causal", "la_causal_with_state", "la_decode_step", "la_status_string",
+    for n in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc", "la_decode_step", "la_status_string",
               "la_version"):
         assert n in names
 
@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_status_strings():
     assert L.version() >> 16 == 1
-    for code in range(8):
+    for code in range(9):
         s = L.status_string(code)
         assert isinstance(s, str) and s
     assert L.status_string(99) == "unknown status"
@@ -53,7 +53,7 @@ def seq(fn="la_causal", q=P, k=P, v=P, out=P, S=P, z=P, B=1, H=1, N=8, dk=32, dv
     return getattr(L.lib, fn)(q, k, v, out, S, z, B, H, N, dk, dv, eps, dt, stream)
 
 
-@pytest.mark.parametrize("fn", ["la_causal", "la_global", "la_causal_with_state"])
+@pytest.mark.parametrize("fn", ["la_causal", "la_global", "la_causal_with_state", "la_causal_noalloc"])
 def test_sequence_validation(fn):
     assert seq(fn, q=None) == INVALID
     assert seq(fn, v=None) == INVALID
