@@ -119,70 +119,114 @@ def ncu_traffic(kernel_key: str):
 # --- clocks --------------------------------------------------------------------
 
 class ClockSampler:
+    """SM clock, power and throttle reasons sampled every few milliseconds while
+    the bench runs (read-only queries).  NVML through ctypes when the driver's
+    library loads, else `nvidia-smi --loop-ms` (100 ms period)."""
+
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clocks-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+    PERIOD_S = 0.005
 
     def __init__(self, index: int):
-        self.index, self.lines, self.proc = index, [], None
+        self.index, self.samples, self.proc, self.nvml, self.source = index, [], None, None, None
+        self.stop = threading.Event()
+
+    def _nvml_open(self):
+        import ctypes
+
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        dev = ctypes.c_void_p()
+        idx = self.index
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x for x in vis.split(",") if x.strip()]
+        if ids and all(x.strip().isdigit() for x in ids) and self.index < len(ids):
+            idx = int(ids[self.index])
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(dev)) != 0:
+            raise OSError("no NVML handle")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.nvml = (ctypes, lib, dev, reasons)
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+
+    def _nvml_loop(self):
+        ctypes, lib, dev, reasons = self.nvml
+        clk, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            lib.nvmlDeviceGetClockInfo(dev, 1, ctypes.byref(clk))  # NVML_CLOCK_SM
+            lib.nvmlDeviceGetPowerUsage(dev, ctypes.byref(mw))
+            reasons(dev, ctypes.byref(rs))
+            names = [n for bit, n in self.REASONS.items() if rs.value & bit]
+            self.samples.append((time.time(), float(clk.value), mw.value / 1e3, names))
+            time.sleep(self.PERIOD_S)
+
+    def _smi_loop(self):
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, mx, pw = float(f[0]), float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            self.max_mhz = mx
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            self.samples.append((time.time(), sm, pw, [n for n, v in zip(names, f[5:9]) if v.lower() == "active"]))
 
     def __enter__(self):
+        self.max_mhz = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-        except OSError:
-            self.proc = None
+            self._nvml_open()
+            self.source = f"nvml every {self.PERIOD_S * 1e3:.0f} ms"
+            self.t = threading.Thread(target=self._nvml_loop, daemon=True)
+        except (OSError, AttributeError):
+            self.nvml = None
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                return self
+            self.source = "nvidia-smi every 100 ms"
+            self.t = threading.Thread(target=self._smi_loop, daemon=True)
+        self.t.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
-
-    def mark(self):
-        return time.time()
-
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.source:
             self.t.join(timeout=2)
+        if self.nvml:
+            self.nvml[1].nvmlShutdown()
 
     def summary(self, t0: float, t1: float):
-        rows = []
-        for ts, line in self.lines:
-            if t0 <= ts <= t1:
-                f = [x.strip() for x in line.split(",")]
-                if len(f) >= 9:
-                    rows.append(f)
+        rows = [r for r in self.samples if t0 <= r[0] <= t1]
         if not rows:
             return None
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-
-        loaded = [r for r in rows if (num(r[3]) or 0) >= 50] or rows
-        sm = [num(r[0]) for r in loaded if num(r[0]) is not None]
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in loaded:
-            for n, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(loaded[0][1]),
-                "power_w_max": max((num(r[2]) or 0) for r in loaded), "samples": len(loaded),
-                "reasons": sorted(reasons)}
+        reasons = sorted({n for r in rows for n in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": self.max_mhz,
+                "power_w_max": round(max(r[2] for r in rows), 1), "samples": len(rows), "reasons": reasons,
+                "source": self.source}
 
 
 # --- timing helpers ---------------------------------------------------------------
+
+LAST_WINDOW = [0.0, 0.0]  # host wall-clock bounds of the last timed region
+
 
 def time_device(fn, steps: int, warmup: int, world: int, stream):
     for _ in range(warmup):
@@ -191,11 +235,13 @@ def time_device(fn, steps: int, warmup: int, world: int, stream):
     barrier(world)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    LAST_WINDOW[0] = time.time()
     a.record(stream)
     for _ in range(steps):
         fn()
     b.record(stream)
     torch.cuda.synchronize()
+    LAST_WINDOW[1] = time.time()
     barrier(world)
     return a.elapsed_time(b) / steps  # ms per step (this rank)
 
@@ -305,27 +351,29 @@ def main_ours(args):
     stream = torch.cuda.current_stream()
     w = rank_workload(inputs.WORKLOADS[args.workload], rank)
     with ClockSampler(local) as clk:
-        t0 = clk.mark()
         head, bufs = run_seq_form(L, w, args.steps, args.warmup, world, stream, hbm, src)
-        t1 = clk.mark()
+        t0, t1 = LAST_WINDOW
         forms = {}
+        extras = [] if args.no_extras else [f for f in args.forms.split(",") if f]
         if not args.no_extras:
             for name in ("global_bf16", "causal_bf16_long"):
-                if name == args.workload:
+                if name == args.workload or name not in extras:
                     continue
                 wx = rank_workload(inputs.WORKLOADS[name], rank)
                 steps = max(3, args.steps // (10 if name == "causal_bf16_long" else 1))
                 forms[name], _ = run_seq_form(L, wx, steps, args.warmup, world, stream, hbm, src)
+                forms[name]["clocks"] = clk.summary(*LAST_WINDOW)
                 torch.cuda.empty_cache()
+        if "decode_bf16" in extras:
             wd = rank_workload(inputs.WORKLOADS["decode_bf16"], rank)
             forms["decode_bf16"] = run_decode(L, wd, args.decode_steps, args.warmup, world, stream, hbm, src)
+            forms["decode_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
-        t2 = clk.mark()
     e2e = run_e2e(L, w, bufs, max(3, args.steps // 10), args.warmup, stream)
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     if rank != 0:
         return
-    clocks = clk.summary(t0, t1) or clk.summary(t0, t2)
+    clocks = clk.summary(t0, t1)
     ms = head["ms_per_call"]
     line = {
         "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -373,6 +421,8 @@ def parse(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-extras", action="store_true", help="time the headline workload only")
+    ap.add_argument("--forms", default="global_bf16,causal_bf16_long,decode_bf16",
+                    help="comma-separated other forms timed after the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-step-s", type=float, default=10.0, help="max CPU seconds per reference step")
     a = ap.parse_args(argv)

@@ -17,91 +17,104 @@ namespace la {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxRows = 16;  // rows per thread: dk * dv / (4 * kThreads) <= 16
 
-template <typename Tin>
+// Head sizes are template parameters: with runtime sizes the per-thread row
+// loop cannot be resolved at compile time, the kernel needs ~140 registers,
+// and only one CTA fits per SM, which leaves HBM a third idle.
+template <typename Tin, int DK, int DV>
 __global__ void __launch_bounds__(kThreads)
     decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
-                  float *__restrict__ out, float *__restrict__ S_g, float *__restrict__ z_g, int dk,
-                  int dv, float eps) {
-  __shared__ float fk[128], fq[128], vv[128];
-  __shared__ float part[kThreads * 4];
+                  float *__restrict__ out, float *__restrict__ S_g, float *__restrict__ z_g, float eps) {
+  constexpr int kQuads = DV / 4;               // float4 column quads per row
+  constexpr int kGroups = kThreads / kQuads;   // row groups
+  constexpr int kRows = DK / kGroups;          // rows per thread
+  static_assert(kRows >= 1 && kRows * kGroups == DK, "rows must split evenly over the row groups");
+  __shared__ float fk[DK], fq[DK], vv[DV];
+  __shared__ float4 part[kThreads];
   __shared__ float wden[kThreads / 32];
   const long bh = blockIdx.x;
   const int tid = threadIdx.x;
-  const int nq = dv >> 2;           // float4 column quads per row
-  const int groups = kThreads / nq; // row groups
-  const int cq = tid % nq, g = tid / nq;
-  const int nr = dk / groups;       // rows per thread
+  const int cq = tid % kQuads, g = tid / kQuads;
 
-  float4 *S4 = reinterpret_cast<float4 *>(S_g + bh * (long)dk * dv);
-  float4 s[kMaxRows];
+  float4 *S4 = reinterpret_cast<float4 *>(S_g + bh * (long)DK * DV);
+  float4 s[kRows];
 #pragma unroll
-  for (int r = 0; r < kMaxRows; ++r)
-    if (r < nr) s[r] = __ldcs(S4 + (long)(g + r * groups) * nq + cq);
+  for (int r = 0; r < kRows; ++r) s[r] = __ldcs(S4 + (g + r * kGroups) * kQuads + cq);
 
-  if (tid < dk) {
-    fk[tid] = phi(ldf(k + bh * dk + tid));
-    fq[tid] = phi(ldf(q + bh * dk + tid));
-  }
-  if (tid < dv) vv[tid] = ldf(v + bh * dv + tid);
-  __syncthreads();
-
-  const float4 vq = make_float4(vv[4 * cq], vv[4 * cq + 1], vv[4 * cq + 2], vv[4 * cq + 3]);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) {
-    if (r < nr) {
-      const int i = g + r * groups;
-      const float a = fk[i], b = fq[i];
-      float4 x = s[r];
-      x.x = fmaf(a, vq.x, x.x);
-      x.y = fmaf(a, vq.y, x.y);
-      x.z = fmaf(a, vq.z, x.z);
-      x.w = fmaf(a, vq.w, x.w);
-      __stcs(S4 + (long)i * nq + cq, x);
-      acc.x = fmaf(b, x.x, acc.x);
-      acc.y = fmaf(b, x.y, acc.y);
-      acc.z = fmaf(b, x.z, acc.z);
-      acc.w = fmaf(b, x.w, acc.w);
-    }
-  }
-  reinterpret_cast<float4 *>(part)[g * nq + cq] = acc;
-
-  // normalizer: z += phi(k), den = phi(q) . z_new
+  // normalizer first (its loads overlap the state's): z += phi(k), den = phi(q) . z_new
   float d = 0.f;
-  if (tid < dk) {
-    const float zn = z_g[bh * dk + tid] + fk[tid];
-    z_g[bh * dk + tid] = zn;
-    d = fq[tid] * zn;
+  if (tid < DK) {
+    const float a = phi(ldf(k + bh * DK + tid)), b = phi(ldf(q + bh * DK + tid));
+    const float zn = z_g[bh * DK + tid] + a;
+    fk[tid] = a;
+    fq[tid] = b;
+    z_g[bh * DK + tid] = zn;
+    d = b * zn;
   }
+  if (tid < DV) vv[tid] = ldf(v + bh * DV + tid);
   d = warp_sum(d);
   if ((tid & 31) == 0) wden[tid >> 5] = d;
   __syncthreads();
-  if (tid < dv) {
+
+  const float4 vq = reinterpret_cast<const float4 *>(vv)[cq];
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int i = g + r * kGroups;
+    const float a = fk[i], b = fq[i];
+    float4 x = s[r];
+    x.x = fmaf(a, vq.x, x.x);
+    x.y = fmaf(a, vq.y, x.y);
+    x.z = fmaf(a, vq.z, x.z);
+    x.w = fmaf(a, vq.w, x.w);
+    __stcs(S4 + i * kQuads + cq, x);
+    acc.x = fmaf(b, x.x, acc.x);
+    acc.y = fmaf(b, x.y, acc.y);
+    acc.z = fmaf(b, x.z, acc.z);
+    acc.w = fmaf(b, x.w, acc.w);
+  }
+  part[g * kQuads + cq] = acc;
+  __syncthreads();
+  if (tid < DV) {
     float den = 0.f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) den += wden[w];
+    const float *pf = reinterpret_cast<const float *>(part);
     float num = 0.f;
-    for (int gg = 0; gg < groups; ++gg) num += part[gg * dv + tid];
-    out[bh * dv + tid] = num / (den + eps);
+#pragma unroll
+    for (int gg = 0; gg < kGroups; ++gg) num += pf[gg * DV + tid];
+    out[bh * DV + tid] = num / (den + eps);
   }
 }
 
-template <typename Tin>
+template <typename Tin, int DK, int DV>
 cudaError_t launch_t(const Problem &p) {
-  decode_kernel<Tin><<<p.BH, kThreads, 0, p.stream>>>((const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, p.out,
-                                                    p.S, p.z, p.dk, p.dv, p.eps);
+  decode_kernel<Tin, DK, DV><<<p.BH, kThreads, 0, p.stream>>>((const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v,
+                                                            p.out, p.S, p.z, p.eps);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
 }
 
+template <typename Tin, int DK>
+cudaError_t launch_dv(const Problem &p) {
+  if (p.dv == 32) return launch_t<Tin, DK, 32>(p);
+  if (p.dv == 64) return launch_t<Tin, DK, 64>(p);
+  return launch_t<Tin, DK, 128>(p);
+}
+
+template <typename Tin>
+cudaError_t launch_dk(const Problem &p) {
+  if (p.dk == 32) return launch_dv<Tin, 32>(p);
+  if (p.dk == 64) return launch_dv<Tin, 64>(p);
+  return launch_dv<Tin, 128>(p);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const Problem &p) {
-  if (p.dt == LA_F32) return launch_t<float>(p);
-  return launch_t<__nv_bfloat16>(p);
+  if (p.dt == LA_F32) return launch_dk<float>(p);
+  return launch_dk<__nv_bfloat16>(p);
 }
 
 }  // namespace la

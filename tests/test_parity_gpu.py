@@ -120,7 +120,7 @@ def test_workload_decode_full_size(cuda_lib):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 128)])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (32, 128), (64, 64), (64, 128), (128, 32), (128, 128)])
 def test_decode_every_element_from_random_state(cuda_lib, dtype, dk, dv):
     base = W["causal_f32_small"] if dtype == "f32" else W["decode_bf16"]
     w = dataclasses.replace(base, dk=dk, dv=dv)
