@@ -228,29 +228,78 @@ class ClockSampler:
 LAST_WINDOW = [0.0, 0.0]  # host wall-clock bounds of the last timed region
 
 
-def time_device(fn, steps: int, warmup: int, world: int, stream):
+def time_device(fn, steps: int, warmup: int, world: int, stream, L=None):
+    """ms per step over `steps` timed steps.  With the library binding `L`,
+    its per-kernel event timing runs over the same timed steps."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if L is not None:
+        L.profile_enable(True)
     LAST_WINDOW[0] = time.time()
     a.record(stream)
     for _ in range(steps):
         fn()
     b.record(stream)
+    if L is not None:
+        L.profile_enable(False)
     torch.cuda.synchronize()
     LAST_WINDOW[1] = time.time()
     barrier(world)
     return a.elapsed_time(b) / steps  # ms per step (this rank)
 
 
-def roofline(alg_bytes: float, ms: float, hbm: float, src: str, traffic):
+def kernel_table(L, steps):
+    """Per-kernel launches and mean device time over the last timed region."""
+    rows = {}
+    for name in L.KERNELS:
+        ms, n = L.profile_read(name)
+        if n:
+            rows[name] = {"launches": n, "ms_per_launch": ms / n}
+    tot = sum(r["ms_per_launch"] * r["launches"] for r in rows.values())
+    for r in rows.values():
+        r["share"] = round(r["ms_per_launch"] * r["launches"] / tot, 4) if tot else None
+    return rows
+
+
+def kernel_bytes(w, kernel: str) -> float:
+    """Algorithmic HBM bytes of one launch of `kernel` on workload `w`: the
+    operands it must read and the results it must write, each once."""
+    ib = in_bytes(w)
+    state = 4 * (w.dk * w.dv + w.dk)
+    if kernel == "causal_main":  # all q, k, v; outputs except each head's exact leading rows; final state
+        ne = min(w.N, 64)
+        return w.BH * (w.N * (2 * w.dk + w.dv) * ib + (w.N - ne) * 4 * w.dv + state)
+    if kernel == "global_state":
+        return w.BH * (w.N * (w.dk + w.dv) * ib + state)
+    if kernel == "global_read":
+        return w.BH * (w.N * w.dk * ib + state + w.N * 4 * w.dv)
+    if kernel == "decode":
+        return decode_bytes(w)
+    return seq_bytes(w)
+
+
+def roofline(alg_bytes: float, ms: float, hbm: float, src: str, traffic, kernel=None):
     achieved = alg_bytes / (ms * 1e-3) / 1e9
-    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
-            "alg_bytes_per_launch": alg_bytes}
+    r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+         "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
+         "alg_bytes_per_launch": alg_bytes}
+    if kernel:
+        r = {"kernel": kernel, "ms_per_launch": round(ms, 5), **r}
+    return r
+
+
+def dominant_roofline(L, w, steps, hbm, src, key):
+    """Roofline of the kernel with the largest device time in the timed region,
+    timed live with its own event pairs, plus the per-kernel table."""
+    table = kernel_table(L, steps)
+    name = max(table, key=lambda n: table[n]["ms_per_launch"] * table[n]["launches"])
+    t = table[name]
+    return roofline(kernel_bytes(w, name), t["ms_per_launch"], hbm, src, ncu_traffic(f"{key}:{name}"),
+                    kernel=name), table
 
 
 # --- our arm -----------------------------------------------------------------------
@@ -264,13 +313,14 @@ def run_seq_form(L, w, steps, warmup, world, stream, hbm, src, gen_device="cuda"
     fn = L.la_causal if w.form == "causal" else L.la_global
     call = lambda: fn(q, k, v, out=out, S=S, z=z, eps=w.eps, stream=stream)
     n0 = L.kernel_launches()
-    ms = time_device(call, steps, warmup, world, stream)
+    ms = time_device(call, steps, warmup, world, stream, L)
     launches = (L.kernel_launches() - n0) // (steps + warmup) * steps
     ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
     tok = w.BH * w.N
+    rl, table = dominant_roofline(L, w, steps, hbm, src, w.name)
     res = {"workload": w.name, "tokens_per_s": world * tok / (ms * 1e-3), "ms_per_call": ms,
-           "roofline": roofline(seq_bytes(w), ms, hbm, src, ncu_traffic(f"{w.form}:{w.name}")),
-           "gpu_launches": launches}
+           "roofline": rl, "step_roofline": roofline(seq_bytes(w), ms, hbm, src, None),
+           "kernels": table, "gpu_launches": launches}
     return res, (q, k, v, out, S, z, fn)
 
 
@@ -306,13 +356,14 @@ def run_decode(L, w, steps, warmup, world, stream, hbm, src):
     it = iter(staged)
     call = lambda: L.la_decode_step(*next(it), S, z, out=out, eps=w.eps, stream=stream)
     n0 = L.kernel_launches()
-    ms = time_device(call, steps, warmup, world, stream)
+    ms = time_device(call, steps, warmup, world, stream, L)
     launches = (L.kernel_launches() - n0) // nstage * steps
     ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
-    rl = roofline(decode_bytes(w), ms, hbm, src, ncu_traffic(f"decode:{w.name}"))
-    return {"workload": w.name, "us_per_step": ms * 1e3, "gbs": rl["achieved"], "frac_hbm": rl["frac"],
+    rl, table = dominant_roofline(L, w, steps, hbm, src, w.name)
+    step = roofline(decode_bytes(w), ms, hbm, src, None)
+    return {"workload": w.name, "us_per_step": ms * 1e3, "gbs": step["achieved"], "frac_hbm": step["frac"],
             "seq_tokens_per_s": world * w.B / (ms * 1e-3), "steps_timed": steps, "roofline": rl,
-            "gpu_launches": launches}
+            "step_roofline": step, "kernels": table, "gpu_launches": launches}
 
 
 def cpu_baseline(w, target_s: float = 12.0):
@@ -383,7 +434,8 @@ def main_ours(args):
                    "inputs": "q,k ~ N(0,1)/sqrt(128), v ~ N(0,1), bf16; out/S/z fp32",
                    "l2": "inputs (402.7 MB) larger than L2 (129 MB); no flush needed",
                    "parallelism": f"replicas x{world} (heads independent)"},
-        "roofline": head["roofline"], "gpu_launches": head["gpu_launches"], "e2e": e2e, "clocks": clocks,
+        "roofline": head["roofline"], "step_roofline": head["step_roofline"], "kernels": head["kernels"],
+        "gpu_launches": head["gpu_launches"], "e2e": e2e, "clocks": clocks,
         "cpu_baseline": cpu, "forms": forms,
     }
     print(json.dumps(line))

@@ -121,10 +121,12 @@ cudaError_t launch_t(const Problem &p, long n_proc, bool from_state, bool write_
   cudaError_t e = cudaFuncSetAttribute(causal_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
+  LaunchTimer timer(kKCausalSimt, p.stream);
   causal_simt_kernel<Tin><<<p.BH, kThreads, smem, p.stream>>>(
       (const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, p.out, p.S, p.z, p.N, n_proc, p.dk, p.dv, p.eps,
       from_state ? 1 : 0, write_state ? 1 : 0);
   e = cudaGetLastError();
+  timer.done(e);
   if (e == cudaSuccess) count_launch();
   return e;
 }
@@ -216,9 +218,11 @@ cudaError_t launch_head_t(const Problem &p, int ne, const float *S0, const float
                                        (int)smem);
   if (e != cudaSuccess) return e;
   const unsigned row_blocks = (unsigned)((ne + kHeadRows - 1) / kHeadRows);
+  LaunchTimer timer(kKExactHead, p.stream);
   causal_exact_head_kernel<Tin><<<dim3(p.BH, row_blocks), kHeadRows * 32, smem, p.stream>>>(
       (const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, p.out, S0, z0, p.N, ne, p.dk, p.dv, p.eps);
   e = cudaGetLastError();
+  timer.done(e);
   if (e == cudaSuccess) count_launch();
   return e;
 }

@@ -737,8 +737,10 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream) {
                                                 (int)Layout<kStateOnly>::Alloc);
   });
   if (attr_err[kStateOnly] != cudaSuccess) return attr_err[kStateOnly];
+  LaunchTimer timer(kStateOnly ? kKCausalState : kKCausalMain, stream);
   causal_tc_kernel<kStateOnly><<<grid, kThreads, Layout<kStateOnly>::Alloc, stream>>>(tp);
   const cudaError_t e = cudaGetLastError();
+  timer.done(e);
   if (e == cudaSuccess) {
     count_launch();
   } else if (getenv("LA_DEBUG")) {

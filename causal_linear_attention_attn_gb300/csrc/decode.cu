@@ -89,9 +89,11 @@ __global__ void __launch_bounds__(kThreads)
 
 template <typename Tin, int DK, int DV>
 cudaError_t launch_t(const Problem &p) {
+  LaunchTimer timer(kKDecode, p.stream);
   decode_kernel<Tin, DK, DV><<<p.BH, kThreads, 0, p.stream>>>((const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v,
                                                             p.out, p.S, p.z, p.eps);
   const cudaError_t e = cudaGetLastError();
+  timer.done(e);
   if (e == cudaSuccess) count_launch();
   return e;
 }

@@ -119,9 +119,11 @@ cudaError_t launch_t(const Problem &p) {
   const size_t smem1 = sizeof(float) * ((size_t)kT * (p.dk + 1) + (size_t)kT * p.dv);
   e = cudaFuncSetAttribute(global_state_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
   if (e != cudaSuccess) return e;
+  LaunchTimer t1(kKGlobalState, p.stream);
   global_state_kernel<Tin><<<dim3(p.BH, (unsigned)splits), kThreads, smem1, p.stream>>>(
       (const Tin *)p.k, (const Tin *)p.v, p.S, p.z, p.N, p.dk, p.dv, (int)splits);
   e = cudaGetLastError();
+  t1.done(e);
   if (e != cudaSuccess) return e;
   count_launch();
   const size_t smem2 = sizeof(float) * ((size_t)p.dk * p.dv + p.dk + (size_t)kReadTokens * (p.dk + 1) +
@@ -129,9 +131,11 @@ cudaError_t launch_t(const Problem &p) {
   e = cudaFuncSetAttribute(global_read_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
   if (e != cudaSuccess) return e;
   const unsigned tiles = (unsigned)((p.N + kReadTokens - 1) / kReadTokens);
+  LaunchTimer t2(kKGlobalRead, p.stream);
   global_read_kernel<Tin><<<dim3(p.BH, tiles), kThreads, smem2, p.stream>>>((const Tin *)p.q, p.S, p.z, p.out,
                                                                           p.N, p.dk, p.dv, p.eps);
   e = cudaGetLastError();
+  t2.done(e);
   if (e == cudaSuccess) count_launch();
   return e;
 }

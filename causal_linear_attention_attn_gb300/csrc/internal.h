@@ -51,6 +51,32 @@ cudaError_t launch_decode(const Problem &p);
 // Count one successful kernel launch (reported by la_kernel_launches).
 void count_launch(unsigned n = 1);
 
+// Kernel ids of the device-time diagnostics (same values as la_kernel).
+enum KernelId : int {
+  kKCausalMain = 0,
+  kKCausalState = 1,
+  kKExactHead = 2,
+  kKCausalSimt = 3,
+  kKGlobalState = 4,
+  kKGlobalRead = 5,
+  kKDecode = 6,
+  kKNumKernels = 7
+};
+
+// While profiling is on (la_profile_enable), brackets one launch with a CUDA
+// event pair on its stream; construct it just before the launch and call
+// done() with the launch's error just after.  Costs nothing when off.
+class LaunchTimer {
+ public:
+  LaunchTimer(int kernel, cudaStream_t stream);
+  void done(cudaError_t launch_error);
+
+ private:
+  int kernel_;
+  cudaStream_t stream_;
+  cudaEvent_t start_ = nullptr;
+};
+
 // Per-device attributes, filled once per device.
 struct DeviceInfo {
   int sm_count = 0;

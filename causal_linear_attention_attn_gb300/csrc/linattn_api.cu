@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdio>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "linattn.h"
@@ -70,6 +71,63 @@ la_status current_device(int *dev) {
 }  // namespace
 
 void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// --- device-time diagnostics --------------------------------------------------------
+namespace {
+struct PendingTiming {
+  int kernel;
+  cudaEvent_t start, end;
+};
+std::atomic<bool> g_profiling{false};
+std::mutex g_prof_mu;
+std::vector<PendingTiming> g_pending;
+double g_prof_ms[kKNumKernels];
+long long g_prof_n[kKNumKernels];
+
+// Fold finished event pairs into the totals (caller holds g_prof_mu).
+cudaError_t resolve_pending() {
+  cudaError_t first = cudaSuccess;
+  for (const PendingTiming &t : g_pending) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(t.end);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.start, t.end);
+    if (e == cudaSuccess) {
+      g_prof_ms[t.kernel] += ms;
+      g_prof_n[t.kernel] += 1;
+    } else if (first == cudaSuccess) {
+      first = e;
+    }
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.end);
+  }
+  g_pending.clear();
+  return first;
+}
+}  // namespace
+
+LaunchTimer::LaunchTimer(int kernel, cudaStream_t stream) : kernel_(kernel), stream_(stream) {
+  if (!g_profiling.load(std::memory_order_relaxed)) return;
+  if (cudaEventCreate(&start_) != cudaSuccess || cudaEventRecord(start_, stream_) != cudaSuccess) {
+    if (start_) cudaEventDestroy(start_);
+    start_ = nullptr;
+    cudaGetLastError();
+  }
+}
+
+void LaunchTimer::done(cudaError_t launch_error) {
+  if (!start_) return;
+  cudaEvent_t end = nullptr;
+  if (launch_error != cudaSuccess || cudaEventCreate(&end) != cudaSuccess ||
+      cudaEventRecord(end, stream_) != cudaSuccess) {
+    cudaEventDestroy(start_);
+    if (end) cudaEventDestroy(end);
+    start_ = nullptr;
+    return;
+  }
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_pending.push_back({kernel_, start_, end});
+  start_ = nullptr;
+}
 
 const DeviceInfo &device_info(int dev) {
   if (dev < 0) cudaGetDevice(&dev);
@@ -155,6 +213,25 @@ la_status la_causal(const void *q, const void *k, const void *v, float *out, flo
 la_status la_causal_with_state(const void *q, const void *k, const void *v, float *out, float *S, float *z,
                                int B, int H, int N, int d_k, int d_v, float eps, la_dtype dt, void *stream) {
   return causal_impl(q, k, v, out, S, z, B, H, N, d_k, d_v, eps, dt, stream, true);
+}
+
+la_status la_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(la::g_prof_mu);
+  if (on) {
+    la::resolve_pending();
+    for (int i = 0; i < la::kKNumKernels; ++i) la::g_prof_ms[i] = 0.0, la::g_prof_n[i] = 0;
+  }
+  la::g_profiling.store(on != 0);
+  return LA_OK;
+}
+
+la_status la_profile_read(la_kernel kernel, double *ms_total, long long *launches) {
+  if ((int)kernel < 0 || (int)kernel >= la::kKNumKernels || !ms_total || !launches) return LA_ERR_INVALID_VALUE;
+  std::lock_guard<std::mutex> lk(la::g_prof_mu);
+  const cudaError_t e = la::resolve_pending();
+  *ms_total = la::g_prof_ms[kernel];
+  *launches = la::g_prof_n[kernel];
+  return la::from_cuda(e);
 }
 
 la_status la_causal_noalloc(const void *q, const void *k, const void *v, float *out, float *S, float *z, int B,

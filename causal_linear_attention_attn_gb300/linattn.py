@@ -42,6 +42,14 @@ lib.la_last_error_detail.argtypes = []
 lib.la_last_error_detail.restype = ctypes.c_char_p
 lib.la_kernel_launches.argtypes = []
 lib.la_kernel_launches.restype = ctypes.c_ulonglong
+lib.la_profile_enable.argtypes = [_i]
+lib.la_profile_enable.restype = _i
+lib.la_profile_read.argtypes = [_i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
+lib.la_profile_read.restype = _i
+
+# la_kernel ids of the device-time diagnostics
+KERNELS = {"causal_main": 0, "causal_state": 1, "exact_head": 2, "causal_simt": 3, "global_state": 4,
+           "global_read": 5, "decode": 6}
 
 
 class LinAttnError(RuntimeError):
@@ -161,6 +169,20 @@ def la_decode_step(q, k, v, S, z, out=None, eps: float = 1e-6, stream=None):
 def device_status(stream=None) -> int:
     """Synchronize the stream and return (and clear) the device status: 0 = OK, 6 = a bounded wait timed out."""
     return int(lib.la_device_status(_stream(stream)))
+
+
+def profile_enable(on: bool = True) -> None:
+    """Start (clearing the totals) or stop per-launch device timing."""
+    lib.la_profile_enable(1 if on else 0)
+
+
+def profile_read(kernel: str):
+    """(total milliseconds, timed launches) of one kernel since profile_enable(True)."""
+    ms, n = ctypes.c_double(), ctypes.c_longlong()
+    rc = lib.la_profile_read(KERNELS[kernel], ctypes.byref(ms), ctypes.byref(n))
+    if rc != 0:
+        raise LinAttnError("la_profile_read", rc)
+    return ms.value, n.value
 
 
 def kernel_launches() -> int:

@@ -197,6 +197,34 @@ LA_API const char *la_last_error_detail(void);
  */
 LA_API unsigned long long la_kernel_launches(void);
 
+/* Kernels whose device time la_profile_read reports. */
+typedef enum {
+  LA_KERNEL_CAUSAL_MAIN = 0,   /* tensor-core causal pass (bf16, d_k = d_v = 128) */
+  LA_KERNEL_CAUSAL_STATE = 1,  /* its state-only first pass over earlier segments */
+  LA_KERNEL_EXACT_HEAD = 2,    /* exact fp32 pass over each head's leading tokens */
+  LA_KERNEL_CAUSAL_SIMT = 3,   /* fp32 chunked causal kernel (other shapes) */
+  LA_KERNEL_GLOBAL_STATE = 4,  /* global form: state build */
+  LA_KERNEL_GLOBAL_READ = 5,   /* global form: read */
+  LA_KERNEL_DECODE = 6         /* recurrent decode step */
+} la_kernel;
+
+/*
+ * Diagnostics: per-kernel device time.  la_profile_enable(1) clears the
+ * totals and from then on brackets every launch of this library with a CUDA
+ * event pair recorded on the launch's own stream (two event creations and
+ * records per launch: host cost only, nothing is added to the kernels);
+ * la_profile_enable(0) stops recording.  la_profile_read waits for the
+ * recorded pairs to complete and returns, for one kernel, the summed
+ * milliseconds between its events and the number of timed launches since
+ * the last enable.  A kernel that shares the GPU with a concurrent one (the
+ * exact leading-token pass runs beside the tensor-core pass) is timed as it
+ * ran, contention included.  Thread-safe.  Errors: LA_ERR_INVALID_VALUE for an
+ * unknown kernel or NULL outputs; a failed event query maps like a launch
+ * error (the totals still hold the pairs that completed).
+ */
+LA_API la_status la_profile_enable(int on);
+LA_API la_status la_profile_read(la_kernel kernel, double *ms_total, long long *launches);
+
 #ifdef __cplusplus
 }
 #endif

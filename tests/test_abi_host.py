@@ -109,3 +109,14 @@ def test_binding_rejects_bad_tensors_before_the_library():
         L.la_causal(q, q, q)  # CPU tensors
     with pytest.raises(ValueError):
         L.la_decode_step(q, q, q, None, None)
+
+
+def test_profile_diagnostics_without_launches():
+    L.profile_enable(True)
+    for name in L.KERNELS:
+        assert L.profile_read(name) == (0.0, 0)
+    L.profile_enable(False)
+    ms, n = ctypes.c_double(), ctypes.c_longlong()
+    assert L.lib.la_profile_read(7, ctypes.byref(ms), ctypes.byref(n)) == INVALID
+    assert L.lib.la_profile_read(-1, ctypes.byref(ms), ctypes.byref(n)) == INVALID
+    assert L.lib.la_profile_read(0, None, ctypes.byref(n)) == INVALID
