@@ -47,6 +47,23 @@ namespace la {
 
 __device__ unsigned int g_device_status;
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+
 namespace {
 using namespace tc;
 
@@ -102,45 +119,6 @@ struct TcParams {
   float eps;
 };
 
-// OR of a per-thread flag over a named barrier's threads (also a barrier).
-__device__ __forceinline__ bool bar_or(uint32_t id, uint32_t threads, bool flag) {
-  uint32_t r;
-  asm volatile(
-      "{\n.reg .pred pi, po;\nsetp.ne.u32 pi, %1, 0;\nbar.red.or.pred po, %2, %3, pi;\nselp.u32 %0, 1, 0, po;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)flag), "r"(id), "r"(threads)
-      : "memory");
-  return r != 0;
-}
-
-// Bounded wait that ignores the abort word: used only to drain copies and MMAs
-// already in flight before the CTA exits.
-__device__ __forceinline__ void wait_drain(uint64_t *bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > kWaitNs) {
-      atomicOr(&g_device_status, kAbortTimeout);
-      return;
-    }
-}
-
-// phi on two packed bf16 values.  Both branches are evaluated for both
-// halves and the result picked by the sign bit (no divergence): exp in fp32
-// rounded to bf16, and x + 1 as a bf16x2 add (the exact sum rounded once, the
-// same value as the fp32 sum rounded to bf16).  x = +-0 gives 1 either way.
-__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
-  const float a = __uint_as_float(x << 16), b = __uint_as_float(x & 0xffff0000u);
-  const __nv_bfloat162 e2 = __floats2bfloat162_rn(__expf(a), __expf(b));
-  const __nv_bfloat162 x1 = __hadd2(*reinterpret_cast<const __nv_bfloat162 *>(&x), __floats2bfloat162_rn(1.f, 1.f));
-  const uint32_t e = *reinterpret_cast<const uint32_t *>(&e2), p1 = *reinterpret_cast<const uint32_t *>(&x1);
-  const uint32_t m = ((x >> 15) & 0x00010001u) * 0xffffu;  // halves with the sign bit set take exp
-  return (e & m) | (p1 & ~m);
-}
-
-__device__ __forceinline__ uint4 phi8(uint4 x) {
-  return make_uint4(phi_bf16x2(x.x), phi_bf16x2(x.y), phi_bf16x2(x.z), phi_bf16x2(x.w));
-}
-
 __device__ __forceinline__ float dot8(uint4 y, const float *z) {
   const uint32_t w[4] = {y.x, y.y, y.z, y.w};
   const float4 z0 = *reinterpret_cast<const float4 *>(z), z1 = *reinterpret_cast<const float4 *>(z + 4);
@@ -152,11 +130,6 @@ __device__ __forceinline__ float dot8(uint4 y, const float *z) {
     s = fmaf(__uint_as_float(w[e] & 0xffff0000u), zz[2 * e + 1], s);
   }
   return s;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t *>(&r);
 }
 
 // Write 32 values (columns col0 .. col0+31 of row `row`) as bf16 into a
@@ -213,12 +186,6 @@ __device__ __forceinline__ int column_pair_sums_8w(const uint8_t *tile, int w, i
   s0 = a0;
   s1 = a1;
   return c;
-}
-
-// Byte offset of fp32 element (row, col) in a [128 rows x 32] fp32 box written
-// with 128-byte rows and the 128-byte swizzle (16-byte chunks XOR row mod 8).
-__device__ __forceinline__ uint32_t sw128_offset_f32(uint32_t row, uint32_t col) {
-  return (row >> 3) * 1024u + (row & 7u) * 128u + ((((col >> 2) ^ row) & 7u) << 4) + ((col & 3u) << 2);
 }
 
 template <bool kStateOnly>
@@ -326,11 +293,11 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       // every issued copy must land before shared memory is released
       if (!kStateOnly)
         for (int c = max(0, issued_q - kStages); c < issued_q; ++c)
-          wait_drain(&full_q[c % kStages], (c / kStages) & 1);
+          wait_drain(&full_q[c % kStages], (c / kStages) & 1, status);
       for (int c = max(0, issued_k - kStages); c < issued_k; ++c)
-        wait_drain(&full_k[c % kStages], (c / kStages) & 1);
+        wait_drain(&full_k[c % kStages], (c / kStages) & 1, status);
       for (int c = max(0, issued_v - kStages); c < issued_v; ++c)
-        wait_drain(&full_v[c % kStages], (c / kStages) & 1);
+        wait_drain(&full_v[c % kStages], (c / kStages) & 1, status);
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer (one thread) ----------------
@@ -388,7 +355,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       }
       if (kStateOnly) mma_commit(s_full);
       mma_commit(drain);
-      wait_drain(drain, 0);
+      wait_drain(drain, 0, status);
     }
   } else if (warp < kWarpEpi) {
     // ---------------- feature-map warps (8) ----------------
@@ -685,21 +652,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    else
-      cudaGetLastError();
-  });
-  return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
 
 // [BH][N][128] bf16 viewed as a 3-D tensor; boxes of 64 features x 128 tokens x 1 head.
 bool make_map(CUtensorMap *m, const void *base, long BH, long N) {

@@ -1,0 +1,616 @@
+// Global (non-causal) linear attention on the sm_103a tensor cores.
+//
+// S = sum_j phi(k_j) v_j^T and z = sum_j phi(k_j) over the whole sequence,
+// then o_i = phi(q_i)^T S / (phi(q_i)^T z + eps) for every position
+// ("Linear Attention Math", "Linear attention by associativity";
+// "线性注意力从头到尾讲清楚" §4 and the sketch in §8).  Two kernels:
+//
+// 1. State build: a cluster of G CTAs per head, each over a contiguous range
+//    of tokens.  TMA lands K and V tiles (128-byte swizzle); eight warps
+//    apply phi to K in place (bf16) and zero the rows past the end; one
+//    thread issues S += phi(K)^T V (M = N = 128) and z += phi(K)^T 1 (N = 16
+//    against a constant ones operand) into fp32 tensor-memory accumulators.
+//    For d = 64 the 128 rows of M are two 128-token sub-tiles side by side:
+//    the MMA forms [K_a | K_b]^T [V_a | V_b], whose two diagonal 64x64 blocks
+//    are the sub-tiles' contributions (the off-diagonal blocks are unused).
+//    The partial states meet through distributed shared memory and the
+//    cluster writes S and z.
+// 2. Read: persistent CTAs over 128-token tiles.  phi is applied to the Q
+//    tile in place; B = [bf16(S) | hi and lo bf16 parts of z | 0] is built
+//    once per head in a K-major layout, so one MMA (M = 128, N = d + 16,
+//    K = d) gives every numerator and the denominator; eight warps
+//    normalise and stage fp32 rows that TMA stores write out.
+//
+// Every mbarrier wait is bounded: a wait that runs out raises the CTA's
+// abort word and the device status word, and the CTA drains its copies and
+// MMAs, frees tensor memory and exits.
+#include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace la {
+
+__device__ unsigned int g_global_status;
+
+namespace {
+using namespace tc;
+
+constexpr uint32_t kBlk = 16384;           // [128 rows x 128 bytes], 128-byte swizzled
+constexpr uint32_t kAbortMisaligned = 2u;  // status bit: shared memory base not 1024-aligned
+
+// ------------------------------------------------------------------ state build
+
+constexpr int kBuildThreads = 320;  // warp 0 TMA, 1 MMA, 2-9 phi(K) and the epilogue
+constexpr int kBuildStages = 3;
+constexpr int kBuildPhi = 256;
+constexpr uint32_t kBarBuild = 1;  // named barrier of warps 2-9
+
+template <int D>
+struct BuildLayout {
+  static constexpr uint32_t kStage = 2 * kBlk;  // one K or V stage: 32 KB
+  static constexpr uint32_t K = 0;
+  static constexpr uint32_t V = K + kBuildStages * kStage;
+  static constexpr uint32_t Ones = V + kBuildStages * kStage;  // K-major [16 x 128] bf16, row 0 all ones
+  static constexpr uint32_t Bars = Ones + 4096;
+  static constexpr int kNumBars = 3 * kBuildStages + 2;
+  static constexpr uint32_t Misc = Bars + kNumBars * 8;
+  static constexpr uint32_t Bytes = Misc + 16;
+  // partial state [128 rows][D + 4] fp32 (column D holds z), written over the K stages
+  static constexpr int kPStride = D + 4;
+  static_assert(128 * kPStride * 4 <= kBuildStages * kStage, "partial state fits over the K stages");
+};
+static_assert(BuildLayout<128>::Bytes <= 232448, "shared memory budget");
+
+struct BuildParams {
+  CUtensorMap tk, tv;  // [BH][N][D] bf16, box 64 x 128 x 1, 128-byte swizzle
+  float *S, *z;
+  long N;
+  int units;  // token units per head: 256 tokens (d = 64) or 128 (d = 128)
+};
+
+template <int D>
+__global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid_constant__ BuildParams p) {
+  using Lay = BuildLayout<D>;
+  constexpr int kUnit = D == 64 ? 256 : 128;
+  constexpr int kPS = Lay::kPStride;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // every CTA sees the same base, so either all return here or none does
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(&g_global_status, kAbortMisaligned);
+    return;
+  }
+  uint8_t *sm = smem_raw;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::Bars);
+  uint64_t *full = bars, *phi_done = bars + kBuildStages, *empty = bars + 2 * kBuildStages,
+           *acc_full = bars + 3 * kBuildStages, *drain = acc_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::Misc);
+  volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
+  unsigned int *status = &g_global_status;
+  float *P = reinterpret_cast<float *>(sm + Lay::K);
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int G = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int u0 = (int)((long)p.units * rank / G), u1 = (int)((long)p.units * (rank + 1) / G);
+  const int nu = u1 - u0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kBuildStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&phi_done[s], kBuildPhi);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_word = 0;
+    fence_barrier_init();
+  }
+  // the ones operand: two 64-wide K atoms of 16 rows; row 0 of each is all ones
+  for (int i = threadIdx.x; i < 256; i += kBuildThreads) {
+    const uint32_t one2 = 0x3f803f80u;  // two bf16 ones
+    const bool first_row = ((i & 127) >> 3) == 0;
+    *reinterpret_cast<uint4 *>(sm + Lay::Ones + i * 16) =
+        first_row ? make_uint4(one2, one2, one2, one2) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_async_smem();
+  if (warp == 1) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tZ = tmem + 128;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&p.tk);
+      prefetch_tmap(&p.tv);
+      int issued = 0;
+      for (int i = 0; i < nu; ++i) {
+        const int s = i % kBuildStages;
+        const uint32_t r = i / kBuildStages;
+        if (i >= kBuildStages && !mbar_wait(&empty[s], (r - 1) & 1, abort_word, status)) break;
+        const int tok = (u0 + i) * kUnit;
+        uint8_t *k = sm + Lay::K + s * Lay::kStage, *v = sm + Lay::V + s * Lay::kStage;
+        mbar_arrive_expect_tx(&full[s], 2 * Lay::kStage);
+        // d = 64: two 128-token sub-tiles; d = 128: the two 64-feature halves of one tile
+        const int x1 = D == 64 ? 0 : 64, t1 = D == 64 ? tok + 128 : tok;
+        tma_load_3d(k, &p.tk, &full[s], 0, tok, bh);
+        tma_load_3d(k + kBlk, &p.tk, &full[s], x1, t1, bh);
+        tma_load_3d(v, &p.tv, &full[s], 0, tok, bh);
+        tma_load_3d(v + kBlk, &p.tv, &full[s], x1, t1, bh);
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - kBuildStages); i < issued; ++i)
+        wait_drain(&full[i % kBuildStages], (i / kBuildStages) & 1, status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t iS = idesc_bf16_f32(128, 128, 1, 1);
+      constexpr uint32_t iZ = idesc_bf16_f32(128, 16, 1, 0);
+      const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V), sO = smem_u32(sm + Lay::Ones);
+      for (int i = 0; i < nu; ++i) {
+        const int s = i % kBuildStages;
+        if (!mbar_wait(&phi_done[s], (i / kBuildStages) & 1, abort_word, status)) break;
+        tc_fence_after();
+        const uint32_t k = sK + s * Lay::kStage, v = sV + s * Lay::kStage;
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t a = sw128_desc(k + ks * 2048, kBlk, 1024);  // MN-major: 16 tokens per step
+          const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
+          mma_bf16(tS, a, sw128_desc(v + ks * 2048, kBlk, 1024), iS, acc);
+          mma_bf16(tZ, a, sw128_desc(sO + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024), iZ, acc);
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(acc_full);
+      mma_commit(drain);
+      wait_drain(drain, 0, status);
+    }
+  } else {
+    // ---------------- phi(K) in place, then the partial state ----------------
+    const int pt = threadIdx.x - 64;
+    bool failed = false;
+    for (int i = 0; i < nu; ++i) {
+      const int s = i % kBuildStages;
+      const bool ok = mbar_wait(&full[s], (i / kBuildStages) & 1, abort_word, status);
+      if (bar_or(kBarBuild, kBuildPhi, !ok)) {
+        failed = true;
+        break;
+      }
+      uint8_t *k = sm + Lay::K + s * Lay::kStage;
+      const long tok0 = (long)(u0 + i) * kUnit;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int ch = pt + kBuildPhi * j;  // 16-byte chunk; 8 per 128-byte row
+        const int row = ch >> 3;            // 0..255 over the two blocks
+        const long tok = tok0 + (D == 64 ? row : (row & 127));
+        uint4 *c = reinterpret_cast<uint4 *>(k + ch * 16);
+        *c = tok < p.N ? phi8(*c) : make_uint4(0u, 0u, 0u, 0u);  // rows past the end add nothing
+      }
+      fence_async_smem();
+      mbar_arrive(&phi_done[s]);
+    }
+    bool ok = !failed && mbar_wait(acc_full, 0, abort_word, status);
+    ok = !bar_or(kBarBuild, kBuildPhi, !ok);
+    const int quarter = warp & 3, half = (warp - 2) >> 2, row = quarter * 32 + lane;
+    float *prow = P + row * kPS;
+    if (ok && nu > 0) {
+      tc_fence_after();
+      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+      uint32_t v[32];
+      constexpr int kParts = D == 64 ? 1 : 2;
+#pragma unroll
+      for (int c = 0; c < kParts; ++c) {
+        // d = 64: rows 0-63 hold K_a^T V_a in columns 0-63, rows 64-127 K_b^T V_b in columns 64-127
+        const int src = D == 64 ? (row < 64 ? 0 : 64) + 32 * half : 64 * half + 32 * c;
+        const int dst = D == 64 ? 32 * half : 64 * half + 32 * c;
+        tmem_ld32(tS + lanes + src, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4 *>(prow + dst + 4 * q) =
+              make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                          __uint_as_float(v[4 * q + 3]));
+      }
+      const float zv = __uint_as_float(tmem_ld1(tZ + lanes));
+      if (half == 0) prow[D] = zv;
+    } else {
+      const int w = D == 64 ? 32 : 64;
+      for (int c = 0; c < w; ++c) prow[w * half + c] = 0.f;
+      if (half == 0) prow[D] = 0.f;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  cluster.sync();  // every partial state of the cluster is in shared memory
+  {
+    // this CTA sums rows [r0, r0 + D/G) of S (and those entries of z) over the cluster
+    const int rows = D / G, r0 = rank * rows;
+    for (int e = threadIdx.x; e < rows * (D + 1); e += kBuildThreads) {
+      const int i = r0 + e / (D + 1), j = e % (D + 1);
+      float acc = 0.f;
+      for (int c = 0; c < G; ++c) {
+        const float *Pc = cluster.map_shared_rank(P, c);
+        acc += Pc[i * kPS + j];
+        if (D == 64) acc += Pc[(64 + i) * kPS + j];
+      }
+      if (j < D)
+        p.S[((long)bh * D + i) * D + j] = acc;
+      else
+        p.z[(long)bh * D + i] = acc;
+    }
+  }
+  cluster.sync();  // remote reads are done before any CTA of the cluster exits
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ------------------------------------------------------------------ read
+
+constexpr int kReadThreads = 448;  // warp 0 TMA, 1 MMA, 2-5 phi(Q) and B, 6-13 epilogue
+constexpr int kReadPhi = 128, kReadEpi = 256;
+constexpr uint32_t kBarEpi = 1, kBarPhi = 2;
+
+template <int D>
+struct ReadLayout {
+  static constexpr int kStages = D == 64 ? 3 : 2;  // Q tiles in flight
+  static constexpr int NB = D + 16;             // B rows: d columns of S, z hi, z lo, zero padding
+  static constexpr uint32_t kQ = D * 2 * 128;   // one Q tile (D/64 swizzled 16 KB blocks)
+  static constexpr uint32_t kAtomB = NB * 128;  // one 64-wide K atom of B
+  static constexpr uint32_t kB = (D / 64) * kAtomB;
+  static constexpr int kOutBufs = D == 64 ? 2 : 1;
+  static constexpr uint32_t kOut = D * 4 * 128;  // one fp32 tile: D/32 boxes of [128 x 32]
+  static constexpr uint32_t Q = 0;
+  static constexpr uint32_t B = Q + kStages * kQ;  // two buffers (heads alternate)
+  static constexpr uint32_t O = B + 2 * kB;
+  static constexpr uint32_t Bars = O + kOutBufs * kOut;
+  static constexpr int kNumBars = 3 * kStages + 8;
+  static constexpr uint32_t Misc = Bars + kNumBars * 8;
+  static constexpr uint32_t Bytes = Misc + 16;
+  static constexpr uint32_t kAccCols = D == 64 ? 128 : 256;  // column distance of the two accumulators
+  static constexpr uint32_t TmemCols = 2 * kAccCols;
+  static_assert(kAtomB % 1024 == 0 && kB % 1024 == 0, "B atoms stay 1024-aligned");
+};
+static_assert(ReadLayout<128>::Bytes <= 232448, "shared memory budget");
+
+struct ReadParams {
+  CUtensorMap tq;  // [BH][N][D] bf16, box 64 x 128 x 1, 128-byte swizzle
+  CUtensorMap to;  // [BH][N][D] fp32, box 32 x 128 x 1, 128-byte swizzle
+  const float *S, *z;
+  long N;
+  long tiles_per_head, total_tiles;
+  float eps;
+};
+
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+// B for one head, K-major and 128-byte swizzled: row n < D holds column n of
+// S over the D key features (bf16), rows D and D+1 the hi and lo bf16 parts
+// of z, the rest zeros.  128 threads; consecutive threads take consecutive
+// rows, so the reads of S are coalesced and the swizzled stores conflict-free.
+template <int D>
+__device__ __forceinline__ void build_b(uint8_t *B, const float *__restrict__ S, const float *__restrict__ z,
+                                        int t) {
+  using Lay = ReadLayout<D>;
+  constexpr int NB = Lay::NB, kChunks = D / 8;  // 16-byte chunks per row
+  for (int e = t; e < kChunks * NB; e += kReadPhi) {
+    const int n = e % NB, c = e / NB;
+    uint32_t w[4];
+    if (n < D) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = pack_bf16(S[(8 * c + 2 * j) * D + n], S[(8 * c + 2 * j + 1) * D + n]);
+    } else if (n < D + 2) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = z[8 * c + 2 * j], b = z[8 * c + 2 * j + 1];
+        const float ah = __bfloat162float(__float2bfloat16_rn(a)), bh = __bfloat162float(__float2bfloat16_rn(b));
+        w[j] = n == D ? pack_bf16(ah, bh) : pack_bf16(a - ah, b - bh);
+      }
+    } else {
+      w[0] = w[1] = w[2] = w[3] = 0u;
+    }
+    const int atom = c >> 3, cc = c & 7;
+    *reinterpret_cast<uint4 *>(B + atom * Lay::kAtomB + n * 128 + ((cc ^ (n & 7)) << 4)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kReadThreads, 1) global_read_tc(const __grid_constant__ ReadParams p) {
+  using Lay = ReadLayout<D>;
+  constexpr int NB = Lay::NB;
+  constexpr int kStages = Lay::kStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(&g_global_status, kAbortMisaligned);
+    return;
+  }
+  uint8_t *sm = smem_raw;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::Bars);
+  uint64_t *full = bars, *phi_done = bars + kStages, *q_empty = bars + 2 * kStages,
+           *acc_full = bars + 3 * kStages,  // [2]
+      *acc_empty = acc_full + 2,                // [2]
+      *b_free = acc_full + 4,                   // [2]
+      *drain = acc_full + 6;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::Misc);
+  volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
+  unsigned int *status = &g_global_status;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long t_lo = p.total_tiles * blockIdx.x / gridDim.x;
+  const long t_hi = p.total_tiles * (blockIdx.x + 1) / gridDim.x;
+  const int n = (int)(t_hi - t_lo);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&phi_done[s], kReadPhi);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kReadEpi / 32);
+      mbar_init(&b_free[b], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_word = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, Lay::TmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&p.tq);
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % kStages;
+        const uint32_t r = i / kStages;
+        if (i >= kStages && !mbar_wait(&q_empty[s], (r - 1) & 1, abort_word, status)) break;
+        const long tile = t_lo + i;
+        const int bh = (int)(tile / p.tiles_per_head), tok = (int)(tile % p.tiles_per_head) * 128;
+        uint8_t *q = sm + Lay::Q + s * Lay::kQ;
+        mbar_arrive_expect_tx(&full[s], Lay::kQ);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) tma_load_3d(q + b * kBlk, &p.tq, &full[s], 64 * b, tok, bh);
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        wait_drain(&full[i % kStages], (i / kStages) & 1, status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t iR = idesc_bf16_f32(128, NB, 0, 0);
+      const uint32_t sQ = smem_u32(sm + Lay::Q), sB = smem_u32(sm + Lay::B);
+      int hl = 0;  // local head index: B buffer hl & 1
+      for (int i = 0; i < n; ++i) {
+        const int s = i % kStages, buf = i & 1;
+        const long tile = t_lo + i;
+        if (i > 0 && tile / p.tiles_per_head != (tile - 1) / p.tiles_per_head) ++hl;
+        if (!mbar_wait(&phi_done[s], (i / kStages) & 1, abort_word, status)) break;
+        if (i >= 2 && !mbar_wait(&acc_empty[buf], ((i >> 1) - 1) & 1, abort_word, status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * Lay::kAccCols, q = sQ + s * Lay::kQ, b = sB + (hl & 1) * Lay::kB;
+#pragma unroll 1
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16(d, sw128_desc(q + (ks >> 2) * kBlk + (ks & 3) * 32, 16, 1024),
+                   sw128_desc(b + (ks >> 2) * Lay::kAtomB + (ks & 3) * 32, 16, 1024), iR, ks > 0 ? 1u : 0u);
+        mma_commit(&q_empty[s]);
+        mma_commit(&acc_full[buf]);
+        // the last tile of a head frees its B buffer once these MMAs complete
+        if (i == n - 1 || (tile + 1) / p.tiles_per_head != tile / p.tiles_per_head) mma_commit(&b_free[hl & 1]);
+      }
+      mma_commit(drain);
+      wait_drain(drain, 0, status);
+    }
+  } else if (warp < 6) {
+    // ---------------- phi(Q) in place, and B per head ----------------
+    const int pt = threadIdx.x - 64;
+    int hl = -1;
+    long prev_bh = -1;
+    for (int i = 0; i < n; ++i) {
+      const int s = i % kStages;
+      const long tile = t_lo + i, bh = tile / p.tiles_per_head;
+      if (bh != prev_bh) {
+        ++hl;
+        // B buffer hl & 1 last served head hl - 2
+        const bool ok = hl < 2 || mbar_wait(&b_free[hl & 1], ((hl >> 1) - 1) & 1, abort_word, status);
+        if (bar_or(kBarPhi, kReadPhi, !ok)) break;
+        build_b<D>(sm + Lay::B + (hl & 1) * Lay::kB, p.S + bh * D * D, p.z + bh * D, pt);
+        prev_bh = bh;
+      }
+      const bool ok = mbar_wait(&full[s], (i / kStages) & 1, abort_word, status);
+      if (bar_or(kBarPhi, kReadPhi, !ok)) break;
+      uint8_t *q = sm + Lay::Q + s * Lay::kQ;
+#pragma unroll
+      for (int j = 0; j < (int)(Lay::kQ / 16) / kReadPhi; ++j) {
+        uint4 *c = reinterpret_cast<uint4 *>(q + (pt + kReadPhi * j) * 16);
+        *c = phi8(*c);
+      }
+      fence_async_smem();
+      mbar_arrive(&phi_done[s]);
+    }
+  } else {
+    // ---------------- epilogue: normalise, stage, TMA store ----------------
+    const int et = threadIdx.x - 192;  // 0..255
+    const int quarter = warp & 3, half = (warp - 6) >> 2, row = quarter * 32 + lane;
+    const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+    for (int i = 0; i < n; ++i) {
+      const int buf = i & 1, ob = i % Lay::kOutBufs;
+      const long tile = t_lo + i;
+      const int bh = (int)(tile / p.tiles_per_head), tok = (int)(tile % p.tiles_per_head) * 128;
+      const bool ok = mbar_wait(&acc_full[buf], (i >> 1) & 1, abort_word, status);
+      if (bar_or(kBarEpi, kReadEpi, !ok)) break;
+      tc_fence_after();
+      const uint32_t ta = tmem + buf * Lay::kAccCols + lanes;
+      const float den = __uint_as_float(tmem_ld1(ta + D)) + __uint_as_float(tmem_ld1(ta + D + 1));
+      const float inv = 1.f / (den + p.eps);
+      constexpr int kParts = D / 64;  // 32-column loads per thread
+      uint32_t v[kParts][32];
+#pragma unroll
+      for (int c = 0; c < kParts; ++c) tmem_ld32(ta + (D / 2) * half + 32 * c, v[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      // the staging buffer is free once the store issued from it kOutBufs tiles ago has read it
+      if (et == 0) {
+        if (Lay::kOutBufs == 2)
+          bulk_wait_read_1();
+        else
+          bulk_wait_read();
+      }
+      named_bar(kBarEpi, kReadEpi);
+      uint8_t *stage = sm + Lay::O + ob * Lay::kOut;
+#pragma unroll
+      for (int c = 0; c < kParts; ++c) {
+        uint8_t *box = stage + ((D / 64) * half + c) * kBlk;  // box b holds columns [32b, 32b + 32)
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          *reinterpret_cast<float4 *>(box + sw128_offset_f32(row, 4 * q4)) =
+              make_float4(__uint_as_float(v[c][4 * q4]) * inv, __uint_as_float(v[c][4 * q4 + 1]) * inv,
+                          __uint_as_float(v[c][4 * q4 + 2]) * inv, __uint_as_float(v[c][4 * q4 + 3]) * inv);
+      }
+      fence_async_smem();
+      named_bar(kBarEpi, kReadEpi);
+      if (et == 0) {
+#pragma unroll
+        for (int b = 0; b < D / 32; ++b) tma_store_3d(&p.to, stage + b * kBlk, 32 * b, tok, bh);
+        bulk_commit();
+      }
+    }
+    if (et == 0) bulk_wait_all();  // output stores complete before the CTA exits
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lay::TmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t elem, const void *base, long BH, long N, int D,
+              uint32_t box_x) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * elem, (cuuint64_t)N * D * elem};
+  cuuint32_t box[3] = {box_x, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename F>
+cudaError_t set_smem_once(F *kernel, uint32_t bytes, std::once_flag &once, cudaError_t &err) {
+  std::call_once(once, [&] {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  });
+  return err;
+}
+
+template <int D>
+cudaError_t launch_t(const Problem &p) {
+  const DeviceInfo &di = device_info(-1);
+  const long sms = std::max(1, di.sm_count);
+  BuildParams bp;
+  ReadParams rp;
+  if (!make_map(&bp.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k, p.BH, p.N, D, 64) ||
+      !make_map(&bp.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v, p.BH, p.N, D, 64) ||
+      !make_map(&rp.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q, p.BH, p.N, D, 64) ||
+      !make_map(&rp.to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.out, p.BH, p.N, D, 32))
+    return cudaErrorInvalidValue;
+  constexpr int kUnit = D == 64 ? 256 : 128;
+  bp.S = p.S;
+  bp.z = p.z;
+  bp.N = p.N;
+  bp.units = (int)((p.N + kUnit - 1) / kUnit);
+  // cluster size: a power of two <= 8 so that the build covers the SMs about once, >= 4 units a CTA
+  int G = 1;
+  while (G < 8 && p.BH * (2 * G) <= sms && bp.units / (2 * G) >= 4) G *= 2;
+
+  static std::once_flag once_b, once_r;
+  static cudaError_t err_b, err_r;
+  cudaError_t e = set_smem_once(global_build_tc<D>, BuildLayout<D>::Bytes, once_b, err_b);
+  if (e != cudaSuccess) return e;
+  e = set_smem_once(global_read_tc<D>, ReadLayout<D>::Bytes, once_r, err_r);
+  if (e != cudaSuccess) return e;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)G;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)G, (unsigned)p.BH);
+  cfg.blockDim = dim3(kBuildThreads);
+  cfg.dynamicSmemBytes = BuildLayout<D>::Bytes;
+  cfg.stream = p.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  {
+    LaunchTimer timer(kKGlobalState, p.stream);
+    e = cudaLaunchKernelEx(&cfg, global_build_tc<D>, bp);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    timer.done(e);
+  }
+  if (e != cudaSuccess) return e;
+  count_launch();
+
+  rp.S = p.S;
+  rp.z = p.z;
+  rp.N = p.N;
+  rp.tiles_per_head = (p.N + 127) / 128;
+  rp.total_tiles = rp.tiles_per_head * p.BH;
+  rp.eps = p.eps;
+  const unsigned grid = (unsigned)std::min<long>(rp.total_tiles, sms);
+  {
+    LaunchTimer timer(kKGlobalRead, p.stream);
+    global_read_tc<D><<<grid, kReadThreads, ReadLayout<D>::Bytes, p.stream>>>(rp);
+    e = cudaGetLastError();
+    timer.done(e);
+  }
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+}  // namespace
+
+bool global_tc_supported(const Problem &p) {
+  const DeviceInfo &di = device_info(-1);
+  return p.dt == LA_BF16 && p.dk == p.dv && (p.dk == 64 || p.dk == 128) && p.N >= 1 && p.N <= 0x7fffffffL &&
+         p.BH <= 65535 && di.cc_major == 10 && di.cc_minor == 3 && tensor_map_encoder() != nullptr;
+}
+
+cudaError_t launch_global_tc(const Problem &p) { return p.dk == 64 ? launch_t<64>(p) : launch_t<128>(p); }
+
+cudaError_t read_and_clear_global_tc_status(unsigned int *value) {
+  const unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_global_status, sizeof(unsigned int));
+  if (e == cudaSuccess && *value) e = cudaMemcpyToSymbol(g_global_status, &zero, sizeof(unsigned int));
+  return e;
+}
+
+}  // namespace la

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "linattn.h"
 
@@ -38,6 +39,15 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state);
 // Sets *too_large (and launches nothing) if they would not fit.
 cudaError_t launch_causal_tc_noalloc(const Problem &p, int dev, bool *too_large);
 size_t noalloc_scratch_capacity_bytes();
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (the library
+// does not link libcuda); nullptr if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// Tensor-core global form (bf16, d_k = d_v in {64, 128}): state build, then read.
+bool global_tc_supported(const Problem &p);
+cudaError_t launch_global_tc(const Problem &p);
+cudaError_t read_and_clear_global_tc_status(unsigned int *value);
 
 // Read and clear the device status word (bounded-wait timeouts).
 cudaError_t read_and_clear_device_status(unsigned int *value);

@@ -162,9 +162,11 @@ la_status la_device_status(void *stream) {
   if (st != LA_OK) return st;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return la::from_cuda(e);
-  unsigned int v = 0;
+  unsigned int v = 0, vg = 0;
   e = la::read_and_clear_device_status(&v);
+  if (e == cudaSuccess) e = la::read_and_clear_global_tc_status(&vg);
   if (e != cudaSuccess) return la::from_cuda(e);
+  v |= vg;
   if (v & 1u) return LA_ERR_TIMEOUT;
   return v ? LA_ERR_LAUNCH : LA_OK;  // other bits: a kernel refused to run (e.g. misaligned shared memory)
 }
@@ -262,6 +264,7 @@ la_status la_global(const void *q, const void *k, const void *v, float *out, flo
   int dev;
   if ((st = la::current_device(&dev)) != LA_OK) return st;
   Problem p{q, k, v, out, S, z, B * H, (long)N, d_k, d_v, eps, dt, (cudaStream_t)stream};
+  if (la::global_tc_supported(p)) return la::from_cuda(la::launch_global_tc(p));
   return la::from_cuda(la::launch_global_simt(p));
 }
 

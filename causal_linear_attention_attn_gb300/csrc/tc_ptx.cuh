@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace la {
@@ -270,6 +271,59 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 // rows hold 64 two-byte elements (one 16 KB block holds 128 rows).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
   return (row >> 3) * 1024u + (row & 7u) * 128u + ((((col >> 3) ^ row) & 7u) << 4) + ((col & 7u) << 1);
+}
+
+// ---------------------------------------------------------------------------
+// Small helpers shared by the tensor-core kernels.
+// ---------------------------------------------------------------------------
+// OR of a per-thread flag over a named barrier's threads (also a barrier).
+__device__ __forceinline__ bool bar_or(uint32_t id, uint32_t threads, bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred pi, po;\nsetp.ne.u32 pi, %1, 0;\nbar.red.or.pred po, %2, %3, pi;\nselp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)flag), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that ignores the abort word: used only to drain copies and MMAs
+// already in flight before the CTA exits.
+__device__ __forceinline__ void wait_drain(uint64_t *bar, uint32_t parity, unsigned int *status) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      atomicOr(status, kAbortTimeout);
+      return;
+    }
+}
+
+// phi on two packed bf16 values.  Both branches are evaluated for both
+// halves and the result picked by the sign bit (no divergence): exp in fp32
+// rounded to bf16, and x + 1 as a bf16x2 add (the exact sum rounded once, the
+// same value as the fp32 sum rounded to bf16).  x = +-0 gives 1 either way.
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
+  const float a = __uint_as_float(x << 16), b = __uint_as_float(x & 0xffff0000u);
+  const __nv_bfloat162 e2 = __floats2bfloat162_rn(__expf(a), __expf(b));
+  const __nv_bfloat162 x1 = __hadd2(*reinterpret_cast<const __nv_bfloat162 *>(&x), __floats2bfloat162_rn(1.f, 1.f));
+  const uint32_t e = *reinterpret_cast<const uint32_t *>(&e2), p1 = *reinterpret_cast<const uint32_t *>(&x1);
+  const uint32_t m = ((x >> 15) & 0x00010001u) * 0xffffu;  // halves with the sign bit set take exp
+  return (e & m) | (p1 & ~m);
+}
+
+__device__ __forceinline__ uint4 phi8(uint4 x) {
+  return make_uint4(phi_bf16x2(x.x), phi_bf16x2(x.y), phi_bf16x2(x.z), phi_bf16x2(x.w));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// Byte offset of fp32 element (row, col) in a [128 rows x 32] fp32 box written
+// with 128-byte rows and the 128-byte swizzle (16-byte chunks XOR row mod 8).
+__device__ __forceinline__ uint32_t sw128_offset_f32(uint32_t row, uint32_t col) {
+  return (row >> 3) * 1024u + (row & 7u) * 128u + ((((col >> 2) ^ row) & 7u) << 4) + ((col & 3u) << 2);
 }
 
 }  // namespace tc

@@ -57,6 +57,25 @@ def test_small_shapes_every_element(cuda_lib, form, dtype, shape):
     assert_close(z, rz, tau, "z")
 
 
+# Tensor-core global form (bf16, d_k = d_v in {64, 128}): clusters of 1 to 8 CTAs
+# per head in the state build, persistent read CTAs that cross many heads.
+GLOBAL_TC = [(1, 1, 1, 64), (1, 1, 8192, 64), (1, 1, 16384, 64), (2, 3, 129, 64), (4, 40, 200, 64),
+             (10, 100, 100, 64), (1, 2, 5000, 128), (2, 2, 383, 128), (1, 1, 1, 128), (3, 60, 130, 128)]
+
+
+@pytest.mark.parametrize("shape", GLOBAL_TC, ids=lambda s: "x".join(map(str, s)))
+def test_global_tensor_core_shapes_every_element(cuda_lib, shape):
+    B, H, N, d = shape
+    w = dataclasses.replace(W["global_bf16"], dk=d, dv=d)
+    q, k, v = inputs.make_qkv(w, N=N, B=B, H=H)
+    out, S, z = _run(cuda_lib, "global", q, k, v, w.eps)
+    ro, rS, rz = oracle_seq("global", q, k, v, w.eps)
+    assert_close(out, ro, 2e-2, "out")
+    assert_close(S, rS, 2e-2, "S")
+    assert_close(z, rz, 2e-2, "z")
+    assert cuda_lib.device_status() == 0
+
+
 def test_workload_causal_f32_small_every_element(cuda_lib):
     w = W["causal_f32_small"]
     q, k, v = inputs.make_qkv(w)
