@@ -10,6 +10,8 @@
 // over the first chunk of bf16 sequences, and the general fallback.
 #include <algorithm>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -134,94 +136,164 @@ cudaError_t launch_t(const Problem &p, long n_proc, bool from_state, bool write_
 // Exact fp32 outputs for tokens [0, ne) of a head (ne <= 64).  The leading
 // tokens of a sequence read a state built from few tokens, so their outputs
 // are O(1) while later ones average down; they get full fp32 weights here
-// instead of the tensor cores' bf16 operands.  One warp per query row t:
-// lanes split the keys j <= t for the weights phi(q_t).phi(k_j), then split
-// the output columns for sum_j w_j v_j.  A CTA covers 16 rows of one head.
-constexpr int kHeadRows = 16;
+// instead of the tensor cores' bf16 operands.  One CTA per head: phi(Q),
+// phi(K) and V of the leading rows are staged in fp32, the masked weights
+// W = tril(phi(Q) phi(K)^T) and the outputs W V (plus phi(Q) S0 and
+// phi(Q).z0 for a carried state) are formed with register micro-tiles, and
+// every row is divided by its own denominator sum_j W_tj (+ phi(q_t).z0) + eps.
+constexpr int kHeadThreads = 256;
+constexpr int kHeadMax = 64;
 
-template <typename Tin>
-__global__ void __launch_bounds__(kHeadRows * 32)
+template <int DK, int DV>
+struct HeadSmem {
+  static constexpr int P = DK + 1;  // padded rows of phi(Q), phi(K): column reads conflict-free
+  static constexpr int WP = kHeadMax + 1;
+  static constexpr size_t Bytes = sizeof(float) * ((size_t)2 * kHeadMax * P + kHeadMax * DV + kHeadMax * WP + kHeadMax);
+};
+
+template <typename Tin, int DK, int DV>
+__global__ void __launch_bounds__(kHeadThreads)
     causal_exact_head_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                              float *__restrict__ out, const float *__restrict__ S0, const float *__restrict__ z0,
-                             long N, int ne, int dk, int dv, float eps) {
+                             long N, int ne, float eps) {
+  using L = HeadSmem<DK, DV>;
+  constexpr int P = L::P, WP = L::WP;
   extern __shared__ float sm[];
-  const int dkp = dk + 1;
+  float *Kf = sm, *Qf = Kf + kHeadMax * P, *Vf = Qf + kHeadMax * P, *W = Vf + kHeadMax * DV, *den = W + kHeadMax * WP;
   const long bh = blockIdx.x;
-  const int r0 = blockIdx.y * kHeadRows;
-  const int rows = min(kHeadRows, ne - r0);
-  const int nk = r0 + rows;  // keys visible to these rows
-  float *Ks = sm;                      // [kT][dkp]
-  float *Vs = Ks + kT * dkp;           // [kT][dv]
-  float *Qs = Vs + kT * dv;            // [kHeadRows][dk]
-  float *W = Qs + kHeadRows * dk;      // [kHeadRows][kT] weights of each row
-  const int tid = threadIdx.x, nthr = kHeadRows * 32;
-  const int warp = tid >> 5, lane = tid & 31;
-  const Tin *qh = q + (bh * N + r0) * dk, *kh = k + bh * N * dk, *vh = v + bh * N * dv;
-  // eight elements per load (rows are 16-byte aligned for the supported sizes)
-  for (int e = 8 * tid; e < nk * dk; e += 8 * nthr) {
-    const int t = e / dk, i = e - t * dk;
-    float f[8];
-    ld8(kh + e, f);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Tin *qh = q + bh * N * DK, *kh = k + bh * N * DK, *vh = v + bh * N * DV;
+  // stage rows [0, ne) in fp32 (eight elements per 16-byte-aligned load); rows past ne are zero
+  for (int e = 8 * tid; e < kHeadMax * DK; e += 8 * kHeadThreads) {
+    const int t = e / DK, i = e % DK;
+    float fq[8], fk[8];
+    if (t < ne) {
+      ld8(qh + e, fq);
+      ld8(kh + e, fk);
+    }
 #pragma unroll
-    for (int x = 0; x < 8; ++x) Ks[t * dkp + i + x] = phi(f[x]);
+    for (int x = 0; x < 8; ++x) {
+      Qf[t * P + i + x] = t < ne ? phi(fq[x]) : 0.f;
+      Kf[t * P + i + x] = t < ne ? phi(fk[x]) : 0.f;
+    }
   }
-  for (int e = 8 * tid; e < nk * dv; e += 8 * nthr) {
+  for (int e = 8 * tid; e < kHeadMax * DV; e += 8 * kHeadThreads) {
+    const int t = e / DV;
     float f[8];
-    ld8(vh + e, f);
+    if (t < ne) ld8(vh + e, f);
 #pragma unroll
-    for (int x = 0; x < 8; ++x) Vs[e + x] = f[x];
-  }
-  for (int e = 8 * tid; e < rows * dk; e += 8 * nthr) {
-    float f[8];
-    ld8(qh + e, f);
-#pragma unroll
-    for (int x = 0; x < 8; ++x) Qs[e + x] = phi(f[x]);
+    for (int x = 0; x < 8; ++x) Vf[e + x] = t < ne ? f[x] : 0.f;
   }
   __syncthreads();
-  if (warp >= rows) return;
-  const int t = r0 + warp;  // this warp's query row
-  const float *qt = Qs + warp * dk;
-  float *wt = W + warp * kT;
-  // weights: lane handles keys j = lane, lane + 32
-  float wsum = 0.f;
-  for (int j = lane; j <= t; j += 32) {
-    float a = 0.f;
-    for (int i = 0; i < dk; ++i) a = fmaf(qt[i], Ks[j * dkp + i], a);
-    wt[j] = a;
-    wsum += a;
+  {
+    // W: thread (ty, tx) forms rows ty + 16 r and keys tx + 16 c, r, c < 4
+    const int ty = tid >> 4, tx = tid & 15;
+    float a[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) a[r][c] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < DK; ++i) {
+      float qv[4], kv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) qv[r] = Qf[(ty + 16 * r) * P + i];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) kv[c] = Kf[(tx + 16 * c) * P + i];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) a[r][c] = fmaf(qv[r], kv[c], a[r][c]);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = ty + 16 * r, j = tx + 16 * c;
+        W[i * WP + j] = j <= i ? a[r][c] : 0.f;  // inclusive causal mask
+      }
   }
-  wsum = warp_sum(wsum);
-  float d = 0.f;
-  if (S0) {
-    for (int i = lane; i < dk; i += 32) d = fmaf(qt[i], z0[bh * dk + i], d);
-    d = warp_sum(d);
+  __syncthreads();
+  // denominators, one warp per row at a time
+  for (int i = warp; i < kHeadMax; i += kHeadThreads / 32) {
+    float s = W[i * WP + lane] + W[i * WP + lane + 32];
+    if (z0)
+      for (int f = lane; f < DK; f += 32) s = fmaf(Qf[i * P + f], z0[bh * DK + f], s);
+    s = warp_sum(s);
+    if (lane == 0) den[i] = s + eps;
   }
-  const float den = (d + wsum) + eps;
-  __syncwarp();
-  // outputs: lane handles columns c = lane, lane + 32, ...
-  const float *Sh = S0 ? S0 + bh * dk * dv : nullptr;
-  for (int c = lane; c < dv; c += 32) {
-    float n = 0.f;
-    if (Sh)
-      for (int i = 0; i < dk; ++i) n = fmaf(qt[i], Sh[i * dv + c], n);
-    float m = 0.f;
-    for (int j = 0; j <= t; ++j) m = fmaf(wt[j], Vs[j * dv + c], m);
-    out[(bh * N + t) * dv + c] = (n + m) / den;
+  __syncthreads();
+  {
+    // outputs: warp w takes rows 8w .. 8w + 7, lane the columns lane + 32 c
+    constexpr int kCols = DV / 32;
+    const int r0 = 8 * warp;
+    float o[8][kCols];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) o[r][c] = 0.f;
+    const int jmax = min(ne, r0 + 8);  // keys visible to the last of these rows
+    for (int j = 0; j < jmax; ++j) {
+      float vv[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) vv[c] = Vf[j * DV + lane + 32 * c];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float w = W[(r0 + r) * WP + j];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) o[r][c] = fmaf(w, vv[c], o[r][c]);
+      }
+    }
+    if (S0) {
+      const float *Sh = S0 + bh * DK * DV;
+      for (int f = 0; f < DK; ++f) {
+        float sv[kCols];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) sv[c] = Sh[f * DV + lane + 32 * c];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const float qf = Qf[(r0 + r) * P + f];
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) o[r][c] = fmaf(qf, sv[c], o[r][c]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int t = r0 + r;
+      if (t < ne)
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) out[(bh * N + t) * DV + lane + 32 * c] = o[r][c] / den[t];
+    }
   }
+  // When launched early beside the previous kernel of the stream, this grid
+  // completes only after that kernel: the last CTA waits for it.
+  if (blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <typename Tin>
-cudaError_t launch_head_t(const Problem &p, int ne, const float *S0, const float *z0) {
-  const size_t smem = sizeof(float) * ((size_t)kT * (p.dk + 1) + (size_t)kT * p.dv + (size_t)kHeadRows * p.dk +
-                                       (size_t)kHeadRows * kT);
-  cudaError_t e = cudaFuncSetAttribute(causal_exact_head_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  const unsigned row_blocks = (unsigned)((ne + kHeadRows - 1) / kHeadRows);
+template <typename Tin, int DK, int DV>
+cudaError_t launch_head_t(const Problem &p, int ne, const float *S0, const float *z0, bool pdl) {
+  static std::once_flag once;
+  static cudaError_t attr;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(causal_exact_head_kernel<Tin, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)HeadSmem<DK, DV>::Bytes);
+  });
+  if (attr != cudaSuccess) return attr;
   LaunchTimer timer(kKExactHead, p.stream);
-  causal_exact_head_kernel<Tin><<<dim3(p.BH, row_blocks), kHeadRows * 32, smem, p.stream>>>(
-      (const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, p.out, S0, z0, p.N, ne, p.dk, p.dv, p.eps);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute early[1];
+  early[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  early[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)p.BH);
+  cfg.blockDim = dim3(kHeadThreads);
+  cfg.dynamicSmemBytes = HeadSmem<DK, DV>::Bytes;
+  cfg.stream = p.stream;
+  cfg.attrs = early;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, causal_exact_head_kernel<Tin, DK, DV>, (const Tin *)p.q, (const Tin *)p.k,
+                                     (const Tin *)p.v, p.out, S0, z0, p.N, ne, p.eps);
+  if (e == cudaSuccess) e = cudaGetLastError();
   timer.done(e);
   if (e == cudaSuccess) count_launch();
   return e;
@@ -229,11 +301,12 @@ cudaError_t launch_head_t(const Problem &p, int ne, const float *S0, const float
 
 }  // namespace
 
-cudaError_t launch_causal_exact_head(const Problem &p, long n_exact, const float *S0, const float *z0) {
+cudaError_t launch_causal_exact_head(const Problem &p, long n_exact, const float *S0, const float *z0, bool pdl) {
   if (n_exact <= 0) return cudaSuccess;
-  const int ne = (int)std::min<long>(n_exact, kT);
-  if (p.dt == LA_F32) return launch_head_t<float>(p, ne, S0, z0);
-  return launch_head_t<__nv_bfloat16>(p, ne, S0, z0);
+  if (p.dk != 128 || p.dv != 128) return cudaErrorInvalidValue;  // serves the d = 128 tensor-core pass
+  const int ne = (int)std::min<long>(n_exact, kHeadMax);
+  if (p.dt == LA_F32) return launch_head_t<float, 128, 128>(p, ne, S0, z0, pdl);
+  return launch_head_t<__nv_bfloat16, 128, 128>(p, ne, S0, z0, pdl);
 }
 
 cudaError_t launch_causal_simt(const Problem &p, long n_proc, bool from_state, bool write_state) {

@@ -256,6 +256,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     fence_barrier_init();
   }
   if (warp == kWarpMma) tmem_alloc(tmem_slot, Lay::TmemCols);
+  // the exact leading-token pass queued after this kernel may start on the SMs this grid leaves free
+  if (threadIdx.x == 0) pdl_trigger();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -365,6 +367,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     const int quarter = warp & 3;
     const int half = (warp - kWarpPhi) >> 2;
     const int row = quarter * 32 + lane;
+    if (init_parts > 0) pdl_wait();  // the first pass's partial states are complete and visible
     if (pt < kD) {
       // partial states of the first pass start from zero; a segment starts from the caller's state plus them
       float z = (!kStateOnly && p.z0) ? p.z0[(long)bh * kD + pt] : 0.f;
@@ -447,6 +450,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     bool ok = true;
     if (!kStateOnly) {
       uint8_t *Sb = sm + Lay::Sb;
+      if (init_parts > 0) pdl_wait();  // the first pass's partial states are complete and visible
       // initial state: caller's state plus the parts before this segment
       for (int cb = 0; cb < 4; ++cb) {
         float v[32];
@@ -681,7 +685,7 @@ bool make_out_map(CUtensorMap *m, void *base, long BH, long N, uint32_t rows) {
 }
 
 template <bool kStateOnly>
-cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream) {
+cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bool pdl) {
   static std::once_flag once[2];
   static cudaError_t attr_err[2];
   std::call_once(once[kStateOnly], [] {
@@ -691,8 +695,19 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream) {
   });
   if (attr_err[kStateOnly] != cudaSuccess) return attr_err[kStateOnly];
   LaunchTimer timer(kStateOnly ? kKCausalState : kKCausalMain, stream);
-  causal_tc_kernel<kStateOnly><<<grid, kThreads, Layout<kStateOnly>::Alloc, stream>>>(tp);
-  const cudaError_t e = cudaGetLastError();
+  // pdl: may start while the previous kernel of the stream (the first pass) still runs
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<kStateOnly>::Alloc;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, causal_tc_kernel<kStateOnly>, tp);
+  if (e == cudaSuccess) e = cudaGetLastError();
   timer.done(e);
   if (e == cudaSuccess) {
     count_launch();
@@ -714,31 +729,21 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream) {
 
 }  // namespace
 
-// A low-priority stream per device for work forked off the caller's stream,
-// with the two events of the fork and the join.  Created once per device.
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  bool ok = false;
-  std::mutex mu;  // held from the fork record to the join wait (the events are shared)
-};
-
-SideStream &side_stream(int dev) {
-  constexpr int kMaxDev = 64;
-  static SideStream slots[kMaxDev];
-  static std::once_flag once[kMaxDev];
-  if (dev < 0) cudaGetDevice(&dev);
-  if (dev < 0 || dev >= kMaxDev) dev = 0;
-  std::call_once(once[dev], [dev] {
-    SideStream &s = slots[dev];
-    int lo = 0, hi = 0;
-    cudaDeviceGetStreamPriorityRange(&lo, &hi);  // lo = numerically largest = lowest priority
-    s.ok = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, lo) == cudaSuccess &&
-           cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) == cudaSuccess;
-    if (!s.ok) cudaGetLastError();
-  });
-  return slots[dev];
+// The passes of one call, all on the caller's stream, each allowed to start
+// early (programmatic dependent launch) on the SMs its predecessor leaves free:
+//   1. partial states of the earlier segments (first pass, when split);
+//   2. the main tensor-core pass; segments that read partial states wait for
+//      pass 1 to complete first;
+//   3. the exact pass over each head's leading tokens, which reads nothing the
+//      main pass writes and so runs beside it; its last CTA waits for pass 2,
+//      so that the stream's next work follows all three.
+cudaError_t launch_passes(const Problem &p, const TcParams &tp, long G, long nparts, float *part_S, float *part_z,
+                          const float *S0, const float *z0) {
+  cudaError_t e = cudaSuccess;
+  if (nparts > 0) e = launch_range_states(p, tp.part_len, (int)nparts, part_S, part_z, kKCausalState);
+  if (e == cudaSuccess) e = launch_kernel<false>(tp, dim3((unsigned)G, (unsigned)p.BH), p.stream, nparts > 0);
+  if (e == cudaSuccess) e = launch_causal_exact_head(p, tp.n_exact, S0, z0, true);
+  return e;
 }
 
 bool causal_tc_supported(const Problem &p) {
@@ -815,22 +820,7 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
   tp.n_exact = (int)std::min<long>(p.N, kExact);
   tp.eps = p.eps;
 
-  // The exact pass over each head's leading tokens runs on a low-priority side
-  // stream, concurrently with the tensor-core passes (which leave those rows to it).
-  SideStream &side = side_stream(-1);
-  std::lock_guard<std::mutex> lock(side.mu);
-  if (!side.ok) e = cudaErrorNotReady;
-  if (e == cudaSuccess) e = cudaEventRecord(side.fork, p.stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
-  if (nparts > 0 && e == cudaSuccess) e = launch_kernel<true>(tp, dim3((unsigned)nparts, (unsigned)p.BH), p.stream);
-  if (e == cudaSuccess) e = launch_kernel<false>(tp, dim3((unsigned)G, (unsigned)p.BH), p.stream);
-  if (e == cudaSuccess) {
-    Problem ps = p;
-    ps.stream = side.stream;
-    e = launch_causal_exact_head(ps, tp.n_exact, S0, z0);
-  }
-  if (e == cudaSuccess) e = cudaEventRecord(side.join, side.stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(p.stream, side.join, 0);
+  e = launch_passes(p, tp, G, nparts, part_S, part_z, S0, z0);
   if (scratch) {
     const cudaError_t f = cudaFreeAsync(scratch, p.stream);
     if (e == cudaSuccess) e = f;
@@ -923,12 +913,7 @@ cudaError_t launch_causal_tc_noalloc(const Problem &p, int dev, bool *too_large)
   tp.parts_per_seg = (int)r;
   tp.n_exact = (int)std::min<long>(p.N, kExact);
   tp.eps = p.eps;
-  cudaError_t e = cudaSuccess;
-  if (nparts > 0) e = launch_kernel<true>(tp, dim3((unsigned)nparts, (unsigned)p.BH), p.stream);
-  if (e == cudaSuccess) e = launch_kernel<false>(tp, dim3((unsigned)G, (unsigned)p.BH), p.stream);
-  // the exact pass over the leading tokens, after the main pass on the same stream
-  if (e == cudaSuccess) e = launch_causal_exact_head(p, tp.n_exact, nullptr, nullptr);
-  return e;
+  return launch_passes(p, tp, G, nparts, part_S, part_z, nullptr, nullptr);
 }
 
 cudaError_t read_and_clear_device_status(unsigned int *value) {

@@ -7,16 +7,18 @@
 //
 // 1. State build: a cluster of G CTAs per head, each over a contiguous range
 //    of tokens.  TMA lands K and V tiles (128-byte swizzle); eight warps
-//    apply phi to K in place (bf16) and zero the rows past the end; one
-//    thread issues S += phi(K)^T V (M = N = 128) and z += phi(K)^T 1 (N = 16
-//    against a constant ones operand) into fp32 tensor-memory accumulators.
+//    apply phi to K in place (bf16), zero the rows past the end and add the
+//    rounded values into fp32 column sums (z); one thread issues
+//    S += phi(K)^T V (M = N = 128) into an fp32 tensor-memory accumulator.
 //    For d = 64 the 128 rows of M are two 128-token sub-tiles side by side:
 //    the MMA forms [K_a | K_b]^T [V_a | V_b], whose two diagonal 64x64 blocks
 //    are the sub-tiles' contributions (the off-diagonal blocks are unused).
 //    The partial states meet through distributed shared memory and the
-//    cluster writes S and z.
-// 2. Read: persistent CTAs over 128-token tiles.  phi is applied to the Q
-//    tile in place; B = [bf16(S) | hi and lo bf16 parts of z | 0] is built
+//    cluster writes S and z.  phi costs one exp per element on the MUFU
+//    unit, about as long as the tile's load, so each thread loads all of its
+//    chunks before transforming any (the exp latencies overlap).
+// 2. Read: persistent CTAs over 128-token tiles.  Eight warps apply phi to
+//    the Q tile in place; B = [bf16(S) | hi and lo bf16 parts of z | 0] is built
 //    once per head in a K-major layout, so one MMA (M = 128, N = d + 16,
 //    K = d) gives every numerator and the denominator; eight warps
 //    normalise and stage fp32 rows that TMA stores write out.
@@ -47,40 +49,70 @@ using namespace tc;
 constexpr uint32_t kBlk = 16384;           // [128 rows x 128 bytes], 128-byte swizzled
 constexpr uint32_t kAbortMisaligned = 2u;  // status bit: shared memory base not 1024-aligned
 
+// phi in place on a tile of 16-byte chunks: thread t of `kThr` takes chunks
+// t, t + kThr, ...; all loads are issued before any exp so that their
+// latencies overlap.  Chunk c covers row c / 8 of a 128-byte-row tile.
+template <int kPer, int kThr, typename F>
+__device__ __forceinline__ void phi_chunks(uint8_t *tile, int t, F &&each) {
+  uint4 x[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) x[j] = reinterpret_cast<const uint4 *>(tile)[t + kThr * j];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) x[j] = each(j, t + kThr * j, x[j]);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) reinterpret_cast<uint4 *>(tile)[t + kThr * j] = x[j];
+}
+
+__device__ __forceinline__ void add8_bf16(float *acc, uint4 y) {
+  const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    acc[2 * e] += __uint_as_float(w[e] << 16);
+    acc[2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
+  }
+}
+
 // ------------------------------------------------------------------ state build
 
 constexpr int kBuildThreads = 320;  // warp 0 TMA, 1 MMA, 2-9 phi(K) and the epilogue
-constexpr int kBuildStages = 3;
+constexpr int kBuildStages = 6;
 constexpr int kBuildPhi = 256;
-constexpr uint32_t kBarBuild = 1;  // named barrier of warps 2-9
+constexpr uint32_t kBarBuild = 1;   // named barrier of warps 2-9
+constexpr uint32_t kHalf = 8192;    // [64 rows x 128 bytes], 128-byte swizzled
 
+// Stages are 64-token (d = 128) or 128-token (d = 64, two 64-token sub-tiles)
+// K and V tiles of 16 KB each: a stage is held only for its phi and four
+// MMAs, so most of the six stages are loads in flight.
 template <int D>
 struct BuildLayout {
-  static constexpr uint32_t kStage = 2 * kBlk;  // one K or V stage: 32 KB
+  static constexpr uint32_t kStage = 2 * kHalf;  // one K or V stage: 16 KB
   static constexpr uint32_t K = 0;
   static constexpr uint32_t V = K + kBuildStages * kStage;
-  static constexpr uint32_t Ones = V + kBuildStages * kStage;  // K-major [16 x 128] bf16, row 0 all ones
-  static constexpr uint32_t Bars = Ones + 4096;
+  static constexpr int kZ = D == 64 ? 8 : 16;  // column sums per feature-map thread
+  static constexpr uint32_t Zred = V + kBuildStages * kStage;  // [256 threads][kZ] column sums, then z partial
+  static constexpr uint32_t Bars = Zred + kBuildPhi * kZ * 4 + D * 4;
   static constexpr int kNumBars = 3 * kBuildStages + 2;
   static constexpr uint32_t Misc = Bars + kNumBars * 8;
   static constexpr uint32_t Bytes = Misc + 16;
-  // partial state [128 rows][D + 4] fp32 (column D holds z), written over the K stages
+  // partial state [128 rows][D + 4] fp32, written over the K stages
   static constexpr int kPStride = D + 4;
   static_assert(128 * kPStride * 4 <= kBuildStages * kStage, "partial state fits over the K stages");
 };
 static_assert(BuildLayout<128>::Bytes <= 232448, "shared memory budget");
 
 struct BuildParams {
-  CUtensorMap tk, tv;  // [BH][N][D] bf16, box 64 x 128 x 1, 128-byte swizzle
-  float *S, *z;
+  CUtensorMap tk, tv;  // [BH][N][D] bf16, box 64 x 64 x 1, 128-byte swizzle
+  float *S, *z;        // whole-sequence mode: final state, summed over the cluster
+  float *part_S, *part_z;  // range mode (non-null): [BH][parts][D][D], [BH][parts][D], one per CTA
   long N;
-  int units;  // token units per head: 256 tokens (d = 64) or 128 (d = 128)
+  int units;       // stage units per head: 128 tokens (d = 64) or 64 (d = 128)
+  int part_units;  // range mode: units per CTA (part p covers units [p * part_units, ...))
 };
 
 template <int D>
 __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid_constant__ BuildParams p) {
   using Lay = BuildLayout<D>;
-  constexpr int kUnit = D == 64 ? 256 : 128;
+  constexpr int kUnit = D == 64 ? 128 : 64;
   constexpr int kPS = Lay::kPStride;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // every CTA sees the same base, so either all return here or none does
@@ -96,13 +128,22 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
   unsigned int *status = &g_global_status;
   float *P = reinterpret_cast<float *>(sm + Lay::K);
+  float *zred = reinterpret_cast<float *>(sm + Lay::Zred), *zpart = zred + kBuildPhi * Lay::kZ;
 
+  const bool range_mode = p.part_S != nullptr;
   cg::cluster_group cluster = cg::this_cluster();
-  const int G = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+  const int G = range_mode ? 1 : (int)cluster.num_blocks(), rank = range_mode ? 0 : (int)cluster.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
-  const int u0 = (int)((long)p.units * rank / G), u1 = (int)((long)p.units * (rank + 1) / G);
-  const int nu = u1 - u0;
+  int u0, u1;
+  if (range_mode) {
+    u0 = blockIdx.x * p.part_units;
+    u1 = min(p.units, u0 + p.part_units);
+  } else {
+    u0 = (int)((long)p.units * rank / G);
+    u1 = (int)((long)p.units * (rank + 1) / G);
+  }
+  const int nu = max(0, u1 - u0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kBuildStages; ++s) {
@@ -115,20 +156,14 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
     *abort_word = 0;
     fence_barrier_init();
   }
-  // the ones operand: two 64-wide K atoms of 16 rows; row 0 of each is all ones
-  for (int i = threadIdx.x; i < 256; i += kBuildThreads) {
-    const uint32_t one2 = 0x3f803f80u;  // two bf16 ones
-    const bool first_row = ((i & 127) >> 3) == 0;
-    *reinterpret_cast<uint4 *>(sm + Lay::Ones + i * 16) =
-        first_row ? make_uint4(one2, one2, one2, one2) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  fence_async_smem();
-  if (warp == 1) tmem_alloc(tmem_slot, 256);
+  if (warp == 1) tmem_alloc(tmem_slot, 128);
+  // the kernel queued after this one (the read, or the main causal pass) may start on free SMs
+  if (threadIdx.x == 0) pdl_trigger();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tZ = tmem + 128;
+  const uint32_t tS = tmem;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -143,12 +178,12 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
         const int tok = (u0 + i) * kUnit;
         uint8_t *k = sm + Lay::K + s * Lay::kStage, *v = sm + Lay::V + s * Lay::kStage;
         mbar_arrive_expect_tx(&full[s], 2 * Lay::kStage);
-        // d = 64: two 128-token sub-tiles; d = 128: the two 64-feature halves of one tile
-        const int x1 = D == 64 ? 0 : 64, t1 = D == 64 ? tok + 128 : tok;
+        // d = 64: two 64-token sub-tiles; d = 128: the two 64-feature halves of one tile
+        const int x1 = D == 64 ? 0 : 64, t1 = D == 64 ? tok + 64 : tok;
         tma_load_3d(k, &p.tk, &full[s], 0, tok, bh);
-        tma_load_3d(k + kBlk, &p.tk, &full[s], x1, t1, bh);
+        tma_load_3d(k + kHalf, &p.tk, &full[s], x1, t1, bh);
         tma_load_3d(v, &p.tv, &full[s], 0, tok, bh);
-        tma_load_3d(v + kBlk, &p.tv, &full[s], x1, t1, bh);
+        tma_load_3d(v + kHalf, &p.tv, &full[s], x1, t1, bh);
         issued = i + 1;
       }
       for (int i = max(0, issued - kBuildStages); i < issued; ++i)
@@ -158,20 +193,16 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t iS = idesc_bf16_f32(128, 128, 1, 1);
-      constexpr uint32_t iZ = idesc_bf16_f32(128, 16, 1, 0);
-      const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V), sO = smem_u32(sm + Lay::Ones);
+      const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V);
       for (int i = 0; i < nu; ++i) {
         const int s = i % kBuildStages;
         if (!mbar_wait(&phi_done[s], (i / kBuildStages) & 1, abort_word, status)) break;
         tc_fence_after();
         const uint32_t k = sK + s * Lay::kStage, v = sV + s * Lay::kStage;
 #pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t a = sw128_desc(k + ks * 2048, kBlk, 1024);  // MN-major: 16 tokens per step
-          const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
-          mma_bf16(tS, a, sw128_desc(v + ks * 2048, kBlk, 1024), iS, acc);
-          mma_bf16(tZ, a, sw128_desc(sO + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024), iZ, acc);
-        }
+        for (int ks = 0; ks < 4; ++ks)  // both operands MN-major: 16 tokens per step, 64-wide blocks 8 KB apart
+          mma_bf16(tS, sw128_desc(k + ks * 2048, kHalf, 1024), sw128_desc(v + ks * 2048, kHalf, 1024), iS,
+                   (i > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&empty[s]);
       }
       mma_commit(acc_full);
@@ -179,8 +210,15 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
       wait_drain(drain, 0, status);
     }
   } else {
-    // ---------------- phi(K) in place, then the partial state ----------------
+    // ---------------- phi(K) in place, column sums, then the partial state ----------------
     const int pt = threadIdx.x - 64;
+    // Chunk pt + 256 j sits at position pt & 7 of row (pt >> 3) + 32 j; with the
+    // 128-byte swizzle it holds the features 8 g .. 8 g + 7, g = (pt & 7) ^ ((pt >> 3) & 7),
+    // of its row (of the 64-feature block j / 2 for d = 128), the same g for every j.
+    constexpr int kZ = Lay::kZ;
+    float zacc[kZ];
+#pragma unroll
+    for (int a = 0; a < kZ; ++a) zacc[a] = 0.f;
     bool failed = false;
     for (int i = 0; i < nu; ++i) {
       const int s = i % kBuildStages;
@@ -191,16 +229,27 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
       }
       uint8_t *k = sm + Lay::K + s * Lay::kStage;
       const long tok0 = (long)(u0 + i) * kUnit;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int ch = pt + kBuildPhi * j;  // 16-byte chunk; 8 per 128-byte row
-        const int row = ch >> 3;            // 0..255 over the two blocks
-        const long tok = tok0 + (D == 64 ? row : (row & 127));
-        uint4 *c = reinterpret_cast<uint4 *>(k + ch * 16);
-        *c = tok < p.N ? phi8(*c) : make_uint4(0u, 0u, 0u, 0u);  // rows past the end add nothing
-      }
+      phi_chunks<4, kBuildPhi>(k, pt, [&](int j, int ch, uint4 x) {
+        const int row = ch >> 3;  // 0..127 over the two blocks
+        const long tok = tok0 + (D == 64 ? row : (row & 63));
+        const uint4 y = tok < p.N ? phi8(x) : make_uint4(0u, 0u, 0u, 0u);  // rows past the end add nothing
+        add8_bf16(zacc + (D == 64 ? 0 : 8 * (j >> 1)), y);
+        return y;
+      });
       fence_async_smem();
       mbar_arrive(&phi_done[s]);
+    }
+    // column sums: feature f = 64 b + 8 g + e is held, as entry 8 b + e (d = 128) or e,
+    // by the 32 threads 8 m + (g ^ (m & 7)), m = 0..31
+#pragma unroll
+    for (int a = 0; a < kZ; ++a) zred[pt * kZ + a] = zacc[a];
+    named_bar(kBarBuild, kBuildPhi);
+    if (pt < D) {
+      const int b = pt >> 6, g = (pt >> 3) & 7, e = pt & 7;
+      float zs = 0.f;
+#pragma unroll 8
+      for (int m = 0; m < 32; ++m) zs += zred[(8 * m + (g ^ (m & 7))) * kZ + (D == 64 ? e : 8 * b + e)];
+      zpart[pt] = failed ? 0.f : zs;
     }
     bool ok = !failed && mbar_wait(acc_full, 0, abort_word, status);
     ok = !bar_or(kBarBuild, kBuildPhi, !ok);
@@ -223,25 +272,40 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
               make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
                           __uint_as_float(v[4 * q + 3]));
       }
-      const float zv = __uint_as_float(tmem_ld1(tZ + lanes));
-      if (half == 0) prow[D] = zv;
     } else {
       const int w = D == 64 ? 32 : 64;
       for (int c = 0; c < w; ++c) prow[w * half + c] = 0.f;
-      if (half == 0) prow[D] = 0.f;
     }
   }
 
   __syncwarp();
   tc_fence_before();
-  cluster.sync();  // every partial state of the cluster is in shared memory
-  {
+  if (range_mode) {
+    // this CTA's partial state for its token range
+    __syncthreads();
+    const long part = (long)bh * gridDim.x + blockIdx.x;
+    for (int e = threadIdx.x; e < D * (D + 1); e += kBuildThreads) {
+      const int i = e / (D + 1), j = e % (D + 1);
+      if (j == D) {
+        p.part_z[part * D + i] = zpart[i];
+      } else {
+        float acc = P[i * kPS + j];
+        if (D == 64) acc += P[(64 + i) * kPS + j];
+        p.part_S[(part * D + i) * D + j] = acc;
+      }
+    }
+  } else {
+    cluster.sync();  // every partial state of the cluster is in shared memory
     // this CTA sums rows [r0, r0 + D/G) of S (and those entries of z) over the cluster
     const int rows = D / G, r0 = rank * rows;
     for (int e = threadIdx.x; e < rows * (D + 1); e += kBuildThreads) {
       const int i = r0 + e / (D + 1), j = e % (D + 1);
       float acc = 0.f;
       for (int c = 0; c < G; ++c) {
+        if (j == D) {
+          acc += cluster.map_shared_rank(zpart, c)[i];
+          continue;
+        }
         const float *Pc = cluster.map_shared_rank(P, c);
         acc += Pc[i * kPS + j];
         if (D == 64) acc += Pc[(64 + i) * kPS + j];
@@ -251,23 +315,23 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
       else
         p.z[(long)bh * D + i] = acc;
     }
+    cluster.sync();  // remote reads are done before any CTA of the cluster exits
   }
-  cluster.sync();  // remote reads are done before any CTA of the cluster exits
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 128);
   }
 }
 
 // ------------------------------------------------------------------ read
 
-constexpr int kReadThreads = 448;  // warp 0 TMA, 1 MMA, 2-5 phi(Q) and B, 6-13 epilogue
-constexpr int kReadPhi = 128, kReadEpi = 256;
+constexpr int kReadThreads = 576;  // warp 0 TMA, 1 MMA, 2-9 phi(Q) and B, 10-17 epilogue
+constexpr int kReadPhi = 256, kReadEpi = 256;
 constexpr uint32_t kBarEpi = 1, kBarPhi = 2;
 
 template <int D>
 struct ReadLayout {
-  static constexpr int kStages = D == 64 ? 3 : 2;  // Q tiles in flight
+  static constexpr int kStages = D == 64 ? 6 : 2;  // Q tiles in flight
   static constexpr int NB = D + 16;             // B rows: d columns of S, z hi, z lo, zero padding
   static constexpr uint32_t kQ = D * 2 * 128;   // one Q tile (D/64 swizzled 16 KB blocks)
   static constexpr uint32_t kAtomB = NB * 128;  // one 64-wide K atom of B
@@ -292,15 +356,32 @@ struct ReadParams {
   CUtensorMap to;  // [BH][N][D] fp32, box 32 x 128 x 1, 128-byte swizzle
   const float *S, *z;
   long N;
-  long tiles_per_head, total_tiles;
+  int tiles_per_head;
+  long total_tiles;
   float eps;
+};
+
+// Walks a CTA's contiguous run of 128-token tiles as (head, tile in head)
+// pairs: one division at the start, none per tile (64-bit division is a long
+// software sequence and sat on every role's per-tile path).
+struct TileWalk {
+  int bh, t, tph;
+  __device__ TileWalk(long first, int tiles_per_head)
+      : bh((int)(first / tiles_per_head)), t((int)(first % tiles_per_head)), tph(tiles_per_head) {}
+  __device__ void next() {
+    if (++t == tph) {
+      t = 0;
+      ++bh;
+    }
+  }
+  __device__ bool last_of_head() const { return t == tph - 1; }
 };
 
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
 // B for one head, K-major and 128-byte swizzled: row n < D holds column n of
 // S over the D key features (bf16), rows D and D+1 the hi and lo bf16 parts
-// of z, the rest zeros.  128 threads; consecutive threads take consecutive
+// of z, the rest zeros.  256 threads; consecutive threads take consecutive
 // rows, so the reads of S are coalesced and the swizzled stores conflict-free.
 template <int D>
 __device__ __forceinline__ void build_b(uint8_t *B, const float *__restrict__ S, const float *__restrict__ z,
@@ -380,13 +461,14 @@ __global__ void __launch_bounds__(kReadThreads, 1) global_read_tc(const __grid_c
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       prefetch_tmap(&p.tq);
+      TileWalk w(t_lo, p.tiles_per_head);
       int issued = 0;
       for (int i = 0; i < n; ++i) {
         const int s = i % kStages;
         const uint32_t r = i / kStages;
         if (i >= kStages && !mbar_wait(&q_empty[s], (r - 1) & 1, abort_word, status)) break;
-        const long tile = t_lo + i;
-        const int bh = (int)(tile / p.tiles_per_head), tok = (int)(tile % p.tiles_per_head) * 128;
+        const int bh = w.bh, tok = w.t * 128;
+        w.next();
         uint8_t *q = sm + Lay::Q + s * Lay::kQ;
         mbar_arrive_expect_tx(&full[s], Lay::kQ);
 #pragma unroll
@@ -402,10 +484,10 @@ __global__ void __launch_bounds__(kReadThreads, 1) global_read_tc(const __grid_c
       constexpr uint32_t iR = idesc_bf16_f32(128, NB, 0, 0);
       const uint32_t sQ = smem_u32(sm + Lay::Q), sB = smem_u32(sm + Lay::B);
       int hl = 0;  // local head index: B buffer hl & 1
-      for (int i = 0; i < n; ++i) {
+      TileWalk w(t_lo, p.tiles_per_head);
+      for (int i = 0; i < n; ++i, w.next()) {
         const int s = i % kStages, buf = i & 1;
-        const long tile = t_lo + i;
-        if (i > 0 && tile / p.tiles_per_head != (tile - 1) / p.tiles_per_head) ++hl;
+        if (i > 0 && w.t == 0) ++hl;
         if (!mbar_wait(&phi_done[s], (i / kStages) & 1, abort_word, status)) break;
         if (i >= 2 && !mbar_wait(&acc_empty[buf], ((i >> 1) - 1) & 1, abort_word, status)) break;
         tc_fence_after();
@@ -417,47 +499,43 @@ __global__ void __launch_bounds__(kReadThreads, 1) global_read_tc(const __grid_c
         mma_commit(&q_empty[s]);
         mma_commit(&acc_full[buf]);
         // the last tile of a head frees its B buffer once these MMAs complete
-        if (i == n - 1 || (tile + 1) / p.tiles_per_head != tile / p.tiles_per_head) mma_commit(&b_free[hl & 1]);
+        if (i == n - 1 || w.last_of_head()) mma_commit(&b_free[hl & 1]);
       }
       mma_commit(drain);
       wait_drain(drain, 0, status);
     }
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ---------------- phi(Q) in place, and B per head ----------------
     const int pt = threadIdx.x - 64;
     int hl = -1;
-    long prev_bh = -1;
-    for (int i = 0; i < n; ++i) {
+    TileWalk w(t_lo, p.tiles_per_head);
+    for (int i = 0; i < n; ++i, w.next()) {
       const int s = i % kStages;
-      const long tile = t_lo + i, bh = tile / p.tiles_per_head;
-      if (bh != prev_bh) {
+      const long bh = w.bh;
+      if (i == 0 || w.t == 0) {
         ++hl;
         // B buffer hl & 1 last served head hl - 2
         const bool ok = hl < 2 || mbar_wait(&b_free[hl & 1], ((hl >> 1) - 1) & 1, abort_word, status);
         if (bar_or(kBarPhi, kReadPhi, !ok)) break;
+        if (hl == 0) pdl_wait();  // S and z come from the state build: complete and visible
         build_b<D>(sm + Lay::B + (hl & 1) * Lay::kB, p.S + bh * D * D, p.z + bh * D, pt);
-        prev_bh = bh;
       }
       const bool ok = mbar_wait(&full[s], (i / kStages) & 1, abort_word, status);
       if (bar_or(kBarPhi, kReadPhi, !ok)) break;
-      uint8_t *q = sm + Lay::Q + s * Lay::kQ;
-#pragma unroll
-      for (int j = 0; j < (int)(Lay::kQ / 16) / kReadPhi; ++j) {
-        uint4 *c = reinterpret_cast<uint4 *>(q + (pt + kReadPhi * j) * 16);
-        *c = phi8(*c);
-      }
+      phi_chunks<(int)(Lay::kQ / 16) / kReadPhi, kReadPhi>(sm + Lay::Q + s * Lay::kQ, pt,
+                                                          [](int, int, uint4 x) { return phi8(x); });
       fence_async_smem();
       mbar_arrive(&phi_done[s]);
     }
   } else {
     // ---------------- epilogue: normalise, stage, TMA store ----------------
-    const int et = threadIdx.x - 192;  // 0..255
-    const int quarter = warp & 3, half = (warp - 6) >> 2, row = quarter * 32 + lane;
+    const int et = threadIdx.x - 320;  // 0..255
+    const int quarter = warp & 3, half = (warp - 10) >> 2, row = quarter * 32 + lane;
     const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-    for (int i = 0; i < n; ++i) {
+    TileWalk w(t_lo, p.tiles_per_head);
+    for (int i = 0; i < n; ++i, w.next()) {
       const int buf = i & 1, ob = i % Lay::kOutBufs;
-      const long tile = t_lo + i;
-      const int bh = (int)(tile / p.tiles_per_head), tok = (int)(tile % p.tiles_per_head) * 128;
+      const int bh = w.bh, tok = w.t * 128;
       const bool ok = mbar_wait(&acc_full[buf], (i >> 1) & 1, abort_word, status);
       if (bar_or(kBarEpi, kReadEpi, !ok)) break;
       tc_fence_after();
@@ -511,12 +589,12 @@ __global__ void __launch_bounds__(kReadThreads, 1) global_read_tc(const __grid_c
 // ------------------------------------------------------------------ host
 
 bool make_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t elem, const void *base, long BH, long N, int D,
-              uint32_t box_x) {
+              uint32_t box_x, uint32_t box_rows) {
   auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)D * elem, (cuuint64_t)N * D * elem};
-  cuuint32_t box[3] = {box_x, 128, 1};
+  cuuint32_t box[3] = {box_x, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -532,29 +610,38 @@ cudaError_t set_smem_once(F *kernel, uint32_t bytes, std::once_flag &once, cudaE
 }
 
 template <int D>
+cudaError_t build_smem() {
+  static std::once_flag once;
+  static cudaError_t err;
+  return set_smem_once(global_build_tc<D>, BuildLayout<D>::Bytes, once, err);
+}
+
+template <int D>
 cudaError_t launch_t(const Problem &p) {
   const DeviceInfo &di = device_info(-1);
   const long sms = std::max(1, di.sm_count);
   BuildParams bp;
   ReadParams rp;
-  if (!make_map(&bp.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k, p.BH, p.N, D, 64) ||
-      !make_map(&bp.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v, p.BH, p.N, D, 64) ||
-      !make_map(&rp.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q, p.BH, p.N, D, 64) ||
-      !make_map(&rp.to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.out, p.BH, p.N, D, 32))
+  if (!make_map(&bp.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k, p.BH, p.N, D, 64, 64) ||
+      !make_map(&bp.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v, p.BH, p.N, D, 64, 64) ||
+      !make_map(&rp.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q, p.BH, p.N, D, 64, 128) ||
+      !make_map(&rp.to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.out, p.BH, p.N, D, 32, 128))
     return cudaErrorInvalidValue;
-  constexpr int kUnit = D == 64 ? 256 : 128;
+  constexpr int kUnit = D == 64 ? 128 : 64;
   bp.S = p.S;
   bp.z = p.z;
+  bp.part_S = bp.part_z = nullptr;
   bp.N = p.N;
   bp.units = (int)((p.N + kUnit - 1) / kUnit);
-  // cluster size: a power of two <= 8 so that the build covers the SMs about once, >= 4 units a CTA
+  bp.part_units = 0;
+  // cluster size: a power of two <= 8 so that the build covers the SMs about once, >= 8 units a CTA
   int G = 1;
-  while (G < 8 && p.BH * (2 * G) <= sms && bp.units / (2 * G) >= 4) G *= 2;
+  while (G < 8 && p.BH * (2 * G) <= sms && bp.units / (2 * G) >= 8) G *= 2;
 
-  static std::once_flag once_b, once_r;
-  static cudaError_t err_b, err_r;
-  cudaError_t e = set_smem_once(global_build_tc<D>, BuildLayout<D>::Bytes, once_b, err_b);
+  cudaError_t e = build_smem<D>();
   if (e != cudaSuccess) return e;
+  static std::once_flag once_r;
+  static cudaError_t err_r;
   e = set_smem_once(global_read_tc<D>, ReadLayout<D>::Bytes, once_r, err_r);
   if (e != cudaSuccess) return e;
 
@@ -582,14 +669,26 @@ cudaError_t launch_t(const Problem &p) {
   rp.S = p.S;
   rp.z = p.z;
   rp.N = p.N;
-  rp.tiles_per_head = (p.N + 127) / 128;
-  rp.total_tiles = rp.tiles_per_head * p.BH;
+  rp.tiles_per_head = (int)((p.N + 127) / 128);
+  rp.total_tiles = (long)rp.tiles_per_head * p.BH;
   rp.eps = p.eps;
   const unsigned grid = (unsigned)std::min<long>(rp.total_tiles, sms);
   {
+    // starts early beside the build (programmatic dependent launch): Q loads and
+    // phi(Q) overlap the build's tail; S and z are read only after it completes
     LaunchTimer timer(kKGlobalRead, p.stream);
-    global_read_tc<D><<<grid, kReadThreads, ReadLayout<D>::Bytes, p.stream>>>(rp);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t rc = {};
+    cudaLaunchAttribute ra[1];
+    ra[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    ra[0].val.programmaticStreamSerializationAllowed = 1;
+    rc.gridDim = dim3(grid);
+    rc.blockDim = dim3(kReadThreads);
+    rc.dynamicSmemBytes = ReadLayout<D>::Bytes;
+    rc.stream = p.stream;
+    rc.attrs = ra;
+    rc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&rc, global_read_tc<D>, rp);
+    if (e == cudaSuccess) e = cudaGetLastError();
     timer.done(e);
   }
   if (e == cudaSuccess) count_launch();
@@ -605,6 +704,29 @@ bool global_tc_supported(const Problem &p) {
 }
 
 cudaError_t launch_global_tc(const Problem &p) { return p.dk == 64 ? launch_t<64>(p) : launch_t<128>(p); }
+
+cudaError_t launch_range_states(const Problem &p, long part_tokens, int nparts, float *part_S, float *part_z,
+                                int kernel_id) {
+  if (p.dt != LA_BF16 || p.dk != 128 || p.dv != 128 || part_tokens % 64 != 0 || nparts < 1) return cudaErrorInvalidValue;
+  BuildParams bp;
+  if (!make_map(&bp.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k, p.BH, p.N, 128, 64, 64) ||
+      !make_map(&bp.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v, p.BH, p.N, 128, 64, 64))
+    return cudaErrorInvalidValue;
+  bp.S = bp.z = nullptr;
+  bp.part_S = part_S;
+  bp.part_z = part_z;
+  bp.N = p.N;
+  bp.units = (int)((p.N + 63) / 64);
+  bp.part_units = (int)(part_tokens / 64);
+  cudaError_t e = build_smem<128>();
+  if (e != cudaSuccess) return e;
+  LaunchTimer timer(kernel_id, p.stream);
+  global_build_tc<128><<<dim3((unsigned)nparts, (unsigned)p.BH), kBuildThreads, BuildLayout<128>::Bytes, p.stream>>>(bp);
+  e = cudaGetLastError();
+  timer.done(e);
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
 
 cudaError_t read_and_clear_global_tc_status(unsigned int *value) {
   const unsigned int zero = 0;

@@ -27,8 +27,11 @@ struct Problem {
 cudaError_t launch_causal_simt(const Problem &p, long n_proc, bool from_state, bool write_state);
 
 // Exact fp32 pass over tokens [0, n_exact) of every head (outputs only),
-// starting from (S0, z0) when given (device pointers), else from zero.
-cudaError_t launch_causal_exact_head(const Problem &p, long n_exact, const float *S0, const float *z0);
+// starting from (S0, z0) when given (device pointers), else from zero.  With
+// pdl it may start while the previous kernel of the stream runs (it must not
+// read that kernel's results); its last CTA waits for that kernel, so the
+// stream's later work still follows both.
+cudaError_t launch_causal_exact_head(const Problem &p, long n_exact, const float *S0, const float *z0, bool pdl);
 
 // Tensor-core chunked causal path (bf16, d_k = d_v = 128, sm_103).
 bool causal_tc_supported(const Problem &p);
@@ -48,6 +51,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 bool global_tc_supported(const Problem &p);
 cudaError_t launch_global_tc(const Problem &p);
 cudaError_t read_and_clear_global_tc_status(unsigned int *value);
+
+// Partial states of token ranges on the tensor cores (bf16, d_k = d_v = 128):
+// CTA (r, h) sums phi(k) v^T and phi(k) over tokens [r * part_tokens,
+// (r + 1) * part_tokens) of head h into part_S[h][r] ([128][128]) and
+// part_z[h][r] ([128]), starting from zero.  part_tokens % 64 == 0.
+cudaError_t launch_range_states(const Problem &p, long part_tokens, int nparts, float *part_S, float *part_z,
+                                int kernel_id);
 
 // Read and clear the device status word (bounded-wait timeouts).
 cudaError_t read_and_clear_device_status(unsigned int *value);

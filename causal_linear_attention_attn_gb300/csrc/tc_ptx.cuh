@@ -276,6 +276,14 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
 // ---------------------------------------------------------------------------
 // Small helpers shared by the tensor-core kernels.
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  pdl_trigger lets the next kernel of the
+// stream (launched with programmatic stream serialization) start once every
+// CTA of this one has triggered or exited; pdl_wait blocks until the kernel
+// this one depends on has completed and its memory writes are visible.  A
+// kernel launched without the attribute passes both at once.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // OR of a per-thread flag over a named barrier's threads (also a barrier).
 __device__ __forceinline__ bool bar_or(uint32_t id, uint32_t threads, bool flag) {
   uint32_t r;
