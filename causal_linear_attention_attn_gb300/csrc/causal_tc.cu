@@ -18,9 +18,9 @@
 // weights, z never passes through bf16, and the state stays fp32.
 //
 // One CTA owns a contiguous segment of one head's tokens.  Long sequences are
-// split into segments; a first pass (the same kernel in state-only mode)
-// reduces K^T V over parts of the earlier segments, and each segment starts
-// from the sum of the parts before it.
+// split into segments; a first pass (the range-state kernel of the global
+// form) reduces K^T V and the key sums over parts of the earlier segments, and
+// each segment starts from the sum of the parts before it.
 //
 // Warp roles (18 warps): 0 TMA producer; 1 MMA issuer and TMEM owner;
 // 2-5 phi(Q) into tensor memory and the cross-chunk denominator phi(Q).z;
@@ -78,16 +78,15 @@ constexpr int kPhiThreads = 256;  // feature-map warps 2-9
 constexpr uint32_t kBarPhi = 1, kBarEpi = 2;  // named barrier ids
 constexpr int kExact = 64;  // leading tokens of each head computed by the exact fp32 pass
 
-template <bool kStateOnly>
 struct Layout {
-  static constexpr int kStages = kStateOnly ? 3 : 2;
+  static constexpr int kStages = 2;
   static constexpr uint32_t Q = 0;
-  static constexpr uint32_t K = kStateOnly ? 0 : kStages * kTile;
+  static constexpr uint32_t K = kStages * kTile;
   static constexpr uint32_t V = K + kStages * kTile;
-  static constexpr uint32_t Sb = V + kStages * kTile;  // bf16 copy of the carried state (main mode)
-  static constexpr uint32_t DenX = kStateOnly ? Sb : Sb + kTile;       // phi(q).z per row, per stage
-  static constexpr uint32_t Den = DenX + (kStateOnly ? 0 : kStages * kC * 4);  // final denominators, 2 chunks
-  static constexpr uint32_t Z = Den + (kStateOnly ? 0 : 2 * kC * 4);
+  static constexpr uint32_t Sb = V + kStages * kTile;  // bf16 copy of the carried state
+  static constexpr uint32_t DenX = Sb + kTile;          // phi(q).z per row, per stage
+  static constexpr uint32_t Den = DenX + kStages * kC * 4;  // final denominators, 2 chunks
+  static constexpr uint32_t Z = Den + 2 * kC * 4;
   static constexpr uint32_t Bars = Z + kD * 4;
   static constexpr int kNumBars = 34;
   static constexpr uint32_t Misc = Bars + kNumBars * 8;
@@ -95,10 +94,9 @@ struct Layout {
   // The dynamic shared memory base follows the 1 KB reserved per block and is
   // 1024-aligned; the kernel checks this and refuses to run otherwise.
   static constexpr uint32_t Alloc = Bytes;
-  static constexpr uint32_t TmemCols = kStateOnly ? 128 : 512;
+  static constexpr uint32_t TmemCols = 512;
 };
-static_assert(Layout<false>::Alloc <= 232448, "shared memory budget");
-static_assert(Layout<true>::Alloc <= 232448, "shared memory budget");
+static_assert(Layout::Alloc <= 232448, "shared memory budget");
 
 // TMEM columns (main mode): S accumulator, P (fp32, then split bf16 hi/lo in
 // place), the output accumulator, and two buffers of phi(Q) packed as bf16
@@ -112,7 +110,7 @@ struct TcParams {
   CUtensorMap to_tail;     // the same tensor, box 32 x 64 x 1: rows 64..127 of a head's first chunk
   float *out, *S_out, *z_out;
   const float *S0, *z0;      // initial state (nullable = zero)
-  float *part_S, *part_z;    // state-only outputs / main-mode prefix inputs: [BH][nparts][128][128], [..][128]
+  float *part_S, *part_z;    // first-pass partial states: [BH][nparts][128][128], [BH][nparts][128]
   long N;
   int seg_len, nseg, part_len, nparts, parts_per_seg;
   int n_exact;
@@ -188,9 +186,8 @@ __device__ __forceinline__ int column_pair_sums_8w(const uint8_t *tile, int w, i
   return c;
 }
 
-template <bool kStateOnly>
 __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParams p) {
-  using Lay = Layout<kStateOnly>;
+  using Lay = Layout;
   constexpr int kStages = Lay::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
@@ -214,20 +211,10 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
-  long t_begin, t_end;
-  int init_parts;
-  bool last_seg;
-  if (kStateOnly) {
-    t_begin = (long)blockIdx.x * p.part_len;
-    t_end = min(p.N, t_begin + p.part_len);
-    init_parts = 0;
-    last_seg = false;
-  } else {
-    t_begin = (long)blockIdx.x * p.seg_len;
-    t_end = min(p.N, t_begin + p.seg_len);
-    init_parts = blockIdx.x * p.parts_per_seg;
-    last_seg = (int)blockIdx.x == p.nseg - 1;
-  }
+  const long t_begin = (long)blockIdx.x * p.seg_len;
+  const long t_end = min(p.N, t_begin + p.seg_len);
+  const int init_parts = blockIdx.x * p.parts_per_seg;  // first-pass parts before this segment
+  const bool last_seg = (int)blockIdx.x == p.nseg - 1;
   const int nchunks = (int)((t_end - t_begin + kC - 1) / kC);
 
   if (threadIdx.x == 0) {
@@ -237,8 +224,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       mbar_init(&full_v[s], 1);
       mbar_init(&phi_done[s], kPhiThreads);
       mbar_init(&q_empty[s], kPhiThreads);
-      // main mode: the MMA commit plus the epilogue's 128 threads once they have read den_x[s]
-      mbar_init(&k_empty[s], kStateOnly ? 1 : 129);
+      // the MMA commit plus the epilogue's 128 threads once they have read den_x[s]
+      mbar_init(&k_empty[s], 129);
       mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
@@ -266,7 +253,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
   if (warp == kWarpTma) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      if (!kStateOnly) prefetch_tmap(&p.tq);
+      prefetch_tmap(&p.tq);
       prefetch_tmap(&p.tk);
       prefetch_tmap(&p.tv);
       int issued_q = 0, issued_k = 0, issued_v = 0;
@@ -274,12 +261,10 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         const int s = c % kStages;
         const uint32_t u = c / kStages;
         const int tok = (int)(t_begin + (long)c * kC);
-        if (!kStateOnly) {
-          if (c >= kStages && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_word, status)) break;
-          mbar_arrive_expect_tx(&full_q[s], kTile);
-          tma_load_3d(sm + Lay::Q + s * kTile, &p.tq, &full_q[s], 0, tok, bh);
-          tma_load_3d(sm + Lay::Q + s * kTile + kBlk, &p.tq, &full_q[s], 64, tok, bh);
-        }
+        if (c >= kStages && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_word, status)) break;
+        mbar_arrive_expect_tx(&full_q[s], kTile);
+        tma_load_3d(sm + Lay::Q + s * kTile, &p.tq, &full_q[s], 0, tok, bh);
+        tma_load_3d(sm + Lay::Q + s * kTile + kBlk, &p.tq, &full_q[s], 64, tok, bh);
         issued_q = c + 1;
         if (c >= kStages && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_word, status)) break;
         mbar_arrive_expect_tx(&full_k[s], kTile);
@@ -293,9 +278,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         issued_v = c + 1;
       }
       // every issued copy must land before shared memory is released
-      if (!kStateOnly)
-        for (int c = max(0, issued_q - kStages); c < issued_q; ++c)
-          wait_drain(&full_q[c % kStages], (c / kStages) & 1, status);
+      for (int c = max(0, issued_q - kStages); c < issued_q; ++c)
+        wait_drain(&full_q[c % kStages], (c / kStages) & 1, status);
       for (int c = max(0, issued_k - kStages); c < issued_k; ++c)
         wait_drain(&full_k[c % kStages], (c / kStages) & 1, status);
       for (int c = max(0, issued_v - kStages); c < issued_v; ++c)
@@ -315,14 +299,6 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         if (!mbar_wait(&phi_done[s], u & 1, abort_word, status)) break;
         if (!mbar_wait(&full_v[s], u & 1, abort_word, status)) break;
         const uint32_t k = sK + s * kTile, v = sV + s * kTile;
-        if (kStateOnly) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tS, mndesc(k, ks), mndesc(v, ks), iMM, c > 0 || ks > 0);
-          mma_commit(&k_empty[s]);
-          mma_commit(&v_empty[s]);
-          continue;
-        }
         const uint32_t tQ = tmem + kColQ + 64 * (c & 1);
         // the single P tile is free once the previous chunk's P V has completed
         if (c > 0 && !mbar_wait(o_full, (c - 1) & 1, abort_word, status)) break;
@@ -355,7 +331,6 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         }
         mma_commit(o_full);
       }
-      if (kStateOnly) mma_commit(s_full);
       mma_commit(drain);
       wait_drain(drain, 0, status);
     }
@@ -370,10 +345,10 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     if (init_parts > 0) pdl_wait();  // the first pass's partial states are complete and visible
     if (pt < kD) {
       // partial states of the first pass start from zero; a segment starts from the caller's state plus them
-      float z = (!kStateOnly && p.z0) ? p.z0[(long)bh * kD + pt] : 0.f;
+      float z = p.z0 ? p.z0[(long)bh * kD + pt] : 0.f;
       for (int qp = 0; qp < init_parts; ++qp) z += p.part_z[((long)bh * p.nparts + qp) * kD + pt];
       zs[pt] = z;
-      if (!kStateOnly) den_x[pt] = den_x[kC + pt] = 0.f;
+      den_x[pt] = den_x[kC + pt] = 0.f;
     }
     named_bar(kBarPhi, kPhiThreads);
     for (int c = 0; c < nchunks; ++c) {
@@ -382,13 +357,11 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       const int tv = (int)min((long)kC, t_end - (t_begin + (long)c * kC));
       uint8_t *Kt = sm + Lay::K + s * kTile;
       bool ok = mbar_wait(&full_k[s], u & 1, abort_word, status);
-      if (!kStateOnly) {
-        ok = ok && mbar_wait(&full_q[s], u & 1, abort_word, status);
-        // this chunk's phi(Q) buffer is free once Q K^T and Q S of the chunk two back have completed
-        if (ok && c >= 2) ok = mbar_wait(&qt_free[c & 1], ((c >> 1) - 1) & 1, abort_word, status);
-      }
+      ok = ok && mbar_wait(&full_q[s], u & 1, abort_word, status);
+      // this chunk's phi(Q) buffer is free once Q K^T and Q S of the chunk two back have completed
+      if (ok && c >= 2) ok = mbar_wait(&qt_free[c & 1], ((c >> 1) - 1) & 1, abort_word, status);
       if (bar_or(kBarPhi, kPhiThreads, !ok)) break;
-      if (!kStateOnly) {
+      {
         // phi(Q) half row -> packed bf16 pairs -> tensor memory; the partial phi(q).z_prev
         // from the same rounded values meets its other half in shared memory
         const uint8_t *Qb = sm + Lay::Q + s * kTile + half * kBlk;
@@ -438,8 +411,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       named_bar(kBarPhi, kPhiThreads);  // z complete before the next chunk reads it
     }
     if (!*abort_word && pt < kD) {
-      if (kStateOnly) p.part_z[((long)bh * p.nparts + blockIdx.x) * kD + pt] = zs[pt];
-      else if (last_seg) p.z_out[(long)bh * kD + pt] = zs[pt];
+      if (last_seg) p.z_out[(long)bh * kD + pt] = zs[pt];
     }
   } else if (warp < kWarpOut) {
     // ---------------- P split, denominator and state copy (warps 10-13) ----------------
@@ -448,7 +420,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     uint32_t r[32];
     bool ok = true;
-    if (!kStateOnly) {
+    {
       uint8_t *Sb = sm + Lay::Sb;
       if (init_parts > 0) pdl_wait();  // the first pass's partial states are complete and visible
       // initial state: caller's state plus the parts before this segment
@@ -551,15 +523,10 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         tc_fence_before();
         mbar_arrive(sb_ready);
       }
-    } else {
-      const bool w = mbar_wait(s_full, 0, abort_word, status);
-      ok = !bar_or(kBarEpi, 128, !w);
-      tc_fence_after();
     }
     // final (or partial) state, fp32
-    if (ok && !*abort_word && (kStateOnly || last_seg)) {
-      float *dst = kStateOnly ? p.part_S + (((long)bh * p.nparts + blockIdx.x) * kD + T) * kD
-                              : p.S_out + ((long)bh * kD + T) * kD;
+    if (ok && !*abort_word && last_seg) {
+      float *dst = p.S_out + ((long)bh * kD + T) * kD;
       for (int cb = 0; cb < 4; ++cb) {
         tmem_ld32(tl + kColS + cb * 32, r);
         float4 *d4 = reinterpret_cast<float4 *>(dst + cb * 32);
@@ -569,7 +536,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
                               __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
       }
     }
-  } else if (!kStateOnly) {
+  } else {
     // ---------------- normalised outputs (warps 14-17) ----------------
     const int quarter = warp & 3;
     const int T = quarter * 32 + lane;  // TMEM lane = chunk row
@@ -684,17 +651,15 @@ bool make_out_map(CUtensorMap *m, void *base, long BH, long N, uint32_t rows) {
          CUDA_SUCCESS;
 }
 
-template <bool kStateOnly>
 cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bool pdl) {
-  static std::once_flag once[2];
-  static cudaError_t attr_err[2];
-  std::call_once(once[kStateOnly], [] {
-    attr_err[kStateOnly] = cudaFuncSetAttribute(causal_tc_kernel<kStateOnly>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)Layout<kStateOnly>::Alloc);
+  static std::once_flag once;
+  static cudaError_t attr_err;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(causal_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)Layout::Alloc);
   });
-  if (attr_err[kStateOnly] != cudaSuccess) return attr_err[kStateOnly];
-  LaunchTimer timer(kStateOnly ? kKCausalState : kKCausalMain, stream);
+  if (attr_err != cudaSuccess) return attr_err;
+  LaunchTimer timer(kKCausalMain, stream);
   // pdl: may start while the previous kernel of the stream (the first pass) still runs
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -702,11 +667,11 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Layout<kStateOnly>::Alloc;
+  cfg.dynamicSmemBytes = Layout::Alloc;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, causal_tc_kernel<kStateOnly>, tp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, causal_tc_kernel, tp);
   if (e == cudaSuccess) e = cudaGetLastError();
   timer.done(e);
   if (e == cudaSuccess) {
@@ -714,14 +679,13 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bo
   } else if (getenv("LA_DEBUG")) {
     cudaFuncAttributes fa;
     int blocks = -1;
-    cudaFuncGetAttributes(&fa, causal_tc_kernel<kStateOnly>);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, causal_tc_kernel<kStateOnly>, kThreads,
-                                                  Layout<kStateOnly>::Alloc);
+    cudaFuncGetAttributes(&fa, causal_tc_kernel);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, causal_tc_kernel, kThreads, Layout::Alloc);
     fprintf(stderr,
-            "linattn: causal_tc_kernel<%d> launch failed (%s): regs %d, max threads %d, static smem %zu, "
+            "linattn: causal_tc_kernel launch failed (%s): regs %d, max threads %d, static smem %zu, "
             "max dynamic smem %d, requested dynamic %u, threads %d, occupancy %d\n",
-            (int)kStateOnly, cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes,
-            fa.maxDynamicSharedSizeBytes, Layout<kStateOnly>::Alloc, kThreads, blocks);
+            cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes,
+            fa.maxDynamicSharedSizeBytes, Layout::Alloc, kThreads, blocks);
     cudaGetLastError();
   }
   return e;
@@ -741,7 +705,7 @@ cudaError_t launch_passes(const Problem &p, const TcParams &tp, long G, long npa
                           const float *S0, const float *z0) {
   cudaError_t e = cudaSuccess;
   if (nparts > 0) e = launch_range_states(p, tp.part_len, (int)nparts, part_S, part_z, kKCausalState);
-  if (e == cudaSuccess) e = launch_kernel<false>(tp, dim3((unsigned)G, (unsigned)p.BH), p.stream, nparts > 0);
+  if (e == cudaSuccess) e = launch_kernel(tp, dim3((unsigned)G, (unsigned)p.BH), p.stream, nparts > 0);
   if (e == cudaSuccess) e = launch_causal_exact_head(p, tp.n_exact, S0, z0, true);
   return e;
 }

@@ -249,12 +249,16 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
       float zs = 0.f;
 #pragma unroll 8
       for (int m = 0; m < 32; ++m) zs += zred[(8 * m + (g ^ (m & 7))) * kZ + (D == 64 ? e : 8 * b + e)];
-      zpart[pt] = failed ? 0.f : zs;
+      zs = failed ? 0.f : zs;
+      zpart[pt] = zs;
+      if (range_mode) p.part_z[((long)bh * gridDim.x + blockIdx.x) * D + pt] = zs;
     }
     bool ok = !failed && mbar_wait(acc_full, 0, abort_word, status);
     ok = !bar_or(kBarBuild, kBuildPhi, !ok);
     const int quarter = warp & 3, half = (warp - 2) >> 2, row = quarter * 32 + lane;
-    float *prow = P + row * kPS;
+    // range mode, d = 128: row `row` of the partial state goes straight to global memory
+    float *prow = (range_mode && D == 128) ? p.part_S + (((long)bh * gridDim.x + blockIdx.x) * D + row) * D
+                                           : P + row * kPS;
     if (ok && nu > 0) {
       tc_fence_after();
       const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
@@ -281,18 +285,13 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
   __syncwarp();
   tc_fence_before();
   if (range_mode) {
-    // this CTA's partial state for its token range
+    // d = 128: rows and z were written above; d = 64: add the two diagonal blocks.
+    // The barrier also keeps tensor memory allocated until every read of it is done.
     __syncthreads();
-    const long part = (long)bh * gridDim.x + blockIdx.x;
-    for (int e = threadIdx.x; e < D * (D + 1); e += kBuildThreads) {
-      const int i = e / (D + 1), j = e % (D + 1);
-      if (j == D) {
-        p.part_z[part * D + i] = zpart[i];
-      } else {
-        float acc = P[i * kPS + j];
-        if (D == 64) acc += P[(64 + i) * kPS + j];
-        p.part_S[(part * D + i) * D + j] = acc;
-      }
+    if (D == 64) {
+      const long part = (long)bh * gridDim.x + blockIdx.x;
+      for (int e = threadIdx.x; e < D * D; e += kBuildThreads)
+        p.part_S[part * D * D + e] = P[(e / D) * kPS + e % D] + P[(64 + e / D) * kPS + e % D];
     }
   } else {
     cluster.sync();  // every partial state of the cluster is in shared memory
