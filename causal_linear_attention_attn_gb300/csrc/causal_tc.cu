@@ -110,9 +110,13 @@ struct TcParams {
   CUtensorMap to_tail;     // the same tensor, box 32 x 64 x 1: rows 64..127 of a head's first chunk
   float *out, *S_out, *z_out;
   const float *S0, *z0;      // initial state (nullable = zero)
-  float *part_S, *part_z;    // first-pass partial states: [BH][nparts][128][128], [BH][nparts][128]
+  float *part_S, *part_z;    // first-pass pieces: [2 fp_ctas][128][128], [2 fp_ctas][128]
   long N;
-  int seg_len, nseg, part_len, nparts, parts_per_seg;
+  int seg_len, nseg;
+  // first pass (see prefix_pieces): fp_ranges leading segments of every head,
+  // fp_range_units 64-token units each, fp_units in all, cut into fp_ctas runs
+  long fp_units;
+  int fp_ctas, fp_range_units, fp_ranges, fp_pieces_per_cta;
   int n_exact;
   float eps;
 };
@@ -186,6 +190,35 @@ __device__ __forceinline__ int column_pair_sums_8w(const uint8_t *tile, int w, i
   return c;
 }
 
+// The first pass cut the leading segments of all heads, one after another,
+// into fp_ctas even runs of units, each at most one segment long.  With two
+// pieces a run, run c's part in its first segment is piece 2c and the rest
+// piece 2c + 1 (all zeros when the run stays in one segment); with one piece a
+// run, the runs divide the segments and run c is piece c.  Pieces are in unit
+// order, and head bh's segments [0, seg) are exactly the pieces [first, last]
+// returned here.
+struct PieceRange {
+  long first, last;
+};
+__device__ __forceinline__ PieceRange prefix_pieces(const TcParams &p, int bh, int seg) {
+  const long L = p.fp_range_units, U = p.fp_units, C = p.fp_ctas;
+  const long ub = (long)bh * p.fp_ranges * L, ue = ub + (long)seg * L;  // units [ub, ue)
+  if (p.fp_pieces_per_cta == 1) {
+    const long run = U / C;
+    return PieceRange{ub / run, ue / run - 1};
+  }
+  // the runs holding units ub and ue - 1
+  long c0 = max(0L, ub * C / U - 1);
+  while (U * (c0 + 1) / C <= ub) ++c0;
+  long c1 = max(c0, (ue - 1) * C / U - 1);
+  while (U * (c1 + 1) / C <= ue - 1) ++c1;
+  PieceRange r;
+  r.first = 2 * c0 + (U * c0 / C < ub ? 1 : 0);  // run c0 crosses into segment rb at ub
+  const long s1 = U * c1 / C;
+  r.last = 2 * c1 + ((s1 / L + 1) * L <= ue - 1 ? 1 : 0);  // unit ue - 1 after run c1's crossing
+  return r;
+}
+
 __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParams p) {
   using Lay = Layout;
   constexpr int kStages = Lay::kStages;
@@ -213,7 +246,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
   const int bh = blockIdx.y;
   const long t_begin = (long)blockIdx.x * p.seg_len;
   const long t_end = min(p.N, t_begin + p.seg_len);
-  const int init_parts = blockIdx.x * p.parts_per_seg;  // first-pass parts before this segment
+  const int seg = blockIdx.x;  // segments before this one arrive as first-pass pieces
   const bool last_seg = (int)blockIdx.x == p.nseg - 1;
   const int nchunks = (int)((t_end - t_begin + kC - 1) / kC);
 
@@ -342,11 +375,14 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     const int quarter = warp & 3;
     const int half = (warp - kWarpPhi) >> 2;
     const int row = quarter * 32 + lane;
-    if (init_parts > 0) pdl_wait();  // the first pass's partial states are complete and visible
+    if (seg > 0) pdl_wait();  // the first pass's pieces are complete and visible
     if (pt < kD) {
-      // partial states of the first pass start from zero; a segment starts from the caller's state plus them
+      // first-pass pieces start from zero; a segment starts from the caller's state plus them
       float z = p.z0 ? p.z0[(long)bh * kD + pt] : 0.f;
-      for (int qp = 0; qp < init_parts; ++qp) z += p.part_z[((long)bh * p.nparts + qp) * kD + pt];
+      if (seg > 0) {
+        const PieceRange pr = prefix_pieces(p, bh, seg);
+        for (long piece = pr.first; piece <= pr.last; ++piece) z += p.part_z[piece * kD + pt];
+      }
       zs[pt] = z;
       den_x[pt] = den_x[kC + pt] = 0.f;
     }
@@ -422,8 +458,9 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     bool ok = true;
     {
       uint8_t *Sb = sm + Lay::Sb;
-      if (init_parts > 0) pdl_wait();  // the first pass's partial states are complete and visible
-      // initial state: caller's state plus the parts before this segment
+      if (seg > 0) pdl_wait();  // the first pass's pieces are complete and visible
+      // initial state: caller's state plus the first-pass pieces before this segment
+      const PieceRange pr = seg > 0 ? prefix_pieces(p, bh, seg) : PieceRange{0, -1};
       for (int cb = 0; cb < 4; ++cb) {
         float v[32];
 #pragma unroll
@@ -436,9 +473,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
             v[4 * e] += x.x, v[4 * e + 1] += x.y, v[4 * e + 2] += x.z, v[4 * e + 3] += x.w;
           }
         }
-        for (int qp = 0; qp < init_parts; ++qp) {
-          const float4 *src = reinterpret_cast<const float4 *>(
-              p.part_S + (((long)bh * p.nparts + qp) * kD + T) * kD + cb * 32);
+        for (long piece = pr.first; piece <= pr.last; ++piece) {
+          const float4 *src = reinterpret_cast<const float4 *>(p.part_S + (piece * kD + T) * kD + cb * 32);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float4 x = src[e];
@@ -701,11 +737,13 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bo
 //   3. the exact pass over each head's leading tokens, which reads nothing the
 //      main pass writes and so runs beside it; its last CTA waits for pass 2,
 //      so that the stream's next work follows all three.
-cudaError_t launch_passes(const Problem &p, const TcParams &tp, long G, long nparts, float *part_S, float *part_z,
-                          const float *S0, const float *z0) {
+cudaError_t launch_passes(const Problem &p, const TcParams &tp, const float *S0, const float *z0) {
   cudaError_t e = cudaSuccess;
-  if (nparts > 0) e = launch_range_states(p, tp.part_len, (int)nparts, part_S, part_z, kKCausalState);
-  if (e == cudaSuccess) e = launch_kernel(tp, dim3((unsigned)G, (unsigned)p.BH), p.stream, nparts > 0);
+  const bool split = tp.nseg > 1;
+  if (split)
+    e = launch_range_states(p, tp.seg_len, tp.fp_ranges, tp.fp_ctas, tp.fp_pieces_per_cta, tp.part_S, tp.part_z,
+                            kKCausalState);
+  if (e == cudaSuccess) e = launch_kernel(tp, dim3((unsigned)tp.nseg, (unsigned)p.BH), p.stream, split);
   if (e == cudaSuccess) e = launch_causal_exact_head(p, tp.n_exact, S0, z0, true);
   return e;
 }
@@ -716,26 +754,64 @@ bool causal_tc_supported(const Problem &p) {
          p.N <= 0x7fffffffL && encode_fn() != nullptr;
 }
 
-cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
-  const DeviceInfo &di = device_info(-1);
-  const long sms = std::max(1, di.sm_count);
+// How one call cuts the work: G segments of seg_chunks chunks per head for the
+// main pass, and (G > 1) a first pass over each head's G - 1 leading segments
+// cut into `ctas` even runs of 64-token units, with one or two pieces a run;
+// at most max_pieces pieces (the scratch that holds them).
+struct Partition {
+  long G = 1, seg_chunks = 0, ctas = 0, pieces_per_cta = 1;
+  long pieces() const { return pieces_per_cta * ctas; }
+};
+
+Partition plan_partition(const Problem &p, long sms, long max_pieces) {
+  Partition t;
   const long chunks = (p.N + kC - 1) / kC;
   // segments per head: enough CTAs to cover the SMs once, at least 4 chunks each
-  long G = std::max(1L, std::min(sms / p.BH, chunks / 4));
-  const long seg_chunks = (chunks + G - 1) / G;
-  G = (chunks + seg_chunks - 1) / seg_chunks;
-  // first-pass parts per segment: the largest divisor of seg_chunks that keeps the pass within one wave
-  long r = 1;
-  if (G > 1)
-    for (long d = seg_chunks; d >= 1; --d)
-      if (seg_chunks % d == 0 && p.BH * (G - 1) * d <= sms) {
+  t.G = std::max(1L, std::min(sms / p.BH, chunks / 4));
+  t.seg_chunks = (chunks + t.G - 1) / t.G;
+  t.G = (chunks + t.seg_chunks - 1) / t.seg_chunks;
+  if (t.G > 1) {
+    const long ranges = p.BH * (t.G - 1), L = t.seg_chunks * 2;  // first-pass segments, units each
+    // runs that divide the segments (one piece each): the most CTAs within one wave
+    long r = 1;
+    for (long d = L; d >= 1; --d)
+      if (L % d == 0 && ranges * d <= std::min(sms, max_pieces)) {
         r = d;
         break;
       }
-  const long nparts = (G - 1) * r;
+    if (ranges * r * 5 >= sms * 4) {
+      // they fill at least 80 % of the SMs: keep them (each main-pass segment then reads few pieces)
+      t.ctas = ranges * r;
+      t.pieces_per_cta = 1;
+    } else {
+      // otherwise one run per SM (fewer if the units run out), two pieces each; a run must not
+      // exceed one segment
+      t.ctas = std::min(std::min(sms, ranges * L), max_pieces / 2);
+      t.pieces_per_cta = 2;
+      if (t.ctas < ranges) t.ctas = 0;  // cannot be cut finely enough
+    }
+  }
+  return t;
+}
 
+void set_first_pass(TcParams &tp, const Problem &p, const Partition &t) {
+  tp.seg_len = (int)(t.seg_chunks * kC);
+  tp.nseg = (int)t.G;
+  tp.fp_ranges = (int)(t.G - 1);
+  tp.fp_range_units = (int)(t.seg_chunks * 2);
+  tp.fp_units = p.BH * (t.G - 1) * t.seg_chunks * 2;
+  tp.fp_ctas = (int)t.ctas;
+  tp.fp_pieces_per_cta = (int)t.pieces_per_cta;
+}
+
+cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
+  const DeviceInfo &di = device_info(-1);
+  const long sms = std::max(1, di.sm_count);
+  const Partition t = plan_partition(p, sms, 2 * sms);
+  if (t.G > 1 && t.ctas == 0) return cudaErrorInvalidValue;  // not reached: BH * G <= SMs
+  const long nparts = t.pieces();
   const size_t state_f = (size_t)kD * kD + kD;
-  const size_t scratch_f = (size_t)p.BH * nparts * state_f + (from_state ? (size_t)p.BH * state_f : 0);
+  const size_t scratch_f = (size_t)nparts * state_f + (from_state ? (size_t)p.BH * state_f : 0);
   float *scratch = nullptr;
   cudaError_t e = cudaSuccess;
   if (scratch_f) {
@@ -743,11 +819,11 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
     if (e != cudaSuccess) return e;
   }
   float *part_S = scratch;
-  float *part_z = scratch ? part_S + (size_t)p.BH * nparts * kD * kD : nullptr;
+  float *part_z = scratch ? part_S + (size_t)nparts * kD * kD : nullptr;
   const float *S0 = nullptr, *z0 = nullptr;
   if (from_state) {
     // the last segment overwrites the caller's state, so every reader uses a copy
-    float *Sc = part_z + (size_t)p.BH * nparts * kD;
+    float *Sc = part_z + (size_t)nparts * kD;
     float *zc = Sc + (size_t)p.BH * kD * kD;
     e = cudaMemcpyAsync(Sc, p.S, sizeof(float) * p.BH * kD * kD, cudaMemcpyDeviceToDevice, p.stream);
     if (e == cudaSuccess)
@@ -776,15 +852,11 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
   tp.part_S = part_S;
   tp.part_z = part_z;
   tp.N = p.N;
-  tp.seg_len = (int)(seg_chunks * kC);
-  tp.nseg = (int)G;
-  tp.part_len = (int)(seg_chunks / r * kC);
-  tp.nparts = (int)nparts;
-  tp.parts_per_seg = (int)r;
+  set_first_pass(tp, p, t);
   tp.n_exact = (int)std::min<long>(p.N, kExact);
   tp.eps = p.eps;
 
-  e = launch_passes(p, tp, G, nparts, part_S, part_z, S0, z0);
+  e = launch_passes(p, tp, S0, z0);
   if (scratch) {
     const cudaError_t f = cudaFreeAsync(scratch, p.stream);
     if (e == cudaSuccess) e = f;
@@ -800,7 +872,7 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
 // start at zero (every partial state is written before it is read), but calls
 // that overlap on the GPU would race on it.
 // ---------------------------------------------------------------------------
-constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;  // 16 MiB
+constexpr size_t kNoAllocScratchFloats = size_t(5) << 20;  // 20 MiB: the pieces of 158 first-pass CTAs
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
 namespace {
@@ -833,30 +905,21 @@ cudaError_t launch_causal_tc_noalloc(const Problem &p, int dev, bool *too_large)
   *too_large = false;
   const DeviceInfo &di = device_info(dev);
   const long sms = std::max(1, di.sm_count);
-  const long chunks = (p.N + kC - 1) / kC;
-  // the same partition as la_causal: segments per head, first-pass parts per segment
-  long G = std::max(1L, std::min(sms / p.BH, chunks / 4));
-  const long seg_chunks = (chunks + G - 1) / G;
-  G = (chunks + seg_chunks - 1) / seg_chunks;
-  long r = 1;
-  if (G > 1)
-    for (long d = seg_chunks; d >= 1; --d)
-      if (seg_chunks % d == 0 && p.BH * (G - 1) * d <= sms) {
-        r = d;
-        break;
-      }
-  const long nparts = (G - 1) * r;
-  const size_t need = (size_t)p.BH * nparts * ((size_t)kD * kD + kD);
-  if (need > kNoAllocScratchFloats) {
+  // the same partition as la_causal, with no more first-pass pieces than the fixed array holds
+  const size_t state_f = (size_t)kD * kD + kD;
+  const Partition t = plan_partition(p, sms, (long)(kNoAllocScratchFloats / state_f));
+  if (t.G > 1 && t.ctas == 0) {
     *too_large = true;
     return cudaSuccess;
   }
+  const long nparts = t.pieces();
+  const size_t need = (size_t)nparts * state_f;
   float *part_S = nullptr, *part_z = nullptr;
   if (need) {
     NoAllocScratch &sc = noalloc_scratch(dev);
     if (sc.err != cudaSuccess) return sc.err;
     part_S = sc.ptr;
-    part_z = part_S + (size_t)p.BH * nparts * kD * kD;
+    part_z = part_S + (size_t)nparts * kD * kD;
   }
   TcParams tp;
   memset(&tp, 0, sizeof tp);
@@ -870,14 +933,10 @@ cudaError_t launch_causal_tc_noalloc(const Problem &p, int dev, bool *too_large)
   tp.part_S = part_S;
   tp.part_z = part_z;
   tp.N = p.N;
-  tp.seg_len = (int)(seg_chunks * kC);
-  tp.nseg = (int)G;
-  tp.part_len = (int)(seg_chunks / r * kC);
-  tp.nparts = (int)nparts;
-  tp.parts_per_seg = (int)r;
+  set_first_pass(tp, p, t);
   tp.n_exact = (int)std::min<long>(p.N, kExact);
   tp.eps = p.eps;
-  return launch_passes(p, tp, G, nparts, part_S, part_z, nullptr, nullptr);
+  return launch_passes(p, tp, nullptr, nullptr);
 }
 
 cudaError_t read_and_clear_device_status(unsigned int *value) {

@@ -103,10 +103,31 @@ static_assert(BuildLayout<128>::Bytes <= 232448, "shared memory budget");
 struct BuildParams {
   CUtensorMap tk, tv;  // [BH][N][D] bf16, box 64 x 64 x 1, 128-byte swizzle
   float *S, *z;        // whole-sequence mode: final state, summed over the cluster
-  float *part_S, *part_z;  // range mode (non-null): [BH][parts][D][D], [BH][parts][D], one per CTA
+  // Range mode (part_S non-null, d = 128): the first pass of the causal form.  Head h's
+  // ranges r = h * ranges_per_head + s (s < ranges_per_head) cover its units
+  // [s * range_units, (s + 1) * range_units); all heads' ranges, one after another, form
+  // units_total flattened units, split evenly over the CTAs of a 1-D grid.  A CTA's run
+  // is at most one range long, so it touches at most two ranges: its pieces 0 and 1 go to
+  // part_S[(2 c + k)][D][D] and part_z[(2 c + k)][D] (an empty piece 1 is written as zeros).
+  // With pieces_per_cta == 1 the runs divide the ranges evenly and CTA c writes piece c only.
+  float *part_S, *part_z;
   long N;
-  int units;       // stage units per head: 128 tokens (d = 64) or 64 (d = 128)
-  int part_units;  // range mode: units per CTA (part p covers units [p * part_units, ...))
+  int units;  // stage units per head: 128 tokens (d = 64) or 64 (d = 128)
+  long units_total;
+  int range_units, ranges_per_head, pieces_per_cta;
+};
+
+// Walks stage units as (head, unit in head) pairs without per-unit division.
+struct UnitWalk {
+  int h;
+  long u;
+  long per_head;
+  __device__ void next() {
+    if (++u == per_head) {
+      u = 0;
+      ++h;
+    }
+  }
 };
 
 template <int D>
@@ -130,20 +151,28 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
   float *P = reinterpret_cast<float *>(sm + Lay::K);
   float *zred = reinterpret_cast<float *>(sm + Lay::Zred), *zpart = zred + kBuildPhi * Lay::kZ;
 
-  const bool range_mode = p.part_S != nullptr;
+  const bool range_mode = D == 128 && p.part_S != nullptr;
   cg::cluster_group cluster = cg::this_cluster();
   const int G = range_mode ? 1 : (int)cluster.num_blocks(), rank = range_mode ? 0 : (int)cluster.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  int u0, u1;
+  // this CTA's units: nu of them from (h0, uh0); the units from nb on form piece 1
+  UnitWalk start;
+  int nu, nb;
   if (range_mode) {
-    u0 = blockIdx.x * p.part_units;
-    u1 = min(p.units, u0 + p.part_units);
+    start.per_head = (long)p.ranges_per_head * p.range_units;
+    const long f0 = p.units_total * blockIdx.x / gridDim.x, f1 = p.units_total * (blockIdx.x + 1) / gridDim.x;
+    nu = (int)(f1 - f0);
+    start.h = (int)(f0 / start.per_head);
+    start.u = f0 - (long)start.h * start.per_head;
+    nb = p.pieces_per_cta == 1 ? nu : (int)min((long)nu, (f0 / p.range_units + 1) * p.range_units - f0);
   } else {
-    u0 = (int)((long)p.units * rank / G);
-    u1 = (int)((long)p.units * (rank + 1) / G);
+    start.per_head = p.units;
+    start.h = blockIdx.y;
+    start.u = (long)p.units * rank / G;
+    nu = (int)((long)p.units * (rank + 1) / G - start.u);
+    nb = nu;
   }
-  const int nu = max(0, u1 - u0);
+  nu = max(nu, 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kBuildStages; ++s) {
@@ -156,34 +185,35 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
     *abort_word = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 128);
+  if (warp == 1) tmem_alloc(tmem_slot, 256);
   // the kernel queued after this one (the read, or the main causal pass) may start on free SMs
   if (threadIdx.x == 0) pdl_trigger();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;
+  const uint32_t tS = tmem;  // piece k accumulates at columns 128 k
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       prefetch_tmap(&p.tk);
       prefetch_tmap(&p.tv);
+      UnitWalk w = start;
       int issued = 0;
-      for (int i = 0; i < nu; ++i) {
+      for (int i = 0; i < nu; ++i, w.next()) {
         const int s = i % kBuildStages;
         const uint32_t r = i / kBuildStages;
         if (i >= kBuildStages && !mbar_wait(&empty[s], (r - 1) & 1, abort_word, status)) break;
-        const int tok = (u0 + i) * kUnit;
+        const int tok = (int)w.u * kUnit;
         uint8_t *k = sm + Lay::K + s * Lay::kStage, *v = sm + Lay::V + s * Lay::kStage;
         mbar_arrive_expect_tx(&full[s], 2 * Lay::kStage);
         // d = 64: two 64-token sub-tiles; d = 128: the two 64-feature halves of one tile
         const int x1 = D == 64 ? 0 : 64, t1 = D == 64 ? tok + 64 : tok;
-        tma_load_3d(k, &p.tk, &full[s], 0, tok, bh);
-        tma_load_3d(k + kHalf, &p.tk, &full[s], x1, t1, bh);
-        tma_load_3d(v, &p.tv, &full[s], 0, tok, bh);
-        tma_load_3d(v + kHalf, &p.tv, &full[s], x1, t1, bh);
+        tma_load_3d(k, &p.tk, &full[s], 0, tok, w.h);
+        tma_load_3d(k + kHalf, &p.tk, &full[s], x1, t1, w.h);
+        tma_load_3d(v, &p.tv, &full[s], 0, tok, w.h);
+        tma_load_3d(v + kHalf, &p.tv, &full[s], x1, t1, w.h);
         issued = i + 1;
       }
       for (int i = max(0, issued - kBuildStages); i < issued; ++i)
@@ -199,10 +229,12 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
         if (!mbar_wait(&phi_done[s], (i / kBuildStages) & 1, abort_word, status)) break;
         tc_fence_after();
         const uint32_t k = sK + s * Lay::kStage, v = sV + s * Lay::kStage;
+        const uint32_t d = tS + (i >= nb ? 128u : 0u);
+        const bool first = i == 0 || i == nb;  // a piece's first unit overwrites its accumulator
 #pragma unroll 1
         for (int ks = 0; ks < 4; ++ks)  // both operands MN-major: 16 tokens per step, 64-wide blocks 8 KB apart
-          mma_bf16(tS, sw128_desc(k + ks * 2048, kHalf, 1024), sw128_desc(v + ks * 2048, kHalf, 1024), iS,
-                   (i > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16(d, sw128_desc(k + ks * 2048, kHalf, 1024), sw128_desc(v + ks * 2048, kHalf, 1024), iS,
+                   (!first || ks > 0) ? 1u : 0u);
         mma_commit(&empty[s]);
       }
       mma_commit(acc_full);
@@ -210,17 +242,18 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
       wait_drain(drain, 0, status);
     }
   } else {
-    // ---------------- phi(K) in place, column sums, then the partial state ----------------
+    // ---------------- phi(K) in place, column sums, then the partial states ----------------
     const int pt = threadIdx.x - 64;
     // Chunk pt + 256 j sits at position pt & 7 of row (pt >> 3) + 32 j; with the
     // 128-byte swizzle it holds the features 8 g .. 8 g + 7, g = (pt & 7) ^ ((pt >> 3) & 7),
     // of its row (of the 64-feature block j / 2 for d = 128), the same g for every j.
     constexpr int kZ = Lay::kZ;
-    float zacc[kZ];
+    float zacc0[kZ], zacc1[kZ];  // per piece (kept in registers: selected by uniform branches)
 #pragma unroll
-    for (int a = 0; a < kZ; ++a) zacc[a] = 0.f;
+    for (int a = 0; a < kZ; ++a) zacc0[a] = zacc1[a] = 0.f;
     bool failed = false;
-    for (int i = 0; i < nu; ++i) {
+    UnitWalk w = start;
+    for (int i = 0; i < nu; ++i, w.next()) {
       const int s = i % kBuildStages;
       const bool ok = mbar_wait(&full[s], (i / kBuildStages) & 1, abort_word, status);
       if (bar_or(kBarBuild, kBuildPhi, !ok)) {
@@ -228,72 +261,89 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
         break;
       }
       uint8_t *k = sm + Lay::K + s * Lay::kStage;
-      const long tok0 = (long)(u0 + i) * kUnit;
-      phi_chunks<4, kBuildPhi>(k, pt, [&](int j, int ch, uint4 x) {
-        const int row = ch >> 3;  // 0..127 over the two blocks
-        const long tok = tok0 + (D == 64 ? row : (row & 63));
-        const uint4 y = tok < p.N ? phi8(x) : make_uint4(0u, 0u, 0u, 0u);  // rows past the end add nothing
-        add8_bf16(zacc + (D == 64 ? 0 : 8 * (j >> 1)), y);
-        return y;
-      });
+      const long tok0 = w.u * kUnit;
+      // phi in place; the rounded values also go into the column sums of this unit's piece
+      auto phi_sum = [&](float *za) {
+        phi_chunks<4, kBuildPhi>(k, pt, [&](int j, int ch, uint4 x) {
+          const int row = ch >> 3;  // 0..127 over the two blocks
+          const long tok = tok0 + (D == 64 ? row : (row & 63));
+          const uint4 y = tok < p.N ? phi8(x) : make_uint4(0u, 0u, 0u, 0u);  // rows past the end add nothing
+          add8_bf16(za + (D == 64 ? 0 : 8 * (j >> 1)), y);
+          return y;
+        });
+      };
+      if (i < nb)
+        phi_sum(zacc0);
+      else
+        phi_sum(zacc1);
       fence_async_smem();
       mbar_arrive(&phi_done[s]);
-    }
-    // column sums: feature f = 64 b + 8 g + e is held, as entry 8 b + e (d = 128) or e,
-    // by the 32 threads 8 m + (g ^ (m & 7)), m = 0..31
-#pragma unroll
-    for (int a = 0; a < kZ; ++a) zred[pt * kZ + a] = zacc[a];
-    named_bar(kBarBuild, kBuildPhi);
-    if (pt < D) {
-      const int b = pt >> 6, g = (pt >> 3) & 7, e = pt & 7;
-      float zs = 0.f;
-#pragma unroll 8
-      for (int m = 0; m < 32; ++m) zs += zred[(8 * m + (g ^ (m & 7))) * kZ + (D == 64 ? e : 8 * b + e)];
-      zs = failed ? 0.f : zs;
-      zpart[pt] = zs;
-      if (range_mode) p.part_z[((long)bh * gridDim.x + blockIdx.x) * D + pt] = zs;
     }
     bool ok = !failed && mbar_wait(acc_full, 0, abort_word, status);
     ok = !bar_or(kBarBuild, kBuildPhi, !ok);
     const int quarter = warp & 3, half = (warp - 2) >> 2, row = quarter * 32 + lane;
-    // range mode, d = 128: row `row` of the partial state goes straight to global memory
-    float *prow = (range_mode && D == 128) ? p.part_S + (((long)bh * gridDim.x + blockIdx.x) * D + row) * D
-                                           : P + row * kPS;
-    if (ok && nu > 0) {
-      tc_fence_after();
-      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-      uint32_t v[32];
-      constexpr int kParts = D == 64 ? 1 : 2;
+    const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+    const int npieces = range_mode ? p.pieces_per_cta : 1;
 #pragma unroll
-      for (int c = 0; c < kParts; ++c) {
-        // d = 64: rows 0-63 hold K_a^T V_a in columns 0-63, rows 64-127 K_b^T V_b in columns 64-127
-        const int src = D == 64 ? (row < 64 ? 0 : 64) + 32 * half : 64 * half + 32 * c;
-        const int dst = D == 64 ? 32 * half : 64 * half + 32 * c;
-        tmem_ld32(tS + lanes + src, v);
+    for (int piece = 0; piece < 2; ++piece) {
+      if (piece >= npieces) break;
+      const bool filled = ok && (piece == 0 ? min(nu, nb) > 0 : nu > nb);
+      const float *zp = piece == 0 ? zacc0 : zacc1;
+      // column sums: feature f = 64 b + 8 g + e is held, as entry 8 b + e (d = 128) or e,
+      // by the 32 threads 8 m + (g ^ (m & 7)), m = 0..31
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4 *>(prow + dst + 4 * q) =
-              make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                          __uint_as_float(v[4 * q + 3]));
+      for (int a = 0; a < kZ; ++a) zred[pt * kZ + a] = zp[a];
+      named_bar(kBarBuild, kBuildPhi);
+      if (pt < D) {
+        const int b = pt >> 6, g = (pt >> 3) & 7, e = pt & 7;
+        float zs = 0.f;
+#pragma unroll 8
+        for (int m = 0; m < 32; ++m) zs += zred[(8 * m + (g ^ (m & 7))) * kZ + (D == 64 ? e : 8 * b + e)];
+        zs = filled ? zs : 0.f;
+        if (range_mode)
+          p.part_z[((long)p.pieces_per_cta * blockIdx.x + piece) * D + pt] = zs;
+        else
+          zpart[pt] = zs;
       }
-    } else {
-      const int w = D == 64 ? 32 : 64;
-      for (int c = 0; c < w; ++c) prow[w * half + c] = 0.f;
+      named_bar(kBarBuild, kBuildPhi);  // zred is free for the next piece
+      // range mode: row `row` of the piece goes straight to global memory; otherwise to shared memory
+      const long slot = (long)p.pieces_per_cta * blockIdx.x + piece;
+      float *prow = range_mode ? p.part_S + (slot * D + row) * D : P + row * kPS;
+      if (filled) {
+        tc_fence_after();
+        uint32_t v[32];
+        constexpr int kParts = D == 64 ? 1 : 2;
+#pragma unroll
+        for (int c = 0; c < kParts; ++c) {
+          // d = 64: rows 0-63 hold K_a^T V_a in columns 0-63, rows 64-127 K_b^T V_b in columns 64-127
+          const int src = D == 64 ? (row < 64 ? 0 : 64) + 32 * half : 64 * half + 32 * c;
+          const int dst = D == 64 ? 32 * half : 64 * half + 32 * c;
+          tmem_ld32(tS + 128 * piece + lanes + src, v);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(prow + dst + 4 * q) =
+                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+      } else if (range_mode) {
+        // an empty piece reads as zeros: coalesced 16-byte stores over the whole [D][D] piece
+        float4 *z4 = reinterpret_cast<float4 *>(p.part_S + slot * D * D);
+        for (int e = pt; e < D * D / 4; e += kBuildPhi) z4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        const int wd = D == 64 ? 32 : 64;
+        for (int c = 0; c < wd; ++c) prow[wd * half + c] = 0.f;
+      }
     }
   }
 
   __syncwarp();
   tc_fence_before();
   if (range_mode) {
-    // d = 128: rows and z were written above; d = 64: add the two diagonal blocks.
-    // The barrier also keeps tensor memory allocated until every read of it is done.
+    // pieces and their key sums were written above; the barrier keeps tensor
+    // memory allocated until every read of it is done
     __syncthreads();
-    if (D == 64) {
-      const long part = (long)bh * gridDim.x + blockIdx.x;
-      for (int e = threadIdx.x; e < D * D; e += kBuildThreads)
-        p.part_S[part * D * D + e] = P[(e / D) * kPS + e % D] + P[(64 + e / D) * kPS + e % D];
-    }
   } else {
+    const int bh = blockIdx.y;
     cluster.sync();  // every partial state of the cluster is in shared memory
     // this CTA sums rows [r0, r0 + D/G) of S (and those entries of z) over the cluster
     const int rows = D / G, r0 = rank * rows;
@@ -318,7 +368,7 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
   }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -632,7 +682,8 @@ cudaError_t launch_t(const Problem &p) {
   bp.part_S = bp.part_z = nullptr;
   bp.N = p.N;
   bp.units = (int)((p.N + kUnit - 1) / kUnit);
-  bp.part_units = 0;
+  bp.units_total = 0;
+  bp.range_units = bp.ranges_per_head = bp.pieces_per_cta = 0;
   // cluster size: a power of two <= 8 so that the build covers the SMs about once, >= 8 units a CTA
   int G = 1;
   while (G < 8 && p.BH * (2 * G) <= sms && bp.units / (2 * G) >= 8) G *= 2;
@@ -704,23 +755,34 @@ bool global_tc_supported(const Problem &p) {
 
 cudaError_t launch_global_tc(const Problem &p) { return p.dk == 64 ? launch_t<64>(p) : launch_t<128>(p); }
 
-cudaError_t launch_range_states(const Problem &p, long part_tokens, int nparts, float *part_S, float *part_z,
-                                int kernel_id) {
-  if (p.dt != LA_BF16 || p.dk != 128 || p.dv != 128 || part_tokens % 64 != 0 || nparts < 1) return cudaErrorInvalidValue;
+cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_per_head, int ctas, int pieces_per_cta,
+                                float *piece_S, float *piece_z, int kernel_id) {
+  if (p.dt != LA_BF16 || p.dk != 128 || p.dv != 128 || range_tokens % 64 != 0 || ranges_per_head < 1 || ctas < 1 ||
+      pieces_per_cta < 1 || pieces_per_cta > 2)
+    return cudaErrorInvalidValue;
+  const long range_units = range_tokens / 64;
+  const long units_total = (long)p.BH * ranges_per_head * range_units;
+  // a CTA's run may span at most one range boundary; one piece a CTA needs runs that divide the ranges
+  if ((units_total + ctas - 1) / ctas > range_units || ctas > units_total) return cudaErrorInvalidValue;
+  if (pieces_per_cta == 1 && (units_total % ctas != 0 || range_units % (units_total / ctas) != 0))
+    return cudaErrorInvalidValue;
   BuildParams bp;
   if (!make_map(&bp.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k, p.BH, p.N, 128, 64, 64) ||
       !make_map(&bp.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v, p.BH, p.N, 128, 64, 64))
     return cudaErrorInvalidValue;
   bp.S = bp.z = nullptr;
-  bp.part_S = part_S;
-  bp.part_z = part_z;
+  bp.part_S = piece_S;
+  bp.part_z = piece_z;
   bp.N = p.N;
   bp.units = (int)((p.N + 63) / 64);
-  bp.part_units = (int)(part_tokens / 64);
+  bp.units_total = units_total;
+  bp.range_units = (int)range_units;
+  bp.ranges_per_head = ranges_per_head;
+  bp.pieces_per_cta = pieces_per_cta;
   cudaError_t e = build_smem<128>();
   if (e != cudaSuccess) return e;
   LaunchTimer timer(kernel_id, p.stream);
-  global_build_tc<128><<<dim3((unsigned)nparts, (unsigned)p.BH), kBuildThreads, BuildLayout<128>::Bytes, p.stream>>>(bp);
+  global_build_tc<128><<<(unsigned)ctas, kBuildThreads, BuildLayout<128>::Bytes, p.stream>>>(bp);
   e = cudaGetLastError();
   timer.done(e);
   if (e == cudaSuccess) count_launch();

@@ -52,12 +52,18 @@ bool global_tc_supported(const Problem &p);
 cudaError_t launch_global_tc(const Problem &p);
 cudaError_t read_and_clear_global_tc_status(unsigned int *value);
 
-// Partial states of token ranges on the tensor cores (bf16, d_k = d_v = 128):
-// CTA (r, h) sums phi(k) v^T and phi(k) over tokens [r * part_tokens,
-// (r + 1) * part_tokens) of head h into part_S[h][r] ([128][128]) and
-// part_z[h][r] ([128]), starting from zero.  part_tokens % 64 == 0.
-cudaError_t launch_range_states(const Problem &p, long part_tokens, int nparts, float *part_S, float *part_z,
-                                int kernel_id);
+// First pass of the split causal form on the tensor cores (bf16, d_k = d_v = 128).
+// Each head's first ranges_per_head ranges of range_tokens tokens (range s of
+// head h is r = h * ranges_per_head + s), all heads one after another, are cut
+// evenly into `ctas` runs of 64-token units, one per CTA; a run must be at most
+// one range long (ctas >= BH * ranges_per_head), so it spans at most two ranges.
+// CTA c writes the sums of phi(k) v^T and phi(k) over the part of its run in its
+// first range to piece 2c and over the rest to piece 2c + 1 (zeros if none):
+// piece_S[piece][128][128], piece_z[piece][128].  range_tokens % 64 == 0.  With
+// pieces_per_cta == 1 the runs must divide the ranges evenly; CTA c then writes
+// piece c only.
+cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_per_head, int ctas, int pieces_per_cta,
+                                float *piece_S, float *piece_z, int kernel_id);
 
 // Read and clear the device status word (bounded-wait timeouts).
 cudaError_t read_and_clear_device_status(unsigned int *value);

@@ -132,12 +132,13 @@ LA_API la_status la_causal_with_state(const void *q, const void *k, const void *
  * stream-ordered allocation made by la_causal could fail mid-run.
  *
  * Same arguments, results and errors as la_causal.  The partial states that
- * la_causal allocates per call (for long sequences split into segments) live
- * here in one fixed 16 MiB device array inside the library instead; every
- * GPU that loads the library keeps that array until the process exits.  If
- * a problem would need more than 16 MiB of partial states (more than 254
- * segment parts of 128x128 fp32 in total), the call returns
- * LA_ERR_TOO_LARGE and launches nothing.  All calls share the array, so
+ * la_causal allocates per call (for long sequences split into segments: at
+ * most two 128x128 fp32 states per first-pass CTA, at most one CTA per SM) live here
+ * in one fixed 20 MiB device array inside the library instead; every GPU
+ * that loads the library keeps that array until the process exits.  It holds
+ * the partial states of 158 first-pass CTAs; a problem whose first pass would
+ * need more (B * H * (segments - 1) > 158) returns LA_ERR_TOO_LARGE and
+ * launches nothing.  All calls share the array, so
  * calls whose work overlaps on the GPU (different streams, or different host
  * threads on the same device) race on it and give wrong results: order them.
  * The first call on each device looks up the array's device address
