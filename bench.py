@@ -331,26 +331,55 @@ def run_seq_form(L, w, steps, warmup, world, stream, hbm, src, gen_device="cuda"
     return res, (q, k, v, out, S, z, fn)
 
 
-def run_e2e(L, w, bufs, steps, warmup, stream):
-    """Same call through host buffers: pinned q,k,v copied in, out/S/z copied back, every step."""
+def run_e2e(L, w, bufs, steps, warmup, stream, groups: int = 4):
+    """Same call through host buffers: every step copies q, k, v in from pinned
+    host memory and out, S, z back.  The heads go through in `groups` groups
+    on three streams (copy in, compute, copy out), so that the copies of one
+    group overlap the call on another; a step still ends only when all of its
+    results are on the host."""
     q, k, v, out, S, z, fn = bufs
-    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    ho, hS, hz = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out, S, z))
+    BH = w.BH
+    flat = lambda t: t.view(BH, *t.shape[2:])
+    dev = [flat(t) for t in (q, k, v, out, S, z)]
+    host = [t.cpu().pin_memory() for t in dev[:3]] + [torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                                                      for t in dev[3:]]
+    cuts = [BH * g // groups for g in range(groups + 1)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        fn(q, k, v, out=out, S=S, z=z, eps=w.eps, stream=stream)
-        ho.copy_(out, non_blocking=True)
-        hS.copy_(S, non_blocking=True)
-        hz.copy_(z, non_blocking=True)
+        start = torch.cuda.Event()
+        start.record(stream)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        done_in = [torch.cuda.Event() for _ in range(groups)]
+        done_call = [torch.cuda.Event() for _ in range(groups)]
+        for g in range(groups):
+            a, b = cuts[g], cuts[g + 1]
+            with torch.cuda.stream(s_in):
+                for d, h in zip(dev[:3], host[:3]):
+                    d[a:b].copy_(h[a:b], non_blocking=True)
+                done_in[g].record(s_in)
+        for g in range(groups):
+            a, b = cuts[g], cuts[g + 1]
+            stream.wait_event(done_in[g])
+            fn(*(t[a:b].unsqueeze(0) for t in dev[:3]), out=dev[3][a:b].unsqueeze(0), S=dev[4][a:b].unsqueeze(0),
+               z=dev[5][a:b].unsqueeze(0), eps=w.eps, stream=stream)
+            done_call[g].record(stream)
+        for g in range(groups):
+            a, b = cuts[g], cuts[g + 1]
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_call[g])
+                for d, h in zip(dev[3:], host[3:]):
+                    h[a:b].copy_(d[a:b], non_blocking=True)
+        finished = torch.cuda.Event()
+        finished.record(s_out)
+        stream.wait_event(finished)
 
     ms = time_device(step, steps, warmup, 1, stream)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hS, hz))
+    h2d = sum(t.numel() * t.element_size() for t in host[:3])
+    d2h = sum(t.numel() * t.element_size() for t in host[3:])
     return {"value": w.BH * w.N / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "head_groups": groups}
 
 
 def run_decode(L, w, steps, warmup, world, stream, hbm, src):
