@@ -331,6 +331,23 @@ def run_seq_form(L, w, steps, warmup, world, stream, hbm, src, gen_device="cuda"
     return res, (q, k, v, out, S, z, fn)
 
 
+def run_continue(L, w, steps, warmup, world, stream, hbm, src):
+    """Prefill that continues from a carried state (la_causal_with_state): the
+    state a call leaves is the state the next call starts from."""
+    q, k, v = (t.cuda() for t in inputs.make_qkv(w, device="cuda"))
+    out, S, z = L.la_causal(q, k, v, eps=w.eps, stream=stream)
+    call = lambda: L.la_causal_with_state(q, k, v, S, z, out=out, eps=w.eps, stream=stream)
+    n0 = L.kernel_launches()
+    ms = time_device(call, steps, warmup, world, stream, L)
+    launches = (L.kernel_launches() - n0) // (2 * steps + warmup) * steps
+    ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
+    rl, table = dominant_roofline(L, w, steps, hbm, src, w.name + "_with_state")
+    step_bytes = seq_bytes(w) + w.BH * (w.dk * w.dv + w.dk) * 4  # the incoming state is read too
+    return {"workload": w.name + " continued from a carried state", "tokens_per_s": world * w.BH * w.N / (ms * 1e-3),
+            "ms_per_call": ms, "roofline": rl, "step_roofline": roofline(step_bytes, ms, hbm, src, None),
+            "kernels": table, "gpu_launches": launches}
+
+
 def run_e2e(L, w, bufs, steps, warmup, stream, groups: int = 4):
     """Same call through host buffers: every step copies q, k, v in from pinned
     host memory and out, S, z back.  The heads go through in `groups` groups
@@ -451,6 +468,12 @@ def main_ours(args):
                 forms[name], _ = run_seq_form(L, wx, steps, args.warmup, world, stream, hbm, src)
                 forms[name]["clocks"] = clk.summary(*LAST_WINDOW)
                 torch.cuda.empty_cache()
+        if "causal_bf16_with_state" in extras:
+            wc = rank_workload(inputs.WORKLOADS["causal_bf16"], rank)
+            forms["causal_bf16_with_state"] = run_continue(L, wc, max(3, args.steps // 2), args.warmup, world, stream,
+                                                           hbm, src)
+            forms["causal_bf16_with_state"]["clocks"] = clk.summary(*LAST_WINDOW)
+            torch.cuda.empty_cache()
         if "decode_bf16" in extras:
             wd = rank_workload(inputs.WORKLOADS["decode_bf16"], rank)
             forms["decode_bf16"] = run_decode(L, wd, args.decode_steps, args.warmup, world, stream, hbm, src)
@@ -509,7 +532,7 @@ def parse(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-extras", action="store_true", help="time the headline workload only")
-    ap.add_argument("--forms", default="global_bf16,causal_bf16_long,decode_bf16",
+    ap.add_argument("--forms", default="global_bf16,causal_bf16_long,causal_bf16_with_state,decode_bf16",
                     help="comma-separated other forms timed after the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-step-s", type=float, default=10.0, help="max CPU seconds per reference step")

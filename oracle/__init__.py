@@ -55,6 +55,8 @@ def _load():
         lib.lao_decode_step.argtypes = [dp, dp, dp, dp, dp, dp, L, I, I, D, I, I]
         lib.lao_decode_step.restype = I
         lib.lao_state_scalars.argtypes = [I, I]
+        lib.lao_retention.argtypes = [dp, dp, dp, dp, dp, dp, dp, L, L, I, I, I]
+        lib.lao_retention.restype = I
         lib.lao_state_scalars.restype = L
         lib.lao_version.restype = I
         _lib = lib
@@ -143,6 +145,24 @@ def decode_step(q, k, v, S, z, eps: float = 1e-6, phi: str = "elu1", nthreads: i
                              BH, dk, dv, float(eps), PHI_KINDS[phi], int(nthreads))
     _check(rc, "decode_step")
     return out, S, z
+
+
+def retention(q, k, v, gamma, S0=None, nthreads: int = 1):
+    """Causal retention with decay: S_t = gamma S_{t-1} + k_t v_t^T, out_t = q_t^T S_t.
+
+    q, k: [..., N, dk]; v: [..., N, dv]; gamma: a scalar, or one value per
+    leading index (per head).  Returns (out [..., N, dv], S [..., dk, dv]).
+    """
+    lib = _load()
+    q, k, v, lead, BH, N, dk, dv = _split(q, k, v)
+    g = _f64(np.broadcast_to(np.asarray(gamma, dtype=np.float64), lead))
+    out = np.empty(lead + (N, dv))
+    S = np.empty(lead + (dk, dv))
+    S0 = None if S0 is None else _f64(np.broadcast_to(S0, lead + (dk, dv)))
+    rc = lib.lao_retention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(S), _ptr(S0), _ptr(g), BH, N, dk, dv,
+                           int(nthreads))
+    _check(rc, "retention")
+    return out, S
 
 
 def state_scalars(m: int, dv: int) -> int:

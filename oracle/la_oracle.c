@@ -235,3 +235,81 @@ int lao_decode_step(const double *q, const double *k, const double *v, double *o
  * vector ("Linear Attention: From Pairwise Reads to a Recurrent State",
  * "Linear in which variable?"). */
 long lao_state_scalars(int m, int dv) { return (long)m * dv + m; }
+
+/* ---------------------------------------------------------------------------
+ * Retention: linear attention with an explicit decay and no denominator
+ * ("Linear Attention Math", "The kernel cousins: SSMs and RetNet"):
+ *   S_t = gamma S_{t-1} + k_t v_t^T,   out_t = q_t^T S_t
+ * with q and k used as given (the recurrence is written on k_t itself, with
+ * no feature map) and the read taken after the update, as for every other
+ * form here.  gamma is per head (one value per flattened (b,h)).  The pages
+ * replace the denominator by a gated normalization they do not define; the
+ * output here is the ungated retention q_t^T S_t.
+ * -------------------------------------------------------------------------*/
+typedef struct {
+  const double *q, *k, *v, *S0, *gamma;
+  double *out, *S;
+  long N, h0, h1;
+  int dk, dv;
+} ret_job_t;
+
+static void retention_head(const ret_job_t *jb, long h) {
+  const int dk = jb->dk, dv = jb->dv;
+  const double g = jb->gamma[h];
+  double *S = jb->S + h * (long)dk * dv;
+  if (jb->S0)
+    memcpy(S, jb->S0 + h * (long)dk * dv, sizeof(double) * dk * dv);
+  else
+    memset(S, 0, sizeof(double) * dk * dv);
+  for (long t = 0; t < jb->N; ++t) {
+    const double *q = jb->q + (h * jb->N + t) * dk, *k = jb->k + (h * jb->N + t) * dk;
+    const double *v = jb->v + (h * jb->N + t) * dv;
+    double *o = jb->out + (h * jb->N + t) * dv;
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) S[i * dv + j] = g * S[i * dv + j] + k[i] * v[j];
+    for (int j = 0; j < dv; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += q[i] * S[i * dv + j];
+      o[j] = acc;
+    }
+  }
+}
+
+static void *retention_worker(void *arg) {
+  const ret_job_t *jb = (const ret_job_t *)arg;
+  for (long h = jb->h0; h < jb->h1; ++h) retention_head(jb, h);
+  return NULL;
+}
+
+/* Causal retention over [BH, N, .] with per-head decay gamma[BH]; S receives
+ * the final state, S0 (nullable) gives the initial one. */
+int lao_retention(const double *q, const double *k, const double *v, double *out, double *S,
+                  const double *S0, const double *gamma, long BH, long N, int dk, int dv, int nthreads) {
+  if (!q || !k || !v || !out || !S || !gamma || BH < 0 || N < 0 || dk <= 0 || dv <= 0) return LAO_EINVAL;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > BH) nthreads = BH > 0 ? (int)BH : 1;
+  ret_job_t *jobs = (ret_job_t *)calloc((size_t)nthreads, sizeof(ret_job_t));
+  pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+  char *created = (char *)calloc((size_t)nthreads, 1);
+  if (!jobs || !tids || !created) {
+    free(jobs);
+    free(tids);
+    free(created);
+    return LAO_ENOMEM;
+  }
+  for (int w = 0; w < nthreads; ++w) {
+    ret_job_t jb = {q, k, v, S0, gamma, out, S, N, BH * w / nthreads, BH * (w + 1) / nthreads, dk, dv};
+    jobs[w] = jb;
+    /* run a worker inline if its thread cannot be started */
+    if (nthreads > 1 && pthread_create(&tids[w], NULL, retention_worker, &jobs[w]) == 0)
+      created[w] = 1;
+    else
+      retention_worker(&jobs[w]);
+  }
+  for (int w = 0; w < nthreads; ++w)
+    if (created[w]) pthread_join(tids[w], NULL);
+  free(jobs);
+  free(tids);
+  free(created);
+  return LAO_OK;
+}
