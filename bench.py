@@ -3,7 +3,8 @@
 One JSON line on rank 0.  The headline ``value`` is causal prefill
 throughput (B*H*N tokens/s) on the B=4, H=16, N=8192, d=128 bf16 workload;
 one step is one ``la_causal`` call on device-resident inputs.  The other
-forms on the hot path (global read, long-context causal prefill, the
+forms on the hot path (global read, long-context causal prefill, prefill
+continued from a carried state, retention with per-head decay, the
 recurrent decode step) are timed in the same run and reported under
 ``forms`` with their own roofline fractions.
 
@@ -280,6 +281,8 @@ def kernel_bytes(w, kernel: str) -> float:
     if kernel == "causal_main":  # all q, k, v; outputs except each head's exact leading rows; final state
         ne = min(w.N, 64)
         return w.BH * (w.N * (2 * w.dk + w.dv) * ib + (w.N - ne) * 4 * w.dv + state)
+    if kernel == "retention_main":  # all q, k, v; every output row; final S (no normalizer)
+        return w.BH * (w.N * (2 * w.dk + w.dv) * ib + w.N * 4 * w.dv + 4 * w.dk * w.dv)
     if kernel == "global_state":
         return w.BH * (w.N * (w.dk + w.dv) * ib + state)
     if kernel == "global_read":
@@ -445,6 +448,28 @@ def cpu_baseline(w, target_s: float = 12.0):
             "sample": f"{q.shape[0]} of {w.BH} heads x {q.shape[1]} tokens of {w.name}, {dt:.1f} s wall"}
 
 
+def retention_bytes(w) -> float:
+    """Algorithmic HBM bytes of one retention call: q,k,v read, fp32 out and S written."""
+    return w.BH * (w.N * (2 * w.dk + w.dv) * in_bytes(w) + w.N * 4 * w.dv + 4 * w.dk * w.dv)
+
+
+def run_retention(L, w, steps, warmup, world, stream, hbm, src):
+    """Retention prefill (per-head decays, no denominator) from the zero state."""
+    q, k, v = (t.cuda() for t in inputs.make_qkv(w, device="cuda"))
+    gamma = inputs.retention_gamma(w.H)
+    out = torch.empty(w.B, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
+    S = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device="cuda")
+    call = lambda: L.la_retention(q, k, v, gamma, out=out, S=S, stream=stream)
+    n0 = L.kernel_launches()
+    ms = time_device(call, steps, warmup, world, stream, L)
+    launches = (L.kernel_launches() - n0) // (2 * steps + warmup) * steps
+    ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
+    rl, table = dominant_roofline(L, w, steps, hbm, src, w.name)
+    return {"workload": w.name, "tokens_per_s": world * w.BH * w.N / (ms * 1e-3), "ms_per_call": ms,
+            "roofline": rl, "step_roofline": roofline(retention_bytes(w), ms, hbm, src, None),
+            "kernels": table, "gpu_launches": launches}
+
+
 def main_ours(args):
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -473,6 +498,11 @@ def main_ours(args):
             forms["causal_bf16_with_state"] = run_continue(L, wc, max(3, args.steps // 2), args.warmup, world, stream,
                                                            hbm, src)
             forms["causal_bf16_with_state"]["clocks"] = clk.summary(*LAST_WINDOW)
+            torch.cuda.empty_cache()
+        if "retention_bf16" in extras:
+            wr = rank_workload(inputs.WORKLOADS["retention_bf16"], rank)
+            forms["retention_bf16"] = run_retention(L, wr, args.steps, args.warmup, world, stream, hbm, src)
+            forms["retention_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
         if "decode_bf16" in extras:
             wd = rank_workload(inputs.WORKLOADS["decode_bf16"], rank)
@@ -532,7 +562,7 @@ def parse(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-extras", action="store_true", help="time the headline workload only")
-    ap.add_argument("--forms", default="global_bf16,causal_bf16_long,causal_bf16_with_state,decode_bf16",
+    ap.add_argument("--forms", default="global_bf16,causal_bf16_long,causal_bf16_with_state,retention_bf16,decode_bf16",
                     help="comma-separated other forms timed after the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-step-s", type=float, default=10.0, help="max CPU seconds per reference step")

@@ -104,6 +104,7 @@ static_assert(Layout::Alloc <= 232448, "shared memory budget");
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 256, kColQ = 384;
 constexpr uint32_t kAbortMisaligned = 2u;  // status bit: shared memory base not 1024-aligned
 
+
 struct TcParams {
   CUtensorMap tq, tk, tv;  // 3-D maps over [BH][N][128] bf16, box 64 x 128 x 1, 128-byte swizzle
   CUtensorMap to;          // 3-D map over the fp32 output [BH][N][128], box 32 x 128 x 1, 128-byte swizzle
@@ -119,6 +120,9 @@ struct TcParams {
   int fp_ctas, fp_range_units, fp_ranges, fp_pieces_per_cta;
   int n_exact;
   float eps;
+  // retention (decayed state, no denominator): log2 of the decay of head h % ret_H
+  int ret_H;
+  float log2g[kMaxRetentionHeads];
 };
 
 __device__ __forceinline__ float dot8(uint4 y, const float *z) {
@@ -144,6 +148,25 @@ __device__ __forceinline__ void store_row32_bf16(uint8_t *tile, int row, int col
     const float *v = reinterpret_cast<const float *>(r) + 8 * q;
     *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c)) =
         make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+  }
+}
+
+// As store_row32_bf16, as a bf16 pair: hi = bf16(x) into `hi`, lo = bf16(x - hi) into `lo`.
+__device__ __forceinline__ void store_row32_split(uint8_t *hi, uint8_t *lo, int row, int col0,
+                                                  const uint32_t (&r)[32]) {
+  const int off = (col0 >> 6) * kBlk;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c = (col0 & 63) + q * 8;
+    const float *v = reinterpret_cast<const float *>(r) + 8 * q;
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      h[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+      l[e] = pack_bf16(v[2 * e] - __uint_as_float(h[e] << 16), v[2 * e + 1] - __uint_as_float(h[e] & 0xffff0000u));
+    }
+    *reinterpret_cast<uint4 *>(hi + off + sw128_offset(row, c)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo + off + sw128_offset(row, c)) = make_uint4(l[0], l[1], l[2], l[3]);
   }
 }
 
@@ -219,6 +242,34 @@ __device__ __forceinline__ PieceRange prefix_pieces(const TcParams &p, int bh, i
   return r;
 }
 
+// Head-local end (in 64-token units) of first-pass piece `piece` of head bh.
+__device__ __forceinline__ long piece_end_units(const TcParams &p, int bh, long piece) {
+  const long L = p.fp_range_units, U = p.fp_units, C = p.fp_ctas;
+  long e;
+  if (p.fp_pieces_per_cta == 1) {
+    e = (piece + 1) * (U / C);
+  } else {
+    const long c = piece >> 1, s0 = U * c / C, e0 = U * (c + 1) / C;
+    e = (piece & 1) ? e0 : min(e0, (s0 / L + 1) * L);
+  }
+  return e - (long)bh * p.fp_ranges * L;
+}
+
+// kRet: retention instead of normalized linear attention.  With the decay
+// gamma, a chunk of C valid tokens, chunk-local rows i (query) and j (key),
+// key weights w_j = gamma^(C-1-j) and S the state before the chunk, tensor
+// memory holds A = gamma^C S and
+//   out_i = gamma^(i+1-C) (q_i A + sum_{j <= i} ((q_i . k_j) w_j) v_j)
+//   S_new = A + (w k)^T V   (then times the next chunk's gamma^C)
+// q and k are used as given, so the dot products cancel and every operand
+// that is not an input goes to the tensor cores as a bf16 hi/lo pair:
+// (q_i . k_j) w_j is split as P is; the weighted keys, formed once Q K^T has
+// read the raw ones, are split into the K tile (hi) and the consumed Q slot
+// (lo), which is reloaded only after the state update has read it (so Q has
+// one stage); the copy of A that Q reads is split into Sb (hi) and the other
+// Q slot (lo).  Every factor lies within 2^+-54 for gamma >= 0.75.  There is
+// no z, no denominator and no exact leading-token pass.
+template <bool kRet>
 __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParams p) {
   using Lay = Layout;
   constexpr int kStages = Lay::kStages;
@@ -237,7 +288,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
            *k_empty = bars + 15, *v_empty = bars + 18;
   uint64_t *s_full = bars + 21, *pp_ready = bars + 22, *o_full = bars + 23, *sb_ready = bars + 24,
            *o_free = bars + 25, *drain = bars + 26, *p_full = bars + 27, *den_ready = bars + 28,  // [2]
-           *qt_free = bars + 30;  // [2]: phi(Q) tensor-memory buffers
+           *qt_free = bars + 30,  // [2]: phi(Q) tensor-memory buffers
+           *k_ready = bars + 32;  // retention: keys weighted for the state update
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::Misc);
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
   unsigned int *status = &g_device_status;
@@ -256,7 +308,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       mbar_init(&full_k[s], 1);
       mbar_init(&full_v[s], 1);
       mbar_init(&phi_done[s], kPhiThreads);
-      mbar_init(&q_empty[s], kPhiThreads);
+      mbar_init(&q_empty[s], kRet ? 1 : kPhiThreads);  // retention: the state update's commit
       // the MMA commit plus the epilogue's 128 threads once they have read den_x[s]
       mbar_init(&k_empty[s], 129);
       mbar_init(&v_empty[s], 1);
@@ -272,6 +324,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     mbar_init(p_full, 1);
     mbar_init(&den_ready[0], 128);
     mbar_init(&den_ready[1], 128);
+    mbar_init(k_ready, kPhiThreads);
     *abort_word = 0;
     fence_barrier_init();
   }
@@ -290,15 +343,24 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       prefetch_tmap(&p.tk);
       prefetch_tmap(&p.tv);
       int issued_q = 0, issued_k = 0, issued_v = 0;
+      // Q of chunk c: stage c % 2, or (retention) always slot 0, after the previous chunk's state update
+      auto load_q = [&](int c, int tok) -> bool {
+        const int qs = kRet ? 0 : c % kStages;
+        if (kRet ? c >= 1 : c >= kStages) {
+          const uint32_t ph = kRet ? (uint32_t)(c - 1) & 1 : (uint32_t)(c / kStages - 1) & 1;
+          if (!mbar_wait(&q_empty[qs], ph, abort_word, status)) return false;
+        }
+        mbar_arrive_expect_tx(&full_q[qs], kTile);
+        tma_load_3d(sm + Lay::Q + qs * kTile, &p.tq, &full_q[qs], 0, tok, bh);
+        tma_load_3d(sm + Lay::Q + qs * kTile + kBlk, &p.tq, &full_q[qs], 64, tok, bh);
+        issued_q = c + 1;
+        return true;
+      };
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
         const uint32_t u = c / kStages;
         const int tok = (int)(t_begin + (long)c * kC);
-        if (c >= kStages && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_word, status)) break;
-        mbar_arrive_expect_tx(&full_q[s], kTile);
-        tma_load_3d(sm + Lay::Q + s * kTile, &p.tq, &full_q[s], 0, tok, bh);
-        tma_load_3d(sm + Lay::Q + s * kTile + kBlk, &p.tq, &full_q[s], 64, tok, bh);
-        issued_q = c + 1;
+        if (!kRet && !load_q(c, tok)) break;
         if (c >= kStages && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_word, status)) break;
         mbar_arrive_expect_tx(&full_k[s], kTile);
         tma_load_3d(sm + Lay::K + s * kTile, &p.tk, &full_k[s], 0, tok, bh);
@@ -309,10 +371,11 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         tma_load_3d(sm + Lay::V + s * kTile, &p.tv, &full_v[s], 0, tok, bh);
         tma_load_3d(sm + Lay::V + s * kTile + kBlk, &p.tv, &full_v[s], 64, tok, bh);
         issued_v = c + 1;
+        if (kRet && !load_q(c, tok)) break;
       }
       // every issued copy must land before shared memory is released
-      for (int c = max(0, issued_q - kStages); c < issued_q; ++c)
-        wait_drain(&full_q[c % kStages], (c / kStages) & 1, status);
+      for (int c = max(0, issued_q - (kRet ? 1 : kStages)); c < issued_q; ++c)
+        wait_drain(&full_q[kRet ? 0 : c % kStages], kRet ? (uint32_t)c & 1 : (uint32_t)(c / kStages) & 1, status);
       for (int c = max(0, issued_k - kStages); c < issued_k; ++c)
         wait_drain(&full_k[c % kStages], (c / kStages) & 1, status);
       for (int c = max(0, issued_v - kStages); c < issued_v; ++c)
@@ -326,11 +389,15 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       constexpr uint32_t iKM = idesc_bf16_f32(128, 128, 0, 1);
       constexpr uint32_t iMM = idesc_bf16_f32(128, 128, 1, 1);
       const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V), sSb = smem_u32(sm + Lay::Sb);
+      // retention: low parts of the weighted keys (Q slot 0) and of the state copy (Q slot 1)
+      const uint32_t sKlo = smem_u32(sm + Lay::Q), sSblo = smem_u32(sm + Lay::Q + kTile);
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
         const uint32_t u = c / kStages;
         if (!mbar_wait(&phi_done[s], u & 1, abort_word, status)) break;
         if (!mbar_wait(&full_v[s], u & 1, abort_word, status)) break;
+        // retention: the keys reach Q K^T as loaded (no in-place pass before it)
+        if (kRet && !mbar_wait(&full_k[s], u & 1, abort_word, status)) break;
         const uint32_t k = sK + s * kTile, v = sV + s * kTile;
         const uint32_t tQ = tmem + kColQ + 64 * (c & 1);
         // the single P tile is free once the previous chunk's P V has completed
@@ -342,14 +409,24 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         mma_commit(p_full);
         // S += K^T V once the previous state has been copied out
         if (!mbar_wait(sb_ready, c & 1, abort_word, status)) break;
+        if (kRet && !mbar_wait(k_ready, c & 1, abort_word, status)) break;  // the keys' state weights
         tc_fence_after();
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tS, mndesc(k, ks), mndesc(v, ks), iMM, 1);
+        if (kRet) {
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tS, mndesc(sKlo, ks), mndesc(v, ks), iMM, 1);
+          mma_commit(&q_empty[0]);  // the Q slot may take the next chunk's Q
+        }
         // O = Q bf16(S_prev) once the previous outputs have been read
         if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status)) break;
         tc_fence_after();
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSb, ks), iKM, ks > 0);
+        if (kRet) {
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSblo, ks), iKM, 1);
+        }
         mma_commit(s_full);
         mma_commit(&qt_free[c & 1]);
         mma_commit(&k_empty[s]);
@@ -375,8 +452,9 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     const int quarter = warp & 3;
     const int half = (warp - kWarpPhi) >> 2;
     const int row = quarter * 32 + lane;
-    if (seg > 0) pdl_wait();  // the first pass's pieces are complete and visible
-    if (pt < kD) {
+    const float lg = kRet ? p.log2g[bh % max(p.ret_H, 1)] : 0.f;  // retention: log2 gamma
+    if (seg > 0 && !kRet) pdl_wait();  // the first pass's pieces are complete and visible
+    if (!kRet && pt < kD) {
       // first-pass pieces start from zero; a segment starts from the caller's state plus them
       float z = p.z0 ? p.z0[(long)bh * kD + pt] : 0.f;
       if (seg > 0) {
@@ -386,6 +464,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       zs[pt] = z;
       den_x[pt] = den_x[kC + pt] = 0.f;
     }
+    if (kRet && pt < kD) den_x[pt] = den_x[kC + pt] = 0.f;
     named_bar(kBarPhi, kPhiThreads);
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % kStages;
@@ -393,14 +472,14 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       const int tv = (int)min((long)kC, t_end - (t_begin + (long)c * kC));
       uint8_t *Kt = sm + Lay::K + s * kTile;
       bool ok = mbar_wait(&full_k[s], u & 1, abort_word, status);
-      ok = ok && mbar_wait(&full_q[s], u & 1, abort_word, status);
+      ok = ok && mbar_wait(&full_q[kRet ? 0 : s], kRet ? (uint32_t)c & 1 : u & 1, abort_word, status);
       // this chunk's phi(Q) buffer is free once Q K^T and Q S of the chunk two back have completed
       if (ok && c >= 2) ok = mbar_wait(&qt_free[c & 1], ((c >> 1) - 1) & 1, abort_word, status);
       if (bar_or(kBarPhi, kPhiThreads, !ok)) break;
       {
         // phi(Q) half row -> packed bf16 pairs -> tensor memory; the partial phi(q).z_prev
         // from the same rounded values meets its other half in shared memory
-        const uint8_t *Qb = sm + Lay::Q + s * kTile + half * kBlk;
+        const uint8_t *Qb = sm + Lay::Q + (kRet ? 0 : s) * kTile + half * kBlk;
         const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + 64 * (c & 1) + 32 * half;
         float dx = 0.f;
 #pragma unroll 1
@@ -411,42 +490,65 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const uint4 y = phi8(xv[e]);
+            const uint4 y = kRet ? xv[e] : phi8(xv[e]);
             w[4 * e] = y.x, w[4 * e + 1] = y.y, w[4 * e + 2] = y.z, w[4 * e + 3] = y.w;
-            dx += dot8(y, zs + half * 64 + g * 32 + e * 8);
+            if (!kRet) dx += dot8(y, zs + half * 64 + g * 32 + e * 8);
           }
           tmem_st16(tq + 16 * g, w);
         }
-        atomicAdd(&den_x[s * kC + row], dx);
-        mbar_arrive(&q_empty[s]);  // raw Q consumed
+        if (!kRet) {
+          atomicAdd(&den_x[s * kC + row], dx);
+          mbar_arrive(&q_empty[s]);  // raw Q consumed
+        }
       }
-      {
-        // phi(K) half row in place (all loads of a step first: the in-place stores would order them)
-        uint8_t *Kb = Kt + half * kBlk;
+      // phi(K) half row in place (all loads of a step first: the in-place stores would order them);
+      // retention: the raw keys times their state weight w_row, once Q K^T has read them, as the
+      // high parts in place and the low parts in the consumed Q slot
+      auto transform_k = [&](float wk) {
+        uint8_t *Kb = Kt + half * kBlk, *Lb = sm + Lay::Q + half * kBlk;
 #pragma unroll 1
         for (int g = 0; g < 2; ++g) {
           uint4 kv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) kv[e] = *reinterpret_cast<const uint4 *>(Kb + sw128_offset(row, g * 32 + e * 8));
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<uint4 *>(Kb + sw128_offset(row, g * 32 + e * 8)) = phi8(kv[e]);
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t off = sw128_offset(row, g * 32 + e * 8);
+            if (kRet) {
+              uint4 hi, lo;
+              split8(kv[e], wk, hi, lo);
+              *reinterpret_cast<uint4 *>(Kb + off) = hi;
+              *reinterpret_cast<uint4 *>(Lb + off) = lo;
+            } else {
+              *reinterpret_cast<uint4 *>(Kb + off) = phi8(kv[e]);
+            }
+          }
         }
-      }
+      };
+      if (!kRet) transform_k(1.f);
       named_bar(kBarPhi, kPhiThreads);  // every K row transformed; every read of zs done
-      // column sums of phi(K) over the valid rows (bf16 values, as the MMA sees them)
-      float s0, s1;
-      const int col = column_pair_sums_8w(Kt, warp - kWarpPhi, lane, tv, s0, s1);
-      if (lane < 8) {
-        zs[col] += s0;
-        zs[col + 1] += s1;
+      if (!kRet) {
+        // column sums of phi(K) over the valid rows (bf16 values, as the MMA sees them)
+        float s0, s1;
+        const int col = column_pair_sums_8w(Kt, warp - kWarpPhi, lane, tv, s0, s1);
+        if (lane < 8) {
+          zs[col] += s0;
+          zs[col + 1] += s1;
+        }
       }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&phi_done[s]);
+      if (kRet) {
+        const bool okp = mbar_wait(p_full, c & 1, abort_word, status);  // Q K^T has read the raw keys
+        if (bar_or(kBarPhi, kPhiThreads, !okp)) break;
+        transform_k(exp2f((float)(tv - 1 - row) * lg));
+        fence_async_smem();
+        mbar_arrive(k_ready);
+      }
       named_bar(kBarPhi, kPhiThreads);  // z complete before the next chunk reads it
     }
-    if (!*abort_word && pt < kD) {
+    if (!kRet && !*abort_word && pt < kD) {
       if (last_seg) p.z_out[(long)bh * kD + pt] = zs[pt];
     }
   } else if (warp < kWarpOut) {
@@ -460,31 +562,41 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       uint8_t *Sb = sm + Lay::Sb;
       if (seg > 0) pdl_wait();  // the first pass's pieces are complete and visible
       // initial state: caller's state plus the first-pass pieces before this segment
+      // (retention: each decayed over the tokens from its end to the segment start)
+      // (retention: tensor memory holds the state times gamma^C of the chunk about to be read)
       const PieceRange pr = seg > 0 ? prefix_pieces(p, bh, seg) : PieceRange{0, -1};
+      const float lg = kRet ? p.log2g[bh % max(p.ret_H, 1)] : 0.f;
+      const float c0 = (float)min((long)kC, t_end - t_begin);
+      if (kRet) den_s[T] = exp2f((float)(kC - 1 - T) * lg);  // key weights gamma^(127-j), in the denominators' slot
       for (int cb = 0; cb < 4; ++cb) {
         float v[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = 0.f;
         if (p.S0) {
           const float4 *src = reinterpret_cast<const float4 *>(p.S0 + ((long)bh * kD + T) * kD + cb * 32);
+          const float f = kRet ? exp2f(((float)t_begin + c0) * lg) : 1.f;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float4 x = src[e];
-            v[4 * e] += x.x, v[4 * e + 1] += x.y, v[4 * e + 2] += x.z, v[4 * e + 3] += x.w;
+            v[4 * e] += f * x.x, v[4 * e + 1] += f * x.y, v[4 * e + 2] += f * x.z, v[4 * e + 3] += f * x.w;
           }
         }
         for (long piece = pr.first; piece <= pr.last; ++piece) {
           const float4 *src = reinterpret_cast<const float4 *>(p.part_S + (piece * kD + T) * kD + cb * 32);
+          const float f = kRet ? exp2f(((float)(t_begin - 64 * piece_end_units(p, bh, piece)) + c0) * lg) : 1.f;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float4 x = src[e];
-            v[4 * e] += x.x, v[4 * e + 1] += x.y, v[4 * e + 2] += x.z, v[4 * e + 3] += x.w;
+            v[4 * e] += f * x.x, v[4 * e + 1] += f * x.y, v[4 * e + 2] += f * x.z, v[4 * e + 3] += f * x.w;
           }
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(v[e]);
         tmem_st32(tl + kColS + cb * 32, r);
-        store_row32_bf16(Sb, T, cb * 32, r);
+        if (kRet)
+          store_row32_split(Sb, sm + Lay::Q + kTile, T, cb * 32, r);
+        else
+          store_row32_bf16(Sb, T, cb * 32, r);
       }
       fence_async_smem();
       tc_fence_before();
@@ -503,6 +615,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
           break;
         }
         tc_fence_after();
+        // retention: key j's weight gamma^(tv-1-j) = table[j] * gamma^(tv-128)
+        const float wc = kRet ? exp2f((float)(tv - kC) * lg) : 1.f;
         float den = den_x[s * kC + T];
         den_x[s * kC + T] = 0.f;  // the feature-map warps accumulate the next use of this slot
         mbar_arrive(&k_empty[s]);
@@ -523,8 +637,13 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
 #pragma unroll
               for (int m = 0; m < 8; ++m) {
                 const int j = cb * 32 + g * 16 + 2 * m;
-                const float p0 = (j <= T && j < tv) ? __uint_as_float(r[g * 16 + 2 * m]) : 0.f;
-                const float p1 = (j + 1 <= T && j + 1 < tv) ? __uint_as_float(r[g * 16 + 2 * m + 1]) : 0.f;
+                float p0 = (j <= T && j < tv) ? __uint_as_float(r[g * 16 + 2 * m]) : 0.f;
+                float p1 = (j + 1 <= T && j + 1 < tv) ? __uint_as_float(r[g * 16 + 2 * m + 1]) : 0.f;
+                if (kRet) {
+                  const float2 wj = *reinterpret_cast<const float2 *>(den_s + j);
+                  p0 *= wj.x * wc;
+                  p1 *= wj.y * wc;
+                }
                 const uint32_t hw = pack_bf16(p0, p1);
                 const float h0 = __uint_as_float(hw << 16), h1 = __uint_as_float(hw & 0xffff0000u);
                 const uint32_t lw = pack_bf16(p0 - h0, p1 - h1);
@@ -539,7 +658,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
           tmem_st32(tP + cb * 32, r);
         }
         den = (den + rs) + p.eps;
-        den_s[(c & 1) * kC + T] = den;
+        if (!kRet) den_s[(c & 1) * kC + T] = den;
         tc_fence_before();
         mbar_arrive(pp_ready);
         mbar_arrive(&den_ready[c & 1]);
@@ -550,10 +669,20 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
           break;
         }
         tc_fence_after();
+        // retention: the state times the next chunk's gamma^C, in place, before the copy
+        // (after the last chunk tensor memory keeps the final state itself)
+        const float gC = kRet && c + 1 < nchunks ? exp2f((float)min((long)kC, t_end - tok - kC) * lg) : 1.f;
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           tmem_ld32(tl + kColS + cb * 32, r);
-          store_row32_bf16(Sb, T, cb * 32, r);
+          if (kRet) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * gC);
+            if (c + 1 < nchunks) tmem_st32(tl + kColS + cb * 32, r);
+            store_row32_split(Sb, sm + Lay::Q + kTile, T, cb * 32, r);
+          } else {
+            store_row32_bf16(Sb, T, cb * 32, r);
+          }
         }
         fence_async_smem();
         tc_fence_before();
@@ -578,6 +707,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     const int T = quarter * 32 + lane;  // TMEM lane = chunk row
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     uint32_t r[32], r2[32];
+    const float lg = kRet ? p.log2g[bh % max(p.ret_H, 1)] : 0.f;  // retention: log2 gamma
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % kStages;
       const long tok = t_begin + (long)c * kC;
@@ -585,7 +715,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
                mbar_wait(&den_ready[c & 1], (c >> 1) & 1, abort_word, status);
       if (bar_or(kBarOut, 128, !w)) break;
       tc_fence_after();
-      const float inv = 1.f / den_s[(c & 1) * kC + T];
+      // normalizer, or (retention) the row's decay gamma^(T+1-C)
+      const float inv = kRet ? exp2f((float)(T + 1 - min((long)kC, t_end - tok)) * lg) : 1.f / den_s[(c & 1) * kC + T];
       // normalised rows -> the V tile of this stage (free: P V has completed) as two
       // [128 x 32] fp32 swizzled boxes per half of the columns -> TMA stores.  Rows past
       // the sequence end are clipped by the store; the leading exact rows are rewritten later.
@@ -687,15 +818,16 @@ bool make_out_map(CUtensorMap *m, void *base, long BH, long N, uint32_t rows) {
          CUDA_SUCCESS;
 }
 
+template <bool kRet>
 cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bool pdl) {
   static std::once_flag once;
   static cudaError_t attr_err;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(causal_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(causal_tc_kernel<kRet>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)Layout::Alloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  LaunchTimer timer(kKCausalMain, stream);
+  LaunchTimer timer(kRet ? kKRetentionMain : kKCausalMain, stream);
   // pdl: may start while the previous kernel of the stream (the first pass) still runs
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -707,7 +839,7 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bo
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, causal_tc_kernel, tp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, causal_tc_kernel<kRet>, tp);
   if (e == cudaSuccess) e = cudaGetLastError();
   timer.done(e);
   if (e == cudaSuccess) {
@@ -715,8 +847,8 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bo
   } else if (getenv("LA_DEBUG")) {
     cudaFuncAttributes fa;
     int blocks = -1;
-    cudaFuncGetAttributes(&fa, causal_tc_kernel);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, causal_tc_kernel, kThreads, Layout::Alloc);
+    cudaFuncGetAttributes(&fa, causal_tc_kernel<kRet>);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, causal_tc_kernel<kRet>, kThreads, Layout::Alloc);
     fprintf(stderr,
             "linattn: causal_tc_kernel launch failed (%s): regs %d, max threads %d, static smem %zu, "
             "max dynamic smem %d, requested dynamic %u, threads %d, occupancy %d\n",
@@ -737,14 +869,18 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bo
 //   3. the exact pass over each head's leading tokens, which reads nothing the
 //      main pass writes and so runs beside it; its last CTA waits for pass 2,
 //      so that the stream's next work follows all three.
+// Retention (tp.ret_H > 0) runs passes 1 and 2 only: its segments past the
+// first wait for pass 1, so pass 2 completes after it.
 cudaError_t launch_passes(const Problem &p, const TcParams &tp, const float *S0, const float *z0) {
   cudaError_t e = cudaSuccess;
-  const bool split = tp.nseg > 1;
+  const bool split = tp.nseg > 1, ret = tp.ret_H > 0;
   if (split)
     e = launch_range_states(p, tp.seg_len, tp.fp_ranges, tp.fp_ctas, tp.fp_pieces_per_cta, tp.part_S, tp.part_z,
-                            kKCausalState);
-  if (e == cudaSuccess) e = launch_kernel(tp, dim3((unsigned)tp.nseg, (unsigned)p.BH), p.stream, split);
-  if (e == cudaSuccess) e = launch_causal_exact_head(p, tp.n_exact, S0, z0, true);
+                            ret ? kKRetentionState : kKCausalState, ret ? tp.log2g : nullptr, tp.ret_H);
+  const dim3 grid((unsigned)tp.nseg, (unsigned)p.BH);
+  if (e == cudaSuccess)
+    e = ret ? launch_kernel<true>(tp, grid, p.stream, split) : launch_kernel<false>(tp, grid, p.stream, split);
+  if (e == cudaSuccess && !ret) e = launch_causal_exact_head(p, tp.n_exact, S0, z0, true);
   return e;
 }
 
@@ -804,7 +940,10 @@ void set_first_pass(TcParams &tp, const Problem &p, const Partition &t) {
   tp.fp_pieces_per_cta = (int)t.pieces_per_cta;
 }
 
-cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
+// One call of the tensor-core path: normalized attention (log2g null) or
+// retention with head h's decay 2^log2g[h % ret_H].
+cudaError_t launch_tc(const Problem &p, bool from_state, const float *log2g, int ret_H) {
+  const bool ret = log2g != nullptr;
   const DeviceInfo &di = device_info(-1);
   const long sms = std::max(1, di.sm_count);
   const Partition t = plan_partition(p, sms, 2 * sms);
@@ -826,14 +965,14 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
     float *Sc = part_z + (size_t)nparts * kD;
     float *zc = Sc + (size_t)p.BH * kD * kD;
     e = cudaMemcpyAsync(Sc, p.S, sizeof(float) * p.BH * kD * kD, cudaMemcpyDeviceToDevice, p.stream);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !ret)
       e = cudaMemcpyAsync(zc, p.z, sizeof(float) * p.BH * kD, cudaMemcpyDeviceToDevice, p.stream);
     if (e != cudaSuccess) {
       cudaFreeAsync(scratch, p.stream);
       return e;
     }
     S0 = Sc;
-    z0 = zc;
+    z0 = ret ? nullptr : zc;
   }
 
   TcParams tp;
@@ -853,8 +992,10 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
   tp.part_z = part_z;
   tp.N = p.N;
   set_first_pass(tp, p, t);
-  tp.n_exact = (int)std::min<long>(p.N, kExact);
+  tp.n_exact = ret ? 0 : (int)std::min<long>(p.N, kExact);
   tp.eps = p.eps;
+  tp.ret_H = ret ? ret_H : 0;
+  for (int h = 0; ret && h < ret_H; ++h) tp.log2g[h] = log2g[h];
 
   e = launch_passes(p, tp, S0, z0);
   if (scratch) {
@@ -862,6 +1003,13 @@ cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
     if (e == cudaSuccess) e = f;
   }
   return e;
+}
+
+cudaError_t launch_causal_tc(const Problem &p, bool from_state) { return launch_tc(p, from_state, nullptr, 0); }
+
+cudaError_t launch_retention_tc(const Problem &p, bool from_state, const float *log2g, int H) {
+  if (!log2g || H < 1 || H > kMaxRetentionHeads) return cudaErrorInvalidValue;
+  return launch_tc(p, from_state, log2g, H);
 }
 
 // ---------------------------------------------------------------------------

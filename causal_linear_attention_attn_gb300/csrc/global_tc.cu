@@ -82,23 +82,27 @@ constexpr uint32_t kHalf = 8192;    // [64 rows x 128 bytes], 128-byte swizzled
 
 // Stages are 64-token (d = 128) or 128-token (d = 64, two 64-token sub-tiles)
 // K and V tiles of 16 KB each: a stage is held only for its phi and four
-// MMAs, so most of the six stages are loads in flight.
-template <int D>
+// MMAs, so most of the six stages are loads in flight.  Retention (kRet)
+// adds the low bf16 parts of the weighted keys per stage, in four stages.
+template <int D, bool kRet = false>
 struct BuildLayout {
+  static constexpr int kStages = kRet ? 4 : kBuildStages;
   static constexpr uint32_t kStage = 2 * kHalf;  // one K or V stage: 16 KB
   static constexpr uint32_t K = 0;
-  static constexpr uint32_t V = K + kBuildStages * kStage;
+  static constexpr uint32_t V = K + kStages * kStage;
+  static constexpr uint32_t Klo = V + kStages * kStage;  // retention only
   static constexpr int kZ = D == 64 ? 8 : 16;  // column sums per feature-map thread
-  static constexpr uint32_t Zred = V + kBuildStages * kStage;  // [256 threads][kZ] column sums, then z partial
+  static constexpr uint32_t Zred = Klo + (kRet ? kStages * kStage : 0);  // [256 threads][kZ] column sums, then z
   static constexpr uint32_t Bars = Zred + kBuildPhi * kZ * 4 + D * 4;
-  static constexpr int kNumBars = 3 * kBuildStages + 2;
+  static constexpr int kNumBars = 3 * kStages + 2;
   static constexpr uint32_t Misc = Bars + kNumBars * 8;
   static constexpr uint32_t Bytes = Misc + 16;
-  // partial state [128 rows][D + 4] fp32, written over the K stages
+  // partial state [128 rows][D + 4] fp32, written over the K stages (whole-sequence mode)
   static constexpr int kPStride = D + 4;
-  static_assert(128 * kPStride * 4 <= kBuildStages * kStage, "partial state fits over the K stages");
+  static_assert(kRet || 128 * kPStride * 4 <= kStages * kStage, "partial state fits over the K stages");
 };
 static_assert(BuildLayout<128>::Bytes <= 232448, "shared memory budget");
+static_assert(BuildLayout<128, true>::Bytes <= 232448, "shared memory budget");
 
 struct BuildParams {
   CUtensorMap tk, tv;  // [BH][N][D] bf16, box 64 x 64 x 1, 128-byte swizzle
@@ -115,6 +119,10 @@ struct BuildParams {
   int units;  // stage units per head: 128 tokens (d = 64) or 64 (d = 128)
   long units_total;
   int range_units, ranges_per_head, pieces_per_cta;
+  // Retention (range mode, kRet): key rows of a piece are weighted by gamma^(piece end - 1 - t)
+  // with head bh's gamma = 2^log2g[bh % ret_H]; the key sums are not formed.
+  int ret_H;
+  float log2g[kMaxRetentionHeads];
 };
 
 // Walks stage units as (head, unit in head) pairs without per-unit division.
@@ -130,9 +138,10 @@ struct UnitWalk {
   }
 };
 
-template <int D>
+template <int D, bool kRet = false>
 __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid_constant__ BuildParams p) {
-  using Lay = BuildLayout<D>;
+  using Lay = BuildLayout<D, kRet>;
+  constexpr int kBuildStages = Lay::kStages;
   constexpr int kUnit = D == 64 ? 128 : 64;
   constexpr int kPS = Lay::kPStride;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t iS = idesc_bf16_f32(128, 128, 1, 1);
-      const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V);
+      const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V), sKlo = smem_u32(sm + Lay::Klo);
       for (int i = 0; i < nu; ++i) {
         const int s = i % kBuildStages;
         if (!mbar_wait(&phi_done[s], (i / kBuildStages) & 1, abort_word, status)) break;
@@ -232,9 +241,13 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
         const uint32_t d = tS + (i >= nb ? 128u : 0u);
         const bool first = i == 0 || i == nb;  // a piece's first unit overwrites its accumulator
 #pragma unroll 1
-        for (int ks = 0; ks < 4; ++ks)  // both operands MN-major: 16 tokens per step, 64-wide blocks 8 KB apart
+        for (int ks = 0; ks < 4; ++ks) {  // both operands MN-major: 16 tokens per step, 64-wide blocks 8 KB apart
           mma_bf16(d, sw128_desc(k + ks * 2048, kHalf, 1024), sw128_desc(v + ks * 2048, kHalf, 1024), iS,
                    (!first || ks > 0) ? 1u : 0u);
+          if (kRet)  // the weighted keys' low parts
+            mma_bf16(d, sw128_desc(sKlo + s * Lay::kStage + ks * 2048, kHalf, 1024),
+                     sw128_desc(v + ks * 2048, kHalf, 1024), iS, 1u);
+        }
         mma_commit(&empty[s]);
       }
       mma_commit(acc_full);
@@ -262,20 +275,39 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
       }
       uint8_t *k = sm + Lay::K + s * Lay::kStage;
       const long tok0 = w.u * kUnit;
-      // phi in place; the rounded values also go into the column sums of this unit's piece
-      auto phi_sum = [&](float *za) {
-        phi_chunks<4, kBuildPhi>(k, pt, [&](int j, int ch, uint4 x) {
-          const int row = ch >> 3;  // 0..127 over the two blocks
-          const long tok = tok0 + (D == 64 ? row : (row & 63));
-          const uint4 y = tok < p.N ? phi8(x) : make_uint4(0u, 0u, 0u, 0u);  // rows past the end add nothing
-          add8_bf16(za + (D == 64 ? 0 : 8 * (j >> 1)), y);
-          return y;
-        });
-      };
-      if (i < nb)
-        phi_sum(zacc0);
-      else
-        phi_sum(zacc1);
+      if constexpr (kRet) {
+        // retention: row t of the unit weighted by gamma^(tokens from t to the piece end - 1), as a
+        // bf16 pair: the high parts in place, the low parts in this stage's Klo tile
+        const float lg = p.log2g[w.h % max(p.ret_H, 1)];
+        const float to_end = (float)(kUnit * ((i < nb ? nb : nu) - i));
+        uint4 *kt = reinterpret_cast<uint4 *>(k), *lt = reinterpret_cast<uint4 *>(sm + Lay::Klo + s * Lay::kStage);
+        uint4 x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = kt[pt + kBuildPhi * j];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ch = pt + kBuildPhi * j, row = (ch >> 3) & 63;  // the unit's token row
+          uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;          // rows past the end add nothing
+          if (tok0 + row < p.N) split8(x[j], exp2f((to_end - 1.f - (float)row) * lg), hi, lo);
+          kt[ch] = hi;
+          lt[ch] = lo;
+        }
+      } else {
+        // phi in place; the rounded values also go into the column sums of this unit's piece
+        auto phi_sum = [&](float *za) {
+          phi_chunks<4, kBuildPhi>(k, pt, [&](int j, int ch, uint4 x) {
+            const int row = ch >> 3;  // 0..127 over the two blocks
+            const long tok = tok0 + (D == 64 ? row : (row & 63));
+            const uint4 y = tok < p.N ? phi8(x) : make_uint4(0u, 0u, 0u, 0u);  // rows past the end add nothing
+            add8_bf16(za + (D == 64 ? 0 : 8 * (j >> 1)), y);
+            return y;
+          });
+        };
+        if (i < nb)
+          phi_sum(zacc0);
+        else
+          phi_sum(zacc1);
+      }
       fence_async_smem();
       mbar_arrive(&phi_done[s]);
     }
@@ -658,11 +690,11 @@ cudaError_t set_smem_once(F *kernel, uint32_t bytes, std::once_flag &once, cudaE
   return err;
 }
 
-template <int D>
+template <int D, bool kRet = false>
 cudaError_t build_smem() {
   static std::once_flag once;
   static cudaError_t err;
-  return set_smem_once(global_build_tc<D>, BuildLayout<D>::Bytes, once, err);
+  return set_smem_once(global_build_tc<D, kRet>, BuildLayout<D, kRet>::Bytes, once, err);
 }
 
 template <int D>
@@ -684,6 +716,7 @@ cudaError_t launch_t(const Problem &p) {
   bp.units = (int)((p.N + kUnit - 1) / kUnit);
   bp.units_total = 0;
   bp.range_units = bp.ranges_per_head = bp.pieces_per_cta = 0;
+  bp.ret_H = 0;
   // cluster size: a power of two <= 8 so that the build covers the SMs about once, >= 8 units a CTA
   int G = 1;
   while (G < 8 && p.BH * (2 * G) <= sms && bp.units / (2 * G) >= 8) G *= 2;
@@ -756,9 +789,9 @@ bool global_tc_supported(const Problem &p) {
 cudaError_t launch_global_tc(const Problem &p) { return p.dk == 64 ? launch_t<64>(p) : launch_t<128>(p); }
 
 cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_per_head, int ctas, int pieces_per_cta,
-                                float *piece_S, float *piece_z, int kernel_id) {
+                                float *piece_S, float *piece_z, int kernel_id, const float *log2g, int ret_H) {
   if (p.dt != LA_BF16 || p.dk != 128 || p.dv != 128 || range_tokens % 64 != 0 || ranges_per_head < 1 || ctas < 1 ||
-      pieces_per_cta < 1 || pieces_per_cta > 2)
+      pieces_per_cta < 1 || pieces_per_cta > 2 || (log2g && (ret_H < 1 || ret_H > kMaxRetentionHeads)))
     return cudaErrorInvalidValue;
   const long range_units = range_tokens / 64;
   const long units_total = (long)p.BH * ranges_per_head * range_units;
@@ -779,10 +812,15 @@ cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_
   bp.range_units = (int)range_units;
   bp.ranges_per_head = ranges_per_head;
   bp.pieces_per_cta = pieces_per_cta;
-  cudaError_t e = build_smem<128>();
+  bp.ret_H = log2g ? ret_H : 0;
+  for (int h = 0; h < kMaxRetentionHeads; ++h) bp.log2g[h] = log2g && h < ret_H ? log2g[h] : 0.f;
+  cudaError_t e = log2g ? build_smem<128, true>() : build_smem<128>();
   if (e != cudaSuccess) return e;
   LaunchTimer timer(kernel_id, p.stream);
-  global_build_tc<128><<<(unsigned)ctas, kBuildThreads, BuildLayout<128>::Bytes, p.stream>>>(bp);
+  if (log2g)
+    global_build_tc<128, true><<<(unsigned)ctas, kBuildThreads, BuildLayout<128, true>::Bytes, p.stream>>>(bp);
+  else
+    global_build_tc<128><<<(unsigned)ctas, kBuildThreads, BuildLayout<128>::Bytes, p.stream>>>(bp);
   e = cudaGetLastError();
   timer.done(e);
   if (e == cudaSuccess) count_launch();

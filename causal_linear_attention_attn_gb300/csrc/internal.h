@@ -36,6 +36,8 @@ cudaError_t launch_causal_exact_head(const Problem &p, long n_exact, const float
 // Tensor-core chunked causal path (bf16, d_k = d_v = 128, sm_103).
 bool causal_tc_supported(const Problem &p);
 cudaError_t launch_causal_tc(const Problem &p, bool from_state);
+// Retention on the same path: head bh decays by 2^log2g[bh % H] (host array, H <= 128).
+cudaError_t launch_retention_tc(const Problem &p, bool from_state, const float *log2g, int H);
 
 // Allocation-free tensor-core causal pass from the zero state: the first
 // pass's partial states use a fixed device array instead of an allocation.
@@ -62,8 +64,13 @@ cudaError_t read_and_clear_global_tc_status(unsigned int *value);
 // piece_S[piece][128][128], piece_z[piece][128].  range_tokens % 64 == 0.  With
 // pieces_per_cta == 1 the runs must divide the ranges evenly; CTA c then writes
 // piece c only.
+// Retention: per-head decays gamma_h carried in launch parameters, at most this many heads.
+constexpr int kMaxRetentionHeads = 128;
+
+// log2g (host array of ret_H values, or null): retention weights instead of phi and key sums.
 cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_per_head, int ctas, int pieces_per_cta,
-                                float *piece_S, float *piece_z, int kernel_id);
+                                float *piece_S, float *piece_z, int kernel_id, const float *log2g = nullptr,
+                                int ret_H = 0);
 
 // Read and clear the device status word (bounded-wait timeouts).
 cudaError_t read_and_clear_device_status(unsigned int *value);
@@ -86,7 +93,9 @@ enum KernelId : int {
   kKGlobalState = 4,
   kKGlobalRead = 5,
   kKDecode = 6,
-  kKNumKernels = 7
+  kKRetentionMain = 7,
+  kKRetentionState = 8,
+  kKNumKernels = 9
 };
 
 // While profiling is on (la_profile_enable), brackets one launch with a CUDA

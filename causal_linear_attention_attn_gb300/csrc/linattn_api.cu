@@ -217,6 +217,47 @@ la_status la_causal_with_state(const void *q, const void *k, const void *v, floa
   return causal_impl(q, k, v, out, S, z, B, H, N, d_k, d_v, eps, dt, stream, true);
 }
 
+static la_status retention_impl(const void *q, const void *k, const void *v, float *out, float *S,
+                                const float *gamma, int B, int H, int N, int d_k, int d_v, la_dtype dt,
+                                void *stream, bool from_state) {
+  if (B < 0 || H < 0 || N < 0 || d_k <= 0 || d_v <= 0) return LA_ERR_INVALID_VALUE;
+  const long BH = (long)B * H;
+  if (BH > 0x7fffffffL) return LA_ERR_INVALID_VALUE;
+  if (BH == 0) return LA_OK;
+  if (!S || !gamma || (N > 0 && (!q || !k || !v || !out))) return LA_ERR_INVALID_VALUE;
+  for (int h = 0; h < H; ++h)
+    if (!std::isfinite(gamma[h])) return LA_ERR_INVALID_VALUE;
+  if (dt != LA_BF16 || d_k != 128 || d_v != 128 || H > la::kMaxRetentionHeads) return LA_ERR_UNSUPPORTED;
+  for (int h = 0; h < H; ++h)
+    if (!(gamma[h] >= 0.75f && gamma[h] <= 1.f)) return LA_ERR_UNSUPPORTED;
+  const void *ptrs[5] = {q, k, v, out, S};
+  for (const void *ptr : ptrs)
+    if (ptr && !la::aligned16(ptr)) return LA_ERR_MISALIGNED;
+  int dev;
+  la_status st = la::current_device(&dev);
+  if (st != LA_OK) return st;
+  Problem p{q, k, v, out, S, nullptr, (int)BH, (long)N, d_k, d_v, 0.f, dt, (cudaStream_t)stream};
+  if (N == 0) {
+    if (from_state) return LA_OK;
+    return la::from_cuda(cudaMemsetAsync(S, 0, sizeof(float) * (size_t)BH * d_k * d_v, p.stream));
+  }
+  if (!la::causal_tc_supported(p)) return LA_ERR_UNSUPPORTED;
+  float log2g[la::kMaxRetentionHeads];
+  for (int h = 0; h < H; ++h) log2g[h] = (float)std::log2((double)gamma[h]);
+  return la::from_cuda(la::launch_retention_tc(p, from_state, log2g, H));
+}
+
+la_status la_retention(const void *q, const void *k, const void *v, float *out, float *S, const float *gamma,
+                       int B, int H, int N, int d_k, int d_v, la_dtype dt, void *stream) {
+  return retention_impl(q, k, v, out, S, gamma, B, H, N, d_k, d_v, dt, stream, false);
+}
+
+la_status la_retention_with_state(const void *q, const void *k, const void *v, float *out, float *S,
+                                  const float *gamma, int B, int H, int N, int d_k, int d_v, la_dtype dt,
+                                  void *stream) {
+  return retention_impl(q, k, v, out, S, gamma, B, H, N, d_k, d_v, dt, stream, true);
+}
+
 la_status la_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(la::g_prof_mu);
   if (on) {

@@ -328,6 +328,31 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&r);
 }
 
+// Eight packed bf16 values times f, rounded back to bf16.
+__device__ __forceinline__ uint4 scale8(uint4 x, float f) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    o[e] = pack_bf16(__uint_as_float(w[e] << 16) * f, __uint_as_float(w[e] & 0xffff0000u) * f);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Eight packed bf16 values times f as a bf16 pair: hi = bf16(x f), lo = bf16(x f - hi),
+// so that hi + lo carries x f to about 2^-17 relative.
+__device__ __forceinline__ void split8(uint4 x, float f, uint4 &hi, uint4 &lo) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = __uint_as_float(w[e] << 16) * f, b = __uint_as_float(w[e] & 0xffff0000u) * f;
+    h[e] = pack_bf16(a, b);
+    l[e] = pack_bf16(a - __uint_as_float(h[e] << 16), b - __uint_as_float(h[e] & 0xffff0000u));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 // Byte offset of fp32 element (row, col) in a [128 rows x 32] fp32 box written
 // with 128-byte rows and the 128-byte swizzle (16-byte chunks XOR row mod 8).
 __device__ __forceinline__ uint32_t sw128_offset_f32(uint32_t row, uint32_t col) {

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the five workloads (no attention arithmetic here).
+"""Seeded synthetic inputs for the six workloads (no attention arithmetic here).
 
 Every tensor is drawn as float32 ``torch.randn`` from a seeded generator,
 multiplied by its scale, then rounded to the workload's input dtype
@@ -23,7 +23,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    form: str  # "causal", "global" or "decode"
+    form: str  # "causal", "global", "retention" or "decode"
     B: int
     H: int
     N: int
@@ -59,11 +59,24 @@ WORKLOADS = {
                  note="causal prefill bf16, B=4 H=16 N=8192 d=128, q,k ~ N(0,1)/sqrt(128), v ~ N(0,1)"),
         Workload("causal_bf16_long", "causal", 1, 32, 131072, 128, 128, "bf16", 1 / math.sqrt(128), 1.0, 1e-6,
                  1004, note="long-context causal prefill bf16, B=1 H=32 N=131072 d=128"),
+        Workload("retention_bf16", "retention", 4, 16, 8192, 128, 128, "bf16", 1 / math.sqrt(128), 1.0, 0.0, 1006,
+                 note="retention bf16, B=4 H=16 N=8192 d=128, q,k ~ N(0,1)/sqrt(128), v ~ N(0,1), "
+                      "gamma_h = 1 - 2^-(5 + h mod 8)"),
         Workload("decode_bf16", "decode", 256, 32, 1, 128, 128, "bf16", 1 / math.sqrt(128), 1.0, 1e-6, 1005,
                  prefix=1024, prefix_scale=1.0, steps=1000,
                  note="decode step, batch 256 H=32 m=d_v=128, fp32 state from a 1024-token N(0,1) prefix"),
     ]
 }
+
+
+def retention_gamma(H: int) -> list[float]:
+    """Per-head decays of the retention inputs: gamma_h = 1 - 2^-(5 + h mod 8).
+
+    Eight scales from 0.96875 (a key's weight halves in about 22 tokens) to
+    1 - 2^-12 (about 2800 tokens), repeated over the heads; every value is
+    exact in float32.
+    """
+    return [1.0 - 2.0 ** -(5 + h % 8) for h in range(H)]
 
 
 def _gen(seed: int, device: str):

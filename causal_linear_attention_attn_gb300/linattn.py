@@ -30,6 +30,9 @@ _SEQ_ARGS = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _i, _vp]
 for _name in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc"):
     getattr(lib, _name).argtypes = _SEQ_ARGS
     getattr(lib, _name).restype = _i
+for _name in ("la_retention", "la_retention_with_state"):
+    getattr(lib, _name).argtypes = [_vp, _vp, _vp, _fp, _fp, ctypes.POINTER(_f), _i, _i, _i, _i, _i, _i, _vp]
+    getattr(lib, _name).restype = _i
 lib.la_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _f, _i, _vp]
 lib.la_decode_step.restype = _i
 lib.la_status_string.argtypes = [_i]
@@ -49,7 +52,7 @@ lib.la_profile_read.restype = _i
 
 # la_kernel ids of the device-time diagnostics
 KERNELS = {"causal_main": 0, "causal_state": 1, "exact_head": 2, "causal_simt": 3, "global_state": 4,
-           "global_read": 5, "decode": 6}
+           "global_read": 5, "decode": 6, "retention_main": 7, "retention_state": 8}
 
 
 class LinAttnError(RuntimeError):
@@ -149,6 +152,41 @@ def la_causal_noalloc(q, k, v, out=None, S=None, z=None, eps: float = 1e-6, stre
 def la_causal_with_state(q, k, v, S, z, out=None, eps: float = 1e-6, stream=None):
     """Causal prefill continuing from (S, z), which are updated in place; returns (out, S, z)."""
     return _seq_call("la_causal_with_state", q, k, v, out, S, z, eps, stream, need_state_in=True)
+
+
+def _retention_call(fn, q, k, v, gamma, out, S, stream, need_state_in=False):
+    _check_in(q, k, v, 4)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    g = [float(x) for x in gamma]
+    if len(g) != H:
+        raise ValueError(f"gamma must hold one decay per head ({H}), got {len(g)}")
+    if need_state_in and S is None:
+        raise ValueError(f"{fn} needs the initial state S")
+    if S is None:
+        S = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+    if S.dtype != torch.float32 or not S.is_contiguous() or tuple(S.shape) != (B, H, dk, dv):
+        raise ValueError(f"S must be a contiguous float32 {(B, H, dk, dv)} tensor")
+    if out is None:
+        out = torch.empty(B, H, N, dv, dtype=torch.float32, device=q.device)
+    if out.dtype != torch.float32 or not out.is_contiguous() or tuple(out.shape) != (B, H, N, dv):
+        raise ValueError("out must be a contiguous float32 [B, H, N, d_v] tensor")
+    garr = (_f * max(H, 1))(*g)
+    rc = getattr(lib, fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(S), garr, B, H, N, dk, dv, _dt(q),
+                          _stream(stream))
+    if rc != 0:
+        raise LinAttnError(fn, rc)
+    return out, S
+
+
+def la_retention(q, k, v, gamma, out=None, S=None, stream=None):
+    """Retention from the zero state (decay gamma[h] per head, no denominator); returns (out, S)."""
+    return _retention_call("la_retention", q, k, v, gamma, out, S, stream)
+
+
+def la_retention_with_state(q, k, v, S, gamma, out=None, stream=None):
+    """Retention continuing from S, which is updated in place; returns (out, S)."""
+    return _retention_call("la_retention_with_state", q, k, v, gamma, out, S, stream, need_state_in=True)
 
 
 def la_decode_step(q, k, v, S, z, out=None, eps: float = 1e-6, stream=None):

@@ -151,6 +151,42 @@ LA_API la_status la_causal_noalloc(const void *q, const void *k, const void *v, 
                                    void *stream);
 
 /*
+ * Retention: the causal recurrence with an explicit per-head decay and no
+ * denominator,
+ *     S_t = gamma_h S_{t-1} + k_t v_t^T,   out_t = q_t^T S_t,   S_{-1} = 0,
+ * q and k used as given (no feature map), the read taken after the update as
+ * in la_causal.  Source: "Linear Attention Math", "The kernel cousins: SSMs
+ * and RetNet" (linear attention plus a decay gamma < 1, fixed or one per
+ * head, without the denominator).  The pages' gated normalization that
+ * replaces the denominator is a separate layer on top of out and is not
+ * part of this call.
+ *
+ * q, k: [B,H,N,d_k]; v: [B,H,N,d_v] (dtype dt); out: [B,H,N,d_v] float32;
+ * S: [B,H,d_k,d_v] float32, OVERWRITTEN with S_{N-1} (zeroed when N == 0).
+ * gamma: HOST array of H floats, head h (of every batch row) decaying by
+ * gamma[h]; read during the call only.
+ *
+ * Supported: dt == LA_BF16, d_k == d_v == 128, an sm_103 device, H <= 128,
+ * every gamma[h] in [0.75, 1] (the chunked kernel weighs a key 128 tokens
+ * ahead by gamma^-128, which must stay well inside float range); anything
+ * else returns LA_ERR_UNSUPPORTED.  LA_ERR_INVALID_VALUE for a NULL gamma
+ * or a gamma that is not finite; other errors as la_causal.  Allocates
+ * stream-ordered scratch on `stream` for long sequences split into segments.
+ */
+LA_API la_status la_retention(const void *q, const void *k, const void *v, float *out, float *S,
+                              const float *gamma, int B, int H, int N, int d_k, int d_v, la_dtype dt,
+                              void *stream);
+
+/*
+ * Retention continuing from a given state: as la_retention, but the
+ * recurrence starts from the caller's S, which is read and then OVERWRITTEN
+ * with the state after the N new tokens (N == 0 leaves it unchanged).
+ */
+LA_API la_status la_retention_with_state(const void *q, const void *k, const void *v, float *out, float *S,
+                                         const float *gamma, int B, int H, int N, int d_k, int d_v,
+                                         la_dtype dt, void *stream);
+
+/*
  * One recurrent decode step per (b,h) on a persistent state: update, then
  * read the updated state,
  *     S += phi(k) v^T;  z += phi(k);  out = phi(q)^T S / (phi(q)^T z + eps).

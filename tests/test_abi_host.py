@@ -26,7 +26,7 @@ def _declared_symbols():
 def test_header_declares_the_entry_points():
     names = _declared_symbols()
     for n in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc", "la_decode_step", "la_status_string",
-              "la_version"):
+              "la_version", "la_retention", "la_retention_with_state"):
         assert n in names
 
 
@@ -97,10 +97,41 @@ def test_decode_validation():
     assert call(B=0) == OK
 
 
+def ret(fn="la_retention", q=P, k=P, v=P, out=P, S=P, gamma=(0.9,), B=1, H=1, N=8, dk=128, dv=128, dt=1,
+        stream=None):
+    g = None if gamma is None else (ctypes.c_float * max(len(gamma), 1))(*gamma)
+    return getattr(L.lib, fn)(q, k, v, out, S, g, B, H, N, dk, dv, dt, stream)
+
+
+@pytest.mark.parametrize("fn", ["la_retention", "la_retention_with_state"])
+def test_retention_validation(fn):
+    assert ret(fn, q=None) == INVALID
+    assert ret(fn, out=None) == INVALID
+    assert ret(fn, S=None) == INVALID
+    assert ret(fn, gamma=None) == INVALID
+    assert ret(fn, gamma=(float("nan"),)) == INVALID
+    assert ret(fn, gamma=(float("inf"),)) == INVALID
+    assert ret(fn, N=-1) == INVALID
+    assert ret(fn, dk=0) == INVALID
+    # outside the tensor-core retention path
+    assert ret(fn, dt=0) == UNSUPPORTED
+    assert ret(fn, dk=64) == UNSUPPORTED
+    assert ret(fn, dv=32) == UNSUPPORTED
+    assert ret(fn, gamma=(0.5,)) == UNSUPPORTED
+    assert ret(fn, gamma=(1.01,)) == UNSUPPORTED
+    assert ret(fn, H=2, gamma=(0.9, 0.7)) == UNSUPPORTED
+    assert ret(fn, H=129, gamma=(0.9,) * 129) == UNSUPPORTED
+    assert ret(fn, v=P + 8) == MISALIGNED
+    assert ret(fn, S=P + 4) == MISALIGNED
+    assert ret(fn, B=0) == OK
+    assert ret(fn, H=0, gamma=None, q=None, k=None, v=None, out=None, S=None) == OK
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_valid_call_without_a_device_reports_no_device():
     assert seq("la_causal") == NO_DEVICE
     assert seq("la_global") == NO_DEVICE
+    assert ret("la_retention") == NO_DEVICE
 
 
 def test_binding_rejects_bad_tensors_before_the_library():
@@ -109,6 +140,11 @@ def test_binding_rejects_bad_tensors_before_the_library():
         L.la_causal(q, q, q)  # CPU tensors
     with pytest.raises(ValueError):
         L.la_decode_step(q, q, q, None, None)
+    with pytest.raises(ValueError):
+        L.la_retention(q, q, q, [0.9])
+    qc = torch.zeros(1, 2, 4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        L.la_retention(qc, qc, qc, [0.9])  # CPU tensors; also one decay for two heads
 
 
 def test_profile_diagnostics_without_launches():
@@ -117,6 +153,6 @@ def test_profile_diagnostics_without_launches():
         assert L.profile_read(name) == (0.0, 0)
     L.profile_enable(False)
     ms, n = ctypes.c_double(), ctypes.c_longlong()
-    assert L.lib.la_profile_read(7, ctypes.byref(ms), ctypes.byref(n)) == INVALID
+    assert L.lib.la_profile_read(len(L.KERNELS), ctypes.byref(ms), ctypes.byref(n)) == INVALID
     assert L.lib.la_profile_read(-1, ctypes.byref(ms), ctypes.byref(n)) == INVALID
     assert L.lib.la_profile_read(0, None, ctypes.byref(n)) == INVALID

@@ -8,12 +8,19 @@ from causal_linear_attention_attn_gb300 import inputs
 W = inputs.WORKLOADS
 
 
-def test_workloads_match_the_five_configurations():
+def test_workloads_match_the_five_configurations_and_retention():
     assert [(w.B, w.H, w.N, w.dk, w.dv, w.dtype) for w in W.values()] == [
         (1, 2, 256, 32, 32, "f32"), (8, 16, 4096, 64, 64, "bf16"), (4, 16, 8192, 128, 128, "bf16"),
-        (1, 32, 131072, 128, 128, "bf16"), (256, 32, 1, 128, 128, "bf16")]
+        (1, 32, 131072, 128, 128, "bf16"), (4, 16, 8192, 128, 128, "bf16"), (256, 32, 1, 128, 128, "bf16")]
     assert W["decode_bf16"].prefix == 1024 and W["decode_bf16"].steps == 1000
-    assert all(w.eps == 1e-6 for w in W.values())
+    assert all(w.eps == 1e-6 for w in W.values() if w.form != "retention")
+
+
+def test_retention_gammas():
+    g = inputs.retention_gamma(16)
+    assert g[0] == 1 - 2 ** -5 and g[7] == 1 - 2 ** -12 and g[8:] == g[:8]
+    # exact in float32, inside the supported range [0.75, 1)
+    assert all(float(torch.tensor(x, dtype=torch.float32)) == x and 0.75 <= x < 1 for x in g)
 
 
 def test_deterministic_and_per_head_reproducible():

@@ -1,0 +1,142 @@
+"""GPU parity of retention (decayed state, no denominator) against the fp64 oracle.
+
+Retention as "Linear Attention Math", "The kernel cousins: SSMs and RetNet"
+states it: S_t = gamma_h S_{t-1} + k_t v_t^T and out_t = q_t^T S_t, q and k
+used as given.  The kernel path is the tensor-core causal pass in its
+retention mode.  Small cases compare every element of out and S, across
+shapes that cut heads into segments both ways (first-pass CTAs aligned to
+the segments, or flattened runs of two pieces), ragged tails, continuation
+from a given state, the extreme decays 0.75 and 1, and the full-size
+retention workload on sampled heads, all within the float32 tolerance.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from causal_linear_attention_attn_gb300 import inputs
+from paritylib import TAU, assert_close, f64
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+W = inputs.WORKLOADS["retention_bf16"]
+DEV = "cuda"
+# The inputs are bf16, but every operand the kernel forms from them (the
+# weighted scores, the weighted keys, the state copy read by the queries)
+# reaches the tensor cores as a bf16 hi/lo pair (about 2^-17 relative) with
+# fp32 accumulation, so the results meet the float32 inputs' bar.
+TOL = TAU[torch.float32]
+
+
+def _poison(*shape):
+    return torch.full(shape, float("nan"), dtype=torch.float32, device=DEV)
+
+
+def _oracle(q, k, v, gamma, S0=None):
+    B, H = q.shape[:2]
+    g = np.tile(np.asarray(gamma, np.float64), B).reshape(B, H)
+    return oracle.retention(f64(q), f64(k), f64(v), g, S0=S0, nthreads=8)
+
+
+def _run(L, q, k, v, gamma):
+    B, H, N, d = q.shape
+    out, S = _poison(B, H, N, d), _poison(B, H, d, d)
+    L.la_retention(q.to(DEV), k.to(DEV), v.to(DEV), gamma, out=out, S=S)
+    torch.cuda.synchronize()
+    return out, S
+
+
+# (B, H, N): one chunk, ragged single segments, and heads split into segments
+# whose first pass runs flattened (few heads) or aligned (38 heads of 1024 tokens)
+SHAPES = [(1, 1, 1), (1, 2, 127), (1, 1, 128), (1, 3, 300), (2, 2, 1100), (1, 1, 2000), (3, 1, 4097),
+          (2, 19, 1024), (1, 8, 5000)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_retention_every_element(cuda_lib, shape):
+    B, H, N = shape
+    q, k, v = inputs.make_qkv(W, N=N, B=B, H=H)
+    gamma = inputs.retention_gamma(H)
+    out, S = _run(cuda_lib, q, k, v, gamma)
+    ro, rS = _oracle(q, k, v, gamma)
+    assert_close(out, ro, TOL, "out")
+    assert_close(S, rS, TOL, "S")
+
+
+@pytest.mark.parametrize("g", [0.75, 0.9, 1.0])
+@pytest.mark.parametrize("N", [300, 2500])
+def test_retention_fixed_decay(cuda_lib, g, N):
+    q, k, v = inputs.make_qkv(W, N=N, B=1, H=2)
+    out, S = _run(cuda_lib, q, k, v, [g, g])
+    ro, rS = _oracle(q, k, v, [g, g])
+    assert_close(out, ro, TOL, "out")
+    assert_close(S, rS, TOL, "S")
+
+
+@pytest.mark.parametrize("split,N", [(1, 700), (128, 700), (200, 700), (1000, 3000), (129, 2200)])
+def test_retention_with_state_continues_the_prefix(cuda_lib, split, N):
+    q, k, v = inputs.make_qkv(W, N=N, B=1, H=3)
+    gamma = inputs.retention_gamma(3)
+    ro, rS = _oracle(q, k, v, gamma)
+    d = lambda t: t.contiguous().to(DEV)
+    L = cuda_lib
+    o1, S = L.la_retention(d(q[:, :, :split]), d(k[:, :, :split]), d(v[:, :, :split]), gamma)
+    o2, S = L.la_retention_with_state(d(q[:, :, split:]), d(k[:, :, split:]), d(v[:, :, split:]), S, gamma)
+    torch.cuda.synchronize()
+    assert_close(torch.cat([o1, o2], 2), ro, TOL, "out")
+    assert_close(S, rS, TOL, "S")
+
+
+def test_retention_from_a_carried_state(cuda_lib):
+    """Start from the oracle's state after an independent 1000-token prefix (a
+    carried state of the same distribution), with decays from 0.75 to 1."""
+    B, H, N = 1, 4, 1500
+    q, k, v = inputs.make_qkv(W, N=N, B=B, H=H)
+    gamma = [0.75, 0.95, 0.999, 1.0]
+    _, kp, vp = inputs.make_qkv(dataclasses.replace(W, seed=W.seed + 1), N=1000, B=B, H=H)
+    _, S0 = _oracle(kp, kp, vp, gamma)
+    S0 = torch.from_numpy(S0).float()
+    ro, rS = _oracle(q, k, v, gamma, S0=f64(S0))
+    S = S0.to(DEV)
+    out = _poison(B, H, N, 128)
+    cuda_lib.la_retention_with_state(q.to(DEV), k.to(DEV), v.to(DEV), S, gamma, out=out)
+    torch.cuda.synchronize()
+    assert_close(out, ro, TOL, "out")
+    assert_close(S, rS, TOL, "S")
+
+
+def test_retention_workload_full_size(cuda_lib):
+    """The full retention workload on the GPU; every output of three sampled heads."""
+    q, k, v = inputs.make_qkv(W)
+    gamma = inputs.retention_gamma(W.H)
+    out, S = _run(cuda_lib, q, k, v, gamma)
+    heads = [0, 23, 63]
+    qs, ks, vs = (t.view(W.BH, W.N, -1)[heads] for t in (q, k, v))
+    g = [gamma[h % W.H] for h in heads]
+    ro, rS = oracle.retention(f64(qs), f64(ks), f64(vs), np.asarray(g), nthreads=3)
+    assert_close(out.view(W.BH, W.N, -1)[heads], ro, TOL, "out")
+    assert_close(S.view(W.BH, 128, 128)[heads], rS, TOL, "S")
+    assert torch.isfinite(out).all() and torch.isfinite(S).all()
+
+
+def test_retention_edge_cases(cuda_lib):
+    L = cuda_lib
+    e = torch.empty(2, 3, 0, 128, dtype=torch.bfloat16, device=DEV)
+    out, S = L.la_retention(e, e, e, [0.9] * 3, S=_poison(2, 3, 128, 128))
+    torch.cuda.synchronize()
+    assert out.shape == (2, 3, 0, 128) and torch.count_nonzero(S) == 0
+    S0 = torch.randn(2, 3, 128, 128, device=DEV)
+    S1 = S0.clone()
+    L.la_retention_with_state(e, e, e, S1, [0.9] * 3)
+    torch.cuda.synchronize()
+    assert torch.equal(S0, S1)
+    with pytest.raises(L.LinAttnError, match="UNSUPPORTED"):
+        q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16, device=DEV)
+        L.la_retention(q, q, q, [0.9])
+    with pytest.raises(L.LinAttnError, match="UNSUPPORTED"):
+        q = torch.zeros(1, 1, 8, 128, dtype=torch.bfloat16, device=DEV)
+        L.la_retention(q, q, q, [0.5])
+    assert L.device_status() == 0
