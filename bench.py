@@ -320,16 +320,24 @@ def run_seq_form(L, w, steps, warmup, world, stream, hbm, src, gen_device="cuda"
     out = torch.empty(w.B, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
     S = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device="cuda")
     z = torch.empty(w.B, w.H, w.dk, dtype=torch.float32, device="cuda")
-    fn = L.la_causal if w.form == "causal" else L.la_global
-    call = lambda: fn(q, k, v, out=out, S=S, z=z, eps=w.eps, stream=stream)
+    # fn(q, k, v, out, S, z, h0): one call on heads [h0, h0 + q.shape[1]) of the flattened batch
+    if w.form == "retention":
+        gam = inputs.retention_gamma(w.H)
+        fn = lambda q_, k_, v_, o_, S_, z_, h0: L.la_retention(
+            q_, k_, v_, [gam[(h0 + i) % w.H] for i in range(q_.shape[1])], out=o_, S=S_, stream=stream)
+    else:
+        f = L.la_causal if w.form == "causal" else L.la_global
+        fn = lambda q_, k_, v_, o_, S_, z_, h0: f(q_, k_, v_, out=o_, S=S_, z=z_, eps=w.eps, stream=stream)
+    call = lambda: fn(q, k, v, out, S, z, 0)
     n0 = L.kernel_launches()
     ms = time_device(call, steps, warmup, world, stream, L)
     launches = (L.kernel_launches() - n0) // (2 * steps + warmup) * steps
     ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
     tok = w.BH * w.N
     rl, table = dominant_roofline(L, w, steps, hbm, src, w.name)
+    step_bytes = retention_bytes(w) if w.form == "retention" else seq_bytes(w)
     res = {"workload": w.name, "tokens_per_s": world * tok / (ms * 1e-3), "ms_per_call": ms,
-           "roofline": rl, "step_roofline": roofline(seq_bytes(w), ms, hbm, src, None),
+           "roofline": rl, "step_roofline": roofline(step_bytes, ms, hbm, src, None),
            "kernels": table, "gpu_launches": launches}
     return res, (q, k, v, out, S, z, fn)
 
@@ -382,8 +390,7 @@ def run_e2e(L, w, bufs, steps, warmup, stream, groups: int = 4):
         for g in range(groups):
             a, b = cuts[g], cuts[g + 1]
             stream.wait_event(done_in[g])
-            fn(*(t[a:b].unsqueeze(0) for t in dev[:3]), out=dev[3][a:b].unsqueeze(0), S=dev[4][a:b].unsqueeze(0),
-               z=dev[5][a:b].unsqueeze(0), eps=w.eps, stream=stream)
+            fn(*(t[a:b].unsqueeze(0) for t in dev), a)
             done_call[g].record(stream)
         for g in range(groups):
             a, b = cuts[g], cuts[g + 1]
@@ -422,26 +429,64 @@ def run_decode(L, w, steps, warmup, world, stream, hbm, src):
             "step_roofline": step, "kernels": table, "gpu_launches": launches}
 
 
+def retention_decode_bytes(w) -> float:
+    """Algorithmic HBM bytes of one retention step: S read and written (fp32, no z),
+    q,k,v read, fp32 out written."""
+    return w.BH * (2 * w.dk * w.dv * 4 + (2 * w.dk + w.dv) * in_bytes(w) + w.dv * 4)
+
+
+def run_retention_decode(L, w, steps, warmup, world, stream, hbm, src):
+    """Retention step on the decode workload's batch: the state from a retention
+    prefill over the same prefix, then one token per head per step."""
+    kp, vp = inputs.decode_prefix(w, device="cuda")
+    gamma = inputs.retention_gamma(w.H)
+    _, S = L.la_retention(kp, kp, vp, gamma, stream=stream)
+    del kp, vp
+    nstage = steps + warmup
+    staged = [inputs.decode_step_qkv(w, s, device="cuda") for s in range(nstage)]
+    out = torch.empty(w.B, w.H, w.dv, dtype=torch.float32, device="cuda")
+    it = itertools.cycle(staged)
+    call = lambda: L.la_retention_decode_step(*next(it), S, gamma, out=out, stream=stream)
+    n0 = L.kernel_launches()
+    ms = time_device(call, steps, warmup, world, stream, L)
+    launches = (L.kernel_launches() - n0) // (nstage + steps) * steps
+    ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
+    table = kernel_table(L, steps)
+    t = table["retention_decode"]
+    rl = roofline(retention_decode_bytes(w), t["ms_per_launch"], hbm, src, None, kernel="retention_decode")
+    step = roofline(retention_decode_bytes(w), ms, hbm, src, None)
+    return {"workload": "retention step on " + w.name, "us_per_step": ms * 1e3, "gbs": step["achieved"],
+            "frac_hbm": step["frac"], "steps_timed": steps, "roofline": rl, "step_roofline": step, "kernels": table,
+            "gpu_launches": launches}
+
+
 def cpu_baseline(w, target_s: float = 12.0):
     """The oracle as it stands, token-serial fp64, heads spread over the host cores."""
     import numpy as np
 
     import oracle
 
+    def run(q, k, v, nthreads):
+        # heads 0 .. n-1 of the workload, as the oracle's form for it
+        if w.form == "retention":
+            g = inputs.retention_gamma(w.H)
+            return oracle.retention(q, k, v, np.array([g[h % w.H] for h in range(q.shape[0])]), nthreads=nthreads)
+        fn = oracle.causal if w.form == "causal" else oracle.global_
+        return fn(q, k, v, eps=w.eps, nthreads=nthreads)
+
     cores = len(os.sched_getaffinity(0))
     # calibrate on a short prefix of one head, then size the sample
     q, k, v = inputs.make_qkv(w, N=min(w.N, 1024), heads=[0])
     t = time.perf_counter()
-    oracle.causal(q.double().numpy(), k.double().numpy(), v.double().numpy(), eps=w.eps)
+    run(q.double().numpy(), k.double().numpy(), v.double().numpy(), 1)
     per_tok = (time.perf_counter() - t) / q.shape[1]
     heads = max(1, min(w.BH, int(target_s * cores / (per_tok * w.N))))
     N = w.N if heads > 1 or per_tok * w.N * 1.0 <= target_s else max(1, int(target_s / per_tok))
     q, k, v = inputs.make_qkv(w, N=N, heads=list(range(min(heads, w.BH))))
-    fn = oracle.causal if w.form == "causal" else oracle.global_
     args = [np.ascontiguousarray(t.double().numpy()) for t in (q, k, v)]
     nthreads = min(cores, q.shape[0])
     t = time.perf_counter()
-    fn(*args, eps=w.eps, nthreads=nthreads)
+    run(*args, nthreads)
     dt = time.perf_counter() - t
     tok = q.shape[0] * q.shape[1]
     return {"value": tok / dt, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
@@ -451,23 +496,6 @@ def cpu_baseline(w, target_s: float = 12.0):
 def retention_bytes(w) -> float:
     """Algorithmic HBM bytes of one retention call: q,k,v read, fp32 out and S written."""
     return w.BH * (w.N * (2 * w.dk + w.dv) * in_bytes(w) + w.N * 4 * w.dv + 4 * w.dk * w.dv)
-
-
-def run_retention(L, w, steps, warmup, world, stream, hbm, src):
-    """Retention prefill (per-head decays, no denominator) from the zero state."""
-    q, k, v = (t.cuda() for t in inputs.make_qkv(w, device="cuda"))
-    gamma = inputs.retention_gamma(w.H)
-    out = torch.empty(w.B, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
-    S = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device="cuda")
-    call = lambda: L.la_retention(q, k, v, gamma, out=out, S=S, stream=stream)
-    n0 = L.kernel_launches()
-    ms = time_device(call, steps, warmup, world, stream, L)
-    launches = (L.kernel_launches() - n0) // (2 * steps + warmup) * steps
-    ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
-    rl, table = dominant_roofline(L, w, steps, hbm, src, w.name)
-    return {"workload": w.name, "tokens_per_s": world * w.BH * w.N / (ms * 1e-3), "ms_per_call": ms,
-            "roofline": rl, "step_roofline": roofline(retention_bytes(w), ms, hbm, src, None),
-            "kernels": table, "gpu_launches": launches}
 
 
 def main_ours(args):
@@ -499,15 +527,21 @@ def main_ours(args):
                                                            hbm, src)
             forms["causal_bf16_with_state"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
-        if "retention_bf16" in extras:
+        if "retention_bf16" in extras and args.workload != "retention_bf16":
             wr = rank_workload(inputs.WORKLOADS["retention_bf16"], rank)
-            forms["retention_bf16"] = run_retention(L, wr, args.steps, args.warmup, world, stream, hbm, src)
+            forms["retention_bf16"], _ = run_seq_form(L, wr, args.steps, args.warmup, world, stream, hbm, src)
             forms["retention_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
         if "decode_bf16" in extras:
             wd = rank_workload(inputs.WORKLOADS["decode_bf16"], rank)
             forms["decode_bf16"] = run_decode(L, wd, args.decode_steps, args.warmup, world, stream, hbm, src)
             forms["decode_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
+            torch.cuda.empty_cache()
+        if "retention_decode_bf16" in extras:
+            wd = rank_workload(inputs.WORKLOADS["decode_bf16"], rank)
+            forms["retention_decode_bf16"] = run_retention_decode(L, wd, args.decode_steps, args.warmup, world,
+                                                                  stream, hbm, src)
+            forms["retention_decode_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
     e2e = run_e2e(L, w, bufs, max(3, args.steps // 10), args.warmup, stream)
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
@@ -562,7 +596,8 @@ def parse(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-extras", action="store_true", help="time the headline workload only")
-    ap.add_argument("--forms", default="global_bf16,causal_bf16_long,causal_bf16_with_state,retention_bf16,decode_bf16",
+    ap.add_argument("--forms", default="global_bf16,causal_bf16_long,causal_bf16_with_state,retention_bf16,decode_bf16,"
+                                     "retention_decode_bf16",
                     help="comma-separated other forms timed after the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-step-s", type=float, default=10.0, help="max CPU seconds per reference step")

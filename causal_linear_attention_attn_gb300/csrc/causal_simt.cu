@@ -149,6 +149,8 @@ struct HeadSmem {
   static constexpr int P = DK + 1;  // padded rows of phi(Q), phi(K): column reads conflict-free
   static constexpr int WP = kHeadMax + 1;
   static constexpr size_t Bytes = sizeof(float) * ((size_t)2 * kHeadMax * P + kHeadMax * DV + kHeadMax * WP + kHeadMax);
+  // the caller's state, once the keys and values are done with, over phi(K) and V (contiguous)
+  static_assert((size_t)kHeadMax * P + kHeadMax * DV >= (size_t)DK * DV, "the state fits over phi(K) and V");
 };
 
 template <typename Tin, int DK, int DV>
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(kHeadThreads)
   using L = HeadSmem<DK, DV>;
   constexpr int P = L::P, WP = L::WP;
   extern __shared__ float sm[];
-  float *Kf = sm, *Qf = Kf + kHeadMax * P, *Vf = Qf + kHeadMax * P, *W = Vf + kHeadMax * DV, *den = W + kHeadMax * WP;
+  float *Qf = sm, *Kf = Qf + kHeadMax * P, *Vf = Kf + kHeadMax * P, *W = Vf + kHeadMax * DV, *den = W + kHeadMax * WP;
   const long bh = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Tin *qh = q + bh * N * DK, *kh = k + bh * N * DK, *vh = v + bh * N * DV;
@@ -245,7 +247,12 @@ __global__ void __launch_bounds__(kHeadThreads)
       }
     }
     if (S0) {
-      const float *Sh = S0 + bh * DK * DV;
+      // stage the caller's state over phi(K) and V (every read of those is done), all loads in flight
+      float *Sh = Kf;
+      __syncthreads();
+      const float4 *src = reinterpret_cast<const float4 *>(S0 + bh * DK * DV);
+      for (int e = tid; e < DK * DV / 4; e += kHeadThreads) reinterpret_cast<float4 *>(Sh)[e] = src[e];
+      __syncthreads();
       for (int f = 0; f < DK; ++f) {
         float sv[kCols];
 #pragma unroll

@@ -80,6 +80,8 @@ cudaError_t launch_global_simt(const Problem &p);
 
 // One decode step, S and z in place.
 cudaError_t launch_decode(const Problem &p);
+// Retention decode step: S = gamma[bh % H] S + k v^T, out = q^T S (host gamma array, H <= 128; no z).
+cudaError_t launch_retention_decode(const Problem &p, const float *gamma, int H);
 
 // Count one successful kernel launch (reported by la_kernel_launches).
 void count_launch(unsigned n = 1);
@@ -95,7 +97,8 @@ enum KernelId : int {
   kKDecode = 6,
   kKRetentionMain = 7,
   kKRetentionState = 8,
-  kKNumKernels = 9
+  kKRetentionDecode = 9,
+  kKNumKernels = 10
 };
 
 // While profiling is on (la_profile_enable), brackets one launch with a CUDA

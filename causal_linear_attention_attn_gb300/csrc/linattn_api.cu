@@ -320,4 +320,27 @@ la_status la_decode_step(const void *q, const void *k, const void *v, float *out
   return la::from_cuda(la::launch_decode(p));
 }
 
+la_status la_retention_decode_step(const void *q, const void *k, const void *v, float *out, float *S,
+                                   const float *gamma, int B, int H, int d_k, int d_v, la_dtype dt, void *stream) {
+  if (B < 0 || H < 0 || d_k <= 0 || d_v <= 0) return LA_ERR_INVALID_VALUE;
+  const long BH = (long)B * H;
+  if (BH > 0x7fffffffL) return LA_ERR_INVALID_VALUE;
+  if (BH == 0) return LA_OK;
+  if (!q || !k || !v || !out || !S || !gamma) return LA_ERR_INVALID_VALUE;
+  for (int h = 0; h < H; ++h)
+    if (!std::isfinite(gamma[h])) return LA_ERR_INVALID_VALUE;
+  if (dt != LA_F32 && dt != LA_BF16) return LA_ERR_UNSUPPORTED;
+  if (!la::supported_dim(d_k) || !la::supported_dim(d_v) || H > la::kMaxRetentionHeads) return LA_ERR_UNSUPPORTED;
+  for (int h = 0; h < H; ++h)
+    if (!(gamma[h] >= 0.f && gamma[h] <= 1.f)) return LA_ERR_UNSUPPORTED;
+  const void *ptrs[5] = {q, k, v, out, S};
+  for (const void *ptr : ptrs)
+    if (!la::aligned16(ptr)) return LA_ERR_MISALIGNED;
+  int dev;
+  la_status st = la::current_device(&dev);
+  if (st != LA_OK) return st;
+  Problem p{q, k, v, out, S, nullptr, (int)BH, 1L, d_k, d_v, 0.f, dt, (cudaStream_t)stream};
+  return la::from_cuda(la::launch_retention_decode(p, gamma, H));
+}
+
 }  // extern "C"

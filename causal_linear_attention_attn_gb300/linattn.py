@@ -34,6 +34,8 @@ for _name in ("la_retention", "la_retention_with_state"):
     getattr(lib, _name).argtypes = [_vp, _vp, _vp, _fp, _fp, ctypes.POINTER(_f), _i, _i, _i, _i, _i, _i, _vp]
     getattr(lib, _name).restype = _i
 lib.la_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _f, _i, _vp]
+lib.la_retention_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, ctypes.POINTER(_f), _i, _i, _i, _i, _i, _vp]
+lib.la_retention_decode_step.restype = _i
 lib.la_decode_step.restype = _i
 lib.la_status_string.argtypes = [_i]
 lib.la_status_string.restype = ctypes.c_char_p
@@ -52,7 +54,7 @@ lib.la_profile_read.restype = _i
 
 # la_kernel ids of the device-time diagnostics
 KERNELS = {"causal_main": 0, "causal_state": 1, "exact_head": 2, "causal_simt": 3, "global_state": 4,
-           "global_read": 5, "decode": 6, "retention_main": 7, "retention_state": 8}
+           "global_read": 5, "decode": 6, "retention_main": 7, "retention_state": 8, "retention_decode": 9}
 
 
 class LinAttnError(RuntimeError):
@@ -201,6 +203,25 @@ def la_decode_step(q, k, v, S, z, out=None, eps: float = 1e-6, stream=None):
                             _dt(q), _stream(stream))
     if rc != 0:
         raise LinAttnError("la_decode_step", rc)
+    return out
+
+
+def la_retention_decode_step(q, k, v, S, gamma, out=None, stream=None):
+    """One retention step; q, k [B, H, d_k], v [B, H, d_v]; S updated in place; returns out."""
+    _check_in(q, k, v, 3)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    g = [float(x) for x in gamma]
+    if len(g) != H:
+        raise ValueError(f"gamma must hold one decay per head ({H}), got {len(g)}")
+    if S is None or S.dtype != torch.float32 or not S.is_contiguous() or tuple(S.shape) != (B, H, dk, dv):
+        raise ValueError(f"S must be a contiguous float32 {(B, H, dk, dv)} tensor")
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=torch.float32, device=q.device)
+    rc = lib.la_retention_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(S), (_f * max(H, 1))(*g), B, H,
+                                      dk, dv, _dt(q), _stream(stream))
+    if rc != 0:
+        raise LinAttnError("la_retention_decode_step", rc)
     return out
 
 

@@ -203,6 +203,28 @@ LA_API la_status la_decode_step(const void *q, const void *k, const void *v, flo
                          void *stream);
 
 /*
+ * One recurrent retention step per (b,h) on a persistent state: decay,
+ * update, then read,
+ *     S = gamma_h S + k v^T;   out = q^T S,
+ * q and k used as given, no normalizer.  Source: "Linear Attention Math",
+ * "The kernel cousins: SSMs and RetNet" (the recurrent form of retention).
+ * Continues the state left by la_retention / la_retention_with_state.
+ *
+ * q, k: [B,H,d_k]; v: [B,H,d_v] (dtype dt).  out: [B,H,d_v] float32,
+ * written.  S: [B,H,d_k,d_v] float32, read and written IN PLACE.  gamma:
+ * HOST array of H floats (head h decays by gamma[h]), read during the call.
+ * Allocates nothing.
+ *
+ * Supported: dt LA_F32 or LA_BF16; d_k, d_v in {32, 64, 128}; H <= 128;
+ * every gamma[h] in [0, 1] (else LA_ERR_UNSUPPORTED).  LA_ERR_INVALID_VALUE
+ * for a NULL pointer or a gamma that is not finite; LA_ERR_MISALIGNED for a
+ * pointer that is not 16-byte aligned.  B*H == 0 is a no-op returning LA_OK.
+ */
+LA_API la_status la_retention_decode_step(const void *q, const void *k, const void *v, float *out, float *S,
+                                          const float *gamma, int B, int H, int d_k, int d_v, la_dtype dt,
+                                          void *stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the library's device status
  * word on the current device.  Returns LA_ERR_TIMEOUT if a bounded
  * device-side wait inside one of the library's kernels gave up since the
@@ -242,7 +264,10 @@ typedef enum {
   LA_KERNEL_CAUSAL_SIMT = 3,   /* fp32 chunked causal kernel (other shapes) */
   LA_KERNEL_GLOBAL_STATE = 4,  /* global form: state build */
   LA_KERNEL_GLOBAL_READ = 5,   /* global form: read */
-  LA_KERNEL_DECODE = 6         /* recurrent decode step */
+  LA_KERNEL_DECODE = 6,         /* recurrent decode step */
+  LA_KERNEL_RETENTION_MAIN = 7,   /* tensor-core retention pass */
+  LA_KERNEL_RETENTION_STATE = 8,  /* its first pass over earlier segments */
+  LA_KERNEL_RETENTION_DECODE = 9  /* recurrent retention step */
 } la_kernel;
 
 /*

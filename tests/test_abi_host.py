@@ -26,7 +26,7 @@ def _declared_symbols():
 def test_header_declares_the_entry_points():
     names = _declared_symbols()
     for n in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc", "la_decode_step", "la_status_string",
-              "la_version", "la_retention", "la_retention_with_state"):
+              "la_version", "la_retention", "la_retention_with_state", "la_retention_decode_step"):
         assert n in names
 
 
@@ -125,6 +125,27 @@ def test_retention_validation(fn):
     assert ret(fn, S=P + 4) == MISALIGNED
     assert ret(fn, B=0) == OK
     assert ret(fn, H=0, gamma=None, q=None, k=None, v=None, out=None, S=None) == OK
+
+
+def test_retention_decode_validation():
+    f = L.lib.la_retention_decode_step
+
+    def call(q=P, k=P, v=P, out=P, S=P, gamma=(0.9, 0.9), B=2, H=2, dk=64, dv=64, dt=1):
+        g = None if gamma is None else (ctypes.c_float * max(len(gamma), 1))(*gamma)
+        return f(q, k, v, out, S, g, B, H, dk, dv, dt, None)
+
+    assert call(k=None) == INVALID
+    assert call(S=None) == INVALID
+    assert call(gamma=None) == INVALID
+    assert call(gamma=(0.9, float("nan"))) == INVALID
+    assert call(H=-1) == INVALID
+    assert call(dv=96) == UNSUPPORTED
+    assert call(dt=3) == UNSUPPORTED
+    assert call(gamma=(0.9, -0.1)) == UNSUPPORTED
+    assert call(gamma=(1.5, 0.9)) == UNSUPPORTED
+    assert call(H=129, gamma=(0.9,) * 129) == UNSUPPORTED
+    assert call(S=P + 4) == MISALIGNED
+    assert call(B=0) == OK
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")

@@ -140,3 +140,42 @@ def test_retention_edge_cases(cuda_lib):
         q = torch.zeros(1, 1, 8, 128, dtype=torch.bfloat16, device=DEV)
         L.la_retention(q, q, q, [0.5])
     assert L.device_status() == 0
+
+
+# --- the recurrent retention step ----------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (32, 128), (64, 64), (128, 32), (128, 128)])
+def test_retention_decode_step_every_element(cuda_lib, dtype, dk, dv):
+    """One step from a random state, decays 0 .. 1 across the heads; the step
+    is fp32 arithmetic on the given inputs, so both dtypes meet the float32 bar."""
+    B, H = 3, 5
+    gen = torch.Generator().manual_seed(dk * 1000 + dv)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    q, k = (torch.randn(B, H, dk, generator=gen) / dk ** 0.5 for _ in range(2))
+    v = torch.randn(B, H, dv, generator=gen)
+    q, k, v = q.to(tdt), k.to(tdt), v.to(tdt)
+    S0 = torch.randn(B, H, dk, dv, generator=gen)
+    gamma = [0.0, 0.5, 0.9, 0.999, 1.0]
+    ro, rS = _oracle(q[:, :, None], k[:, :, None], v[:, :, None], gamma, S0=f64(S0))
+    S = S0.to(DEV)
+    out = cuda_lib.la_retention_decode_step(q.to(DEV), k.to(DEV), v.to(DEV), S, gamma)
+    torch.cuda.synchronize()
+    assert_close(out, ro[:, :, 0], TOL, "out")
+    assert_close(S, rS, TOL, "S")
+
+
+def test_retention_prefill_then_decode_equals_longer_prefill(cuda_lib):
+    B, H, N, steps = 2, 3, 700, 4
+    q, k, v = inputs.make_qkv(W, N=N + steps, B=B, H=H)
+    gamma = inputs.retention_gamma(H)
+    ro, rS = _oracle(q, k, v, gamma)
+    d = lambda t: t.contiguous().to(DEV)
+    L = cuda_lib
+    out, S = L.la_retention(d(q[:, :, :N]), d(k[:, :, :N]), d(v[:, :, :N]), gamma)
+    outs = [out]
+    for t in range(N, N + steps):
+        outs.append(L.la_retention_decode_step(d(q[:, :, t]), d(k[:, :, t]), d(v[:, :, t]), S, gamma)[:, :, None])
+    torch.cuda.synchronize()
+    assert_close(torch.cat(outs, 2), ro, TOL, "out")
+    assert_close(S, rS, TOL, "S")
