@@ -411,8 +411,9 @@ def run_e2e(L, w, bufs, steps, warmup, stream, groups: int = 4):
 
 def run_decode(L, w, steps, warmup, world, stream, hbm, src):
     kp, vp = inputs.decode_prefix(w, device="cuda")
-    _, S, z = L.la_causal(kp, kp, vp, eps=w.eps, stream=stream)
+    S, z = L.la_causal(kp, kp, vp, eps=w.eps, stream=stream)[1:]
     del kp, vp
+    torch.cuda.empty_cache()  # only the state stays on the device
     nstage = steps + warmup
     staged = [inputs.decode_step_qkv(w, s, device="cuda") for s in range(nstage)]
     out = torch.empty(w.B, w.H, w.dv, dtype=torch.float32, device="cuda")
@@ -440,8 +441,9 @@ def run_retention_decode(L, w, steps, warmup, world, stream, hbm, src):
     prefill over the same prefix, then one token per head per step."""
     kp, vp = inputs.decode_prefix(w, device="cuda")
     gamma = inputs.retention_gamma(w.H)
-    _, S = L.la_retention(kp, kp, vp, gamma, stream=stream)
+    S = L.la_retention(kp, kp, vp, gamma, stream=stream)[1]
     del kp, vp
+    torch.cuda.empty_cache()  # only the state stays on the device
     nstage = steps + warmup
     staged = [inputs.decode_step_qkv(w, s, device="cuda") for s in range(nstage)]
     out = torch.empty(w.B, w.H, w.dv, dtype=torch.float32, device="cuda")
@@ -453,7 +455,8 @@ def run_retention_decode(L, w, steps, warmup, world, stream, hbm, src):
     ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
     table = kernel_table(L, steps)
     t = table["retention_decode"]
-    rl = roofline(retention_decode_bytes(w), t["ms_per_launch"], hbm, src, None, kernel="retention_decode")
+    rl = roofline(retention_decode_bytes(w), t["ms_per_launch"], hbm, src, ncu_traffic(f"{w.name}:retention_decode"),
+                  kernel="retention_decode")
     step = roofline(retention_decode_bytes(w), ms, hbm, src, None)
     return {"workload": "retention step on " + w.name, "us_per_step": ms * 1e3, "gbs": step["achieved"],
             "frac_hbm": step["frac"], "steps_timed": steps, "roofline": rl, "step_roofline": step, "kernels": table,
@@ -498,6 +501,12 @@ def retention_bytes(w) -> float:
     return w.BH * (w.N * (2 * w.dk + w.dv) * in_bytes(w) + w.N * 4 * w.dv + 4 * w.dk * w.dv)
 
 
+def decode_workload(args):
+    """The decode workload, with its batch reduced by --decode-batch (small profiling runs)."""
+    w = inputs.WORKLOADS["decode_bf16"]
+    return dataclasses.replace(w, B=args.decode_batch) if args.decode_batch else w
+
+
 def main_ours(args):
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -533,12 +542,12 @@ def main_ours(args):
             forms["retention_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
         if "decode_bf16" in extras:
-            wd = rank_workload(inputs.WORKLOADS["decode_bf16"], rank)
+            wd = rank_workload(decode_workload(args), rank)
             forms["decode_bf16"] = run_decode(L, wd, args.decode_steps, args.warmup, world, stream, hbm, src)
             forms["decode_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
         if "retention_decode_bf16" in extras:
-            wd = rank_workload(inputs.WORKLOADS["decode_bf16"], rank)
+            wd = rank_workload(decode_workload(args), rank)
             forms["retention_decode_bf16"] = run_retention_decode(L, wd, args.decode_steps, args.warmup, world,
                                                                   stream, hbm, src)
             forms["retention_decode_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
@@ -595,6 +604,7 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--decode-batch", type=int, default=0, help="decode forms: batch instead of 256 (profiling)")
     ap.add_argument("--no-extras", action="store_true", help="time the headline workload only")
     ap.add_argument("--forms", default="global_bf16,causal_bf16_long,causal_bf16_with_state,retention_bf16,decode_bf16,"
                                      "retention_decode_bf16",
