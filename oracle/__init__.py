@@ -17,6 +17,10 @@ formula are cited in that file's header:
 * decode step: one update-then-read of the causal recurrence on a persistent
   state ("线性注意力从头到尾讲清楚" §7, last paragraph; "Linear Attention
   Math", "The recurrent form").
+* retention: "Linear Attention Math", "The kernel cousins: SSMs and RetNet".
+* causal backward: the derivative of the causal definition (the pages name
+  training through the chunked form but write no backward pass); pinned by
+  finite differences of the forward.
 
 Arrays: q, k are ``[..., N, dk]``; v is ``[..., N, dv]``; leading dimensions
 are flattened into independent heads.  Results are float64.
@@ -57,6 +61,8 @@ def _load():
         lib.lao_state_scalars.argtypes = [I, I]
         lib.lao_retention.argtypes = [dp, dp, dp, dp, dp, dp, dp, L, L, I, I, I]
         lib.lao_retention.restype = I
+        lib.lao_causal_backward.argtypes = [dp] * 13 + [L, L, I, I, D, I, I]
+        lib.lao_causal_backward.restype = I
         lib.lao_state_scalars.restype = L
         lib.lao_version.restype = I
         _lib = lib
@@ -168,3 +174,28 @@ def retention(q, k, v, gamma, S0=None, nthreads: int = 1):
 def state_scalars(m: int, dv: int) -> int:
     """Persistent state size per head (matrix plus normalizer vector)."""
     return int(_load().lao_state_scalars(m, dv))
+
+
+def causal_backward(q, k, v, dout, eps: float = 1e-6, phi: str = "elu1", S0=None, z0=None, dS=None, dz=None,
+                    nthreads: int = 1):
+    """Gradients of the causal prefill for the upstream gradient ``dout`` of its
+    output (and, optionally, ``dS``, ``dz`` of its final state).
+
+    Returns (dq, dk, dv, dS0, dz0): the gradients w.r.t. q, k, v and the
+    initial state (S0, z0; zero when the forward started from zero).
+    """
+    lib = _load()
+    q, k, v, lead, BH, N, dk, dv = _split(q, k, v)
+    dout = _f64(dout)
+    if dout.shape != v.shape:
+        raise ValueError("causal_backward: dout must have v's shape")
+    bc = lambda a, shape: None if a is None else _f64(np.broadcast_to(a, shape))
+    S0, dS = bc(S0, lead + (dk, dv)), bc(dS, lead + (dk, dv))
+    z0, dz = bc(z0, lead + (dk,)), bc(dz, lead + (dk,))
+    dq, dkk, dvv = np.empty(q.shape), np.empty(k.shape), np.empty(v.shape)
+    dS0, dz0 = np.empty(lead + (dk, dv)), np.empty(lead + (dk,))
+    rc = lib.lao_causal_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(S0), _ptr(z0), _ptr(dS), _ptr(dz),
+                                 _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dS0), _ptr(dz0), BH, N, dk, dv, float(eps),
+                                 PHI_KINDS[phi], int(nthreads))
+    _check(rc, "causal_backward")
+    return dq, dkk, dvv, dS0, dz0

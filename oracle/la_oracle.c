@@ -313,3 +313,156 @@ int lao_retention(const double *q, const double *k, const double *v, double *out
   free(created);
   return LAO_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * Gradient of the causal prefill.  The pages mention training through the
+ * chunked form but do not write the backward pass out; this is the plain
+ * derivative of the causal definition above, evaluated token by token.
+ * With o_t = num_t / den_t, num_t = phi(q_t)^T S_t, den_t = phi(q_t)^T z_t + eps
+ * and an upstream gradient dO_t (plus, optionally, gradients dS_N, dz_N of a
+ * loss that also uses the final state):
+ *   gnum_t = dO_t / den_t,   gden_t = -(dO_t . o_t) / den_t
+ *   dphi(q_t) = S_t gnum_t + z_t gden_t                       (forward sweep)
+ *   U_j = dS_N + sum_{t >= j} phi(q_t) gnum_t^T,  u_j = dz_N + sum_{t >= j} phi(q_t) gden_t
+ *   dphi(k_j) = U_j v_j + u_j,   dv_j = U_j^T phi(k_j)        (reverse sweep)
+ *   dS_0 = U_0,  dz_0 = u_0                                   (the initial state's gradient)
+ *   dq = dphi(q) * phi'(q),  dk = dphi(k) * phi'(k),  phi'(x) = 1 (x > 0), exp(x) (x <= 0).
+ * -------------------------------------------------------------------------*/
+typedef struct {
+  const double *q, *k, *v, *dout, *S0, *z0, *dSN, *dzN;
+  double *dq, *dk, *dv, *dS0, *dz0;
+  long N, h0, h1;
+  int dk_, dv_, kind;
+  double eps;
+  int status;
+} bwd_job_t;
+
+static double lao_dphi(double x, int kind) {
+  if (kind == LAO_PHI_IDENTITY || x > 0.0) return 1.0;
+  return exp(x);
+}
+
+static int backward_head(const bwd_job_t *jb, long h) {
+  const int m = jb->dk_, dv = jb->dv_;
+  const long N = jb->N;
+  const double *q = jb->q + h * N * m, *k = jb->k + h * N * m, *v = jb->v + h * N * dv;
+  const double *dO = jb->dout + h * N * dv;
+  double *dq = jb->dq + h * N * m, *dk = jb->dk + h * N * m, *dvo = jb->dv + h * N * dv;
+  double *S = (double *)malloc(sizeof(double) * m * dv), *z = (double *)malloc(sizeof(double) * m);
+  double *gnum = (double *)malloc(sizeof(double) * (N > 0 ? N : 1) * dv);
+  double *gden = (double *)malloc(sizeof(double) * (N > 0 ? N : 1));
+  double *qt = (double *)malloc(sizeof(double) * m), *kt = (double *)malloc(sizeof(double) * m);
+  double *o = (double *)malloc(sizeof(double) * dv);
+  if (!S || !z || !gnum || !gden || !qt || !kt || !o) {
+    free(S), free(z), free(gnum), free(gden), free(qt), free(kt), free(o);
+    return LAO_ENOMEM;
+  }
+  if (jb->S0) memcpy(S, jb->S0 + h * (long)m * dv, sizeof(double) * m * dv);
+  else memset(S, 0, sizeof(double) * m * dv);
+  if (jb->z0) memcpy(z, jb->z0 + h * (long)m, sizeof(double) * m);
+  else memset(z, 0, sizeof(double) * m);
+  /* forward sweep: the state after token t, the read, and dphi(q_t) */
+  for (long t = 0; t < N; ++t) {
+    for (int i = 0; i < m; ++i) {
+      kt[i] = lao_phi(k[t * m + i], jb->kind);
+      qt[i] = lao_phi(q[t * m + i], jb->kind);
+    }
+    for (int i = 0; i < m; ++i)
+      for (int j = 0; j < dv; ++j) S[i * dv + j] += kt[i] * v[t * dv + j];
+    for (int i = 0; i < m; ++i) z[i] += kt[i];
+    double den = jb->eps;
+    for (int i = 0; i < m; ++i) den += qt[i] * z[i];
+    double dot = 0.0;
+    for (int j = 0; j < dv; ++j) {
+      double num = 0.0;
+      for (int i = 0; i < m; ++i) num += qt[i] * S[i * dv + j];
+      o[j] = num / den;
+      gnum[t * dv + j] = dO[t * dv + j] / den;
+      dot += dO[t * dv + j] * o[j];
+    }
+    gden[t] = -dot / den;
+    for (int i = 0; i < m; ++i) {
+      double g = z[i] * gden[t];
+      for (int j = 0; j < dv; ++j) g += S[i * dv + j] * gnum[t * dv + j];
+      dq[t * m + i] = g * lao_dphi(q[t * m + i], jb->kind);
+    }
+  }
+  /* reverse sweep: U, u collect the reads at and after each token */
+  double *U = S, *u = z;
+  if (jb->dSN) memcpy(U, jb->dSN + h * (long)m * dv, sizeof(double) * m * dv);
+  else memset(U, 0, sizeof(double) * m * dv);
+  if (jb->dzN) memcpy(u, jb->dzN + h * (long)m, sizeof(double) * m);
+  else memset(u, 0, sizeof(double) * m);
+  for (long t = N - 1; t >= 0; --t) {
+    for (int i = 0; i < m; ++i) {
+      kt[i] = lao_phi(k[t * m + i], jb->kind);
+      qt[i] = lao_phi(q[t * m + i], jb->kind);
+    }
+    for (int i = 0; i < m; ++i) {
+      for (int j = 0; j < dv; ++j) U[i * dv + j] += qt[i] * gnum[t * dv + j];
+      u[i] += qt[i] * gden[t];
+    }
+    for (int i = 0; i < m; ++i) {
+      double g = u[i];
+      for (int j = 0; j < dv; ++j) g += U[i * dv + j] * v[t * dv + j];
+      dk[t * m + i] = g * lao_dphi(k[t * m + i], jb->kind);
+    }
+    for (int j = 0; j < dv; ++j) {
+      double g = 0.0;
+      for (int i = 0; i < m; ++i) g += U[i * dv + j] * kt[i];
+      dvo[t * dv + j] = g;
+    }
+  }
+  if (jb->dS0) memcpy(jb->dS0 + h * (long)m * dv, U, sizeof(double) * m * dv);
+  if (jb->dz0) memcpy(jb->dz0 + h * (long)m, u, sizeof(double) * m);
+  free(S), free(z), free(gnum), free(gden), free(qt), free(kt), free(o);
+  return LAO_OK;
+}
+
+static void *backward_worker(void *arg) {
+  bwd_job_t *jb = (bwd_job_t *)arg;
+  jb->status = LAO_OK;
+  for (long h = jb->h0; h < jb->h1; ++h) {
+    const int st = backward_head(jb, h);
+    if (st != LAO_OK) jb->status = st;
+  }
+  return NULL;
+}
+
+/* Gradients of the causal prefill over [BH, N, .].  S0, z0 (nullable) are the
+ * forward's initial state; dSN, dzN (nullable) the gradient w.r.t. its final
+ * state; dS0, dz0 (nullable) receive the gradient w.r.t. the initial state. */
+int lao_causal_backward(const double *q, const double *k, const double *v, const double *dout,
+                        const double *S0, const double *z0, const double *dSN, const double *dzN,
+                        double *dq, double *dk, double *dv, double *dS0, double *dz0, long BH, long N,
+                        int m, int dv_, double eps, int phi_kind, int nthreads) {
+  if (!q || !k || !v || !dout || !dq || !dk || !dv || BH < 0 || N < 0 || m <= 0 || dv_ <= 0 || !(eps >= 0.0))
+    return LAO_EINVAL;
+  if (phi_kind != LAO_PHI_ELU1 && phi_kind != LAO_PHI_IDENTITY) return LAO_EINVAL;
+  if (BH == 0) return LAO_OK;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > BH) nthreads = (int)BH;
+  bwd_job_t *jobs = (bwd_job_t *)calloc((size_t)nthreads, sizeof(bwd_job_t));
+  pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+  char *created = (char *)calloc((size_t)nthreads, 1);
+  if (!jobs || !tids || !created) {
+    free(jobs), free(tids), free(created);
+    return LAO_ENOMEM;
+  }
+  for (int w = 0; w < nthreads; ++w) {
+    bwd_job_t jb = {q, k, v, dout, S0, z0, dSN, dzN, dq, dk, dv, dS0, dz0, N,
+                    BH * w / nthreads, BH * (w + 1) / nthreads, m, dv_, phi_kind, eps, LAO_OK};
+    jobs[w] = jb;
+    if (nthreads > 1 && pthread_create(&tids[w], NULL, backward_worker, &jobs[w]) == 0)
+      created[w] = 1;
+    else
+      backward_worker(&jobs[w]);
+  }
+  int status = LAO_OK;
+  for (int w = 0; w < nthreads; ++w) {
+    if (created[w]) pthread_join(tids[w], NULL);
+    if (jobs[w].status != LAO_OK) status = jobs[w].status;
+  }
+  free(jobs), free(tids), free(created);
+  return status;
+}
