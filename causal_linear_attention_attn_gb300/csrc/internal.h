@@ -21,6 +21,17 @@ struct Problem {
   cudaStream_t stream;
 };
 
+// Gradient of the causal prefill: the problem's q, k, v, eps and sizes, the
+// upstream gradient of the output, the forward's initial state (nullable)
+// and the gradient of its final state (nullable); the gradients of q, k, v
+// and (nullable) of the initial state are written.  All device pointers.
+struct BackwardProblem {
+  Problem p;
+  const float *dout, *S0, *z0, *dS, *dz;
+  float *dq, *dk, *dv, *dS0, *dz0;
+};
+cudaError_t launch_causal_backward(const BackwardProblem &b);
+
 // Exact fp32 CUDA-core chunked causal pass.  Processes tokens [0, n_proc) of
 // every head.  from_state: start from the caller's S, z instead of zero.
 // write_state: store the final S, z.
@@ -98,7 +109,8 @@ enum KernelId : int {
   kKRetentionMain = 7,
   kKRetentionState = 8,
   kKRetentionDecode = 9,
-  kKNumKernels = 10
+  kKBackward = 10,
+  kKNumKernels = 11
 };
 
 // While profiling is on (la_profile_enable), brackets one launch with a CUDA

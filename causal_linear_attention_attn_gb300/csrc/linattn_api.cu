@@ -320,6 +320,29 @@ la_status la_decode_step(const void *q, const void *k, const void *v, float *out
   return la::from_cuda(la::launch_decode(p));
 }
 
+la_status la_causal_backward(const void *q, const void *k, const void *v, const float *dout, const float *S0,
+                             const float *z0, const float *dS, const float *dz, float *dq, float *dk, float *dv,
+                             float *dS0, float *dz0, int B, int H, int N, int d_k, int d_v, float eps, la_dtype dt,
+                             void *stream) {
+  if (B < 0 || H < 0 || N < 0 || d_k <= 0 || d_v <= 0) return LA_ERR_INVALID_VALUE;
+  if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_VALUE;
+  const long BH = (long)B * H;
+  if (BH > 0x7fffffffL) return LA_ERR_INVALID_VALUE;
+  if (BH == 0) return LA_OK;
+  if (N > 0 && (!q || !k || !v || !dout || !dq || !dk || !dv)) return LA_ERR_INVALID_VALUE;
+  if (dt != LA_F32 && dt != LA_BF16) return LA_ERR_UNSUPPORTED;
+  if (!la::supported_dim(d_k) || !la::supported_dim(d_v)) return LA_ERR_UNSUPPORTED;
+  const void *ptrs[13] = {q, k, v, dout, S0, z0, dS, dz, dq, dk, dv, dS0, dz0};
+  for (const void *ptr : ptrs)
+    if (ptr && !la::aligned16(ptr)) return LA_ERR_MISALIGNED;
+  int dev;
+  la_status st = la::current_device(&dev);
+  if (st != LA_OK) return st;
+  la::BackwardProblem b{{q, k, v, nullptr, nullptr, nullptr, (int)BH, (long)N, d_k, d_v, eps, dt, (cudaStream_t)stream},
+                        dout, S0, z0, dS, dz, dq, dk, dv, dS0, dz0};
+  return la::from_cuda(la::launch_causal_backward(b));
+}
+
 la_status la_retention_decode_step(const void *q, const void *k, const void *v, float *out, float *S,
                                    const float *gamma, int B, int H, int d_k, int d_v, la_dtype dt, void *stream) {
   if (B < 0 || H < 0 || d_k <= 0 || d_v <= 0) return LA_ERR_INVALID_VALUE;

@@ -36,6 +36,8 @@ for _name in ("la_retention", "la_retention_with_state"):
 lib.la_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _f, _i, _vp]
 lib.la_retention_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, ctypes.POINTER(_f), _i, _i, _i, _i, _i, _vp]
 lib.la_retention_decode_step.restype = _i
+lib.la_causal_backward.argtypes = [_vp] * 13 + [_i, _i, _i, _i, _i, _f, _i, _vp]
+lib.la_causal_backward.restype = _i
 lib.la_decode_step.restype = _i
 lib.la_status_string.argtypes = [_i]
 lib.la_status_string.restype = ctypes.c_char_p
@@ -54,7 +56,8 @@ lib.la_profile_read.restype = _i
 
 # la_kernel ids of the device-time diagnostics
 KERNELS = {"causal_main": 0, "causal_state": 1, "exact_head": 2, "causal_simt": 3, "global_state": 4,
-           "global_read": 5, "decode": 6, "retention_main": 7, "retention_state": 8, "retention_decode": 9}
+           "global_read": 5, "decode": 6, "retention_main": 7, "retention_state": 8, "retention_decode": 9,
+           "backward": 10}
 
 
 class LinAttnError(RuntimeError):
@@ -223,6 +226,36 @@ def la_retention_decode_step(q, k, v, S, gamma, out=None, stream=None):
     if rc != 0:
         raise LinAttnError("la_retention_decode_step", rc)
     return out
+
+
+def la_causal_backward(q, k, v, dout, S0=None, z0=None, dS=None, dz=None, need_state_grad: bool = False,
+                       eps: float = 1e-6, stream=None):
+    """Gradients of la_causal (la_causal_with_state when S0, z0 are given) for the
+    upstream gradient ``dout`` of its output and, optionally, ``dS``, ``dz`` of its
+    final state.  Returns (dq, dk, dv), plus (dS0, dz0) when ``need_state_grad``."""
+    _check_in(q, k, v, 4)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+
+    def f32(t, shape, name):
+        if t is None:
+            return None
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape {shape}")
+        return t
+
+    dout = f32(dout, (B, H, N, dv), "dout")
+    S0, dS = f32(S0, (B, H, dk, dv), "S0"), f32(dS, (B, H, dk, dv), "dS")
+    z0, dz = f32(z0, (B, H, dk), "z0"), f32(dz, (B, H, dk), "dz")
+    new = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=q.device)
+    dq, dkk, dvv = new(B, H, N, dk), new(B, H, N, dk), new(B, H, N, dv)
+    dS0, dz0 = (new(B, H, dk, dv), new(B, H, dk)) if need_state_grad else (None, None)
+    rc = lib.la_causal_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(S0), _ptr(z0), _ptr(dS), _ptr(dz),
+                                _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dS0), _ptr(dz0), B, H, N, dk, dv, float(eps),
+                                _dt(q), _stream(stream))
+    if rc != 0:
+        raise LinAttnError("la_causal_backward", rc)
+    return (dq, dkk, dvv, dS0, dz0) if need_state_grad else (dq, dkk, dvv)
 
 
 def device_status(stream=None) -> int:

@@ -187,6 +187,35 @@ LA_API la_status la_retention_with_state(const void *q, const void *k, const voi
                                          la_dtype dt, void *stream);
 
 /*
+ * Gradient of la_causal / la_causal_with_state.  The pages name training
+ * through the chunked causal form ("Linear Attention: From Pairwise Reads to
+ * a Recurrent State", "A recurrence need not force token-serial training")
+ * but write no backward pass; this is the derivative of the causal
+ * definition above.  With den_t = phi(q_t)^T z_t + eps, o_t the output and
+ * dO_t its upstream gradient:
+ *     gnum_t = dO_t / den_t,   gden_t = -(dO_t . o_t) / den_t
+ *     dq_t = (S_t gnum_t + z_t gden_t) * phi'(q_t)
+ *     dk_j = (U_j v_j + u_j) * phi'(k_j),   dv_j = U_j^T phi(k_j)
+ *     U_j = dS + sum_{t >= j} phi(q_t) gnum_t^T,   u_j = dz + sum_{t >= j} phi(q_t) gden_t
+ * and the initial state's gradient is (U_0, u_0).  phi'(x) = 1 for x > 0,
+ * exp(x) otherwise.
+ *
+ * q, k: [B,H,N,d_k]; v: [B,H,N,d_v] (dtype dt), the forward's inputs.
+ * dout: [B,H,N,d_v] float32, the gradient of the forward's out.  S0, z0
+ * (nullable, each independently; NULL = zero): the forward's initial state.
+ * dS, dz (nullable; NULL = zero): the gradient of the forward's final state.
+ * dq, dk: [B,H,N,d_k], dv: [B,H,N,d_v] float32, written.  dS0: [B,H,d_k,d_v],
+ * dz0: [B,H,d_k] float32 (nullable), written with the initial state's gradient.
+ * The forward output is recomputed, not read.  Allocates stream-ordered
+ * scratch of B*H*N*(d_v+1) floats on `stream`.  Errors as la_causal; every
+ * non-NULL pointer must be 16-byte aligned.  B*H == 0 is a no-op.
+ */
+LA_API la_status la_causal_backward(const void *q, const void *k, const void *v, const float *dout,
+                                    const float *S0, const float *z0, const float *dS, const float *dz,
+                                    float *dq, float *dk, float *dv, float *dS0, float *dz0, int B, int H,
+                                    int N, int d_k, int d_v, float eps, la_dtype dt, void *stream);
+
+/*
  * One recurrent decode step per (b,h) on a persistent state: update, then
  * read the updated state,
  *     S += phi(k) v^T;  z += phi(k);  out = phi(q)^T S / (phi(q)^T z + eps).
@@ -267,7 +296,8 @@ typedef enum {
   LA_KERNEL_DECODE = 6,         /* recurrent decode step */
   LA_KERNEL_RETENTION_MAIN = 7,   /* tensor-core retention pass */
   LA_KERNEL_RETENTION_STATE = 8,  /* its first pass over earlier segments */
-  LA_KERNEL_RETENTION_DECODE = 9  /* recurrent retention step */
+  LA_KERNEL_RETENTION_DECODE = 9, /* recurrent retention step */
+  LA_KERNEL_BACKWARD = 10         /* causal backward */
 } la_kernel;
 
 /*

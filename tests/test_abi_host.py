@@ -26,7 +26,8 @@ def _declared_symbols():
 def test_header_declares_the_entry_points():
     names = _declared_symbols()
     for n in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc", "la_decode_step", "la_status_string",
-              "la_version", "la_retention", "la_retention_with_state", "la_retention_decode_step"):
+              "la_version", "la_retention", "la_retention_with_state", "la_retention_decode_step",
+              "la_causal_backward"):
         assert n in names
 
 
@@ -145,6 +146,26 @@ def test_retention_decode_validation():
     assert call(gamma=(1.5, 0.9)) == UNSUPPORTED
     assert call(H=129, gamma=(0.9,) * 129) == UNSUPPORTED
     assert call(S=P + 4) == MISALIGNED
+    assert call(B=0) == OK
+
+
+def test_backward_validation():
+    f = L.lib.la_causal_backward
+
+    def call(q=P, k=P, v=P, dout=P, S0=None, z0=None, dS=None, dz=None, dq=P, dk=P, dv=P, dS0=None, dz0=None,
+             B=1, H=2, N=8, d_k=64, d_v=64, eps=1e-6, dt=1):
+        return f(q, k, v, dout, S0, z0, dS, dz, dq, dk, dv, dS0, dz0, B, H, N, d_k, d_v, eps, dt, None)
+
+    assert call(dout=None) == INVALID
+    assert call(dq=None) == INVALID
+    assert call(v=None) == INVALID
+    assert call(N=-1) == INVALID
+    assert call(eps=float("nan")) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(d_k=48) == UNSUPPORTED
+    assert call(dt=2) == UNSUPPORTED
+    assert call(dS=P + 4) == MISALIGNED
+    assert call(dz0=P + 8) == MISALIGNED
     assert call(B=0) == OK
 
 
