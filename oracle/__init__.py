@@ -18,6 +18,8 @@ formula are cited in that file's header:
   state ("线性注意力从头到尾讲清楚" §7, last paragraph; "Linear Attention
   Math", "The recurrent form").
 * retention: "Linear Attention Math", "The kernel cousins: SSMs and RetNet".
+* positive random features: "Linear Attention Math", "Feature maps: elu+1
+  and positive random features"; "线性注意力从头到尾讲清楚" §9.
 * causal backward: the derivative of the causal definition (the pages name
   training through the chunked form but write no backward pass); pinned by
   finite differences of the forward.
@@ -63,6 +65,8 @@ def _load():
         lib.lao_retention.restype = I
         lib.lao_causal_backward.argtypes = [dp] * 13 + [L, L, I, I, D, I, I]
         lib.lao_causal_backward.restype = I
+        lib.lao_favor_features.argtypes = [dp, dp, dp, L, I, I]
+        lib.lao_favor_features.restype = I
         lib.lao_state_scalars.restype = L
         lib.lao_version.restype = I
         _lib = lib
@@ -199,3 +203,18 @@ def causal_backward(q, k, v, dout, eps: float = 1e-6, phi: str = "elu1", S0=None
                                  PHI_KINDS[phi], int(nthreads))
     _check(rc, "causal_backward")
     return dq, dkk, dvv, dS0, dz0
+
+
+def favor_features(x, W):
+    """Positive random features phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m) of every
+    row of ``x`` ([..., d]) for the projections ``W`` ([m, d]); returns [..., m]."""
+    lib = _load()
+    x, W = _f64(x), _f64(W)
+    d = x.shape[-1]
+    if W.ndim != 2 or W.shape[1] != d:
+        raise ValueError("favor_features: W must be [m, d] with x's last dimension d")
+    m = W.shape[0]
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    out = np.empty(x.shape[:-1] + (m,))
+    _check(lib.lao_favor_features(_ptr(x), _ptr(W), _ptr(out), rows, d, m), "favor_features")
+    return out

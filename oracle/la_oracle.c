@@ -466,3 +466,27 @@ int lao_causal_backward(const double *q, const double *k, const double *v, const
   free(jobs), free(tids), free(created);
   return status;
 }
+
+/* ---------------------------------------------------------------------------
+ * Positive random features ("Linear Attention Math", "Feature maps: elu+1 and
+ * positive random features"; "线性注意力从头到尾讲清楚" §9): for random
+ * projections w_r (the rows of W, [m, d]),
+ *   phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m),
+ * so that E[phi(x) . phi(y)] = exp(x . y) for w_r ~ N(0, I).  Applied to every
+ * row x of X ([rows, d]); out is [rows, m].
+ * -------------------------------------------------------------------------*/
+int lao_favor_features(const double *X, const double *W, double *out, long rows, int d, int m) {
+  if (!X || !W || !out || rows < 0 || d <= 0 || m <= 0) return LAO_EINVAL;
+  const double inv_sqrt_m = 1.0 / sqrt((double)m);
+  for (long r = 0; r < rows; ++r) {
+    const double *x = X + r * d;
+    double nrm = 0.0;
+    for (int i = 0; i < d; ++i) nrm += x[i] * x[i];
+    for (int f = 0; f < m; ++f) {
+      double wx = 0.0;
+      for (int i = 0; i < d; ++i) wx += W[(long)f * d + i] * x[i];
+      out[r * m + f] = exp(wx - 0.5 * nrm) * inv_sqrt_m;
+    }
+  }
+  return LAO_OK;
+}
