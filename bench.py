@@ -279,7 +279,7 @@ def kernel_bytes(w, kernel: str) -> float:
     ib = in_bytes(w)
     state = 4 * (w.dk * w.dv + w.dk)
     if kernel == "causal_main":  # all q, k, v; outputs except each head's exact leading rows; final state
-        ne = min(w.N, 64)
+        ne = min(w.N, 64) if w.form == "causal" else 0  # given features: no exact leading rows
         return w.BH * (w.N * (2 * w.dk + w.dv) * ib + (w.N - ne) * 4 * w.dv + state)
     if kernel == "retention_main":  # all q, k, v; every output row; final S (no normalizer)
         return w.BH * (w.N * (2 * w.dk + w.dv) * ib + w.N * 4 * w.dv + 4 * w.dk * w.dv)
@@ -289,6 +289,8 @@ def kernel_bytes(w, kernel: str) -> float:
         return w.BH * (w.N * w.dk * ib + state + w.N * 4 * w.dv)
     if kernel == "decode":
         return decode_bytes(w)
+    if kernel == "favor":  # one launch: the rows of q (or k) in, their 128 features out, the projections
+        return w.BH * w.N * (w.dk + 128) * ib + 128 * w.dk * ib
     return seq_bytes(w)
 
 
@@ -430,6 +432,32 @@ def run_decode(L, w, steps, warmup, world, stream, hbm, src):
             "step_roofline": step, "kernels": table, "gpu_launches": launches}
 
 
+def run_favor(L, w, steps, warmup, world, stream, hbm, src):
+    """FAVOR+ causal prefill: positive random features of q and k (m = 128), then
+    the normalized causal read on them."""
+    q, k, v = (t.cuda() for t in inputs.make_qkv(w, device="cuda"))
+    P = inputs.favor_projections(w, device="cuda")
+    fq, fk = (torch.empty(w.B, w.H, w.N, 128, dtype=q.dtype, device="cuda") for _ in range(2))
+    out = torch.empty(w.B, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
+    S = torch.empty(w.B, w.H, 128, w.dv, dtype=torch.float32, device="cuda")
+    z = torch.empty(w.B, w.H, 128, dtype=torch.float32, device="cuda")
+
+    def call():
+        L.la_favor_features(q, P, out=fq, stream=stream)
+        L.la_favor_features(k, P, out=fk, stream=stream)
+        L.la_causal_features(fq, fk, v, out=out, S=S, z=z, eps=w.eps, stream=stream)
+
+    n0 = L.kernel_launches()
+    ms = time_device(call, steps, warmup, world, stream, L)
+    launches = (L.kernel_launches() - n0) // (2 * steps + warmup) * steps
+    ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
+    rl, table = dominant_roofline(L, w, steps, hbm, src, w.name)
+    step_bytes = 2 * kernel_bytes(w, "favor") + seq_bytes(w)
+    return {"workload": w.name, "tokens_per_s": world * w.BH * w.N / (ms * 1e-3), "ms_per_call": ms,
+            "roofline": rl, "step_roofline": roofline(step_bytes, ms, hbm, src, None), "kernels": table,
+            "gpu_launches": launches}
+
+
 def retention_decode_bytes(w) -> float:
     """Algorithmic HBM bytes of one retention step: S read and written (fp32, no z),
     q,k,v read, fp32 out written."""
@@ -541,6 +569,11 @@ def main_ours(args):
             forms["retention_bf16"], _ = run_seq_form(L, wr, args.steps, args.warmup, world, stream, hbm, src)
             forms["retention_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
+        if "favor_bf16" in extras:
+            wf = rank_workload(inputs.WORKLOADS["favor_bf16"], rank)
+            forms["favor_bf16"] = run_favor(L, wf, args.steps, args.warmup, world, stream, hbm, src)
+            forms["favor_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
+            torch.cuda.empty_cache()
         if "decode_bf16" in extras:
             wd = rank_workload(decode_workload(args), rank)
             forms["decode_bf16"] = run_decode(L, wd, args.decode_steps, args.warmup, world, stream, hbm, src)
@@ -606,8 +639,8 @@ def parse(argv=None):
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--decode-batch", type=int, default=0, help="decode forms: batch instead of 256 (profiling)")
     ap.add_argument("--no-extras", action="store_true", help="time the headline workload only")
-    ap.add_argument("--forms", default="global_bf16,causal_bf16_long,causal_bf16_with_state,retention_bf16,decode_bf16,"
-                                     "retention_decode_bf16",
+    ap.add_argument("--forms", default="global_bf16,causal_bf16_long,causal_bf16_with_state,retention_bf16,favor_bf16,"
+                                     "decode_bf16,retention_decode_bf16",
                     help="comma-separated other forms timed after the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-step-s", type=float, default=10.0, help="max CPU seconds per reference step")

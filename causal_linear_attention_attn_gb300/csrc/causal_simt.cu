@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kThreads)
     causal_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                        float *__restrict__ out, float *__restrict__ S_g, float *__restrict__ z_g,
                        long N, long n_proc, int dk, int dv, float eps, int from_state,
-                       int write_state) {
+                       int write_state, int identity) {
   extern __shared__ float sm[];
   const int dkp = dk + 1;  // padded row: conflict-free column walks
   float *S = sm;                  // [dk][dv]  carried state
@@ -60,8 +60,9 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();  // the previous chunk is fully consumed
     for (int e = tid; e < T * dk; e += kThreads) {
       const int t = e / dk, i = e - t * dk;
-      Qs[t * dkp + i] = phi(ldf(qh + (t0 + t) * dk + i));
-      Ks[t * dkp + i] = phi(ldf(kh + (t0 + t) * dk + i));
+      const float xq = ldf(qh + (t0 + t) * dk + i), xk = ldf(kh + (t0 + t) * dk + i);
+      Qs[t * dkp + i] = identity ? xq : phi(xq);  // identity: q and k are given features
+      Ks[t * dkp + i] = identity ? xk : phi(xk);
     }
     for (int e = tid; e < T * dv; e += kThreads) Vs[e] = ldf(vh + t0 * dv + e);
     __syncthreads();
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 template <typename Tin>
-cudaError_t launch_t(const Problem &p, long n_proc, bool from_state, bool write_state) {
+cudaError_t launch_t(const Problem &p, long n_proc, bool from_state, bool write_state, bool identity) {
   const size_t smem = simt_smem_bytes(p.dk, p.dv);
   cudaError_t e = cudaFuncSetAttribute(causal_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -126,7 +127,7 @@ cudaError_t launch_t(const Problem &p, long n_proc, bool from_state, bool write_
   LaunchTimer timer(kKCausalSimt, p.stream);
   causal_simt_kernel<Tin><<<p.BH, kThreads, smem, p.stream>>>(
       (const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, p.out, p.S, p.z, p.N, n_proc, p.dk, p.dv, p.eps,
-      from_state ? 1 : 0, write_state ? 1 : 0);
+      from_state ? 1 : 0, write_state ? 1 : 0, identity ? 1 : 0);
   e = cudaGetLastError();
   timer.done(e);
   if (e == cudaSuccess) count_launch();
@@ -316,9 +317,9 @@ cudaError_t launch_causal_exact_head(const Problem &p, long n_exact, const float
   return launch_head_t<__nv_bfloat16, 128, 128>(p, ne, S0, z0, pdl);
 }
 
-cudaError_t launch_causal_simt(const Problem &p, long n_proc, bool from_state, bool write_state) {
-  if (p.dt == LA_F32) return launch_t<float>(p, n_proc, from_state, write_state);
-  return launch_t<__nv_bfloat16>(p, n_proc, from_state, write_state);
+cudaError_t launch_causal_simt(const Problem &p, long n_proc, bool from_state, bool write_state, bool identity) {
+  if (p.dt == LA_F32) return launch_t<float>(p, n_proc, from_state, write_state, identity);
+  return launch_t<__nv_bfloat16>(p, n_proc, from_state, write_state, identity);
 }
 
 }  // namespace la

@@ -269,8 +269,15 @@ __device__ __forceinline__ long piece_end_units(const TcParams &p, int bh, long 
 // one stage); the copy of A that Q reads is split into Sb (hi) and the other
 // Q slot (lo).  Every factor lies within 2^+-54 for gamma >= 0.75.  There is
 // no z, no denominator and no exact leading-token pass.
-template <bool kRet>
+// kModeIdentity: q and k are already features; they reach the MMAs as given,
+// with the normalizer, denominators and no exact leading-token pass.  Given
+// features can be heavy-tailed (a few keys dominate each read while the state
+// sums all of them), so this mode too reads the carried state as a hi/lo pair.
+template <int kMode>
 __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParams p) {
+  constexpr bool kRet = kMode == kModeRetention, kRaw = kMode != kModeElu;
+  // one Q slot; the other holds the low parts of the state copy read by the queries
+  constexpr bool kQ1 = kMode != kModeElu, kSplitS = kQ1;
   using Lay = Layout;
   constexpr int kStages = Lay::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -345,9 +352,9 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       int issued_q = 0, issued_k = 0, issued_v = 0;
       // Q of chunk c: stage c % 2, or (retention) always slot 0, after the previous chunk's state update
       auto load_q = [&](int c, int tok) -> bool {
-        const int qs = kRet ? 0 : c % kStages;
-        if (kRet ? c >= 1 : c >= kStages) {
-          const uint32_t ph = kRet ? (uint32_t)(c - 1) & 1 : (uint32_t)(c / kStages - 1) & 1;
+        const int qs = kQ1 ? 0 : c % kStages;
+        if (kQ1 ? c >= 1 : c >= kStages) {
+          const uint32_t ph = kQ1 ? (uint32_t)(c - 1) & 1 : (uint32_t)(c / kStages - 1) & 1;
           if (!mbar_wait(&q_empty[qs], ph, abort_word, status)) return false;
         }
         mbar_arrive_expect_tx(&full_q[qs], kTile);
@@ -374,8 +381,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         if (kRet && !load_q(c, tok)) break;
       }
       // every issued copy must land before shared memory is released
-      for (int c = max(0, issued_q - (kRet ? 1 : kStages)); c < issued_q; ++c)
-        wait_drain(&full_q[kRet ? 0 : c % kStages], kRet ? (uint32_t)c & 1 : (uint32_t)(c / kStages) & 1, status);
+      for (int c = max(0, issued_q - (kQ1 ? 1 : kStages)); c < issued_q; ++c)
+        wait_drain(&full_q[kQ1 ? 0 : c % kStages], kQ1 ? (uint32_t)c & 1 : (uint32_t)(c / kStages) & 1, status);
       for (int c = max(0, issued_k - kStages); c < issued_k; ++c)
         wait_drain(&full_k[c % kStages], (c / kStages) & 1, status);
       for (int c = max(0, issued_v - kStages); c < issued_v; ++c)
@@ -423,7 +430,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         tc_fence_after();
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSb, ks), iKM, ks > 0);
-        if (kRet) {
+        if (kSplitS) {
 #pragma unroll 1
           for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSblo, ks), iKM, 1);
         }
@@ -472,14 +479,14 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       const int tv = (int)min((long)kC, t_end - (t_begin + (long)c * kC));
       uint8_t *Kt = sm + Lay::K + s * kTile;
       bool ok = mbar_wait(&full_k[s], u & 1, abort_word, status);
-      ok = ok && mbar_wait(&full_q[kRet ? 0 : s], kRet ? (uint32_t)c & 1 : u & 1, abort_word, status);
+      ok = ok && mbar_wait(&full_q[kQ1 ? 0 : s], kQ1 ? (uint32_t)c & 1 : u & 1, abort_word, status);
       // this chunk's phi(Q) buffer is free once Q K^T and Q S of the chunk two back have completed
       if (ok && c >= 2) ok = mbar_wait(&qt_free[c & 1], ((c >> 1) - 1) & 1, abort_word, status);
       if (bar_or(kBarPhi, kPhiThreads, !ok)) break;
       {
         // phi(Q) half row -> packed bf16 pairs -> tensor memory; the partial phi(q).z_prev
         // from the same rounded values meets its other half in shared memory
-        const uint8_t *Qb = sm + Lay::Q + (kRet ? 0 : s) * kTile + half * kBlk;
+        const uint8_t *Qb = sm + Lay::Q + (kQ1 ? 0 : s) * kTile + half * kBlk;
         const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + 64 * (c & 1) + 32 * half;
         float dx = 0.f;
 #pragma unroll 1
@@ -490,7 +497,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const uint4 y = kRet ? xv[e] : phi8(xv[e]);
+            const uint4 y = kRaw ? xv[e] : phi8(xv[e]);
             w[4 * e] = y.x, w[4 * e + 1] = y.y, w[4 * e + 2] = y.z, w[4 * e + 3] = y.w;
             if (!kRet) dx += dot8(y, zs + half * 64 + g * 32 + e * 8);
           }
@@ -498,7 +505,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         }
         if (!kRet) {
           atomicAdd(&den_x[s * kC + row], dx);
-          mbar_arrive(&q_empty[s]);  // raw Q consumed
+          mbar_arrive(&q_empty[kQ1 ? 0 : s]);  // raw Q consumed
         }
       }
       // phi(K) half row in place (all loads of a step first: the in-place stores would order them);
@@ -525,7 +532,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
           }
         }
       };
-      if (!kRet) transform_k(1.f);
+      if (!kRaw) transform_k(1.f);
       named_bar(kBarPhi, kPhiThreads);  // every K row transformed; every read of zs done
       if (!kRet) {
         // column sums of phi(K) over the valid rows (bf16 values, as the MMA sees them)
@@ -593,7 +600,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
 #pragma unroll
         for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(v[e]);
         tmem_st32(tl + kColS + cb * 32, r);
-        if (kRet)
+        if (kSplitS)
           store_row32_split(Sb, sm + Lay::Q + kTile, T, cb * 32, r);
         else
           store_row32_bf16(Sb, T, cb * 32, r);
@@ -679,10 +686,11 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * gC);
             if (c + 1 < nchunks) tmem_st32(tl + kColS + cb * 32, r);
-            store_row32_split(Sb, sm + Lay::Q + kTile, T, cb * 32, r);
-          } else {
-            store_row32_bf16(Sb, T, cb * 32, r);
           }
+          if (kSplitS)
+            store_row32_split(Sb, sm + Lay::Q + kTile, T, cb * 32, r);
+          else
+            store_row32_bf16(Sb, T, cb * 32, r);
         }
         fence_async_smem();
         tc_fence_before();
@@ -818,12 +826,13 @@ bool make_out_map(CUtensorMap *m, void *base, long BH, long N, uint32_t rows) {
          CUDA_SUCCESS;
 }
 
-template <bool kRet>
+template <int kMode>
 cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bool pdl) {
+  constexpr bool kRet = kMode == kModeRetention;
   static std::once_flag once;
   static cudaError_t attr_err;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(causal_tc_kernel<kRet>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(causal_tc_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)Layout::Alloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -839,7 +848,7 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bo
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, causal_tc_kernel<kRet>, tp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, causal_tc_kernel<kMode>, tp);
   if (e == cudaSuccess) e = cudaGetLastError();
   timer.done(e);
   if (e == cudaSuccess) {
@@ -847,8 +856,8 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bo
   } else if (getenv("LA_DEBUG")) {
     cudaFuncAttributes fa;
     int blocks = -1;
-    cudaFuncGetAttributes(&fa, causal_tc_kernel<kRet>);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, causal_tc_kernel<kRet>, kThreads, Layout::Alloc);
+    cudaFuncGetAttributes(&fa, causal_tc_kernel<kMode>);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, causal_tc_kernel<kMode>, kThreads, Layout::Alloc);
     fprintf(stderr,
             "linattn: causal_tc_kernel launch failed (%s): regs %d, max threads %d, static smem %zu, "
             "max dynamic smem %d, requested dynamic %u, threads %d, occupancy %d\n",
@@ -871,16 +880,18 @@ cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bo
 //      so that the stream's next work follows all three.
 // Retention (tp.ret_H > 0) runs passes 1 and 2 only: its segments past the
 // first wait for pass 1, so pass 2 completes after it.
-cudaError_t launch_passes(const Problem &p, const TcParams &tp, const float *S0, const float *z0) {
+cudaError_t launch_passes(const Problem &p, const TcParams &tp, const float *S0, const float *z0, int mode) {
   cudaError_t e = cudaSuccess;
-  const bool split = tp.nseg > 1, ret = tp.ret_H > 0;
+  const bool split = tp.nseg > 1, ret = mode == kModeRetention;
   if (split)
     e = launch_range_states(p, tp.seg_len, tp.fp_ranges, tp.fp_ctas, tp.fp_pieces_per_cta, tp.part_S, tp.part_z,
-                            ret ? kKRetentionState : kKCausalState, ret ? tp.log2g : nullptr, tp.ret_H);
+                            ret ? kKRetentionState : kKCausalState, ret ? tp.log2g : nullptr, tp.ret_H, mode);
   const dim3 grid((unsigned)tp.nseg, (unsigned)p.BH);
   if (e == cudaSuccess)
-    e = ret ? launch_kernel<true>(tp, grid, p.stream, split) : launch_kernel<false>(tp, grid, p.stream, split);
-  if (e == cudaSuccess && !ret) e = launch_causal_exact_head(p, tp.n_exact, S0, z0, true);
+    e = ret                         ? launch_kernel<kModeRetention>(tp, grid, p.stream, split)
+        : mode == kModeIdentity ? launch_kernel<kModeIdentity>(tp, grid, p.stream, split)
+                                : launch_kernel<kModeElu>(tp, grid, p.stream, split);
+  if (e == cudaSuccess && tp.n_exact > 0) e = launch_causal_exact_head(p, tp.n_exact, S0, z0, true);
   return e;
 }
 
@@ -940,10 +951,10 @@ void set_first_pass(TcParams &tp, const Problem &p, const Partition &t) {
   tp.fp_pieces_per_cta = (int)t.pieces_per_cta;
 }
 
-// One call of the tensor-core path: normalized attention (log2g null) or
-// retention with head h's decay 2^log2g[h % ret_H].
-cudaError_t launch_tc(const Problem &p, bool from_state, const float *log2g, int ret_H) {
-  const bool ret = log2g != nullptr;
+// One call of the tensor-core path in one mode; retention decays head h by
+// 2^log2g[h % ret_H].
+cudaError_t launch_tc(const Problem &p, bool from_state, int mode, const float *log2g, int ret_H) {
+  const bool ret = mode == kModeRetention;
   const DeviceInfo &di = device_info(-1);
   const long sms = std::max(1, di.sm_count);
   const Partition t = plan_partition(p, sms, 2 * sms);
@@ -992,12 +1003,12 @@ cudaError_t launch_tc(const Problem &p, bool from_state, const float *log2g, int
   tp.part_z = part_z;
   tp.N = p.N;
   set_first_pass(tp, p, t);
-  tp.n_exact = ret ? 0 : (int)std::min<long>(p.N, kExact);
+  tp.n_exact = mode == kModeElu ? (int)std::min<long>(p.N, kExact) : 0;
   tp.eps = p.eps;
   tp.ret_H = ret ? ret_H : 0;
   for (int h = 0; ret && h < ret_H; ++h) tp.log2g[h] = log2g[h];
 
-  e = launch_passes(p, tp, S0, z0);
+  e = launch_passes(p, tp, S0, z0, mode);
   if (scratch) {
     const cudaError_t f = cudaFreeAsync(scratch, p.stream);
     if (e == cudaSuccess) e = f;
@@ -1005,11 +1016,17 @@ cudaError_t launch_tc(const Problem &p, bool from_state, const float *log2g, int
   return e;
 }
 
-cudaError_t launch_causal_tc(const Problem &p, bool from_state) { return launch_tc(p, from_state, nullptr, 0); }
+cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
+  return launch_tc(p, from_state, kModeElu, nullptr, 0);
+}
+
+cudaError_t launch_causal_features_tc(const Problem &p, bool from_state) {
+  return launch_tc(p, from_state, kModeIdentity, nullptr, 0);
+}
 
 cudaError_t launch_retention_tc(const Problem &p, bool from_state, const float *log2g, int H) {
   if (!log2g || H < 1 || H > kMaxRetentionHeads) return cudaErrorInvalidValue;
-  return launch_tc(p, from_state, log2g, H);
+  return launch_tc(p, from_state, kModeRetention, log2g, H);
 }
 
 // ---------------------------------------------------------------------------
@@ -1084,7 +1101,7 @@ cudaError_t launch_causal_tc_noalloc(const Problem &p, int dev, bool *too_large)
   set_first_pass(tp, p, t);
   tp.n_exact = (int)std::min<long>(p.N, kExact);
   tp.eps = p.eps;
-  return launch_passes(p, tp, nullptr, nullptr);
+  return launch_passes(p, tp, nullptr, nullptr, kModeElu);
 }
 
 cudaError_t read_and_clear_device_status(unsigned int *value) {

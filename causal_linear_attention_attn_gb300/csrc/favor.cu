@@ -1,0 +1,286 @@
+// Positive random features ("Linear Attention Math", "Feature maps: elu+1 and
+// positive random features"; "线性注意力从头到尾讲清楚" §9):
+//   phi(x)_r = exp(w_r . x - |x|^2 / 2) / sqrt(m)
+// for every row x of X ([rows, d]) and the m projections w_r (the rows of W).
+//
+// Tensor-core path (bf16, m = 128, d in {64, 128}): one persistent CTA per SM
+// walks 128-row tiles.  Thread 0 issues the TMA loads (W once, X tiles
+// double-buffered) and the MMA D = X W^T into an fp32 tensor-memory
+// accumulator; every thread owns one row (its tensor-memory lane), forms
+// |x|^2 from the staged bf16 tile, applies the exponential, and writes bf16
+// features into a swizzled staging tile that TMA stores copy out.  Other
+// shapes and fp32 inputs take a plain CUDA-core kernel.  Every mbarrier wait
+// is bounded; a wait that runs out raises the device status word and the
+// CTA drains what it issued and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace la {
+
+__device__ unsigned int g_favor_status;
+
+namespace {
+using namespace tc;
+
+constexpr int kFavThreads = 128;
+constexpr int kFavM = 128;                 // features of the tensor-core path
+constexpr uint32_t kBlk = 16384;           // [128 rows x 128 bytes], 128-byte swizzled
+constexpr uint32_t kAbortMisaligned = 2u;  // status bit: shared memory base not 1024-aligned
+constexpr uint32_t kBarFav = 1;
+
+template <int D>
+struct FavLayout {
+  static constexpr uint32_t kTile = (D / 64) * kBlk;  // one [128 x D] bf16 tile
+  static constexpr uint32_t W = 0;                    // the projections, [128 x D]
+  static constexpr uint32_t X = W + kTile;            // two stages of X
+  static constexpr uint32_t O = X + 2 * kTile;        // [128 x 128] bf16 output staging
+  static constexpr uint32_t Bars = O + 2 * kBlk;
+  static constexpr uint32_t Misc = Bars + 4 * 8;
+  static constexpr uint32_t Bytes = Misc + 16;
+};
+
+struct FavorParams {
+  CUtensorMap tx, tw, to;  // X [1][rows][D], W [1][128][D], out [1][rows][128], bf16, boxes 64 x 128
+  int tiles;
+};
+
+// K-major operand (rows of 64 K-elements per 16 KB block): k-step ks covers K elements [16ks, 16ks+16).
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int ks) {
+  return sw128_desc(tile + (ks >> 2) * kBlk + (ks & 3) * 32, 16, 1024);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFavThreads, 1) favor_tc_kernel(const __grid_constant__ FavorParams p) {
+  using Lay = FavLayout<D>;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  if (smem_u32(sm) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(&g_favor_status, kAbortMisaligned);
+    return;
+  }
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::Bars);
+  uint64_t *w_full = bars, *x_full = bars + 1, *mma_done = bars + 3;  // x_full[2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::Misc);
+  volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
+  unsigned int *status = &g_favor_status;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int n = blockIdx.x < p.tiles ? (p.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
+  if (tid == 0) {
+    mbar_init(w_full, 1);
+    mbar_init(&x_full[0], 1);
+    mbar_init(&x_full[1], 1);
+    mbar_init(mma_done, 1);
+    *abort_word = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int issued = 0, mmas = 0;  // thread 0: X loads and MMAs issued
+  auto load_x = [&](int i) {
+    const int s = i & 1;
+    mbar_arrive_expect_tx(&x_full[s], Lay::kTile);
+    for (int b = 0; b < D / 64; ++b)
+      tma_load_3d(sm + Lay::X + s * Lay::kTile + b * kBlk, &p.tx, &x_full[s], 64 * b,
+                  ((int)blockIdx.x + i * (int)gridDim.x) * 128, 0);
+    issued = i + 1;
+  };
+  if (tid == 0 && n > 0) {
+    prefetch_tmap(&p.tx);
+    prefetch_tmap(&p.tw);
+    prefetch_tmap(&p.to);
+    mbar_arrive_expect_tx(w_full, Lay::kTile);
+    for (int b = 0; b < D / 64; ++b) tma_load_3d(sm + Lay::W + b * kBlk, &p.tw, w_full, 64 * b, 0, 0);
+    load_x(0);
+    if (n > 1) load_x(1);
+  }
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128, 0, 0);
+  const float inv_sqrt_m = 1.f / sqrtf((float)kFavM);
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+  bool w_ready = false;
+  for (int i = 0; i < n; ++i) {
+    const int s = i & 1;
+    const uint8_t *xs = sm + Lay::X + s * Lay::kTile;
+    bool ok = mbar_wait(&x_full[s], (i >> 1) & 1, abort_word, status);
+    if (bar_or(kBarFav, kFavThreads, !ok)) break;
+    // this thread's row norm from the staged bf16 tile
+    float nrm = 0.f;
+#pragma unroll
+    for (int b = 0; b < D / 64; ++b)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(xs + b * kBlk + sw128_offset(tid, 8 * c));
+        const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(e[j] << 16), hi = __uint_as_float(e[j] & 0xffff0000u);
+          nrm = fmaf(lo, lo, nrm);
+          nrm = fmaf(hi, hi, nrm);
+        }
+      }
+    if (tid == 0) {
+      if (!w_ready) ok = w_ready = mbar_wait(w_full, 0, abort_word, status);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t xa = smem_u32(xs), wa = smem_u32(sm + Lay::W);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, kdesc(xa, ks), kdesc(wa, ks), kIdesc, ks > 0);
+        mma_commit(mma_done);
+        mmas = i + 1;
+      }
+    }
+    if (bar_or(kBarFav, kFavThreads, !ok)) break;
+    ok = mbar_wait(mma_done, i & 1, abort_word, status);
+    if (tid == 0) bulk_wait_read();  // the previous tile's stores have read the staging tile
+    if (bar_or(kBarFav, kFavThreads, !ok)) break;  // also: every row norm of this stage is read
+    tc_fence_after();
+    if (tid == 0 && i + 2 < n) load_x(i + 2);  // the stage is free again
+    // features of this row: exp(w . x - |x|^2 / 2) / sqrt(m), bf16, into the staging tile
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      uint32_t r[32];
+      tmem_ld32(lane_base + cb * 32, r);
+      uint8_t *blk = sm + Lay::O + (cb >> 1) * kBlk;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a = __expf(__uint_as_float(r[8 * q + 2 * j]) - 0.5f * nrm) * inv_sqrt_m;
+          const float b = __expf(__uint_as_float(r[8 * q + 2 * j + 1]) - 0.5f * nrm) * inv_sqrt_m;
+          o[j] = pack_bf16(a, b);
+        }
+        *reinterpret_cast<uint4 *>(blk + sw128_offset(tid, (cb & 1) * 32 + 8 * q)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    tc_fence_before();
+    fence_async_smem();
+    named_bar(kBarFav, kFavThreads);
+    if (tid == 0) {
+      const int row0 = ((int)blockIdx.x + i * (int)gridDim.x) * 128;
+      tma_store_3d(&p.to, sm + Lay::O, 0, row0, 0);
+      tma_store_3d(&p.to, sm + Lay::O + kBlk, 64, row0, 0);
+      bulk_commit();
+    }
+  }
+  if (tid == 0) {
+    bulk_wait_all();
+    // after an abort: copies and MMAs still in flight land before the memory is released
+    if (mmas > 0) wait_drain(mma_done, (mmas - 1) & 1, status);
+    for (int i = max(0, issued - 2); i < issued; ++i) wait_drain(&x_full[i & 1], (i >> 1) & 1, status);
+    if (!w_ready && n > 0) wait_drain(w_full, 0, status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+// One row per block: the row in shared memory, its norm by a block reduction,
+// then every feature as a plain dot product with its projection.
+template <typename Tin>
+__global__ void __launch_bounds__(128) favor_simt_kernel(const Tin *__restrict__ X, const Tin *__restrict__ W,
+                                                         Tin *__restrict__ out, int d, int m) {
+  extern __shared__ float xs[];
+  __shared__ float part[4];
+  const long row = blockIdx.x;
+  const int tid = threadIdx.x;
+  float nrm = 0.f;
+  for (int i = tid; i < d; i += 128) {
+    const float x = ldf(X + row * d + i);
+    xs[i] = x;
+    nrm = fmaf(x, x, nrm);
+  }
+  nrm = warp_sum(nrm);
+  if ((tid & 31) == 0) part[tid >> 5] = nrm;
+  __syncthreads();
+  nrm = part[0] + part[1] + part[2] + part[3];
+  const float inv_sqrt_m = 1.f / sqrtf((float)m);
+  for (int f = tid; f < m; f += 128) {
+    float wx = 0.f;
+    for (int i = 0; i < d; ++i) wx = fmaf(ldf(W + (long)f * d + i), xs[i], wx);
+    const float y = expf(wx - 0.5f * nrm) * inv_sqrt_m;
+    if constexpr (sizeof(Tin) == 4)
+      out[row * m + f] = y;
+    else
+      out[row * m + f] = __float2bfloat16_rn(y);
+  }
+}
+
+bool make_map2(CUtensorMap *map, const void *base, long rows, int cols) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)rows * cols * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_tc(const void *X, const void *W, void *out, long rows, cudaStream_t stream) {
+  using Lay = FavLayout<D>;
+  static std::once_flag once;
+  static cudaError_t attr;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(favor_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::Bytes);
+  });
+  if (attr != cudaSuccess) return attr;
+  FavorParams p;
+  if (!make_map2(&p.tx, X, rows, D) || !make_map2(&p.tw, W, kFavM, D) || !make_map2(&p.to, out, rows, kFavM))
+    return cudaErrorInvalidValue;
+  p.tiles = (int)((rows + 127) / 128);
+  const int sms = std::max(1, device_info(-1).sm_count);
+  LaunchTimer timer(kKFavor, stream);
+  favor_tc_kernel<D><<<std::min(p.tiles, sms), kFavThreads, Lay::Bytes, stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  timer.done(e);
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_favor_features(const void *X, const void *W, void *out, long rows, int d, int m, la_dtype dt,
+                                  cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const DeviceInfo &di = device_info(-1);
+  const bool tc = dt == LA_BF16 && m == kFavM && (d == 64 || d == 128) && rows <= 0x7fffff80L &&
+                  di.cc_major == 10 && di.cc_minor == 3 && tensor_map_encoder() != nullptr;
+  if (tc) return d == 64 ? launch_tc<64>(X, W, out, rows, stream) : launch_tc<128>(X, W, out, rows, stream);
+  LaunchTimer timer(kKFavor, stream);
+  if (dt == LA_F32)
+    favor_simt_kernel<float><<<(unsigned)rows, 128, sizeof(float) * d, stream>>>(
+        (const float *)X, (const float *)W, (float *)out, d, m);
+  else
+    favor_simt_kernel<__nv_bfloat16><<<(unsigned)rows, 128, sizeof(float) * d, stream>>>(
+        (const __nv_bfloat16 *)X, (const __nv_bfloat16 *)W, (__nv_bfloat16 *)out, d, m);
+  const cudaError_t e = cudaGetLastError();
+  timer.done(e);
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+cudaError_t read_and_clear_favor_status(unsigned int *value) {
+  const unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_favor_status, sizeof(unsigned int));
+  if (e == cudaSuccess && *value) e = cudaMemcpyToSymbol(g_favor_status, &zero, sizeof(unsigned int));
+  return e;
+}
+
+}  // namespace la

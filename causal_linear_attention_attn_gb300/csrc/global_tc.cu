@@ -138,8 +138,9 @@ struct UnitWalk {
   }
 };
 
-template <int D, bool kRet = false>
+template <int D, int kMode = kModeElu>
 __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid_constant__ BuildParams p) {
+  constexpr bool kRet = kMode == kModeRetention;
   using Lay = BuildLayout<D, kRet>;
   constexpr int kBuildStages = Lay::kStages;
   constexpr int kUnit = D == 64 ? 128 : 64;
@@ -298,7 +299,8 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
           phi_chunks<4, kBuildPhi>(k, pt, [&](int j, int ch, uint4 x) {
             const int row = ch >> 3;  // 0..127 over the two blocks
             const long tok = tok0 + (D == 64 ? row : (row & 63));
-            const uint4 y = tok < p.N ? phi8(x) : make_uint4(0u, 0u, 0u, 0u);  // rows past the end add nothing
+            // rows past the end add nothing; given features (identity mode) pass unchanged
+            const uint4 y = tok >= p.N ? make_uint4(0u, 0u, 0u, 0u) : kMode == kModeIdentity ? x : phi8(x);
             add8_bf16(za + (D == 64 ? 0 : 8 * (j >> 1)), y);
             return y;
           });
@@ -690,11 +692,11 @@ cudaError_t set_smem_once(F *kernel, uint32_t bytes, std::once_flag &once, cudaE
   return err;
 }
 
-template <int D, bool kRet = false>
+template <int D, int kMode = kModeElu>
 cudaError_t build_smem() {
   static std::once_flag once;
   static cudaError_t err;
-  return set_smem_once(global_build_tc<D, kRet>, BuildLayout<D, kRet>::Bytes, once, err);
+  return set_smem_once(global_build_tc<D, kMode>, BuildLayout<D, kMode == kModeRetention>::Bytes, once, err);
 }
 
 template <int D>
@@ -789,7 +791,8 @@ bool global_tc_supported(const Problem &p) {
 cudaError_t launch_global_tc(const Problem &p) { return p.dk == 64 ? launch_t<64>(p) : launch_t<128>(p); }
 
 cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_per_head, int ctas, int pieces_per_cta,
-                                float *piece_S, float *piece_z, int kernel_id, const float *log2g, int ret_H) {
+                                float *piece_S, float *piece_z, int kernel_id, const float *log2g, int ret_H,
+                                int mode) {
   if (p.dt != LA_BF16 || p.dk != 128 || p.dv != 128 || range_tokens % 64 != 0 || ranges_per_head < 1 || ctas < 1 ||
       pieces_per_cta < 1 || pieces_per_cta > 2 || (log2g && (ret_H < 1 || ret_H > kMaxRetentionHeads)))
     return cudaErrorInvalidValue;
@@ -814,11 +817,17 @@ cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_
   bp.pieces_per_cta = pieces_per_cta;
   bp.ret_H = log2g ? ret_H : 0;
   for (int h = 0; h < kMaxRetentionHeads; ++h) bp.log2g[h] = log2g && h < ret_H ? log2g[h] : 0.f;
-  cudaError_t e = log2g ? build_smem<128, true>() : build_smem<128>();
+  if ((mode == kModeRetention) != (log2g != nullptr)) return cudaErrorInvalidValue;
+  cudaError_t e = mode == kModeRetention  ? build_smem<128, kModeRetention>()
+                  : mode == kModeIdentity ? build_smem<128, kModeIdentity>()
+                                          : build_smem<128>();
   if (e != cudaSuccess) return e;
   LaunchTimer timer(kernel_id, p.stream);
-  if (log2g)
-    global_build_tc<128, true><<<(unsigned)ctas, kBuildThreads, BuildLayout<128, true>::Bytes, p.stream>>>(bp);
+  if (mode == kModeRetention)
+    global_build_tc<128, kModeRetention>
+        <<<(unsigned)ctas, kBuildThreads, BuildLayout<128, true>::Bytes, p.stream>>>(bp);
+  else if (mode == kModeIdentity)
+    global_build_tc<128, kModeIdentity><<<(unsigned)ctas, kBuildThreads, BuildLayout<128>::Bytes, p.stream>>>(bp);
   else
     global_build_tc<128><<<(unsigned)ctas, kBuildThreads, BuildLayout<128>::Bytes, p.stream>>>(bp);
   e = cudaGetLastError();

@@ -35,7 +35,9 @@ cudaError_t launch_causal_backward(const BackwardProblem &b);
 // Exact fp32 CUDA-core chunked causal pass.  Processes tokens [0, n_proc) of
 // every head.  from_state: start from the caller's S, z instead of zero.
 // write_state: store the final S, z.
-cudaError_t launch_causal_simt(const Problem &p, long n_proc, bool from_state, bool write_state);
+// identity: q and k are given features (no phi).
+cudaError_t launch_causal_simt(const Problem &p, long n_proc, bool from_state, bool write_state,
+                               bool identity = false);
 
 // Exact fp32 pass over tokens [0, n_exact) of every head (outputs only),
 // starting from (S0, z0) when given (device pointers), else from zero.  With
@@ -49,6 +51,14 @@ bool causal_tc_supported(const Problem &p);
 cudaError_t launch_causal_tc(const Problem &p, bool from_state);
 // Retention on the same path: head bh decays by 2^log2g[bh % H] (host array, H <= 128).
 cudaError_t launch_retention_tc(const Problem &p, bool from_state, const float *log2g, int H);
+// Normalized causal attention on given features (q, k are phi(q), phi(k)).
+cudaError_t launch_causal_features_tc(const Problem &p, bool from_state);
+
+// Positive random features of `rows` rows of X ([rows, d]) for W ([m, d]) into out ([rows, m]),
+// all of dtype dt; the tensor cores take bf16 with m = 128 and d in {64, 128}.
+cudaError_t launch_favor_features(const void *X, const void *W, void *out, long rows, int d, int m, la_dtype dt,
+                                  cudaStream_t stream);
+cudaError_t read_and_clear_favor_status(unsigned int *value);
 
 // Allocation-free tensor-core causal pass from the zero state: the first
 // pass's partial states use a fixed device array instead of an allocation.
@@ -78,10 +88,14 @@ cudaError_t read_and_clear_global_tc_status(unsigned int *value);
 // Retention: per-head decays gamma_h carried in launch parameters, at most this many heads.
 constexpr int kMaxRetentionHeads = 128;
 
+// What the tensor-core causal passes compute: normalized attention with phi = ELU + 1, retention
+// (decay, no denominator), or normalized attention on features the caller has already applied.
+enum TcMode : int { kModeElu = 0, kModeRetention = 1, kModeIdentity = 2 };
+
 // log2g (host array of ret_H values, or null): retention weights instead of phi and key sums.
 cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_per_head, int ctas, int pieces_per_cta,
                                 float *piece_S, float *piece_z, int kernel_id, const float *log2g = nullptr,
-                                int ret_H = 0);
+                                int ret_H = 0, int mode = kModeElu);
 
 // Read and clear the device status word (bounded-wait timeouts).
 cudaError_t read_and_clear_device_status(unsigned int *value);
@@ -110,7 +124,8 @@ enum KernelId : int {
   kKRetentionState = 8,
   kKRetentionDecode = 9,
   kKBackward = 10,
-  kKNumKernels = 11
+  kKFavor = 11,
+  kKNumKernels = 12
 };
 
 // While profiling is on (la_profile_enable), brackets one launch with a CUDA

@@ -163,10 +163,12 @@ la_status la_device_status(void *stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return la::from_cuda(e);
   unsigned int v = 0, vg = 0;
+  unsigned int vf = 0;
   e = la::read_and_clear_device_status(&v);
   if (e == cudaSuccess) e = la::read_and_clear_global_tc_status(&vg);
+  if (e == cudaSuccess) e = la::read_and_clear_favor_status(&vf);
   if (e != cudaSuccess) return la::from_cuda(e);
-  v |= vg;
+  v |= vg | vf;
   if (v & 1u) return LA_ERR_TIMEOUT;
   return v ? LA_ERR_LAUNCH : LA_OK;  // other bits: a kernel refused to run (e.g. misaligned shared memory)
 }
@@ -256,6 +258,39 @@ la_status la_retention_with_state(const void *q, const void *k, const void *v, f
                                   const float *gamma, int B, int H, int N, int d_k, int d_v, la_dtype dt,
                                   void *stream) {
   return retention_impl(q, k, v, out, S, gamma, B, H, N, d_k, d_v, dt, stream, true);
+}
+
+la_status la_causal_features(const void *phi_q, const void *phi_k, const void *v, float *out, float *S, float *z,
+                             int B, int H, int N, int m, int d_v, float eps, la_dtype dt, void *stream) {
+  la_status st = la::validate(phi_q, phi_k, v, out, S, z, B, H, N, m, d_v, eps, dt);
+  if (st != LA_OK) return st;
+  if ((long)B * H == 0) return LA_OK;
+  int dev;
+  if ((st = la::current_device(&dev)) != LA_OK) return st;
+  Problem p{phi_q, phi_k, v, out, S, z, B * H, (long)N, m, d_v, eps, dt, (cudaStream_t)stream};
+  if (N == 0) {
+    cudaError_t e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)p.BH * m * d_v, p.stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(z, 0, sizeof(float) * (size_t)p.BH * m, p.stream);
+    return la::from_cuda(e);
+  }
+  if (la::causal_tc_supported(p)) return la::from_cuda(la::launch_causal_features_tc(p, false));
+  return la::from_cuda(la::launch_causal_simt(p, p.N, false, true, true));
+}
+
+la_status la_favor_features(const void *x, const void *W, void *phi, int B, int H, int N, int d, int m,
+                            la_dtype dt, void *stream) {
+  if (B < 0 || H < 0 || N < 0 || d <= 0 || m <= 0) return LA_ERR_INVALID_VALUE;
+  const long rows = (long)B * H * N;
+  if ((long)B * H > 0x7fffffffL || rows > 0x7fffffffL) return LA_ERR_INVALID_VALUE;
+  if (rows == 0) return LA_OK;
+  if (!x || !W || !phi) return LA_ERR_INVALID_VALUE;
+  if (dt != LA_F32 && dt != LA_BF16) return LA_ERR_UNSUPPORTED;
+  if (!la::supported_dim(d) || !la::supported_dim(m)) return LA_ERR_UNSUPPORTED;
+  if (!la::aligned16(x) || !la::aligned16(W) || !la::aligned16(phi)) return LA_ERR_MISALIGNED;
+  int dev;
+  la_status st = la::current_device(&dev);
+  if (st != LA_OK) return st;
+  return la::from_cuda(la::launch_favor_features(x, W, phi, rows, d, m, dt, (cudaStream_t)stream));
 }
 
 la_status la_profile_enable(int on) {

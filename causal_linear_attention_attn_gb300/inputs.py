@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the six workloads (no attention arithmetic here).
+"""Seeded synthetic inputs for the seven workloads (no attention arithmetic here).
 
 Every tensor is drawn as float32 ``torch.randn`` from a seeded generator,
 multiplied by its scale, then rounded to the workload's input dtype
@@ -23,7 +23,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    form: str  # "causal", "global", "retention" or "decode"
+    form: str  # "causal", "global", "retention", "favor" or "decode"
     B: int
     H: int
     N: int
@@ -62,6 +62,9 @@ WORKLOADS = {
         Workload("retention_bf16", "retention", 4, 16, 8192, 128, 128, "bf16", 1 / math.sqrt(128), 1.0, 0.0, 1006,
                  note="retention bf16, B=4 H=16 N=8192 d=128, q,k ~ N(0,1)/sqrt(128), v ~ N(0,1), "
                       "gamma_h = 1 - 2^-(5 + h mod 8)"),
+        Workload("favor_bf16", "favor", 4, 16, 8192, 128, 128, "bf16", 128 ** -0.25, 1.0, 1e-6, 1007,
+                 note="causal prefill on positive random features, B=4 H=16 N=8192 d=128, m=128 projections "
+                      "W ~ N(0,1); q,k ~ N(0,1)/128^(1/4) (the softmax kernel exp(q.k/sqrt(d))), v ~ N(0,1)"),
         Workload("decode_bf16", "decode", 256, 32, 1, 128, 128, "bf16", 1 / math.sqrt(128), 1.0, 1e-6, 1005,
                  prefix=1024, prefix_scale=1.0, steps=1000,
                  note="decode step, batch 256 H=32 m=d_v=128, fp32 state from a 1024-token N(0,1) prefix"),
@@ -77,6 +80,12 @@ def retention_gamma(H: int) -> list[float]:
     exact in float32.
     """
     return [1.0 - 2.0 ** -(5 + h % 8) for h in range(H)]
+
+
+def favor_projections(w: Workload, m: int = 128, device: str = "cpu"):
+    """The m random projections of the positive random features, [m, d] ~ N(0, 1),
+    drawn from the workload's seed and rounded to its input dtype."""
+    return _draw((m, w.dk), 1.0, w.torch_dtype, _gen(w.seed * 1_000_003 + 70_000_000, device), device)
 
 
 def _gen(seed: int, device: str):

@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "LA_OK", 1: "LA_ERR_INVALID_VALUE", 2: "LA_ERR_UNSUPPORTED", 
 
 _vp, _fp, _i, _f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _SEQ_ARGS = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _i, _vp]
-for _name in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc"):
+for _name in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc", "la_causal_features"):
     getattr(lib, _name).argtypes = _SEQ_ARGS
     getattr(lib, _name).restype = _i
 for _name in ("la_retention", "la_retention_with_state"):
@@ -38,6 +38,8 @@ lib.la_retention_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, ctypes.POINTER
 lib.la_retention_decode_step.restype = _i
 lib.la_causal_backward.argtypes = [_vp] * 13 + [_i, _i, _i, _i, _i, _f, _i, _vp]
 lib.la_causal_backward.restype = _i
+lib.la_favor_features.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]
+lib.la_favor_features.restype = _i
 lib.la_decode_step.restype = _i
 lib.la_status_string.argtypes = [_i]
 lib.la_status_string.restype = ctypes.c_char_p
@@ -57,7 +59,7 @@ lib.la_profile_read.restype = _i
 # la_kernel ids of the device-time diagnostics
 KERNELS = {"causal_main": 0, "causal_state": 1, "exact_head": 2, "causal_simt": 3, "global_state": 4,
            "global_read": 5, "decode": 6, "retention_main": 7, "retention_state": 8, "retention_decode": 9,
-           "backward": 10}
+           "backward": 10, "favor": 11}
 
 
 class LinAttnError(RuntimeError):
@@ -152,6 +154,29 @@ def la_causal_noalloc(q, k, v, out=None, S=None, z=None, eps: float = 1e-6, stre
     binding only allocates the outputs that were not supplied.
     """
     return _seq_call("la_causal_noalloc", q, k, v, out, S, z, eps, stream)
+
+
+def la_causal_features(phi_q, phi_k, v, out=None, S=None, z=None, eps: float = 1e-6, stream=None):
+    """Causal prefill on given (non-negative) features; returns (out, S, z)."""
+    return _seq_call("la_causal_features", phi_q, phi_k, v, out, S, z, eps, stream)
+
+
+def la_favor_features(x, W, out=None, stream=None):
+    """Positive random features of x [B, H, N, d] for projections W [m, d]: [B, H, N, m], x's dtype."""
+    if not x.is_cuda or not x.is_contiguous() or x.dim() != 4:
+        raise ValueError("x must be a contiguous 4-d CUDA tensor")
+    if not W.is_cuda or not W.is_contiguous() or W.dim() != 2 or W.shape[1] != x.shape[-1] or W.dtype != x.dtype:
+        raise ValueError("W must be a contiguous [m, d] CUDA tensor of x's dtype")
+    B, H, N, d = x.shape
+    m = W.shape[0]
+    if out is None:
+        out = torch.empty(B, H, N, m, dtype=x.dtype, device=x.device)
+    if out.dtype != x.dtype or not out.is_contiguous() or tuple(out.shape) != (B, H, N, m):
+        raise ValueError("out must be a contiguous [B, H, N, m] tensor of x's dtype")
+    rc = lib.la_favor_features(_ptr(x), _ptr(W), _ptr(out), B, H, N, d, m, _dt(x), _stream(stream))
+    if rc != 0:
+        raise LinAttnError("la_favor_features", rc)
+    return out
 
 
 def la_causal_with_state(q, k, v, S, z, out=None, eps: float = 1e-6, stream=None):

@@ -151,6 +151,40 @@ LA_API la_status la_causal_noalloc(const void *q, const void *k, const void *v, 
                                    void *stream);
 
 /*
+ * Positive random features (FAVOR+): for every row x of x ([B,H,N,d]) and the
+ * m projections w_r (the rows of W, [m, d]),
+ *     phi[b,h,t,r] = exp(w_r . x - |x|^2 / 2) / sqrt(m),
+ * so that E[phi(q) . phi(k)] = exp(q . k) for w_r ~ N(0, I).  Source:
+ * "Linear Attention Math", "Feature maps: elu+1 and positive random
+ * features"; "线性注意力从头到尾讲清楚" §9 (approximating the softmax kernel
+ * exp(q^T k / sqrt(d_k)): scale q and k by d_k^(-1/4) first).  W is an input
+ * (random or orthogonal random projections, drawn by the caller).
+ *
+ * x: [B,H,N,d], W: [m,d], phi: [B,H,N,m], all of dtype dt (phi is written).
+ * d and m in {32, 64, 128}.  Tensor cores for bf16 with m = 128 and d in {64,
+ * 128}; CUDA cores otherwise.  Allocates nothing.  Errors as la_causal.
+ * The features feed la_causal_features (or la_global / la_causal with any
+ * caller-side map) as phi(q), phi(k).
+ */
+LA_API la_status la_favor_features(const void *x, const void *W, void *phi, int B, int H, int N, int d, int m,
+                                   la_dtype dt, void *stream);
+
+/*
+ * Causal prefill on features the caller has already applied: as la_causal
+ * with phi the identity, i.e. out_t = phi_q_t^T S_t / (phi_q_t^T z_t + eps),
+ * S_t = sum_{j<=t} phi_k_j v_j^T, z_t = sum_{j<=t} phi_k_j.  For any
+ * non-negative feature map, e.g. la_favor_features ("Linear Attention Math",
+ * "Feature maps: elu+1 and positive random features": the normalized read
+ * needs non-negative features).  phi_q, phi_k: [B,H,N,m] (dtype dt, m in
+ * {32, 64, 128}); other arguments, results and errors as la_causal.  The
+ * tensor-core path (bf16, m = d_v = 128) takes the features as given, so no
+ * leading tokens are recomputed in fp32.
+ */
+LA_API la_status la_causal_features(const void *phi_q, const void *phi_k, const void *v, float *out, float *S,
+                                    float *z, int B, int H, int N, int m, int d_v, float eps, la_dtype dt,
+                                    void *stream);
+
+/*
  * Retention: the causal recurrence with an explicit per-head decay and no
  * denominator,
  *     S_t = gamma_h S_{t-1} + k_t v_t^T,   out_t = q_t^T S_t,   S_{-1} = 0,
@@ -297,7 +331,8 @@ typedef enum {
   LA_KERNEL_RETENTION_MAIN = 7,   /* tensor-core retention pass */
   LA_KERNEL_RETENTION_STATE = 8,  /* its first pass over earlier segments */
   LA_KERNEL_RETENTION_DECODE = 9, /* recurrent retention step */
-  LA_KERNEL_BACKWARD = 10         /* causal backward */
+  LA_KERNEL_BACKWARD = 10,        /* causal backward */
+  LA_KERNEL_FAVOR = 11            /* positive random features */
 } la_kernel;
 
 /*

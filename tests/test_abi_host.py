@@ -27,7 +27,7 @@ def test_header_declares_the_entry_points():
     names = _declared_symbols()
     for n in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc", "la_decode_step", "la_status_string",
               "la_version", "la_retention", "la_retention_with_state", "la_retention_decode_step",
-              "la_causal_backward"):
+              "la_causal_backward", "la_favor_features", "la_causal_features"):
         assert n in names
 
 
@@ -147,6 +147,26 @@ def test_retention_decode_validation():
     assert call(H=129, gamma=(0.9,) * 129) == UNSUPPORTED
     assert call(S=P + 4) == MISALIGNED
     assert call(B=0) == OK
+
+
+def test_favor_validation():
+    f = L.lib.la_favor_features
+
+    def call(x=P, Wp=P, phi=P, B=1, H=2, N=8, d=128, m=128, dt=1):
+        return f(x, Wp, phi, B, H, N, d, m, dt, None)
+
+    assert call(x=None) == INVALID
+    assert call(phi=None) == INVALID
+    assert call(N=-1) == INVALID
+    assert call(m=0) == INVALID
+    assert call(m=96) == UNSUPPORTED
+    assert call(d=48) == UNSUPPORTED
+    assert call(dt=4) == UNSUPPORTED
+    assert call(Wp=P + 2) == MISALIGNED
+    assert call(B=0) == OK
+    assert call(N=0, x=None, Wp=None, phi=None) == OK
+    assert seq("la_causal_features", q=None) == INVALID
+    assert seq("la_causal_features", dk=48) == UNSUPPORTED
 
 
 def test_backward_validation():

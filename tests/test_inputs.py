@@ -8,12 +8,21 @@ from causal_linear_attention_attn_gb300 import inputs
 W = inputs.WORKLOADS
 
 
-def test_workloads_match_the_five_configurations_and_retention():
+def test_workloads_match_the_five_configurations_and_the_next_rows():
     assert [(w.B, w.H, w.N, w.dk, w.dv, w.dtype) for w in W.values()] == [
         (1, 2, 256, 32, 32, "f32"), (8, 16, 4096, 64, 64, "bf16"), (4, 16, 8192, 128, 128, "bf16"),
-        (1, 32, 131072, 128, 128, "bf16"), (4, 16, 8192, 128, 128, "bf16"), (256, 32, 1, 128, 128, "bf16")]
+        (1, 32, 131072, 128, 128, "bf16"), (4, 16, 8192, 128, 128, "bf16"), (4, 16, 8192, 128, 128, "bf16"),
+        (256, 32, 1, 128, 128, "bf16")]
     assert W["decode_bf16"].prefix == 1024 and W["decode_bf16"].steps == 1000
     assert all(w.eps == 1e-6 for w in W.values() if w.form != "retention")
+
+
+def test_favor_projections():
+    w = W["favor_bf16"]
+    P = inputs.favor_projections(w)
+    assert P.shape == (128, 128) and P.dtype == torch.bfloat16
+    assert torch.equal(P, inputs.favor_projections(w))
+    assert abs(P.float().std().item() - 1.0) < 0.05
 
 
 def test_retention_gammas():
