@@ -289,6 +289,8 @@ def kernel_bytes(w, kernel: str) -> float:
         return w.BH * (w.N * w.dk * ib + state + w.N * 4 * w.dv)
     if kernel == "decode":
         return decode_bytes(w)
+    if kernel == "backward":
+        return backward_bytes(w)
     if kernel == "favor":  # one launch: the rows of q (or k) in, their 128 features out, the projections
         return w.BH * w.N * (w.dk + 128) * ib + 128 * w.dk * ib
     return seq_bytes(w)
@@ -458,6 +460,29 @@ def run_favor(L, w, steps, warmup, world, stream, hbm, src):
             "gpu_launches": launches}
 
 
+def backward_bytes(w) -> float:
+    """Algorithmic HBM bytes of one causal backward: q, k, v and the fp32 upstream
+    gradient read, fp32 dq, dk, dv written."""
+    return w.BH * w.N * ((2 * w.dk + w.dv) * in_bytes(w) + 4 * w.dv + 4 * (2 * w.dk + w.dv))
+
+
+def run_backward(L, w, steps, warmup, world, stream, hbm, src):
+    """Gradient of the causal prefill (la_causal_backward) for a seeded upstream gradient."""
+    q, k, v = (t.cuda() for t in inputs.make_qkv(w, device="cuda"))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed + 17)
+    dO = torch.randn(w.B, w.H, w.N, w.dv, generator=g, device="cuda")
+    call = lambda: L.la_causal_backward(q, k, v, dO, eps=w.eps, stream=stream)
+    n0 = L.kernel_launches()
+    ms = time_device(call, steps, warmup, world, stream, L)
+    launches = (L.kernel_launches() - n0) // (2 * steps + warmup) * steps
+    ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
+    rl, table = dominant_roofline(L, w, steps, hbm, src, w.name + "_backward")
+    return {"workload": w.name + " backward", "roofline": rl, "tokens_per_s": world * w.BH * w.N / (ms * 1e-3), "ms_per_call": ms,
+            "step_roofline": roofline(backward_bytes(w), ms, hbm, src, None), "kernels": table,
+            "gpu_launches": launches, "note": "exact fp32 CUDA-core kernel (one CTA per head)"}
+
+
 def retention_decode_bytes(w) -> float:
     """Algorithmic HBM bytes of one retention step: S read and written (fp32, no z),
     q,k,v read, fp32 out written."""
@@ -574,6 +599,11 @@ def main_ours(args):
             forms["favor_bf16"] = run_favor(L, wf, args.steps, args.warmup, world, stream, hbm, src)
             forms["favor_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
+        if "causal_bf16_backward" in extras:
+            wb = rank_workload(inputs.WORKLOADS["causal_bf16"], rank)
+            forms["causal_bf16_backward"] = run_backward(L, wb, 3, args.warmup, world, stream, hbm, src)
+            forms["causal_bf16_backward"]["clocks"] = clk.summary(*LAST_WINDOW)
+            torch.cuda.empty_cache()
         if "decode_bf16" in extras:
             wd = rank_workload(decode_workload(args), rank)
             forms["decode_bf16"] = run_decode(L, wd, args.decode_steps, args.warmup, world, stream, hbm, src)
@@ -640,7 +670,7 @@ def parse(argv=None):
     ap.add_argument("--decode-batch", type=int, default=0, help="decode forms: batch instead of 256 (profiling)")
     ap.add_argument("--no-extras", action="store_true", help="time the headline workload only")
     ap.add_argument("--forms", default="global_bf16,causal_bf16_long,causal_bf16_with_state,retention_bf16,favor_bf16,"
-                                     "decode_bf16,retention_decode_bf16",
+                                     "causal_bf16_backward,decode_bf16,retention_decode_bf16",
                     help="comma-separated other forms timed after the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-step-s", type=float, default=10.0, help="max CPU seconds per reference step")
