@@ -33,8 +33,8 @@ constexpr int kT = 64;  // tokens per chunk
 constexpr int kThreads = 256;
 
 size_t bwd_smem_bytes(int dk, int dv) {
-  const size_t dkp = dk + 1;
-  return sizeof(float) * ((size_t)dk * dv + dk + 2 * kT * dkp + 2 * (size_t)kT * dv + 2 * (size_t)kT * (kT + 1) +
+  const size_t dkp = dk + 1, dvp = dv + 1;
+  return sizeof(float) * ((size_t)dk * dvp + dk + 2 * kT * dkp + kT * dvp + (size_t)kT * dv + 2 * (size_t)kT * (kT + 1) +
                           2 * kT);
 }
 
@@ -47,13 +47,14 @@ __global__ void __launch_bounds__(kThreads)
                            float *__restrict__ dv_g, float *__restrict__ dS0, float *__restrict__ dz0,
                            float *__restrict__ G, long N, int dk, int dv, float eps) {
   extern __shared__ float sm[];
-  const int dkp = dk + 1;  // padded rows: conflict-free column walks
-  float *S = sm;                   // [dk][dv] state (pass 1), U (pass 2)
-  float *z = S + dk * dv;          // [dk]     normalizer (pass 1), u (pass 2)
+  // padded rows (dk + 1, dv + 1): lanes that walk consecutive rows hit distinct banks
+  const int dkp = dk + 1, dvp = dv + 1;
+  float *S = sm;                   // [dk][dvp] state (pass 1), U (pass 2)
+  float *z = S + dk * dvp;         // [dk]      normalizer (pass 1), u (pass 2)
   float *Qs = z + dk;              // [kT][dkp] phi(q)
   float *Ks = Qs + kT * dkp;       // [kT][dkp] phi(k)
-  float *Vs = Ks + kT * dkp;       // [kT][dv]  v
-  float *Gs = Vs + kT * dv;        // [kT][dv]  dO, then gnum
+  float *Vs = Ks + kT * dkp;       // [kT][dvp] v
+  float *Gs = Vs + kT * dvp;       // [kT][dv]  dO, then gnum
   float *A = Gs + kT * dv;         // [kT][kT+1] phi(q_t).phi(k_j), j <= t
   float *Bm = A + kT * (kT + 1);   // [kT][kT+1] v_j.gnum_t + gden_t, j <= t
   float *den = Bm + kT * (kT + 1); // [kT]
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kThreads)
   float *dqh = dq + bh * N * dk, *dkh = dk_g + bh * N * dk, *dvh = dv_g + bh * N * dv;
   float *Gh = G + bh * N * (dv + 1);  // per token: gnum (dv), gden
 
-  for (int e = tid; e < dk * dv; e += kThreads) S[e] = S0 ? S0[bh * dk * dv + e] : 0.f;
+  for (int e = tid; e < dk * dv; e += kThreads) S[(e / dv) * dvp + e % dv] = S0 ? S0[bh * dk * dv + e] : 0.f;
   for (int i = tid; i < dk; i += kThreads) z[i] = z0 ? z0[bh * dk + i] : 0.f;
 
   // ---------------- pass 1: chunks in order ----------------
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(kThreads)
       Ks[t * dkp + i] = phi(ldf(kh + (t0 + t) * dk + i));
     }
     for (int e = tid; e < T * dv; e += kThreads) {
-      Vs[e] = ldf(vh + t0 * dv + e);
+      Vs[(e / dv) * dvp + e % dv] = ldf(vh + t0 * dv + e);
       Gs[e] = oh[t0 * dv + e];
     }
     __syncthreads();
@@ -106,8 +107,9 @@ __global__ void __launch_bounds__(kThreads)
         float dot = 0.f;
         for (int c = lane; c < dv; c += 32) {
           float n = 0.f;
-          for (int i = 0; i < dk; ++i) n = fmaf(Qs[t * dkp + i], S[i * dv + c], n);
-          for (int j = 0; j <= t; ++j) n = fmaf(A[t * (kT + 1) + j], Vs[j * dv + c], n);
+#pragma unroll 8
+          for (int i = 0; i < dk; ++i) n = fmaf(Qs[t * dkp + i], S[i * dvp + c], n);
+          for (int j = 0; j <= t; ++j) n = fmaf(A[t * (kT + 1) + j], Vs[j * dvp + c], n);
           dot = fmaf(Gs[t * dv + c], n / den[t], dot);
         }
         dot = warp_sum(dot);
@@ -125,7 +127,8 @@ __global__ void __launch_bounds__(kThreads)
       const int t = e / T, j = e - t * T;
       float b = 0.f;
       if (j <= t) {
-        for (int c = 0; c < dv; ++c) b = fmaf(Vs[j * dv + c], Gs[t * dv + c], b);
+#pragma unroll 8
+        for (int c = 0; c < dv; ++c) b = fmaf(Vs[j * dvp + c], Gs[t * dv + c], b);
         b += gd[t];
       }
       Bm[t * (kT + 1) + j] = b;
@@ -139,7 +142,8 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = tid; e < T * dk; e += kThreads) {
       const int t = e / dk, i = e - t * dk;
       float g = z[i] * gd[t];
-      for (int c = 0; c < dv; ++c) g = fmaf(S[i * dv + c], Gs[t * dv + c], g);
+#pragma unroll 8
+      for (int c = 0; c < dv; ++c) g = fmaf(S[i * dvp + c], Gs[t * dv + c], g);
       for (int j = 0; j <= t; ++j) g = fmaf(Bm[t * (kT + 1) + j], Ks[j * dkp + i], g);
       dqh[(t0 + t) * dk + i] = g * fminf(Qs[t * dkp + i], 1.f);
     }
@@ -148,8 +152,9 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = tid; e < dk * dv; e += kThreads) {
       const int i = e / dv, c = e - i * dv;
       float s = 0.f;
-      for (int j = 0; j < T; ++j) s = fmaf(Ks[j * dkp + i], Vs[j * dv + c], s);
-      S[e] += s;
+#pragma unroll 8
+      for (int j = 0; j < T; ++j) s = fmaf(Ks[j * dkp + i], Vs[j * dvp + c], s);
+      S[i * dvp + c] += s;
     }
     for (int i = tid; i < dk; i += kThreads) {
       float s = 0.f;
@@ -160,7 +165,7 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---------------- pass 2: chunks in reverse ----------------
   __syncthreads();
-  for (int e = tid; e < dk * dv; e += kThreads) S[e] = dSN ? dSN[bh * dk * dv + e] : 0.f;  // U
+  for (int e = tid; e < dk * dv; e += kThreads) S[(e / dv) * dvp + e % dv] = dSN ? dSN[bh * dk * dv + e] : 0.f;  // U
   for (int i = tid; i < dk; i += kThreads) z[i] = dzN ? dzN[bh * dk + i] : 0.f;            // u
   const long nch = (N + kT - 1) / kT;
   for (long ci = nch - 1; ci >= 0; --ci) {
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     for (int e = tid; e < T * dv; e += kThreads) {
       const int t = e / dv, c = e - t * dv;
-      Vs[e] = ldf(vh + t0 * dv + e);
+      Vs[t * dvp + c] = ldf(vh + t0 * dv + e);
       Gs[e] = Gh[(t0 + t) * (dv + 1) + c];
     }
     for (int t = tid; t < T; t += kThreads) gd[t] = Gh[(t0 + t) * (dv + 1) + dv];
@@ -183,8 +188,10 @@ __global__ void __launch_bounds__(kThreads)
       const int t = e / T, j = e - t * T;
       float a = 0.f, b = 0.f;
       if (j <= t) {
+#pragma unroll 8
         for (int i = 0; i < dk; ++i) a = fmaf(Qs[t * dkp + i], Ks[j * dkp + i], a);
-        for (int c = 0; c < dv; ++c) b = fmaf(Vs[j * dv + c], Gs[t * dv + c], b);
+#pragma unroll 8
+        for (int c = 0; c < dv; ++c) b = fmaf(Vs[j * dvp + c], Gs[t * dv + c], b);
         b += gd[t];
       }
       A[t * (kT + 1) + j] = a;
@@ -195,7 +202,8 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = tid; e < T * dk; e += kThreads) {
       const int j = e / dk, i = e - j * dk;
       float g = z[i];
-      for (int c = 0; c < dv; ++c) g = fmaf(S[i * dv + c], Vs[j * dv + c], g);
+#pragma unroll 8
+      for (int c = 0; c < dv; ++c) g = fmaf(S[i * dvp + c], Vs[j * dvp + c], g);
       for (int t = j; t < T; ++t) g = fmaf(Bm[t * (kT + 1) + j], Qs[t * dkp + i], g);
       dkh[(t0 + j) * dk + i] = g * fminf(Ks[j * dkp + i], 1.f);
     }
@@ -203,7 +211,8 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = tid; e < T * dv; e += kThreads) {
       const int j = e / dv, c = e - j * dv;
       float g = 0.f;
-      for (int i = 0; i < dk; ++i) g = fmaf(S[i * dv + c], Ks[j * dkp + i], g);
+#pragma unroll 8
+      for (int i = 0; i < dk; ++i) g = fmaf(S[i * dvp + c], Ks[j * dkp + i], g);
       for (int t = j; t < T; ++t) g = fmaf(A[t * (kT + 1) + j], Gs[t * dv + c], g);
       dvh[(t0 + j) * dv + c] = g;
     }
@@ -212,8 +221,9 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = tid; e < dk * dv; e += kThreads) {
       const int i = e / dv, c = e - i * dv;
       float s = 0.f;
+#pragma unroll 8
       for (int t = 0; t < T; ++t) s = fmaf(Qs[t * dkp + i], Gs[t * dv + c], s);
-      S[e] += s;
+      S[i * dvp + c] += s;
     }
     for (int i = tid; i < dk; i += kThreads) {
       float s = 0.f;
@@ -223,7 +233,7 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
   if (dS0)
-    for (int e = tid; e < dk * dv; e += kThreads) dS0[bh * dk * dv + e] = S[e];
+    for (int e = tid; e < dk * dv; e += kThreads) dS0[bh * dk * dv + e] = S[(e / dv) * dvp + e % dv];
   if (dz0)
     for (int i = tid; i < dk; i += kThreads) dz0[bh * dk + i] = z[i];
 }
