@@ -21,6 +21,12 @@
 //     gden (kept in a scratch row per token), and dq;
 //   pass 2 (chunks in reverse): U, u in place of S, z; per chunk dk and dv
 //     from the carried U, u and the chunk's own masked terms.
+// Every product is a small matrix product over shared-memory operands: the
+// 256 threads form a 16 x 16 grid and thread (ty, tx) accumulates the rows
+// ty + 16 r and columns tx + 16 c of the result in registers, loading each
+// operand once per row or column it serves.  Rows of phi(Q), phi(K), V and S
+// are padded by one float so that lanes walking consecutive rows hit
+// distinct banks.
 #include <algorithm>
 
 #include "common.cuh"
@@ -29,230 +35,317 @@
 namespace la {
 namespace {
 
-constexpr int kT = 64;  // tokens per chunk
-constexpr int kThreads = 256;
+constexpr int kT = 64;          // tokens per chunk
+constexpr int kThreads = 256;   // a 16 x 16 grid of threads
 
-size_t bwd_smem_bytes(int dk, int dv) {
-  const size_t dkp = dk + 1, dvp = dv + 1;
-  return sizeof(float) * ((size_t)dk * dvp + dk + 2 * kT * dkp + kT * dvp + (size_t)kT * dv + 2 * (size_t)kT * (kT + 1) +
-                          2 * kT);
+template <int DK, int DV>
+struct BwdSmem {
+  static constexpr int KP = DK + 1, VP = DV + 1, AP = kT + 1;  // padded row lengths
+  static constexpr size_t Floats =
+      (size_t)DK * VP + DK + 2 * (size_t)kT * KP + (size_t)kT * VP + (size_t)kT * DV + 2 * (size_t)kT * AP + 2 * kT;
+  static constexpr size_t Bytes = Floats * sizeof(float);
+};
+static_assert(BwdSmem<128, 128>::Bytes <= 232448, "shared memory budget");
+
+// acc[r][c] += sum_{k < K} a(ty + 16 r, k) b(k, tx + 16 c)
+template <int TR, int TC, typename FA, typename FB>
+__device__ __forceinline__ void tile_fma(float (&acc)[TR][TC], int K, int ty, int tx, FA a, FB b) {
+#pragma unroll 4
+  for (int k = 0; k < K; ++k) {
+    float av[TR], bv[TC];
+#pragma unroll
+    for (int r = 0; r < TR; ++r) av[r] = a(ty + 16 * r, k);
+#pragma unroll
+    for (int c = 0; c < TC; ++c) bv[c] = b(k, tx + 16 * c);
+#pragma unroll
+    for (int r = 0; r < TR; ++r)
+#pragma unroll
+      for (int c = 0; c < TC; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+  }
 }
 
-template <typename Tin>
-__global__ void __launch_bounds__(kThreads)
+template <int TR, int TC>
+__device__ __forceinline__ void zero(float (&acc)[TR][TC]) {
+#pragma unroll
+  for (int r = 0; r < TR; ++r)
+#pragma unroll
+    for (int c = 0; c < TC; ++c) acc[r][c] = 0.f;
+}
+
+template <typename Tin, int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
     causal_backward_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                            const float *__restrict__ dout, const float *__restrict__ S0,
                            const float *__restrict__ z0, const float *__restrict__ dSN,
                            const float *__restrict__ dzN, float *__restrict__ dq, float *__restrict__ dk_g,
                            float *__restrict__ dv_g, float *__restrict__ dS0, float *__restrict__ dz0,
-                           float *__restrict__ G, long N, int dk, int dv, float eps) {
+                           float *__restrict__ G, long N, float eps) {
+  using L = BwdSmem<DK, DV>;
+  constexpr int KP = L::KP, VP = L::VP, AP = L::AP;
+  constexpr int RK = DK / 16, RV = DV / 16;  // register tile widths over features and values
   extern __shared__ float sm[];
-  // padded rows (dk + 1, dv + 1): lanes that walk consecutive rows hit distinct banks
-  const int dkp = dk + 1, dvp = dv + 1;
-  float *S = sm;                   // [dk][dvp] state (pass 1), U (pass 2)
-  float *z = S + dk * dvp;         // [dk]      normalizer (pass 1), u (pass 2)
-  float *Qs = z + dk;              // [kT][dkp] phi(q)
-  float *Ks = Qs + kT * dkp;       // [kT][dkp] phi(k)
-  float *Vs = Ks + kT * dkp;       // [kT][dvp] v
-  float *Gs = Vs + kT * dvp;       // [kT][dv]  dO, then gnum
-  float *A = Gs + kT * dv;         // [kT][kT+1] phi(q_t).phi(k_j), j <= t
-  float *Bm = A + kT * (kT + 1);   // [kT][kT+1] v_j.gnum_t + gden_t, j <= t
-  float *den = Bm + kT * (kT + 1); // [kT]
-  float *gd = den + kT;            // [kT] gden
+  float *S = sm;              // [DK][VP] state (pass 1), U (pass 2)
+  float *z = S + DK * VP;     // [DK]     normalizer (pass 1), u (pass 2)
+  float *Qs = z + DK;         // [kT][KP] phi(q)
+  float *Ks = Qs + kT * KP;   // [kT][KP] phi(k)
+  float *Vs = Ks + kT * KP;   // [kT][VP] v
+  float *Gs = Vs + kT * VP;   // [kT][DV] dO, then gnum
+  float *A = Gs + kT * DV;    // [kT][AP] phi(q_t).phi(k_j), j <= t
+  float *Bm = A + kT * AP;    // [kT][AP] v_j.gnum_t + gden_t, j <= t
+  float *den = Bm + kT * AP;  // [kT]
+  float *gd = den + kT;       // [kT] gden
 
   const long bh = blockIdx.x;
-  const int tid = threadIdx.x;
-  const Tin *qh = q + bh * N * dk, *kh = k + bh * N * dk, *vh = v + bh * N * dv;
-  const float *oh = dout + bh * N * dv;
-  float *dqh = dq + bh * N * dk, *dkh = dk_g + bh * N * dk, *dvh = dv_g + bh * N * dv;
-  float *Gh = G + bh * N * (dv + 1);  // per token: gnum (dv), gden
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const Tin *qh = q + bh * N * DK, *kh = k + bh * N * DK, *vh = v + bh * N * DV;
+  const float *oh = dout + bh * N * DV;
+  float *dqh = dq + bh * N * DK, *dkh = dk_g + bh * N * DK, *dvh = dv_g + bh * N * DV;
+  float *Gh = G + bh * N * (DV + 1);  // per token: gnum (DV), gden
 
-  for (int e = tid; e < dk * dv; e += kThreads) S[(e / dv) * dvp + e % dv] = S0 ? S0[bh * dk * dv + e] : 0.f;
-  for (int i = tid; i < dk; i += kThreads) z[i] = z0 ? z0[bh * dk + i] : 0.f;
+  // operand accessors (row, column) of the products below
+  auto aQ = [&](int t, int i) { return Qs[t * KP + i]; };
+  auto bKt = [&](int i, int j) { return Ks[j * KP + i]; };
+  auto bS = [&](int i, int c) { return S[i * VP + c]; };
+  auto bSt = [&](int c, int i) { return S[i * VP + c]; };
+  auto aA = [&](int t, int j) { return A[t * AP + j]; };
+  auto bV = [&](int j, int c) { return Vs[j * VP + c]; };
+  auto bVt = [&](int c, int j) { return Vs[j * VP + c]; };
+  auto aG = [&](int t, int c) { return Gs[t * DV + c]; };
+
+  for (int e = tid; e < DK * DV; e += kThreads) S[(e / DV) * VP + e % DV] = S0 ? S0[bh * DK * DV + e] : 0.f;
+  for (int i = tid; i < DK; i += kThreads) z[i] = z0 ? z0[bh * DK + i] : 0.f;
+
+  // masked scores A = tril(phi(Q) phi(K)^T) and score gradients Bm = tril(gnum V^T + gden)
+  auto scores = [&](int T, bool with_b) {
+    float acc[4][4];
+    zero(acc);
+    tile_fma(acc, DK, ty, tx, aQ, bKt);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int t = ty + 16 * r, j = tx + 16 * c;
+        A[t * AP + j] = (j <= t && t < T) ? acc[r][c] : 0.f;
+      }
+    if (!with_b) return;
+    zero(acc);
+    tile_fma(acc, DV, ty, tx, aG, bVt);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int t = ty + 16 * r, j = tx + 16 * c;
+        Bm[t * AP + j] = (j <= t && t < T) ? acc[r][c] + gd[t] : 0.f;
+      }
+  };
 
   // ---------------- pass 1: chunks in order ----------------
   for (long t0 = 0; t0 < N; t0 += kT) {
     const int T = (int)min((long)kT, N - t0);
     __syncthreads();  // the previous chunk is fully consumed
-    for (int e = tid; e < T * dk; e += kThreads) {
-      const int t = e / dk, i = e - t * dk;
-      Qs[t * dkp + i] = phi(ldf(qh + (t0 + t) * dk + i));
-      Ks[t * dkp + i] = phi(ldf(kh + (t0 + t) * dk + i));
+    for (int e = tid; e < T * DK; e += kThreads) {
+      const int t = e / DK, i = e - t * DK;
+      Qs[t * KP + i] = phi(ldf(qh + (t0 + t) * DK + i));
+      Ks[t * KP + i] = phi(ldf(kh + (t0 + t) * DK + i));
     }
-    for (int e = tid; e < T * dv; e += kThreads) {
-      Vs[(e / dv) * dvp + e % dv] = ldf(vh + t0 * dv + e);
-      Gs[e] = oh[t0 * dv + e];
+    for (int e = tid; e < T * DV; e += kThreads) {
+      Vs[(e / DV) * VP + e % DV] = ldf(vh + t0 * DV + e);
+      Gs[e] = oh[t0 * DV + e];
     }
     __syncthreads();
-    for (int e = tid; e < T * T; e += kThreads) {
-      const int t = e / T, j = e - t * T;
-      float a = 0.f;
-      if (j <= t)
-        for (int i = 0; i < dk; ++i) a = fmaf(Qs[t * dkp + i], Ks[j * dkp + i], a);
-      A[t * (kT + 1) + j] = a;
-    }
+    scores(T, false);
     __syncthreads();
     for (int t = tid; t < T; t += kThreads) {
       float d = 0.f;
-      for (int i = 0; i < dk; ++i) d = fmaf(Qs[t * dkp + i], z[i], d);
+      for (int i = 0; i < DK; ++i) d = fmaf(Qs[t * KP + i], z[i], d);
       float a = 0.f;
-      for (int j = 0; j <= t; ++j) a += A[t * (kT + 1) + j];
+      for (int j = 0; j <= t; ++j) a += A[t * AP + j];
       den[t] = (d + a) + eps;
     }
     __syncthreads();
-    // outputs o_t (recomputed), dO_t . o_t per row by one warp each
     {
-      const int warp = tid >> 5, lane = tid & 31;
-      for (int t = warp; t < T; t += kThreads / 32) {
+      // outputs o_t = (phi(q_t) S_prev + sum_j A_tj v_j) / den_t, then gden_t = -(dO_t . o_t) / den_t
+      float acc[4][RV];
+      zero(acc);
+      tile_fma(acc, DK, ty, tx, aQ, bS);
+      tile_fma(acc, T, ty, tx, aA, bV);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int t = ty + 16 * r;
         float dot = 0.f;
-        for (int c = lane; c < dv; c += 32) {
-          float n = 0.f;
-#pragma unroll 8
-          for (int i = 0; i < dk; ++i) n = fmaf(Qs[t * dkp + i], S[i * dvp + c], n);
-          for (int j = 0; j <= t; ++j) n = fmaf(A[t * (kT + 1) + j], Vs[j * dvp + c], n);
-          dot = fmaf(Gs[t * dv + c], n / den[t], dot);
+        if (t < T) {
+          const float inv = 1.f / den[t];
+#pragma unroll
+          for (int c = 0; c < RV; ++c) dot = fmaf(Gs[t * DV + tx + 16 * c], acc[r][c] * inv, dot);
         }
-        dot = warp_sum(dot);
-        if (lane == 0) gd[t] = -dot / den[t];
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (tx == 0 && t < T) gd[t] = -dot / den[t];
       }
     }
     __syncthreads();
-    for (int e = tid; e < T * dv; e += kThreads) {
-      const int t = e / dv;
-      Gs[e] /= den[t];  // gnum
+    for (int e = tid; e < T * DV; e += kThreads) Gs[e] /= den[e / DV];  // gnum
+    __syncthreads();
+    for (int e = tid; e < T * (DV + 1); e += kThreads) {
+      const int t = e / (DV + 1), c = e - t * (DV + 1);
+      Gh[(t0 + t) * (DV + 1) + c] = c < DV ? Gs[t * DV + c] : gd[t];
+    }
+    {
+      // Bm (the masked score gradients), as in pass 2
+      float acc[4][4];
+      zero(acc);
+      tile_fma(acc, DV, ty, tx, aG, bVt);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int t = ty + 16 * r, j = tx + 16 * c;
+          Bm[t * AP + j] = (j <= t && t < T) ? acc[r][c] + gd[t] : 0.f;
+        }
     }
     __syncthreads();
-    // B_tj = v_j . gnum_t + gden_t (j <= t); the scratch rows of gnum and gden
-    for (int e = tid; e < T * T; e += kThreads) {
-      const int t = e / T, j = e - t * T;
-      float b = 0.f;
-      if (j <= t) {
-#pragma unroll 8
-        for (int c = 0; c < dv; ++c) b = fmaf(Vs[j * dvp + c], Gs[t * dv + c], b);
-        b += gd[t];
+    {
+      // dphi(q_t) = S_prev gnum_t + z_prev gden_t + sum_{j <= t} Bm_tj phi(k_j)
+      float acc[4][RK];
+      zero(acc);
+      tile_fma(acc, DV, ty, tx, aG, bSt);
+      tile_fma(acc, T, ty, tx, [&](int t, int j) { return Bm[t * AP + j]; }, [&](int j, int i) { return Ks[j * KP + i]; });
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int t = ty + 16 * r;
+        if (t < T)
+#pragma unroll
+          for (int c = 0; c < RK; ++c) {
+            const int i = tx + 16 * c;
+            dqh[(t0 + t) * DK + i] = (acc[r][c] + z[i] * gd[t]) * fminf(Qs[t * KP + i], 1.f);
+          }
       }
-      Bm[t * (kT + 1) + j] = b;
-    }
-    for (int e = tid; e < T * (dv + 1); e += kThreads) {
-      const int t = e / (dv + 1), c = e - t * (dv + 1);
-      Gh[(t0 + t) * (dv + 1) + c] = c < dv ? Gs[t * dv + c] : gd[t];
     }
     __syncthreads();
-    // dphi(q_t) = S_prev gnum_t + z_prev gden_t + sum_{j <= t} B_tj phi(k_j)
-    for (int e = tid; e < T * dk; e += kThreads) {
-      const int t = e / dk, i = e - t * dk;
-      float g = z[i] * gd[t];
-#pragma unroll 8
-      for (int c = 0; c < dv; ++c) g = fmaf(S[i * dvp + c], Gs[t * dv + c], g);
-      for (int j = 0; j <= t; ++j) g = fmaf(Bm[t * (kT + 1) + j], Ks[j * dkp + i], g);
-      dqh[(t0 + t) * dk + i] = g * fminf(Qs[t * dkp + i], 1.f);
-    }
-    __syncthreads();
-    // fold the chunk into the state
-    for (int e = tid; e < dk * dv; e += kThreads) {
-      const int i = e / dv, c = e - i * dv;
-      float s = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < T; ++j) s = fmaf(Ks[j * dkp + i], Vs[j * dvp + c], s);
-      S[i * dvp + c] += s;
-    }
-    for (int i = tid; i < dk; i += kThreads) {
-      float s = 0.f;
-      for (int j = 0; j < T; ++j) s += Ks[j * dkp + i];
-      z[i] += s;
+    {
+      // fold the chunk into the state: S += phi(K)^T V, z += colsum phi(K)
+      float acc[RK][RV];
+      zero(acc);
+      tile_fma(acc, T, ty, tx, [&](int i, int j) { return Ks[j * KP + i]; }, bV);
+#pragma unroll
+      for (int r = 0; r < RK; ++r)
+#pragma unroll
+        for (int c = 0; c < RV; ++c) S[(ty + 16 * r) * VP + tx + 16 * c] += acc[r][c];
+      for (int i = tid; i < DK; i += kThreads) {
+        float s = 0.f;
+        for (int j = 0; j < T; ++j) s += Ks[j * KP + i];
+        z[i] += s;
+      }
     }
   }
 
   // ---------------- pass 2: chunks in reverse ----------------
   __syncthreads();
-  for (int e = tid; e < dk * dv; e += kThreads) S[(e / dv) * dvp + e % dv] = dSN ? dSN[bh * dk * dv + e] : 0.f;  // U
-  for (int i = tid; i < dk; i += kThreads) z[i] = dzN ? dzN[bh * dk + i] : 0.f;            // u
+  for (int e = tid; e < DK * DV; e += kThreads) S[(e / DV) * VP + e % DV] = dSN ? dSN[bh * DK * DV + e] : 0.f;  // U
+  for (int i = tid; i < DK; i += kThreads) z[i] = dzN ? dzN[bh * DK + i] : 0.f;                                // u
   const long nch = (N + kT - 1) / kT;
   for (long ci = nch - 1; ci >= 0; --ci) {
     const long t0 = ci * kT;
     const int T = (int)min((long)kT, N - t0);
     __syncthreads();
-    for (int e = tid; e < T * dk; e += kThreads) {
-      const int t = e / dk, i = e - t * dk;
-      Qs[t * dkp + i] = phi(ldf(qh + (t0 + t) * dk + i));
-      Ks[t * dkp + i] = phi(ldf(kh + (t0 + t) * dk + i));
+    for (int e = tid; e < T * DK; e += kThreads) {
+      const int t = e / DK, i = e - t * DK;
+      Qs[t * KP + i] = phi(ldf(qh + (t0 + t) * DK + i));
+      Ks[t * KP + i] = phi(ldf(kh + (t0 + t) * DK + i));
     }
-    for (int e = tid; e < T * dv; e += kThreads) {
-      const int t = e / dv, c = e - t * dv;
-      Vs[t * dvp + c] = ldf(vh + t0 * dv + e);
-      Gs[e] = Gh[(t0 + t) * (dv + 1) + c];
+    for (int e = tid; e < T * DV; e += kThreads) {
+      const int t = e / DV, c = e - t * DV;
+      Vs[t * VP + c] = ldf(vh + t0 * DV + e);
+      Gs[e] = Gh[(t0 + t) * (DV + 1) + c];
     }
-    for (int t = tid; t < T; t += kThreads) gd[t] = Gh[(t0 + t) * (dv + 1) + dv];
+    for (int t = tid; t < T; t += kThreads) gd[t] = Gh[(t0 + t) * (DV + 1) + DV];
     __syncthreads();
-    for (int e = tid; e < T * T; e += kThreads) {
-      const int t = e / T, j = e - t * T;
-      float a = 0.f, b = 0.f;
-      if (j <= t) {
-#pragma unroll 8
-        for (int i = 0; i < dk; ++i) a = fmaf(Qs[t * dkp + i], Ks[j * dkp + i], a);
-#pragma unroll 8
-        for (int c = 0; c < dv; ++c) b = fmaf(Vs[j * dvp + c], Gs[t * dv + c], b);
-        b += gd[t];
+    scores(T, true);
+    __syncthreads();
+    {
+      // dphi(k_j) = U v_j + u + sum_{t >= j} Bm_tj phi(q_t)
+      float acc[4][RK];
+      zero(acc);
+      tile_fma(acc, DV, ty, tx, [&](int j, int c) { return Vs[j * VP + c]; }, bSt);
+      tile_fma(acc, T, ty, tx, [&](int j, int t) { return Bm[t * AP + j]; }, [&](int t, int i) { return Qs[t * KP + i]; });
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int j = ty + 16 * r;
+        if (j < T)
+#pragma unroll
+          for (int c = 0; c < RK; ++c) {
+            const int i = tx + 16 * c;
+            dkh[(t0 + j) * DK + i] = (acc[r][c] + z[i]) * fminf(Ks[j * KP + i], 1.f);
+          }
       }
-      A[t * (kT + 1) + j] = a;
-      Bm[t * (kT + 1) + j] = b;
+    }
+    {
+      // dv_j = U^T phi(k_j) + sum_{t >= j} A_tj gnum_t
+      float acc[4][RV];
+      zero(acc);
+      tile_fma(acc, DK, ty, tx, [&](int j, int i) { return Ks[j * KP + i]; }, bS);
+      tile_fma(acc, T, ty, tx, [&](int j, int t) { return A[t * AP + j]; }, [&](int t, int c) { return Gs[t * DV + c]; });
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int j = ty + 16 * r;
+        if (j < T)
+#pragma unroll
+          for (int c = 0; c < RV; ++c) dvh[(t0 + j) * DV + tx + 16 * c] = acc[r][c];
+      }
     }
     __syncthreads();
-    // dphi(k_j) = U v_j + u + sum_{t >= j} B_tj phi(q_t)
-    for (int e = tid; e < T * dk; e += kThreads) {
-      const int j = e / dk, i = e - j * dk;
-      float g = z[i];
-#pragma unroll 8
-      for (int c = 0; c < dv; ++c) g = fmaf(S[i * dvp + c], Vs[j * dvp + c], g);
-      for (int t = j; t < T; ++t) g = fmaf(Bm[t * (kT + 1) + j], Qs[t * dkp + i], g);
-      dkh[(t0 + j) * dk + i] = g * fminf(Ks[j * dkp + i], 1.f);
-    }
-    // dv_j = U^T phi(k_j) + sum_{t >= j} A_tj gnum_t
-    for (int e = tid; e < T * dv; e += kThreads) {
-      const int j = e / dv, c = e - j * dv;
-      float g = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < dk; ++i) g = fmaf(S[i * dvp + c], Ks[j * dkp + i], g);
-      for (int t = j; t < T; ++t) g = fmaf(A[t * (kT + 1) + j], Gs[t * dv + c], g);
-      dvh[(t0 + j) * dv + c] = g;
-    }
-    __syncthreads();
-    // U += sum_t phi(q_t) gnum_t^T, u += sum_t phi(q_t) gden_t
-    for (int e = tid; e < dk * dv; e += kThreads) {
-      const int i = e / dv, c = e - i * dv;
-      float s = 0.f;
-#pragma unroll 8
-      for (int t = 0; t < T; ++t) s = fmaf(Qs[t * dkp + i], Gs[t * dv + c], s);
-      S[i * dvp + c] += s;
-    }
-    for (int i = tid; i < dk; i += kThreads) {
-      float s = 0.f;
-      for (int t = 0; t < T; ++t) s = fmaf(Qs[t * dkp + i], gd[t], s);
-      z[i] += s;
+    {
+      // U += phi(Q)^T gnum, u += phi(Q)^T gden
+      float acc[RK][RV];
+      zero(acc);
+      tile_fma(acc, T, ty, tx, [&](int i, int t) { return Qs[t * KP + i]; }, [&](int t, int c) { return Gs[t * DV + c]; });
+#pragma unroll
+      for (int r = 0; r < RK; ++r)
+#pragma unroll
+        for (int c = 0; c < RV; ++c) S[(ty + 16 * r) * VP + tx + 16 * c] += acc[r][c];
+      for (int i = tid; i < DK; i += kThreads) {
+        float s = 0.f;
+        for (int t = 0; t < T; ++t) s = fmaf(Qs[t * KP + i], gd[t], s);
+        z[i] += s;
+      }
     }
   }
   __syncthreads();
   if (dS0)
-    for (int e = tid; e < dk * dv; e += kThreads) dS0[bh * dk * dv + e] = S[(e / dv) * dvp + e % dv];
+    for (int e = tid; e < DK * DV; e += kThreads) dS0[bh * DK * DV + e] = S[(e / DV) * VP + e % DV];
   if (dz0)
-    for (int i = tid; i < dk; i += kThreads) dz0[bh * dk + i] = z[i];
+    for (int i = tid; i < DK; i += kThreads) dz0[bh * DK + i] = z[i];
 }
 
-template <typename Tin>
+template <typename Tin, int DK, int DV>
 cudaError_t launch_t(const BackwardProblem &b, float *G) {
   const Problem &p = b.p;
-  const size_t smem = bwd_smem_bytes(p.dk, p.dv);
-  cudaError_t e = cudaFuncSetAttribute(causal_backward_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  constexpr size_t smem = BwdSmem<DK, DV>::Bytes;
+  cudaError_t e = cudaFuncSetAttribute(causal_backward_kernel<Tin, DK, DV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   LaunchTimer timer(kKBackward, p.stream);
-  causal_backward_kernel<Tin><<<p.BH, kThreads, smem, p.stream>>>(
+  causal_backward_kernel<Tin, DK, DV><<<p.BH, kThreads, smem, p.stream>>>(
       (const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, b.dout, b.S0, b.z0, b.dS, b.dz, b.dq, b.dk, b.dv,
-      b.dS0, b.dz0, G, p.N, p.dk, p.dv, p.eps);
+      b.dS0, b.dz0, G, p.N, p.eps);
   e = cudaGetLastError();
   timer.done(e);
   if (e == cudaSuccess) count_launch();
   return e;
+}
+
+template <typename Tin, int DK>
+cudaError_t launch_dv(const BackwardProblem &b, float *G) {
+  if (b.p.dv == 32) return launch_t<Tin, DK, 32>(b, G);
+  if (b.p.dv == 64) return launch_t<Tin, DK, 64>(b, G);
+  return launch_t<Tin, DK, 128>(b, G);
+}
+
+template <typename Tin>
+cudaError_t launch_dk(const BackwardProblem &b, float *G) {
+  if (b.p.dk == 32) return launch_dv<Tin, 32>(b, G);
+  if (b.p.dk == 64) return launch_dv<Tin, 64>(b, G);
+  return launch_dv<Tin, 128>(b, G);
 }
 
 }  // namespace
@@ -264,7 +357,7 @@ cudaError_t launch_causal_backward(const BackwardProblem &b) {
   float *G = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&G), std::max<size_t>(g_bytes, 16), p.stream);
   if (e != cudaSuccess) return e;
-  e = p.dt == LA_F32 ? launch_t<float>(b, G) : launch_t<__nv_bfloat16>(b, G);
+  e = p.dt == LA_F32 ? launch_dk<float>(b, G) : launch_dk<__nv_bfloat16>(b, G);
   const cudaError_t f = cudaFreeAsync(G, p.stream);
   return e != cudaSuccess ? e : f;
 }
