@@ -15,12 +15,20 @@
 // (U_0, u_0).  phi = ELU + 1 gives phi'(x) = min(phi(x), 1), so only phi of
 // the inputs is kept.
 //
-// One CTA per head, 64-token chunks, all arithmetic in fp32:
-//   pass 1 (chunks in order): the state S, z; per chunk the masked scores
-//     A = tril(phi(Q) phi(K)^T), the denominators, the outputs, gnum and
-//     gden (kept in a scratch row per token), and dq;
-//   pass 2 (chunks in reverse): U, u in place of S, z; per chunk dk and dv
-//     from the carried U, u and the chunk's own masked terms.
+// 64-token chunks, all arithmetic in fp32.  Each head's sequence is cut into
+// segments, one CTA per (segment, head), and a call runs four phases of one
+// kernel template:
+//   segment sums: phi(K)^T V and colsum phi(K) of every segment but the last;
+//   pass 1 (chunks in order from S0 plus the earlier segments' sums): the
+//     state S, z; per chunk the masked scores A = tril(phi(Q) phi(K)^T), the
+//     denominators, the outputs, gnum and gden (kept in a scratch row per
+//     token), and dq;
+//   gradient sums: phi(Q)^T gnum and phi(Q)^T gden of every segment but the
+//     first;
+//   pass 2 (chunks in reverse from dS plus the later segments' sums): U, u in
+//     place of S, z; per chunk dk and dv from the carried U, u and the
+//     chunk's own masked terms; the first segment's final U, u are the
+//     initial state's gradient.
 // Every product is a small matrix product over shared-memory operands: the
 // 256 threads form a 16 x 16 grid and thread (ty, tx) accumulates the rows
 // ty + 16 r and columns tx + 16 c of the result in registers, loading each
@@ -72,14 +80,33 @@ __device__ __forceinline__ void zero(float (&acc)[TR][TC]) {
     for (int c = 0; c < TC; ++c) acc[r][c] = 0.f;
 }
 
-template <typename Tin, int DK, int DV>
-__global__ void __launch_bounds__(kThreads, 1)
-    causal_backward_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
-                           const float *__restrict__ dout, const float *__restrict__ S0,
-                           const float *__restrict__ z0, const float *__restrict__ dSN,
-                           const float *__restrict__ dzN, float *__restrict__ dq, float *__restrict__ dk_g,
-                           float *__restrict__ dv_g, float *__restrict__ dS0, float *__restrict__ dz0,
-                           float *__restrict__ G, long N, float eps) {
+// One call's pointers and sizes (device pointers; see BackwardProblem).
+struct BwdArgs {
+  const void *q, *k, *v;
+  const float *dout, *S0, *z0, *dSN, *dzN;
+  float *dq, *dk, *dv, *dS0, *dz0;
+  float *G;     // [BH][N][DV + 1]: gnum, gden of every token
+  float *segS;  // [BH][nseg][DK * DV + DK]: phi(K)^T V, colsum phi(K) of each segment
+  float *segU;  // [BH][nseg][DK * DV + DK]: phi(Q)^T gnum, phi(Q)^T gden of each segment
+  long N;
+  int seg_chunks, nseg;
+  float eps;
+};
+
+enum BwdPhase : int { kSegSums = 0, kPass1 = 1, kGradSums = 2, kPass2 = 3 };
+
+template <typename Tin, int DK, int DV, int kPhase>
+__global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __grid_constant__ BwdArgs arg) {
+  const Tin *__restrict__ q = static_cast<const Tin *>(arg.q);
+  const Tin *__restrict__ k = static_cast<const Tin *>(arg.k);
+  const Tin *__restrict__ v = static_cast<const Tin *>(arg.v);
+  const float *__restrict__ dout = arg.dout;
+  float *__restrict__ dq = arg.dq;
+  float *__restrict__ dk_g = arg.dk;
+  float *__restrict__ dv_g = arg.dv;
+  float *__restrict__ G = arg.G;
+  const long N = arg.N;
+  const float eps = arg.eps;
   using L = BwdSmem<DK, DV>;
   constexpr int KP = L::KP, VP = L::VP, AP = L::AP;
   constexpr int RK = DK / 16, RV = DV / 16;  // register tile widths over features and values
@@ -95,8 +122,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *den = Bm + kT * AP;  // [kT]
   float *gd = den + kT;       // [kT] gden
 
-  const long bh = blockIdx.x;
+  const long bh = blockIdx.y;
+  const int seg = blockIdx.x;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const long nch = (N + kT - 1) / kT;
+  const long c_begin = (long)seg * arg.seg_chunks, c_end = min(nch, c_begin + arg.seg_chunks);
+  constexpr int kSum = DK * DV + DK;  // one segment sum: matrix then vector
   const Tin *qh = q + bh * N * DK, *kh = k + bh * N * DK, *vh = v + bh * N * DV;
   const float *oh = dout + bh * N * DV;
   float *dqh = dq + bh * N * DK, *dkh = dk_g + bh * N * DK, *dvh = dv_g + bh * N * DV;
@@ -112,8 +143,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bVt = [&](int c, int j) { return Vs[j * VP + c]; };
   auto aG = [&](int t, int c) { return Gs[t * DV + c]; };
 
-  for (int e = tid; e < DK * DV; e += kThreads) S[(e / DV) * VP + e % DV] = S0 ? S0[bh * DK * DV + e] : 0.f;
-  for (int i = tid; i < DK; i += kThreads) z[i] = z0 ? z0[bh * DK + i] : 0.f;
+  // starting state: pass 1 from S0 plus the earlier segments' sums; the sum phases from zero
+  {
+    const float *part = arg.segS + bh * arg.nseg * (long)kSum;
+    for (int e = tid; e < DK * DV + DK; e += kThreads) {
+      float x = 0.f;
+      if (kPhase == kPass1) {
+        x = e < DK * DV ? (arg.S0 ? arg.S0[bh * DK * DV + e] : 0.f) : (arg.z0 ? arg.z0[bh * DK + e - DK * DV] : 0.f);
+        for (int s2 = 0; s2 < seg; ++s2) x += part[s2 * (long)kSum + e];
+      }
+      if (e < DK * DV) S[(e / DV) * VP + e % DV] = x;
+      else z[e - DK * DV] = x;
+    }
+  }
 
   // masked scores A = tril(phi(Q) phi(K)^T) and score gradients Bm = tril(gnum V^T + gden)
   auto scores = [&](int T, bool with_b) {
@@ -139,8 +181,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
   };
 
+  if constexpr (kPhase == kSegSums) {
+    // phi(K)^T V and colsum phi(K) over the segment
+    for (long ci = c_begin; ci < c_end; ++ci) {
+      const long t0 = ci * kT;
+      const int T = (int)min((long)kT, N - t0);
+      __syncthreads();
+      for (int e = tid; e < T * DK; e += kThreads) {
+        const int t = e / DK, i = e - t * DK;
+        Ks[t * KP + i] = phi(ldf(kh + (t0 + t) * DK + i));
+      }
+      for (int e = tid; e < T * DV; e += kThreads) Vs[(e / DV) * VP + e % DV] = ldf(vh + t0 * DV + e);
+      __syncthreads();
+      float acc[RK][RV];
+      zero(acc);
+      tile_fma(acc, T, ty, tx, [&](int i, int j) { return Ks[j * KP + i]; }, bV);
+#pragma unroll
+      for (int r = 0; r < RK; ++r)
+#pragma unroll
+        for (int c = 0; c < RV; ++c) S[(ty + 16 * r) * VP + tx + 16 * c] += acc[r][c];
+      for (int i = tid; i < DK; i += kThreads) {
+        float sum = 0.f;
+        for (int j = 0; j < T; ++j) sum += Ks[j * KP + i];
+        z[i] += sum;
+      }
+    }
+    __syncthreads();
+    float *dst = arg.segS + (bh * arg.nseg + seg) * (long)kSum;
+    for (int e = tid; e < DK * DV + DK; e += kThreads) dst[e] = e < DK * DV ? S[(e / DV) * VP + e % DV] : z[e - DK * DV];
+    return;
+  }
+
+  if constexpr (kPhase == kGradSums) {
+    // phi(Q)^T gnum and phi(Q)^T gden over the segment (the first segment's is never read)
+    if (seg == 0) return;
+    for (long ci = c_begin; ci < c_end; ++ci) {
+      const long t0 = ci * kT;
+      const int T = (int)min((long)kT, N - t0);
+      __syncthreads();
+      for (int e = tid; e < T * DK; e += kThreads) {
+        const int t = e / DK, i = e - t * DK;
+        Qs[t * KP + i] = phi(ldf(qh + (t0 + t) * DK + i));
+      }
+      for (int e = tid; e < T * DV; e += kThreads) Gs[e] = Gh[(t0 + e / DV) * (DV + 1) + e % DV];
+      for (int t = tid; t < T; t += kThreads) gd[t] = Gh[(t0 + t) * (DV + 1) + DV];
+      __syncthreads();
+      float acc[RK][RV];
+      zero(acc);
+      tile_fma(acc, T, ty, tx, [&](int i, int t) { return Qs[t * KP + i]; }, [&](int t, int c) { return Gs[t * DV + c]; });
+#pragma unroll
+      for (int r = 0; r < RK; ++r)
+#pragma unroll
+        for (int c = 0; c < RV; ++c) S[(ty + 16 * r) * VP + tx + 16 * c] += acc[r][c];
+      for (int i = tid; i < DK; i += kThreads) {
+        float sum = 0.f;
+        for (int t = 0; t < T; ++t) sum = fmaf(Qs[t * KP + i], gd[t], sum);
+        z[i] += sum;
+      }
+    }
+    __syncthreads();
+    float *dst = arg.segU + (bh * arg.nseg + seg) * (long)kSum;
+    for (int e = tid; e < DK * DV + DK; e += kThreads) dst[e] = e < DK * DV ? S[(e / DV) * VP + e % DV] : z[e - DK * DV];
+    return;
+  }
+
   // ---------------- pass 1: chunks in order ----------------
-  for (long t0 = 0; t0 < N; t0 += kT) {
+  if constexpr (kPhase == kPass1) for (long t0 = c_begin * kT; t0 < c_end * kT && t0 < N; t0 += kT) {
     const int T = (int)min((long)kT, N - t0);
     __syncthreads();  // the previous chunk is fully consumed
     for (int e = tid; e < T * DK; e += kThreads) {
@@ -239,12 +345,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if constexpr (kPhase == kPass1) return;
+
   // ---------------- pass 2: chunks in reverse ----------------
-  __syncthreads();
-  for (int e = tid; e < DK * DV; e += kThreads) S[(e / DV) * VP + e % DV] = dSN ? dSN[bh * DK * DV + e] : 0.f;  // U
-  for (int i = tid; i < DK; i += kThreads) z[i] = dzN ? dzN[bh * DK + i] : 0.f;                                // u
-  const long nch = (N + kT - 1) / kT;
-  for (long ci = nch - 1; ci >= 0; --ci) {
+  // U, u at the segment's end: dS, dz plus the later segments' gradient sums
+  {
+    const float *part = arg.segU + bh * arg.nseg * (long)kSum;
+    __syncthreads();
+    for (int e = tid; e < DK * DV + DK; e += kThreads) {
+      float x = e < DK * DV ? (arg.dSN ? arg.dSN[bh * DK * DV + e] : 0.f)
+                            : (arg.dzN ? arg.dzN[bh * DK + e - DK * DV] : 0.f);
+      for (int s2 = seg + 1; s2 < arg.nseg; ++s2) x += part[s2 * (long)kSum + e];
+      if (e < DK * DV) S[(e / DV) * VP + e % DV] = x;
+      else z[e - DK * DV] = x;
+    }
+  }
+  for (long ci = c_end - 1; ci >= c_begin; --ci) {
     const long t0 = ci * kT;
     const int T = (int)min((long)kT, N - t0);
     __syncthreads();
@@ -311,53 +427,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  if (dS0)
-    for (int e = tid; e < DK * DV; e += kThreads) dS0[bh * DK * DV + e] = S[(e / DV) * VP + e % DV];
-  if (dz0)
-    for (int i = tid; i < DK; i += kThreads) dz0[bh * DK + i] = z[i];
+  if (seg == 0 && arg.dS0)
+    for (int e = tid; e < DK * DV; e += kThreads) arg.dS0[bh * DK * DV + e] = S[(e / DV) * VP + e % DV];
+  if (seg == 0 && arg.dz0)
+    for (int i = tid; i < DK; i += kThreads) arg.dz0[bh * DK + i] = z[i];
 }
 
-template <typename Tin, int DK, int DV>
-cudaError_t launch_t(const BackwardProblem &b, float *G) {
-  const Problem &p = b.p;
+template <typename Tin, int DK, int DV, int kPhase>
+cudaError_t launch_phase(const BwdArgs &a, dim3 grid, cudaStream_t stream) {
   constexpr size_t smem = BwdSmem<DK, DV>::Bytes;
-  cudaError_t e = cudaFuncSetAttribute(causal_backward_kernel<Tin, DK, DV>,
+  cudaError_t e = cudaFuncSetAttribute(causal_backward_kernel<Tin, DK, DV, kPhase>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  LaunchTimer timer(kKBackward, p.stream);
-  causal_backward_kernel<Tin, DK, DV><<<p.BH, kThreads, smem, p.stream>>>(
-      (const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, b.dout, b.S0, b.z0, b.dS, b.dz, b.dq, b.dk, b.dv,
-      b.dS0, b.dz0, G, p.N, p.eps);
+  causal_backward_kernel<Tin, DK, DV, kPhase><<<grid, kThreads, smem, stream>>>(a);
   e = cudaGetLastError();
-  timer.done(e);
   if (e == cudaSuccess) count_launch();
   return e;
 }
 
+template <typename Tin, int DK, int DV>
+cudaError_t launch_t(const BwdArgs &a, int BH, cudaStream_t stream) {
+  LaunchTimer timer(kKBackward, stream);
+  cudaError_t e = cudaSuccess;
+  if (a.nseg > 1) e = launch_phase<Tin, DK, DV, kSegSums>(a, dim3(a.nseg - 1, BH), stream);
+  if (e == cudaSuccess) e = launch_phase<Tin, DK, DV, kPass1>(a, dim3(a.nseg, BH), stream);
+  if (e == cudaSuccess && a.nseg > 1) e = launch_phase<Tin, DK, DV, kGradSums>(a, dim3(a.nseg, BH), stream);
+  if (e == cudaSuccess) e = launch_phase<Tin, DK, DV, kPass2>(a, dim3(a.nseg, BH), stream);
+  timer.done(e);
+  return e;
+}
+
 template <typename Tin, int DK>
-cudaError_t launch_dv(const BackwardProblem &b, float *G) {
-  if (b.p.dv == 32) return launch_t<Tin, DK, 32>(b, G);
-  if (b.p.dv == 64) return launch_t<Tin, DK, 64>(b, G);
-  return launch_t<Tin, DK, 128>(b, G);
+cudaError_t launch_dv(const BwdArgs &a, int BH, int dv, cudaStream_t s) {
+  if (dv == 32) return launch_t<Tin, DK, 32>(a, BH, s);
+  if (dv == 64) return launch_t<Tin, DK, 64>(a, BH, s);
+  return launch_t<Tin, DK, 128>(a, BH, s);
 }
 
 template <typename Tin>
-cudaError_t launch_dk(const BackwardProblem &b, float *G) {
-  if (b.p.dk == 32) return launch_dv<Tin, 32>(b, G);
-  if (b.p.dk == 64) return launch_dv<Tin, 64>(b, G);
-  return launch_dv<Tin, 128>(b, G);
+cudaError_t launch_dk(const BwdArgs &a, int BH, int dk, int dv, cudaStream_t s) {
+  if (dk == 32) return launch_dv<Tin, 32>(a, BH, dv, s);
+  if (dk == 64) return launch_dv<Tin, 64>(a, BH, dv, s);
+  return launch_dv<Tin, 128>(a, BH, dv, s);
 }
 
 }  // namespace
 
 cudaError_t launch_causal_backward(const BackwardProblem &b) {
   const Problem &p = b.p;
-  // scratch: gnum and gden of every token, written by pass 1 and read by pass 2
-  const size_t g_bytes = sizeof(float) * (size_t)p.BH * p.N * (p.dv + 1);
+  // segments per head: enough CTAs to cover the SMs once, at least 4 chunks each
+  const long nch = (p.N + kT - 1) / kT;
+  const long sms = std::max(1, device_info(-1).sm_count);
+  long nseg = std::max(1L, std::min(sms / std::max(1, p.BH), nch / 4));
+  const long seg_chunks = std::max(1L, (nch + nseg - 1) / nseg);
+  nseg = std::max(1L, (nch + seg_chunks - 1) / seg_chunks);
+  // scratch: gnum and gden of every token, then the segment sums of the state and of the gradients
+  const size_t sum_f = (size_t)p.dk * p.dv + p.dk;
+  const size_t g_f = (size_t)p.BH * p.N * (p.dv + 1), seg_f = (size_t)p.BH * nseg * sum_f;
   float *G = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&G), std::max<size_t>(g_bytes, 16), p.stream);
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&G), std::max<size_t>(sizeof(float) * (g_f + 2 * seg_f), 16),
+                                  p.stream);
   if (e != cudaSuccess) return e;
-  e = p.dt == LA_F32 ? launch_dk<float>(b, G) : launch_dk<__nv_bfloat16>(b, G);
+  BwdArgs a;
+  a.q = p.q, a.k = p.k, a.v = p.v;
+  a.dout = b.dout, a.S0 = b.S0, a.z0 = b.z0, a.dSN = b.dS, a.dzN = b.dz;
+  a.dq = b.dq, a.dk = b.dk, a.dv = b.dv, a.dS0 = b.dS0, a.dz0 = b.dz0;
+  a.G = G, a.segS = G + g_f, a.segU = G + g_f + seg_f;
+  a.N = p.N, a.seg_chunks = (int)seg_chunks, a.nseg = (int)nseg, a.eps = p.eps;
+  e = p.dt == LA_F32 ? launch_dk<float>(a, p.BH, p.dk, p.dv, p.stream)
+                     : launch_dk<__nv_bfloat16>(a, p.BH, p.dk, p.dv, p.stream);
   const cudaError_t f = cudaFreeAsync(G, p.stream);
   return e != cudaSuccess ? e : f;
 }

@@ -39,8 +39,9 @@ def _state(B, H, dk, dv, seed):
     return torch.randn(B, H, dk, dv, generator=g), torch.rand(B, H, dk, generator=g) * 4 + 1
 
 
+# heads cut into 1 to 8 segments (the backward spreads each head over about 152 / heads CTAs)
 SHAPES = [(1, 1, 2, 32, 32), (1, 2, 63, 64, 32), (2, 1, 129, 32, 128), (1, 3, 300, 128, 128),
-          (1, 2, 700, 128, 64), (2, 2, 257, 64, 64)]
+          (1, 2, 700, 128, 64), (2, 2, 257, 64, 64), (1, 1, 2000, 64, 64), (1, 2, 1500, 128, 128)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
