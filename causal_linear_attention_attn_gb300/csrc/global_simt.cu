@@ -21,7 +21,7 @@ constexpr int kReadTokens = 128;                    // tokens per read CTA
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
     global_state_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v, float *__restrict__ S_g,
-                        float *__restrict__ z_g, long N, int dk, int dv, int splits) {
+                        float *__restrict__ z_g, long N, int dk, int dv, int splits, int identity) {
   extern __shared__ float sm[];
   const int dkp = dk + 1;
   float *Ks = sm;             // [kT][dkp]
@@ -43,7 +43,8 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     for (int e = tid; e < T * dk; e += kThreads) {
       const int t = e / dk, i = e - t * dk;
-      Ks[t * dkp + i] = phi(ldf(kh + (t0 + t) * dk + i));
+      const float x = ldf(kh + (t0 + t) * dk + i);
+      Ks[t * dkp + i] = identity ? x : phi(x);  // identity: k is a given feature
     }
     for (int e = tid; e < T * dv; e += kThreads) Vs[e] = ldf(vh + t0 * dv + e);
     __syncthreads();
@@ -71,7 +72,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
     global_read_kernel(const Tin *__restrict__ q, const float *__restrict__ S_g,
                        const float *__restrict__ z_g, float *__restrict__ out, long N, int dk, int dv,
-                       float eps) {
+                       float eps, int identity) {
   extern __shared__ float sm[];
   const int dkp = dk + 1;
   float *S = sm;                    // [dk][dv]
@@ -87,7 +88,8 @@ __global__ void __launch_bounds__(kThreads)
   const Tin *qh = q + (bh * N + t0) * dk;
   for (int e = tid; e < T * dk; e += kThreads) {
     const int t = e / dk, i = e - t * dk;
-    Qs[t * dkp + i] = phi(ldf(qh + e));
+    const float x = ldf(qh + e);
+    Qs[t * dkp + i] = identity ? x : phi(x);
   }
   __syncthreads();
   for (int t = tid; t < T; t += kThreads) {
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 template <typename Tin>
-cudaError_t launch_t(const Problem &p) {
+cudaError_t launch_t(const Problem &p, bool identity) {
   const DeviceInfo &di = device_info(-1);
   cudaError_t e = cudaMemsetAsync(p.S, 0, sizeof(float) * (size_t)p.BH * p.dk * p.dv, p.stream);
   if (e != cudaSuccess) return e;
@@ -121,7 +123,7 @@ cudaError_t launch_t(const Problem &p) {
   if (e != cudaSuccess) return e;
   LaunchTimer t1(kKGlobalState, p.stream);
   global_state_kernel<Tin><<<dim3(p.BH, (unsigned)splits), kThreads, smem1, p.stream>>>(
-      (const Tin *)p.k, (const Tin *)p.v, p.S, p.z, p.N, p.dk, p.dv, (int)splits);
+      (const Tin *)p.k, (const Tin *)p.v, p.S, p.z, p.N, p.dk, p.dv, (int)splits, identity ? 1 : 0);
   e = cudaGetLastError();
   t1.done(e);
   if (e != cudaSuccess) return e;
@@ -133,7 +135,7 @@ cudaError_t launch_t(const Problem &p) {
   const unsigned tiles = (unsigned)((p.N + kReadTokens - 1) / kReadTokens);
   LaunchTimer t2(kKGlobalRead, p.stream);
   global_read_kernel<Tin><<<dim3(p.BH, tiles), kThreads, smem2, p.stream>>>((const Tin *)p.q, p.S, p.z, p.out,
-                                                                          p.N, p.dk, p.dv, p.eps);
+                                                                          p.N, p.dk, p.dv, p.eps, identity ? 1 : 0);
   e = cudaGetLastError();
   t2.done(e);
   if (e == cudaSuccess) count_launch();
@@ -142,9 +144,9 @@ cudaError_t launch_t(const Problem &p) {
 
 }  // namespace
 
-cudaError_t launch_global_simt(const Problem &p) {
-  if (p.dt == LA_F32) return launch_t<float>(p);
-  return launch_t<__nv_bfloat16>(p);
+cudaError_t launch_global_simt(const Problem &p, bool identity) {
+  if (p.dt == LA_F32) return launch_t<float>(p, identity);
+  return launch_t<__nv_bfloat16>(p, identity);
 }
 
 }  // namespace la

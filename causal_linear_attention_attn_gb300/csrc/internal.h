@@ -101,7 +101,8 @@ cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_
 cudaError_t read_and_clear_device_status(unsigned int *value);
 
 // Global form: state build (S, z are zeroed and accumulated) then the read.
-cudaError_t launch_global_simt(const Problem &p);
+// identity: q and k are given features (no phi).
+cudaError_t launch_global_simt(const Problem &p, bool identity = false);
 
 // One decode step, S and z in place.
 cudaError_t launch_decode(const Problem &p);

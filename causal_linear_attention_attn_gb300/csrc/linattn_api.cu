@@ -277,6 +277,17 @@ la_status la_causal_features(const void *phi_q, const void *phi_k, const void *v
   return la::from_cuda(la::launch_causal_simt(p, p.N, false, true, true));
 }
 
+la_status la_global_features(const void *phi_q, const void *phi_k, const void *v, float *out, float *S, float *z,
+                             int B, int H, int N, int m, int d_v, float eps, la_dtype dt, void *stream) {
+  la_status st = la::validate(phi_q, phi_k, v, out, S, z, B, H, N, m, d_v, eps, dt);
+  if (st != LA_OK) return st;
+  if ((long)B * H == 0) return LA_OK;
+  int dev;
+  if ((st = la::current_device(&dev)) != LA_OK) return st;
+  Problem p{phi_q, phi_k, v, out, S, z, B * H, (long)N, m, d_v, eps, dt, (cudaStream_t)stream};
+  return la::from_cuda(la::launch_global_simt(p, true));
+}
+
 la_status la_favor_features(const void *x, const void *W, void *phi, int B, int H, int N, int d, int m,
                             la_dtype dt, void *stream) {
   if (B < 0 || H < 0 || N < 0 || d <= 0 || m <= 0) return LA_ERR_INVALID_VALUE;

@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "LA_OK", 1: "LA_ERR_INVALID_VALUE", 2: "LA_ERR_UNSUPPORTED", 
 
 _vp, _fp, _i, _f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _SEQ_ARGS = [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _i, _vp]
-for _name in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc", "la_causal_features"):
+for _name in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc", "la_causal_features",
+              "la_global_features"):
     getattr(lib, _name).argtypes = _SEQ_ARGS
     getattr(lib, _name).restype = _i
 for _name in ("la_retention", "la_retention_with_state"):
@@ -159,6 +160,11 @@ def la_causal_noalloc(q, k, v, out=None, S=None, z=None, eps: float = 1e-6, stre
 def la_causal_features(phi_q, phi_k, v, out=None, S=None, z=None, eps: float = 1e-6, stream=None):
     """Causal prefill on given (non-negative) features; returns (out, S, z)."""
     return _seq_call("la_causal_features", phi_q, phi_k, v, out, S, z, eps, stream)
+
+
+def la_global_features(phi_q, phi_k, v, out=None, S=None, z=None, eps: float = 1e-6, stream=None):
+    """Global read on given (non-negative) features; returns (out, S, z)."""
+    return _seq_call("la_global_features", phi_q, phi_k, v, out, S, z, eps, stream)
 
 
 def la_favor_features(x, W, out=None, stream=None):

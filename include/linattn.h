@@ -185,6 +185,18 @@ LA_API la_status la_causal_features(const void *phi_q, const void *phi_k, const 
                                     void *stream);
 
 /*
+ * Global (non-causal) read on features the caller has already applied: as
+ * la_global with phi the identity.  Arguments, results and errors as
+ * la_causal_features.  Computed in fp32 on CUDA cores: the tensor-core
+ * global read takes the state as one bf16 operand, which heavy-tailed
+ * features (a few keys dominating each read while the state sums all of
+ * them) do not tolerate.
+ */
+LA_API la_status la_global_features(const void *phi_q, const void *phi_k, const void *v, float *out, float *S,
+                                    float *z, int B, int H, int N, int m, int d_v, float eps, la_dtype dt,
+                                    void *stream);
+
+/*
  * Retention: the causal recurrence with an explicit per-head decay and no
  * denominator,
  *     S_t = gamma_h S_{t-1} + k_t v_t^T,   out_t = q_t^T S_t,   S_{-1} = 0,

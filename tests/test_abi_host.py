@@ -27,7 +27,7 @@ def test_header_declares_the_entry_points():
     names = _declared_symbols()
     for n in ("la_global", "la_causal", "la_causal_with_state", "la_causal_noalloc", "la_decode_step", "la_status_string",
               "la_version", "la_retention", "la_retention_with_state", "la_retention_decode_step",
-              "la_causal_backward", "la_favor_features", "la_causal_features"):
+              "la_causal_backward", "la_favor_features", "la_causal_features", "la_global_features"):
         assert n in names
 
 
@@ -167,6 +167,8 @@ def test_favor_validation():
     assert call(N=0, x=None, Wp=None, phi=None) == OK
     assert seq("la_causal_features", q=None) == INVALID
     assert seq("la_causal_features", dk=48) == UNSUPPORTED
+    assert seq("la_global_features", v=None) == INVALID
+    assert seq("la_global_features", dv=96) == UNSUPPORTED
 
 
 def test_backward_validation():

@@ -74,6 +74,24 @@ def test_causal_on_given_features_every_element(cuda_lib, shape, dtype):
     assert_close(z, rz, tau, "z")
 
 
+@pytest.mark.parametrize("shape", [(1, 2, 300, 128, 128), (2, 3, 1000, 64, 128), (1, 1, 129, 32, 32)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_global_on_given_features_every_element(cuda_lib, shape, dtype):
+    B, H, N, m, dv = shape
+    w = dataclasses.replace(W, dk=128, dv=dv, dtype=dtype)
+    q, k, v = inputs.make_qkv(w, N=N, B=B, H=H)
+    P = inputs.favor_projections(w, m=m).to(DEV)
+    fq, fk = cuda_lib.la_favor_features(q.to(DEV), P), cuda_lib.la_favor_features(k.to(DEV), P)
+    out, S, z = cuda_lib.la_global_features(fq, fk, v.to(DEV), eps=w.eps)
+    torch.cuda.synchronize()
+    ro, rS, rz = oracle.global_(f64(fq), f64(fk), f64(v), eps=w.eps, phi="identity", nthreads=8)
+    tau = TAU[w.torch_dtype]
+    assert_close(out, ro, tau, "out")
+    assert_close(S, rS, tau, "S")
+    assert_close(z, rz, tau, "z")
+
+
 def test_favor_causal_end_to_end_workload_shape(cuda_lib):
     """The workload (4 x 16 x 8192, d = m = 128, bf16): features and read on the
     GPU; every output of three sampled heads against the oracle's features of
