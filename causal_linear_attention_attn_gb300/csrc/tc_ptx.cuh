@@ -306,17 +306,19 @@ __device__ __forceinline__ void wait_drain(uint64_t *bar, uint32_t parity, unsig
     }
 }
 
-// phi on two packed bf16 values.  Both branches are evaluated for both
-// halves and the result picked by the sign bit (no divergence): exp in fp32
-// rounded to bf16, and x + 1 as a bf16x2 add (the exact sum rounded once, the
-// same value as the fp32 sum rounded to bf16).  x = +-0 gives 1 either way.
+// phi on two packed bf16 values without branches.  e^x >= 1 + x for every x,
+// so phi(x) = max(min(e^x, 1), 1 + x): for x <= 0 the min is e^x and the max
+// keeps it; for x > 0 the min is 1 and the max gives 1 + x.  Rounding is
+// monotone, so the same holds for the bf16 values: exp in fp32 rounded to
+// bf16, and x + 1 as a bf16x2 add (the exact sum rounded once, the same value
+// as the fp32 sum rounded to bf16).  x = +-0 gives 1.
 __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
   const float a = __uint_as_float(x << 16), b = __uint_as_float(x & 0xffff0000u);
-  const __nv_bfloat162 e2 = __floats2bfloat162_rn(__expf(a), __expf(b));
-  const __nv_bfloat162 x1 = __hadd2(*reinterpret_cast<const __nv_bfloat162 *>(&x), __floats2bfloat162_rn(1.f, 1.f));
-  const uint32_t e = *reinterpret_cast<const uint32_t *>(&e2), p1 = *reinterpret_cast<const uint32_t *>(&x1);
-  const uint32_t m = ((x >> 15) & 0x00010001u) * 0xffffu;  // halves with the sign bit set take exp
-  return (e & m) | (p1 & ~m);
+  const __nv_bfloat162 one = __floats2bfloat162_rn(1.f, 1.f);
+  const __nv_bfloat162 e2 = __hmin2(__floats2bfloat162_rn(__expf(a), __expf(b)), one);
+  const __nv_bfloat162 x1 = __hadd2(*reinterpret_cast<const __nv_bfloat162 *>(&x), one);
+  const __nv_bfloat162 r = __hmax2(e2, x1);
+  return *reinterpret_cast<const uint32_t *>(&r);
 }
 
 __device__ __forceinline__ uint4 phi8(uint4 x) {
