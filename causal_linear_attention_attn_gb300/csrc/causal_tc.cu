@@ -128,14 +128,13 @@ struct TcParams {
 __device__ __forceinline__ float dot8(uint4 y, const float *z) {
   const uint32_t w[4] = {y.x, y.y, y.z, y.w};
   const float4 z0 = *reinterpret_cast<const float4 *>(z), z1 = *reinterpret_cast<const float4 *>(z + 4);
-  const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-  float s = 0.f;
+  const float2 zz[4] = {make_float2(z0.x, z0.y), make_float2(z0.z, z0.w), make_float2(z1.x, z1.y),
+                        make_float2(z1.z, z1.w)};
+  float2 s = make_float2(0.f, 0.f);  // even and odd features, one packed FMA per pair
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    s = fmaf(__uint_as_float(w[e] << 16), zz[2 * e], s);
-    s = fmaf(__uint_as_float(w[e] & 0xffff0000u), zz[2 * e + 1], s);
-  }
-  return s;
+  for (int e = 0; e < 4; ++e)
+    s = __ffma2_rn(make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u)), zz[e], s);
+  return s.x + s.y;
 }
 
 // Write 32 values (columns col0 .. col0+31 of row `row`) as bf16 into a
@@ -170,6 +169,13 @@ __device__ __forceinline__ void store_row32_split(uint8_t *hi, uint8_t *lo, int 
   }
 }
 
+// Four fp32 values (as raw bits) times f, by two packed multiplies.
+__device__ __forceinline__ float4 scale4(const uint32_t *r, float f) {
+  const float2 a = __fmul2_rn(make_float2(__uint_as_float(r[0]), __uint_as_float(r[1])), make_float2(f, f));
+  const float2 b = __fmul2_rn(make_float2(__uint_as_float(r[2]), __uint_as_float(r[3])), make_float2(f, f));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 // K-major operand (rows of 64 K-elements): k-step ks covers K elements [16ks, 16ks+16).
 __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int ks) {
   return sw128_desc(tile + (ks >> 2) * kBlk + (ks & 3) * 32, 16, 1024);
@@ -190,15 +196,16 @@ __device__ __forceinline__ int column_pair_sums_8w(const uint8_t *tile, int w, i
   const uint8_t *blk = tile + (c >> 6) * kBlk;
   const int cc = c & 63;
   const uint32_t off0 = sw128_offset(ph, cc), off1 = sw128_offset(ph + 4, cc);
-  float a0 = 0.f, a1 = 0.f;
+  float2 a = make_float2(0.f, 0.f);  // the pair's two columns, packed adds
   const int full = rows >> 3;
 #pragma unroll 4
   for (int g = 0; g < full; ++g) {
     const uint32_t x = *reinterpret_cast<const uint32_t *>(blk + g * 1024 + off0);
     const uint32_t y = *reinterpret_cast<const uint32_t *>(blk + g * 1024 + off1);
-    a0 += __uint_as_float(x << 16) + __uint_as_float(y << 16);
-    a1 += __uint_as_float(x & 0xffff0000u) + __uint_as_float(y & 0xffff0000u);
+    a = __fadd2_rn(a, __fadd2_rn(make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u)),
+                                 make_float2(__uint_as_float(y << 16), __uint_as_float(y & 0xffff0000u))));
   }
+  float a0 = a.x, a1 = a.y;
   for (int t = 8 * full + ph; t < rows; t += 4) {
     const uint32_t x = *reinterpret_cast<const uint32_t *>(blk + sw128_offset(t, cc));
     a0 += __uint_as_float(x << 16);
@@ -630,7 +637,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         // P -> causal mask -> bf16 hi/lo, written back over the same columns:
         // keys [16g, 16g+16) become 8 columns of P_hi pairs then 8 of P_lo pairs.
         // Key blocks right of this warp's rows are all masked (zeros).
-        float rs = 0.f;
+        float2 rs2 = make_float2(0.f, 0.f);  // row sum over even and odd keys
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           if (cb > quarter) {
@@ -646,15 +653,16 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
                 const int j = cb * 32 + g * 16 + 2 * m;
                 float p0 = (j <= T && j < tv) ? __uint_as_float(r[g * 16 + 2 * m]) : 0.f;
                 float p1 = (j + 1 <= T && j + 1 < tv) ? __uint_as_float(r[g * 16 + 2 * m + 1]) : 0.f;
+                float2 pp = make_float2(p0, p1);  // packed fp32 pairs from here on
                 if (kRet) {
                   const float2 wj = *reinterpret_cast<const float2 *>(den_s + j);
-                  p0 *= wj.x * wc;
-                  p1 *= wj.y * wc;
+                  pp = __fmul2_rn(pp, __fmul2_rn(wj, make_float2(wc, wc)));
                 }
-                const uint32_t hw = pack_bf16(p0, p1);
-                const float h0 = __uint_as_float(hw << 16), h1 = __uint_as_float(hw & 0xffff0000u);
-                const uint32_t lw = pack_bf16(p0 - h0, p1 - h1);
-                rs += p0 + p1;  // equals the sum of hi + lo to within 2^-16 relative
+                const uint32_t hw = pack_bf16(pp.x, pp.y);
+                const float2 hh = make_float2(__uint_as_float(hw << 16), __uint_as_float(hw & 0xffff0000u));
+                const float2 ll = __ffma2_rn(hh, make_float2(-1.f, -1.f), pp);  // pp - hh, exact
+                const uint32_t lw = pack_bf16(ll.x, ll.y);
+                rs2 = __fadd2_rn(rs2, pp);  // the row sum equals that of hi + lo to within 2^-16 relative
                 o[m] = hw;
                 o[8 + m] = lw;
               }
@@ -664,7 +672,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
           }
           tmem_st32(tP + cb * 32, r);
         }
-        den = (den + rs) + p.eps;
+        den = (den + (rs2.x + rs2.y)) + p.eps;
         if (!kRet) den_s[(c & 1) * kC + T] = den;
         tc_fence_before();
         mbar_arrive(pp_ready);
@@ -735,10 +743,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         tmem_ld32(tl + kColO + b * 32, r);
         uint8_t *box = stage_o + b * kBlk;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4 *>(box + sw128_offset_f32(T, 4 * q)) =
-              make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
-                          __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+        for (int q = 0; q < 8; ++q) *reinterpret_cast<float4 *>(box + sw128_offset_f32(T, 4 * q)) = scale4(r + 4 * q, inv);
       }
       fence_async_smem();
       named_bar(kBarOut, 128);
@@ -763,12 +768,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       named_bar(kBarOut, 128);  // the staging tile is free again
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        *reinterpret_cast<float4 *>(stage_o + sw128_offset_f32(T, 4 * q)) =
-            make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
-                        __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
-        *reinterpret_cast<float4 *>(stage_o + kBlk + sw128_offset_f32(T, 4 * q)) =
-            make_float4(__uint_as_float(r2[4 * q]) * inv, __uint_as_float(r2[4 * q + 1]) * inv,
-                        __uint_as_float(r2[4 * q + 2]) * inv, __uint_as_float(r2[4 * q + 3]) * inv);
+        *reinterpret_cast<float4 *>(stage_o + sw128_offset_f32(T, 4 * q)) = scale4(r + 4 * q, inv);
+        *reinterpret_cast<float4 *>(stage_o + kBlk + sw128_offset_f32(T, 4 * q)) = scale4(r2 + 4 * q, inv);
       }
       fence_async_smem();
       named_bar(kBarOut, 128);
