@@ -55,9 +55,11 @@ struct BwdSmem {
 };
 static_assert(BwdSmem<128, 128>::Bytes <= 232448, "shared memory budget");
 
-// acc[r][c] += sum_{k < K} a(ty + 16 r, k) b(k, tx + 16 c)
+// acc[r][c] += sum_{k < K} a(ty + 16 r, k) b(k, tx + 16 c); pairs of columns share one
+// packed fp32 FMA (TC is even)
 template <int TR, int TC, typename FA, typename FB>
 __device__ __forceinline__ void tile_fma(float (&acc)[TR][TC], int K, int ty, int tx, FA a, FB b) {
+  static_assert(TC % 2 == 0, "columns go in pairs");
 #pragma unroll 4
   for (int k = 0; k < K; ++k) {
     float av[TR], bv[TC];
@@ -68,7 +70,12 @@ __device__ __forceinline__ void tile_fma(float (&acc)[TR][TC], int K, int ty, in
 #pragma unroll
     for (int r = 0; r < TR; ++r)
 #pragma unroll
-      for (int c = 0; c < TC; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+      for (int c = 0; c < TC; c += 2) {
+        const float2 y = __ffma2_rn(make_float2(av[r], av[r]), make_float2(bv[c], bv[c + 1]),
+                                    make_float2(acc[r][c], acc[r][c + 1]));
+        acc[r][c] = y.x;
+        acc[r][c + 1] = y.y;
+      }
   }
 }
 

@@ -63,13 +63,13 @@ __device__ __forceinline__ void phi_chunks(uint8_t *tile, int t, F &&each) {
   for (int j = 0; j < kPer; ++j) reinterpret_cast<uint4 *>(tile)[t + kThr * j] = x[j];
 }
 
+// acc[0..7] += the eight bf16 values of y, by packed fp32 adds (acc is 8-byte aligned)
 __device__ __forceinline__ void add8_bf16(float *acc, uint4 y) {
   const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+  float2 *a2 = reinterpret_cast<float2 *>(acc);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    acc[2 * e] += __uint_as_float(w[e] << 16);
-    acc[2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
-  }
+  for (int e = 0; e < 4; ++e)
+    a2[e] = __fadd2_rn(a2[e], make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u)));
 }
 
 // ------------------------------------------------------------------ state build
@@ -645,10 +645,14 @@ __global__ void __launch_bounds__(kReadThreads, 1) global_read_tc(const __grid_c
       for (int c = 0; c < kParts; ++c) {
         uint8_t *box = stage + ((D / 64) * half + c) * kBlk;  // box b holds columns [32b, 32b + 32)
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          *reinterpret_cast<float4 *>(box + sw128_offset_f32(row, 4 * q4)) =
-              make_float4(__uint_as_float(v[c][4 * q4]) * inv, __uint_as_float(v[c][4 * q4 + 1]) * inv,
-                          __uint_as_float(v[c][4 * q4 + 2]) * inv, __uint_as_float(v[c][4 * q4 + 3]) * inv);
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float2 a = __fmul2_rn(make_float2(__uint_as_float(v[c][4 * q4]), __uint_as_float(v[c][4 * q4 + 1])),
+                                      make_float2(inv, inv));
+          const float2 b = __fmul2_rn(make_float2(__uint_as_float(v[c][4 * q4 + 2]),
+                                                  __uint_as_float(v[c][4 * q4 + 3])),
+                                      make_float2(inv, inv));
+          *reinterpret_cast<float4 *>(box + sw128_offset_f32(row, 4 * q4)) = make_float4(a.x, a.y, b.x, b.y);
+        }
       }
       fence_async_smem();
       named_bar(kBarEpi, kReadEpi);
