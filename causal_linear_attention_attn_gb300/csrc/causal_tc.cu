@@ -638,6 +638,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         // keys [16g, 16g+16) become 8 columns of P_hi pairs then 8 of P_lo pairs.
         // Key blocks right of this warp's rows are all masked (zeros).
         float2 rs2 = make_float2(0.f, 0.f);  // row sum over even and odd keys
+        const int jmax = min(T, tv - 1);       // key j is kept when j <= T (inclusive) and j < tv
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           if (cb > quarter) {
@@ -651,8 +652,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
 #pragma unroll
               for (int m = 0; m < 8; ++m) {
                 const int j = cb * 32 + g * 16 + 2 * m;
-                float p0 = (j <= T && j < tv) ? __uint_as_float(r[g * 16 + 2 * m]) : 0.f;
-                float p1 = (j + 1 <= T && j + 1 < tv) ? __uint_as_float(r[g * 16 + 2 * m + 1]) : 0.f;
+                float p0 = j <= jmax ? __uint_as_float(r[g * 16 + 2 * m]) : 0.f;
+                float p1 = j + 1 <= jmax ? __uint_as_float(r[g * 16 + 2 * m + 1]) : 0.f;
                 float2 pp = make_float2(p0, p1);  // packed fp32 pairs from here on
                 if (kRet) {
                   const float2 wj = *reinterpret_cast<const float2 *>(den_s + j);
