@@ -615,7 +615,7 @@ def main_ours(args):
                                                                   stream, hbm, src)
             forms["retention_decode_bf16"]["clocks"] = clk.summary(*LAST_WINDOW)
             torch.cuda.empty_cache()
-    e2e = run_e2e(L, w, bufs, max(3, args.steps // 10), args.warmup, stream)
+    e2e = run_e2e(L, w, bufs, max(3, args.steps // 10), args.warmup, stream, args.e2e_groups)
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     if rank != 0:
         return
@@ -673,6 +673,7 @@ def parse(argv=None):
                                      "causal_bf16_backward,decode_bf16,retention_decode_bf16",
                     help="comma-separated other forms timed after the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=4, help="head groups the end-to-end leg pipelines over")
     ap.add_argument("--ref-step-s", type=float, default=10.0, help="max CPU seconds per reference step")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)

@@ -45,6 +45,7 @@ namespace {
 
 constexpr int kT = 64;          // tokens per chunk
 constexpr int kThreads = 256;   // a 16 x 16 grid of threads
+static_assert(kThreads >= 64, "one thread per token of a chunk");
 
 template <int DK, int DV>
 struct BwdSmem {
@@ -79,6 +80,59 @@ __device__ __forceinline__ void tile_fma(float (&acc)[TR][TC], int K, int ty, in
   }
 }
 
+// Eight consecutive inputs as loaded by one 16-byte (bf16) or two 16-byte (fp32) loads.
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) { u = __ldg(reinterpret_cast<const uint4 *>(p)); }
+  __device__ __forceinline__ float operator[](int e) const {
+    const uint32_t w = e < 2 ? u.x : e < 4 ? u.y : e < 6 ? u.z : u.w;
+    return __uint_as_float(e & 1 ? (w & 0xffff0000u) : (w << 16));  // bf16 is the top half of an fp32
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float *p) {
+    a = __ldg(reinterpret_cast<const float4 *>(p));
+    b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  }
+  __device__ __forceinline__ float operator[](int e) const {
+    return e < 4 ? (e < 2 ? (e ? a.y : a.x) : (e == 2 ? a.z : a.w)) : (e < 6 ? (e == 4 ? b.x : b.y) : (e == 6 ? b.z : b.w));
+  }
+};
+
+// One chunk's rows [0, T) of a row-major [*][W] block, staged in two steps so
+// that the loads of several blocks are all in flight before any is stored:
+// load() issues 16-byte loads (the C ABI requires 16-byte aligned inputs, and
+// every chunk of a head starts at a multiple of 64 rows), store() writes f(x)
+// into shared memory rows of P floats.
+template <int W, typename T>
+struct ChunkRows {
+  static constexpr int kIt = kT * W / (8 * kThreads);
+  static_assert(kIt >= 1 && kT * W % (8 * kThreads) == 0, "whole vectors per thread");
+  Raw8<T> r[kIt];
+  __device__ __forceinline__ void load(const T *src, int T_, int tid) {
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int e = 8 * (tid + kThreads * it);
+      if (e / W < T_) r[it].load(src + e);
+    }
+  }
+  template <typename F>
+  __device__ __forceinline__ void store(float *dst, int P, int T_, int tid, F f) const {
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int e = 8 * (tid + kThreads * it), t = e / W, c = e - t * W;
+      if (t < T_)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dst[t * P + c + u] = f(r[it][u]);
+    }
+  }
+};
+
 template <int TR, int TC>
 __device__ __forceinline__ void zero(float (&acc)[TR][TC]) {
 #pragma unroll
@@ -92,11 +146,14 @@ struct BwdArgs {
   const void *q, *k, *v;
   const float *dout, *S0, *z0, *dSN, *dzN;
   float *dq, *dk, *dv, *dS0, *dz0;
-  float *G;     // [BH][N][DV + 1]: gnum, gden of every token
-  float *segS;  // [BH][nseg][DK * DV + DK]: phi(K)^T V, colsum phi(K) of each segment
-  float *segU;  // [BH][nseg][DK * DV + DK]: phi(Q)^T gnum, phi(Q)^T gden of each segment
+  float *gnum;  // [BH][N][DV]: gnum of every token
+  float *gden;  // [BH][N]: gden of every token
+  // sums over the nsub parts of each segment (part f of segment s at s * nsub + f):
+  float *segS;  // [BH][nseg * nsub][DK * DV + DK]: phi(K)^T V, colsum phi(K)
+  float *segU;  // [BH][nseg * nsub][DK * DV + DK]: phi(Q)^T gnum, phi(Q)^T gden
   long N;
   int seg_chunks, nseg;
+  int sub_chunks, nsub;  // a segment's parts for the sum phases: nsub runs of sub_chunks chunks
   float eps;
 };
 
@@ -111,7 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
   float *__restrict__ dq = arg.dq;
   float *__restrict__ dk_g = arg.dk;
   float *__restrict__ dv_g = arg.dv;
-  float *__restrict__ G = arg.G;
   const long N = arg.N;
   const float eps = arg.eps;
   using L = BwdSmem<DK, DV>;
@@ -130,15 +186,25 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
   float *gd = den + kT;       // [kT] gden
 
   const long bh = blockIdx.y;
-  const int seg = blockIdx.x;
+  // the sum phases run one CTA per part of a segment, the passes one per segment
+  constexpr bool kSumPhase = kPhase == kSegSums || kPhase == kGradSums;
+  const int seg = kSumPhase ? (int)blockIdx.x / arg.nsub : (int)blockIdx.x;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const long nch = (N + kT - 1) / kT;
-  const long c_begin = (long)seg * arg.seg_chunks, c_end = min(nch, c_begin + arg.seg_chunks);
+  long c_begin = (long)seg * arg.seg_chunks, c_end = min(nch, c_begin + arg.seg_chunks);
+  if (kSumPhase) {
+    const long b = c_begin + (long)(blockIdx.x % arg.nsub) * arg.sub_chunks;
+    c_end = min(c_end, b + arg.sub_chunks);
+    c_begin = b;  // at or past c_end: an empty part, whose sum is zero
+  }
   constexpr int kSum = DK * DV + DK;  // one segment sum: matrix then vector
+  const long nparts = (long)arg.nseg * arg.nsub;
   const Tin *qh = q + bh * N * DK, *kh = k + bh * N * DK, *vh = v + bh * N * DV;
   const float *oh = dout + bh * N * DV;
   float *dqh = dq + bh * N * DK, *dkh = dk_g + bh * N * DK, *dvh = dv_g + bh * N * DV;
-  float *Gh = G + bh * N * (DV + 1);  // per token: gnum (DV), gden
+  float *gnum_h = arg.gnum + bh * N * DV, *gden_h = arg.gden + bh * N;
+  const auto phi_f = [](float x) { return phi(x); };
+  const auto id_f = [](float x) { return x; };
 
   // operand accessors (row, column) of the products below
   auto aQ = [&](int t, int i) { return Qs[t * KP + i]; };
@@ -152,12 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
 
   // starting state: pass 1 from S0 plus the earlier segments' sums; the sum phases from zero
   {
-    const float *part = arg.segS + bh * arg.nseg * (long)kSum;
+    const float *part = arg.segS + bh * nparts * kSum;
     for (int e = tid; e < DK * DV + DK; e += kThreads) {
       float x = 0.f;
       if (kPhase == kPass1) {
         x = e < DK * DV ? (arg.S0 ? arg.S0[bh * DK * DV + e] : 0.f) : (arg.z0 ? arg.z0[bh * DK + e - DK * DV] : 0.f);
-        for (int s2 = 0; s2 < seg; ++s2) x += part[s2 * (long)kSum + e];
+        for (long s2 = 0; s2 < (long)seg * arg.nsub; ++s2) x += part[s2 * kSum + e];
       }
       if (e < DK * DV) S[(e / DV) * VP + e % DV] = x;
       else z[e - DK * DV] = x;
@@ -193,12 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
     for (long ci = c_begin; ci < c_end; ++ci) {
       const long t0 = ci * kT;
       const int T = (int)min((long)kT, N - t0);
-      __syncthreads();
-      for (int e = tid; e < T * DK; e += kThreads) {
-        const int t = e / DK, i = e - t * DK;
-        Ks[t * KP + i] = phi(ldf(kh + (t0 + t) * DK + i));
-      }
-      for (int e = tid; e < T * DV; e += kThreads) Vs[(e / DV) * VP + e % DV] = ldf(vh + t0 * DV + e);
+      ChunkRows<DK, Tin> lk;
+      ChunkRows<DV, Tin> lv;
+      lk.load(kh + t0 * DK, T, tid);
+      lv.load(vh + t0 * DV, T, tid);
+      __syncthreads();  // the previous chunk is fully consumed
+      lk.store(Ks, KP, T, tid, phi_f);
+      lv.store(Vs, VP, T, tid, id_f);
       __syncthreads();
       float acc[RK][RV];
       zero(acc);
@@ -214,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
       }
     }
     __syncthreads();
-    float *dst = arg.segS + (bh * arg.nseg + seg) * (long)kSum;
+    float *dst = arg.segS + (bh * nparts + blockIdx.x) * kSum;
     for (int e = tid; e < DK * DV + DK; e += kThreads) dst[e] = e < DK * DV ? S[(e / DV) * VP + e % DV] : z[e - DK * DV];
     return;
   }
@@ -225,13 +292,15 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
     for (long ci = c_begin; ci < c_end; ++ci) {
       const long t0 = ci * kT;
       const int T = (int)min((long)kT, N - t0);
-      __syncthreads();
-      for (int e = tid; e < T * DK; e += kThreads) {
-        const int t = e / DK, i = e - t * DK;
-        Qs[t * KP + i] = phi(ldf(qh + (t0 + t) * DK + i));
-      }
-      for (int e = tid; e < T * DV; e += kThreads) Gs[e] = Gh[(t0 + e / DV) * (DV + 1) + e % DV];
-      for (int t = tid; t < T; t += kThreads) gd[t] = Gh[(t0 + t) * (DV + 1) + DV];
+      ChunkRows<DK, Tin> lq;
+      ChunkRows<DV, float> lg;
+      lq.load(qh + t0 * DK, T, tid);
+      lg.load(gnum_h + t0 * DV, T, tid);
+      const float gd_t = tid < T ? __ldg(gden_h + t0 + tid) : 0.f;  // kThreads >= kT
+      __syncthreads();  // the previous chunk is fully consumed
+      lq.store(Qs, KP, T, tid, phi_f);
+      lg.store(Gs, DV, T, tid, id_f);
+      if (tid < T) gd[tid] = gd_t;
       __syncthreads();
       float acc[RK][RV];
       zero(acc);
@@ -247,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
       }
     }
     __syncthreads();
-    float *dst = arg.segU + (bh * arg.nseg + seg) * (long)kSum;
+    float *dst = arg.segU + (bh * nparts + blockIdx.x) * kSum;
     for (int e = tid; e < DK * DV + DK; e += kThreads) dst[e] = e < DK * DV ? S[(e / DV) * VP + e % DV] : z[e - DK * DV];
     return;
   }
@@ -255,16 +324,18 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
   // ---------------- pass 1: chunks in order ----------------
   if constexpr (kPhase == kPass1) for (long t0 = c_begin * kT; t0 < c_end * kT && t0 < N; t0 += kT) {
     const int T = (int)min((long)kT, N - t0);
+    ChunkRows<DK, Tin> lq, lk;
+    ChunkRows<DV, Tin> lv;
+    ChunkRows<DV, float> lo;
+    lq.load(qh + t0 * DK, T, tid);
+    lk.load(kh + t0 * DK, T, tid);
+    lv.load(vh + t0 * DV, T, tid);
+    lo.load(oh + t0 * DV, T, tid);
     __syncthreads();  // the previous chunk is fully consumed
-    for (int e = tid; e < T * DK; e += kThreads) {
-      const int t = e / DK, i = e - t * DK;
-      Qs[t * KP + i] = phi(ldf(qh + (t0 + t) * DK + i));
-      Ks[t * KP + i] = phi(ldf(kh + (t0 + t) * DK + i));
-    }
-    for (int e = tid; e < T * DV; e += kThreads) {
-      Vs[(e / DV) * VP + e % DV] = ldf(vh + t0 * DV + e);
-      Gs[e] = oh[t0 * DV + e];
-    }
+    lq.store(Qs, KP, T, tid, phi_f);
+    lk.store(Ks, KP, T, tid, phi_f);
+    lv.store(Vs, VP, T, tid, id_f);
+    lo.store(Gs, DV, T, tid, id_f);
     __syncthreads();
     scores(T, false);
     __syncthreads();
@@ -299,10 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
     __syncthreads();
     for (int e = tid; e < T * DV; e += kThreads) Gs[e] /= den[e / DV];  // gnum
     __syncthreads();
-    for (int e = tid; e < T * (DV + 1); e += kThreads) {
-      const int t = e / (DV + 1), c = e - t * (DV + 1);
-      Gh[(t0 + t) * (DV + 1) + c] = c < DV ? Gs[t * DV + c] : gd[t];
-    }
+    for (int e = tid; e < T * DV; e += kThreads) gnum_h[t0 * DV + e] = Gs[e];
+    for (int t = tid; t < T; t += kThreads) gden_h[t0 + t] = gd[t];
     {
       // Bm (the masked score gradients), as in pass 2
       float acc[4][4];
@@ -357,12 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
   // ---------------- pass 2: chunks in reverse ----------------
   // U, u at the segment's end: dS, dz plus the later segments' gradient sums
   {
-    const float *part = arg.segU + bh * arg.nseg * (long)kSum;
+    const float *part = arg.segU + bh * nparts * kSum;
     __syncthreads();
     for (int e = tid; e < DK * DV + DK; e += kThreads) {
       float x = e < DK * DV ? (arg.dSN ? arg.dSN[bh * DK * DV + e] : 0.f)
                             : (arg.dzN ? arg.dzN[bh * DK + e - DK * DV] : 0.f);
-      for (int s2 = seg + 1; s2 < arg.nseg; ++s2) x += part[s2 * (long)kSum + e];
+      for (long s2 = (long)(seg + 1) * arg.nsub; s2 < nparts; ++s2) x += part[s2 * kSum + e];
       if (e < DK * DV) S[(e / DV) * VP + e % DV] = x;
       else z[e - DK * DV] = x;
     }
@@ -370,18 +439,20 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
   for (long ci = c_end - 1; ci >= c_begin; --ci) {
     const long t0 = ci * kT;
     const int T = (int)min((long)kT, N - t0);
-    __syncthreads();
-    for (int e = tid; e < T * DK; e += kThreads) {
-      const int t = e / DK, i = e - t * DK;
-      Qs[t * KP + i] = phi(ldf(qh + (t0 + t) * DK + i));
-      Ks[t * KP + i] = phi(ldf(kh + (t0 + t) * DK + i));
-    }
-    for (int e = tid; e < T * DV; e += kThreads) {
-      const int t = e / DV, c = e - t * DV;
-      Vs[t * VP + c] = ldf(vh + t0 * DV + e);
-      Gs[e] = Gh[(t0 + t) * (DV + 1) + c];
-    }
-    for (int t = tid; t < T; t += kThreads) gd[t] = Gh[(t0 + t) * (DV + 1) + DV];
+    ChunkRows<DK, Tin> lq, lk;
+    ChunkRows<DV, Tin> lv;
+    ChunkRows<DV, float> lg;
+    lq.load(qh + t0 * DK, T, tid);
+    lk.load(kh + t0 * DK, T, tid);
+    lv.load(vh + t0 * DV, T, tid);
+    lg.load(gnum_h + t0 * DV, T, tid);
+    const float gd_t = tid < T ? __ldg(gden_h + t0 + tid) : 0.f;  // kThreads >= kT
+    __syncthreads();  // the previous chunk is fully consumed
+    lq.store(Qs, KP, T, tid, phi_f);
+    lk.store(Ks, KP, T, tid, phi_f);
+    lv.store(Vs, VP, T, tid, id_f);
+    lg.store(Gs, DV, T, tid, id_f);
+    if (tid < T) gd[tid] = gd_t;
     __syncthreads();
     scores(T, true);
     __syncthreads();
@@ -456,9 +527,9 @@ template <typename Tin, int DK, int DV>
 cudaError_t launch_t(const BwdArgs &a, int BH, cudaStream_t stream) {
   LaunchTimer timer(kKBackward, stream);
   cudaError_t e = cudaSuccess;
-  if (a.nseg > 1) e = launch_phase<Tin, DK, DV, kSegSums>(a, dim3(a.nseg - 1, BH), stream);
+  if (a.nseg > 1) e = launch_phase<Tin, DK, DV, kSegSums>(a, dim3((a.nseg - 1) * a.nsub, BH), stream);
   if (e == cudaSuccess) e = launch_phase<Tin, DK, DV, kPass1>(a, dim3(a.nseg, BH), stream);
-  if (e == cudaSuccess && a.nseg > 1) e = launch_phase<Tin, DK, DV, kGradSums>(a, dim3(a.nseg, BH), stream);
+  if (e == cudaSuccess && a.nseg > 1) e = launch_phase<Tin, DK, DV, kGradSums>(a, dim3(a.nseg * a.nsub, BH), stream);
   if (e == cudaSuccess) e = launch_phase<Tin, DK, DV, kPass2>(a, dim3(a.nseg, BH), stream);
   timer.done(e);
   return e;
@@ -488,9 +559,15 @@ cudaError_t launch_causal_backward(const BackwardProblem &b) {
   long nseg = std::max(1L, std::min(sms / std::max(1, p.BH), nch / 4));
   const long seg_chunks = std::max(1L, (nch + nseg - 1) / nseg);
   nseg = std::max(1L, (nch + seg_chunks - 1) / seg_chunks);
-  // scratch: gnum and gden of every token, then the segment sums of the state and of the gradients
+  // the sum phases cut each segment into nsub parts, so that their CTAs (B H (nseg - 1) nsub
+  // with work) also cover the SMs about once
+  long nsub = 1;
+  if (nseg > 1) nsub = std::max(1L, std::min(seg_chunks, sms / std::max(1L, (long)p.BH * (nseg - 1))));
+  const long sub_chunks = (seg_chunks + nsub - 1) / nsub;
+  nsub = (seg_chunks + sub_chunks - 1) / sub_chunks;
+  // scratch: gnum and gden of every token, then the part sums of the state and of the gradients
   const size_t sum_f = (size_t)p.dk * p.dv + p.dk;
-  const size_t g_f = (size_t)p.BH * p.N * (p.dv + 1), seg_f = (size_t)p.BH * nseg * sum_f;
+  const size_t g_f = (size_t)p.BH * p.N * (p.dv + 1), seg_f = (size_t)p.BH * nseg * nsub * sum_f;
   float *G = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&G), std::max<size_t>(sizeof(float) * (g_f + 2 * seg_f), 16),
                                   p.stream);
@@ -499,8 +576,9 @@ cudaError_t launch_causal_backward(const BackwardProblem &b) {
   a.q = p.q, a.k = p.k, a.v = p.v;
   a.dout = b.dout, a.S0 = b.S0, a.z0 = b.z0, a.dSN = b.dS, a.dzN = b.dz;
   a.dq = b.dq, a.dk = b.dk, a.dv = b.dv, a.dS0 = b.dS0, a.dz0 = b.dz0;
-  a.G = G, a.segS = G + g_f, a.segU = G + g_f + seg_f;
+  a.gnum = G, a.gden = G + (size_t)p.BH * p.N * p.dv, a.segS = G + g_f, a.segU = G + g_f + seg_f;
   a.N = p.N, a.seg_chunks = (int)seg_chunks, a.nseg = (int)nseg, a.eps = p.eps;
+  a.sub_chunks = (int)sub_chunks, a.nsub = (int)nsub;
   e = p.dt == LA_F32 ? launch_dk<float>(a, p.BH, p.dk, p.dv, p.stream)
                      : launch_dk<__nv_bfloat16>(a, p.BH, p.dk, p.dv, p.stream);
   const cudaError_t f = cudaFreeAsync(G, p.stream);
