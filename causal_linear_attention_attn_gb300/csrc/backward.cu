@@ -56,16 +56,17 @@ struct BwdSmem {
 };
 static_assert(BwdSmem<128, 128>::Bytes <= 232448, "shared memory budget");
 
-// acc[r][c] += sum_{k < K} a(ty + 16 r, k) b(k, tx + 16 c); pairs of columns share one
-// packed fp32 FMA (TC is even)
-template <int TR, int TC, typename FA, typename FB>
-__device__ __forceinline__ void tile_fma(float (&acc)[TR][TC], int K, int ty, int tx, FA a, FB b) {
+// acc[r][c] += sum_{k0 <= k < k1} a(row(r), k) b(k, tx + 16 c), where row(r) is ty + 16 r,
+// or TR ty + r with kBlockRows (each thread's rows consecutive, so that a triangular
+// operand bounds its k range); pairs of columns share one packed fp32 FMA (TC is even)
+template <int TR, int TC, bool kBlockRows = false, typename FA, typename FB>
+__device__ __forceinline__ void tile_fma(float (&acc)[TR][TC], int k0, int k1, int ty, int tx, FA a, FB b) {
   static_assert(TC % 2 == 0, "columns go in pairs");
 #pragma unroll 4
-  for (int k = 0; k < K; ++k) {
+  for (int k = k0; k < k1; ++k) {
     float av[TR], bv[TC];
 #pragma unroll
-    for (int r = 0; r < TR; ++r) av[r] = a(ty + 16 * r, k);
+    for (int r = 0; r < TR; ++r) av[r] = a(kBlockRows ? TR * ty + r : ty + 16 * r, k);
 #pragma unroll
     for (int c = 0; c < TC; ++c) bv[c] = b(k, tx + 16 * c);
 #pragma unroll
@@ -78,6 +79,11 @@ __device__ __forceinline__ void tile_fma(float (&acc)[TR][TC], int K, int ty, in
         acc[r][c + 1] = y.y;
       }
   }
+}
+
+template <int TR, int TC, typename FA, typename FB>
+__device__ __forceinline__ void tile_fma(float (&acc)[TR][TC], int K, int ty, int tx, FA a, FB b) {
+  tile_fma<TR, TC, false>(acc, 0, K, ty, tx, a, b);
 }
 
 // Eight consecutive inputs as loaded by one 16-byte (bf16) or two 16-byte (fp32) loads.
@@ -146,6 +152,7 @@ struct BwdArgs {
   const void *q, *k, *v;
   const float *dout, *S0, *z0, *dSN, *dzN;
   float *dq, *dk, *dv, *dS0, *dz0;
+  float *Asc, *Bsc;  // [BH][nch * kT][kT]: pass 1's masked A and Bm of every chunk, for pass 2
   float *gnum;  // [BH][N][DV]: gnum of every token
   float *gden;  // [BH][N]: gden of every token
   // sums over the nsub parts of each segment (part f of segment s at s * nsub + f):
@@ -203,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
   const float *oh = dout + bh * N * DV;
   float *dqh = dq + bh * N * DK, *dkh = dk_g + bh * N * DK, *dvh = dv_g + bh * N * DV;
   float *gnum_h = arg.gnum + bh * N * DV, *gden_h = arg.gden + bh * N;
+  float *Ah = arg.Asc + bh * nch * kT * kT, *Bh = arg.Bsc + bh * nch * kT * kT;  // row t0 + t: chunk t0's row t
   const auto phi_f = [](float x) { return phi(x); };
   const auto id_f = [](float x) { return x; };
 
@@ -230,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
     }
   }
 
-  // masked scores A = tril(phi(Q) phi(K)^T) and score gradients Bm = tril(gnum V^T + gden)
-  auto scores = [&](int T, bool with_b) {
+  // masked scores A = tril(phi(Q) phi(K)^T)
+  auto scores = [&](int T) {
     float acc[4][4];
     zero(acc);
     tile_fma(acc, DK, ty, tx, aQ, bKt);
@@ -241,16 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
       for (int c = 0; c < 4; ++c) {
         const int t = ty + 16 * r, j = tx + 16 * c;
         A[t * AP + j] = (j <= t && t < T) ? acc[r][c] : 0.f;
-      }
-    if (!with_b) return;
-    zero(acc);
-    tile_fma(acc, DV, ty, tx, aG, bVt);
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int t = ty + 16 * r, j = tx + 16 * c;
-        Bm[t * AP + j] = (j <= t && t < T) ? acc[r][c] + gd[t] : 0.f;
       }
   };
 
@@ -337,25 +335,42 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
     lv.store(Vs, VP, T, tid, id_f);
     lo.store(Gs, DV, T, tid, id_f);
     __syncthreads();
-    scores(T, false);
+    scores(T);
     __syncthreads();
-    for (int t = tid; t < T; t += kThreads) {
-      float d = 0.f;
-      for (int i = 0; i < DK; ++i) d = fmaf(Qs[t * KP + i], z[i], d);
-      float a = 0.f;
-      for (int j = 0; j <= t; ++j) a += A[t * AP + j];
-      den[t] = (d + a) + eps;
+    {
+      // four lanes per token, each a quarter of phi(q_t).z and of the row sum of A (rotated
+      // start columns keep the 32 lanes of a warp on distinct banks)
+      static_assert(kThreads == 4 * kT, "four lanes per token");
+      const int t = tid >> 2, part = tid & 3;
+      constexpr int QI = DK / 4;
+      float d = 0.f, a = 0.f;
+#pragma unroll 4
+      for (int m = 0; m < QI; ++m) {
+        const int i = part * QI + (m + 8 * part) % QI;
+        d = fmaf(Qs[t * KP + i], z[i], d);
+      }
+#pragma unroll 4
+      for (int m = 0; m < kT / 4; ++m) {
+        const int j = part * (kT / 4) + m;
+        if (j <= t) a += A[t * AP + j];
+      }
+      d += __shfl_xor_sync(0xffffffffu, d, 1);
+      a += __shfl_xor_sync(0xffffffffu, a, 1);
+      d += __shfl_xor_sync(0xffffffffu, d, 2);
+      a += __shfl_xor_sync(0xffffffffu, a, 2);
+      if (part == 0 && t < T) den[t] = (d + a) + eps;
     }
     __syncthreads();
     {
       // outputs o_t = (phi(q_t) S_prev + sum_j A_tj v_j) / den_t, then gden_t = -(dO_t . o_t) / den_t
+      // rows 4 ty .. 4 ty + 3: A_tj is zero past j = t
       float acc[4][RV];
       zero(acc);
-      tile_fma(acc, DK, ty, tx, aQ, bS);
-      tile_fma(acc, T, ty, tx, aA, bV);
+      tile_fma<4, RV, true>(acc, 0, DK, ty, tx, aQ, bS);
+      tile_fma<4, RV, true>(acc, 0, min(T, 4 * ty + 4), ty, tx, aA, bV);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int t = ty + 16 * r;
+        const int t = 4 * ty + r;
         float dot = 0.f;
         if (t < T) {
           const float inv = 1.f / den[t];
@@ -373,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
     for (int e = tid; e < T * DV; e += kThreads) gnum_h[t0 * DV + e] = Gs[e];
     for (int t = tid; t < T; t += kThreads) gden_h[t0 + t] = gd[t];
     {
-      // Bm (the masked score gradients), as in pass 2
+      // Bm = tril(gnum V^T + gden), the masked score gradients
       float acc[4][4];
       zero(acc);
       tile_fma(acc, DV, ty, tx, aG, bVt);
@@ -386,15 +401,23 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
         }
     }
     __syncthreads();
+    // A and Bm for pass 2, which reads them instead of forming them again
+    for (int e = tid; e < kT * kT; e += kThreads) {
+      const int t = e / kT, j = e - t * kT;
+      Ah[t0 * kT + e] = A[t * AP + j];
+      Bh[t0 * kT + e] = Bm[t * AP + j];
+    }
     {
       // dphi(q_t) = S_prev gnum_t + z_prev gden_t + sum_{j <= t} Bm_tj phi(k_j)
+      // rows 4 ty .. 4 ty + 3: Bm_tj is zero past j = t
       float acc[4][RK];
       zero(acc);
-      tile_fma(acc, DV, ty, tx, aG, bSt);
-      tile_fma(acc, T, ty, tx, [&](int t, int j) { return Bm[t * AP + j]; }, [&](int j, int i) { return Ks[j * KP + i]; });
+      tile_fma<4, RK, true>(acc, 0, DV, ty, tx, aG, bSt);
+      tile_fma<4, RK, true>(acc, 0, min(T, 4 * ty + 4), ty, tx, [&](int t, int j) { return Bm[t * AP + j]; },
+                            [&](int j, int i) { return Ks[j * KP + i]; });
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int t = ty + 16 * r;
+        const int t = 4 * ty + r;
         if (t < T)
 #pragma unroll
           for (int c = 0; c < RK; ++c) {
@@ -447,24 +470,29 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
     lv.load(vh + t0 * DV, T, tid);
     lg.load(gnum_h + t0 * DV, T, tid);
     const float gd_t = tid < T ? __ldg(gden_h + t0 + tid) : 0.f;  // kThreads >= kT
+    ChunkRows<kT, float> la, lb;  // pass 1's A and Bm (all kT rows: zero past T)
+    la.load(Ah + t0 * kT, kT, tid);
+    lb.load(Bh + t0 * kT, kT, tid);
     __syncthreads();  // the previous chunk is fully consumed
     lq.store(Qs, KP, T, tid, phi_f);
     lk.store(Ks, KP, T, tid, phi_f);
     lv.store(Vs, VP, T, tid, id_f);
     lg.store(Gs, DV, T, tid, id_f);
+    la.store(A, AP, kT, tid, id_f);
+    lb.store(Bm, AP, kT, tid, id_f);
     if (tid < T) gd[tid] = gd_t;
-    __syncthreads();
-    scores(T, true);
     __syncthreads();
     {
       // dphi(k_j) = U v_j + u + sum_{t >= j} Bm_tj phi(q_t)
+      // rows 4 ty .. 4 ty + 3: Bm_tj is zero before t = j
       float acc[4][RK];
       zero(acc);
-      tile_fma(acc, DV, ty, tx, [&](int j, int c) { return Vs[j * VP + c]; }, bSt);
-      tile_fma(acc, T, ty, tx, [&](int j, int t) { return Bm[t * AP + j]; }, [&](int t, int i) { return Qs[t * KP + i]; });
+      tile_fma<4, RK, true>(acc, 0, DV, ty, tx, [&](int j, int c) { return Vs[j * VP + c]; }, bSt);
+      tile_fma<4, RK, true>(acc, 4 * ty, T, ty, tx, [&](int j, int t) { return Bm[t * AP + j]; },
+                            [&](int t, int i) { return Qs[t * KP + i]; });
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int j = ty + 16 * r;
+        const int j = 4 * ty + r;
         if (j < T)
 #pragma unroll
           for (int c = 0; c < RK; ++c) {
@@ -475,13 +503,15 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
     }
     {
       // dv_j = U^T phi(k_j) + sum_{t >= j} A_tj gnum_t
+      // rows 4 ty .. 4 ty + 3: A_tj is zero before t = j
       float acc[4][RV];
       zero(acc);
-      tile_fma(acc, DK, ty, tx, [&](int j, int i) { return Ks[j * KP + i]; }, bS);
-      tile_fma(acc, T, ty, tx, [&](int j, int t) { return A[t * AP + j]; }, [&](int t, int c) { return Gs[t * DV + c]; });
+      tile_fma<4, RV, true>(acc, 0, DK, ty, tx, [&](int j, int i) { return Ks[j * KP + i]; }, bS);
+      tile_fma<4, RV, true>(acc, 4 * ty, T, ty, tx, [&](int j, int t) { return A[t * AP + j]; },
+                            [&](int t, int c) { return Gs[t * DV + c]; });
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int j = ty + 16 * r;
+        const int j = 4 * ty + r;
         if (j < T)
 #pragma unroll
           for (int c = 0; c < RV; ++c) dvh[(t0 + j) * DV + tx + 16 * c] = acc[r][c];
@@ -565,9 +595,11 @@ cudaError_t launch_causal_backward(const BackwardProblem &b) {
   if (nseg > 1) nsub = std::max(1L, std::min(seg_chunks, sms / std::max(1L, (long)p.BH * (nseg - 1))));
   const long sub_chunks = (seg_chunks + nsub - 1) / nsub;
   nsub = (seg_chunks + sub_chunks - 1) / sub_chunks;
-  // scratch: gnum and gden of every token, then the part sums of the state and of the gradients
+  // scratch: A and Bm of every chunk, gnum and gden of every token, then the part sums of the
+  // state and of the gradients (every block starts 16-byte aligned)
   const size_t sum_f = (size_t)p.dk * p.dv + p.dk;
-  const size_t g_f = (size_t)p.BH * p.N * (p.dv + 1), seg_f = (size_t)p.BH * nseg * nsub * sum_f;
+  const size_t ab_f = (size_t)p.BH * nch * kT * kT;
+  const size_t g_f = 2 * ab_f + (size_t)p.BH * p.N * (p.dv + 1), seg_f = (size_t)p.BH * nseg * nsub * sum_f;
   float *G = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&G), std::max<size_t>(sizeof(float) * (g_f + 2 * seg_f), 16),
                                   p.stream);
@@ -576,7 +608,8 @@ cudaError_t launch_causal_backward(const BackwardProblem &b) {
   a.q = p.q, a.k = p.k, a.v = p.v;
   a.dout = b.dout, a.S0 = b.S0, a.z0 = b.z0, a.dSN = b.dS, a.dzN = b.dz;
   a.dq = b.dq, a.dk = b.dk, a.dv = b.dv, a.dS0 = b.dS0, a.dz0 = b.dz0;
-  a.gnum = G, a.gden = G + (size_t)p.BH * p.N * p.dv, a.segS = G + g_f, a.segU = G + g_f + seg_f;
+  a.Asc = G, a.Bsc = G + ab_f;
+  a.gnum = G + 2 * ab_f, a.gden = a.gnum + (size_t)p.BH * p.N * p.dv, a.segS = G + g_f, a.segU = G + g_f + seg_f;
   a.N = p.N, a.seg_chunks = (int)seg_chunks, a.nseg = (int)nseg, a.eps = p.eps;
   a.sub_chunks = (int)sub_chunks, a.nsub = (int)nsub;
   e = p.dt == LA_F32 ? launch_dk<float>(a, p.BH, p.dk, p.dv, p.stream)
