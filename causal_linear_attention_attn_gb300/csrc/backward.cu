@@ -360,35 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
       a += __shfl_xor_sync(0xffffffffu, a, 2);
       if (part == 0 && t < T) den[t] = (d + a) + eps;
     }
-    __syncthreads();
+    // dO_t . o_t = (phi(q_t) . Y_t + sum_j A_tj C_tj) / den_t with Y = dO S_prev^T and C = dO V^T;
+    // Y_t / den_t is also dq's state term, so one product serves both
+    float accy[4][RK];  // Y, rows 4 ty .. 4 ty + 3
     {
-      // outputs o_t = (phi(q_t) S_prev + sum_j A_tj v_j) / den_t, then gden_t = -(dO_t . o_t) / den_t
-      // rows 4 ty .. 4 ty + 3: A_tj is zero past j = t
-      float acc[4][RV];
-      zero(acc);
-      tile_fma<4, RV, true>(acc, 0, DK, ty, tx, aQ, bS);
-      tile_fma<4, RV, true>(acc, 0, min(T, 4 * ty + 4), ty, tx, aA, bV);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int t = 4 * ty + r;
-        float dot = 0.f;
-        if (t < T) {
-          const float inv = 1.f / den[t];
-#pragma unroll
-          for (int c = 0; c < RV; ++c) dot = fmaf(Gs[t * DV + tx + 16 * c], acc[r][c] * inv, dot);
-        }
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (tx == 0 && t < T) gd[t] = -dot / den[t];
-      }
-    }
-    __syncthreads();
-    for (int e = tid; e < T * DV; e += kThreads) Gs[e] /= den[e / DV];  // gnum
-    __syncthreads();
-    for (int e = tid; e < T * DV; e += kThreads) gnum_h[t0 * DV + e] = Gs[e];
-    for (int t = tid; t < T; t += kThreads) gden_h[t0 + t] = gd[t];
-    {
-      // Bm = tril(gnum V^T + gden), the masked score gradients
+      // C, masked (j <= t < T), in Bm's slot until Bm is formed from it
       float acc[4][4];
       zero(acc);
       tile_fma(acc, DV, ty, tx, aG, bVt);
@@ -397,10 +373,50 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int t = ty + 16 * r, j = tx + 16 * c;
-          Bm[t * AP + j] = (j <= t && t < T) ? acc[r][c] + gd[t] : 0.f;
+          Bm[t * AP + j] = (j <= t && t < T) ? acc[r][c] : 0.f;
         }
     }
+    zero(accy);
+    tile_fma<4, RK, true>(accy, 0, DV, ty, tx, aG, bSt);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      // phi(q_t) . Y_t, held in gd[t] until gden_t replaces it
+      const int t = 4 * ty + r;
+      float x = 0.f;
+      if (t < T)
+#pragma unroll
+        for (int c = 0; c < RK; ++c) x = fmaf(Qs[t * KP + tx + 16 * c], accy[r][c], x);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (tx == 0 && t < T) gd[t] = x;
+    }
     __syncthreads();
+    {
+      // gden_t = -(dO_t . o_t) / den_t, four lanes per token for sum_j A_tj C_tj
+      const int t = tid >> 2, part = tid & 3;
+      float ac = 0.f;
+#pragma unroll 4
+      for (int m = 0; m < kT / 4; ++m) {
+        const int j = part * (kT / 4) + m;
+        ac = fmaf(A[t * AP + j], Bm[t * AP + j], ac);
+      }
+      ac += __shfl_xor_sync(0xffffffffu, ac, 1);
+      ac += __shfl_xor_sync(0xffffffffu, ac, 2);
+      if (part == 0 && t < T) {
+        const float dt = den[t];
+        gd[t] = -((gd[t] + ac) / dt) / dt;
+      }
+    }
+    __syncthreads();
+    // gnum = dO / den; Bm = tril(C / den + gden), the masked score gradients
+    for (int e = tid; e < T * DV; e += kThreads) Gs[e] /= den[e / DV];
+    for (int e = tid; e < kT * kT; e += kThreads) {
+      const int t = e / kT, j = e - t * kT;
+      Bm[t * AP + j] = (j <= t && t < T) ? Bm[t * AP + j] / den[t] + gd[t] : 0.f;
+    }
+    __syncthreads();
+    for (int e = tid; e < T * DV; e += kThreads) gnum_h[t0 * DV + e] = Gs[e];
+    for (int t = tid; t < T; t += kThreads) gden_h[t0 + t] = gd[t];
     // A and Bm for pass 2, which reads them instead of forming them again
     for (int e = tid; e < kT * kT; e += kThreads) {
       const int t = e / kT, j = e - t * kT;
@@ -408,12 +424,16 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
       Bh[t0 * kT + e] = Bm[t * AP + j];
     }
     {
-      // dphi(q_t) = S_prev gnum_t + z_prev gden_t + sum_{j <= t} Bm_tj phi(k_j)
+      // dphi(q_t) = Y_t / den_t + z_prev gden_t + sum_{j <= t} Bm_tj phi(k_j)
       // rows 4 ty .. 4 ty + 3: Bm_tj is zero past j = t
-      float acc[4][RK];
-      zero(acc);
-      tile_fma<4, RK, true>(acc, 0, DV, ty, tx, aG, bSt);
-      tile_fma<4, RK, true>(acc, 0, min(T, 4 * ty + 4), ty, tx, [&](int t, int j) { return Bm[t * AP + j]; },
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int t = 4 * ty + r;
+        if (t < T)
+#pragma unroll
+          for (int c = 0; c < RK; ++c) accy[r][c] /= den[t];
+      }
+      tile_fma<4, RK, true>(accy, 0, min(T, 4 * ty + 4), ty, tx, [&](int t, int j) { return Bm[t * AP + j]; },
                             [&](int j, int i) { return Ks[j * KP + i]; });
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
@@ -422,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
 #pragma unroll
           for (int c = 0; c < RK; ++c) {
             const int i = tx + 16 * c;
-            dqh[(t0 + t) * DK + i] = (acc[r][c] + z[i] * gd[t]) * fminf(Qs[t * KP + i], 1.f);
+            dqh[(t0 + t) * DK + i] = (accy[r][c] + z[i] * gd[t]) * fminf(Qs[t * KP + i], 1.f);
           }
       }
     }
