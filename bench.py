@@ -466,6 +466,27 @@ def backward_bytes(w) -> float:
     return w.BH * w.N * ((2 * w.dk + w.dv) * in_bytes(w) + 4 * w.dv + 4 * (2 * w.dk + w.dv))
 
 
+# fp32 CUDA-core peak of a GB300: 152 SMs x 128 fp32 lanes x 2 FLOP per multiply-add x 2.07 GHz
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def backward_flops(w, chunk: int = 64) -> float:
+    """FLOPs (2 per multiply-add) that a chunked causal backward needs: per token, five
+    d_k x d_v state products (the fold S += phi(k) v^T; the read dO S^T, which serves
+    both gden and dq; the fold U += phi(q) gnum^T; the state terms U v and U^T phi(k)
+    of dk and dv), the intra-chunk scores phi(q).phi(k) and dO.v over one chunk,
+    and the three products with a triangular operand at half a chunk."""
+    per_token = 5 * w.dk * w.dv + chunk * (w.dk + w.dv) + chunk // 2 * (2 * w.dk + w.dv)
+    return 2.0 * w.BH * w.N * per_token
+
+
+def alu_roofline(flops: float, ms: float) -> dict:
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_PEAK_TFLOPS, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / FP32_PEAK_TFLOPS, 4),
+            "peak_source": "152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz", "alg_flops_per_call": flops}
+
+
 def run_backward(L, w, steps, warmup, world, stream, hbm, src):
     """Gradient of the causal prefill (la_causal_backward) for a seeded upstream gradient."""
     q, k, v = (t.cuda() for t in inputs.make_qkv(w, device="cuda"))
@@ -479,8 +500,9 @@ def run_backward(L, w, steps, warmup, world, stream, hbm, src):
     ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
     rl, table = dominant_roofline(L, w, steps, hbm, src, w.name + "_backward")
     return {"workload": w.name + " backward", "roofline": rl, "tokens_per_s": world * w.BH * w.N / (ms * 1e-3), "ms_per_call": ms,
-            "step_roofline": roofline(backward_bytes(w), ms, hbm, src, None), "kernels": table,
-            "gpu_launches": launches, "note": "exact fp32 CUDA-core kernel (one CTA per head)"}
+            "step_roofline": roofline(backward_bytes(w), ms, hbm, src, None),
+            "alu_roofline": alu_roofline(backward_flops(w), ms), "kernels": table,
+            "gpu_launches": launches, "note": "exact fp32 CUDA-core kernel, each head cut into segments"}
 
 
 def retention_decode_bytes(w) -> float:

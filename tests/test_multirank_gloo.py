@@ -61,3 +61,14 @@ def test_algorithmic_bytes_of_the_workloads():
     assert abs(bench.seq_bytes(W["causal_bf16_long"]) / 1e6 - 5370.8) < 0.1
     assert abs(bench.seq_bytes(W["global_bf16"]) / 1e6 - 337.7) < 0.1
     assert abs(bench.decode_bytes(W["decode_bf16"]) / 1e6 - 1092.6) < 0.1
+
+
+def test_backward_arithmetic_roofline():
+    # d = 128, 64-token chunks: 5 d^2 + 64 (2 d) + 32 (3 d) = 110,592 multiply-adds per token
+    w = inputs.WORKLOADS["causal_bf16"]
+    assert bench.backward_flops(w) == 2.0 * 4 * 16 * 8192 * 110592
+    assert abs(bench.FP32_PEAK_TFLOPS - 80.55) < 0.01
+    r = bench.alu_roofline(bench.backward_flops(w), 5.0)
+    assert r["bound"] == "alu" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - 2.0 * 4 * 16 * 8192 * 110592 / 5e-3 / 1e12) < 0.01
+    assert abs(r["frac"] - r["achieved"] / bench.FP32_PEAK_TFLOPS) < 1e-3
