@@ -18,23 +18,27 @@
 // 64-token chunks, all arithmetic in fp32.  Each head's sequence is cut into
 // segments, one CTA per (segment, head), and a call runs four phases of one
 // kernel template:
-//   segment sums: phi(K)^T V and colsum phi(K) of every segment but the last;
-//   pass 1 (chunks in order from S0 plus the earlier segments' sums): the
-//     state S, z; per chunk the masked scores A = tril(phi(Q) phi(K)^T), the
-//     denominators, the outputs, gnum and gden (kept in a scratch row per
-//     token), and dq;
+//   segment sums: phi(K)^T V and colsum phi(K) of every segment but the last,
+//     each segment in parts with a CTA each;
+//   pass 1 (chunks in order from S0 plus the earlier segments' part sums):
+//     the state S, z; per chunk the masked scores A = tril(phi(Q) phi(K)^T),
+//     the denominators, gnum and gden, and dq.  The outputs themselves are
+//     never formed: with Y = dO S_prev^T and C = dO V^T,
+//     dO_t . o_t = (phi(q_t) . Y_t + sum_j A_tj C_tj) / den_t, and Y_t / den_t
+//     is dq's state term.  gnum, gden, A and the score gradients
+//     Bm = tril(C / den + gden) go to scratch for pass 2;
 //   gradient sums: phi(Q)^T gnum and phi(Q)^T gden of every segment but the
-//     first;
-//   pass 2 (chunks in reverse from dS plus the later segments' sums): U, u in
-//     place of S, z; per chunk dk and dv from the carried U, u and the
-//     chunk's own masked terms; the first segment's final U, u are the
-//     initial state's gradient.
+//     first, in parts;
+//   pass 2 (chunks in reverse from dS plus the later segments' part sums):
+//     U, u in place of S, z; per chunk dk and dv from the carried U, u and
+//     pass 1's A and Bm; the first segment's final U, u are the initial
+//     state's gradient.
 // Every product is a small matrix product over shared-memory operands: the
 // 256 threads form a 16 x 16 grid and thread (ty, tx) accumulates the rows
-// ty + 16 r and columns tx + 16 c of the result in registers, loading each
-// operand once per row or column it serves.  Rows of phi(Q), phi(K), V and S
-// are padded by one float so that lanes walking consecutive rows hit
-// distinct banks.
+// ty + 16 r (or, where an operand is triangular, the rows 4 ty .. 4 ty + 3,
+// so that its k loop stops at the diagonal) and the columns tx + 16 c of the
+// result in registers.  Rows of phi(Q), phi(K), V and S are padded by one
+// float so that lanes walking consecutive rows hit distinct banks.
 #include <algorithm>
 
 #include "common.cuh"
@@ -219,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1) causal_backward_kernel(const __gr
   auto bKt = [&](int i, int j) { return Ks[j * KP + i]; };
   auto bS = [&](int i, int c) { return S[i * VP + c]; };
   auto bSt = [&](int c, int i) { return S[i * VP + c]; };
-  auto aA = [&](int t, int j) { return A[t * AP + j]; };
   auto bV = [&](int j, int c) { return Vs[j * VP + c]; };
   auto bVt = [&](int c, int j) { return Vs[j * VP + c]; };
   auto aG = [&](int t, int c) { return Gs[t * DV + c]; };
