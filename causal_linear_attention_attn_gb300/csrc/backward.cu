@@ -622,7 +622,9 @@ cudaError_t launch_causal_backward(const BackwardProblem &b) {
   // state and of the gradients (every block starts 16-byte aligned)
   const size_t sum_f = (size_t)p.dk * p.dv + p.dk;
   const size_t ab_f = (size_t)p.BH * nch * kT * kT;
-  const size_t g_f = 2 * ab_f + (size_t)p.BH * p.N * (p.dv + 1), seg_f = (size_t)p.BH * nseg * nsub * sum_f;
+  // (with one segment no part sums exist, and the passes read none)
+  const size_t g_f = 2 * ab_f + (size_t)p.BH * p.N * (p.dv + 1);
+  const size_t seg_f = nseg > 1 ? (size_t)p.BH * nseg * nsub * sum_f : 0;
   float *G = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&G), std::max<size_t>(sizeof(float) * (g_f + 2 * seg_f), 16),
                                   p.stream);

@@ -252,9 +252,13 @@ LA_API la_status la_retention_with_state(const void *q, const void *k, const voi
  * dS, dz (nullable; NULL = zero): the gradient of the forward's final state.
  * dq, dk: [B,H,N,d_k], dv: [B,H,N,d_v] float32, written.  dS0: [B,H,d_k,d_v],
  * dz0: [B,H,d_k] float32 (nullable), written with the initial state's gradient.
- * The forward output is recomputed, not read.  Allocates stream-ordered
- * scratch of B*H*N*(d_v+1) floats on `stream`.  Errors as la_causal; every
- * non-NULL pointer must be 16-byte aligned.  B*H == 0 is a no-op.
+ * The forward output is neither read nor formed: dO_t . o_t comes from the
+ * state read dO S^T and the chunk's scores.  Allocates stream-ordered scratch
+ * on `stream`: B*H*(N*(d_v+1) + 2*64*64*ceil(N/64)) floats (gnum, gden, and
+ * each 64-token chunk's masked scores and score gradients), plus, when heads
+ * are cut into segments, at most 4 * (SM count) * (d_k*d_v + d_k) floats of
+ * segment part sums.  Errors as la_causal; every non-NULL pointer must be
+ * 16-byte aligned.  B*H == 0 is a no-op.
  */
 LA_API la_status la_causal_backward(const void *q, const void *k, const void *v, const float *dout,
                                     const float *S0, const float *z0, const float *dS, const float *dz,
