@@ -21,7 +21,6 @@ import argparse
 import dataclasses
 import itertools
 import json
-import math
 import os
 import statistics
 import subprocess
