@@ -230,6 +230,19 @@ def test_weighted_average_properties():
     assert np.all(out_e < 3.25) and np.all(out_e > 0)
 
 
+def test_normalizer_dot_query_is_the_sum_of_scores():
+    # "Linear Attention: Accumulating KV in a Fixed-Size State", "Divide by the sum of scores",
+    # Figure 6: q's dot with the normalizer z is the sum of its similarity scores with every key
+    # read so far
+    q, k, v = _rand(5, 2, 30, 6, 3)
+    _, S, z = oracle.global_(q, k, v)
+    pq, pk = _phi_lib(q), _phi_lib(k)
+    for h in range(2):
+        np.testing.assert_allclose(pq[h] @ z[h], (pq[h] @ pk[h].T).sum(1), rtol=1e-12)
+        # and S is the sum of the outer products phi(k_j) v_j^T
+        np.testing.assert_allclose(S[h], sum(np.outer(pk[h, j], v[h, j]) for j in range(30)), rtol=1e-12)
+
+
 def test_duplicating_every_pair_leaves_global_read_unchanged():
     q, k, v = _rand(3, 1, 20, 5, 3)
     out, _, _ = oracle.global_(q, k, v, eps=0.0)
