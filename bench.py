@@ -10,6 +10,10 @@ recurrent decode step) are timed in the same run and reported under
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+``--gpus N`` without a launcher starts N ranks itself through
+torch.distributed.run (one process per GPU); under a launcher, N must match
+WORLD_SIZE.
+
 ``--impl reference`` times the fp64 CPU oracle (token-serial recurrence) on
 the host cores instead, on a bounded sample of the same workload.
 Multi-GPU (torchrun): every rank runs its own seeded batch (weak scaling,
@@ -66,6 +70,25 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def launch_plan(gpus: int, env, argv):
+    """How `bench.py --gpus N` runs: None to run in this process, else the command
+    that starts N ranks (one process per GPU, as the driver's torchrun does).
+    Under a launcher WORLD_SIZE must equal --gpus."""
+    if "WORLD_SIZE" in env:
+        world = int(env["WORLD_SIZE"])
+        if world != gpus:
+            raise SystemExit(f"bench.py: --gpus {gpus} but the launcher started {world} ranks")
+        return None
+    if gpus <= 1:
+        return None
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={gpus}",
+            "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *argv]
 
 
 def rank_workload(w: inputs.Workload, rank: int) -> inputs.Workload:
@@ -130,7 +153,7 @@ class ClockSampler:
     # NVML clocks-event reason bits
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown"}
-    PERIOD_S = 0.005
+    PERIOD_S = 0.002
 
     def __init__(self, index: int):
         self.index, self.samples, self.proc, self.nvml, self.source = index, [], None, None, None
@@ -215,13 +238,23 @@ class ClockSampler:
             self.nvml[1].nvmlShutdown()
 
     def summary(self, t0: float, t1: float):
+        """Clock record of the timed window [t0, t1].  A window shorter than the
+        sampling period can hold no sample; then the samples within 20 ms of it
+        are used (the GPU is busy with the same kernels just before and after)
+        and the record says so."""
         rows = [r for r in self.samples if t0 <= r[0] <= t1]
+        widened = not rows
+        if widened:
+            rows = [r for r in self.samples if t0 - 0.02 <= r[0] <= t1 + 0.02]
         if not rows:
             return None
         reasons = sorted({n for r in rows for n in r[3]})
-        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": self.max_mhz,
-                "power_w_max": round(max(r[2] for r in rows), 1), "samples": len(rows), "reasons": reasons,
-                "source": self.source}
+        out = {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": self.max_mhz,
+               "power_w_max": round(max(r[2] for r in rows), 1), "samples": len(rows), "reasons": reasons,
+               "source": self.source}
+        if widened:
+            out["window"] = "timed region +-20 ms (shorter than the sampling period)"
+        return out
 
 
 # --- timing helpers ---------------------------------------------------------------
@@ -581,6 +614,81 @@ def decode_workload(args):
     return dataclasses.replace(w, B=args.decode_batch) if args.decode_batch else w
 
 
+def compact(res: dict) -> dict:
+    """The figures of one form that the bench line carries: step time, rate, step
+    roofline fraction, and the dominant kernel's name, live time and fraction."""
+    rl, step = res["roofline"], res["step_roofline"]
+    c = {"ms": round(res.get("ms_per_call", res.get("us_per_step", 0.0) / 1e3), 5)}
+    if "tokens_per_s" in res:
+        c["tokens_per_s"] = float(f"{res['tokens_per_s']:.4g}")
+    if "gbs" in res:
+        c["gbs"] = res["gbs"]
+    c["step_frac"] = step["frac"]
+    c["kernel"] = rl["kernel"]
+    c["kernel_ms"] = rl["ms_per_launch"]
+    c["kernel_frac"] = rl["frac"]
+    if rl.get("traffic"):
+        c["traffic"] = rl["traffic"]
+    if "alu_roofline" in res:
+        c["alu_frac"] = res["alu_roofline"]["frac"]
+    if "tensor_roofline" in res:
+        c["tensor_frac"] = res["tensor_roofline"]["frac"]
+    c["launches"] = res["gpu_launches"]
+    clk = res.get("clocks") or {}
+    c["sm_mhz"] = clk.get("sm_mhz")
+    if clk.get("reasons"):
+        c["clock_reasons"] = clk["reasons"]
+    return c
+
+
+def carry_study(args):
+    """Times the causal prefill with each head carried by one CTA (G = 1) and cut
+    into G segments (the first pass's pieces start each segment), G as forced by
+    la_diag_force_segments, against the planner's choice (G = 0), on the causal
+    workloads.  Prints one JSON line with the step times."""
+    torch.cuda.set_device(0)
+    from causal_linear_attention_attn_gb300 import linattn as L
+
+    hbm, src = peaks()
+    stream = torch.cuda.current_stream()
+    rows = {}
+    for name in ("causal_bf16", "causal_bf16_long"):
+        w = inputs.WORKLOADS[name]
+        for G in (0, 1, 2, 4, 8, 16):
+            if name == "causal_bf16_long" and G in (2, 4):
+                continue
+            L.diag_force_segments(G)
+            try:
+                r, _ = run_seq_form(L, w, max(3, args.steps // (10 if name == "causal_bf16_long" else 1)),
+                                    args.warmup, 1, stream, hbm, src)
+            finally:
+                L.diag_force_segments(0)
+            rows[f"{name} G={G or 'auto'}"] = {"ms": round(r["ms_per_call"], 4),
+                                               "step_frac": r["step_roofline"]["frac"],
+                                               "kernels": {k: round(v["ms_per_launch"], 4)
+                                                           for k, v in r["kernels"].items()}}
+            torch.cuda.empty_cache()
+    print(json.dumps({"carry_study": rows}))
+
+
+def dry_run(args):
+    """The multi-rank plumbing without a GPU (gloo): barrier, per-rank work, max over
+    ranks and the whole-job value, printed by rank 0 in the bench line's shape."""
+    world, rank, _ = dist_env()
+    init_dist(world, "gloo")
+    barrier(world)
+    t = time.perf_counter()
+    time.sleep(0.05 * (rank + 1))  # rank r "steps" for 50 (r + 1) ms
+    ms = max_over_ranks((time.perf_counter() - t) * 1e3, world)
+    barrier(world)
+    if rank == 0:
+        units = 1000  # per rank (weak scaling)
+        print(json.dumps({"metric": METRIC, "dry_run": True, "n_gpus": world, "ms_per_step": ms,
+                          "value": world * units / (ms * 1e-3), "scaling": "weak"}))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main_ours(args):
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -596,7 +704,7 @@ def main_ours(args):
         forms = {}
         extras = [] if args.no_extras else [f for f in args.forms.split(",") if f]
         if not args.no_extras:
-            for name in ("global_bf16", "causal_bf16_long"):
+            for name in ("causal_bf16_long", "global_bf16"):
                 if name == args.workload or name not in extras:
                     continue
                 wx = rank_workload(inputs.WORKLOADS[name], rank)
@@ -650,10 +758,15 @@ def main_ours(args):
                    "inputs": "q,k ~ N(0,1)/sqrt(128), v ~ N(0,1), bf16; out/S/z fp32",
                    "l2": "inputs (402.7 MB) larger than L2 (129 MB); no flush needed",
                    "parallelism": f"replicas x{world} (heads independent)"},
-        "roofline": head["roofline"], "step_roofline": head["step_roofline"], "kernels": head["kernels"],
+        "roofline": head["roofline"], "step_roofline": head["step_roofline"],
         "gpu_launches": head["gpu_launches"], "e2e": e2e, "clocks": clocks,
-        "cpu_baseline": cpu, "forms": forms,
+        "cpu_baseline": cpu,
+        # every other form, compact and last on the line (long-context causal and global first)
+        "forms": {name: compact(r) for name, r in forms.items()},
     }
+    if args.detail:
+        with open(args.detail, "w") as f:
+            json.dump(dict(line, kernels=head["kernels"], forms=forms), f, indent=1)
     print(json.dumps(line))
 
 
@@ -696,6 +809,10 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-groups", type=int, default=4, help="head groups the end-to-end leg pipelines over")
     ap.add_argument("--ref-step-s", type=float, default=10.0, help="max CPU seconds per reference step")
+    ap.add_argument("--detail", default="", help="also write every form's full record (kernel tables) to this file")
+    ap.add_argument("--dry-run", action="store_true", help="multi-rank plumbing only, on CPU (gloo); no GPU work")
+    ap.add_argument("--carry-study", action="store_true",
+                    help="time the causal prefill at forced segment counts (one JSON line; not the bench line)")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     return a
@@ -703,7 +820,14 @@ def parse(argv=None):
 
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    cmd = launch_plan(a.gpus, os.environ, sys.argv[1:])
+    if cmd is not None:  # --gpus N without a launcher: start N ranks like the driver's torchrun
+        sys.exit(subprocess.call(cmd))
+    if a.dry_run:
+        dry_run(a)
+    elif a.carry_study:
+        carry_study(a)
+    elif a.impl == "reference":
         main_reference(a)
     else:
         main_ours(a)

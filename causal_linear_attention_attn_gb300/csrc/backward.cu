@@ -619,11 +619,12 @@ cudaError_t launch_causal_backward(const BackwardProblem &b) {
   const long sub_chunks = (seg_chunks + nsub - 1) / nsub;
   nsub = (seg_chunks + sub_chunks - 1) / sub_chunks;
   // scratch: A and Bm of every chunk, gnum and gden of every token, then the part sums of the
-  // state and of the gradients (every block starts 16-byte aligned)
+  // state and of the gradients; each block starts on a 256-byte boundary (g_f is rounded up
+  // to 64 floats, and every other block size is a multiple of 32 floats)
   const size_t sum_f = (size_t)p.dk * p.dv + p.dk;
   const size_t ab_f = (size_t)p.BH * nch * kT * kT;
   // (with one segment no part sums exist, and the passes read none)
-  const size_t g_f = 2 * ab_f + (size_t)p.BH * p.N * (p.dv + 1);
+  const size_t g_f = (2 * ab_f + (size_t)p.BH * p.N * (p.dv + 1) + 63) / 64 * 64;
   const size_t seg_f = nseg > 1 ? (size_t)p.BH * nseg * nsub * sum_f : 0;
   float *G = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&G), std::max<size_t>(sizeof(float) * (g_f + 2 * seg_f), 16),

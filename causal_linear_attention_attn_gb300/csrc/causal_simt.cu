@@ -281,12 +281,8 @@ __global__ void __launch_bounds__(kHeadThreads)
 
 template <typename Tin, int DK, int DV>
 cudaError_t launch_head_t(const Problem &p, int ne, const float *S0, const float *z0, bool pdl) {
-  static std::once_flag once;
-  static cudaError_t attr;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(causal_exact_head_kernel<Tin, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)HeadSmem<DK, DV>::Bytes);
-  });
+  const cudaError_t attr =
+      ensure_smem_optin((const void *)causal_exact_head_kernel<Tin, DK, DV>, (int)HeadSmem<DK, DV>::Bytes);
   if (attr != cudaSuccess) return attr;
   LaunchTimer timer(kKExactHead, p.stream);
   cudaLaunchConfig_t cfg = {};

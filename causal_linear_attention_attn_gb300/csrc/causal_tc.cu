@@ -34,6 +34,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -41,6 +42,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "per_device.h"
 #include "tc_ptx.cuh"
 
 namespace la {
@@ -123,6 +125,11 @@ struct TcParams {
   // retention (decayed state, no denominator): log2 of the decay of head h % ret_H
   int ret_H;
   float log2g[kMaxRetentionHeads];
+  // how long an mbarrier wait may take before the CTA gives up (kWaitNs unless a
+  // test armed la_test_inject_missing_load), and the chunk whose key load CTA
+  // (0, 0) leaves out on such a test launch (-1: none)
+  unsigned long long wait_ns;
+  int skip_k_chunk;
 };
 
 __device__ __forceinline__ float dot8(uint4 y, const float *z) {
@@ -357,12 +364,15 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       prefetch_tmap(&p.tk);
       prefetch_tmap(&p.tv);
       int issued_q = 0, issued_k = 0, issued_v = 0;
+      // a test launch (la_test_inject_missing_load) leaves out one key load of CTA (0, 0): the
+      // consumers' bounded waits then run out, and the CTA drains and exits with the timeout set
+      const int skip_k = blockIdx.x == 0 && blockIdx.y == 0 ? p.skip_k_chunk : -1;
       // Q of chunk c: stage c % 2, or (retention) always slot 0, after the previous chunk's state update
       auto load_q = [&](int c, int tok) -> bool {
         const int qs = kQ1 ? 0 : c % kStages;
         if (kQ1 ? c >= 1 : c >= kStages) {
           const uint32_t ph = kQ1 ? (uint32_t)(c - 1) & 1 : (uint32_t)(c / kStages - 1) & 1;
-          if (!mbar_wait(&q_empty[qs], ph, abort_word, status)) return false;
+          if (!mbar_wait(&q_empty[qs], ph, abort_word, status, p.wait_ns)) return false;
         }
         mbar_arrive_expect_tx(&full_q[qs], kTile);
         tma_load_3d(sm + Lay::Q + qs * kTile, &p.tq, &full_q[qs], 0, tok, bh);
@@ -375,12 +385,14 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         const uint32_t u = c / kStages;
         const int tok = (int)(t_begin + (long)c * kC);
         if (!kRet && !load_q(c, tok)) break;
-        if (c >= kStages && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_word, status)) break;
-        mbar_arrive_expect_tx(&full_k[s], kTile);
-        tma_load_3d(sm + Lay::K + s * kTile, &p.tk, &full_k[s], 0, tok, bh);
-        tma_load_3d(sm + Lay::K + s * kTile + kBlk, &p.tk, &full_k[s], 64, tok, bh);
+        if (c >= kStages && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_word, status, p.wait_ns)) break;
+        if (c != skip_k) {
+          mbar_arrive_expect_tx(&full_k[s], kTile);
+          tma_load_3d(sm + Lay::K + s * kTile, &p.tk, &full_k[s], 0, tok, bh);
+          tma_load_3d(sm + Lay::K + s * kTile + kBlk, &p.tk, &full_k[s], 64, tok, bh);
+        }
         issued_k = c + 1;
-        if (c >= kStages && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_word, status)) break;
+        if (c >= kStages && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_word, status, p.wait_ns)) break;
         mbar_arrive_expect_tx(&full_v[s], kTile);
         tma_load_3d(sm + Lay::V + s * kTile, &p.tv, &full_v[s], 0, tok, bh);
         tma_load_3d(sm + Lay::V + s * kTile + kBlk, &p.tv, &full_v[s], 64, tok, bh);
@@ -391,7 +403,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       for (int c = max(0, issued_q - (kQ1 ? 1 : kStages)); c < issued_q; ++c)
         wait_drain(&full_q[kQ1 ? 0 : c % kStages], kQ1 ? (uint32_t)c & 1 : (uint32_t)(c / kStages) & 1, status);
       for (int c = max(0, issued_k - kStages); c < issued_k; ++c)
-        wait_drain(&full_k[c % kStages], (c / kStages) & 1, status);
+        if (c != skip_k) wait_drain(&full_k[c % kStages], (c / kStages) & 1, status);
       for (int c = max(0, issued_v - kStages); c < issued_v; ++c)
         wait_drain(&full_v[c % kStages], (c / kStages) & 1, status);
     }
@@ -408,22 +420,22 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
         const uint32_t u = c / kStages;
-        if (!mbar_wait(&phi_done[s], u & 1, abort_word, status)) break;
-        if (!mbar_wait(&full_v[s], u & 1, abort_word, status)) break;
+        if (!mbar_wait(&phi_done[s], u & 1, abort_word, status, p.wait_ns)) break;
+        if (!mbar_wait(&full_v[s], u & 1, abort_word, status, p.wait_ns)) break;
         // retention: the keys reach Q K^T as loaded (no in-place pass before it)
-        if (kRet && !mbar_wait(&full_k[s], u & 1, abort_word, status)) break;
+        if (kRet && !mbar_wait(&full_k[s], u & 1, abort_word, status, p.wait_ns)) break;
         const uint32_t k = sK + s * kTile, v = sV + s * kTile;
         const uint32_t tQ = tmem + kColQ + 64 * (c & 1);
         // the single P tile is free once the previous chunk's P V has completed
-        if (c > 0 && !mbar_wait(o_full, (c - 1) & 1, abort_word, status)) break;
+        if (c > 0 && !mbar_wait(o_full, (c - 1) & 1, abort_word, status, p.wait_ns)) break;
         tc_fence_after();
         // P = Q K^T, phi(Q) from tensor memory (8 columns per 16 features)
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tP, tQ + 8 * ks, kdesc(k, ks), iKK, ks > 0);
         mma_commit(p_full);
         // S += K^T V once the previous state has been copied out
-        if (!mbar_wait(sb_ready, c & 1, abort_word, status)) break;
-        if (kRet && !mbar_wait(k_ready, c & 1, abort_word, status)) break;  // the keys' state weights
+        if (!mbar_wait(sb_ready, c & 1, abort_word, status, p.wait_ns)) break;
+        if (kRet && !mbar_wait(k_ready, c & 1, abort_word, status, p.wait_ns)) break;  // the keys' state weights
         tc_fence_after();
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tS, mndesc(k, ks), mndesc(v, ks), iMM, 1);
@@ -433,7 +445,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
           mma_commit(&q_empty[0]);  // the Q slot may take the next chunk's Q
         }
         // O = Q bf16(S_prev) once the previous outputs have been read
-        if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status)) break;
+        if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status, p.wait_ns)) break;
         tc_fence_after();
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSb, ks), iKM, ks > 0);
@@ -444,7 +456,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         mma_commit(s_full);
         mma_commit(&qt_free[c & 1]);
         mma_commit(&k_empty[s]);
-        if (!mbar_wait(pp_ready, c & 1, abort_word, status)) break;
+        if (!mbar_wait(pp_ready, c & 1, abort_word, status, p.wait_ns)) break;
         tc_fence_after();
         // O += P_hi V + P_lo V, P read from tensor memory: for keys [16ks, 16ks+16)
         // columns 16ks..16ks+7 hold P_hi and 16ks+8..16ks+15 hold P_lo
@@ -485,10 +497,10 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       const uint32_t u = c / kStages;
       const int tv = (int)min((long)kC, t_end - (t_begin + (long)c * kC));
       uint8_t *Kt = sm + Lay::K + s * kTile;
-      bool ok = mbar_wait(&full_k[s], u & 1, abort_word, status);
-      ok = ok && mbar_wait(&full_q[kQ1 ? 0 : s], kQ1 ? (uint32_t)c & 1 : u & 1, abort_word, status);
+      bool ok = mbar_wait(&full_k[s], u & 1, abort_word, status, p.wait_ns);
+      ok = ok && mbar_wait(&full_q[kQ1 ? 0 : s], kQ1 ? (uint32_t)c & 1 : u & 1, abort_word, status, p.wait_ns);
       // this chunk's phi(Q) buffer is free once Q K^T and Q S of the chunk two back have completed
-      if (ok && c >= 2) ok = mbar_wait(&qt_free[c & 1], ((c >> 1) - 1) & 1, abort_word, status);
+      if (ok && c >= 2) ok = mbar_wait(&qt_free[c & 1], ((c >> 1) - 1) & 1, abort_word, status, p.wait_ns);
       if (bar_or(kBarPhi, kPhiThreads, !ok)) break;
       {
         // phi(Q) half row -> packed bf16 pairs -> tensor memory; the partial phi(q).z_prev
@@ -554,7 +566,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       tc_fence_before();
       mbar_arrive(&phi_done[s]);
       if (kRet) {
-        const bool okp = mbar_wait(p_full, c & 1, abort_word, status);  // Q K^T has read the raw keys
+        const bool okp = mbar_wait(p_full, c & 1, abort_word, status, p.wait_ns);  // Q K^T has read the raw keys
         if (bar_or(kBarPhi, kPhiThreads, !okp)) break;
         transform_k(exp2f((float)(tv - 1 - row) * lg));
         fence_async_smem();
@@ -622,8 +634,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         const long tok = t_begin + (long)c * kC;
         const int tv = (int)min((long)kC, t_end - tok);
         const uint32_t tP = tl + kColP;
-        bool w = mbar_wait(&phi_done[s], u & 1, abort_word, status) &&
-                 mbar_wait(p_full, c & 1, abort_word, status);
+        bool w = mbar_wait(&phi_done[s], u & 1, abort_word, status, p.wait_ns) &&
+                 mbar_wait(p_full, c & 1, abort_word, status, p.wait_ns);
         if (bar_or(kBarEpi, 128, !w)) {
           ok = false;
           break;
@@ -679,7 +691,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         mbar_arrive(pp_ready);
         mbar_arrive(&den_ready[c & 1]);
         // bf16 copy of the updated state for the next chunk's cross read
-        w = mbar_wait(s_full, c & 1, abort_word, status);
+        w = mbar_wait(s_full, c & 1, abort_word, status, p.wait_ns);
         if (bar_or(kBarEpi, 128, !w)) {
           ok = false;
           break;
@@ -728,8 +740,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % kStages;
       const long tok = t_begin + (long)c * kC;
-      bool w = mbar_wait(o_full, c & 1, abort_word, status) &&
-               mbar_wait(&den_ready[c & 1], (c >> 1) & 1, abort_word, status);
+      bool w = mbar_wait(o_full, c & 1, abort_word, status, p.wait_ns) &&
+               mbar_wait(&den_ready[c & 1], (c >> 1) & 1, abort_word, status, p.wait_ns);
       if (bar_or(kBarOut, 128, !w)) break;
       tc_fence_after();
       // normalizer, or (retention) the row's decay gamma^(T+1-C)
@@ -828,15 +840,23 @@ bool make_out_map(CUtensorMap *m, void *base, long BH, long N, uint32_t rows) {
          CUDA_SUCCESS;
 }
 
+// One armed test injection (la_test_inject_missing_load): the chunk whose key
+// load is left out and the wait limit in microseconds, packed as
+// (chunk << 32) | wait_us; 0 when nothing is armed.  The next launch of the
+// tensor-core causal pass takes it.
+std::atomic<unsigned long long> g_inject{0};
+
 template <int kMode>
-cudaError_t launch_kernel(const TcParams &tp, dim3 grid, cudaStream_t stream, bool pdl) {
+cudaError_t launch_kernel(const TcParams &tp_in, dim3 grid, cudaStream_t stream, bool pdl) {
   constexpr bool kRet = kMode == kModeRetention;
-  static std::once_flag once;
-  static cudaError_t attr_err;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(causal_tc_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)Layout::Alloc);
-  });
+  TcParams tp = tp_in;
+  tp.wait_ns = kWaitNs;
+  tp.skip_k_chunk = -1;
+  if (const unsigned long long inj = g_inject.exchange(0)) {
+    tp.skip_k_chunk = (int)(inj >> 32);
+    tp.wait_ns = (inj & 0xffffffffull) * 1000ull;
+  }
+  const cudaError_t attr_err = ensure_smem_optin((const void *)causal_tc_kernel<kMode>, (int)Layout::Alloc);
   if (attr_err != cudaSuccess) return attr_err;
   LaunchTimer timer(kRet ? kKRetentionMain : kKCausalMain, stream);
   // pdl: may start while the previous kernel of the stream (the first pass) still runs
@@ -912,11 +932,16 @@ struct Partition {
   long pieces() const { return pieces_per_cta * ctas; }
 };
 
-Partition plan_partition(const Problem &p, long sms, long max_pieces) {
+// Segments per head forced by la_diag_force_segments (0: the planner's choice).
+std::atomic<int> g_force_segments{0};
+
+Partition plan_partition(const Problem &p, long sms, long max_pieces, bool allow_force = false) {
   Partition t;
   const long chunks = (p.N + kC - 1) / kC;
   // segments per head: enough CTAs to cover the SMs once, at least 4 chunks each
   t.G = std::max(1L, std::min(sms / p.BH, chunks / 4));
+  const int forced = allow_force ? g_force_segments.load() : 0;
+  if (forced > 0) t.G = std::min<long>(forced, chunks);
   t.seg_chunks = (chunks + t.G - 1) / t.G;
   t.G = (chunks + t.seg_chunks - 1) / t.seg_chunks;
   if (t.G > 1) {
@@ -959,7 +984,7 @@ cudaError_t launch_tc(const Problem &p, bool from_state, int mode, const float *
   const bool ret = mode == kModeRetention;
   const DeviceInfo &di = device_info(-1);
   const long sms = std::max(1, di.sm_count);
-  const Partition t = plan_partition(p, sms, 2 * sms);
+  const Partition t = plan_partition(p, sms, 2 * sms, true);
   if (t.G > 1 && t.ctas == 0) return cudaErrorInvalidValue;  // not reached: BH * G <= SMs
   const long nparts = t.pieces();
   const size_t state_f = (size_t)kD * kD + kD;
@@ -1018,6 +1043,12 @@ cudaError_t launch_tc(const Problem &p, bool from_state, int mode, const float *
   return e;
 }
 
+void force_segments(int G) { g_force_segments.store(G); }
+
+void arm_missing_load(int chunk, unsigned int wait_us) {
+  g_inject.store(((unsigned long long)(unsigned)chunk << 32) | wait_us);
+}
+
 cudaError_t launch_causal_tc(const Problem &p, bool from_state) {
   return launch_tc(p, from_state, kModeElu, nullptr, 0);
 }
@@ -1049,20 +1080,18 @@ struct NoAllocScratch {
 };
 
 // Device address of the fixed scratch array, looked up once per device (with
-// that device current) on the first call that needs it.
-NoAllocScratch &noalloc_scratch(int dev) {
-  constexpr int kMaxDev = 64;
-  static NoAllocScratch slots[kMaxDev];
-  static std::once_flag once[kMaxDev];
-  if (dev < 0 || dev >= kMaxDev) dev = 0;
-  std::call_once(once[dev], [dev] {
+// that device current, which the caller guarantees) on the first call that
+// needs it.
+NoAllocScratch noalloc_scratch(int dev) {
+  static PerDeviceCache<int, NoAllocScratch> cache;
+  return cache.get(dev, 0, [] {
+    NoAllocScratch s;
     void *ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    slots[dev].err = e;
-    if (e == cudaSuccess) slots[dev].ptr = static_cast<float *>(ptr);
+    s.err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (s.err == cudaSuccess) s.ptr = static_cast<float *>(ptr);
     else cudaGetLastError();
+    return s;
   });
-  return slots[dev];
 }
 }  // namespace
 
@@ -1083,7 +1112,7 @@ cudaError_t launch_causal_tc_noalloc(const Problem &p, int dev, bool *too_large)
   const size_t need = (size_t)nparts * state_f;
   float *part_S = nullptr, *part_z = nullptr;
   if (need) {
-    NoAllocScratch &sc = noalloc_scratch(dev);
+    const NoAllocScratch sc = noalloc_scratch(dev);
     if (sc.err != cudaSuccess) return sc.err;
     part_S = sc.ptr;
     part_z = part_S + (size_t)nparts * kD * kD;

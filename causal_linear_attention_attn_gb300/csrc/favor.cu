@@ -261,11 +261,7 @@ bool make_map2(CUtensorMap *map, const void *base, long rows, int cols) {
 template <int D>
 cudaError_t launch_tc(const void *X, const void *W, void *out, long rows, cudaStream_t stream) {
   using Lay = FavLayout<D>;
-  static std::once_flag once;
-  static cudaError_t attr;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(favor_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::Bytes);
-  });
+  const cudaError_t attr = ensure_smem_optin((const void *)favor_tc_kernel<D>, (int)Lay::Bytes);
   if (attr != cudaSuccess) return attr;
   FavorParams p;
   if (!make_map2(&p.tx, X, rows, D) || !make_map2(&p.tw, W, kFavM, D) || !make_map2(&p.to, out, rows, kFavM))

@@ -688,19 +688,9 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t elem, const void 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename F>
-cudaError_t set_smem_once(F *kernel, uint32_t bytes, std::once_flag &once, cudaError_t &err) {
-  std::call_once(once, [&] {
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  });
-  return err;
-}
-
 template <int D, int kMode = kModeElu>
 cudaError_t build_smem() {
-  static std::once_flag once;
-  static cudaError_t err;
-  return set_smem_once(global_build_tc<D, kMode>, BuildLayout<D, kMode == kModeRetention>::Bytes, once, err);
+  return ensure_smem_optin((const void *)global_build_tc<D, kMode>, (int)BuildLayout<D, kMode == kModeRetention>::Bytes);
 }
 
 template <int D>
@@ -729,9 +719,7 @@ cudaError_t launch_t(const Problem &p) {
 
   cudaError_t e = build_smem<D>();
   if (e != cudaSuccess) return e;
-  static std::once_flag once_r;
-  static cudaError_t err_r;
-  e = set_smem_once(global_read_tc<D>, ReadLayout<D>::Bytes, once_r, err_r);
+  e = ensure_smem_optin((const void *)global_read_tc<D>, (int)ReadLayout<D>::Bytes);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};

@@ -97,6 +97,14 @@ cudaError_t launch_range_states(const Problem &p, long range_tokens, int ranges_
                                 float *piece_S, float *piece_z, int kernel_id, const float *log2g = nullptr,
                                 int ret_H = 0, int mode = kModeElu);
 
+// Testing: the next launch of the tensor-core causal pass leaves out the key
+// load of `chunk` in its first CTA and gives every mbarrier wait wait_us
+// microseconds (see la_test_inject_missing_load).
+void arm_missing_load(int chunk, unsigned int wait_us);
+
+// Diagnostics: segments per head of the tensor-core causal passes (0: planner).
+void force_segments(int G);
+
 // Read and clear the device status word (bounded-wait timeouts).
 cudaError_t read_and_clear_device_status(unsigned int *value);
 
@@ -143,12 +151,18 @@ class LaunchTimer {
   cudaEvent_t start_ = nullptr;
 };
 
-// Per-device attributes, filled once per device.
+// Opt a kernel in to `bytes` of dynamic shared memory on the current device.
+// The attribute lives in each device's context, so it is set once per
+// (device, kernel, size) and the result is remembered for that device only.
+cudaError_t ensure_smem_optin(const void *kernel, int bytes);
+
+// Per-device attributes, read once per device (dev < 0: the current device;
+// all zero if there is none).
 struct DeviceInfo {
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
   int max_smem_optin = 0;
 };
-const DeviceInfo &device_info(int dev);
+DeviceInfo device_info(int dev);
 
 }  // namespace la

@@ -12,13 +12,11 @@
 
 #include "internal.h"
 #include "linattn.h"
+#include "per_device.h"
 
 namespace la {
 
 namespace {
-constexpr int kMaxDevices = 64;
-DeviceInfo g_info[kMaxDevices];
-std::once_flag g_once[kMaxDevices];
 
 std::atomic<unsigned long long> g_launches{0};
 
@@ -129,17 +127,33 @@ void LaunchTimer::done(cudaError_t launch_error) {
   start_ = nullptr;
 }
 
-const DeviceInfo &device_info(int dev) {
-  if (dev < 0) cudaGetDevice(&dev);
-  if (dev < 0 || dev >= kMaxDevices) dev = 0;
-  std::call_once(g_once[dev], [dev] {
-    DeviceInfo &i = g_info[dev];
+cudaError_t ensure_smem_optin(const void *kernel, int bytes) {
+  static PerDeviceCache<std::pair<const void *, int>, cudaError_t> cache;
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return cache.get(dev, std::make_pair(kernel, bytes), [&] {
+    const cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (r != cudaSuccess) cudaGetLastError();
+    return r;
+  });
+}
+
+DeviceInfo device_info(int dev) {
+  static PerDeviceCache<int, DeviceInfo> cache;
+  if (dev < 0 && cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DeviceInfo{};
+  }
+  return cache.get(dev, 0, [dev] {
+    DeviceInfo i;
     cudaDeviceGetAttribute(&i.sm_count, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&i.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&i.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&i.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaGetLastError();
+    return i;
   });
-  return g_info[dev];
 }
 
 }  // namespace la
@@ -171,6 +185,18 @@ la_status la_device_status(void *stream) {
   v |= vg | vf;
   if (v & 1u) return LA_ERR_TIMEOUT;
   return v ? LA_ERR_LAUNCH : LA_OK;  // other bits: a kernel refused to run (e.g. misaligned shared memory)
+}
+
+la_status la_diag_force_segments(int segments) {
+  if (segments < 0 || segments > 4096) return LA_ERR_INVALID_VALUE;
+  la::force_segments(segments);
+  return LA_OK;
+}
+
+la_status la_test_inject_missing_load(int chunk, unsigned int wait_us) {
+  if (chunk < 0 || wait_us < 1 || wait_us > 1000000) return LA_ERR_INVALID_VALUE;
+  la::arm_missing_load(chunk, wait_us);
+  return LA_OK;
 }
 
 unsigned long long la_kernel_launches(void) { return la::g_launches.load(std::memory_order_relaxed); }

@@ -60,17 +60,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false if the
-// wait gave up: either it ran past kWaitNs (this thread then raises the abort
+// wait gave up: either it ran past limit_ns (this thread then raises the abort
 // word and the device status word) or another thread already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_word,
-                                          unsigned int *status) {
+                                          unsigned int *status, unsigned long long limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (;;) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_word) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) break;
+    if (globaltimer_ns() - t0 > limit_ns) break;
   }
   atomicOr((unsigned int *)abort_word, kAbortTimeout);
   if (status) atomicOr(status, kAbortTimeout);

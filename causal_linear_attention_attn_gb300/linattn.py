@@ -52,6 +52,10 @@ lib.la_last_error_detail.argtypes = []
 lib.la_last_error_detail.restype = ctypes.c_char_p
 lib.la_kernel_launches.argtypes = []
 lib.la_kernel_launches.restype = ctypes.c_ulonglong
+lib.la_diag_force_segments.argtypes = [_i]
+lib.la_diag_force_segments.restype = _i
+lib.la_test_inject_missing_load.argtypes = [_i, ctypes.c_uint]
+lib.la_test_inject_missing_load.restype = _i
 lib.la_profile_enable.argtypes = [_i]
 lib.la_profile_enable.restype = _i
 lib.la_profile_read.argtypes = [_i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
@@ -292,6 +296,21 @@ def la_causal_backward(q, k, v, dout, S0=None, z0=None, dS=None, dz=None, need_s
 def device_status(stream=None) -> int:
     """Synchronize the stream and return (and clear) the device status: 0 = OK, 6 = a bounded wait timed out."""
     return int(lib.la_device_status(_stream(stream)))
+
+
+def diag_force_segments(segments: int) -> None:
+    """Diagnostics: segments per head of the tensor-core causal passes (0: the planner's choice)."""
+    rc = lib.la_diag_force_segments(int(segments))
+    if rc != 0:
+        raise LinAttnError("la_diag_force_segments", rc)
+
+
+def test_inject_missing_load(chunk: int, wait_us: int) -> None:
+    """Testing only: the next tensor-core causal launch leaves out one key load of its
+    first CTA and gives every wait ``wait_us`` microseconds (see linattn.h)."""
+    rc = lib.la_test_inject_missing_load(int(chunk), int(wait_us))
+    if rc != 0:
+        raise LinAttnError("la_test_inject_missing_load", rc)
 
 
 def profile_enable(on: bool = True) -> None:

@@ -99,7 +99,7 @@ LA_API la_status la_global(const void *q, const void *k, const void *v, float *o
  *     out_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps),   S_{-1} = 0, z_{-1} = 0.
  * Source: "线性注意力从头到尾讲清楚" §7; "Linear Attention Math", "The
  * recurrent form"; "Linear Attention: Accumulating KV in a Fixed-Size
- * State" (add the token, then read the updated state).  Computed in
+ * State" (token t joins the state before its query reads it).  Computed in
  * chunks ("Linear Attention: From Pairwise Reads to a Recurrent State",
  * "A recurrence need not force token-serial training").
  *
@@ -136,9 +136,11 @@ LA_API la_status la_causal_with_state(const void *q, const void *k, const void *
  * most two 128x128 fp32 states per first-pass CTA, at most one CTA per SM) live here
  * in one fixed 20 MiB device array inside the library instead; every GPU
  * that loads the library keeps that array until the process exits.  It holds
- * the partial states of 158 first-pass CTAs; a problem whose first pass would
- * need more (B * H * (segments - 1) > 158) returns LA_ERR_TOO_LARGE and
- * launches nothing.  All calls share the array, so
+ * the partial states of 158 first-pass CTAs.  The planner gives the first pass
+ * at most one CTA per SM, so on a GB300 (152 SMs) every problem fits; only on
+ * a device with more than 158 SMs can a problem need more (B * H * (segments
+ * - 1) > 158), and there the call returns LA_ERR_TOO_LARGE and launches
+ * nothing.  All calls share the array, so
  * calls whose work overlaps on the GPU (different streams, or different host
  * threads on the same device) race on it and give wrong results: order them.
  * The first call on each device looks up the array's device address
@@ -314,6 +316,35 @@ LA_API la_status la_retention_decode_step(const void *q, const void *k, const vo
  */
 LA_API la_status la_device_status(void *stream);
 
+/*
+ * Diagnostics, for measuring the carry of the causal prefill: fixes how many
+ * segments each head is cut into by the tensor-core passes of la_causal,
+ * la_causal_with_state, la_causal_features and la_retention (1 = one CTA
+ * carries each head's state through all of its chunks; G > 1 = G segments
+ * whose starting states come from the first pass over the earlier ones),
+ * clamped to the number of 128-token chunks.  0 restores the planner's
+ * choice (enough segments to cover the SMs once, at least 4 chunks each).
+ * Process-wide; results are the same up to rounding for every value.
+ * la_causal_noalloc ignores it.  LA_ERR_INVALID_VALUE outside [0, 4096].
+ */
+LA_API la_status la_diag_force_segments(int segments);
+/*
+ * Testing only: exercises the bounded-wait failure path on the GPU without a
+ * fault.  Arms a one-shot injection taken by the NEXT launch of the
+ * tensor-core causal pass (la_causal, la_causal_with_state or
+ * la_causal_noalloc with bf16 inputs and d_k = d_v = 128), from any host
+ * thread: in that launch the first CTA (segment 0 of head 0) does not issue
+ * the key load of chunk `chunk` (128-token chunks of its segment), and every
+ * mbarrier wait of the launch gives up after wait_us microseconds instead of
+ * 4 s.  The waits that depend on the missing load run out; the CTA raises its
+ * abort word, drains the copies and tensor-core work already issued, frees its
+ * tensor memory and exits, and the next la_device_status returns
+ * LA_ERR_TIMEOUT.  That call's outputs are not valid; later calls are
+ * unaffected.  If the chunk does not exist in that launch nothing is left out.
+ * LA_ERR_INVALID_VALUE for chunk < 0 or wait_us outside [1, 1000000].  No
+ * counterpart in the pages: it tests this library's error reporting.
+ */
+LA_API la_status la_test_inject_missing_load(int chunk, unsigned int wait_us);
 /* Static English description of a status code (never NULL). */
 LA_API const char *la_status_string(la_status s);
 

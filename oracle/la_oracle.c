@@ -55,8 +55,9 @@ double lao_phi(double x, int kind) {
   return exp(x);
 }
 
-/* One token of the recurrence on state (S, z): add phi(k) v^T and phi(k),
- * then read the updated state with phi(q).  Writes dv outputs. */
+/* One token of the recurrence on state (S, z): phi(k) v^T and phi(k) join
+ * the state first, and phi(q) reads the state that now includes them.
+ * Writes dv outputs. */
 static void step_update_then_read(const double *q, const double *k, const double *v,
                                   double *o, double *S, double *z, int dk, int dv,
                                   double eps, int kind, double *qt, double *kt) {

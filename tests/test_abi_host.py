@@ -220,3 +220,18 @@ def test_profile_diagnostics_without_launches():
     assert L.lib.la_profile_read(len(L.KERNELS), ctypes.byref(ms), ctypes.byref(n)) == INVALID
     assert L.lib.la_profile_read(-1, ctypes.byref(ms), ctypes.byref(n)) == INVALID
     assert L.lib.la_profile_read(0, None, ctypes.byref(n)) == INVALID
+
+
+def test_fault_injection_hook_validates_its_arguments():
+    """Only invalid arguments here: a valid call would arm the one-shot injection for a
+    later GPU test in the same process."""
+    f = L.lib.la_test_inject_missing_load
+    assert f(-1, 1000) == INVALID
+    assert f(0, 0) == INVALID
+    assert f(0, 1000001) == INVALID
+
+
+def test_segment_override_validates_and_resets():
+    f = L.lib.la_diag_force_segments
+    assert f(-1) == INVALID and f(4097) == INVALID
+    assert f(0) == OK  # the planner's choice (the default)

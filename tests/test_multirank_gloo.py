@@ -4,14 +4,19 @@ The path shards by independent heads, so ranks exchange nothing on the data
 path; what crosses ranks is the barrier around the timed region and the max
 of the per-rank step times.  Each rank must draw a distinct batch.
 """
+import json
 import os
 import socket
+import subprocess
+import sys
 
+import pytest
 import torch
 import torch.multiprocessing as mp
 
 import bench
 from causal_linear_attention_attn_gb300 import inputs
+from conftest import ROOT
 
 
 def _free_port():
@@ -72,3 +77,33 @@ def test_backward_arithmetic_roofline():
     assert r["bound"] == "alu" and r["unit"] == "TFLOP/s"
     assert abs(r["achieved"] - 2.0 * 4 * 16 * 8192 * 110592 / 5e-3 / 1e12) < 0.01
     assert abs(r["frac"] - r["achieved"] / bench.FP32_PEAK_TFLOPS) < 1e-3
+
+
+def test_launch_plan_of_gpus_flag():
+    """--gpus N without a launcher starts N ranks (torch.distributed.run, one per GPU);
+    under a launcher the rank count must match."""
+    cmd = bench.launch_plan(2, {}, ["--gpus", "2", "--steps", "3"])
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=2" in cmd and "--master-addr=127.0.0.1" in cmd
+    assert cmd[-4:] == [os.path.abspath(bench.__file__), "--gpus", "2", "--steps", "3"][-4:]
+    assert bench.launch_plan(2, {"WORLD_SIZE": "2"}, []) is None
+    assert bench.launch_plan(1, {}, []) is None
+    with pytest.raises(SystemExit):
+        bench.launch_plan(4, {"WORLD_SIZE": "2"}, [])
+
+
+def test_gpus_two_runs_two_ranks_and_takes_the_slowest():
+    """`bench.py --gpus 2 --dry-run` on CPU: two gloo ranks, rank 1 the slower (100 ms
+    against 50 ms); rank 0 prints one line with n_gpus 2 and the whole-job value over
+    the max time."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--dry-run"], cwd=ROOT,
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["dry_run"]
+    assert line["ms_per_step"] >= 100.0
+    assert abs(line["value"] - 2 * 1000 / (line["ms_per_step"] * 1e-3)) < 1e-6 * line["value"]
