@@ -1,0 +1,1129 @@
+// Gradient of the causal prefill on the sm_103a tensor cores (tcgen05, TMEM).
+//
+// The forward is o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps) with the state
+// inclusive of token t ("线性注意力从头到尾讲清楚" §7; "Linear Attention Math",
+// "The recurrent form").  The pages name training through chunked matrix
+// products ("Linear Attention: From Pairwise Reads to a Recurrent State", "A
+// recurrence need not force token-serial training"; "Linear in which
+// variable?": chunk boundary states and gradients) but write no backward
+// pass; this is the derivative of the definition, in 128-token chunks.
+// Within a chunk (rows t = queries, j = keys, i = key features, c = value
+// components), with Q = phi(q), K = phi(k) and the state S_prev, z_prev
+// carried in from the earlier chunks:
+//   A    = tril(Q K^T),  C = tril(dO V^T),  Y = dO S_prev^T
+//   den  = Q z_prev + rowsum(A) + eps
+//   gden = -(rowsum(Q * Y) + rowsum(A * C)) / den^2          (= -(dO . o) / den)
+//   B'   = tril(C + den gden)                                (= den * dO-score gradient)
+//   dQ   = ((Y + B' K) / den + gden z_prev^T) * phi'(q)
+// and in reverse order, with U, u the gradient of the state carried in from
+// the later chunks (dS, dz at the end) and gnum = dO / den:
+//   dV   = K U + triu(K Q^T) gnum
+//   dK   = (V U^T + triu(V gnum^T + gden) Q + u) * phi'(k)
+//   U   += Q^T gnum,  u += Q^T gden.
+// phi = ELU + 1 gives phi'(x) = min(phi(x), 1).
+//
+// Precision.  At early tokens the query gradient is a difference of terms
+// about a thousand times larger than itself, so every operand that is not a
+// bf16 input (Q, K, dO, S_prev, B', U, the key-side scores and gnum) reaches
+// the tensor cores as a bf16 pair hi + lo (hi = bf16(x), lo = bf16(x - hi),
+// about 16 significant bits); a product of two pairs is taken as
+// hi hi + hi lo + lo hi, a pair against V as two products.  All
+// accumulation is fp32 in tensor memory; den, gden, z and u are fp32.
+//
+// Two kernels, one CTA per head (a CTA carries its head's state through all
+// chunks in order):
+//   pass 1 (chunks in order): dq, and den, gden of every token for pass 2;
+//   pass 2 (chunks in reverse), two CTA roles per head: role 0 computes dv
+//     and the initial state's dS0, role 1 dk and dz0; both carry U.
+// Operands are staged by threads from global memory (one chunk ahead in L2
+// through bulk prefetches) into 128-byte-swizzled shared tiles or straight
+// into tensor memory; one thread issues the MMAs.  Every mbarrier wait is
+// bounded: a wait that runs out raises the CTA's abort word and the device
+// status word, the CTA drains its MMAs, frees tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace la {
+
+__device__ unsigned int g_bwd_status;
+
+namespace {
+using namespace tc;
+
+constexpr int kC = 128;               // tokens per chunk
+constexpr int kD = 128;               // d_k = d_v
+constexpr uint32_t kBlk = 16384;      // [128 rows x 64] bf16, 128-byte swizzled
+constexpr uint32_t kTile = 2 * kBlk;  // [128 x 128] bf16 tile
+constexpr uint32_t kAbortMisaligned = 2u;
+
+// ---------------------------------------------------------------------------
+// Small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// phi(a), phi(b) in fp32: x + 1 above zero, e^x = 2^(x log2 e) on the MUFU unit
+// below (relative error near 2^-22, far below the 2^-17 of a bf16 pair).
+__device__ __forceinline__ float2 phi2(float a, float b) {
+  const float2 y = __fmul2_rn(make_float2(a, b), make_float2(1.4426950408889634f, 1.4426950408889634f));
+  return make_float2(a > 0.f ? a + 1.f : ex2_approx(y.x), b > 0.f ? b + 1.f : ex2_approx(y.y));
+}
+
+// Two fp32 values as a bf16 pair: hi word (a, b), lo word (a - hi_a, b - hi_b).
+__device__ __forceinline__ void split2(float a, float b, uint32_t &h, uint32_t &l) {
+  h = pack_bf16(a, b);
+  l = pack_bf16(a - lo16(h), b - hi16(h));
+}
+
+// phi of the eight bf16 inputs packed in x, as bf16 pairs (hi, lo words of
+// feature pairs); v receives hi + lo, the values the tensor cores see.
+__device__ __forceinline__ void phi_split8(uint4 x, uint32_t (&h)[4], uint32_t (&l)[4], float (&v)[8]) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = phi2(lo16(w[e]), hi16(w[e]));
+    split2(f.x, f.y, h[e], l[e]);
+    v[2 * e] = lo16(h[e]) + lo16(l[e]);
+    v[2 * e + 1] = hi16(h[e]) + hi16(l[e]);
+  }
+}
+
+// As phi_split8 without the values: the pair words of eight phi values.
+__device__ __forceinline__ void phi_pair8(uint4 x, uint4 &h, uint4 &l) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t hh[4], ll[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = phi2(lo16(w[e]), hi16(w[e]));
+    split2(f.x, f.y, hh[e], ll[e]);
+  }
+  h = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+  l = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+}
+
+// 16-byte read-only global load that the compiler keeps in program order with
+// the other inline-asm statements (so that a row is not loaded early, beside
+// another row still held in registers).
+__device__ __forceinline__ uint4 ld_row16(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// K-major operand over a [128 x 128] tile (rows of 64 K-elements per block).
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int ks) {
+  return sw128_desc(tile + (ks >> 2) * kBlk + (ks & 3) * 32, 16, 1024);
+}
+// MN-major operand over a [128 x 128] tile (rows = K index, two 64-wide blocks).
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int ks) {
+  return sw128_desc(tile + ks * 2048, kBlk, 1024);
+}
+
+// Row `row`, columns col0 .. col0 + 7 of a [128 x 128] bf16 tile.
+__device__ __forceinline__ uint4 *tile_chunk(uint8_t *tile, int row, int col0) {
+  return reinterpret_cast<uint4 *>(tile + (col0 >> 6) * kBlk + sw128_offset(row, col0 & 63));
+}
+
+// 32 fp32 values (columns col0 .. col0 + 31 of row `row`) as bf16 pairs into tiles hi, lo.
+__device__ __forceinline__ void store_row32_pair(uint8_t *hi, uint8_t *lo, int row, int col0, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split2(__uint_as_float(r[8 * q + 2 * e]), __uint_as_float(r[8 * q + 2 * e + 1]), h[e], l[e]);
+    *tile_chunk(hi, row, col0 + 8 * q) = make_uint4(h[0], h[1], h[2], h[3]);
+    *tile_chunk(lo, row, col0 + 8 * q) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// Split 32 fp32 score columns (keys 32 cb .. 32 cb + 31 of this lane's row) in
+// place into bf16 pairs for use as a tensor-memory A operand: every 16 keys
+// become 8 columns of hi pairs then 8 of lo pairs.  keep(j) selects the
+// entries kept (the others become zeros); f(j, x) transforms a kept value.
+template <typename Keep, typename F>
+__device__ __forceinline__ void split_scores32(uint32_t (&r)[32], int cb, Keep keep, F f) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    uint32_t o[16];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int j = cb * 32 + g * 16 + 2 * m;
+      const float a = keep(j) ? f(j, __uint_as_float(r[g * 16 + 2 * m])) : 0.f;
+      const float b = keep(j + 1) ? f(j + 1, __uint_as_float(r[g * 16 + 2 * m + 1])) : 0.f;
+      split2(a, b, o[m], o[8 + m]);
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) r[g * 16 + e] = o[e];
+  }
+}
+
+// Arguments of both passes (device pointers; [BH][N][128] rows, fp32 unless noted).
+struct BwdTcParams {
+  CUtensorMap tq, tk, tv;  // [BH][N][128] bf16, boxes of 64 features x 128 tokens, 128-byte swizzle
+  const __nv_bfloat16 *q, *k, *v;  // inputs
+  const float *dout;
+  const float *S0, *z0;  // initial state (nullable)
+  const float *dS, *dz;  // gradient of the final state (nullable)
+  float *dq, *dk, *dv;
+  float *dS0, *dz0;  // gradient of the initial state (nullable)
+  float *den, *gden;  // [BH][N]: written by pass 1, read by pass 2
+  long N;
+  float eps;
+};
+
+// Shared-memory layout of pass 1: seven [128 x 128] bf16 tiles (224 KB), then
+// two z buffers, the chunk's phi(q).z, barriers.
+struct P1Layout {
+  static constexpr uint32_t Khi = 0, Klo = kTile, V = 2 * kTile, Ghi = 3 * kTile, Glo = 4 * kTile, Shi = 5 * kTile,
+                            Slo = 6 * kTile;
+  static constexpr uint32_t Z = 7 * kTile;    // [2][128] z carried into the chunk
+  static constexpr uint32_t DenX = Z + 1024;  // [128] phi(q_t) . z_prev
+  static constexpr uint32_t Bars = DenX + 512;
+  static constexpr int kNumBars = 18;
+  static constexpr uint32_t Misc = Bars + kNumBars * 8;
+  static constexpr uint32_t Bytes = Misc + 16;
+};
+static_assert(P1Layout::Bytes <= 232448, "pass 1 shared memory");
+
+// TMEM columns of pass 1: S accumulator; X = A, then Y and Y + B' K; CB = C,
+// then B' as bf16 pairs; phi(Q) as bf16 pairs (hi 64 columns, lo 64).
+constexpr uint32_t kP1S = 0, kP1X = 128, kP1CB = 256, kP1Q = 384;
+
+// Warp roles of pass 1 (13 warps): 0 MMA issuer and tensor-memory owner; 1-4
+// keys (TMA, phi pairs in place), queries (phi pairs into tensor memory) and
+// copies of the state; 5-8 dO pairs (and V by TMA); 9-12 scores, key column
+// sums and dq.
+constexpr int kP1Threads = 416;
+constexpr int kP1WarpG = 5, kP1WarpE = 9;
+constexpr uint32_t kBarQK = 1, kBarG = 2, kBarE = 3;
+
+__global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_constant__ BwdTcParams p) {
+  using L = P1Layout;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(&g_bwd_status, kAbortMisaligned);
+    return;
+  }
+  uint8_t *sm = smem_raw;
+  float *zbuf = reinterpret_cast<float *>(sm + L::Z);
+  float *den_x = reinterpret_cast<float *>(sm + L::DenX);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::Bars);
+  uint64_t *q_ready = bars + 0, *k_ready = bars + 1, *g_ready = bars + 2, *s_ready = bars + 3, *ac_full = bars + 4,
+           *x_free = bars + 5, *y_full = bars + 6, *cb_ready = bars + 7, *d_full = bars + 8, *e3_done = bars + 9,
+           *drain = bars + 10, *z_full = bars + 11 /* [2] */, *z_empty = bars + 13 /* [2] */, *k_full = bars + 15,
+           *v_full = bars + 16;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::Misc);
+  volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + L::Misc + 4);
+  unsigned int *status = &g_bwd_status;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const long N = p.N;
+  const int nch = (int)((N + kC - 1) / kC);
+  const __nv_bfloat16 *qh = p.q + (long)bh * N * kD, *kh = p.k + (long)bh * N * kD, *vh = p.v + (long)bh * N * kD;
+  const float *gh = p.dout + (long)bh * N * kD;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_ready, 128);
+    mbar_init(k_ready, 128);
+    mbar_init(g_ready, 128);
+    mbar_init(s_ready, 128);
+    mbar_init(ac_full, 1);
+    mbar_init(x_free, 128);
+    mbar_init(y_full, 1);
+    mbar_init(cb_ready, 128);
+    mbar_init(d_full, 1);
+    mbar_init(e3_done, 128);
+    mbar_init(drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&z_full[b], 128);
+      mbar_init(&z_empty[b], 128);
+    }
+    mbar_init(k_full, 1);
+    mbar_init(v_full, 1);
+    *abort_word = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto wait = [&](uint64_t *bar, uint32_t parity) { return mbar_wait(bar, parity, abort_word, status); };
+
+  if (warp == 0) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t iKK = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t iKM = idesc_bf16_f32(128, 128, 0, 1);
+      constexpr uint32_t iMM = idesc_bf16_f32(128, 128, 1, 1);
+      const uint32_t sKhi = smem_u32(sm + L::Khi), sKlo = smem_u32(sm + L::Klo), sV = smem_u32(sm + L::V),
+                     sGhi = smem_u32(sm + L::Ghi), sGlo = smem_u32(sm + L::Glo), sShi = smem_u32(sm + L::Shi),
+                     sSlo = smem_u32(sm + L::Slo);
+      const uint32_t tS = tmem + kP1S, tX = tmem + kP1X, tCB = tmem + kP1CB, tQh = tmem + kP1Q,
+                     tQl = tmem + kP1Q + 64;
+      for (int c = 0; c < nch; ++c) {
+        const uint32_t ph = c & 1;
+        if (c + 1 < nch) {  // the next chunk's rows into L2
+          const long t1 = (long)(c + 1) * kC;
+          const uint32_t rows = (uint32_t)min((long)kC, N - t1);
+          prefetch_l2(qh + t1 * kD, rows * kD * 2);
+          prefetch_l2(kh + t1 * kD, rows * kD * 2);
+          prefetch_l2(vh + t1 * kD, rows * kD * 2);
+          prefetch_l2(gh + t1 * kD, rows * kD * 4);
+        }
+        if (!wait(q_ready, ph) || !wait(k_ready, ph) || !wait(g_ready, ph) || !wait(v_full, ph)) break;
+        tc_fence_after();
+        // A = Q K^T (pairs: Qh Kh + Qh Kl + Ql Kh)
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16_ts(tX, tQh + 8 * ks, kdesc(sKhi, ks), iKK, ks > 0);
+          mma_bf16_ts(tX, tQh + 8 * ks, kdesc(sKlo, ks), iKK, 1);
+          mma_bf16_ts(tX, tQl + 8 * ks, kdesc(sKhi, ks), iKK, 1);
+        }
+        // C = dO V^T
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16(tCB, kdesc(sGhi, ks), kdesc(sV, ks), iKK, ks > 0);
+          mma_bf16(tCB, kdesc(sGlo, ks), kdesc(sV, ks), iKK, 1);
+        }
+        mma_commit(ac_full);
+        if (!wait(s_ready, ph) || !wait(x_free, ph)) break;
+        tc_fence_after();
+        // Y = dO S_prev^T (S copy rows = features i, K-major over value components)
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16(tX, kdesc(sGhi, ks), kdesc(sShi, ks), iKK, ks > 0);
+          mma_bf16(tX, kdesc(sGhi, ks), kdesc(sSlo, ks), iKK, 1);
+          mma_bf16(tX, kdesc(sGlo, ks), kdesc(sShi, ks), iKK, 1);
+        }
+        // S += K^T V
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16(tS, mndesc(sKhi, ks), mndesc(sV, ks), iMM, 1);
+          mma_bf16(tS, mndesc(sKlo, ks), mndesc(sV, ks), iMM, 1);
+        }
+        mma_commit(y_full);
+        if (!wait(cb_ready, ph)) break;
+        tc_fence_after();
+        // X += B' K: B' from tensor memory (keys [16 ks, 16 ks + 16): 8 columns hi, 8 lo)
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16_ts(tX, tCB + 16 * ks, mndesc(sKhi, ks), iKM, 1);
+          mma_bf16_ts(tX, tCB + 16 * ks + 8, mndesc(sKhi, ks), iKM, 1);
+          mma_bf16_ts(tX, tCB + 16 * ks, mndesc(sKlo, ks), iKM, 1);
+        }
+        mma_commit(d_full);
+      }
+      mma_commit(drain);
+      wait_drain(drain, 0, status);
+    }
+  } else if (warp < kP1WarpG) {
+    // ---------------- QK warps: keys, queries, copies of the state ----------------
+    const int r = (warp & 3) * 32 + lane;       // tensor-memory lane: chunk row, or state row for the copies
+    const int tid = threadIdx.x - 32;           // 0..127
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    uint8_t *Shi = sm + L::Shi, *Slo = sm + L::Slo;
+    uint4 *kt = reinterpret_cast<uint4 *>(sm + L::Khi), *lt = reinterpret_cast<uint4 *>(sm + L::Klo);
+    int k_issued = 0;
+    auto load_k = [&](int c) {  // raw keys of chunk c into the Khi tile (rows past the end read as zero)
+      mbar_arrive_expect_tx(k_full, kTile);
+      tma_load_3d(sm + L::Khi, &p.tk, k_full, 0, c * kC, bh);
+      tma_load_3d(sm + L::Khi + kBlk, &p.tk, k_full, 64, c * kC, bh);
+      k_issued = c + 1;
+    };
+    if (tid == 0) {
+      prefetch_tmap(&p.tk);
+      load_k(0);
+    }
+    {
+      // initial state S0 into tensor memory and its pair copy; z0 into z buffer 0
+      for (int cb = 0; cb < 8; ++cb) {
+        uint32_t w[16];
+        if (p.S0) {
+          const float4 *src = reinterpret_cast<const float4 *>(p.S0 + ((long)bh * kD + r) * kD + cb * 16);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 f = src[e];
+            w[4 * e] = __float_as_uint(f.x), w[4 * e + 1] = __float_as_uint(f.y);
+            w[4 * e + 2] = __float_as_uint(f.z), w[4 * e + 3] = __float_as_uint(f.w);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = 0u;
+        }
+        tmem_st16(tl + kP1S + cb * 16, w);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t h[4], l[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2(__uint_as_float(w[8 * q + 2 * e]), __uint_as_float(w[8 * q + 2 * e + 1]), h[e], l[e]);
+          *tile_chunk(Shi, r, cb * 16 + 8 * q) = make_uint4(h[0], h[1], h[2], h[3]);
+          *tile_chunk(Slo, r, cb * 16 + 8 * q) = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+      }
+      zbuf[r] = p.z0 ? p.z0[(long)bh * kD + r] : 0.f;
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(s_ready);
+      mbar_arrive(&z_full[0]);
+    }
+    bool ok = true;
+    for (int c = 0; c < nch; ++c) {
+      const long t0 = (long)c * kC;
+      const int T = (int)min((long)kC, N - t0);
+      // this row's queries, loaded while the keys are transformed
+      uint4 x[16];
+      if (r < T) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(qh + (t0 + r) * kD);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = ld_row16(src + e);
+      }
+      // keys: the raw tile has landed; phi pairs in place (hi) and into Klo (lo).  The 16-byte
+      // chunk ch of the tile is row (ch mod 1024) / 8 of block ch / 1024; rows past the end are zeros
+      ok = wait(k_full, c & 1);
+      if (bar_or(kBarQK, 128, !ok)) break;
+#pragma unroll 2
+      for (int i = 0; i < 16; ++i) {
+        const int ch = tid + 128 * i;
+        uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
+        if (((ch & 1023) >> 3) < T) phi_pair8(kt[ch], h, l);
+        kt[ch] = h;
+        lt[ch] = l;
+      }
+      fence_async_smem();
+      mbar_arrive(k_ready);
+      // queries: phi pairs into tensor memory once the previous chunk's last reads are done
+      ok = c == 0 || wait(e3_done, (c - 1) & 1);
+      ok = ok && wait(&z_full[c & 1], (c >> 1) & 1);
+      if (bar_or(kBarQK, 128, !ok)) break;
+      tc_fence_after();
+      const float *z = zbuf + (c & 1) * kD;
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        uint32_t h[4] = {0u, 0u, 0u, 0u}, l[4] = {0u, 0u, 0u, 0u};
+        float vv[8];
+        if (r < T) {
+          phi_split8(x[e], h, l, vv);
+#pragma unroll
+          for (int m = 0; m < 8; ++m) dot = fmaf(vv[m], z[8 * e + m], dot);
+        }
+        // features 8e .. 8e + 7: pair columns 4e .. 4e + 3 (hi) and 64 + 4e .. (lo)
+        tmem_st4_nowait(tl + kP1Q + 4 * e, h[0], h[1], h[2], h[3]);
+        tmem_st4_nowait(tl + kP1Q + 64 + 4 * e, l[0], l[1], l[2], l[3]);
+      }
+      tmem_wait_st();
+      den_x[r] = dot;
+      mbar_arrive(&z_empty[c & 1]);
+      tc_fence_before();
+      mbar_arrive(q_ready);
+      if (c + 1 == nch) break;
+      // pair copy of the state the next chunk reads, once this chunk's Y has read the current
+      // copy and its S update has completed
+      ok = wait(y_full, c & 1);
+      if (bar_or(kBarQK, 128, !ok)) break;
+      tc_fence_after();
+      for (int cb = 0; cb < 8; ++cb) {
+        uint32_t w[16];
+        tmem_ld16(tl + kP1S + cb * 16, w);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t h[4], l[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2(__uint_as_float(w[8 * q + 2 * e]), __uint_as_float(w[8 * q + 2 * e + 1]), h[e], l[e]);
+          *tile_chunk(Shi, r, cb * 16 + 8 * q) = make_uint4(h[0], h[1], h[2], h[3]);
+          *tile_chunk(Slo, r, cb * 16 + 8 * q) = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(s_ready);
+      // the next chunk's raw keys once this chunk's products are done with the K tiles
+      ok = wait(d_full, c & 1);
+      if (bar_or(kBarQK, 128, !ok)) break;
+      if (tid == 0) load_k(c + 1);
+    }
+    if (tid == 0 && k_issued > 0) wait_drain(k_full, (k_issued - 1) & 1, status);
+  } else if (warp < kP1WarpE) {
+    // ---------------- G warps: dO pairs (coalesced rows), V by TMA ----------------
+    const int gt = threadIdx.x - kP1WarpG * 32;  // 0..127
+    const int wg = gt >> 5;                       // rows 32 wg .. 32 wg + 31
+    uint8_t *Ghi = sm + L::Ghi, *Glo = sm + L::Glo;
+    int v_issued = 0;
+    if (gt == 0) prefetch_tmap(&p.tv);
+    for (int c = 0; c < nch; ++c) {
+      const long t0 = (long)c * kC;
+      const int T = (int)min((long)kC, N - t0);
+      const bool ok = c == 0 || wait(y_full, (c - 1) & 1);
+      if (bar_or(kBarG, 128, !ok)) break;
+      if (gt == 0) {
+        mbar_arrive_expect_tx(v_full, kTile);
+        tma_load_3d(sm + L::V, &p.tv, v_full, 0, (int)t0, bh);
+        tma_load_3d(sm + L::V + kBlk, &p.tv, v_full, 64, (int)t0, bh);
+        v_issued = c + 1;
+      }
+      // lane l converts features 4l .. 4l + 3 of each row (one 512-byte row per warp load)
+      const int col = 4 * lane;
+      const uint32_t off = (col >> 6) * kBlk;
+#pragma unroll 1
+      for (int rr = 0; rr < 32; rr += 8) {
+        float4 gg[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int row = 32 * wg + rr + e;
+          gg[e] = row < T ? __ldg(reinterpret_cast<const float4 *>(gh + (t0 + row) * kD + col))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int row = 32 * wg + rr + e;
+          uint32_t h0, l0, h1, l1;
+          split2(gg[e].x, gg[e].y, h0, l0);
+          split2(gg[e].z, gg[e].w, h1, l1);
+          const uint32_t o = off + sw128_offset(row, col & 63);
+          *reinterpret_cast<uint2 *>(Ghi + o) = make_uint2(h0, h1);
+          *reinterpret_cast<uint2 *>(Glo + o) = make_uint2(l0, l1);
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(g_ready);
+    }
+    if (gt == 0 && v_issued > 0) wait_drain(v_full, (v_issued - 1) & 1, status);
+  } else {
+    // ---------------- E warps: scores, den, gden, B', key column sums, dq ----------------
+    const int t = (warp & 3) * 32 + lane;  // tensor-memory lane = chunk row; also feature t of z
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint8_t *Khi = sm + L::Khi, *Klo = sm + L::Klo;
+    for (int c = 0; c < nch; ++c) {
+      const long t0 = (long)c * kC;
+      const int T = (int)min((long)kC, N - t0);
+      const int jmax = min(t, T - 1);  // keys kept: j <= t and j < T
+      uint32_t ra[32], rc[32];
+      // E1: row sums of A and of A * C
+      bool ok = wait(q_ready, c & 1) && wait(k_ready, c & 1) && wait(ac_full, c & 1);
+      if (bar_or(kBarE, 128, !ok)) break;
+      tc_fence_after();
+      float rs = 0.f, ac = 0.f;
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        tmem_ld32x2(tl + kP1X + cb * 32, tl + kP1CB + cb * 32, ra, rc);
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+          const float a = cb * 32 + m <= jmax ? __uint_as_float(ra[m]) : 0.f;
+          rs += a;
+          ac = fmaf(a, __uint_as_float(rc[m]), ac);
+        }
+      }
+      const float den = (den_x[t] + rs) + p.eps;
+      tc_fence_before();
+      mbar_arrive(x_free);
+      // while Y is formed: column t of this chunk's phi(K) pairs, summed over its valid rows
+      float kc = 0.f;
+      {
+        const uint8_t *bh_ = Khi + (t >> 6) * kBlk, *bl_ = Klo + (t >> 6) * kBlk;
+#pragma unroll 4
+        for (int j = 0; j < T; ++j) {
+          const uint32_t off = sw128_offset(j, t & 63);
+          kc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(bh_ + off)) +
+                __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(bl_ + off));
+        }
+      }
+      // E2: gden from phi(q) . Y, then B' = C + den gden in place as bf16 pairs
+      ok = wait(y_full, c & 1);
+      if (bar_or(kBarE, 128, !ok)) break;
+      tc_fence_after();
+      float qy = 0.f;
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+        uint32_t qhw[16], qlw[16];
+        tmem_ld32_16x2(tl + kP1X + b * 32, tl + kP1Q + 16 * b, tl + kP1Q + 64 + 16 * b, ra, qhw, qlw);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          qy = fmaf(lo16(qhw[m]) + lo16(qlw[m]), __uint_as_float(ra[2 * m]), qy);
+          qy = fmaf(hi16(qhw[m]) + hi16(qlw[m]), __uint_as_float(ra[2 * m + 1]), qy);
+        }
+      }
+      const float gden = -((qy + ac) / den) / den;
+      const float dg = den * gden;
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        tmem_ld32(tl + kP1CB + cb * 32, rc);
+        split_scores32(rc, cb, [&](int j) { return j <= jmax; }, [&](int, float x) { return x + dg; });
+        tmem_st32(tl + kP1CB + cb * 32, rc);
+      }
+      tc_fence_before();
+      mbar_arrive(cb_ready);
+      // E3: dq = ((Y + B' K) / den + gden z_prev) phi'(q)
+      ok = wait(d_full, c & 1);
+      if (bar_or(kBarE, 128, !ok)) break;
+      tc_fence_after();
+      const float inv = 1.f / den;
+      const float *z = zbuf + (c & 1) * kD;
+      float *dst = p.dq + ((long)bh * N + t0 + t) * kD;
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+        uint32_t qhw[16], qlw[16];
+        tmem_ld32_16x2(tl + kP1X + b * 32, tl + kP1Q + 16 * b, tl + kP1Q + 64 + 16 * b, ra, qhw, qlw);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float f0 = fminf(lo16(qhw[m]) + lo16(qlw[m]), 1.f), f1 = fminf(hi16(qhw[m]) + hi16(qlw[m]), 1.f);
+          ra[2 * m] = __float_as_uint(fmaf(__uint_as_float(ra[2 * m]), inv, z[32 * b + 2 * m] * gden) * f0);
+          ra[2 * m + 1] =
+              __float_as_uint(fmaf(__uint_as_float(ra[2 * m + 1]), inv, z[32 * b + 2 * m + 1] * gden) * f1);
+        }
+        if (t < T) {
+          float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * b);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            d4[e] = make_float4(__uint_as_float(ra[4 * e]), __uint_as_float(ra[4 * e + 1]),
+                                __uint_as_float(ra[4 * e + 2]), __uint_as_float(ra[4 * e + 3]));
+        }
+      }
+      if (t < T) {
+        p.den[(long)bh * N + t0 + t] = den;
+        p.gden[(long)bh * N + t0 + t] = gden;
+      }
+      // z for the next chunk: z_prev plus this chunk's key column sums (thread t owns feature t)
+      named_bar(kBarE, 128);  // every read of this chunk's z is done
+      if (c + 1 < nch) {
+        const int nb = (c + 1) & 1;
+        ok = c + 1 < 2 || wait(&z_empty[nb], (((c + 1) >> 1) - 1) & 1);
+        if (bar_or(kBarE, 128, !ok)) break;
+        zbuf[nb * kD + t] = z[t] + kc;
+        mbar_arrive(&z_full[nb]);
+      }
+      tc_fence_before();
+      mbar_arrive(e3_done);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: chunks in reverse, U (and u) carried; role 0 dv, role 1 dk.
+// ---------------------------------------------------------------------------
+// Shared memory: phi(Q), gnum and the copy of U as bf16 pairs (six tiles,
+// 192 KB), a staging tile for the raw key operand (32 KB), the chunk's gden,
+// the carried u (role 1), barriers.
+struct P2Layout {
+  static constexpr uint32_t Qhi = 0, Qlo = kTile, Nhi = 2 * kTile, Nlo = 3 * kTile, Uhi = 4 * kTile, Ulo = 5 * kTile,
+                            Kst = 6 * kTile;
+  static constexpr uint32_t Gd = 7 * kTile;  // [128] gden of the chunk
+  static constexpr uint32_t Ub = Gd + 512;   // [128] u carried into the chunk (role 1)
+  static constexpr uint32_t Bars = Ub + 512;
+  static constexpr int kNumBars = 12;
+  static constexpr uint32_t Misc = Bars + kNumBars * 8;
+  static constexpr uint32_t Bytes = Misc + 16;
+};
+static_assert(P2Layout::Bytes <= 232448, "pass 2 shared memory");
+
+// TMEM columns of pass 2: U accumulator; X = the key-side scores (role 0:
+// K Q^T, role 1: V gnum^T), then as bf16 pairs; O = dv or dk; the key operand
+// (role 0: phi(K) as pairs, 128 columns; role 1: V, 64 columns).
+constexpr uint32_t kP2U = 0, kP2X = 128, kP2O = 256, kP2K = 384;
+
+// Warp roles of pass 2 (13 warps): 0 MMA issuer; 1-4 key operand and phi(Q)
+// pairs (both staged by TMA), copies of U; 5-8 gnum pairs (coalesced rows) and
+// gden; 9-12 scores and outputs.
+constexpr int kP2Threads = 416;
+constexpr int kP2WarpN = 5, kP2WarpE = 9;
+
+template <int kRole>
+__device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
+  using L = P2Layout;
+  constexpr bool kDk = kRole == 1;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(&g_bwd_status, kAbortMisaligned);
+    return;
+  }
+  uint8_t *sm = smem_raw;
+  float *gd = reinterpret_cast<float *>(sm + L::Gd);
+  float *ub = reinterpret_cast<float *>(sm + L::Ub);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::Bars);
+  uint64_t *q_ready = bars + 0, *k_ready = bars + 1, *n_ready = bars + 2, *u_ready = bars + 3, *x_full = bars + 4,
+           *x_split = bars + 5, *o_full = bars + 6, *o_done = bars + 7, *drain = bars + 8, *kst_full = bars + 9,
+           *q_full = bars + 10;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::Misc);
+  volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + L::Misc + 4);
+  unsigned int *status = &g_bwd_status;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const long N = p.N;
+  const int nch = (int)((N + kC - 1) / kC);
+  const __nv_bfloat16 *qh = p.q + (long)bh * N * kD, *kh = p.k + (long)bh * N * kD, *vh = p.v + (long)bh * N * kD;
+  const float *gh = p.dout + (long)bh * N * kD;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_ready, 128);
+    mbar_init(k_ready, 128);
+    mbar_init(n_ready, 128);
+    mbar_init(u_ready, 128);
+    mbar_init(x_full, 1);
+    mbar_init(x_split, 128);
+    mbar_init(o_full, 1);
+    mbar_init(o_done, 128);
+    mbar_init(drain, 1);
+    mbar_init(kst_full, 1);
+    mbar_init(q_full, 1);
+    *abort_word = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto wait = [&](uint64_t *bar, uint32_t parity) { return mbar_wait(bar, parity, abort_word, status); };
+
+  if (warp == 0) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t iKK = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t iKM = idesc_bf16_f32(128, 128, 0, 1);
+      constexpr uint32_t iMM = idesc_bf16_f32(128, 128, 1, 1);
+      const uint32_t sQhi = smem_u32(sm + L::Qhi), sQlo = smem_u32(sm + L::Qlo), sNhi = smem_u32(sm + L::Nhi),
+                     sNlo = smem_u32(sm + L::Nlo), sUhi = smem_u32(sm + L::Uhi), sUlo = smem_u32(sm + L::Ulo);
+      const uint32_t tU = tmem + kP2U, tX = tmem + kP2X, tO = tmem + kP2O, tKh = tmem + kP2K,
+                     tKl = tmem + kP2K + 64;
+      for (int it = 0; it < nch; ++it) {
+        const int c = nch - 1 - it;
+        const uint32_t ph = it & 1;
+        if (c > 0) {  // the next chunk's rows into L2
+          const long t1 = (long)(c - 1) * kC;
+          prefetch_l2(qh + t1 * kD, kC * kD * 2);
+          prefetch_l2(kDk ? vh + t1 * kD : kh + t1 * kD, kC * kD * 2);
+          if (kDk) prefetch_l2(kh + t1 * kD, kC * kD * 2);
+          prefetch_l2(gh + t1 * kD, kC * kD * 4);
+        }
+        if (!wait(q_ready, ph) || !wait(k_ready, ph) || !wait(n_ready, ph)) break;
+        if (it > 0 && !wait(o_done, (it - 1) & 1)) break;
+        tc_fence_after();
+        if (!kDk) {
+          // X = K Q^T (rows keys j, columns queries t)
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) {
+            mma_bf16_ts(tX, tKh + 8 * ks, kdesc(sQhi, ks), iKK, ks > 0);
+            mma_bf16_ts(tX, tKh + 8 * ks, kdesc(sQlo, ks), iKK, 1);
+            mma_bf16_ts(tX, tKl + 8 * ks, kdesc(sQhi, ks), iKK, 1);
+          }
+        } else {
+          // X = V gnum^T
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) {
+            mma_bf16_ts(tX, tKh + 8 * ks, kdesc(sNhi, ks), iKK, ks > 0);
+            mma_bf16_ts(tX, tKh + 8 * ks, kdesc(sNlo, ks), iKK, 1);
+          }
+        }
+        if (!wait(u_ready, ph)) break;
+        tc_fence_after();
+        if (!kDk) {
+          // O = K U (U rows = features i: the K index)
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) {
+            mma_bf16_ts(tO, tKh + 8 * ks, mndesc(sUhi, ks), iKM, ks > 0);
+            mma_bf16_ts(tO, tKh + 8 * ks, mndesc(sUlo, ks), iKM, 1);
+            mma_bf16_ts(tO, tKl + 8 * ks, mndesc(sUhi, ks), iKM, 1);
+          }
+        } else {
+          // O = V U^T (U rows = features i: the N index, K-major over value components)
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) {
+            mma_bf16_ts(tO, tKh + 8 * ks, kdesc(sUhi, ks), iKK, ks > 0);
+            mma_bf16_ts(tO, tKh + 8 * ks, kdesc(sUlo, ks), iKK, 1);
+          }
+        }
+        mma_commit(x_full);
+        if (!wait(x_split, ph)) break;
+        tc_fence_after();
+        // O += X B with X from tensor memory as pairs (queries [16 ks, 16 ks + 16): 8 columns hi,
+        // 8 lo) and B = gnum (role 0) or phi(Q) (role 1), rows = queries
+        const uint32_t sBhi = kDk ? sQhi : sNhi, sBlo = kDk ? sQlo : sNlo;
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16_ts(tO, tX + 16 * ks, mndesc(sBhi, ks), iKM, 1);
+          mma_bf16_ts(tO, tX + 16 * ks + 8, mndesc(sBhi, ks), iKM, 1);
+          mma_bf16_ts(tO, tX + 16 * ks, mndesc(sBlo, ks), iKM, 1);
+        }
+        // U += Q^T gnum
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16(tU, mndesc(sQhi, ks), mndesc(sNhi, ks), iMM, 1);
+          mma_bf16(tU, mndesc(sQhi, ks), mndesc(sNlo, ks), iMM, 1);
+          mma_bf16(tU, mndesc(sQlo, ks), mndesc(sNhi, ks), iMM, 1);
+        }
+        mma_commit(o_full);
+      }
+      mma_commit(drain);
+      wait_drain(drain, 0, status);
+    }
+  } else if (warp < kP2WarpN) {
+    // ---------------- QK warps: key operand into tensor memory, phi(Q) pairs, copies of U ----------------
+    const int r = (warp & 3) * 32 + lane;  // tensor-memory lane: chunk row, or state row of U
+    const int tid = threadIdx.x - 32;      // 0..127
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    uint8_t *Uhi = sm + L::Uhi, *Ulo = sm + L::Ulo, *Kst = sm + L::Kst;
+    uint4 *qt = reinterpret_cast<uint4 *>(sm + L::Qhi), *qlt = reinterpret_cast<uint4 *>(sm + L::Qlo);
+    const CUtensorMap *tkey = kDk ? &p.tv : &p.tk;
+    int kst_issued = 0, q_issued = 0;
+    auto load_key = [&](int c) {  // raw key operand rows of chunk c into the staging tile
+      mbar_arrive_expect_tx(kst_full, kTile);
+      tma_load_3d(Kst, tkey, kst_full, 0, c * kC, bh);
+      tma_load_3d(Kst + kBlk, tkey, kst_full, 64, c * kC, bh);
+      ++kst_issued;
+    };
+    auto load_q = [&](int c) {  // raw queries of chunk c into the Qhi tile
+      mbar_arrive_expect_tx(q_full, kTile);
+      tma_load_3d(sm + L::Qhi, &p.tq, q_full, 0, c * kC, bh);
+      tma_load_3d(sm + L::Qhi + kBlk, &p.tq, q_full, 64, c * kC, bh);
+      ++q_issued;
+    };
+    if (tid == 0) {
+      prefetch_tmap(tkey);
+      prefetch_tmap(&p.tq);
+      load_key(nch - 1);
+    }
+    {
+      // U at the end of the sequence: dS (or zero) into tensor memory and its pair copy
+      for (int cb = 0; cb < 8; ++cb) {
+        uint32_t w[16];
+        if (p.dS) {
+          const float4 *src = reinterpret_cast<const float4 *>(p.dS + ((long)bh * kD + r) * kD + cb * 16);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 f = src[e];
+            w[4 * e] = __float_as_uint(f.x), w[4 * e + 1] = __float_as_uint(f.y);
+            w[4 * e + 2] = __float_as_uint(f.z), w[4 * e + 3] = __float_as_uint(f.w);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = 0u;
+        }
+        tmem_st16(tl + kP2U + cb * 16, w);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t h[4], l[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2(__uint_as_float(w[8 * q + 2 * e]), __uint_as_float(w[8 * q + 2 * e + 1]), h[e], l[e]);
+          *tile_chunk(Uhi, r, cb * 16 + 8 * q) = make_uint4(h[0], h[1], h[2], h[3]);
+          *tile_chunk(Ulo, r, cb * 16 + 8 * q) = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+      }
+    }
+    bool ok = true;
+    for (int it = 0; it < nch; ++it) {
+      const int c = nch - 1 - it;
+      const long t0 = (long)c * kC;
+      const int T = (int)min((long)kC, N - t0);
+      ok = it == 0 || wait(o_full, (it - 1) & 1);
+      if (bar_or(kBarQK, 128, !ok)) break;
+      tc_fence_after();
+      if (tid == 0) load_q(c);  // the Q tiles are free: the previous chunk's products have completed
+      // key operand from the staging tile, row r: role 0 phi(k) pairs (hi columns 0-63, lo
+      // 64-127), role 1 v as given; rows past the end are zeros
+      ok = wait(kst_full, it & 1);
+      if (bar_or(kBarQK, 128, !ok)) break;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint4 x = r < T ? *tile_chunk(Kst, r, 8 * e) : make_uint4(0u, 0u, 0u, 0u);
+        if (!kDk) {
+          uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
+          if (r < T) phi_pair8(x, h, l);
+          tmem_st4_nowait(tl + kP2K + 4 * e, h.x, h.y, h.z, h.w);
+          tmem_st4_nowait(tl + kP2K + 64 + 4 * e, l.x, l.y, l.z, l.w);
+        } else {
+          tmem_st4_nowait(tl + kP2K + 4 * e, x.x, x.y, x.z, x.w);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(k_ready);
+      named_bar(kBarQK, 128);  // every row has been read from the staging tile
+      if (tid == 0 && c > 0) load_key(c - 1);
+      if (it > 0) {
+        // the pair copy of U (every chunk after this one folded in); the tiles were last read by
+        // the previous chunk's products, which have completed
+        for (int cb = 0; cb < 8; ++cb) {
+          uint32_t w[16];
+          tmem_ld16(tl + kP2U + cb * 16, w);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t h[4], l[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split2(__uint_as_float(w[8 * q + 2 * e]), __uint_as_float(w[8 * q + 2 * e + 1]), h[e], l[e]);
+            *tile_chunk(Uhi, r, cb * 16 + 8 * q) = make_uint4(h[0], h[1], h[2], h[3]);
+            *tile_chunk(Ulo, r, cb * 16 + 8 * q) = make_uint4(l[0], l[1], l[2], l[3]);
+          }
+        }
+      }
+      // queries: the raw tile has landed; phi pairs in place (hi) and into Qlo (lo)
+      ok = wait(q_full, it & 1);
+      if (bar_or(kBarQK, 128, !ok)) break;
+#pragma unroll 2
+      for (int i = 0; i < 16; ++i) {
+        const int ch = tid + 128 * i;
+        uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
+        if (((ch & 1023) >> 3) < T) phi_pair8(qt[ch], h, l);
+        qt[ch] = h;
+        qlt[ch] = l;
+      }
+      fence_async_smem();
+      mbar_arrive(q_ready);
+      mbar_arrive(u_ready);
+    }
+    if (tid == 0) {
+      if (kst_issued > 0) wait_drain(kst_full, (kst_issued - 1) & 1, status);
+      if (q_issued > 0) wait_drain(q_full, (q_issued - 1) & 1, status);
+    }
+    // role 0: the initial state's gradient dS0 = U after the first chunk
+    if (!kDk && p.dS0) {
+      ok = ok && wait(o_full, (nch - 1) & 1);
+      if (!bar_or(kBarQK, 128, !ok) && !*abort_word) {
+        tc_fence_after();
+        float *dst = p.dS0 + ((long)bh * kD + r) * kD;
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t w[32];
+          tmem_ld32(tl + kP2U + cb * 32, w);
+          float4 *d4 = reinterpret_cast<float4 *>(dst + cb * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            d4[e] = make_float4(__uint_as_float(w[4 * e]), __uint_as_float(w[4 * e + 1]), __uint_as_float(w[4 * e + 2]),
+                                __uint_as_float(w[4 * e + 3]));
+        }
+      }
+    }
+  } else if (warp < kP2WarpE) {
+    // ---------------- N warps: gnum = dO / den as pairs (coalesced rows), gden ----------------
+    const int gt = threadIdx.x - kP2WarpN * 32;  // 0..127
+    const int wg = gt >> 5;                       // rows 32 wg .. 32 wg + 31
+    uint8_t *Nhi = sm + L::Nhi, *Nlo = sm + L::Nlo;
+    const int col = 4 * lane;
+    const uint32_t off = (col >> 6) * kBlk;
+    for (int it = 0; it < nch; ++it) {
+      const int c = nch - 1 - it;
+      const long t0 = (long)c * kC;
+      const int T = (int)min((long)kC, N - t0);
+      // this thread's row 32 wg + lane: its gden, and 1 / den broadcast over the warp below
+      const int myrow = 32 * wg + lane;
+      const float inv_mine = myrow < T ? 1.f / p.den[(long)bh * N + t0 + myrow] : 0.f;
+      const float gdn = myrow < T ? p.gden[(long)bh * N + t0 + myrow] : 0.f;
+      const bool ok = it == 0 || wait(o_full, (it - 1) & 1);
+      if (bar_or(kBarG, 128, !ok)) break;
+#pragma unroll 1
+      for (int rr = 0; rr < 32; rr += 8) {
+        float4 gg[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int row = 32 * wg + rr + e;
+          gg[e] = row < T ? __ldg(reinterpret_cast<const float4 *>(gh + (t0 + row) * kD + col))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int row = 32 * wg + rr + e;
+          const float inv = __shfl_sync(0xffffffffu, inv_mine, rr + e);
+          uint32_t h0, l0, h1, l1;
+          split2(gg[e].x * inv, gg[e].y * inv, h0, l0);
+          split2(gg[e].z * inv, gg[e].w * inv, h1, l1);
+          const uint32_t o = off + sw128_offset(row, col & 63);
+          *reinterpret_cast<uint2 *>(Nhi + o) = make_uint2(h0, h1);
+          *reinterpret_cast<uint2 *>(Nlo + o) = make_uint2(l0, l1);
+        }
+      }
+      gd[myrow] = gdn;
+      fence_async_smem();
+      mbar_arrive(n_ready);
+    }
+  } else {
+    // ---------------- E warps: key-side scores as pairs, then dv or dk ----------------
+    const int j = (warp & 3) * 32 + lane;  // tensor-memory lane = key row (or feature, for u)
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    if (kDk) {
+      ub[j] = p.dz ? p.dz[(long)bh * kD + j] : 0.f;
+      named_bar(kBarE, 128);
+    }
+    const uint8_t *Qhi = sm + L::Qhi, *Qlo = sm + L::Qlo;
+    bool ok = true;
+    for (int it = 0; it < nch; ++it) {
+      const int c = nch - 1 - it;
+      const long t0 = (long)c * kC;
+      const int T = (int)min((long)kC, N - t0);
+      ok = wait(x_full, it & 1) && wait(n_ready, it & 1) && wait(q_ready, it & 1);
+      if (bar_or(kBarE, 128, !ok)) break;
+      tc_fence_after();
+      // queries t >= j of the chunk's valid rows (none when the key row itself is past the end)
+      const int tmin = j, tend = j < T ? T : 0;
+#pragma unroll 1
+      for (int cb = 0; cb < 4; cb += 2) {
+        uint32_t rx[32], ry[32];
+        tmem_ld32x2(tl + kP2X + cb * 32, tl + kP2X + cb * 32 + 32, rx, ry);
+        split_scores32(rx, cb, [&](int t) { return t >= tmin && t < tend; },
+                       [&](int t, float x) { return kDk ? x + gd[t] : x; });
+        split_scores32(ry, cb + 1, [&](int t) { return t >= tmin && t < tend; },
+                       [&](int t, float x) { return kDk ? x + gd[t] : x; });
+        tmem_st32(tl + kP2X + cb * 32, rx);
+        tmem_st32(tl + kP2X + cb * 32 + 32, ry);
+      }
+      float ucol = 0.f;
+      if (kDk) {
+        // this chunk's share of u for feature j: sum over its queries of phi(q_t)_j gden_t.  Read
+        // before x_split: the Q tiles are reloaded as soon as this chunk's products complete
+        const uint8_t *bh_ = Qhi + (j >> 6) * kBlk, *bl_ = Qlo + (j >> 6) * kBlk;
+#pragma unroll 4
+        for (int t = 0; t < T; ++t) {
+          const uint32_t off = sw128_offset(t, j & 63);
+          const float f = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(bh_ + off)) +
+                          __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(bl_ + off));
+          ucol = fmaf(f, gd[t], ucol);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(x_split);
+      ok = wait(o_full, it & 1);
+      if (bar_or(kBarE, 128, !ok)) break;
+      tc_fence_after();
+      float *dst = (kDk ? p.dk : p.dv) + ((long)bh * N + t0 + j) * kD;
+      const uint4 *kr = reinterpret_cast<const uint4 *>(kh + (t0 + j) * kD);
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+        uint32_t ro[32];
+        tmem_ld32(tl + kP2O + b * 32, ro);
+        if (kDk) {
+          // dk = (V U^T + B Q + u) phi'(k), phi'(x) = 1 above zero, e^x below
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint4 kx = j < T ? __ldg(kr + 4 * b + e) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t w4[4] = {kx.x, kx.y, kx.z, kx.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int col = 32 * b + 8 * e + 2 * m;
+              const float2 f = phi2(lo16(w4[m]), hi16(w4[m]));
+              const float da = fminf(f.x, 1.f), db = fminf(f.y, 1.f);
+              ro[8 * e + 2 * m] = __float_as_uint((__uint_as_float(ro[8 * e + 2 * m]) + ub[col]) * da);
+              ro[8 * e + 2 * m + 1] = __float_as_uint((__uint_as_float(ro[8 * e + 2 * m + 1]) + ub[col + 1]) * db);
+            }
+          }
+        }
+        if (j < T) {
+          float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * b);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            d4[e] = make_float4(__uint_as_float(ro[4 * e]), __uint_as_float(ro[4 * e + 1]),
+                                __uint_as_float(ro[4 * e + 2]), __uint_as_float(ro[4 * e + 3]));
+        }
+      }
+      if (kDk) {
+        named_bar(kBarE, 128);  // every read of u for this chunk is done
+        ub[j] += ucol;
+      }
+      tc_fence_before();
+      mbar_arrive(o_done);
+    }
+    if (kDk && p.dz0) {
+      named_bar(kBarE, 128);
+      if (ok && !*abort_word) p.dz0[(long)bh * kD + j] = ub[j];
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Both roles of a head run side by side: blockIdx.y = 0 dv, 1 dk.
+__global__ void __launch_bounds__(kP2Threads, 1) bwd_pass2_tc(const __grid_constant__ BwdTcParams p) {
+  if (blockIdx.y == 0)
+    pass2_role<0>(p);
+  else
+    pass2_role<1>(p);
+}
+
+}  // namespace
+
+// [BH][N][128] bf16 as a 3-D tensor; boxes of 64 features x 128 tokens x 1 head, 128-byte swizzle.
+bool make_bf16_map(CUtensorMap *m, const void *base, long BH, long N) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)N * kD * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool backward_tc_supported(const Problem &p) {
+  const DeviceInfo di = device_info(-1);
+  return p.dt == LA_BF16 && p.dk == kD && p.dv == kD && p.N >= 1 && p.N <= 0x7fffffffL && p.BH <= 65535 &&
+         di.cc_major == 10 && di.cc_minor == 3 && tensor_map_encoder() != nullptr;
+}
+
+cudaError_t launch_causal_backward_tc(const BackwardProblem &b) {
+  const Problem &p = b.p;
+  cudaError_t e = ensure_smem_optin((const void *)bwd_pass1_tc, (int)P1Layout::Bytes);
+  if (e == cudaSuccess) e = ensure_smem_optin((const void *)bwd_pass2_tc, (int)P2Layout::Bytes);
+  if (e != cudaSuccess) return e;
+  // scratch: den and gden of every token, written by pass 1 and read by pass 2
+  float *scratch = nullptr;
+  e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), sizeof(float) * 2 * (size_t)p.BH * p.N, p.stream);
+  if (e != cudaSuccess) return e;
+  BwdTcParams a;
+  memset(&a, 0, sizeof a);
+  if (!make_bf16_map(&a.tq, p.q, p.BH, p.N) || !make_bf16_map(&a.tk, p.k, p.BH, p.N) ||
+      !make_bf16_map(&a.tv, p.v, p.BH, p.N)) {
+    cudaFreeAsync(scratch, p.stream);
+    return cudaErrorInvalidValue;
+  }
+  a.q = static_cast<const __nv_bfloat16 *>(p.q);
+  a.k = static_cast<const __nv_bfloat16 *>(p.k);
+  a.v = static_cast<const __nv_bfloat16 *>(p.v);
+  a.dout = b.dout, a.S0 = b.S0, a.z0 = b.z0, a.dS = b.dS, a.dz = b.dz;
+  a.dq = b.dq, a.dk = b.dk, a.dv = b.dv, a.dS0 = b.dS0, a.dz0 = b.dz0;
+  a.den = scratch;
+  a.gden = scratch + (size_t)p.BH * p.N;
+  a.N = p.N;
+  a.eps = p.eps;
+  {
+    LaunchTimer timer(kKBackward, p.stream);
+    bwd_pass1_tc<<<(unsigned)p.BH, kP1Threads, P1Layout::Bytes, p.stream>>>(a);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) {
+      count_launch();
+      bwd_pass2_tc<<<dim3((unsigned)p.BH, 2), kP2Threads, P2Layout::Bytes, p.stream>>>(a);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) count_launch();
+    timer.done(e);
+  }
+  const cudaError_t f = cudaFreeAsync(scratch, p.stream);
+  return e != cudaSuccess ? e : f;
+}
+
+cudaError_t read_and_clear_backward_status(unsigned int *value) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_bwd_status, sizeof(unsigned int));
+  if (e == cudaSuccess && *value) e = cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(unsigned int));
+  return e;
+}
+
+}  // namespace la

@@ -180,9 +180,11 @@ la_status la_device_status(void *stream) {
   unsigned int vf = 0;
   e = la::read_and_clear_device_status(&v);
   if (e == cudaSuccess) e = la::read_and_clear_global_tc_status(&vg);
+  unsigned int vb = 0;
   if (e == cudaSuccess) e = la::read_and_clear_favor_status(&vf);
+  if (e == cudaSuccess) e = la::read_and_clear_backward_status(&vb);
   if (e != cudaSuccess) return la::from_cuda(e);
-  v |= vg | vf;
+  v |= vg | vf | vb;
   if (v & 1u) return LA_ERR_TIMEOUT;
   return v ? LA_ERR_LAUNCH : LA_OK;  // other bits: a kernel refused to run (e.g. misaligned shared memory)
 }
@@ -412,6 +414,7 @@ la_status la_causal_backward(const void *q, const void *k, const void *v, const 
   if (st != LA_OK) return st;
   la::BackwardProblem b{{q, k, v, nullptr, nullptr, nullptr, (int)BH, (long)N, d_k, d_v, eps, dt, (cudaStream_t)stream},
                         dout, S0, z0, dS, dz, dq, dk, dv, dS0, dz0};
+  if (la::backward_tc_supported(b.p)) return la::from_cuda(la::launch_causal_backward_tc(b));
   return la::from_cuda(la::launch_causal_backward(b));
 }
 
