@@ -118,6 +118,18 @@ __device__ __forceinline__ uint4 ld_row16(const void *p) {
   return r;
 }
 
+// 32-byte global load (read-only path) and store; the address must be 32-byte aligned.
+__device__ __forceinline__ void ld_row32(const void *p, uint32_t (&r)[8]) {
+  asm volatile("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st_row32(void *p, const uint32_t *r) {
+  asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]),
+               "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 // K-major operand over a [128 x 128] tile (rows of 64 K-elements per block).
 __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int ks) {
   return sw128_desc(tile + (ks >> 2) * kBlk + (ks & 3) * 32, 16, 1024);
@@ -179,14 +191,51 @@ struct BwdTcParams {
   float eps;
 };
 
+// phi pairs of a raw [128 x 128] bf16 tile in place: hi over the raw values,
+// lo into the matching chunks of `lo`.  Thread u (of 256) takes the 16-byte
+// chunks u + 256 i; chunk ch is row (ch mod 1024) / 8 of block ch / 1024 and
+// rows past the T valid ones become zeros.
+__device__ __forceinline__ void key_pairs(uint4 *hi, uint4 *lo, int u, int T) {
+#pragma unroll 4
+  for (int i = 0; i < 8; ++i) {
+    const int ch = u + 256 * i;
+    uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
+    if (((ch & 1023) >> 3) < T) phi_pair8(hi[ch], h, l);
+    hi[ch] = h;
+    lo[ch] = l;
+  }
+}
+
+// Column sums of the valid rows of a pair of [128 x 128] bf16 tiles (hi + lo)
+// over 128 threads: thread g takes the column pair 2 p, 2 p + 1 with
+// p = (g & 15) + 16 (g >> 5) over rows of one half ((g >> 4) & 1); the halves
+// meet through a shuffle and lanes 0-15 of each warp hold the pair's sums.
+__device__ __forceinline__ float2 pair_column_sums(const uint8_t *hi, const uint8_t *lo, int g, int T) {
+  const int p = (g & 15) + 16 * (g >> 5), half = (g >> 4) & 1;
+  const int col = 2 * p;
+  const uint32_t boff = (col >> 6) * kBlk;
+  float2 s = make_float2(0.f, 0.f);
+  const int r0 = 64 * half, r1 = min(T, r0 + 64);
+#pragma unroll 8
+  for (int j = r0; j < r1; ++j) {
+    const uint32_t off = boff + sw128_offset(j, col & 63);
+    const uint32_t a = *reinterpret_cast<const uint32_t *>(hi + off), b = *reinterpret_cast<const uint32_t *>(lo + off);
+    s = __fadd2_rn(s, __fadd2_rn(make_float2(lo16(a), hi16(a)), make_float2(lo16(b), hi16(b))));
+  }
+  s.x += __shfl_xor_sync(0xffffffffu, s.x, 16);
+  s.y += __shfl_xor_sync(0xffffffffu, s.y, 16);
+  return s;
+}
+
 // Shared-memory layout of pass 1: seven [128 x 128] bf16 tiles (224 KB), then
 // two z buffers, the chunk's phi(q).z, barriers.
 struct P1Layout {
   static constexpr uint32_t Khi = 0, Klo = kTile, V = 2 * kTile, Ghi = 3 * kTile, Glo = 4 * kTile, Shi = 5 * kTile,
                             Slo = 6 * kTile;
   static constexpr uint32_t Z = 7 * kTile;    // [2][128] z carried into the chunk
-  static constexpr uint32_t DenX = Z + 1024;  // [128] phi(q_t) . z_prev
-  static constexpr uint32_t Bars = DenX + 512;
+  static constexpr uint32_t DenX = Z + 1024;    // [128] phi(q_t) . z_prev
+  static constexpr uint32_t Kcol = DenX + 512;  // [2][128] column sums of the chunk's phi(K)
+  static constexpr uint32_t Bars = Kcol + 1024;
   static constexpr int kNumBars = 18;
   static constexpr uint32_t Misc = Bars + kNumBars * 8;
   static constexpr uint32_t Bytes = Misc + 16;
@@ -198,9 +247,9 @@ static_assert(P1Layout::Bytes <= 232448, "pass 1 shared memory");
 constexpr uint32_t kP1S = 0, kP1X = 128, kP1CB = 256, kP1Q = 384;
 
 // Warp roles of pass 1 (13 warps): 0 MMA issuer and tensor-memory owner; 1-4
-// keys (TMA, phi pairs in place), queries (phi pairs into tensor memory) and
-// copies of the state; 5-8 dO pairs (and V by TMA); 9-12 scores, key column
-// sums and dq.
+// keys (TMA; half of the phi pairs in place), queries (phi pairs into tensor
+// memory) and copies of the state; 5-8 dO pairs (and V by TMA), the other half
+// of the key pairs, key column sums; 9-12 scores and dq.
 constexpr int kP1Threads = 416;
 constexpr int kP1WarpG = 5, kP1WarpE = 9;
 constexpr uint32_t kBarQK = 1, kBarG = 2, kBarE = 3;
@@ -215,11 +264,12 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
   uint8_t *sm = smem_raw;
   float *zbuf = reinterpret_cast<float *>(sm + L::Z);
   float *den_x = reinterpret_cast<float *>(sm + L::DenX);
+  float *kcol = reinterpret_cast<float *>(sm + L::Kcol);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::Bars);
   uint64_t *q_ready = bars + 0, *k_ready = bars + 1, *g_ready = bars + 2, *s_ready = bars + 3, *ac_full = bars + 4,
            *x_free = bars + 5, *y_full = bars + 6, *cb_ready = bars + 7, *d_full = bars + 8, *e3_done = bars + 9,
            *drain = bars + 10, *z_full = bars + 11 /* [2] */, *z_empty = bars + 13 /* [2] */, *k_full = bars + 15,
-           *v_full = bars + 16;
+           *v_full = bars + 16, *kc_ready = bars + 17;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::Misc);
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + L::Misc + 4);
   unsigned int *status = &g_bwd_status;
@@ -233,7 +283,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
 
   if (threadIdx.x == 0) {
     mbar_init(q_ready, 128);
-    mbar_init(k_ready, 128);
+    mbar_init(k_ready, 256);  // both halves of the key pairs
     mbar_init(g_ready, 128);
     mbar_init(s_ready, 128);
     mbar_init(ac_full, 1);
@@ -249,6 +299,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
     }
     mbar_init(k_full, 1);
     mbar_init(v_full, 1);
+    mbar_init(kc_ready, 128);
     *abort_word = 0;
     fence_barrier_init();
   }
@@ -383,22 +434,20 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       // this row's queries, loaded while the keys are transformed
       uint4 x[16];
       if (r < T) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(qh + (t0 + r) * kD);
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(qh + (t0 + r) * kD);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] = ld_row16(src + e);
+        for (int e = 0; e < 8; ++e) {
+          uint32_t w[8];
+          ld_row32(src + 32 * e, w);
+          x[2 * e] = make_uint4(w[0], w[1], w[2], w[3]);
+          x[2 * e + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
       }
-      // keys: the raw tile has landed; phi pairs in place (hi) and into Klo (lo).  The 16-byte
-      // chunk ch of the tile is row (ch mod 1024) / 8 of block ch / 1024; rows past the end are zeros
+      // keys: the raw tile has landed; phi pairs in place (hi) and into Klo (lo), this half of
+      // the chunks (the G warps take the other)
       ok = wait(k_full, c & 1);
       if (bar_or(kBarQK, 128, !ok)) break;
-#pragma unroll 2
-      for (int i = 0; i < 16; ++i) {
-        const int ch = tid + 128 * i;
-        uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
-        if (((ch & 1023) >> 3) < T) phi_pair8(kt[ch], h, l);
-        kt[ch] = h;
-        lt[ch] = l;
-      }
+      key_pairs(kt, lt, tid, T);
       fence_async_smem();
       mbar_arrive(k_ready);
       // queries: phi pairs into tensor memory once the previous chunk's last reads are done
@@ -496,13 +545,27 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       }
       fence_async_smem();
       mbar_arrive(g_ready);
+      // the other half of this chunk's key pairs, then its key column sums (for the E warps' z)
+      bool okk = wait(k_full, c & 1);
+      if (bar_or(kBarG, 128, !okk)) break;
+      key_pairs(reinterpret_cast<uint4 *>(sm + L::Khi), reinterpret_cast<uint4 *>(sm + L::Klo), 128 + gt, T);
+      fence_async_smem();
+      mbar_arrive(k_ready);
+      okk = wait(k_ready, c & 1);  // both halves written
+      if (bar_or(kBarG, 128, !okk)) break;
+      const float2 cs = pair_column_sums(sm + L::Khi, sm + L::Klo, gt, T);
+      if (lane < 16) {
+        const int pc = 2 * ((gt & 15) + 16 * (gt >> 5));
+        kcol[(c & 1) * kD + pc] = cs.x;
+        kcol[(c & 1) * kD + pc + 1] = cs.y;
+      }
+      mbar_arrive(kc_ready);
     }
     if (gt == 0 && v_issued > 0) wait_drain(v_full, (v_issued - 1) & 1, status);
   } else {
     // ---------------- E warps: scores, den, gden, B', key column sums, dq ----------------
     const int t = (warp & 3) * 32 + lane;  // tensor-memory lane = chunk row; also feature t of z
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint8_t *Khi = sm + L::Khi, *Klo = sm + L::Klo;
     for (int c = 0; c < nch; ++c) {
       const long t0 = (long)c * kC;
       const int T = (int)min((long)kC, N - t0);
@@ -526,17 +589,6 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       const float den = (den_x[t] + rs) + p.eps;
       tc_fence_before();
       mbar_arrive(x_free);
-      // while Y is formed: column t of this chunk's phi(K) pairs, summed over its valid rows
-      float kc = 0.f;
-      {
-        const uint8_t *bh_ = Khi + (t >> 6) * kBlk, *bl_ = Klo + (t >> 6) * kBlk;
-#pragma unroll 4
-        for (int j = 0; j < T; ++j) {
-          const uint32_t off = sw128_offset(j, t & 63);
-          kc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(bh_ + off)) +
-                __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(bl_ + off));
-        }
-      }
       // E2: gden from phi(q) . Y, then B' = C + den gden in place as bf16 pairs
       ok = wait(y_full, c & 1);
       if (bar_or(kBarE, 128, !ok)) break;
@@ -554,11 +606,18 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       }
       const float gden = -((qy + ac) / den) / den;
       const float dg = den * gden;
+      // this chunk's key column sums (waited for here, before cb_ready, so that the G warps
+      // cannot complete the next chunk's before this wait)
+      ok = wait(kc_ready, c & 1);
+      if (bar_or(kBarE, 128, !ok)) break;
+      const float kc = kcol[(c & 1) * kD + t];
 #pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        tmem_ld32(tl + kP1CB + cb * 32, rc);
-        split_scores32(rc, cb, [&](int j) { return j <= jmax; }, [&](int, float x) { return x + dg; });
-        tmem_st32(tl + kP1CB + cb * 32, rc);
+      for (int cb = 0; cb < 4; cb += 2) {
+        tmem_ld32x2(tl + kP1CB + cb * 32, tl + kP1CB + cb * 32 + 32, ra, rc);
+        split_scores32(ra, cb, [&](int j) { return j <= jmax; }, [&](int, float x) { return x + dg; });
+        split_scores32(rc, cb + 1, [&](int j) { return j <= jmax; }, [&](int, float x) { return x + dg; });
+        tmem_st32(tl + kP1CB + cb * 32, ra);
+        tmem_st32(tl + kP1CB + cb * 32 + 32, rc);
       }
       tc_fence_before();
       mbar_arrive(cb_ready);
@@ -581,17 +640,15 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
               __float_as_uint(fmaf(__uint_as_float(ra[2 * m + 1]), inv, z[32 * b + 2 * m + 1] * gden) * f1);
         }
         if (t < T) {
-          float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * b);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            d4[e] = make_float4(__uint_as_float(ra[4 * e]), __uint_as_float(ra[4 * e + 1]),
-                                __uint_as_float(ra[4 * e + 2]), __uint_as_float(ra[4 * e + 3]));
+          for (int e = 0; e < 4; ++e) st_row32(dst + 32 * b + 8 * e, ra + 8 * e);
         }
       }
       if (t < T) {
         p.den[(long)bh * N + t0 + t] = den;
         p.gden[(long)bh * N + t0 + t] = gden;
       }
+
       // z for the next chunk: z_prev plus this chunk's key column sums (thread t owns feature t)
       named_bar(kBarE, 128);  // every read of this chunk's z is done
       if (c + 1 < nch) {
@@ -671,7 +728,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
   const float *gh = p.dout + (long)bh * N * kD;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_ready, 128);
+    mbar_init(q_ready, 256);  // both halves of the query pairs
     mbar_init(k_ready, 128);
     mbar_init(n_ready, 128);
     mbar_init(u_ready, 128);
@@ -872,17 +929,11 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           }
         }
       }
-      // queries: the raw tile has landed; phi pairs in place (hi) and into Qlo (lo)
+      // queries: the raw tile has landed; phi pairs in place (hi) and into Qlo (lo), this half of
+      // the chunks (the N warps take the other)
       ok = wait(q_full, it & 1);
       if (bar_or(kBarQK, 128, !ok)) break;
-#pragma unroll 2
-      for (int i = 0; i < 16; ++i) {
-        const int ch = tid + 128 * i;
-        uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
-        if (((ch & 1023) >> 3) < T) phi_pair8(qt[ch], h, l);
-        qt[ch] = h;
-        qlt[ch] = l;
-      }
+      key_pairs(qt, qlt, tid, T);
       fence_async_smem();
       mbar_arrive(q_ready);
       mbar_arrive(u_ready);
@@ -949,6 +1000,12 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       gd[myrow] = gdn;
       fence_async_smem();
       mbar_arrive(n_ready);
+      // the other half of this chunk's query pairs
+      const bool okq = wait(q_full, it & 1);
+      if (bar_or(kBarG, 128, !okq)) break;
+      key_pairs(reinterpret_cast<uint4 *>(sm + L::Qhi), reinterpret_cast<uint4 *>(sm + L::Qlo), 128 + gt, T);
+      fence_async_smem();
+      mbar_arrive(q_ready);
     }
   } else {
     // ---------------- E warps: key-side scores as pairs, then dv or dk ----------------
@@ -999,7 +1056,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       if (bar_or(kBarE, 128, !ok)) break;
       tc_fence_after();
       float *dst = (kDk ? p.dk : p.dv) + ((long)bh * N + t0 + j) * kD;
-      const uint4 *kr = reinterpret_cast<const uint4 *>(kh + (t0 + j) * kD);
+      const uint8_t *kr = reinterpret_cast<const uint8_t *>(kh + (t0 + j) * kD);
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
         uint32_t ro[32];
@@ -1007,25 +1064,22 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         if (kDk) {
           // dk = (V U^T + B Q + u) phi'(k), phi'(x) = 1 above zero, e^x below
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint4 kx = j < T ? __ldg(kr + 4 * b + e) : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t w4[4] = {kx.x, kx.y, kx.z, kx.w};
+          for (int e = 0; e < 2; ++e) {
+            uint32_t w8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            if (j < T) ld_row32(kr + 64 * b + 32 * e, w8);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int col = 32 * b + 8 * e + 2 * m;
-              const float2 f = phi2(lo16(w4[m]), hi16(w4[m]));
+            for (int m = 0; m < 8; ++m) {
+              const int col = 32 * b + 16 * e + 2 * m;
+              const float2 f = phi2(lo16(w8[m]), hi16(w8[m]));
               const float da = fminf(f.x, 1.f), db = fminf(f.y, 1.f);
-              ro[8 * e + 2 * m] = __float_as_uint((__uint_as_float(ro[8 * e + 2 * m]) + ub[col]) * da);
-              ro[8 * e + 2 * m + 1] = __float_as_uint((__uint_as_float(ro[8 * e + 2 * m + 1]) + ub[col + 1]) * db);
+              ro[16 * e + 2 * m] = __float_as_uint((__uint_as_float(ro[16 * e + 2 * m]) + ub[col]) * da);
+              ro[16 * e + 2 * m + 1] = __float_as_uint((__uint_as_float(ro[16 * e + 2 * m + 1]) + ub[col + 1]) * db);
             }
           }
         }
         if (j < T) {
-          float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * b);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            d4[e] = make_float4(__uint_as_float(ro[4 * e]), __uint_as_float(ro[4 * e + 1]),
-                                __uint_as_float(ro[4 * e + 2]), __uint_as_float(ro[4 * e + 3]));
+          for (int e = 0; e < 4; ++e) st_row32(dst + 32 * b + 8 * e, ro + 8 * e);
         }
       }
       if (kDk) {
@@ -1072,8 +1126,13 @@ bool make_bf16_map(CUtensorMap *m, const void *base, long BH, long N) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool backward_tc_supported(const Problem &p) {
+bool backward_tc_supported(const BackwardProblem &b) {
+  const Problem &p = b.p;
   const DeviceInfo di = device_info(-1);
+  // rows are read and written 32 bytes at a time
+  const void *rows[5] = {p.q, p.k, b.dq, b.dk, b.dv};
+  for (const void *r : rows)
+    if (reinterpret_cast<uintptr_t>(r) & 31u) return false;
   return p.dt == LA_BF16 && p.dk == kD && p.dv == kD && p.N >= 1 && p.N <= 0x7fffffffL && p.BH <= 65535 &&
          di.cc_major == 10 && di.cc_minor == 3 && tensor_map_encoder() != nullptr;
 }

@@ -31,8 +31,9 @@ struct BackwardProblem {
   float *dq, *dk, *dv, *dS0, *dz0;
 };
 cudaError_t launch_causal_backward(const BackwardProblem &b);
-// The same gradient on the tensor cores (bf16 inputs, d_k = d_v = 128, N >= 1, sm_103).
-bool backward_tc_supported(const Problem &p);
+// The same gradient on the tensor cores (bf16 inputs, d_k = d_v = 128, N >= 1, sm_103,
+// q, k, dq, dk, dv 32-byte aligned).
+bool backward_tc_supported(const BackwardProblem &b);
 cudaError_t launch_causal_backward_tc(const BackwardProblem &b);
 cudaError_t read_and_clear_backward_status(unsigned int *value);
 

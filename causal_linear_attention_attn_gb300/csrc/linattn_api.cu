@@ -414,7 +414,7 @@ la_status la_causal_backward(const void *q, const void *k, const void *v, const 
   if (st != LA_OK) return st;
   la::BackwardProblem b{{q, k, v, nullptr, nullptr, nullptr, (int)BH, (long)N, d_k, d_v, eps, dt, (cudaStream_t)stream},
                         dout, S0, z0, dS, dz, dq, dk, dv, dS0, dz0};
-  if (la::backward_tc_supported(b.p)) return la::from_cuda(la::launch_causal_backward_tc(b));
+  if (la::backward_tc_supported(b)) return la::from_cuda(la::launch_causal_backward_tc(b));
   return la::from_cuda(la::launch_causal_backward(b));
 }
 

@@ -173,3 +173,28 @@ def test_backward_edge_cases(cuda_lib):
     for g in L.la_causal_backward(q, k, v, z):
         assert torch.count_nonzero(g) == 0
     assert L.device_status() == 0
+
+
+def test_backward_rows_not_32_byte_aligned(cuda_lib):
+    """The tensor-core kernel moves rows 32 bytes at a time; inputs that are only
+    16-byte aligned (what the ABI asks for) take the CUDA-core kernel instead and
+    still match the oracle."""
+    w = inputs.WORKLOADS["causal_bf16"]
+    B, H, N = 1, 2, 300
+    q, k, v = inputs.make_qkv(w, N=N, B=B, H=H)
+    dO = _grad_in((B, H, N, 128), 21)
+
+    def shifted(t):  # the same values at an address 16 bytes past a 32-byte boundary
+        n = t.numel()
+        pad = 16 // t.element_size()
+        buf = torch.empty(n + pad, dtype=t.dtype, device=DEV)
+        out = buf[pad:].view(t.shape)
+        out.copy_(t.to(DEV))
+        assert out.data_ptr() % 32 == 16
+        return out
+
+    dq, dkk, dvv = cuda_lib.la_causal_backward(shifted(q), shifted(k), v.to(DEV), dO.to(DEV), eps=w.eps)
+    torch.cuda.synchronize()
+    r = oracle.causal_backward(f64(q), f64(k), f64(v), f64(dO), eps=w.eps, nthreads=2)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dkk, dvv), r):
+        assert_close(got, ref, TAU[torch.bfloat16], name)
