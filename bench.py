@@ -519,6 +519,20 @@ def alu_roofline(flops: float, ms: float) -> dict:
             "peak_source": "152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz", "alg_flops_per_call": flops}
 
 
+def tensor_roofline(flops: float, ms: float) -> dict:
+    """Algorithmic FLOPs per call against the measured dense bf16 tensor peak."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak, srcp = 1900.0, "fallback 1.9 PFLOP/s"
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        if m.get("bf16_tflops"):
+            peak, srcp = float(m["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "peak_source": srcp, "alg_flops_per_call": flops}
+
+
 def run_backward(L, w, steps, warmup, world, stream, hbm, src):
     """Gradient of the causal prefill (la_causal_backward) for a seeded upstream gradient."""
     q, k, v = (t.cuda() for t in inputs.make_qkv(w, device="cuda"))
@@ -531,10 +545,18 @@ def run_backward(L, w, steps, warmup, world, stream, hbm, src):
     launches = (L.kernel_launches() - n0) // (2 * steps + warmup) * steps
     ms = max_over_ranks(ms, world, "cuda" if world > 1 else None)
     rl, table = dominant_roofline(L, w, steps, hbm, src, w.name + "_backward")
-    return {"workload": w.name + " backward", "roofline": rl, "tokens_per_s": world * w.BH * w.N / (ms * 1e-3), "ms_per_call": ms,
-            "step_roofline": roofline(backward_bytes(w), ms, hbm, src, None),
-            "alu_roofline": alu_roofline(backward_flops(w), ms), "kernels": table,
-            "gpu_launches": launches, "note": "exact fp32 CUDA-core kernel, each head cut into segments"}
+    tc = w.dtype == "bf16" and w.dk == w.dv == 128
+    res = {"workload": w.name + " backward", "roofline": rl, "tokens_per_s": world * w.BH * w.N / (ms * 1e-3),
+           "ms_per_call": ms, "step_roofline": roofline(backward_bytes(w), ms, hbm, src, None), "kernels": table,
+           "gpu_launches": launches}
+    if tc:
+        res["tensor_roofline"] = tensor_roofline(backward_flops(w, chunk=128), ms)
+        res["note"] = ("tcgen05 kernels, 128-token chunks, bf16 hi/lo operand pairs (about 3x the algorithmic "
+                       "tensor work issued); pass 1 in order, pass 2 in reverse with dv and dk roles")
+    else:
+        res["alu_roofline"] = alu_roofline(backward_flops(w), ms)
+        res["note"] = "exact fp32 CUDA-core kernel, each head cut into segments"
+    return res
 
 
 def retention_decode_bytes(w) -> float:

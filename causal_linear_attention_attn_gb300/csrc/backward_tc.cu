@@ -191,6 +191,23 @@ struct BwdTcParams {
   float eps;
 };
 
+// Features 64 h .. 64 h + 63 of a 128-element bf16 row, by four 32-byte loads.
+__device__ __forceinline__ void load_row_half(const __nv_bfloat16 *row, uint4 (&x)[8], int h = 0) {
+  const uint8_t *src = reinterpret_cast<const uint8_t *>(row) + 128 * h;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    uint32_t w[8];
+    ld_row32(src + 32 * e, w);
+    x[2 * e] = make_uint4(w[0], w[1], w[2], w[3]);
+    x[2 * e + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// phi pairs of features 64 h .. 64 h + 63 of this lane's query row into the
+// tensor-memory phi(Q) columns (hi at kP1Q + 32 h .., lo at kP1Q + 64 + 32 h ..;
+// zeros for an invalid row); returns their part of phi(q) . z.
+__device__ __forceinline__ float query_pairs_half(const uint4 (&x)[8], bool valid, const float *z, uint32_t tl, int h);
+
 // phi pairs of a raw [128 x 128] bf16 tile in place: hi over the raw values,
 // lo into the matching chunks of `lo`.  Thread u (of 256) takes the 16-byte
 // chunks u + 256 i; chunk ch is row (ch mod 1024) / 8 of block ch / 1024 and
@@ -233,9 +250,9 @@ struct P1Layout {
   static constexpr uint32_t Khi = 0, Klo = kTile, V = 2 * kTile, Ghi = 3 * kTile, Glo = 4 * kTile, Shi = 5 * kTile,
                             Slo = 6 * kTile;
   static constexpr uint32_t Z = 7 * kTile;    // [2][128] z carried into the chunk
-  static constexpr uint32_t DenX = Z + 1024;    // [128] phi(q_t) . z_prev
-  static constexpr uint32_t Kcol = DenX + 512;  // [2][128] column sums of the chunk's phi(K)
-  static constexpr uint32_t Bars = Kcol + 1024;
+  static constexpr uint32_t DenX = Z + 1024;     // [2][128] phi(q_t) . z_prev over features 0-63, 64-127
+  static constexpr uint32_t Kcol = DenX + 1024;  // [128] column sums of the chunk's phi(K)
+  static constexpr uint32_t Bars = Kcol + 512;
   static constexpr int kNumBars = 18;
   static constexpr uint32_t Misc = Bars + kNumBars * 8;
   static constexpr uint32_t Bytes = Misc + 16;
@@ -247,12 +264,32 @@ static_assert(P1Layout::Bytes <= 232448, "pass 1 shared memory");
 constexpr uint32_t kP1S = 0, kP1X = 128, kP1CB = 256, kP1Q = 384;
 
 // Warp roles of pass 1 (13 warps): 0 MMA issuer and tensor-memory owner; 1-4
-// keys (TMA; half of the phi pairs in place), queries (phi pairs into tensor
-// memory) and copies of the state; 5-8 dO pairs (and V by TMA), the other half
-// of the key pairs, key column sums; 9-12 scores and dq.
+// keys (TMA; half of the phi pairs in place), queries 0-63 (phi pairs into
+// tensor memory) and copies of the state; 5-8 dO pairs (and V by TMA), the
+// other half of the key pairs, key column sums, queries 64-127; 9-12 scores
+// and dq.
 constexpr int kP1Threads = 416;
 constexpr int kP1WarpG = 5, kP1WarpE = 9;
 constexpr uint32_t kBarQK = 1, kBarG = 2, kBarE = 3;
+
+__device__ __forceinline__ float query_pairs_half(const uint4 (&x)[8], bool valid, const float *z, uint32_t tl, int h) {
+  float dot = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+    float vv[8];
+    if (valid) {
+      phi_split8(x[e], hw, lw, vv);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) dot = fmaf(vv[m], z[64 * h + 8 * e + m], dot);
+    }
+    // features 64 h + 8 e .. + 7: pair columns 32 h + 4 e .. + 3 (hi), 64 + 32 h + 4 e .. (lo)
+    tmem_st4_nowait(tl + kP1Q + 32 * h + 4 * e, hw[0], hw[1], hw[2], hw[3]);
+    tmem_st4_nowait(tl + kP1Q + 64 + 32 * h + 4 * e, lw[0], lw[1], lw[2], lw[3]);
+  }
+  tmem_wait_st();
+  return dot;
+}
 
 __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_constant__ BwdTcParams p) {
   using L = P1Layout;
@@ -282,7 +319,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
   const float *gh = p.dout + (long)bh * N * kD;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_ready, 128);
+    mbar_init(q_ready, 256);  // both halves of the query pairs
     mbar_init(k_ready, 256);  // both halves of the key pairs
     mbar_init(g_ready, 128);
     mbar_init(s_ready, 128);
@@ -295,7 +332,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
     mbar_init(drain, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&z_full[b], 128);
-      mbar_init(&z_empty[b], 128);
+      mbar_init(&z_empty[b], 256);  // read by both query halves
     }
     mbar_init(k_full, 1);
     mbar_init(v_full, 1);
@@ -431,18 +468,9 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
     for (int c = 0; c < nch; ++c) {
       const long t0 = (long)c * kC;
       const int T = (int)min((long)kC, N - t0);
-      // this row's queries, loaded while the keys are transformed
-      uint4 x[16];
-      if (r < T) {
-        const uint8_t *src = reinterpret_cast<const uint8_t *>(qh + (t0 + r) * kD);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          uint32_t w[8];
-          ld_row32(src + 32 * e, w);
-          x[2 * e] = make_uint4(w[0], w[1], w[2], w[3]);
-          x[2 * e + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-      }
+      // this row's queries 0-63, loaded while the keys are transformed
+      uint4 x[8];
+      if (r < T) load_row_half(qh + (t0 + r) * kD, x);
       // keys: the raw tile has landed; phi pairs in place (hi) and into Klo (lo), this half of
       // the chunks (the G warps take the other)
       ok = wait(k_full, c & 1);
@@ -455,23 +483,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       ok = ok && wait(&z_full[c & 1], (c >> 1) & 1);
       if (bar_or(kBarQK, 128, !ok)) break;
       tc_fence_after();
-      const float *z = zbuf + (c & 1) * kD;
-      float dot = 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        uint32_t h[4] = {0u, 0u, 0u, 0u}, l[4] = {0u, 0u, 0u, 0u};
-        float vv[8];
-        if (r < T) {
-          phi_split8(x[e], h, l, vv);
-#pragma unroll
-          for (int m = 0; m < 8; ++m) dot = fmaf(vv[m], z[8 * e + m], dot);
-        }
-        // features 8e .. 8e + 7: pair columns 4e .. 4e + 3 (hi) and 64 + 4e .. (lo)
-        tmem_st4_nowait(tl + kP1Q + 4 * e, h[0], h[1], h[2], h[3]);
-        tmem_st4_nowait(tl + kP1Q + 64 + 4 * e, l[0], l[1], l[2], l[3]);
-      }
-      tmem_wait_st();
-      den_x[r] = dot;
+      den_x[r] = query_pairs_half(x, r < T, zbuf + (c & 1) * kD, tl, 0);
       mbar_arrive(&z_empty[c & 1]);
       tc_fence_before();
       mbar_arrive(q_ready);
@@ -551,13 +563,28 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       key_pairs(reinterpret_cast<uint4 *>(sm + L::Khi), reinterpret_cast<uint4 *>(sm + L::Klo), 128 + gt, T);
       fence_async_smem();
       mbar_arrive(k_ready);
-      okk = wait(k_ready, c & 1);  // both halves written
+      // queries 64-127 of row r (this warp's tensor-memory lanes) once the previous chunk's last
+      // reads of the phi(Q) columns are done
+      const int r = (warp & 3) * 32 + lane;
+      const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      uint4 x[8];
+      if (r < T) load_row_half(qh + (t0 + r) * kD, x, 1);
+      okk = c == 0 || wait(e3_done, (c - 1) & 1);
+      okk = okk && wait(&z_full[c & 1], (c >> 1) & 1);
+      if (bar_or(kBarG, 128, !okk)) break;
+      tc_fence_after();
+      den_x[kD + r] = query_pairs_half(x, r < T, zbuf + (c & 1) * kD, tl, 1);
+      mbar_arrive(&z_empty[c & 1]);
+      tc_fence_before();
+      mbar_arrive(q_ready);
+      // this chunk's key column sums, for the E warps' z (both halves of the pairs are written)
+      okk = wait(k_ready, c & 1);
       if (bar_or(kBarG, 128, !okk)) break;
       const float2 cs = pair_column_sums(sm + L::Khi, sm + L::Klo, gt, T);
       if (lane < 16) {
         const int pc = 2 * ((gt & 15) + 16 * (gt >> 5));
-        kcol[(c & 1) * kD + pc] = cs.x;
-        kcol[(c & 1) * kD + pc + 1] = cs.y;
+        kcol[pc] = cs.x;
+        kcol[pc + 1] = cs.y;
       }
       mbar_arrive(kc_ready);
     }
@@ -586,7 +613,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
           ac = fmaf(a, __uint_as_float(rc[m]), ac);
         }
       }
-      const float den = (den_x[t] + rs) + p.eps;
+      const float den = ((den_x[t] + den_x[kD + t]) + rs) + p.eps;
       tc_fence_before();
       mbar_arrive(x_free);
       // E2: gden from phi(q) . Y, then B' = C + den gden in place as bf16 pairs
@@ -610,7 +637,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       // cannot complete the next chunk's before this wait)
       ok = wait(kc_ready, c & 1);
       if (bar_or(kBarE, 128, !ok)) break;
-      const float kc = kcol[(c & 1) * kD + t];
+      const float kc = kcol[t];
 #pragma unroll 1
       for (int cb = 0; cb < 4; cb += 2) {
         tmem_ld32x2(tl + kP1CB + cb * 32, tl + kP1CB + cb * 32 + 32, ra, rc);
@@ -675,8 +702,8 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
 // Pass 2: chunks in reverse, U (and u) carried; role 0 dv, role 1 dk.
 // ---------------------------------------------------------------------------
 // Shared memory: phi(Q), gnum and the copy of U as bf16 pairs (six tiles,
-// 192 KB), a staging tile for the raw key operand (32 KB), the chunk's gden,
-// the carried u (role 1), barriers.
+// 192 KB), a staging tile for the next chunk's raw queries (32 KB), the
+// chunk's gden, the carried u (role 1), barriers.
 struct P2Layout {
   static constexpr uint32_t Qhi = 0, Qlo = kTile, Nhi = 2 * kTile, Nlo = 3 * kTile, Uhi = 4 * kTile, Ulo = 5 * kTile,
                             Kst = 6 * kTile;
@@ -694,11 +721,26 @@ static_assert(P2Layout::Bytes <= 232448, "pass 2 shared memory");
 // (role 0: phi(K) as pairs, 128 columns; role 1: V, 64 columns).
 constexpr uint32_t kP2U = 0, kP2X = 128, kP2O = 256, kP2K = 384;
 
-// Warp roles of pass 2 (13 warps): 0 MMA issuer; 1-4 key operand and phi(Q)
-// pairs (both staged by TMA), copies of U; 5-8 gnum pairs (coalesced rows) and
-// gden; 9-12 scores and outputs.
+// Warp roles of pass 2 (13 warps): 0 MMA issuer; 1-4 key operand (rows into
+// tensor memory), copies of U; 5-8 gnum pairs (coalesced rows), gden and the
+// phi(Q) pairs from the staged raw queries; 9-12 scores and outputs.
 constexpr int kP2Threads = 416;
 constexpr int kP2WarpN = 5, kP2WarpE = 9;
+
+// phi pairs of the staged raw query tile into the Q tiles (same swizzled
+// layout): thread u of 256 takes chunks u + 256 i; rows past T are zeros.
+__device__ __forceinline__ void query_pairs_staged(uint8_t *sm, int u, int T) {
+  const uint4 *raw = reinterpret_cast<const uint4 *>(sm + P2Layout::Kst);
+  uint4 *hi = reinterpret_cast<uint4 *>(sm + P2Layout::Qhi), *lo = reinterpret_cast<uint4 *>(sm + P2Layout::Qlo);
+#pragma unroll 4
+  for (int i = 0; i < 8; ++i) {
+    const int ch = u + 256 * i;
+    uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
+    if (((ch & 1023) >> 3) < T) phi_pair8(raw[ch], h, l);
+    hi[ch] = h;
+    lo[ch] = l;
+  }
+}
 
 template <int kRole>
 __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
@@ -714,8 +756,8 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
   float *ub = reinterpret_cast<float *>(sm + L::Ub);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::Bars);
   uint64_t *q_ready = bars + 0, *k_ready = bars + 1, *n_ready = bars + 2, *u_ready = bars + 3, *x_full = bars + 4,
-           *x_split = bars + 5, *o_full = bars + 6, *o_done = bars + 7, *drain = bars + 8, *kst_full = bars + 9,
-           *q_full = bars + 10;
+           *x_split = bars + 5, *o_full = bars + 6, *o_done = bars + 7, *drain = bars + 8, *q_full = bars + 9,
+           *q_used = bars + 10;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::Misc);
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + L::Misc + 4);
   unsigned int *status = &g_bwd_status;
@@ -737,8 +779,8 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
     mbar_init(o_full, 1);
     mbar_init(o_done, 128);
     mbar_init(drain, 1);
-    mbar_init(kst_full, 1);
     mbar_init(q_full, 1);
+    mbar_init(q_used, 256);
     *abort_word = 0;
     fence_barrier_init();
   }
@@ -831,31 +873,11 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       wait_drain(drain, 0, status);
     }
   } else if (warp < kP2WarpN) {
-    // ---------------- QK warps: key operand into tensor memory, phi(Q) pairs, copies of U ----------------
+    // ---------------- QK warps: key operand into tensor memory, copies of U ----------------
     const int r = (warp & 3) * 32 + lane;  // tensor-memory lane: chunk row, or state row of U
-    const int tid = threadIdx.x - 32;      // 0..127
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    uint8_t *Uhi = sm + L::Uhi, *Ulo = sm + L::Ulo, *Kst = sm + L::Kst;
-    uint4 *qt = reinterpret_cast<uint4 *>(sm + L::Qhi), *qlt = reinterpret_cast<uint4 *>(sm + L::Qlo);
-    const CUtensorMap *tkey = kDk ? &p.tv : &p.tk;
-    int kst_issued = 0, q_issued = 0;
-    auto load_key = [&](int c) {  // raw key operand rows of chunk c into the staging tile
-      mbar_arrive_expect_tx(kst_full, kTile);
-      tma_load_3d(Kst, tkey, kst_full, 0, c * kC, bh);
-      tma_load_3d(Kst + kBlk, tkey, kst_full, 64, c * kC, bh);
-      ++kst_issued;
-    };
-    auto load_q = [&](int c) {  // raw queries of chunk c into the Qhi tile
-      mbar_arrive_expect_tx(q_full, kTile);
-      tma_load_3d(sm + L::Qhi, &p.tq, q_full, 0, c * kC, bh);
-      tma_load_3d(sm + L::Qhi + kBlk, &p.tq, q_full, 64, c * kC, bh);
-      ++q_issued;
-    };
-    if (tid == 0) {
-      prefetch_tmap(tkey);
-      prefetch_tmap(&p.tq);
-      load_key(nch - 1);
-    }
+    uint8_t *Uhi = sm + L::Uhi, *Ulo = sm + L::Ulo;
+    const __nv_bfloat16 *key = kDk ? vh : kh;
     {
       // U at the end of the sequence: dS (or zero) into tensor memory and its pair copy
       for (int cb = 0; cb < 8; ++cb) {
@@ -888,31 +910,32 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       const int c = nch - 1 - it;
       const long t0 = (long)c * kC;
       const int T = (int)min((long)kC, N - t0);
+      // this row of the key operand, loaded while the previous chunk's products finish
+      uint4 x[16];
+      if (r < T) {
+        load_row_half(key + (t0 + r) * kD, *reinterpret_cast<uint4 (*)[8]>(&x[0]), 0);
+        load_row_half(key + (t0 + r) * kD, *reinterpret_cast<uint4 (*)[8]>(&x[8]), 1);
+      }
       ok = it == 0 || wait(o_full, (it - 1) & 1);
       if (bar_or(kBarQK, 128, !ok)) break;
       tc_fence_after();
-      if (tid == 0) load_q(c);  // the Q tiles are free: the previous chunk's products have completed
-      // key operand from the staging tile, row r: role 0 phi(k) pairs (hi columns 0-63, lo
-      // 64-127), role 1 v as given; rows past the end are zeros
-      ok = wait(kst_full, it & 1);
-      if (bar_or(kBarQK, 128, !ok)) break;
+      // key operand, row r: role 0 phi(k) pairs (hi columns 0-63, lo 64-127), role 1 v as given;
+      // rows past the end are zeros
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const uint4 x = r < T ? *tile_chunk(Kst, r, 8 * e) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 xe = r < T ? x[e] : make_uint4(0u, 0u, 0u, 0u);
         if (!kDk) {
           uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
-          if (r < T) phi_pair8(x, h, l);
+          if (r < T) phi_pair8(xe, h, l);
           tmem_st4_nowait(tl + kP2K + 4 * e, h.x, h.y, h.z, h.w);
           tmem_st4_nowait(tl + kP2K + 64 + 4 * e, l.x, l.y, l.z, l.w);
         } else {
-          tmem_st4_nowait(tl + kP2K + 4 * e, x.x, x.y, x.z, x.w);
+          tmem_st4_nowait(tl + kP2K + 4 * e, xe.x, xe.y, xe.z, xe.w);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(k_ready);
-      named_bar(kBarQK, 128);  // every row has been read from the staging tile
-      if (tid == 0 && c > 0) load_key(c - 1);
       if (it > 0) {
         // the pair copy of U (every chunk after this one folded in); the tiles were last read by
         // the previous chunk's products, which have completed
@@ -929,18 +952,15 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           }
         }
       }
-      // queries: the raw tile has landed; phi pairs in place (hi) and into Qlo (lo), this half of
-      // the chunks (the N warps take the other)
+      fence_async_smem();
+      mbar_arrive(u_ready);
+      // half of the phi(Q) pairs from the staged raw queries (the N warps take the other half)
       ok = wait(q_full, it & 1);
       if (bar_or(kBarQK, 128, !ok)) break;
-      key_pairs(qt, qlt, tid, T);
+      query_pairs_staged(sm, threadIdx.x - 32, T);
       fence_async_smem();
       mbar_arrive(q_ready);
-      mbar_arrive(u_ready);
-    }
-    if (tid == 0) {
-      if (kst_issued > 0) wait_drain(kst_full, (kst_issued - 1) & 1, status);
-      if (q_issued > 0) wait_drain(q_full, (q_issued - 1) & 1, status);
+      mbar_arrive(q_used);  // this half is done with the staging tile
     }
     // role 0: the initial state's gradient dS0 = U after the first chunk
     if (!kDk && p.dS0) {
@@ -960,12 +980,23 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       }
     }
   } else if (warp < kP2WarpE) {
-    // ---------------- N warps: gnum = dO / den as pairs (coalesced rows), gden ----------------
+    // ---------------- N warps: gnum = dO / den as pairs (coalesced rows), gden, phi(Q) pairs ----------------
     const int gt = threadIdx.x - kP2WarpN * 32;  // 0..127
     const int wg = gt >> 5;                       // rows 32 wg .. 32 wg + 31
     uint8_t *Nhi = sm + L::Nhi, *Nlo = sm + L::Nlo;
     const int col = 4 * lane;
     const uint32_t off = (col >> 6) * kBlk;
+    int q_issued = 0;
+    auto load_q = [&](int c) {  // raw queries of chunk c into the staging tile
+      mbar_arrive_expect_tx(q_full, kTile);
+      tma_load_3d(sm + L::Kst, &p.tq, q_full, 0, c * kC, bh);
+      tma_load_3d(sm + L::Kst + kBlk, &p.tq, q_full, 64, c * kC, bh);
+      ++q_issued;
+    };
+    if (gt == 0) {
+      prefetch_tmap(&p.tq);
+      load_q(nch - 1);
+    }
     for (int it = 0; it < nch; ++it) {
       const int c = nch - 1 - it;
       const long t0 = (long)c * kC;
@@ -974,7 +1005,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       const int myrow = 32 * wg + lane;
       const float inv_mine = myrow < T ? 1.f / p.den[(long)bh * N + t0 + myrow] : 0.f;
       const float gdn = myrow < T ? p.gden[(long)bh * N + t0 + myrow] : 0.f;
-      const bool ok = it == 0 || wait(o_full, (it - 1) & 1);
+      bool ok = it == 0 || wait(o_full, (it - 1) & 1);
       if (bar_or(kBarG, 128, !ok)) break;
 #pragma unroll 1
       for (int rr = 0; rr < 32; rr += 8) {
@@ -1000,13 +1031,21 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       gd[myrow] = gdn;
       fence_async_smem();
       mbar_arrive(n_ready);
-      // the other half of this chunk's query pairs
-      const bool okq = wait(q_full, it & 1);
-      if (bar_or(kBarG, 128, !okq)) break;
-      key_pairs(reinterpret_cast<uint4 *>(sm + L::Qhi), reinterpret_cast<uint4 *>(sm + L::Qlo), 128 + gt, T);
+      // phi(Q) pairs from the staged raw queries (same swizzled layout), then the next chunk's
+      // raw queries into the staging tile
+      ok = wait(q_full, it & 1);
+      if (bar_or(kBarG, 128, !ok)) break;
+      query_pairs_staged(sm, 128 + gt, T);
       fence_async_smem();
       mbar_arrive(q_ready);
+      mbar_arrive(q_used);
+      // the next chunk's raw queries once both halves are done with the staging tile
+      bool okq = true;
+      if (gt == 0 && c > 0) okq = wait(q_used, it & 1);
+      if (bar_or(kBarG, 128, !okq)) break;
+      if (gt == 0 && c > 0) load_q(c - 1);
     }
+    if (gt == 0 && q_issued > 0) wait_drain(q_full, (q_issued - 1) & 1, status);
   } else {
     // ---------------- E warps: key-side scores as pairs, then dv or dk ----------------
     const int j = (warp & 3) * 32 + lane;  // tensor-memory lane = key row (or feature, for u)
