@@ -536,16 +536,16 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       const int col = 4 * lane;
       const uint32_t off = (col >> 6) * kBlk;
 #pragma unroll 1
-      for (int rr = 0; rr < 32; rr += 8) {
-        float4 gg[8];
+      for (int rr = 0; rr < 32; rr += 16) {  // two rounds of 16 rows in flight
+        float4 gg[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 16; ++e) {
           const int row = 32 * wg + rr + e;
           gg[e] = row < T ? __ldg(reinterpret_cast<const float4 *>(gh + (t0 + row) * kD + col))
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 16; ++e) {
           const int row = 32 * wg + rr + e;
           uint32_t h0, l0, h1, l1;
           split2(gg[e].x, gg[e].y, h0, l0);
@@ -1008,16 +1008,16 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       bool ok = it == 0 || wait(o_full, (it - 1) & 1);
       if (bar_or(kBarG, 128, !ok)) break;
 #pragma unroll 1
-      for (int rr = 0; rr < 32; rr += 8) {
-        float4 gg[8];
+      for (int rr = 0; rr < 32; rr += 16) {  // two rounds of 16 rows in flight
+        float4 gg[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 16; ++e) {
           const int row = 32 * wg + rr + e;
           gg[e] = row < T ? __ldg(reinterpret_cast<const float4 *>(gh + (t0 + row) * kD + col))
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 16; ++e) {
           const int row = 32 * wg + rr + e;
           const float inv = __shfl_sync(0xffffffffu, inv_mine, rr + e);
           uint32_t h0, l0, h1, l1;

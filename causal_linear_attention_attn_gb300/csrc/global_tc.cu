@@ -105,7 +105,7 @@ static_assert(BuildLayout<128>::Bytes <= 232448, "shared memory budget");
 static_assert(BuildLayout<128, true>::Bytes <= 232448, "shared memory budget");
 
 struct BuildParams {
-  CUtensorMap tk, tv;  // [BH][N][D] bf16, box 64 x 64 x 1, 128-byte swizzle
+  CUtensorMap tk, tv;  // [BH][N][D] bf16, boxes 64 x 64 x 1 (d = 128) or 64 x 128 x 1 (d = 64), 128-byte swizzle
   float *S, *z;        // whole-sequence mode: final state, summed over the cluster
   // Range mode (part_S non-null, d = 128): the first pass of the causal form.  Head h's
   // ranges r = h * ranges_per_head + s (s < ranges_per_head) cover its units
@@ -218,12 +218,14 @@ __global__ void __launch_bounds__(kBuildThreads, 1) global_build_tc(const __grid
         const int tok = (int)w.u * kUnit;
         uint8_t *k = sm + Lay::K + s * Lay::kStage, *v = sm + Lay::V + s * Lay::kStage;
         mbar_arrive_expect_tx(&full[s], 2 * Lay::kStage);
-        // d = 64: two 64-token sub-tiles; d = 128: the two 64-feature halves of one tile
-        const int x1 = D == 64 ? 0 : 64, t1 = D == 64 ? tok + 64 : tok;
+        // d = 64: one 128-token box per tensor, whose rows 0-63 and 64-127 are the two 64-token
+        // sub-tiles (fewer, larger copies stream faster); d = 128: the two 64-feature halves
         tma_load_3d(k, &p.tk, &full[s], 0, tok, w.h);
-        tma_load_3d(k + kHalf, &p.tk, &full[s], x1, t1, w.h);
         tma_load_3d(v, &p.tv, &full[s], 0, tok, w.h);
-        tma_load_3d(v + kHalf, &p.tv, &full[s], x1, t1, w.h);
+        if (D == 128) {
+          tma_load_3d(k + kHalf, &p.tk, &full[s], 64, tok, w.h);
+          tma_load_3d(v + kHalf, &p.tv, &full[s], 64, tok, w.h);
+        }
         issued = i + 1;
       }
       for (int i = max(0, issued - kBuildStages); i < issued; ++i)
@@ -699,8 +701,10 @@ cudaError_t launch_t(const Problem &p) {
   const long sms = std::max(1, di.sm_count);
   BuildParams bp;
   ReadParams rp;
-  if (!make_map(&bp.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k, p.BH, p.N, D, 64, 64) ||
-      !make_map(&bp.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v, p.BH, p.N, D, 64, 64) ||
+  // build boxes: 64 features x 64 tokens (d = 128, two per tile) or 64 x 128 (d = 64, one per tile)
+  const uint32_t build_rows = D == 64 ? 128 : 64;
+  if (!make_map(&bp.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k, p.BH, p.N, D, 64, build_rows) ||
+      !make_map(&bp.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v, p.BH, p.N, D, 64, build_rows) ||
       !make_map(&rp.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q, p.BH, p.N, D, 64, 128) ||
       !make_map(&rp.to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.out, p.BH, p.N, D, 32, 128))
     return cudaErrorInvalidValue;
