@@ -187,6 +187,11 @@ struct BwdTcParams {
   float *dq, *dk, *dv;
   float *dS0, *dz0;  // gradient of the initial state (nullable)
   float *den, *gden;  // [BH][N]: written by pass 1, read by pass 2
+  // pass 1's segment split: nseg segments of seg_chunks chunks per head; the state pass sums
+  // segment s < nseg - 1 in `parts` pieces, piece (bh, s, f) at part_S[((bh (nseg - 1) + s) parts
+  // + f) 128 x 128] and part_z[... 128]
+  float *part_S, *part_z;
+  int seg_chunks, nseg, parts;
   long N;
   float eps;
 };
@@ -242,6 +247,160 @@ __device__ __forceinline__ float2 pair_column_sums(const uint8_t *hi, const uint
   s.x += __shfl_xor_sync(0xffffffffu, s.x, 16);
   s.y += __shfl_xor_sync(0xffffffffu, s.y, 16);
   return s;
+}
+
+// ---------------------------------------------------------------------------
+// State pass for pass 1's segment split: the sums phi(K)^T V and colsum phi(K)
+// over parts of the earlier segments, with phi(K) as bf16 pairs (the same
+// operands and fp32 accumulation as pass 1's own state update).
+// ---------------------------------------------------------------------------
+struct StLayout {
+  static constexpr int kStages = 2;
+  static constexpr uint32_t K = 0;                       // raw keys, then the hi pairs in place
+  static constexpr uint32_t Klo = kStages * kTile;       // lo pairs
+  static constexpr uint32_t V = 2 * kStages * kTile;
+  static constexpr uint32_t Bars = 3 * kStages * kTile;  // full, phi_done, empty per stage; acc_full, drain
+  static constexpr uint32_t Misc = Bars + (3 * kStages + 2) * 8;
+  static constexpr uint32_t Bytes = Misc + 16;
+};
+static_assert(StLayout::Bytes <= 232448, "state pass shared memory");
+constexpr int kStThreads = 320;  // warp 0 TMA, 1 MMA, 2-9 phi pairs (2-5 also key column sums and the output)
+constexpr uint32_t kBarSt = 1;
+
+__global__ void __launch_bounds__(kStThreads, 1) bwd_state_tc(const __grid_constant__ BwdTcParams p) {
+  using L = StLayout;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(&g_bwd_status, kAbortMisaligned);
+    return;
+  }
+  uint8_t *sm = smem_raw;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::Bars);
+  uint64_t *full = bars, *phi_done = bars + L::kStages, *empty = bars + 2 * L::kStages,
+           *acc_full = bars + 3 * L::kStages, *drain = acc_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::Misc);
+  volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + L::Misc + 4);
+  unsigned int *status = &g_bwd_status;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int sgm = blockIdx.x / p.parts, part = blockIdx.x % p.parts;  // segment sgm < nseg - 1
+  const long N = p.N;
+  const int nch = (int)((N + kC - 1) / kC);
+  // this part's chunks [cb, ce) of segment sgm
+  const int s0 = sgm * p.seg_chunks, s1 = min(nch, s0 + p.seg_chunks);
+  const int cb = s0 + (int)((long)(s1 - s0) * part / p.parts), ce = s0 + (int)((long)(s1 - s0) * (part + 1) / p.parts);
+  const int n = max(0, ce - cb);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&phi_done[s], 256);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_word = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const long piece = ((long)bh * (p.nseg - 1) + sgm) * p.parts + part;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&p.tk);
+      prefetch_tmap(&p.tv);
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % L::kStages;
+        if (i >= L::kStages && !mbar_wait(&empty[s], ((i / L::kStages) - 1) & 1, abort_word, status)) break;
+        const int tok = (cb + i) * kC;
+        mbar_arrive_expect_tx(&full[s], 2 * kTile);
+        tma_load_3d(sm + L::K + s * kTile, &p.tk, &full[s], 0, tok, bh);
+        tma_load_3d(sm + L::K + s * kTile + kBlk, &p.tk, &full[s], 64, tok, bh);
+        tma_load_3d(sm + L::V + s * kTile, &p.tv, &full[s], 0, tok, bh);
+        tma_load_3d(sm + L::V + s * kTile + kBlk, &p.tv, &full[s], 64, tok, bh);
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - L::kStages); i < issued; ++i)
+        wait_drain(&full[i % L::kStages], (i / L::kStages) & 1, status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t iMM = idesc_bf16_f32(128, 128, 1, 1);
+      for (int i = 0; i < n; ++i) {
+        const int s = i % L::kStages;
+        if (!mbar_wait(&phi_done[s], (i / L::kStages) & 1, abort_word, status)) break;
+        tc_fence_after();
+        const uint32_t kh_ = smem_u32(sm + L::K + s * kTile), kl_ = smem_u32(sm + L::Klo + s * kTile),
+                       v_ = smem_u32(sm + L::V + s * kTile);
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16(tmem, mndesc(kh_, ks), mndesc(v_, ks), iMM, (i > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16(tmem, mndesc(kl_, ks), mndesc(v_, ks), iMM, 1u);
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(acc_full);
+      mma_commit(drain);
+      wait_drain(drain, 0, status);
+    }
+  } else {
+    // phi pairs in place over all 256 threads; threads 0-127 also sum the key columns
+    const int g = threadIdx.x - 64;  // 0..255
+    float2 zacc = make_float2(0.f, 0.f);
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int s = i % L::kStages;
+      const int T = (int)min((long)kC, N - (long)(cb + i) * kC);
+      ok = mbar_wait(&full[s], (i / L::kStages) & 1, abort_word, status);
+      if (bar_or(kBarSt, 256, !ok)) break;
+      uint8_t *kt = sm + L::K + s * kTile, *lt = sm + L::Klo + s * kTile;
+      key_pairs(reinterpret_cast<uint4 *>(kt), reinterpret_cast<uint4 *>(lt), g, T);
+      named_bar(kBarSt, 256);
+      if (g < 128) {
+        const float2 cs = pair_column_sums(kt, lt, g, T);
+        zacc.x += cs.x;
+        zacc.y += cs.y;
+      }
+      fence_async_smem();
+      mbar_arrive(&phi_done[s]);
+    }
+    // the piece: TMEM rows (features) to part_S, the key sums to part_z (threads 0-127)
+    if (g < 128) {
+      const int quarter = warp & 3, r = quarter * 32 + lane;
+      ok = ok && (n == 0 || mbar_wait(acc_full, 0, abort_word, status));
+      float *dst = p.part_S + (piece * kD + r) * kD;
+      if (ok && n > 0) {
+        tc_fence_after();
+        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+        for (int cb2 = 0; cb2 < 4; ++cb2) {
+          uint32_t w[32];
+          tmem_ld32(tl + cb2 * 32, w);
+          float4 *d4 = reinterpret_cast<float4 *>(dst + cb2 * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            d4[e] = make_float4(__uint_as_float(w[4 * e]), __uint_as_float(w[4 * e + 1]), __uint_as_float(w[4 * e + 2]),
+                                __uint_as_float(w[4 * e + 3]));
+        }
+      } else if (n == 0) {
+        for (int c = 0; c < kD; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if ((g & 31) < 16) {
+        const int pc = 2 * ((g & 15) + 16 * (g >> 5));
+        p.part_z[piece * kD + pc] = zacc.x;
+        p.part_z[piece * kD + pc + 1] = zacc.y;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
 }
 
 // Shared-memory layout of pass 1: seven [128 x 128] bf16 tiles (224 KB), then
@@ -312,9 +471,12 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
   unsigned int *status = &g_bwd_status;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
+  // one CTA per (segment, head); the segment's chunks [c0, c0 + nloc) in order
+  const int bh = blockIdx.y, seg = blockIdx.x;
   const long N = p.N;
   const int nch = (int)((N + kC - 1) / kC);
+  const int c0 = seg * p.seg_chunks;
+  const int nloc = min(nch, c0 + p.seg_chunks) - c0;
   const __nv_bfloat16 *qh = p.q + (long)bh * N * kD, *kh = p.k + (long)bh * N * kD, *vh = p.v + (long)bh * N * kD;
   const float *gh = p.dout + (long)bh * N * kD;
 
@@ -358,10 +520,10 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
                      sSlo = smem_u32(sm + L::Slo);
       const uint32_t tS = tmem + kP1S, tX = tmem + kP1X, tCB = tmem + kP1CB, tQh = tmem + kP1Q,
                      tQl = tmem + kP1Q + 64;
-      for (int c = 0; c < nch; ++c) {
+      for (int c = 0; c < nloc; ++c) {
         const uint32_t ph = c & 1;
-        if (c + 1 < nch) {  // the next chunk's rows into L2
-          const long t1 = (long)(c + 1) * kC;
+        if (c + 1 < nloc) {  // the next chunk's rows into L2
+          const long t1 = (long)(c0 + c + 1) * kC;
           const uint32_t rows = (uint32_t)min((long)kC, N - t1);
           prefetch_l2(qh + t1 * kD, rows * kD * 2);
           prefetch_l2(kh + t1 * kD, rows * kD * 2);
@@ -430,24 +592,36 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
     };
     if (tid == 0) {
       prefetch_tmap(&p.tk);
-      load_k(0);
+      load_k(c0);
     }
     {
-      // initial state S0 into tensor memory and its pair copy; z0 into z buffer 0
+      // initial state: S0 plus the sums of the earlier segments (the state pass's pieces), into
+      // tensor memory and its pair copy; z0 plus theirs into z buffer 0
+      const long npre = (long)seg * p.parts;  // pieces of this head before this segment
+      const float *pieces = p.part_S + (long)bh * (p.nseg - 1) * p.parts * kD * kD;
       for (int cb = 0; cb < 8; ++cb) {
-        uint32_t w[16];
+        float f[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) f[e] = 0.f;
         if (p.S0) {
           const float4 *src = reinterpret_cast<const float4 *>(p.S0 + ((long)bh * kD + r) * kD + cb * 16);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float4 f = src[e];
-            w[4 * e] = __float_as_uint(f.x), w[4 * e + 1] = __float_as_uint(f.y);
-            w[4 * e + 2] = __float_as_uint(f.z), w[4 * e + 3] = __float_as_uint(f.w);
+            const float4 x = src[e];
+            f[4 * e] += x.x, f[4 * e + 1] += x.y, f[4 * e + 2] += x.z, f[4 * e + 3] += x.w;
           }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = 0u;
         }
+        for (long pc = 0; pc < npre; ++pc) {
+          const float4 *src = reinterpret_cast<const float4 *>(pieces + (pc * kD + r) * kD + cb * 16);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 x = src[e];
+            f[4 * e] += x.x, f[4 * e + 1] += x.y, f[4 * e + 2] += x.z, f[4 * e + 3] += x.w;
+          }
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(f[e]);
         tmem_st16(tl + kP1S + cb * 16, w);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -458,15 +632,18 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
           *tile_chunk(Slo, r, cb * 16 + 8 * q) = make_uint4(l[0], l[1], l[2], l[3]);
         }
       }
-      zbuf[r] = p.z0 ? p.z0[(long)bh * kD + r] : 0.f;
+      float zr = p.z0 ? p.z0[(long)bh * kD + r] : 0.f;
+      const float *zpieces = p.part_z + (long)bh * (p.nseg - 1) * p.parts * kD;
+      for (long pc = 0; pc < npre; ++pc) zr += zpieces[pc * kD + r];
+      zbuf[r] = zr;
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(s_ready);
       mbar_arrive(&z_full[0]);
     }
     bool ok = true;
-    for (int c = 0; c < nch; ++c) {
-      const long t0 = (long)c * kC;
+    for (int c = 0; c < nloc; ++c) {
+      const long t0 = (long)(c0 + c) * kC;
       const int T = (int)min((long)kC, N - t0);
       // this row's queries 0-63, loaded while the keys are transformed
       uint4 x[8];
@@ -487,7 +664,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       mbar_arrive(&z_empty[c & 1]);
       tc_fence_before();
       mbar_arrive(q_ready);
-      if (c + 1 == nch) break;
+      if (c + 1 == nloc) break;
       // pair copy of the state the next chunk reads, once this chunk's Y has read the current
       // copy and its S update has completed
       ok = wait(y_full, c & 1);
@@ -511,7 +688,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       // the next chunk's raw keys once this chunk's products are done with the K tiles
       ok = wait(d_full, c & 1);
       if (bar_or(kBarQK, 128, !ok)) break;
-      if (tid == 0) load_k(c + 1);
+      if (tid == 0) load_k(c0 + c + 1);
     }
     if (tid == 0 && k_issued > 0) wait_drain(k_full, (k_issued - 1) & 1, status);
   } else if (warp < kP1WarpE) {
@@ -521,8 +698,8 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
     uint8_t *Ghi = sm + L::Ghi, *Glo = sm + L::Glo;
     int v_issued = 0;
     if (gt == 0) prefetch_tmap(&p.tv);
-    for (int c = 0; c < nch; ++c) {
-      const long t0 = (long)c * kC;
+    for (int c = 0; c < nloc; ++c) {
+      const long t0 = (long)(c0 + c) * kC;
       const int T = (int)min((long)kC, N - t0);
       const bool ok = c == 0 || wait(y_full, (c - 1) & 1);
       if (bar_or(kBarG, 128, !ok)) break;
@@ -593,8 +770,8 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
     // ---------------- E warps: scores, den, gden, B', key column sums, dq ----------------
     const int t = (warp & 3) * 32 + lane;  // tensor-memory lane = chunk row; also feature t of z
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    for (int c = 0; c < nch; ++c) {
-      const long t0 = (long)c * kC;
+    for (int c = 0; c < nloc; ++c) {
+      const long t0 = (long)(c0 + c) * kC;
       const int T = (int)min((long)kC, N - t0);
       const int jmax = min(t, T - 1);  // keys kept: j <= t and j < T
       uint32_t ra[32], rc[32];
@@ -678,7 +855,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
 
       // z for the next chunk: z_prev plus this chunk's key column sums (thread t owns feature t)
       named_bar(kBarE, 128);  // every read of this chunk's z is done
-      if (c + 1 < nch) {
+      if (c + 1 < nloc) {
         const int nb = (c + 1) & 1;
         ok = c + 1 < 2 || wait(&z_empty[nb], (((c + 1) >> 1) - 1) & 1);
         if (bar_or(kBarE, 128, !ok)) break;
@@ -1180,10 +1357,23 @@ cudaError_t launch_causal_backward_tc(const BackwardProblem &b) {
   const Problem &p = b.p;
   cudaError_t e = ensure_smem_optin((const void *)bwd_pass1_tc, (int)P1Layout::Bytes);
   if (e == cudaSuccess) e = ensure_smem_optin((const void *)bwd_pass2_tc, (int)P2Layout::Bytes);
+  if (e == cudaSuccess) e = ensure_smem_optin((const void *)bwd_state_tc, (int)StLayout::Bytes);
   if (e != cudaSuccess) return e;
-  // scratch: den and gden of every token, written by pass 1 and read by pass 2
+  // pass 1's segments: enough CTAs to cover the SMs once, at least 4 chunks each; the state pass
+  // sums each earlier segment in `parts` pieces, enough CTAs to cover the SMs about once
+  const long sms = std::max(1, device_info(-1).sm_count);
+  const long nch = (p.N + kC - 1) / kC;
+  long G = std::max(1L, std::min(sms / p.BH, nch / 4));
+  const long seg_chunks = (nch + G - 1) / G;
+  G = (nch + seg_chunks - 1) / seg_chunks;
+  const long parts = G > 1 ? std::max(1L, std::min(seg_chunks, sms / (p.BH * (G - 1)))) : 1;
+  const size_t npieces = (size_t)p.BH * (G - 1) * parts;
+  // scratch: den and gden of every token (pass 1 -> pass 2), then the state pass's pieces
+  // (each block starts on a 256-byte boundary)
+  const size_t dg_f = (2 * (size_t)p.BH * p.N + 63) / 64 * 64;
+  const size_t piece_f = npieces * (kD * kD + kD);
   float *scratch = nullptr;
-  e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), sizeof(float) * 2 * (size_t)p.BH * p.N, p.stream);
+  e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), sizeof(float) * (dg_f + piece_f), p.stream);
   if (e != cudaSuccess) return e;
   BwdTcParams a;
   memset(&a, 0, sizeof a);
@@ -1199,12 +1389,24 @@ cudaError_t launch_causal_backward_tc(const BackwardProblem &b) {
   a.dq = b.dq, a.dk = b.dk, a.dv = b.dv, a.dS0 = b.dS0, a.dz0 = b.dz0;
   a.den = scratch;
   a.gden = scratch + (size_t)p.BH * p.N;
+  a.part_S = scratch + dg_f;
+  a.part_z = a.part_S + npieces * kD * kD;
+  a.seg_chunks = (int)seg_chunks;
+  a.nseg = (int)G;
+  a.parts = (int)parts;
   a.N = p.N;
   a.eps = p.eps;
   {
     LaunchTimer timer(kKBackward, p.stream);
-    bwd_pass1_tc<<<(unsigned)p.BH, kP1Threads, P1Layout::Bytes, p.stream>>>(a);
-    e = cudaGetLastError();
+    if (G > 1) {
+      bwd_state_tc<<<dim3((unsigned)((G - 1) * parts), (unsigned)p.BH), kStThreads, StLayout::Bytes, p.stream>>>(a);
+      e = cudaGetLastError();
+      if (e == cudaSuccess) count_launch();
+    }
+    if (e == cudaSuccess) {
+      bwd_pass1_tc<<<dim3((unsigned)G, (unsigned)p.BH), kP1Threads, P1Layout::Bytes, p.stream>>>(a);
+      e = cudaGetLastError();
+    }
     if (e == cudaSuccess) {
       count_launch();
       bwd_pass2_tc<<<dim3((unsigned)p.BH, 2), kP2Threads, P2Layout::Bytes, p.stream>>>(a);
