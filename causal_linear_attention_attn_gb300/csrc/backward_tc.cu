@@ -107,17 +107,6 @@ __device__ __forceinline__ void phi_pair8(uint4 x, uint4 &h, uint4 &l) {
   l = make_uint4(ll[0], ll[1], ll[2], ll[3]);
 }
 
-// 16-byte read-only global load that the compiler keeps in program order with
-// the other inline-asm statements (so that a row is not loaded early, beside
-// another row still held in registers).
-__device__ __forceinline__ uint4 ld_row16(const void *p) {
-  uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
 // 32-byte global load (read-only path) and store; the address must be 32-byte aligned.
 __device__ __forceinline__ void ld_row32(const void *p, uint32_t (&r)[8]) {
   asm volatile("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -142,18 +131,6 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t tile, int ks) {
 // Row `row`, columns col0 .. col0 + 7 of a [128 x 128] bf16 tile.
 __device__ __forceinline__ uint4 *tile_chunk(uint8_t *tile, int row, int col0) {
   return reinterpret_cast<uint4 *>(tile + (col0 >> 6) * kBlk + sw128_offset(row, col0 & 63));
-}
-
-// 32 fp32 values (columns col0 .. col0 + 31 of row `row`) as bf16 pairs into tiles hi, lo.
-__device__ __forceinline__ void store_row32_pair(uint8_t *hi, uint8_t *lo, int row, int col0, const uint32_t (&r)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) split2(__uint_as_float(r[8 * q + 2 * e]), __uint_as_float(r[8 * q + 2 * e + 1]), h[e], l[e]);
-    *tile_chunk(hi, row, col0 + 8 * q) = make_uint4(h[0], h[1], h[2], h[3]);
-    *tile_chunk(lo, row, col0 + 8 * q) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
 }
 
 // Split 32 fp32 score columns (keys 32 cb .. 32 cb + 31 of this lane's row) in

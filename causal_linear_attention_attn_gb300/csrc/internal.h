@@ -121,6 +121,9 @@ cudaError_t launch_global_simt(const Problem &p, bool identity = false);
 cudaError_t launch_decode(const Problem &p);
 // Retention decode step: S = gamma[bh % H] S + k v^T, out = q^T S (host gamma array, H <= 128; no z).
 cudaError_t launch_retention_decode(const Problem &p, const float *gamma, int H);
+// Retention prefill on CUDA cores, exact fp32, any supported dtype and head size, gamma in [0, 1]
+// (host array, head bh decays by gamma[bh % H], H <= 128).
+cudaError_t launch_retention_simt(const Problem &p, bool from_state, const float *gamma, int H);
 
 // Count one successful kernel launch (reported by la_kernel_launches).
 void count_launch(unsigned n = 1);

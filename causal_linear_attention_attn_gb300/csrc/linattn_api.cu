@@ -257,9 +257,13 @@ static la_status retention_impl(const void *q, const void *k, const void *v, flo
   if (!S || !gamma || (N > 0 && (!q || !k || !v || !out))) return LA_ERR_INVALID_VALUE;
   for (int h = 0; h < H; ++h)
     if (!std::isfinite(gamma[h])) return LA_ERR_INVALID_VALUE;
-  if (dt != LA_BF16 || d_k != 128 || d_v != 128 || H > la::kMaxRetentionHeads) return LA_ERR_UNSUPPORTED;
-  for (int h = 0; h < H; ++h)
-    if (!(gamma[h] >= 0.75f && gamma[h] <= 1.f)) return LA_ERR_UNSUPPORTED;
+  if (dt != LA_F32 && dt != LA_BF16) return LA_ERR_UNSUPPORTED;
+  if (!la::supported_dim(d_k) || !la::supported_dim(d_v) || H > la::kMaxRetentionHeads) return LA_ERR_UNSUPPORTED;
+  bool fast_decay = false;  // a head with gamma < 0.75 is outside the tensor-core path's weight range
+  for (int h = 0; h < H; ++h) {
+    if (!(gamma[h] >= 0.f && gamma[h] <= 1.f)) return LA_ERR_UNSUPPORTED;
+    if (gamma[h] < 0.75f) fast_decay = true;
+  }
   const void *ptrs[5] = {q, k, v, out, S};
   for (const void *ptr : ptrs)
     if (ptr && !la::aligned16(ptr)) return LA_ERR_MISALIGNED;
@@ -271,7 +275,8 @@ static la_status retention_impl(const void *q, const void *k, const void *v, flo
     if (from_state) return LA_OK;
     return la::from_cuda(cudaMemsetAsync(S, 0, sizeof(float) * (size_t)BH * d_k * d_v, p.stream));
   }
-  if (!la::causal_tc_supported(p)) return LA_ERR_UNSUPPORTED;
+  if (fast_decay || !la::causal_tc_supported(p))
+    return la::from_cuda(la::launch_retention_simt(p, from_state, gamma, H));
   float log2g[la::kMaxRetentionHeads];
   for (int h = 0; h < H; ++h) log2g[h] = (float)std::log2((double)gamma[h]);
   return la::from_cuda(la::launch_retention_tc(p, from_state, log2g, H));

@@ -214,12 +214,18 @@ LA_API la_status la_global_features(const void *phi_q, const void *phi_k, const 
  * gamma: HOST array of H floats, head h (of every batch row) decaying by
  * gamma[h]; read during the call only.
  *
- * Supported: dt == LA_BF16, d_k == d_v == 128, an sm_103 device, H <= 128,
- * every gamma[h] in [0.75, 1] (the chunked kernel weighs a key 128 tokens
- * ahead by gamma^-128, which must stay well inside float range); anything
- * else returns LA_ERR_UNSUPPORTED.  LA_ERR_INVALID_VALUE for a NULL gamma
- * or a gamma that is not finite; other errors as la_causal.  Allocates
- * stream-ordered scratch on `stream` for long sequences split into segments.
+ * Supported: dt LA_F32 or LA_BF16, d_k and d_v each 32, 64 or 128, H <= 128,
+ * every gamma[h] in [0, 1] (gamma = 0 keeps only the current token);
+ * anything else returns LA_ERR_UNSUPPORTED.  LA_ERR_INVALID_VALUE for a NULL
+ * gamma or a gamma that is not finite; other errors as la_causal.
+ *
+ * Two kernels serve it.  bf16 with d_k == d_v == 128 on an sm_103 device and
+ * every gamma[h] >= 0.75 runs on the tensor cores: that chunked kernel weighs
+ * a key 128 tokens ahead by gamma^-128, which must stay well inside float
+ * range, and it allocates stream-ordered scratch on `stream` for long
+ * sequences split into segments.  Everything else runs on CUDA cores, exact
+ * fp32 in 64-token chunks whose decay powers never exceed 1, one CTA per
+ * head, allocating nothing.
  */
 LA_API la_status la_retention(const void *q, const void *k, const void *v, float *out, float *S,
                               const float *gamma, int B, int H, int N, int d_k, int d_v, la_dtype dt,

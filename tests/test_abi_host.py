@@ -114,13 +114,13 @@ def test_retention_validation(fn):
     assert ret(fn, gamma=(float("inf"),)) == INVALID
     assert ret(fn, N=-1) == INVALID
     assert ret(fn, dk=0) == INVALID
-    # outside the tensor-core retention path
-    assert ret(fn, dt=0) == UNSUPPORTED
-    assert ret(fn, dk=64) == UNSUPPORTED
-    assert ret(fn, dv=32) == UNSUPPORTED
-    assert ret(fn, gamma=(0.5,)) == UNSUPPORTED
+    # outside every retention kernel (fp32, d in {32, 64, 128} and gamma in [0, 1] are served)
+    assert ret(fn, dt=7) == UNSUPPORTED
+    assert ret(fn, dk=48) == UNSUPPORTED
+    assert ret(fn, dv=96) == UNSUPPORTED
     assert ret(fn, gamma=(1.01,)) == UNSUPPORTED
-    assert ret(fn, H=2, gamma=(0.9, 0.7)) == UNSUPPORTED
+    assert ret(fn, gamma=(-0.01,)) == UNSUPPORTED
+    assert ret(fn, H=2, gamma=(0.5, 1.5)) == UNSUPPORTED
     assert ret(fn, H=129, gamma=(0.9,) * 129) == UNSUPPORTED
     assert ret(fn, v=P + 8) == MISALIGNED
     assert ret(fn, S=P + 4) == MISALIGNED
