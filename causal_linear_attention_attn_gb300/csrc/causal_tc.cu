@@ -277,11 +277,11 @@ __device__ __forceinline__ long piece_end_units(const TcParams &p, int bh, long 
 //   S_new = A + (w k)^T V   (then times the next chunk's gamma^C)
 // q and k are used as given, so the dot products cancel and every operand
 // that is not an input goes to the tensor cores as a bf16 hi/lo pair:
-// (q_i . k_j) w_j is split as P is; the weighted keys, formed once Q K^T has
-// read the raw ones, are split into the K tile (hi) and the consumed Q slot
-// (lo), which is reloaded only after the state update has read it (so Q has
-// one stage); the copy of A that Q reads is split into Sb (hi) and the other
-// Q slot (lo).  Every factor lies within 2^+-54 for gamma >= 0.75.  There is
+// (q_i . k_j) w_j is split as P is; the weighted keys are split into the
+// consumed Q slot (lo, as soon as Q is in tensor memory) and the K tile (hi,
+// once Q K^T has read the raw keys).  The update takes the low parts first and
+// the slot is reloaded as soon as they have been read (so Q has one stage);
+// the copy of A that Q reads is split into Sb (hi) and the other Q slot (lo).  Every factor lies within 2^+-54 for gamma >= 0.75.  There is
 // no z, no denominator and no exact leading-token pass.
 // kModeIdentity: q and k are already features; they reach the MMAs as given,
 // with the normalizer, denominators and no exact leading-token pass.  Given
@@ -310,7 +310,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
   uint64_t *s_full = bars + 21, *pp_ready = bars + 22, *o_full = bars + 23, *sb_ready = bars + 24,
            *o_free = bars + 25, *drain = bars + 26, *p_full = bars + 27, *den_ready = bars + 28,  // [2]
            *qt_free = bars + 30,  // [2]: phi(Q) tensor-memory buffers
-           *k_ready = bars + 32;  // retention: keys weighted for the state update
+           *k_ready = bars + 32,  // retention: high parts of the weighted keys in place
+           *klo_ready = bars + 33;  // retention: their low parts in the Q slot
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::Misc);
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
   unsigned int *status = &g_device_status;
@@ -346,6 +347,7 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
     mbar_init(&den_ready[0], 128);
     mbar_init(&den_ready[1], 128);
     mbar_init(k_ready, kPhiThreads);
+    mbar_init(klo_ready, kPhiThreads);
     *abort_word = 0;
     fence_barrier_init();
   }
@@ -433,28 +435,45 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tP, tQ + 8 * ks, kdesc(k, ks), iKK, ks > 0);
         mma_commit(p_full);
-        // S += K^T V once the previous state has been copied out
+        // S += K^T V; retention: the weighted keys as a pair, the low parts (in the Q slot) first
+        // so that the slot is released for the next chunk's Q as early as possible
+        auto state_update = [&](uint32_t a) {
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tS, mndesc(a, ks), mndesc(v, ks), iMM, 1);
+        };
+        // O = Q bf16(S_prev) (pair modes: hi and lo of the state copy)
+        auto state_read = [&]() {
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSb, ks), iKM, ks > 0);
+          if (kSplitS) {
+#pragma unroll 1
+            for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSblo, ks), iKM, 1);
+          }
+          mma_commit(&qt_free[c & 1]);
+        };
+        // The read needs the copy of the previous state and the previous outputs read out; the
+        // update needs that copy taken and (retention) the keys weighted.  Retention runs the
+        // read between the two halves of the update, while the keys' high parts are formed.
         if (!mbar_wait(sb_ready, c & 1, abort_word, status, p.wait_ns)) break;
-        if (kRet && !mbar_wait(k_ready, c & 1, abort_word, status, p.wait_ns)) break;  // the keys' state weights
-        tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tS, mndesc(k, ks), mndesc(v, ks), iMM, 1);
         if (kRet) {
-#pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tS, mndesc(sKlo, ks), mndesc(v, ks), iMM, 1);
+          if (!mbar_wait(klo_ready, c & 1, abort_word, status, p.wait_ns)) break;
+          tc_fence_after();
+          state_update(sKlo);
           mma_commit(&q_empty[0]);  // the Q slot may take the next chunk's Q
+          if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status, p.wait_ns)) break;
+          tc_fence_after();
+          state_read();
+          if (!mbar_wait(k_ready, c & 1, abort_word, status, p.wait_ns)) break;
+          tc_fence_after();
+          state_update(k);
+        } else {
+          tc_fence_after();
+          state_update(k);
+          if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status, p.wait_ns)) break;
+          tc_fence_after();
+          state_read();
         }
-        // O = Q bf16(S_prev) once the previous outputs have been read
-        if (c > 0 && !mbar_wait(o_free, (c - 1) & 1, abort_word, status, p.wait_ns)) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSb, ks), iKM, ks > 0);
-        if (kSplitS) {
-#pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tO, tQ + 8 * ks, mndesc(sSblo, ks), iKM, 1);
-        }
-        mma_commit(s_full);
-        mma_commit(&qt_free[c & 1]);
+        mma_commit(s_full);  // the update is complete and the copy has been read
         mma_commit(&k_empty[s]);
         if (!mbar_wait(pp_ready, c & 1, abort_word, status, p.wait_ns)) break;
         tc_fence_after();
@@ -528,9 +547,10 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         }
       }
       // phi(K) half row in place (all loads of a step first: the in-place stores would order them);
-      // retention: the raw keys times their state weight w_row, once Q K^T has read them, as the
-      // high parts in place and the low parts in the consumed Q slot
-      auto transform_k = [&](float wk) {
+      // retention: the raw keys times their state weight w_row as a bf16 pair, the low parts into
+      // the consumed Q slot (part 1) and, once Q K^T has read the raw keys, the high parts in
+      // place (part 2)
+      auto transform_k = [&](float wk, int part) {
         uint8_t *Kb = Kt + half * kBlk, *Lb = sm + Lay::Q + half * kBlk;
 #pragma unroll 1
         for (int g = 0; g < 2; ++g) {
@@ -543,15 +563,17 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
             if (kRet) {
               uint4 hi, lo;
               split8(kv[e], wk, hi, lo);
-              *reinterpret_cast<uint4 *>(Kb + off) = hi;
-              *reinterpret_cast<uint4 *>(Lb + off) = lo;
+              if (part == 1)
+                *reinterpret_cast<uint4 *>(Lb + off) = lo;
+              else
+                *reinterpret_cast<uint4 *>(Kb + off) = hi;
             } else {
               *reinterpret_cast<uint4 *>(Kb + off) = phi8(kv[e]);
             }
           }
         }
       };
-      if (!kRaw) transform_k(1.f);
+      if (!kRaw) transform_k(1.f, 0);
       named_bar(kBarPhi, kPhiThreads);  // every K row transformed; every read of zs done
       if (!kRet) {
         // column sums of phi(K) over the valid rows (bf16 values, as the MMA sees them)
@@ -566,9 +588,14 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       tc_fence_before();
       mbar_arrive(&phi_done[s]);
       if (kRet) {
+        // every raw Q read of this slot is done (the barrier above): the low parts may go in
+        const float wk = exp2f((float)(tv - 1 - row) * lg);
+        transform_k(wk, 1);
+        fence_async_smem();
+        mbar_arrive(klo_ready);
         const bool okp = mbar_wait(p_full, c & 1, abort_word, status, p.wait_ns);  // Q K^T has read the raw keys
         if (bar_or(kBarPhi, kPhiThreads, !okp)) break;
-        transform_k(exp2f((float)(tv - 1 - row) * lg));
+        transform_k(wk, 2);
         fence_async_smem();
         mbar_arrive(k_ready);
       }
