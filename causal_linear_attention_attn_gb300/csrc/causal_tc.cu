@@ -369,7 +369,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
       // a test launch (la_test_inject_missing_load) leaves out one key load of CTA (0, 0): the
       // consumers' bounded waits then run out, and the CTA drains and exits with the timeout set
       const int skip_k = blockIdx.x == 0 && blockIdx.y == 0 ? p.skip_k_chunk : -1;
-      // Q of chunk c: stage c % 2, or (retention) always slot 0, after the previous chunk's state update
+      // Q of chunk c: stage c % 2, or (retention) always slot 0, once the previous chunk's state
+      // update has read the low parts of its weighted keys there
       auto load_q = [&](int c, int tok) -> bool {
         const int qs = kQ1 ? 0 : c % kStages;
         if (kQ1 ? c >= 1 : c >= kStages) {
@@ -394,12 +395,14 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
           tma_load_3d(sm + Lay::K + s * kTile + kBlk, &p.tk, &full_k[s], 64, tok, bh);
         }
         issued_k = c + 1;
+        // retention: Q's single slot frees before this V stage does (the stage is also the output
+        // staging of the chunk two back), so Q goes first
+        if (kRet && !load_q(c, tok)) break;
         if (c >= kStages && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_word, status, p.wait_ns)) break;
         mbar_arrive_expect_tx(&full_v[s], kTile);
         tma_load_3d(sm + Lay::V + s * kTile, &p.tv, &full_v[s], 0, tok, bh);
         tma_load_3d(sm + Lay::V + s * kTile + kBlk, &p.tv, &full_v[s], 64, tok, bh);
         issued_v = c + 1;
-        if (kRet && !load_q(c, tok)) break;
       }
       // every issued copy must land before shared memory is released
       for (int c = max(0, issued_q - (kQ1 ? 1 : kStages)); c < issued_q; ++c)
