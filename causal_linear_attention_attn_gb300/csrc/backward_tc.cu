@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kStThreads, 1) bwd_state_tc(const __grid_const
         tc_fence_after();
         const uint32_t kh_ = smem_u32(sm + L::K + s * kTile), kl_ = smem_u32(sm + L::Klo + s * kTile),
                        v_ = smem_u32(sm + L::V + s * kTile);
-#pragma unroll 1
+#pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16(tmem, mndesc(kh_, ks), mndesc(v_, ks), iMM, (i > 0 || ks > 0) ? 1u : 0u);
           mma_bf16(tmem, mndesc(kl_, ks), mndesc(v_, ks), iMM, 1u);
@@ -510,14 +510,14 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
         if (!wait(q_ready, ph) || !wait(k_ready, ph) || !wait(g_ready, ph) || !wait(v_full, ph)) break;
         tc_fence_after();
         // A = Q K^T (pairs: Qh Kh + Qh Kl + Ql Kh)
-#pragma unroll 1
+#pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16_ts(tX, tQh + 8 * ks, kdesc(sKhi, ks), iKK, ks > 0);
           mma_bf16_ts(tX, tQh + 8 * ks, kdesc(sKlo, ks), iKK, 1);
           mma_bf16_ts(tX, tQl + 8 * ks, kdesc(sKhi, ks), iKK, 1);
         }
         // C = dO V^T
-#pragma unroll 1
+#pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16(tCB, kdesc(sGhi, ks), kdesc(sV, ks), iKK, ks > 0);
           mma_bf16(tCB, kdesc(sGlo, ks), kdesc(sV, ks), iKK, 1);
@@ -526,14 +526,14 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
         if (!wait(s_ready, ph) || !wait(x_free, ph)) break;
         tc_fence_after();
         // Y = dO S_prev^T (S copy rows = features i, K-major over value components)
-#pragma unroll 1
+#pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16(tX, kdesc(sGhi, ks), kdesc(sShi, ks), iKK, ks > 0);
           mma_bf16(tX, kdesc(sGhi, ks), kdesc(sSlo, ks), iKK, 1);
           mma_bf16(tX, kdesc(sGlo, ks), kdesc(sShi, ks), iKK, 1);
         }
         // S += K^T V
-#pragma unroll 1
+#pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16(tS, mndesc(sKhi, ks), mndesc(sV, ks), iMM, 1);
           mma_bf16(tS, mndesc(sKlo, ks), mndesc(sV, ks), iMM, 1);
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
         if (!wait(cb_ready, ph)) break;
         tc_fence_after();
         // X += B' K: B' from tensor memory (keys [16 ks, 16 ks + 16): 8 columns hi, 8 lo)
-#pragma unroll 1
+#pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16_ts(tX, tCB + 16 * ks, mndesc(sKhi, ks), iKM, 1);
           mma_bf16_ts(tX, tCB + 16 * ks + 8, mndesc(sKhi, ks), iKM, 1);
@@ -970,7 +970,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         tc_fence_after();
         if (!kDk) {
           // X = K Q^T (rows keys j, columns queries t)
-#pragma unroll 1
+#pragma unroll 4
           for (int ks = 0; ks < 8; ++ks) {
             mma_bf16_ts(tX, tKh + 8 * ks, kdesc(sQhi, ks), iKK, ks > 0);
             mma_bf16_ts(tX, tKh + 8 * ks, kdesc(sQlo, ks), iKK, 1);
@@ -978,7 +978,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           }
         } else {
           // X = V gnum^T
-#pragma unroll 1
+#pragma unroll 4
           for (int ks = 0; ks < 8; ++ks) {
             mma_bf16_ts(tX, tKh + 8 * ks, kdesc(sNhi, ks), iKK, ks > 0);
             mma_bf16_ts(tX, tKh + 8 * ks, kdesc(sNlo, ks), iKK, 1);
@@ -988,7 +988,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         tc_fence_after();
         if (!kDk) {
           // O = K U (U rows = features i: the K index)
-#pragma unroll 1
+#pragma unroll 4
           for (int ks = 0; ks < 8; ++ks) {
             mma_bf16_ts(tO, tKh + 8 * ks, mndesc(sUhi, ks), iKM, ks > 0);
             mma_bf16_ts(tO, tKh + 8 * ks, mndesc(sUlo, ks), iKM, 1);
@@ -996,7 +996,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           }
         } else {
           // O = V U^T (U rows = features i: the N index, K-major over value components)
-#pragma unroll 1
+#pragma unroll 4
           for (int ks = 0; ks < 8; ++ks) {
             mma_bf16_ts(tO, tKh + 8 * ks, kdesc(sUhi, ks), iKK, ks > 0);
             mma_bf16_ts(tO, tKh + 8 * ks, kdesc(sUlo, ks), iKK, 1);
@@ -1008,14 +1008,14 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         // O += X B with X from tensor memory as pairs (queries [16 ks, 16 ks + 16): 8 columns hi,
         // 8 lo) and B = gnum (role 0) or phi(Q) (role 1), rows = queries
         const uint32_t sBhi = kDk ? sQhi : sNhi, sBlo = kDk ? sQlo : sNlo;
-#pragma unroll 1
+#pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16_ts(tO, tX + 16 * ks, mndesc(sBhi, ks), iKM, 1);
           mma_bf16_ts(tO, tX + 16 * ks + 8, mndesc(sBhi, ks), iKM, 1);
           mma_bf16_ts(tO, tX + 16 * ks, mndesc(sBlo, ks), iKM, 1);
         }
         // U += Q^T gnum
-#pragma unroll 1
+#pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16(tU, mndesc(sQhi, ks), mndesc(sNhi, ks), iMM, 1);
           mma_bf16(tU, mndesc(sQhi, ks), mndesc(sNlo, ks), iMM, 1);
