@@ -18,16 +18,18 @@
 namespace la {
 namespace {
 
-constexpr int kT = 64;  // tokens per chunk
 constexpr int kThreads = 256;
 
-size_t simt_smem_bytes(int dk, int dv) {
+// Shared memory of a chunk length kT: the state, z, phi(Q) and phi(K) rows (padded), V, the
+// masked weights and the denominators.
+size_t simt_smem_bytes(int dk, int dv, int kT) {
   const size_t floats = (size_t)dk * dv + dk + 2 * (size_t)kT * (dk + 1) + (size_t)kT * dv +
                         (size_t)kT * (kT + 1) + kT;
   return floats * sizeof(float);
 }
 
-template <typename Tin>
+// kT: tokens per chunk, 64, or 32 where the state is too large for 64 (256 given features).
+template <typename Tin, int kT>
 __global__ void __launch_bounds__(kThreads)
     causal_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                        float *__restrict__ out, float *__restrict__ S_g, float *__restrict__ z_g,
@@ -118,14 +120,14 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <typename Tin>
+template <typename Tin, int kT>
 cudaError_t launch_t(const Problem &p, long n_proc, bool from_state, bool write_state, bool identity) {
-  const size_t smem = simt_smem_bytes(p.dk, p.dv);
-  cudaError_t e = cudaFuncSetAttribute(causal_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = simt_smem_bytes(p.dk, p.dv, kT);
+  cudaError_t e = cudaFuncSetAttribute(causal_simt_kernel<Tin, kT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   LaunchTimer timer(kKCausalSimt, p.stream);
-  causal_simt_kernel<Tin><<<p.BH, kThreads, smem, p.stream>>>(
+  causal_simt_kernel<Tin, kT><<<p.BH, kThreads, smem, p.stream>>>(
       (const Tin *)p.q, (const Tin *)p.k, (const Tin *)p.v, p.out, p.S, p.z, p.N, n_proc, p.dk, p.dv, p.eps,
       from_state ? 1 : 0, write_state ? 1 : 0, identity ? 1 : 0);
   e = cudaGetLastError();
@@ -314,8 +316,15 @@ cudaError_t launch_causal_exact_head(const Problem &p, long n_exact, const float
 }
 
 cudaError_t launch_causal_simt(const Problem &p, long n_proc, bool from_state, bool write_state, bool identity) {
-  if (p.dt == LA_F32) return launch_t<float>(p, n_proc, from_state, write_state, identity);
-  return launch_t<__nv_bfloat16>(p, n_proc, from_state, write_state, identity);
+  // 64-token chunks where they fit the device's shared memory, else 32 (a 256 x 128 state)
+  const size_t optin = (size_t)device_info(-1).max_smem_optin;
+  const bool wide = simt_smem_bytes(p.dk, p.dv, 64) > optin;
+  if (wide && simt_smem_bytes(p.dk, p.dv, 32) > optin) return cudaErrorInvalidValue;
+  if (p.dt == LA_F32)
+    return wide ? launch_t<float, 32>(p, n_proc, from_state, write_state, identity)
+                : launch_t<float, 64>(p, n_proc, from_state, write_state, identity);
+  return wide ? launch_t<__nv_bfloat16, 32>(p, n_proc, from_state, write_state, identity)
+              : launch_t<__nv_bfloat16, 64>(p, n_proc, from_state, write_state, identity);
 }
 
 }  // namespace la

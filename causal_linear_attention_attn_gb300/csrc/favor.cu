@@ -33,7 +33,7 @@ namespace {
 using namespace tc;
 
 constexpr int kFavThreads = 288;         // warp 0: loads and MMAs; warps 1-4 and 5-8: two epilogue groups
-constexpr int kFavM = 128;                 // features of the tensor-core path
+constexpr int kFavM = 128;                 // features one tensor-core launch forms (m = 256: two launches)
 constexpr uint32_t kBlk = 16384;           // [128 rows x 128 bytes], 128-byte swizzled
 constexpr uint32_t kAbortMisaligned = 2u;  // status bit: shared memory base not 1024-aligned
 constexpr uint32_t kBarGroup = 1;          // named barriers 1 and 2: the two epilogue groups
@@ -50,8 +50,10 @@ struct FavLayout {
 };
 
 struct FavorParams {
-  CUtensorMap tx, tw, to;  // X [1][rows][D], W [1][128][D], out [1][rows][128], bf16, boxes 64 x 128
+  CUtensorMap tx, tw, to;  // X [1][rows][D], W [1][128][D] (128 of the m projections), out [1][rows][m], bf16, boxes 64 x 128
   int tiles;
+  int col0;          // this launch's features are columns [col0, col0 + 128) of the m-wide output
+  float inv_sqrt_m;  // 1 / sqrt(m) for the whole feature vector
 };
 
 // K-major operand (rows of 64 K-elements per 16 KB block): k-step ks covers K elements [16ks, 16ks+16).
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(kFavThreads, 1) favor_tc_kernel(const __grid_c
     const int g = (warp - 1) >> 2, gt = tid - 32 - 128 * g;  // gt: the row this thread owns
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;  // its tensor-memory lane quarter
     uint8_t *stage_o = sm + Lay::O + g * 2 * kBlk;
-    const float inv_sqrt_m = 1.f / sqrtf((float)kFavM);
+    const float inv_sqrt_m = p.inv_sqrt_m;
     const int row = 32 * (warp & 3) + lane;  // tensor-memory lane = tile row
     (void)gt;
     for (int i = g; i < n; i += 2) {
@@ -200,8 +202,8 @@ __global__ void __launch_bounds__(kFavThreads, 1) favor_tc_kernel(const __grid_c
       fence_async_smem();
       named_bar(kBarGroup + g, 128);
       if (row == 0) {
-        tma_store_3d(&p.to, stage_o, 0, row0_of(i), 0);
-        tma_store_3d(&p.to, stage_o + kBlk, 64, row0_of(i), 0);
+        tma_store_3d(&p.to, stage_o, p.col0, row0_of(i), 0);
+        tma_store_3d(&p.to, stage_o + kBlk, p.col0 + 64, row0_of(i), 0);
         bulk_commit();
       }
     }
@@ -258,22 +260,30 @@ bool make_map2(CUtensorMap *map, const void *base, long rows, int cols) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// m = 128 h features: one launch per block of 128 projections, each writing its columns of the
+// m-wide rows (X is read once per launch).
 template <int D>
-cudaError_t launch_tc(const void *X, const void *W, void *out, long rows, cudaStream_t stream) {
+cudaError_t launch_tc(const void *X, const void *W, void *out, long rows, int m, cudaStream_t stream) {
   using Lay = FavLayout<D>;
   const cudaError_t attr = ensure_smem_optin((const void *)favor_tc_kernel<D>, (int)Lay::Bytes);
   if (attr != cudaSuccess) return attr;
-  FavorParams p;
-  if (!make_map2(&p.tx, X, rows, D) || !make_map2(&p.tw, W, kFavM, D) || !make_map2(&p.to, out, rows, kFavM))
-    return cudaErrorInvalidValue;
-  p.tiles = (int)((rows + 127) / 128);
   const int sms = std::max(1, device_info(-1).sm_count);
-  LaunchTimer timer(kKFavor, stream);
-  favor_tc_kernel<D><<<std::min(p.tiles, sms), kFavThreads, Lay::Bytes, stream>>>(p);
-  const cudaError_t e = cudaGetLastError();
-  timer.done(e);
-  if (e == cudaSuccess) count_launch();
-  return e;
+  for (int col0 = 0; col0 < m; col0 += kFavM) {
+    FavorParams p;
+    const void *Wb = static_cast<const __nv_bfloat16 *>(W) + (long)col0 * D;
+    if (!make_map2(&p.tx, X, rows, D) || !make_map2(&p.tw, Wb, kFavM, D) || !make_map2(&p.to, out, rows, m))
+      return cudaErrorInvalidValue;
+    p.tiles = (int)((rows + 127) / 128);
+    p.col0 = col0;
+    p.inv_sqrt_m = (float)(1.0 / std::sqrt((double)m));
+    LaunchTimer timer(kKFavor, stream);
+    favor_tc_kernel<D><<<std::min(p.tiles, sms), kFavThreads, Lay::Bytes, stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    timer.done(e);
+    if (e != cudaSuccess) return e;
+    count_launch();
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -282,9 +292,9 @@ cudaError_t launch_favor_features(const void *X, const void *W, void *out, long 
                                   cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const DeviceInfo &di = device_info(-1);
-  const bool tc = dt == LA_BF16 && m == kFavM && (d == 64 || d == 128) && rows <= 0x7fffff80L &&
+  const bool tc = dt == LA_BF16 && (m == kFavM || m == 2 * kFavM) && (d == 64 || d == 128) && rows <= 0x7fffff80L &&
                   di.cc_major == 10 && di.cc_minor == 3 && tensor_map_encoder() != nullptr;
-  if (tc) return d == 64 ? launch_tc<64>(X, W, out, rows, stream) : launch_tc<128>(X, W, out, rows, stream);
+  if (tc) return d == 64 ? launch_tc<64>(X, W, out, rows, m, stream) : launch_tc<128>(X, W, out, rows, m, stream);
   LaunchTimer timer(kKFavor, stream);
   if (dt == LA_F32)
     favor_simt_kernel<float><<<(unsigned)rows, 128, sizeof(float) * d, stream>>>(

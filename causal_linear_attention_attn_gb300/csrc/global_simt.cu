@@ -5,6 +5,9 @@
 // §5 and §8; "Linear Attention Math", "The associativity trick, written
 // out").  The sum over N is split across CTAs that add their partial states
 // into S, z with fp32 atomics (S, z are zeroed first on the same stream).
+// Each build CTA accumulates the 128 state rows [128 z, 128 z + 128), z =
+// blockIdx.z, so that a 256-row state (given features, m = 256) keeps 64
+// entries a thread in registers.
 #include <algorithm>
 
 #include "common.cuh"
@@ -15,8 +18,11 @@ namespace {
 
 constexpr int kT = 64;
 constexpr int kThreads = 256;
-constexpr int kMaxEntries = 128 * 128 / kThreads;  // state entries per thread
-constexpr int kReadTokens = 128;                    // tokens per read CTA
+constexpr int kSliceRows = 128;                           // state rows a build CTA accumulates
+constexpr int kMaxEntries = kSliceRows * 128 / kThreads;  // state entries per thread (d_v <= 128)
+
+// Tokens per read CTA: 128, or 64 where the state is 256 rows (given features, m = 256).
+__host__ __device__ inline int read_tokens(int dk) { return dk > 128 ? 64 : 128; }
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
@@ -31,7 +37,8 @@ __global__ void __launch_bounds__(kThreads)
   const long tb = N * blockIdx.y / splits, te = N * (blockIdx.y + 1) / splits;
   const Tin *kh = k + bh * N * dk;
   const Tin *vh = v + bh * N * dv;
-  const int ne = dk * dv / kThreads;  // >= 4 for the supported sizes
+  const int i0 = blockIdx.z * kSliceRows, dks = min(kSliceRows, dk - i0);  // this CTA's state rows
+  const int ne = dks * dv / kThreads;  // >= 4 for the supported sizes
 
   float acc[kMaxEntries];
 #pragma unroll
@@ -52,20 +59,20 @@ __global__ void __launch_bounds__(kThreads)
     for (int r = 0; r < kMaxEntries; ++r) {
       if (r < ne) {
         const int e = tid + r * kThreads;
-        const int i = e / dv, c = e - i * dv;
+        const int i = i0 + e / dv, c = e % dv;
         float s = acc[r];
         for (int j = 0; j < T; ++j) s = fmaf(Ks[j * dkp + i], Vs[j * dv + c], s);
         acc[r] = s;
       }
     }
-    if (tid < dk)
-      for (int j = 0; j < T; ++j) zacc += Ks[j * dkp + tid];
+    if (tid < dks)
+      for (int j = 0; j < T; ++j) zacc += Ks[j * dkp + i0 + tid];
   }
-  float *Sh = S_g + bh * (long)dk * dv;
+  float *Sh = S_g + bh * (long)dk * dv + (long)i0 * dv;
 #pragma unroll
   for (int r = 0; r < kMaxEntries; ++r)
     if (r < ne) atomicAdd(Sh + tid + r * kThreads, acc[r]);
-  if (tid < dk) atomicAdd(z_g + bh * dk + tid, zacc);
+  if (tid < dks) atomicAdd(z_g + bh * dk + i0 + tid, zacc);
 }
 
 template <typename Tin>
@@ -74,15 +81,15 @@ __global__ void __launch_bounds__(kThreads)
                        const float *__restrict__ z_g, float *__restrict__ out, long N, int dk, int dv,
                        float eps, int identity) {
   extern __shared__ float sm[];
-  const int dkp = dk + 1;
+  const int dkp = dk + 1, rt = read_tokens(dk);
   float *S = sm;                    // [dk][dv]
   float *z = S + dk * dv;           // [dk]
-  float *Qs = z + dk;               // [kReadTokens][dkp]
-  float *den = Qs + kReadTokens * dkp;  // [kReadTokens]
+  float *Qs = z + dk;               // [rt][dkp]
+  float *den = Qs + rt * dkp;       // [rt]
   const long bh = blockIdx.x;
   const int tid = threadIdx.x;
-  const long t0 = (long)blockIdx.y * kReadTokens;
-  const int T = (int)min((long)kReadTokens, N - t0);
+  const long t0 = (long)blockIdx.y * rt;
+  const int T = (int)min((long)rt, N - t0);
   for (int e = tid; e < dk * dv; e += kThreads) S[e] = S_g[bh * dk * dv + e];
   for (int i = tid; i < dk; i += kThreads) z[i] = z_g[bh * dk + i];
   const Tin *qh = q + (bh * N + t0) * dk;
@@ -121,18 +128,19 @@ cudaError_t launch_t(const Problem &p, bool identity) {
   const size_t smem1 = sizeof(float) * ((size_t)kT * (p.dk + 1) + (size_t)kT * p.dv);
   e = cudaFuncSetAttribute(global_state_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
   if (e != cudaSuccess) return e;
+  const unsigned slices = (unsigned)((p.dk + kSliceRows - 1) / kSliceRows);
   LaunchTimer t1(kKGlobalState, p.stream);
-  global_state_kernel<Tin><<<dim3(p.BH, (unsigned)splits), kThreads, smem1, p.stream>>>(
+  global_state_kernel<Tin><<<dim3(p.BH, (unsigned)splits, slices), kThreads, smem1, p.stream>>>(
       (const Tin *)p.k, (const Tin *)p.v, p.S, p.z, p.N, p.dk, p.dv, (int)splits, identity ? 1 : 0);
   e = cudaGetLastError();
   t1.done(e);
   if (e != cudaSuccess) return e;
   count_launch();
-  const size_t smem2 = sizeof(float) * ((size_t)p.dk * p.dv + p.dk + (size_t)kReadTokens * (p.dk + 1) +
-                                        kReadTokens);
+  const int rt = read_tokens(p.dk);
+  const size_t smem2 = sizeof(float) * ((size_t)p.dk * p.dv + p.dk + (size_t)rt * (p.dk + 1) + rt);
   e = cudaFuncSetAttribute(global_read_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
   if (e != cudaSuccess) return e;
-  const unsigned tiles = (unsigned)((p.N + kReadTokens - 1) / kReadTokens);
+  const unsigned tiles = (unsigned)((p.N + rt - 1) / rt);
   LaunchTimer t2(kKGlobalRead, p.stream);
   global_read_kernel<Tin><<<dim3(p.BH, tiles), kThreads, smem2, p.stream>>>((const Tin *)p.q, p.S, p.z, p.out,
                                                                           p.N, p.dk, p.dv, p.eps, identity ? 1 : 0);

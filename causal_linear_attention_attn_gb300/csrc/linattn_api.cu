@@ -22,6 +22,9 @@ std::atomic<unsigned long long> g_launches{0};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+// Feature counts of the calls on given features: the head sizes, and m = 256 (m = 2d at d = 128)
+// when the state (m x d_v fp32) fits the CUDA-core kernels' shared memory (d_v <= 128).
+bool supported_features(int m, int dv) { return supported_dim(m) || (m == 256 && dv <= 128); }
 
 thread_local cudaError_t t_last_error = cudaSuccess;
 
@@ -39,13 +42,14 @@ la_status from_cuda(cudaError_t e) {
   }
 }
 
-// Shared checks.  need_seq: q,k,v,out are read/written (B*H*N > 0).
+// Shared checks.  features: q and k are given features of any supported feature count.
 la_status validate(const void *q, const void *k, const void *v, const float *out, const float *S,
-                   const float *z, int B, int H, long N, int dk, int dv, float eps, la_dtype dt) {
+                   const float *z, int B, int H, long N, int dk, int dv, float eps, la_dtype dt,
+                   bool features = false) {
   if (B < 0 || H < 0 || N < 0 || dk <= 0 || dv <= 0) return LA_ERR_INVALID_VALUE;
   if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_VALUE;
   if (dt != LA_F32 && dt != LA_BF16) return LA_ERR_UNSUPPORTED;
-  if (!supported_dim(dk) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
+  if (!(features ? supported_features(dk, dv) : supported_dim(dk)) || !supported_dim(dv)) return LA_ERR_UNSUPPORTED;
   const long BH = (long)B * H;
   if (BH > 0x7fffffffL) return LA_ERR_INVALID_VALUE;
   if (BH > 0 && (!S || !z)) return LA_ERR_INVALID_VALUE;
@@ -295,7 +299,7 @@ la_status la_retention_with_state(const void *q, const void *k, const void *v, f
 
 la_status la_causal_features(const void *phi_q, const void *phi_k, const void *v, float *out, float *S, float *z,
                              int B, int H, int N, int m, int d_v, float eps, la_dtype dt, void *stream) {
-  la_status st = la::validate(phi_q, phi_k, v, out, S, z, B, H, N, m, d_v, eps, dt);
+  la_status st = la::validate(phi_q, phi_k, v, out, S, z, B, H, N, m, d_v, eps, dt, true);
   if (st != LA_OK) return st;
   if ((long)B * H == 0) return LA_OK;
   int dev;
@@ -312,7 +316,7 @@ la_status la_causal_features(const void *phi_q, const void *phi_k, const void *v
 
 la_status la_global_features(const void *phi_q, const void *phi_k, const void *v, float *out, float *S, float *z,
                              int B, int H, int N, int m, int d_v, float eps, la_dtype dt, void *stream) {
-  la_status st = la::validate(phi_q, phi_k, v, out, S, z, B, H, N, m, d_v, eps, dt);
+  la_status st = la::validate(phi_q, phi_k, v, out, S, z, B, H, N, m, d_v, eps, dt, true);
   if (st != LA_OK) return st;
   if ((long)B * H == 0) return LA_OK;
   int dev;
@@ -329,7 +333,7 @@ la_status la_favor_features(const void *x, const void *W, void *phi, int B, int 
   if (rows == 0) return LA_OK;
   if (!x || !W || !phi) return LA_ERR_INVALID_VALUE;
   if (dt != LA_F32 && dt != LA_BF16) return LA_ERR_UNSUPPORTED;
-  if (!la::supported_dim(d) || !la::supported_dim(m)) return LA_ERR_UNSUPPORTED;
+  if (!la::supported_dim(d) || !(la::supported_dim(m) || m == 256)) return LA_ERR_UNSUPPORTED;
   if (!la::aligned16(x) || !la::aligned16(W) || !la::aligned16(phi)) return LA_ERR_MISALIGNED;
   int dev;
   la_status st = la::current_device(&dev);

@@ -163,8 +163,11 @@ LA_API la_status la_causal_noalloc(const void *q, const void *k, const void *v, 
  * (random or orthogonal random projections, drawn by the caller).
  *
  * x: [B,H,N,d], W: [m,d], phi: [B,H,N,m], all of dtype dt (phi is written).
- * d and m in {32, 64, 128}.  Tensor cores for bf16 with m = 128 and d in {64,
- * 128}; CUDA cores otherwise.  Allocates nothing.  Errors as la_causal.
+ * d in {32, 64, 128}; m in {32, 64, 128, 256} (the page notes that more
+ * features give a closer approximation; m = 256 is m = 2d at d = 128).
+ * Tensor cores for bf16 with m in {128, 256} and d in {64, 128} (one launch
+ * per 128 features, each reading x); CUDA cores otherwise.  Allocates
+ * nothing.  Errors as la_causal.
  * The features feed la_causal_features (or la_global / la_causal with any
  * caller-side map) as phi(q), phi(k).
  */
@@ -178,9 +181,12 @@ LA_API la_status la_favor_features(const void *x, const void *W, void *phi, int 
  * non-negative feature map, e.g. la_favor_features ("Linear Attention Math",
  * "Feature maps: elu+1 and positive random features": the normalized read
  * needs non-negative features).  phi_q, phi_k: [B,H,N,m] (dtype dt, m in
- * {32, 64, 128}); other arguments, results and errors as la_causal.  The
- * tensor-core path (bf16, m = d_v = 128) takes the features as given, so no
- * leading tokens are recomputed in fp32.
+ * {32, 64, 128}, or 256 with d_v <= 128); S: [B,H,m,d_v]; z: [B,H,m]; other
+ * arguments, results and errors as la_causal.  The tensor-core path (bf16,
+ * m = d_v = 128) takes the features as given, so no leading tokens are
+ * recomputed in fp32; every other size runs the exact fp32 CUDA-core pass
+ * (32-token chunks at m = 256, where a 64-token chunk and the 128 KB state
+ * would not fit in shared memory).
  */
 LA_API la_status la_causal_features(const void *phi_q, const void *phi_k, const void *v, float *out, float *S,
                                     float *z, int B, int H, int N, int m, int d_v, float eps, la_dtype dt,

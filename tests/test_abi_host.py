@@ -160,6 +160,8 @@ def test_favor_validation():
     assert call(N=-1) == INVALID
     assert call(m=0) == INVALID
     assert call(m=96) == UNSUPPORTED
+    assert call(m=512) == UNSUPPORTED  # m = 256 (m = 2d at d = 128) is the largest
+    assert call(d=256) == UNSUPPORTED  # the input dimension stays a head size
     assert call(d=48) == UNSUPPORTED
     assert call(dt=4) == UNSUPPORTED
     assert call(Wp=P + 2) == MISALIGNED
@@ -169,6 +171,12 @@ def test_favor_validation():
     assert seq("la_causal_features", dk=48) == UNSUPPORTED
     assert seq("la_global_features", v=None) == INVALID
     assert seq("la_global_features", dv=96) == UNSUPPORTED
+    # 256 given features only with d_v <= 128, and only on the calls that take given features
+    assert seq("la_causal_features", dk=512) == UNSUPPORTED
+    assert seq("la_global_features", dk=256, dv=256) == UNSUPPORTED
+    assert seq("la_causal", dk=256) == UNSUPPORTED
+    assert seq("la_global", dk=256) == UNSUPPORTED
+    assert seq("la_causal_features", dk=256, S=P + 4) == MISALIGNED
 
 
 def test_backward_validation():

@@ -39,7 +39,7 @@ def _rel_err(got, ref):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("d,m", [(128, 128), (64, 128), (128, 64), (32, 32)])
+@pytest.mark.parametrize("d,m", [(128, 128), (64, 128), (128, 64), (32, 32), (128, 256), (64, 256)])
 @pytest.mark.parametrize("N", [1, 129, 1000])
 def test_features_every_element(cuda_lib, dtype, d, m, N):
     w = dataclasses.replace(W, dk=d, dv=d, dtype=dtype)
@@ -52,8 +52,10 @@ def test_features_every_element(cuda_lib, dtype, d, m, N):
     assert _rel_err(phi, ref) <= (2.0 ** -8 if dtype == "bf16" else 1e-5)
 
 
+# (B, H, N, m, d_v); m = 256 is the m = 2d setting (32-token chunks on the CUDA cores)
 SHAPES = [(1, 1, 1, 128, 128), (1, 2, 300, 128, 128), (1, 1, 2000, 128, 128), (3, 1, 4097, 128, 128),
-          (2, 19, 1024, 128, 128), (1, 2, 700, 64, 128), (2, 1, 129, 32, 64)]
+          (2, 19, 1024, 128, 128), (1, 2, 700, 64, 128), (2, 1, 129, 32, 64), (1, 2, 300, 256, 128),
+          (2, 1, 65, 256, 32), (1, 1, 1, 256, 64)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -74,7 +76,8 @@ def test_causal_on_given_features_every_element(cuda_lib, shape, dtype):
     assert_close(z, rz, tau, "z")
 
 
-@pytest.mark.parametrize("shape", [(1, 2, 300, 128, 128), (2, 3, 1000, 64, 128), (1, 1, 129, 32, 32)],
+@pytest.mark.parametrize("shape", [(1, 2, 300, 128, 128), (2, 3, 1000, 64, 128), (1, 1, 129, 32, 32),
+                                   (1, 2, 300, 256, 128), (2, 1, 63, 256, 64)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_global_on_given_features_every_element(cuda_lib, shape, dtype):
@@ -110,4 +113,26 @@ def test_favor_causal_end_to_end_workload_shape(cuda_lib):
     assert_close(out.reshape(W.BH, W.N, -1)[heads], ro, TAU[torch.bfloat16], "out")
     assert_close(S.reshape(W.BH, 128, 128)[heads], rS, TAU[torch.bfloat16], "S")
     assert torch.isfinite(out).all()
+    assert cuda_lib.device_status() == 0
+
+
+def test_favor_twice_the_features_end_to_end(cuda_lib):
+    """m = 2d = 256 features of d = 128 bf16 inputs (two tensor-core feature launches), then the
+    causal read on them (CUDA cores); every output against the oracle's bf16-stored features and
+    its fp64 read, and every feature against the oracle's to 2^-8."""
+    w = dataclasses.replace(W, B=1, H=4, N=1500)
+    q, k, v = inputs.make_qkv(w)
+    P = inputs.favor_projections(w, m=256)
+    Pd = P.to(DEV)
+    fq, fk = cuda_lib.la_favor_features(q.to(DEV), Pd), cuda_lib.la_favor_features(k.to(DEV), Pd)
+    out, S, z = cuda_lib.la_causal_features(fq, fk, v.to(DEV), eps=w.eps)
+    torch.cuda.synchronize()
+    assert fq.shape == (1, 4, 1500, 256) and S.shape == (1, 4, 256, 128)
+    rq64, rk64 = oracle.favor_features(f64(q), f64(P)), oracle.favor_features(f64(k), f64(P))
+    assert _rel_err(fq, rq64) <= 2.0 ** -8 and _rel_err(fk, rk64) <= 2.0 ** -8
+    bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16).double().numpy()
+    ro, rS, rz = oracle.causal(bf16(rq64), bf16(rk64), f64(v), eps=w.eps, phi="identity", nthreads=4)
+    assert_close(out, ro, TAU[torch.bfloat16], "out")
+    assert_close(S, rS, TAU[torch.bfloat16], "S")
+    assert_close(z, rz, TAU[torch.bfloat16], "z")
     assert cuda_lib.device_status() == 0
