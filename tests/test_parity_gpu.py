@@ -60,7 +60,10 @@ def test_small_shapes_every_element(cuda_lib, form, dtype, shape):
 # Tensor-core global form (bf16, d_k = d_v in {64, 128}): clusters of 1 to 8 CTAs
 # per head in the state build, persistent read CTAs that cross many heads.
 GLOBAL_TC = [(1, 1, 1, 64), (1, 1, 8192, 64), (1, 1, 16384, 64), (2, 3, 129, 64), (4, 40, 200, 64),
-             (10, 100, 100, 64), (1, 2, 5000, 128), (2, 2, 383, 128), (1, 1, 1, 128), (3, 60, 130, 128)]
+             (10, 100, 100, 64), (1, 2, 5000, 128), (2, 2, 383, 128), (1, 1, 1, 128), (3, 60, 130, 128),
+             # d = 64 with more heads than half the SMs and fewer than all (one build CTA a head),
+             # ragged tails
+             (1, 100, 1000, 64), (3, 40, 257, 64), (1, 151, 128, 64), (2, 50, 4161, 64), (1, 77, 64, 64)]
 
 
 @pytest.mark.parametrize("shape", GLOBAL_TC, ids=lambda s: "x".join(map(str, s)))
