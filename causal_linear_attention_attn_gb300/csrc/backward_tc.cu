@@ -1159,17 +1159,18 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       const int myrow = 32 * wg + lane;
       const float inv_mine = myrow < T ? 1.f / p.den[(long)bh * N + t0 + myrow] : 0.f;
       const float gdn = myrow < T ? p.gden[(long)bh * N + t0 + myrow] : 0.f;
-      bool ok = it == 0 || wait(o_full, (it - 1) & 1);
-      if (bar_or(kBarG, 128, !ok)) break;
-#pragma unroll 1
-      for (int rr = 0; rr < 32; rr += 16) {  // two rounds of 16 rows in flight
-        float4 gg[16];
+      // gnum rows in two rounds of 16; dO is an input, so the first round's loads go out
+      // before the wait for the previous chunk's products (which still read the N tiles)
+      float4 gg[16];
+      auto load_round = [&](int rr) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int row = 32 * wg + rr + e;
           gg[e] = row < T ? __ldg(reinterpret_cast<const float4 *>(gh + (t0 + row) * kD + col))
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+      };
+      auto store_round = [&](int rr) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int row = 32 * wg + rr + e;
@@ -1181,7 +1182,13 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           *reinterpret_cast<uint2 *>(Nhi + o) = make_uint2(h0, h1);
           *reinterpret_cast<uint2 *>(Nlo + o) = make_uint2(l0, l1);
         }
-      }
+      };
+      load_round(0);
+      bool ok = it == 0 || wait(o_full, (it - 1) & 1);
+      if (bar_or(kBarG, 128, !ok)) break;
+      store_round(0);
+      load_round(16);
+      store_round(16);
       gd[myrow] = gdn;
       fence_async_smem();
       mbar_arrive(n_ready);
