@@ -965,7 +965,9 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           if (kDk) prefetch_l2(kh + t1 * kD, kC * kD * 2);
           prefetch_l2(gh + t1 * kD, kC * kD * 4);
         }
-        if (!wait(q_ready, ph) || !wait(k_ready, ph) || !wait(n_ready, ph)) break;
+        // X needs only the key operand and one other: the query pairs (role 0, X = K Q^T) or the
+        // gnum pairs (role 1, X = V gnum^T); the remaining one is waited for before O += X B
+        if (!wait(k_ready, ph) || !wait(kDk ? n_ready : q_ready, ph)) break;
         if (it > 0 && !wait(o_done, (it - 1) & 1)) break;
         tc_fence_after();
         if (!kDk) {
@@ -1003,7 +1005,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           }
         }
         mma_commit(x_full);
-        if (!wait(x_split, ph)) break;
+        if (!wait(x_split, ph) || !wait(kDk ? q_ready : n_ready, ph)) break;
         tc_fence_after();
         // O += X B with X from tensor memory as pairs (queries [16 ks, 16 ks + 16): 8 columns hi,
         // 8 lo) and B = gnum (role 0) or phi(Q) (role 1), rows = queries
