@@ -507,7 +507,8 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
           prefetch_l2(vh + t1 * kD, rows * kD * 2);
           prefetch_l2(gh + t1 * kD, rows * kD * 4);
         }
-        if (!wait(q_ready, ph) || !wait(k_ready, ph) || !wait(g_ready, ph) || !wait(v_full, ph)) break;
+        // each product waits only for its own operands
+        if (!wait(q_ready, ph) || !wait(k_ready, ph)) break;
         tc_fence_after();
         // A = Q K^T (pairs: Qh Kh + Qh Kl + Ql Kh)
 #pragma unroll 4
@@ -516,6 +517,8 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
           mma_bf16_ts(tX, tQh + 8 * ks, kdesc(sKlo, ks), iKK, 1);
           mma_bf16_ts(tX, tQl + 8 * ks, kdesc(sKhi, ks), iKK, 1);
         }
+        if (!wait(g_ready, ph) || !wait(v_full, ph)) break;
+        tc_fence_after();
         // C = dO V^T
 #pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
@@ -523,20 +526,23 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
           mma_bf16(tCB, kdesc(sGlo, ks), kdesc(sV, ks), iKK, 1);
         }
         mma_commit(ac_full);
-        if (!wait(s_ready, ph) || !wait(x_free, ph)) break;
+        // S += K^T V once the pair copy of S_prev has been taken
+        if (!wait(s_ready, ph)) break;
         tc_fence_after();
-        // Y = dO S_prev^T (S copy rows = features i, K-major over value components)
+#pragma unroll 4
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16(tS, mndesc(sKhi, ks), mndesc(sV, ks), iMM, 1);
+          mma_bf16(tS, mndesc(sKlo, ks), mndesc(sV, ks), iMM, 1);
+        }
+        // Y = dO S_prev^T (S copy rows = features i, K-major over value components), into X once
+        // the epilogue has read A from it
+        if (!wait(x_free, ph)) break;
+        tc_fence_after();
 #pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16(tX, kdesc(sGhi, ks), kdesc(sShi, ks), iKK, ks > 0);
           mma_bf16(tX, kdesc(sGhi, ks), kdesc(sSlo, ks), iKK, 1);
           mma_bf16(tX, kdesc(sGlo, ks), kdesc(sShi, ks), iKK, 1);
-        }
-        // S += K^T V
-#pragma unroll 4
-        for (int ks = 0; ks < 8; ++ks) {
-          mma_bf16(tS, mndesc(sKhi, ks), mndesc(sV, ks), iMM, 1);
-          mma_bf16(tS, mndesc(sKlo, ks), mndesc(sV, ks), iMM, 1);
         }
         mma_commit(y_full);
         if (!wait(cb_ready, ph)) break;
