@@ -429,7 +429,6 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
         const int s = c % kStages;
         const uint32_t u = c / kStages;
         if (!mbar_wait(&phi_done[s], u & 1, abort_word, status, p.wait_ns)) break;
-        if (!mbar_wait(&full_v[s], u & 1, abort_word, status, p.wait_ns)) break;
         // retention: the keys reach Q K^T as loaded (no in-place pass before it)
         if (kRet && !mbar_wait(&full_k[s], u & 1, abort_word, status, p.wait_ns)) break;
         const uint32_t k = sK + s * kTile, v = sV + s * kTile;
@@ -442,6 +441,8 @@ __global__ void __maxnreg__(96) causal_tc_kernel(const __grid_constant__ TcParam
 #pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) mma_bf16_ts(tP, tQ + 8 * ks, kdesc(k, ks), iKK, ks > 0);
         mma_commit(p_full);
+        // V is first read by the state update (Q K^T does not need it)
+        if (!mbar_wait(&full_v[s], u & 1, abort_word, status, p.wait_ns)) break;
         // S += K^T V; retention: the weighted keys as a pair, the low parts (in the Q slot) first
         // so that the slot is released for the next chunk's Q as early as possible
         auto state_update = [&](uint32_t a) {
