@@ -992,6 +992,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
             mma_bf16_ts(tX, tKh + 8 * ks, kdesc(sNlo, ks), iKK, 1);
           }
         }
+        mma_commit(x_full);  // the epilogue splits X while O = K U (or V U^T) runs
         if (!wait(u_ready, ph)) break;
         tc_fence_after();
         if (!kDk) {
@@ -1010,7 +1011,6 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
             mma_bf16_ts(tO, tKh + 8 * ks, kdesc(sUlo, ks), iKK, 1);
           }
         }
-        mma_commit(x_full);
         if (!wait(x_split, ph) || !wait(kDk ? q_ready : n_ready, ph)) break;
         tc_fence_after();
         // O += X B with X from tensor memory as pairs (queries [16 ks, 16 ks + 16): 8 columns hi,
