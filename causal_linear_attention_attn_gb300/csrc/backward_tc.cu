@@ -917,7 +917,8 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::Bars);
   uint64_t *q_ready = bars + 0, *k_ready = bars + 1, *n_ready = bars + 2, *u_ready = bars + 3, *x_full = bars + 4,
            *x_split = bars + 5, *o_full = bars + 6, *o_done = bars + 7, *drain = bars + 8, *q_full = bars + 9,
-           *q_used = bars + 10;
+           *q_used = bars + 10,
+           *u_done = bars + 11;  // the chunk's U update complete: its operand tiles and U are free
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::Misc);
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + L::Misc + 4);
   unsigned int *status = &g_bwd_status;
@@ -937,6 +938,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
     mbar_init(x_full, 1);
     mbar_init(x_split, 128);
     mbar_init(o_full, 1);
+    mbar_init(u_done, 1);
     mbar_init(o_done, 128);
     mbar_init(drain, 1);
     mbar_init(q_full, 1);
@@ -1022,6 +1024,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           mma_bf16_ts(tO, tX + 16 * ks + 8, mndesc(sBhi, ks), iKM, 1);
           mma_bf16_ts(tO, tX + 16 * ks, mndesc(sBlo, ks), iKM, 1);
         }
+        mma_commit(o_full);  // the epilogue reads O while U is updated
         // U += Q^T gnum
 #pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
@@ -1029,7 +1032,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           mma_bf16(tU, mndesc(sQhi, ks), mndesc(sNlo, ks), iMM, 1);
           mma_bf16(tU, mndesc(sQlo, ks), mndesc(sNhi, ks), iMM, 1);
         }
-        mma_commit(o_full);
+        mma_commit(u_done);
       }
       mma_commit(drain);
       wait_drain(drain, 0, status);
@@ -1078,7 +1081,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         load_row_half(key + (t0 + r) * kD, *reinterpret_cast<uint4 (*)[8]>(&x[0]), 0);
         load_row_half(key + (t0 + r) * kD, *reinterpret_cast<uint4 (*)[8]>(&x[8]), 1);
       }
-      ok = it == 0 || wait(o_full, (it - 1) & 1);
+      ok = it == 0 || wait(u_done, (it - 1) & 1);
       if (bar_or(kBarQK, 128, !ok)) break;
       tc_fence_after();
       // key operand, row r: role 0 phi(k) pairs (hi columns 0-63, lo 64-127), role 1 v as given;
@@ -1126,7 +1129,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
     }
     // role 0: the initial state's gradient dS0 = U after the first chunk
     if (!kDk && p.dS0) {
-      ok = ok && wait(o_full, (nch - 1) & 1);
+      ok = ok && wait(u_done, (nch - 1) & 1);
       if (!bar_or(kBarQK, 128, !ok) && !*abort_word) {
         tc_fence_after();
         float *dst = p.dS0 + ((long)bh * kD + r) * kD;
@@ -1192,7 +1195,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         }
       };
       load_round(0);
-      bool ok = it == 0 || wait(o_full, (it - 1) & 1);
+      bool ok = it == 0 || wait(u_done, (it - 1) & 1);
       if (bar_or(kBarG, 128, !ok)) break;
       store_round(0);
       load_round(16);
