@@ -870,7 +870,7 @@ struct P2Layout {
   static constexpr uint32_t Gd = 7 * kTile;  // [128] gden of the chunk
   static constexpr uint32_t Ub = Gd + 512;   // [128] u carried into the chunk (role 1)
   static constexpr uint32_t Bars = Ub + 512;
-  static constexpr int kNumBars = 12;
+  static constexpr int kNumBars = 13;
   static constexpr uint32_t Misc = Bars + kNumBars * 8;
   static constexpr uint32_t Bytes = Misc + 16;
 };
@@ -918,7 +918,8 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
   uint64_t *q_ready = bars + 0, *k_ready = bars + 1, *n_ready = bars + 2, *u_ready = bars + 3, *x_full = bars + 4,
            *x_split = bars + 5, *o_full = bars + 6, *o_done = bars + 7, *drain = bars + 8, *q_full = bars + 9,
            *q_used = bars + 10,
-           *u_done = bars + 11;  // the chunk's U update complete: its operand tiles and U are free
+           *u_done = bars + 11,  // the chunk's U update complete: its operand tiles and U are free
+           *ucol_done = bars + 12;  // role 1: the epilogue's read of the Q tiles and gd for u is done
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::Misc);
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + L::Misc + 4);
   unsigned int *status = &g_bwd_status;
@@ -939,6 +940,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
     mbar_init(x_split, 128);
     mbar_init(o_full, 1);
     mbar_init(u_done, 1);
+    mbar_init(ucol_done, 128);
     mbar_init(o_done, 128);
     mbar_init(drain, 1);
     mbar_init(q_full, 1);
@@ -1101,9 +1103,10 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(k_ready);
-      if (it > 0) {
-        // the pair copy of U (every chunk after this one folded in); the tiles were last read by
-        // the previous chunk's products, which have completed
+      // the pair copy of U (every chunk after this one folded in); the tiles were last read by
+      // the previous chunk's products, which have completed
+      auto copy_u = [&]() {
+        if (it == 0) return;
         for (int cb = 0; cb < 8; ++cb) {
           uint32_t w[16];
           tmem_ld16(tl + kP2U + cb * 16, w);
@@ -1116,16 +1119,24 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
             *tile_chunk(Ulo, r, cb * 16 + 8 * q) = make_uint4(l[0], l[1], l[2], l[3]);
           }
         }
-      }
+      };
+      // half of the phi(Q) pairs from the staged raw queries (the N warps take the other half)
+      auto query_half = [&]() -> bool {
+        // role 1: the epilogue reads the previous chunk's query pairs for u after its split
+        ok = wait(q_full, it & 1) && (!kDk || it == 0 || wait(ucol_done, (it - 1) & 1));
+        if (bar_or(kBarQK, 128, !ok)) return false;
+        query_pairs_staged(sm, threadIdx.x - 32, T);
+        fence_async_smem();
+        mbar_arrive(q_ready);
+        mbar_arrive(q_used);  // this half is done with the staging tile
+        return true;
+      };
+      // role 0's first product X = K Q^T takes the query pairs; role 1's, X = V gnum^T, does not
+      if (!kDk && !query_half()) break;
+      copy_u();
       fence_async_smem();
       mbar_arrive(u_ready);
-      // half of the phi(Q) pairs from the staged raw queries (the N warps take the other half)
-      ok = wait(q_full, it & 1);
-      if (bar_or(kBarQK, 128, !ok)) break;
-      query_pairs_staged(sm, threadIdx.x - 32, T);
-      fence_async_smem();
-      mbar_arrive(q_ready);
-      mbar_arrive(q_used);  // this half is done with the staging tile
+      if (kDk && !query_half()) break;
     }
     // role 0: the initial state's gradient dS0 = U after the first chunk
     if (!kDk && p.dS0) {
@@ -1170,8 +1181,9 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       const int myrow = 32 * wg + lane;
       const float inv_mine = myrow < T ? 1.f / p.den[(long)bh * N + t0 + myrow] : 0.f;
       const float gdn = myrow < T ? p.gden[(long)bh * N + t0 + myrow] : 0.f;
-      // gnum rows in two rounds of 16; dO is an input, so the first round's loads go out
-      // before the wait for the previous chunk's products (which still read the N tiles)
+      // gnum rows in two rounds of 16; dO is an input, so where gnum is needed first (role 1)
+      // the first round's loads go out before the wait for the previous chunk's products (which
+      // still read the N tiles)
       float4 gg[16];
       auto load_round = [&](int rr) {
 #pragma unroll
@@ -1194,28 +1206,45 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           *reinterpret_cast<uint2 *>(Nlo + o) = make_uint2(l0, l1);
         }
       };
-      load_round(0);
-      bool ok = it == 0 || wait(u_done, (it - 1) & 1);
-      if (bar_or(kBarG, 128, !ok)) break;
-      store_round(0);
-      load_round(16);
-      store_round(16);
-      gd[myrow] = gdn;
-      fence_async_smem();
-      mbar_arrive(n_ready);
+      auto gnum_rest = [&]() {  // round 0 already loaded
+        store_round(0);
+        load_round(16);
+        store_round(16);
+        gd[myrow] = gdn;
+        fence_async_smem();
+        mbar_arrive(n_ready);
+      };
       // phi(Q) pairs from the staged raw queries (same swizzled layout), then the next chunk's
-      // raw queries into the staging tile
-      ok = wait(q_full, it & 1);
-      if (bar_or(kBarG, 128, !ok)) break;
-      query_pairs_staged(sm, 128 + gt, T);
-      fence_async_smem();
-      mbar_arrive(q_ready);
-      mbar_arrive(q_used);
-      // the next chunk's raw queries once both halves are done with the staging tile
-      bool okq = true;
-      if (gt == 0 && c > 0) okq = wait(q_used, it & 1);
-      if (bar_or(kBarG, 128, !okq)) break;
-      if (gt == 0 && c > 0) load_q(c - 1);
+      // raw queries into the staging tile once both halves are done with it
+      auto query_half = [&]() -> bool {
+        bool okq = wait(q_full, it & 1);
+        if (bar_or(kBarG, 128, !okq)) return false;
+        query_pairs_staged(sm, 128 + gt, T);
+        fence_async_smem();
+        mbar_arrive(q_ready);
+        mbar_arrive(q_used);
+        okq = true;
+        if (gt == 0 && c > 0) okq = wait(q_used, it & 1);
+        if (bar_or(kBarG, 128, !okq)) return false;
+        if (gt == 0 && c > 0) load_q(c - 1);
+        return true;
+      };
+      if (kDk) {
+        // role 1: X = V gnum^T comes first
+        load_round(0);
+        // the epilogue's read of gd (and of the query pairs) for u must be done before gd changes
+        const bool ok = it == 0 || (wait(u_done, (it - 1) & 1) && wait(ucol_done, (it - 1) & 1));
+        if (bar_or(kBarG, 128, !ok)) break;
+        gnum_rest();
+        if (!query_half()) break;
+      } else {
+        // role 0: X = K Q^T comes first; gnum is first needed by O += X gnum
+        const bool ok = it == 0 || wait(u_done, (it - 1) & 1);
+        if (bar_or(kBarG, 128, !ok)) break;
+        if (!query_half()) break;
+        load_round(0);
+        gnum_rest();
+      }
     }
     if (gt == 0 && q_issued > 0) wait_drain(q_full, (q_issued - 1) & 1, status);
   } else {
@@ -1248,10 +1277,13 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         tmem_st32(tl + kP2X + cb * 32, rx);
         tmem_st32(tl + kP2X + cb * 32 + 32, ry);
       }
+      tc_fence_before();
+      mbar_arrive(x_split);
       float ucol = 0.f;
       if (kDk) {
-        // this chunk's share of u for feature j: sum over its queries of phi(q_t)_j gden_t.  Read
-        // before x_split: the Q tiles are reloaded as soon as this chunk's products complete
+        // this chunk's share of u for feature j: sum over its queries of phi(q_t)_j gden_t, read
+        // while O += X Q and the U update run (the operand warps wait for ucol_done before they
+        // overwrite the query pairs or gd)
         const uint8_t *bh_ = Qhi + (j >> 6) * kBlk, *bl_ = Qlo + (j >> 6) * kBlk;
 #pragma unroll 4
         for (int t = 0; t < T; ++t) {
@@ -1260,14 +1292,13 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
                           __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(bl_ + off));
           ucol = fmaf(f, gd[t], ucol);
         }
+        mbar_arrive(ucol_done);
       }
-      tc_fence_before();
-      mbar_arrive(x_split);
+      const uint8_t *kr = reinterpret_cast<const uint8_t *>(kh + (t0 + j) * kD);
       ok = wait(o_full, it & 1);
       if (bar_or(kBarE, 128, !ok)) break;
       tc_fence_after();
       float *dst = (kDk ? p.dk : p.dv) + ((long)bh * N + t0 + j) * kD;
-      const uint8_t *kr = reinterpret_cast<const uint8_t *>(kh + (t0 + j) * kD);
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
         uint32_t ro[32];
