@@ -636,9 +636,17 @@ def decode_workload(args):
     return dataclasses.replace(w, B=args.decode_batch) if args.decode_batch else w
 
 
+# Forms on the bench line, in this order: a reader of only the line's end (a log that keeps its
+# tail) sees the long-context causal form, the global form and the decode step last.
+FORM_ORDER = ("causal_bf16_backward", "favor_bf16", "retention_bf16", "causal_bf16_with_state",
+              "retention_decode_bf16", "decode_bf16", "global_bf16", "causal_bf16_long")
+
+
 def compact(res: dict) -> dict:
     """The figures of one form that the bench line carries: step time, rate, step
-    roofline fraction, and the dominant kernel's name, live time and fraction."""
+    roofline fraction, and the dominant kernel's name, live time, fraction and
+    traffic (launch counts and clocks are in the --detail record; clock throttle
+    reasons, if any, are kept here)."""
     rl, step = res["roofline"], res["step_roofline"]
     c = {"ms": round(res.get("ms_per_call", res.get("us_per_step", 0.0) / 1e3), 5)}
     if "tokens_per_s" in res:
@@ -655,12 +663,15 @@ def compact(res: dict) -> dict:
         c["alu_frac"] = res["alu_roofline"]["frac"]
     if "tensor_roofline" in res:
         c["tensor_frac"] = res["tensor_roofline"]["frac"]
-    c["launches"] = res["gpu_launches"]
     clk = res.get("clocks") or {}
-    c["sm_mhz"] = clk.get("sm_mhz")
     if clk.get("reasons"):
         c["clock_reasons"] = clk["reasons"]
     return c
+
+
+def ordered_forms(forms: dict) -> dict:
+    names = [n for n in FORM_ORDER if n in forms] + [n for n in forms if n not in FORM_ORDER]
+    return {n: compact(forms[n]) for n in names}
 
 
 def carry_study(args):
@@ -783,8 +794,8 @@ def main_ours(args):
         "roofline": head["roofline"], "step_roofline": head["step_roofline"],
         "gpu_launches": head["gpu_launches"], "e2e": e2e, "clocks": clocks,
         "cpu_baseline": cpu,
-        # every other form, compact and last on the line (long-context causal and global first)
-        "forms": {name: compact(r) for name, r in forms.items()},
+        # every other form, compact and last on the line (long-context causal and global at the very end)
+        "forms": ordered_forms(forms),
     }
     if args.detail:
         with open(args.detail, "w") as f:
