@@ -7,7 +7,7 @@ feature map is checked element by element: the kernel's only rounding is
 the bf16 (or fp32) output, so every feature must be within 2^-8 (bf16) or
 1e-5 (fp32) of the oracle's, relative.  The causal read on given features is
 checked against the oracle's identity-map causal form on the same features
-(the spec bars).  The two together (FAVOR+ causal attention, features
+(1e-4 of the RMS for fp32 inputs, 2e-2 for bf16).  The two together (FAVOR+ causal attention, features
 stored in bf16 as the tensor-core read takes them) are checked on the
 workload's shape with sampled heads against the oracle's features rounded
 to bf16 and its read in fp64.  (Against unrounded fp64 features the
