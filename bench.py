@@ -319,6 +319,8 @@ def kernel_bytes(w, kernel: str) -> float:
         return w.BH * (w.N * (w.dk + w.dv) * ib + state)
     if kernel == "global_read":
         return w.BH * (w.N * w.dk * ib + state + w.N * 4 * w.dv)
+    if kernel == "global_fused":  # q, k, v in, out and the state written
+        return w.BH * (w.N * (2 * w.dk + w.dv) * ib + w.N * 4 * w.dv + state)
     if kernel == "decode":
         return decode_bytes(w)
     if kernel == "backward":

@@ -675,6 +675,328 @@ __global__ void __launch_bounds__(kReadThreads, 1) global_read_tc(const __grid_c
   }
 }
 
+// ------------------------------------------------------------------ one pass (d = 64, a CTA per head)
+
+// When the heads alone fill the SMs, one CTA per head builds S and z and then
+// reads every query of the same head: no kernel boundary and no grid-wide
+// wait lie between the two halves, and the head's first query tiles load
+// while its last key and value units are still being summed.
+//
+// Build: 128-token K | V units in a six-slot ring, phi(K) by sixteen warps,
+// S += phi(K)^T V with the two 64-token sub-tiles side by side (as in the
+// state build).  Hand-over: the column sums and S (the two diagonal blocks of
+// the accumulator) go to global memory and, as B = [bf16(S) | z hi | z lo | 0],
+// to shared memory.  Read: 128-token Q tiles in eight 16 KB stages over the
+// first four ring slots, phi(Q) by eight warps, one M = 128, N = 80, K = 64
+// MMA a tile into one of two accumulators, eight epilogue warps normalising
+// into two fp32 staging tiles over the last two ring slots.
+constexpr int kFusedThreads = 576;  // warp 0 TMA, 1 MMA, 2-17 phi(K); then 2-9 phi(Q), 10-17 epilogue
+constexpr int kFusedA = 512, kFusedPhi = 256, kFusedEpi = 256;
+constexpr uint32_t kBarFusedA = 1, kBarFusedEpi = 2;
+
+struct FusedLayout {
+  static constexpr int kSlots = 6;                  // K | V units
+  static constexpr uint32_t kSlot = 2 * kBlk;       // 32 KB: K then V, [128 tokens x 64] each
+  static constexpr int kQStages = 8;                // Q tiles of 16 KB over slots 0-3
+  static constexpr int NB = 80;                     // B rows: 64 columns of S, z hi, z lo, zeros
+  static constexpr uint32_t Out = 4 * kSlot;        // two fp32 output tiles of 32 KB over slots 4-5
+  static constexpr uint32_t Zred = Out;             // hand-over: [512 threads][8] column sums
+  static constexpr uint32_t Pst = Zred + kFusedA * 8 * 4;  // hand-over: accumulator rows [128][68] fp32
+  static constexpr int kPStride = 68;
+  static constexpr uint32_t B = kSlots * kSlot;
+  static constexpr uint32_t Zs = B + NB * 128;
+  static constexpr uint32_t Bars = Zs + 64 * 4;
+  static constexpr int kNumBars = 3 * kSlots + 2 + 3 * kQStages + 5;
+  static constexpr uint32_t Misc = Bars + kNumBars * 8;
+  static constexpr uint32_t Bytes = Misc + 16;
+  static_assert(Pst + 128 * kPStride * 4 <= B, "hand-over staging fits over slots 4-5");
+  static_assert(kQStages * kBlk <= Out, "Q stages fit over slots 0-3");
+  static_assert(B % 1024 == 0, "B stays 1024-aligned");
+};
+static_assert(FusedLayout::Bytes <= 232448, "shared memory budget");
+
+struct FusedParams {
+  CUtensorMap tk, tv, tq;  // [BH][N][64] bf16, box 64 x 128 x 1, 128-byte swizzle
+  CUtensorMap to;          // [BH][N][64] fp32, box 32 x 128 x 1, 128-byte swizzle
+  float *S, *z;
+  long N;
+  float eps;
+};
+
+__global__ void __launch_bounds__(kFusedThreads, 1) global_fused_tc(const __grid_constant__ FusedParams p) {
+  using Lay = FusedLayout;
+  constexpr int kSA = Lay::kSlots, kSB = Lay::kQStages, NB = Lay::NB, kPS = Lay::kPStride;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(&g_global_status, kAbortMisaligned);
+    return;
+  }
+  uint8_t *sm = smem_raw;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::Bars);
+  // build: unit landed, phi applied, slot free; S complete; B written
+  uint64_t *full = bars, *phi_done = bars + kSA, *empty = bars + 2 * kSA, *s_full = bars + 3 * kSA,
+           *b_ready = s_full + 1;
+  // read: Q landed, phi applied, Q stage free; accumulator full / read out (two of each)
+  uint64_t *full_q = b_ready + 1, *phi_q = full_q + kSB, *q_empty = phi_q + kSB, *acc_full = q_empty + kSB,
+           *acc_empty = acc_full + 2, *drain = acc_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::Misc);
+  volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + Lay::Misc + 4);
+  unsigned int *status = &g_global_status;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int n = (int)((p.N + 127) / 128);  // build units = read tiles
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSA; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&phi_done[s], kFusedA);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(b_ready, kFusedA);
+    for (int t = 0; t < kSB; ++t) {
+      mbar_init(&full_q[t], 1);
+      mbar_init(&phi_q[t], kFusedPhi);
+      mbar_init(&q_empty[t], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kFusedEpi / 32);
+    }
+    mbar_init(drain, 1);
+    *abort_word = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // build: S in columns 0-127; read: accumulators at 0 and 128
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&p.tk);
+      prefetch_tmap(&p.tv);
+      prefetch_tmap(&p.tq);
+      int issued_a = 0, issued_b = 0;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % kSA;
+        if (i >= kSA && !mbar_wait(&empty[s], (uint32_t)(i / kSA - 1) & 1, abort_word, status)) break;
+        uint8_t *u = sm + s * Lay::kSlot;
+        mbar_arrive_expect_tx(&full[s], Lay::kSlot);
+        tma_load_3d(u, &p.tk, &full[s], 0, i * 128, bh);
+        tma_load_3d(u + kBlk, &p.tv, &full[s], 0, i * 128, bh);
+        issued_a = i + 1;
+      }
+      for (int j = 0; issued_a == n && j < n; ++j) {
+        const int t = j % kSB;
+        if (j < kSB) {
+          // stage t lies in slot t / 2: it is free once that slot's last unit has been summed
+          const int s = t >> 1;
+          if (s < n) {
+            const int last = s + kSA * ((n - 1 - s) / kSA);
+            if (!mbar_wait(&empty[s], (uint32_t)(last / kSA) & 1, abort_word, status)) break;
+          }
+        } else if (!mbar_wait(&q_empty[t], (uint32_t)(j / kSB - 1) & 1, abort_word, status)) {
+          break;
+        }
+        mbar_arrive_expect_tx(&full_q[t], kBlk);
+        tma_load_3d(sm + t * kBlk, &p.tq, &full_q[t], 0, j * 128, bh);
+        issued_b = j + 1;
+      }
+      // every issued copy must land before shared memory is released
+      for (int i = max(0, issued_a - kSA); i < issued_a; ++i)
+        wait_drain(&full[i % kSA], (uint32_t)(i / kSA) & 1, status);
+      for (int j = max(0, issued_b - kSB); j < issued_b; ++j)
+        wait_drain(&full_q[j % kSB], (uint32_t)(j / kSB) & 1, status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t iS = idesc_bf16_f32(128, 128, 1, 1);
+      constexpr uint32_t iR = idesc_bf16_f32(128, NB, 0, 0);
+      const uint32_t sR = smem_u32(sm), sB = smem_u32(sm + Lay::B);
+      int i = 0;
+      for (; i < n; ++i) {
+        const int s = i % kSA;
+        if (!mbar_wait(&phi_done[s], (uint32_t)(i / kSA) & 1, abort_word, status)) break;
+        tc_fence_after();
+        const uint32_t k = sR + s * Lay::kSlot, v = k + kBlk;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // both operands MN-major: 16 tokens per step, 64-wide blocks 8 KB apart
+          mma_bf16(tmem, sw128_desc(k + ks * 2048, kHalf, 1024), sw128_desc(v + ks * 2048, kHalf, 1024), iS,
+                   (i > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&empty[s]);
+      }
+      if (i == n) mma_commit(s_full);
+      if (i == n && mbar_wait(b_ready, 0, abort_word, status)) {
+        for (int j = 0; j < n; ++j) {
+          const int t = j % kSB, buf = j & 1;
+          if (!mbar_wait(&phi_q[t], (uint32_t)(j / kSB) & 1, abort_word, status)) break;
+          if (j >= 2 && !mbar_wait(&acc_empty[buf], (uint32_t)((j >> 1) - 1) & 1, abort_word, status)) break;
+          tc_fence_after();
+          const uint32_t d = tmem + 128u * buf, q = sR + t * kBlk;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(d, sw128_desc(q + ks * 32, 16, 1024), sw128_desc(sB + ks * 32, 16, 1024), iR,
+                     ks > 0 ? 1u : 0u);
+          mma_commit(&q_empty[t]);
+          mma_commit(&acc_full[buf]);
+        }
+      }
+      mma_commit(drain);
+      wait_drain(drain, 0, status);
+    }
+  } else {
+    // ---------------- phi(K) in place and column sums (warps 2-17) ----------------
+    // Chunk pt + 512 j sits at position pt & 7 of row (pt >> 3) + 64 j and holds the
+    // features 8 g .. 8 g + 7, g = (pt & 7) ^ ((pt >> 3) & 7), the same g for both j.
+    const int pt = threadIdx.x - 64;  // 0..511
+    float za[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) za[a] = 0.f;
+    bool failed = false;
+    for (int i = 0; i < n; ++i) {
+      const int s = i % kSA;
+      if (!mbar_wait(&full[s], (uint32_t)(i / kSA) & 1, abort_word, status)) {
+        failed = true;
+        break;
+      }
+      const long tok0 = (long)i * 128;
+      phi_chunks<2, kFusedA>(sm + s * Lay::kSlot, pt, [&](int, int ch, uint4 x) {
+        // rows past the end add nothing
+        const uint4 y = tok0 + (ch >> 3) >= p.N ? make_uint4(0u, 0u, 0u, 0u) : phi8(x);
+        add8_bf16(za, y);
+        return y;
+      });
+      fence_async_smem();
+      mbar_arrive(&phi_done[s]);
+    }
+    bool ok = !failed && mbar_wait(s_full, 0, abort_word, status) && *abort_word == 0;
+    ok = !bar_or(kBarFusedA, kFusedA, !ok);
+    // ---------------- hand-over: S and z out, B in ----------------
+    if (ok) {
+      float *zred = reinterpret_cast<float *>(sm + Lay::Zred), *P = reinterpret_cast<float *>(sm + Lay::Pst);
+      float *zs = reinterpret_cast<float *>(sm + Lay::Zs);
+#pragma unroll
+      for (int a = 0; a < 8; ++a) zred[pt * 8 + a] = za[a];
+      tc_fence_after();
+      // rows 0-63 hold K_a^T V_a in columns 0-63, rows 64-127 K_b^T V_b in columns 64-127;
+      // the four warps of a lane quarter take 16 columns each
+      const int quarter = warp & 3, part = (warp - 2) >> 2, row = quarter * 32 + lane;
+      uint32_t r[16];
+      tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (row < 64 ? 0u : 64u) + 16u * part, r);
+      float *prow = P + row * kPS + 16 * part;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        *reinterpret_cast<float4 *>(prow + 4 * q4) =
+            make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]), __uint_as_float(r[4 * q4 + 2]),
+                        __uint_as_float(r[4 * q4 + 3]));
+      named_bar(kBarFusedA, kFusedA);
+      if (pt < 64) {
+        const int g = pt >> 3, e = pt & 7;
+        float zsum = 0.f;
+#pragma unroll 8
+        for (int m = 0; m < 64; ++m) zsum += zred[(8 * m + (g ^ (m & 7))) * 8 + e];
+        zs[pt] = zsum;
+        p.z[(long)bh * 64 + pt] = zsum;
+      }
+      named_bar(kBarFusedA, kFusedA);
+      // B, K-major and 128-byte swizzled: row nn < 64 holds column nn of S over the 64 key
+      // features, rows 64 and 65 the hi and lo bf16 parts of z, the rest zeros
+      uint8_t *B = sm + Lay::B;
+      float *Sg = p.S + (long)bh * 64 * 64;
+      for (int e = pt; e < 8 * NB; e += kFusedA) {
+        const int nn = e % NB, c = e / NB;
+        uint32_t w[4];
+        if (nn < 64) {
+          float sv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            sv[j] = P[(8 * c + j) * kPS + nn] + P[(64 + 8 * c + j) * kPS + nn];
+            Sg[(8 * c + j) * 64 + nn] = sv[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) w[j] = pack_bf16(sv[2 * j], sv[2 * j + 1]);
+        } else if (nn < 66) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float a = zs[8 * c + 2 * j], b = zs[8 * c + 2 * j + 1];
+            const float ah = __bfloat162float(__float2bfloat16_rn(a)), bh2 = __bfloat162float(__float2bfloat16_rn(b));
+            w[j] = nn == 64 ? pack_bf16(ah, bh2) : pack_bf16(a - ah, b - bh2);
+          }
+        } else {
+          w[0] = w[1] = w[2] = w[3] = 0u;
+        }
+        *reinterpret_cast<uint4 *>(B + nn * 128 + ((c ^ (nn & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(b_ready);
+    }
+
+    if (warp < 10) {
+      // ---------------- phi(Q) in place ----------------
+      for (int j = 0; ok && j < n; ++j) {
+        const int t = j % kSB;
+        if (!mbar_wait(&full_q[t], (uint32_t)(j / kSB) & 1, abort_word, status)) break;
+        phi_chunks<4, kFusedPhi>(sm + t * kBlk, pt, [](int, int, uint4 x) { return phi8(x); });
+        fence_async_smem();
+        mbar_arrive(&phi_q[t]);
+      }
+    } else {
+      // ---------------- epilogue: normalise, stage, TMA store ----------------
+      const int et = threadIdx.x - 320;  // 0..255
+      const int quarter = warp & 3, half = (warp - 10) >> 2, row = quarter * 32 + lane;
+      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+      for (int j = 0; ok && j < n; ++j) {
+        const int buf = j & 1;
+        const bool w = mbar_wait(&acc_full[buf], (uint32_t)(j >> 1) & 1, abort_word, status);
+        if (bar_or(kBarFusedEpi, kFusedEpi, !w)) break;
+        tc_fence_after();
+        const uint32_t ta = tmem + 128u * buf + lanes;
+        const float den = __uint_as_float(tmem_ld1(ta + 64)) + __uint_as_float(tmem_ld1(ta + 65));
+        const float inv = 1.f / (den + p.eps);
+        uint32_t v[32];
+        tmem_ld32(ta + 32 * half, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        // the staging tile is free once the store issued from it two tiles ago has read it
+        if (et == 0) bulk_wait_read_1();
+        named_bar(kBarFusedEpi, kFusedEpi);
+        uint8_t *stage = sm + Lay::Out + buf * (2 * kBlk);
+        uint8_t *box = stage + half * kBlk;  // box b holds columns [32 b, 32 b + 32)
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float2 a = __fmul2_rn(make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])),
+                                      make_float2(inv, inv));
+          const float2 b = __fmul2_rn(make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])),
+                                      make_float2(inv, inv));
+          *reinterpret_cast<float4 *>(box + sw128_offset_f32(row, 4 * q4)) = make_float4(a.x, a.y, b.x, b.y);
+        }
+        fence_async_smem();
+        named_bar(kBarFusedEpi, kFusedEpi);
+        if (et == 0) {
+          tma_store_3d(&p.to, stage, 0, j * 128, bh);
+          tma_store_3d(&p.to, stage + kBlk, 32, j * 128, bh);
+          bulk_commit();
+        }
+      }
+      if (et == 0) bulk_wait_all();  // output stores complete before the CTA exits
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 // ------------------------------------------------------------------ host
 
 bool make_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t elem, const void *base, long BH, long N, int D,
@@ -688,6 +1010,28 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t elem, const void 
   return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The one-pass form for d = 64: a CTA per head.
+cudaError_t launch_fused(const Problem &p) {
+  FusedParams fp;
+  if (!make_map(&fp.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k, p.BH, p.N, 64, 64, 128) ||
+      !make_map(&fp.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v, p.BH, p.N, 64, 64, 128) ||
+      !make_map(&fp.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q, p.BH, p.N, 64, 64, 128) ||
+      !make_map(&fp.to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.out, p.BH, p.N, 64, 32, 128))
+    return cudaErrorInvalidValue;
+  fp.S = p.S;
+  fp.z = p.z;
+  fp.N = p.N;
+  fp.eps = p.eps;
+  cudaError_t e = ensure_smem_optin((const void *)global_fused_tc, (int)FusedLayout::Bytes);
+  if (e != cudaSuccess) return e;
+  LaunchTimer timer(kKGlobalFused, p.stream);
+  global_fused_tc<<<(unsigned)p.BH, kFusedThreads, FusedLayout::Bytes, p.stream>>>(fp);
+  e = cudaGetLastError();
+  timer.done(e);
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 template <int D, int kMode = kModeElu>
@@ -720,6 +1064,8 @@ cudaError_t launch_t(const Problem &p) {
   // cluster size: a power of two <= 8 so that the build covers the SMs about once, >= 8 units a CTA
   int G = 1;
   while (G < 8 && p.BH * (2 * G) <= sms && bp.units / (2 * G) >= 8) G *= 2;
+  // a CTA per head covers at least 80 % of the SMs: build and read in one pass
+  if (D == 64 && G == 1 && 5 * p.BH >= 4 * sms) return launch_fused(p);
 
   cudaError_t e = build_smem<D>();
   if (e != cudaSuccess) return e;

@@ -75,7 +75,8 @@ size_t noalloc_scratch_capacity_bytes();
 // does not link libcuda); nullptr if the driver does not provide it.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
-// Tensor-core global form (bf16, d_k = d_v in {64, 128}): state build, then read.
+// Tensor-core global form (bf16, d_k = d_v in {64, 128}): state build, then read (for d = 64
+// with enough heads to fill the SMs, both in one kernel, a CTA per head).
 bool global_tc_supported(const Problem &p);
 cudaError_t launch_global_tc(const Problem &p);
 cudaError_t read_and_clear_global_tc_status(unsigned int *value);
@@ -142,7 +143,8 @@ enum KernelId : int {
   kKRetentionDecode = 9,
   kKBackward = 10,
   kKFavor = 11,
-  kKNumKernels = 12
+  kKGlobalFused = 12,
+  kKNumKernels = 13
 };
 
 // While profiling is on (la_profile_enable), brackets one launch with a CUDA

@@ -64,7 +64,7 @@ lib.la_profile_read.restype = _i
 # la_kernel ids of the device-time diagnostics
 KERNELS = {"causal_main": 0, "causal_state": 1, "exact_head": 2, "causal_simt": 3, "global_state": 4,
            "global_read": 5, "decode": 6, "retention_main": 7, "retention_state": 8, "retention_decode": 9,
-           "backward": 10, "favor": 11}
+           "backward": 10, "favor": 11, "global_fused": 12}
 
 
 class LinAttnError(RuntimeError):

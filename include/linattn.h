@@ -391,7 +391,8 @@ typedef enum {
   LA_KERNEL_RETENTION_STATE = 8,  /* its first pass over earlier segments */
   LA_KERNEL_RETENTION_DECODE = 9, /* recurrent retention step */
   LA_KERNEL_BACKWARD = 10,        /* causal backward */
-  LA_KERNEL_FAVOR = 11            /* positive random features */
+  LA_KERNEL_FAVOR = 11,           /* positive random features */
+  LA_KERNEL_GLOBAL_FUSED = 12     /* global form in one pass: a CTA per head (d = 64, heads >= 80 % of SMs) */
 } la_kernel;
 
 /*

@@ -63,7 +63,10 @@ GLOBAL_TC = [(1, 1, 1, 64), (1, 1, 8192, 64), (1, 1, 16384, 64), (2, 3, 129, 64)
              (10, 100, 100, 64), (1, 2, 5000, 128), (2, 2, 383, 128), (1, 1, 1, 128), (3, 60, 130, 128),
              # d = 64 with more heads than half the SMs and fewer than all (one build CTA a head),
              # ragged tails
-             (1, 100, 1000, 64), (3, 40, 257, 64), (1, 151, 128, 64), (2, 50, 4161, 64), (1, 77, 64, 64)]
+             (1, 100, 1000, 64), (3, 40, 257, 64), (1, 151, 128, 64), (2, 50, 4161, 64), (1, 77, 64, 64),
+             # d = 64 with a CTA per head covering at least 80 % of the SMs (the one-pass kernel):
+             # more tiles than the read's stages and the build's slots, ragged tails, one token
+             (2, 64, 1000, 64), (1, 130, 1537, 64), (1, 122, 3000, 64), (3, 50, 700, 64), (1, 128, 1, 64)]
 
 
 @pytest.mark.parametrize("shape", GLOBAL_TC, ids=lambda s: "x".join(map(str, s)))

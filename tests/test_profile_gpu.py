@@ -37,3 +37,21 @@ def test_profile_counts_and_times_each_kernel(cuda_lib):
     assert L.profile_read("decode")[1] == 1
     assert L.profile_read("causal_main") == (0.0, 0)
     L.profile_enable(False)
+
+
+def test_global_form_takes_one_pass_when_the_heads_fill_the_sms(cuda_lib):
+    """d = 64 with a head per SM: one kernel builds and reads each head; with few heads the
+    state build and the read are two launches."""
+    L = cuda_lib
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    g = torch.Generator(device="cpu").manual_seed(6)
+    for heads, expect in ((sms, {"global_fused": 1}), (4, {"global_state": 1, "global_read": 1})):
+        q, k, v = (torch.randn(1, heads, 300, 64, generator=g).div(8.0).bfloat16().to(DEV) for _ in range(3))
+        L.la_global(q, k, v)  # warm-up (one-time attribute set-up)
+        torch.cuda.synchronize()
+        L.profile_enable(True)
+        L.la_global(q, k, v)
+        L.profile_enable(False)
+        torch.cuda.synchronize()
+        got = {name: L.profile_read(name)[1] for name in L.KERNELS}
+        assert {name: n for name, n in got.items() if n} == expect

@@ -18,7 +18,8 @@ DEV = "cuda"
 
 
 @pytest.mark.parametrize("form,shape", [("causal", (2, 2, 3000, 128)), ("causal", (1, 3, 9000, 128)),
-                                        ("global", (4, 8, 1500, 64)), ("global", (1, 2, 5000, 128))])
+                                        ("global", (4, 8, 1500, 64)), ("global", (1, 2, 5000, 128)),
+                                        ("global", (4, 40, 700, 64))])
 def test_outputs_complete_for_the_next_work_on_the_stream(cuda_lib, form, shape):
     B, H, N, d = shape
     base = inputs.WORKLOADS["causal_bf16" if form == "causal" else "global_bf16"]
