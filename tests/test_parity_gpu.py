@@ -82,6 +82,36 @@ def test_global_tensor_core_shapes_every_element(cuda_lib, shape):
     assert cuda_lib.device_status() == 0
 
 
+# Heads the planner cuts into two segments (51 to 76 heads on 152 SMs, at least 8 chunks):
+# the second segment starts from the first pass's pieces.  Ragged tails, a one-token last
+# chunk, and a carried state.
+TWO_SEGMENT = [(1, 64, 1000, False), (2, 30, 3000, False), (1, 76, 2049, False), (1, 64, 1300, True)]
+
+
+@pytest.mark.parametrize("shape", TWO_SEGMENT, ids=lambda s: "x".join(map(str, s)))
+def test_two_segment_heads_every_element_of_sampled_heads(cuda_lib, shape):
+    B, H, N, from_state = shape
+    w = W["causal_bf16"]
+    q, k, v = inputs.make_qkv(w, N=N, B=B, H=H)
+    g = torch.Generator().manual_seed(11)
+    S0 = torch.randn(B, H, 128, 128, generator=g) if from_state else None
+    z0 = torch.rand(B, H, 128, generator=g) * 50 + 1 if from_state else None
+    if from_state:
+        S, z = S0.to(DEV), z0.to(DEV)
+        out, _, _ = cuda_lib.la_causal_with_state(q.to(DEV), k.to(DEV), v.to(DEV), S, z, eps=w.eps)
+    else:
+        out, S, z = cuda_lib.la_causal(q.to(DEV), k.to(DEV), v.to(DEV), eps=w.eps)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    heads = [0, 1, B * H - 2, B * H - 1]
+    sel = lambda t: t.reshape(B * H, *t.shape[2:])[heads]
+    ro, rS, rz = oracle.causal(f64(sel(q)), f64(sel(k)), f64(sel(v)), eps=w.eps, nthreads=4,
+                               S0=f64(sel(S0)) if from_state else None, z0=f64(sel(z0)) if from_state else None)
+    assert_close(sel(out), ro, 2e-2, "out")
+    assert_close(sel(S), rS, 2e-2, "S")
+    assert_close(sel(z), rz, 2e-2, "z")
+
+
 def test_workload_causal_f32_small_every_element(cuda_lib):
     w = W["causal_f32_small"]
     q, k, v = inputs.make_qkv(w)
