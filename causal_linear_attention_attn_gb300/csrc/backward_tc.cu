@@ -1015,19 +1015,10 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
             mma_bf16_ts(tO, tKh + 8 * ks, kdesc(sUlo, ks), iKK, 1);
           }
         }
-        if (!wait(x_split, ph) || !wait(kDk ? q_ready : n_ready, ph)) break;
+        if (!wait(kDk ? q_ready : n_ready, ph)) break;
         tc_fence_after();
-        // O += X B with X from tensor memory as pairs (queries [16 ks, 16 ks + 16): 8 columns hi,
-        // 8 lo) and B = gnum (role 0) or phi(Q) (role 1), rows = queries
-        const uint32_t sBhi = kDk ? sQhi : sNhi, sBlo = kDk ? sQlo : sNlo;
-#pragma unroll 4
-        for (int ks = 0; ks < 8; ++ks) {
-          mma_bf16_ts(tO, tX + 16 * ks, mndesc(sBhi, ks), iKM, 1);
-          mma_bf16_ts(tO, tX + 16 * ks + 8, mndesc(sBhi, ks), iKM, 1);
-          mma_bf16_ts(tO, tX + 16 * ks, mndesc(sBlo, ks), iKM, 1);
-        }
-        mma_commit(o_full);  // the epilogue reads O while U is updated
-        // U += Q^T gnum
+        // U += Q^T gnum, before O += X B: its commit frees the key operand, U and (role 0) the
+        // query pairs or (role 1) the gnum pairs for the next chunk while O += X B still runs
 #pragma unroll 4
         for (int ks = 0; ks < 8; ++ks) {
           mma_bf16(tU, mndesc(sQhi, ks), mndesc(sNhi, ks), iMM, 1);
@@ -1035,6 +1026,18 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           mma_bf16(tU, mndesc(sQlo, ks), mndesc(sNhi, ks), iMM, 1);
         }
         mma_commit(u_done);
+        if (!wait(x_split, ph)) break;
+        tc_fence_after();
+        // O += X B with X from tensor memory as pairs (queries [16 ks, 16 ks + 16): 8 columns hi,
+        // 8 lo) and B = gnum (role 0) or phi(Q) (role 1), rows = queries; its commit also frees B
+        const uint32_t sBhi = kDk ? sQhi : sNhi, sBlo = kDk ? sQlo : sNlo;
+#pragma unroll 4
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16_ts(tO, tX + 16 * ks, mndesc(sBhi, ks), iKM, 1);
+          mma_bf16_ts(tO, tX + 16 * ks + 8, mndesc(sBhi, ks), iKM, 1);
+          mma_bf16_ts(tO, tX + 16 * ks, mndesc(sBlo, ks), iKM, 1);
+        }
+        mma_commit(o_full);
       }
       mma_commit(drain);
       wait_drain(drain, 0, status);
@@ -1122,8 +1125,10 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       };
       // half of the phi(Q) pairs from the staged raw queries (the N warps take the other half)
       auto query_half = [&]() -> bool {
-        // role 1: the epilogue reads the previous chunk's query pairs for u after its split
-        ok = wait(q_full, it & 1) && (!kDk || it == 0 || wait(ucol_done, (it - 1) & 1));
+        // role 1: the epilogue reads the previous chunk's query pairs for u after its split, and
+        // they are the B operand of that chunk's O += X Q
+        ok = wait(q_full, it & 1) &&
+             (!kDk || it == 0 || (wait(ucol_done, (it - 1) & 1) && wait(o_full, (it - 1) & 1)));
         if (bar_or(kBarQK, 128, !ok)) return false;
         query_pairs_staged(sm, threadIdx.x - 32, T);
         fence_async_smem();
@@ -1217,7 +1222,8 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       // phi(Q) pairs from the staged raw queries (same swizzled layout), then the next chunk's
       // raw queries into the staging tile once both halves are done with it
       auto query_half = [&]() -> bool {
-        bool okq = wait(q_full, it & 1);
+        // role 1: the previous chunk's query pairs are the B operand of its O += X Q
+        bool okq = wait(q_full, it & 1) && (!kDk || it == 0 || wait(o_full, (it - 1) & 1));
         if (bar_or(kBarG, 128, !okq)) return false;
         query_pairs_staged(sm, 128 + gt, T);
         fence_async_smem();
@@ -1238,11 +1244,14 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         gnum_rest();
         if (!query_half()) break;
       } else {
-        // role 0: X = K Q^T comes first; gnum is first needed by O += X gnum
+        // role 0: X = K Q^T comes first; gnum is first needed by the U update, and the previous
+        // chunk's gnum pairs are the B operand of its O += X gnum
         const bool ok = it == 0 || wait(u_done, (it - 1) & 1);
         if (bar_or(kBarG, 128, !ok)) break;
         if (!query_half()) break;
         load_round(0);
+        const bool okn = it == 0 || wait(o_full, (it - 1) & 1);
+        if (bar_or(kBarG, 128, !okn)) break;
         gnum_rest();
       }
     }
