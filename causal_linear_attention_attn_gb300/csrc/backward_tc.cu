@@ -978,7 +978,6 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         // X needs only the key operand and one other: the query pairs (role 0, X = K Q^T) or the
         // gnum pairs (role 1, X = V gnum^T); the remaining one is waited for before O += X B
         if (!wait(k_ready, ph) || !wait(kDk ? n_ready : q_ready, ph)) break;
-        if (it > 0 && !wait(o_done, (it - 1) & 1)) break;
         tc_fence_after();
         if (!kDk) {
           // X = K Q^T (rows keys j, columns queries t)
@@ -997,7 +996,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
           }
         }
         mma_commit(x_full);  // the epilogue splits X while O = K U (or V U^T) runs
-        if (!wait(u_ready, ph)) break;
+        if (!wait(u_ready, ph) || (it > 0 && !wait(o_done, (it - 1) & 1))) break;
         tc_fence_after();
         if (!kDk) {
           // O = K U (U rows = features i: the K index)
