@@ -870,7 +870,7 @@ struct P2Layout {
   static constexpr uint32_t Gd = 7 * kTile;  // [128] gden of the chunk
   static constexpr uint32_t Ub = Gd + 512;   // [128] u carried into the chunk (role 1)
   static constexpr uint32_t Bars = Ub + 512;
-  static constexpr int kNumBars = 13;
+  static constexpr int kNumBars = 14;
   static constexpr uint32_t Misc = Bars + kNumBars * 8;
   static constexpr uint32_t Bytes = Misc + 16;
 };
@@ -878,7 +878,8 @@ static_assert(P2Layout::Bytes <= 232448, "pass 2 shared memory");
 
 // TMEM columns of pass 2: U accumulator; X = the key-side scores (role 0:
 // K Q^T, role 1: V gnum^T), then as bf16 pairs; O = dv or dk; the key operand
-// (role 0: phi(K) as pairs, 128 columns; role 1: V, 64 columns).
+// (role 0: phi(K) as pairs, 128 columns; role 1: V, 64 columns, then the raw
+// keys for phi'(k), 64 columns).
 constexpr uint32_t kP2U = 0, kP2X = 128, kP2O = 256, kP2K = 384;
 
 // Warp roles of pass 2 (13 warps): 0 MMA issuer; 1-4 key operand (rows into
@@ -919,7 +920,8 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
            *x_split = bars + 5, *o_full = bars + 6, *o_done = bars + 7, *drain = bars + 8, *q_full = bars + 9,
            *q_used = bars + 10,
            *u_done = bars + 11,  // the chunk's U update complete: its operand tiles and U are free
-           *ucol_done = bars + 12;  // role 1: the epilogue's read of the Q tiles and gd for u is done
+           *ucol_done = bars + 12,  // role 1: the epilogue's read of the Q tiles and gd for u is done
+           *kp_ready = bars + 13;   // role 1: the chunk's raw keys are in tensor memory
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::Misc);
   volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(sm + L::Misc + 4);
   unsigned int *status = &g_bwd_status;
@@ -941,6 +943,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
     mbar_init(o_full, 1);
     mbar_init(u_done, 1);
     mbar_init(ucol_done, 128);
+    mbar_init(kp_ready, 128);
     mbar_init(o_done, 128);
     mbar_init(drain, 1);
     mbar_init(q_full, 1);
@@ -1140,7 +1143,27 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
       copy_u();
       fence_async_smem();
       mbar_arrive(u_ready);
-      if (kDk && !query_half()) break;
+      if (kDk) {
+        if (!query_half()) break;
+        // role 1: the chunk's raw key rows for phi'(k), into the key-operand columns V leaves
+        // free, once the epilogue has read the previous chunk's
+        uint4 kx[16];
+        if (r < T) {
+          load_row_half(kh + (t0 + r) * kD, *reinterpret_cast<uint4 (*)[8]>(&kx[0]), 0);
+          load_row_half(kh + (t0 + r) * kD, *reinterpret_cast<uint4 (*)[8]>(&kx[8]), 1);
+        }
+        ok = it == 0 || wait(o_done, (it - 1) & 1);
+        if (bar_or(kBarQK, 128, !ok)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint4 xe = r < T ? kx[e] : make_uint4(0u, 0u, 0u, 0u);
+          tmem_st4_nowait(tl + kP2K + 64 + 4 * e, xe.x, xe.y, xe.z, xe.w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(kp_ready);
+      }
     }
     // role 0: the initial state's gradient dS0 = U after the first chunk
     if (!kDk && p.dS0) {
@@ -1302,8 +1325,7 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         }
         mbar_arrive(ucol_done);
       }
-      const uint8_t *kr = reinterpret_cast<const uint8_t *>(kh + (t0 + j) * kD);
-      ok = wait(o_full, it & 1);
+      ok = wait(o_full, it & 1) && (!kDk || wait(kp_ready, it & 1));
       if (bar_or(kBarE, 128, !ok)) break;
       tc_fence_after();
       float *dst = (kDk ? p.dk : p.dv) + ((long)bh * N + t0 + j) * kD;
@@ -1312,15 +1334,16 @@ __device__ __forceinline__ void pass2_role(const BwdTcParams &p) {
         uint32_t ro[32];
         tmem_ld32(tl + kP2O + b * 32, ro);
         if (kDk) {
-          // dk = (V U^T + B Q + u) phi'(k), phi'(x) = 1 above zero, e^x below
+          // dk = (V U^T + B Q + u) phi'(k), phi'(x) = 1 above zero, e^x below; the keys of
+          // features [32 b, 32 b + 32) from tensor memory (zeros past the end)
+          uint32_t kw[16];
+          tmem_ld16(tl + kP2K + 64 + 16 * b, kw);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            uint32_t w8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-            if (j < T) ld_row32(kr + 64 * b + 32 * e, w8);
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
               const int col = 32 * b + 16 * e + 2 * m;
-              const float2 f = phi2(lo16(w8[m]), hi16(w8[m]));
+              const float2 f = phi2(lo16(kw[8 * e + m]), hi16(kw[8 * e + m]));
               const float da = fminf(f.x, 1.f), db = fminf(f.y, 1.f);
               ro[16 * e + 2 * m] = __float_as_uint((__uint_as_float(ro[16 * e + 2 * m]) + ub[col]) * da);
               ro[16 * e + 2 * m + 1] = __float_as_uint((__uint_as_float(ro[16 * e + 2 * m + 1]) + ub[col + 1]) * db);
