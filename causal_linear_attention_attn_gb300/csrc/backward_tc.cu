@@ -395,9 +395,14 @@ struct P1Layout {
 };
 static_assert(P1Layout::Bytes <= 232448, "pass 1 shared memory");
 
-// TMEM columns of pass 1: S accumulator; X = A, then Y and Y + B' K; CB = C,
-// then B' as bf16 pairs; phi(Q) as bf16 pairs (hi 64 columns, lo 64).
+// TMEM columns of pass 1: S accumulator; two score regions that trade roles by
+// chunk parity, so that the next chunk's A = Q K^T can go in while the dq phase
+// still reads this chunk's Y + B' K: region RA(c) holds A, then Y and Y + B' K,
+// region RC(c) holds C, then B' as bf16 pairs, and RA(c + 1) = RC(c); phi(Q)
+// as bf16 pairs (hi 64 columns, lo 64).
 constexpr uint32_t kP1S = 0, kP1X = 128, kP1CB = 256, kP1Q = 384;
+__device__ __forceinline__ uint32_t p1_ra(int c) { return (c & 1) ? kP1CB : kP1X; }
+__device__ __forceinline__ uint32_t p1_rc(int c) { return (c & 1) ? kP1X : kP1CB; }
 
 // Warp roles of pass 1 (13 warps): 0 MMA issuer and tensor-memory owner; 1-4
 // keys (TMA; half of the phi pairs in place), queries 0-63 (phi pairs into
@@ -495,10 +500,10 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       const uint32_t sKhi = smem_u32(sm + L::Khi), sKlo = smem_u32(sm + L::Klo), sV = smem_u32(sm + L::V),
                      sGhi = smem_u32(sm + L::Ghi), sGlo = smem_u32(sm + L::Glo), sShi = smem_u32(sm + L::Shi),
                      sSlo = smem_u32(sm + L::Slo);
-      const uint32_t tS = tmem + kP1S, tX = tmem + kP1X, tCB = tmem + kP1CB, tQh = tmem + kP1Q,
-                     tQl = tmem + kP1Q + 64;
+      const uint32_t tS = tmem + kP1S, tQh = tmem + kP1Q, tQl = tmem + kP1Q + 64;
       for (int c = 0; c < nloc; ++c) {
         const uint32_t ph = c & 1;
+        const uint32_t tX = tmem + p1_ra(c), tCB = tmem + p1_rc(c);
         if (c + 1 < nloc) {  // the next chunk's rows into L2
           const long t1 = (long)(c0 + c + 1) * kC;
           const uint32_t rows = (uint32_t)min((long)kC, N - t1);
@@ -517,7 +522,8 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
           mma_bf16_ts(tX, tQh + 8 * ks, kdesc(sKlo, ks), iKK, 1);
           mma_bf16_ts(tX, tQl + 8 * ks, kdesc(sKhi, ks), iKK, 1);
         }
-        if (!wait(g_ready, ph) || !wait(v_full, ph)) break;
+        // C goes into the region the previous chunk's dq phase reads
+        if (!wait(g_ready, ph) || !wait(v_full, ph) || (c > 0 && !wait(e3_done, (c - 1) & 1))) break;
         tc_fence_after();
         // C = dO V^T
 #pragma unroll 4
@@ -625,12 +631,25 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       mbar_arrive(&z_full[0]);
     }
     bool ok = true;
+    // queries 0-63 of chunk c (row r already loaded into x) as phi pairs into tensor memory, once
+    // the previous chunk's B' phase has read the phi(Q) columns and chunk c's z is complete
+    auto query_pairs = [&](int c, const uint4 (&x)[8], int T) -> bool {
+      ok = wait(&z_full[c & 1], (c >> 1) & 1) && (c == 0 || wait(cb_ready, (c - 1) & 1));
+      if (bar_or(kBarQK, 128, !ok)) return false;
+      tc_fence_after();
+      den_x[r] = query_pairs_half(x, r < T, zbuf + (c & 1) * kD, tl, 0);
+      mbar_arrive(&z_empty[c & 1]);
+      tc_fence_before();
+      mbar_arrive(q_ready);
+      return true;
+    };
     for (int c = 0; c < nloc; ++c) {
       const long t0 = (long)(c0 + c) * kC;
       const int T = (int)min((long)kC, N - t0);
-      // this row's queries 0-63, loaded while the keys are transformed
+      // chunk 0's queries 0-63, loaded while the keys are transformed (later chunks' are formed
+      // in the chunk before)
       uint4 x[8];
-      if (r < T) load_row_half(qh + (t0 + r) * kD, x);
+      if (c == 0 && r < T) load_row_half(qh + (t0 + r) * kD, x);
       // keys: the raw tile has landed; phi pairs in place (hi) and into Klo (lo), this half of
       // the chunks (the G warps take the other)
       ok = wait(k_full, c & 1);
@@ -638,16 +657,12 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       key_pairs(kt, lt, tid, T);
       fence_async_smem();
       mbar_arrive(k_ready);
-      // queries: phi pairs into tensor memory once the previous chunk's last reads are done
-      ok = c == 0 || wait(e3_done, (c - 1) & 1);
-      ok = ok && wait(&z_full[c & 1], (c >> 1) & 1);
-      if (bar_or(kBarQK, 128, !ok)) break;
-      tc_fence_after();
-      den_x[r] = query_pairs_half(x, r < T, zbuf + (c & 1) * kD, tl, 0);
-      mbar_arrive(&z_empty[c & 1]);
-      tc_fence_before();
-      mbar_arrive(q_ready);
+      if (c == 0 && !query_pairs(0, x, T)) break;
       if (c + 1 == nloc) break;
+      // the next chunk's queries, loaded while the state copy is made
+      const long t1 = t0 + kC;
+      const int T1 = (int)min((long)kC, N - t1);
+      if (r < T1) load_row_half(qh + (t1 + r) * kD, x);
       // pair copy of the state the next chunk reads, once this chunk's Y has read the current
       // copy and its S update has completed
       ok = wait(y_full, c & 1);
@@ -668,6 +683,8 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(s_ready);
+      // the next chunk's query pairs as soon as this chunk's B' phase is done
+      if (!query_pairs(c + 1, x, T1)) break;
       // the next chunk's raw keys once this chunk's products are done with the K tiles
       ok = wait(d_full, c & 1);
       if (bar_or(kBarQK, 128, !ok)) break;
@@ -681,11 +698,11 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
     uint8_t *Ghi = sm + L::Ghi, *Glo = sm + L::Glo;
     int v_issued = 0;
     if (gt == 0) prefetch_tmap(&p.tv);
-    for (int c = 0; c < nloc; ++c) {
+    // dO pairs of chunk c and its V (by TMA), once the previous chunk's products are done with
+    // those tiles (the caller waits)
+    auto dO_pairs = [&](int c) {
       const long t0 = (long)(c0 + c) * kC;
       const int T = (int)min((long)kC, N - t0);
-      const bool ok = c == 0 || wait(y_full, (c - 1) & 1);
-      if (bar_or(kBarG, 128, !ok)) break;
       if (gt == 0) {
         mbar_arrive_expect_tx(v_full, kTile);
         tma_load_3d(sm + L::V, &p.tv, v_full, 0, (int)t0, bh);
@@ -717,26 +734,34 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       }
       fence_async_smem();
       mbar_arrive(g_ready);
+    };
+    // queries 64-127 of chunk c (row r already loaded into x) as phi pairs into this warp's
+    // tensor-memory lanes, as the QK warps do 0-63
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    auto query_pairs = [&](int c, const uint4 (&x)[8], int T) -> bool {
+      const bool okq = wait(&z_full[c & 1], (c >> 1) & 1) && (c == 0 || wait(cb_ready, (c - 1) & 1));
+      if (bar_or(kBarG, 128, !okq)) return false;
+      tc_fence_after();
+      den_x[kD + r] = query_pairs_half(x, r < T, zbuf + (c & 1) * kD, tl, 1);
+      mbar_arrive(&z_empty[c & 1]);
+      tc_fence_before();
+      mbar_arrive(q_ready);
+      return true;
+    };
+    if (nloc > 0) dO_pairs(0);
+    for (int c = 0; c < nloc; ++c) {
+      const long t0 = (long)(c0 + c) * kC;
+      const int T = (int)min((long)kC, N - t0);
+      uint4 x[8];
+      if (c == 0 && r < T) load_row_half(qh + (t0 + r) * kD, x, 1);
       // the other half of this chunk's key pairs, then its key column sums (for the E warps' z)
       bool okk = wait(k_full, c & 1);
       if (bar_or(kBarG, 128, !okk)) break;
       key_pairs(reinterpret_cast<uint4 *>(sm + L::Khi), reinterpret_cast<uint4 *>(sm + L::Klo), 128 + gt, T);
       fence_async_smem();
       mbar_arrive(k_ready);
-      // queries 64-127 of row r (this warp's tensor-memory lanes) once the previous chunk's last
-      // reads of the phi(Q) columns are done
-      const int r = (warp & 3) * 32 + lane;
-      const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      uint4 x[8];
-      if (r < T) load_row_half(qh + (t0 + r) * kD, x, 1);
-      okk = c == 0 || wait(e3_done, (c - 1) & 1);
-      okk = okk && wait(&z_full[c & 1], (c >> 1) & 1);
-      if (bar_or(kBarG, 128, !okk)) break;
-      tc_fence_after();
-      den_x[kD + r] = query_pairs_half(x, r < T, zbuf + (c & 1) * kD, tl, 1);
-      mbar_arrive(&z_empty[c & 1]);
-      tc_fence_before();
-      mbar_arrive(q_ready);
+      if (c == 0 && !query_pairs(0, x, T)) break;
       // this chunk's key column sums, for the E warps' z (both halves of the pairs are written)
       okk = wait(k_ready, c & 1);
       if (bar_or(kBarG, 128, !okk)) break;
@@ -747,16 +772,27 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
         kcol[pc + 1] = cs.y;
       }
       mbar_arrive(kc_ready);
+      if (c + 1 == nloc) break;
+      // the next chunk: its queries (loaded first), its dO pairs and V once this chunk's Y has
+      // read the tiles, then its query pairs once this chunk's B' phase is done
+      const long t1 = t0 + kC;
+      const int T1 = (int)min((long)kC, N - t1);
+      if (r < T1) load_row_half(qh + (t1 + r) * kD, x, 1);
+      okk = wait(y_full, c & 1);
+      if (bar_or(kBarG, 128, !okk)) break;
+      dO_pairs(c + 1);
+      if (!query_pairs(c + 1, x, T1)) break;
     }
     if (gt == 0 && v_issued > 0) wait_drain(v_full, (v_issued - 1) & 1, status);
   } else {
-    // ---------------- E warps: scores, den, gden, B', key column sums, dq ----------------
+    // ---------------- E warps: scores, den, gden, B', the next chunk's z, dq ----------------
     const int t = (warp & 3) * 32 + lane;  // tensor-memory lane = chunk row; also feature t of z
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     for (int c = 0; c < nloc; ++c) {
       const long t0 = (long)(c0 + c) * kC;
       const int T = (int)min((long)kC, N - t0);
       const int jmax = min(t, T - 1);  // keys kept: j <= t and j < T
+      const uint32_t rA = tl + p1_ra(c), rC = tl + p1_rc(c);
       uint32_t ra[32], rc[32];
       // E1: row sums of A and of A * C
       bool ok = wait(q_ready, c & 1) && wait(k_ready, c & 1) && wait(ac_full, c & 1);
@@ -765,7 +801,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       float rs = 0.f, ac = 0.f;
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
-        tmem_ld32x2(tl + kP1X + cb * 32, tl + kP1CB + cb * 32, ra, rc);
+        tmem_ld32x2(rA + cb * 32, rC + cb * 32, ra, rc);
 #pragma unroll
         for (int m = 0; m < 32; ++m) {
           const float a = cb * 32 + m <= jmax ? __uint_as_float(ra[m]) : 0.f;
@@ -776,7 +812,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       const float den = ((den_x[t] + den_x[kD + t]) + rs) + p.eps;
       tc_fence_before();
       mbar_arrive(x_free);
-      // E2: gden from phi(q) . Y, then B' = C + den gden in place as bf16 pairs
+      // E2: gden from phi(q) . Y, the next chunk's z, then B' = C + den gden in place as bf16 pairs
       ok = wait(y_full, c & 1);
       if (bar_or(kBarE, 128, !ok)) break;
       tc_fence_after();
@@ -784,7 +820,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
         uint32_t qhw[16], qlw[16];
-        tmem_ld32_16x2(tl + kP1X + b * 32, tl + kP1Q + 16 * b, tl + kP1Q + 64 + 16 * b, ra, qhw, qlw);
+        tmem_ld32_16x2(rA + b * 32, tl + kP1Q + 16 * b, tl + kP1Q + 64 + 16 * b, ra, qhw, qlw);
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
           qy = fmaf(lo16(qhw[m]) + lo16(qlw[m]), __uint_as_float(ra[2 * m]), qy);
@@ -797,31 +833,57 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       // cannot complete the next chunk's before this wait)
       ok = wait(kc_ready, c & 1);
       if (bar_or(kBarE, 128, !ok)) break;
-      const float kc = kcol[t];
+      const float *z = zbuf + (c & 1) * kD;
+      // z for the next chunk: z_prev plus this chunk's key column sums (thread t owns feature t),
+      // before the next chunk's query pairs need it; the previous reads of that buffer (the
+      // query pairs and this group's dq of the chunk before) are done
+      if (c + 1 < nloc) {
+        const int nb = (c + 1) & 1;
+        ok = c + 1 < 2 || wait(&z_empty[nb], (((c + 1) >> 1) - 1) & 1);
+        if (bar_or(kBarE, 128, !ok)) break;
+        zbuf[nb * kD + t] = z[t] + kcol[t];
+        mbar_arrive(&z_full[nb]);
+      }
 #pragma unroll 1
       for (int cb = 0; cb < 4; cb += 2) {
-        tmem_ld32x2(tl + kP1CB + cb * 32, tl + kP1CB + cb * 32 + 32, ra, rc);
+        tmem_ld32x2(rC + cb * 32, rC + cb * 32 + 32, ra, rc);
         split_scores32(ra, cb, [&](int j) { return j <= jmax; }, [&](int, float x) { return x + dg; });
         split_scores32(rc, cb + 1, [&](int j) { return j <= jmax; }, [&](int, float x) { return x + dg; });
-        tmem_st32(tl + kP1CB + cb * 32, ra);
-        tmem_st32(tl + kP1CB + cb * 32 + 32, rc);
+        tmem_st32(rC + cb * 32, ra);
+        tmem_st32(rC + cb * 32 + 32, rc);
       }
       tc_fence_before();
       mbar_arrive(cb_ready);
-      // E3: dq = ((Y + B' K) / den + gden z_prev) phi'(q)
+      // E3: dq = ((Y + B' K) / den + gden z_prev) phi'(q), phi'(q) = min(phi(q), 1) from the
+      // query row itself (the next chunk's pairs may already fill the phi(Q) columns)
+      const uint8_t *qrow = reinterpret_cast<const uint8_t *>(qh + (t0 + t) * kD);
+      uint32_t na[8], nb8[8];  // the next 32 features' query words
+      auto load_q = [&](int b) {
+        if (t < T) {
+          ld_row32(qrow + 64 * b, na);
+          ld_row32(qrow + 64 * b + 32, nb8);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) na[e] = nb8[e] = 0u;
+        }
+      };
+      load_q(0);
       ok = wait(d_full, c & 1);
       if (bar_or(kBarE, 128, !ok)) break;
       tc_fence_after();
       const float inv = 1.f / den;
-      const float *z = zbuf + (c & 1) * kD;
       float *dst = p.dq + ((long)bh * N + t0 + t) * kD;
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
-        uint32_t qhw[16], qlw[16];
-        tmem_ld32_16x2(tl + kP1X + b * 32, tl + kP1Q + 16 * b, tl + kP1Q + 64 + 16 * b, ra, qhw, qlw);
+        uint32_t qw[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qw[e] = na[e], qw[8 + e] = nb8[e];
+        if (b < 3) load_q(b + 1);
+        tmem_ld32(rA + b * 32, ra);
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
-          const float f0 = fminf(lo16(qhw[m]) + lo16(qlw[m]), 1.f), f1 = fminf(hi16(qhw[m]) + hi16(qlw[m]), 1.f);
+          const float2 f = phi2(lo16(qw[m]), hi16(qw[m]));
+          const float f0 = fminf(f.x, 1.f), f1 = fminf(f.y, 1.f);
           ra[2 * m] = __float_as_uint(fmaf(__uint_as_float(ra[2 * m]), inv, z[32 * b + 2 * m] * gden) * f0);
           ra[2 * m + 1] =
               __float_as_uint(fmaf(__uint_as_float(ra[2 * m + 1]), inv, z[32 * b + 2 * m + 1] * gden) * f1);
@@ -834,16 +896,6 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       if (t < T) {
         p.den[(long)bh * N + t0 + t] = den;
         p.gden[(long)bh * N + t0 + t] = gden;
-      }
-
-      // z for the next chunk: z_prev plus this chunk's key column sums (thread t owns feature t)
-      named_bar(kBarE, 128);  // every read of this chunk's z is done
-      if (c + 1 < nloc) {
-        const int nb = (c + 1) & 1;
-        ok = c + 1 < 2 || wait(&z_empty[nb], (((c + 1) >> 1) - 1) & 1);
-        if (bar_or(kBarE, 128, !ok)) break;
-        zbuf[nb * kD + t] = z[t] + kc;
-        mbar_arrive(&z_full[nb]);
       }
       tc_fence_before();
       mbar_arrive(e3_done);
