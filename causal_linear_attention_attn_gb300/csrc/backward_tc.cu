@@ -501,6 +501,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
                      sGhi = smem_u32(sm + L::Ghi), sGlo = smem_u32(sm + L::Glo), sShi = smem_u32(sm + L::Shi),
                      sSlo = smem_u32(sm + L::Slo);
       const uint32_t tS = tmem + kP1S, tQh = tmem + kP1Q, tQl = tmem + kP1Q + 64;
+      int k_issued = 1;  // key loads issued (chunk 0's by the QK warps)
       for (int c = 0; c < nloc; ++c) {
         const uint32_t ph = c & 1;
         const uint32_t tX = tmem + p1_ra(c), tCB = tmem + p1_rc(c);
@@ -561,9 +562,19 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
           mma_bf16_ts(tX, tCB + 16 * ks, mndesc(sKlo, ks), iKM, 1);
         }
         mma_commit(d_full);
+        // the next chunk's raw keys as soon as this chunk's products are done with the K tiles
+        if (c + 1 < nloc) {
+          if (!wait(d_full, ph)) break;
+          mbar_arrive_expect_tx(k_full, kTile);
+          tma_load_3d(sm + L::Khi, &p.tk, k_full, 0, (c0 + c + 1) * kC, bh);
+          tma_load_3d(sm + L::Khi + kBlk, &p.tk, k_full, 64, (c0 + c + 1) * kC, bh);
+          k_issued = c + 2;
+        }
       }
       mma_commit(drain);
       wait_drain(drain, 0, status);
+      // every key load issued must land before shared memory is released (chunk 0's by the QK warps)
+      if (nloc > 0) wait_drain(k_full, (uint32_t)(k_issued - 1) & 1, status);
     }
   } else if (warp < kP1WarpG) {
     // ---------------- QK warps: keys, queries, copies of the state ----------------
@@ -572,16 +583,11 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint8_t *Shi = sm + L::Shi, *Slo = sm + L::Slo;
     uint4 *kt = reinterpret_cast<uint4 *>(sm + L::Khi), *lt = reinterpret_cast<uint4 *>(sm + L::Klo);
-    int k_issued = 0;
-    auto load_k = [&](int c) {  // raw keys of chunk c into the Khi tile (rows past the end read as zero)
-      mbar_arrive_expect_tx(k_full, kTile);
-      tma_load_3d(sm + L::Khi, &p.tk, k_full, 0, c * kC, bh);
-      tma_load_3d(sm + L::Khi + kBlk, &p.tk, k_full, 64, c * kC, bh);
-      k_issued = c + 1;
-    };
-    if (tid == 0) {
+    if (tid == 0) {  // chunk 0's raw keys into the Khi tile (the MMA thread loads the later ones)
       prefetch_tmap(&p.tk);
-      load_k(c0);
+      mbar_arrive_expect_tx(k_full, kTile);
+      tma_load_3d(sm + L::Khi, &p.tk, k_full, 0, c0 * kC, bh);
+      tma_load_3d(sm + L::Khi + kBlk, &p.tk, k_full, 64, c0 * kC, bh);
     }
     {
       // initial state: S0 plus the sums of the earlier segments (the state pass's pieces), into
@@ -685,12 +691,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) bwd_pass1_tc(const __grid_const
       mbar_arrive(s_ready);
       // the next chunk's query pairs as soon as this chunk's B' phase is done
       if (!query_pairs(c + 1, x, T1)) break;
-      // the next chunk's raw keys once this chunk's products are done with the K tiles
-      ok = wait(d_full, c & 1);
-      if (bar_or(kBarQK, 128, !ok)) break;
-      if (tid == 0) load_k(c0 + c + 1);
     }
-    if (tid == 0 && k_issued > 0) wait_drain(k_full, (k_issued - 1) & 1, status);
   } else if (warp < kP1WarpE) {
     // ---------------- G warps: dO pairs (coalesced rows), V by TMA ----------------
     const int gt = threadIdx.x - kP1WarpG * 32;  // 0..127
