@@ -37,3 +37,17 @@ def test_compact_keeps_the_figures_and_drops_the_rest():
                  "kernel_ms": 0.86873, "kernel_frac": 0.9112, "traffic": 634838016}
     throttled = _form("global_bf16", "global_state", clocks={"sm_mhz": 1500.0, "reasons": ["sw_power_cap"]})
     assert bench.compact(throttled)["clock_reasons"] == ["sw_power_cap"]
+
+
+def test_one_pass_global_kernel_counts_the_whole_call_once():
+    """The one-pass global kernel's algorithmic bytes are the call's: q, k, v read and out, S, z
+    written once (640 B per token at d = 64 in bf16), the state not read back as the two-kernel
+    form's read does."""
+    from causal_linear_attention_attn_gb300 import inputs
+
+    w = inputs.WORKLOADS["global_bf16"]
+    fused = bench.kernel_bytes(w, "global_fused")
+    assert fused == bench.seq_bytes(w)
+    assert fused == w.BH * (w.N * 640 + (64 * 64 + 64) * 4)
+    two = bench.kernel_bytes(w, "global_state") + bench.kernel_bytes(w, "global_read")
+    assert two - fused == w.BH * (64 * 64 + 64) * 4
