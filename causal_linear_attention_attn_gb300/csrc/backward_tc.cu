@@ -404,11 +404,12 @@ constexpr uint32_t kP1S = 0, kP1X = 128, kP1CB = 256, kP1Q = 384;
 __device__ __forceinline__ uint32_t p1_ra(int c) { return (c & 1) ? kP1CB : kP1X; }
 __device__ __forceinline__ uint32_t p1_rc(int c) { return (c & 1) ? kP1X : kP1CB; }
 
-// Warp roles of pass 1 (13 warps): 0 MMA issuer and tensor-memory owner; 1-4
-// keys (TMA; half of the phi pairs in place), queries 0-63 (phi pairs into
-// tensor memory) and copies of the state; 5-8 dO pairs (and V by TMA), the
-// other half of the key pairs, key column sums, queries 64-127; 9-12 scores
-// and dq.
+// Warp roles of pass 1 (13 warps): 0 MMA issuer, tensor-memory owner and the
+// key loads of chunks after the first (TMA); 1-4 half of the key pairs in
+// place, queries 0-63 (phi pairs into tensor memory, one chunk ahead) and
+// copies of the state; 5-8 dO pairs (and V by TMA, one chunk ahead), the other
+// half of the key pairs, key column sums, queries 64-127; 9-12 scores, the
+// next chunk's z, and dq.
 constexpr int kP1Threads = 416;
 constexpr int kP1WarpG = 5, kP1WarpE = 9;
 constexpr uint32_t kBarQK = 1, kBarG = 2, kBarE = 3;
